@@ -1,0 +1,505 @@
+#!/usr/bin/env python
+"""Benchmark: chunked gated delta rule forward + backward on one GB300 per rank.
+
+One step = gdn_chunk_fwd + gdn_chunk_bwd over the training-shape workload
+(B=8, T=4096, H=6, Dk=Dv=128, bf16 inputs, fp32 state), inputs resident in HBM.
+Prints ONE JSON line (rank 0). Under torchrun every rank runs its own replica
+(weak scaling; the layer shards over (batch, head) with no exchange), timing
+takes the max over ranks and `value` is the whole job's tokens/s.
+
+--impl reference times the float64 CPU oracle (the only other implementation of
+this method available here) on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import csv
+import hashlib
+import io
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "GDN fwd+bwd tokens/s at B8 T4096 H6 D128 bf16; % tensor peak; decode HBM GB/s"
+WORKLOAD = "train_fwdbwd"
+L2_BYTES = 129 * 1024 * 1024
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="gdn", choices=["gdn", "reference"])
+    ap.add_argument("--no-extras", action="store_true", help="skip decode, e2e and cpu baseline legs")
+    return ap.parse_args()
+
+
+# ------------------------------------------------------------------ distributed helpers
+def dist_setup():
+    import torch
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    else:
+        torch.cuda.set_device(0)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    """Largest x over all ranks (the slowest rank's time bounds the job)."""
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+
+    dev = "cpu" if dist.get_backend() == "gloo" else "cuda"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tokens_per_s(world: int, tokens_per_rank: int, ms_max: float) -> float:
+    """Whole-job throughput: the tokens every rank processed over the slowest rank's time."""
+    return world * tokens_per_rank / (ms_max / 1e3)
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms while running."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except (OSError, ValueError):
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        if not self.path or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"]}
+        rows = []
+        for r in csv.reader(io.StringIO(open(self.path).read())):
+            r = [x.strip() for x in r]
+            if len(r) >= 9:
+                rows.append(r)
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"]}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+
+        sm = [num(r[1]) for r in rows if num(r[1])]
+        smax = [num(r[2]) for r in rows if num(r[2])]
+        under_load = [s for s in sm if s and s > 0.5 * (max(smax) if smax else 1)] or sm
+        reasons = set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            for i, n in enumerate(names):
+                if r[5 + i].lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(under_load) if under_load else None,
+                "sm_max_mhz": max(smax) if smax else None, "reasons": sorted(reasons),
+                "samples": len(rows), "power_w_max": max((num(r[3]) or 0.0) for r in rows)}
+
+
+# ------------------------------------------------------------------ roofline tables
+def kernel_work(B, T, H, D, es=2):
+    """Algorithmic bytes and tensor FLOPs per launch of each chunk-path kernel.
+
+    Bytes are what the kernel's contract must move once (its input records read
+    once, its outputs written once), per 64-token chunk and head, times the
+    chunk-heads of one launch. FLOPs are its dense products (2 per MAC)."""
+    C = 64
+    n = B * H * (T // C)
+    CD, CC, DD = C * D * es, C * C * es, D * D * es
+    gam = D * 4
+    per = {
+        "chunk_prep_kernel": (4 * CD + C * es + 2 * CC + 4 * CD + gam,
+                              2 * (32 * 32 + 32 * 64) * D * 2 + 2 * C * C * D * 2),
+        "chunk_scan_fwd_kernel": (3 * CD + CC + CD + gam + DD + CD + CD,
+                                  2 * C * D * D * 2 + C * C * D * 2 + D * C * D * 2),
+        "chunk_scan_bwd_kernel": (CD + CC + 3 * CD + gam + CD + DD,
+                                  C * C * D * 2 + 3 * C * D * D * 2),
+        "chunk_dstate_kernel": (3 * CD + 2 * DD + 3 * CD + CC + gam,
+                                3 * C * D * D * 2 + C * C * D * 2),
+        "chunk_grads_kernel": (4 * CD + C * es + CC + 2 * CD + CC + 2 * CD + gam + 4 * CD + C * es,
+                               2 * C * C * D * 2 + 2 * C * C * D * 2 + 2 * C * C * C * 2
+                               + (32 * 32 + 32 * 64) * D * 2 + 2 * (2 * C * C * D * 2)),
+    }
+    return {k: (b * n, f * n) for k, (b, f) in per.items()}
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "gated_deltanet_gdn_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        if f.endswith((".cu", ".cuh", ".h")):
+            h.update(open(os.path.join(csrc, f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return {"hbm_gbs": d.get("hbm_gbs"), "bf16_tflops": d.get("bf16_tflops"),
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained"), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+def load_traffic():
+    """Per-launch DRAM bytes from the committed ncu capture, if the kernels are unchanged."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return {}
+    d = json.load(open(p))
+    if d.get("source_hash") != kernel_source_hash():
+        return {}
+    return d.get("per_launch_bytes", {})
+
+
+# ------------------------------------------------------------------ the gdn arm
+def run_gdn(args, world, rank, local):
+    import torch
+
+    import gated_deltanet_gdn_gb300 as gdn
+    from gated_deltanet_gdn_gb300.synthetic import WORKLOADS, make_inputs
+
+    gdn.load(build_if_needed=True)
+    dev = torch.device("cuda", local)
+    w = WORKLOADS[WORKLOAD]
+    host = make_inputs(w)
+    d = {k: (None if v is None else v.to(dev)) for k, v in host.items()}
+    dims = gdn.make_dims(d["q"], d["v"], d["g"])
+    res = torch.empty(gdn.gdn_chunk_residual_bytes(dims), dtype=torch.uint8, device=dev)
+    ws = torch.empty(gdn.gdn_chunk_bwd_workspace_bytes(dims), dtype=torch.uint8, device=dev)
+    out = torch.empty_like(d["v"])
+    hT = torch.empty((w.B, w.H, w.Dk, w.Dv), dtype=torch.float32, device=dev)
+    grads = {"dq": torch.empty_like(d["q"]), "dk": torch.empty_like(d["k"]), "dv": torch.empty_like(d["v"]),
+             "dg": torch.empty_like(d["g"]), "dbeta": torch.empty_like(d["beta"]),
+             "dh0": torch.empty_like(hT)}
+
+    def step(src=d):
+        gdn.gdn_chunk_fwd(src["q"], src["k"], src["v"], src["g"], src["beta"], src["h0"], out=out,
+                          h_final=hT, residuals=res)
+        gdn.gdn_chunk_bwd(src["q"], src["k"], src["v"], src["g"], src["beta"], src["h0"], res, src["dout"],
+                          src["dh_final"], workspace=ws, grads=grads)
+
+    # gate: finite results, and the chunked forward agrees with the recurrent kernel on one batch row
+    step()
+    ro, rh = gdn.gdn_recurrent(d["q"][:1].contiguous(), d["k"][:1].contiguous(), d["v"][:1].contiguous(),
+                               d["g"][:1].contiguous(), d["beta"][:1].contiguous(), d["h0"][:1].contiguous())
+    torch.cuda.synchronize()
+    gate = float((out[:1].float() - ro.float()).norm() / ro.float().norm())
+    finite = all(bool(torch.isfinite(t.float()).all()) for t in list(grads.values()) + [out, hT])
+    if not (finite and gate < 2e-2):
+        raise SystemExit(f"correctness gate failed: finite={finite} chunked-vs-recurrent rel={gate:.3e}")
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        barrier(world)
+        torch.cuda.synchronize()
+        e0.record()
+        for _ in range(args.steps):
+            step()
+        e1.record()
+        torch.cuda.synchronize()
+        barrier(world)
+    ms = e0.elapsed_time(e1) / args.steps
+    ms_max = max_over_ranks(ms, world)
+    tokens = w.B * w.T
+    value = job_tokens_per_s(world, tokens, ms_max)
+
+    # per-kernel launch durations: events on the launch stream around every kernel
+    gdn.gdn_profile_enable(True)
+    for _ in range(args.steps):
+        step()
+    prof = gdn.gdn_profile_read()
+    gdn.gdn_profile_enable(False)
+    total = sum(v[0] for v in prof.values()) or 1.0
+    work = kernel_work(w.B, w.T, w.H, w.Dk)
+    peaks = load_peaks()
+    traffic = load_traffic()
+    kernels = {}
+    for name, (tms, nl) in prof.items():
+        avg = tms / nl
+        b, f = work.get(name, (None, None))
+        kernels[name] = {"launches_per_step": nl // args.steps, "avg_ms": round(avg, 4),
+                         "share": round(tms / total, 4)}
+        if b:
+            kernels[name]["gbs"] = round(b / (avg / 1e3) / 1e9, 1)
+            kernels[name]["tflops"] = round(f / (avg / 1e3) / 1e12, 2)
+    dom = max(prof, key=lambda k: prof[k][0])
+    b, f = work[dom]
+    avg = prof[dom][0] / prof[dom][1]
+    achieved = b / (avg / 1e3) / 1e9
+    roofline = {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
+                "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
+                "traffic": traffic.get(dom), "algorithmic_bytes": b, "peak_source": peaks["source"]}
+    flops_step = sum(v[1] for v in work.values())
+    tensor = {"step_tflops": round(flops_step / (ms / 1e3) / 1e12, 2),
+              "frac_of_sustained_bf16": round(flops_step / (ms / 1e3) / 1e12 / peaks["bf16_tflops_sustained"], 4)}
+
+    result = {
+        "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_max, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": "chunked fwd+bwd, B8 T4096 H6 Dk=Dv=128, bf16 inputs / fp32 state, "
+                               "per-channel decay, chunk 64",
+                   "B": w.B, "T": w.T, "H": w.H, "Dk": w.Dk, "Dv": w.Dv, "tokens_per_step_per_gpu": tokens,
+                   "l2": "inputs larger than L2 (q,k,v,g,dout %.0f MB + residuals %.0f MB > 129 MB)" % (
+                       5 * d["q"].numel() * 2 / 1e6, res.numel() / 1e6),
+                   "parallelism": f"replicas x{world} (no collective)"},
+        "gpu_launches": 5 * args.steps,
+        "roofline": roofline,
+        "tensor": tensor,
+        "kernels": kernels,
+        "clocks": clk.summary(),
+        "correctness_gate": {"chunked_vs_recurrent_rel_l2": round(gate, 6), "finite": finite},
+    }
+    if not args.no_extras:
+        outputs = dict(grads, out=out, h_final=hT)
+        result["e2e"] = e2e_leg(args, host, d, step, outputs, world)
+        if rank == 0:
+            result["decode"] = decode_leg(dev)
+        if rank == 0 and world == 1:
+            result["cpu_baseline"] = cpu_baseline(w, host)
+    if rank == 0:
+        print(json.dumps(result), flush=True)
+
+
+def e2e_leg(args, host, d, step, outputs, world):
+    """The same step through the public API with HOST buffers: each step copies its
+    inputs host->device from pinned memory, runs forward + backward, and reads the
+    output, final state and every gradient back into pinned host memory."""
+    import torch
+
+    dev = d["q"].device
+    pin_in = {k: v.pin_memory() for k, v in host.items() if v is not None}
+    dev_in = {k: (torch.empty_like(pin_in[k], device=dev) if k in pin_in else None) for k in host}
+    pin_out = {k: torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for k, t in outputs.items()}
+    h2d = sum(v.numel() * v.element_size() for v in pin_in.values())
+    d2h = sum(v.numel() * v.element_size() for v in pin_out.values())
+
+    def full_step():
+        for k, v in pin_in.items():
+            dev_in[k].copy_(v, non_blocking=True)
+        step(dev_in)
+        for k, v in pin_out.items():
+            v.copy_(outputs[k], non_blocking=True)
+
+    for _ in range(2):
+        full_step()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    n = max(3, args.steps // 2)
+    barrier(world)
+    torch.cuda.synchronize()
+    e0.record()
+    for _ in range(n):
+        full_step()
+    e1.record()
+    torch.cuda.synchronize()
+    barrier(world)
+    ms = max_over_ranks(e0.elapsed_time(e1) / n, world)
+    tokens = host["q"].shape[0] * host["q"].shape[1]
+    return {"value": round(world * tokens / (ms / 1e3), 1), "unit": "tokens/s", "ms_per_step": round(ms, 4),
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": n}
+
+
+def decode_leg(dev):
+    """Recurrent kernel: decode steps (T = 1) with the state read and written once,
+    L2 flushed between timed steps; a batch whose state exceeds L2; and the
+    2048-token prefill of the same geometry."""
+    import torch
+
+    import gated_deltanet_gdn_gb300 as gdn
+    from gated_deltanet_gdn_gb300.synthetic import WORKLOADS, make_inputs
+
+    res = {}
+    flush = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=dev)
+    for B, label in ((2, "B2 H48 Dk=Dv=128 fp32 (L2 flushed between steps)"),
+                     (32, "B32 H48 Dk=Dv=128 fp32 (state 201 MB > L2)")):
+        w = WORKLOADS["recurrent"].with_(B=B, T=1, h0_std=0.01)
+        d = {k: (None if v is None else v.to(dev)) for k, v in make_inputs(w).items()}
+        state = d["h0"].clone()
+        out = torch.empty_like(d["v"])
+
+        def one():
+            gdn.gdn_recurrent(d["q"], d["k"], d["v"], d["g"], d["beta"], state, out=out, h_final=state)
+
+        for _ in range(5):
+            one()
+        times = []
+        for _ in range(30):
+            if B == 2:
+                flush.zero_()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            one()
+            e1.record()
+            torch.cuda.synchronize()
+            times.append(e0.elapsed_time(e1))
+        ms = statistics.median(times)
+        sb = w.B * w.H * w.Dk * w.Dv * 4
+        io_b = w.B * w.H * (2 * w.Dk + 2 * w.Dv + 2) * 4
+        b = 2 * sb + io_b
+        res["B%d" % B] = {"workload": label, "ms_per_step": round(ms, 5), "bytes_per_step": b,
+                          "hbm_gbs": round(b / (ms / 1e3) / 1e9, 1)}
+    w = WORKLOADS["recurrent"]
+    d = {k: (None if v is None else v.to(dev)) for k, v in make_inputs(w).items()}
+    gdn.gdn_recurrent(d["q"], d["k"], d["v"], d["g"], d["beta"], None)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(3):
+        gdn.gdn_recurrent(d["q"], d["k"], d["v"], d["g"], d["beta"], None)
+    e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / 3
+    res["prefill_B2_T2048_H48"] = {"ms": round(ms, 4), "tokens_per_s": round(w.B * w.T / (ms / 1e3), 1)}
+    peaks = load_peaks()
+    res["hbm_peak_gbs"] = peaks["hbm_gbs"]
+    return res
+
+
+def oracle_sample(w, host, pairs):
+    """float64 oracle forward + reverse pass over the listed (b, h) pairs, full T."""
+    import numpy as np
+
+    import oracle
+    from gated_deltanet_gdn_gb300.synthetic import to_f64
+
+    def sl(name, state=False):
+        t = host[name]
+        if t is None:
+            return None
+        if state:
+            return np.ascontiguousarray(np.stack([to_f64(t[b, h]) for b, h in pairs], 0)[None])
+        return np.ascontiguousarray(np.stack([to_f64(t[b, :, h]) for b, h in pairs], 1)[None])
+
+    a = {n: sl(n, n in ("h0", "dh_final")) for n in ("q", "k", "v", "g", "beta", "h0", "dout", "dh_final")}
+    t0 = time.perf_counter()
+    oracle.fwd(a["q"], a["k"], a["v"], a["g"], a["beta"], a["h0"], nthreads=len(pairs))
+    oracle.bwd(a["q"], a["k"], a["v"], a["g"], a["beta"], a["h0"], a["dout"], a["dh_final"],
+               nthreads=len(pairs))
+    return time.perf_counter() - t0
+
+
+def cpu_pairs(w):
+    cores = os.cpu_count() or 1
+    p = max(1, min(cores, 16, w.B * w.H))
+    return [(i // w.H, i % w.H) for i in range(p)]
+
+
+def cpu_baseline(w, host):
+    import oracle
+
+    oracle.build()
+    pairs = cpu_pairs(w)
+    sec = oracle_sample(w, host, pairs)
+    tokens = len(pairs) * w.T / w.H  # head-sequences expressed in tokens of all H heads
+    return {"value": round(tokens / sec, 1), "unit": "tokens/s", "cores": len(pairs), "kind": "oracle",
+            "sample": f"float64 token-serial forward + reverse pass of {len(pairs)} (batch, head) pairs "
+                      f"x {w.T} tokens = {tokens:.0f} tokens of the {w.H}-head workload, {sec:.2f} s"}
+
+
+def run_reference(args, world, rank):
+    """The float64 CPU oracle timed on the host cores, same workload, metric and unit."""
+    if rank != 0:
+        return
+    import oracle
+    from gated_deltanet_gdn_gb300.synthetic import WORKLOADS, make_inputs
+
+    oracle.build()
+    w = WORKLOADS[WORKLOAD]
+    host = make_inputs(w)
+    pairs = cpu_pairs(w)
+    tokens = len(pairs) * w.T / w.H
+    steps = max(1, min(args.steps, 10))
+    for _ in range(max(0, min(args.warmup, 1))):
+        oracle_sample(w, host, pairs)
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        oracle_sample(w, host, pairs)
+    sec = (time.perf_counter() - t0) / steps
+    value = tokens / sec
+    line = {"impl": "reference", "metric": METRIC, "value": round(value, 1), "unit": "tokens/s",
+            "n_gpus": world, "steps": steps, "warmup": min(args.warmup, 1), "ms_per_step": round(sec * 1e3, 2),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": "chunked fwd+bwd, B8 T4096 H6 Dk=Dv=128 (bounded sample, see cpu_baseline)"},
+            "cpu_baseline": {"value": round(value, 1), "unit": "tokens/s", "cores": len(pairs), "kind": "oracle",
+                             "sample": f"{len(pairs)} (batch, head) pairs x {w.T} tokens per step"},
+            "e2e": {"value": round(value, 1), "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        world = int(os.environ.get("WORLD_SIZE", "1"))
+        rank = int(os.environ.get("RANK", "0"))
+        run_reference(args, world, rank)
+        return
+    world, rank, local = dist_setup()
+    run_gdn(args, world, rank, local)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,293 @@
+// C ABI of the gated delta rule library: argument validation, buffer layouts and
+// dispatch to the kernels. Declared in include/gdn.h.
+#include <cmath>
+#include <cstdint>
+#include <mutex>
+#include <vector>
+
+#include "../../include/gdn.h"
+#include "kernels.h"
+
+namespace gdn {
+namespace {
+
+// Error word written by kernels that gave up on a bounded wait (bit values in common.cuh).
+__device__ unsigned g_device_error;
+
+constexpr int MAX_DEVICES = 64;
+unsigned* g_err_ptr[MAX_DEVICES];
+std::mutex g_err_mutex;
+
+// Device address of the error word on the current device (resolved once per device,
+// with that device current).
+unsigned* device_error_word() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= MAX_DEVICES) return nullptr;
+  std::lock_guard<std::mutex> lock(g_err_mutex);
+  if (!g_err_ptr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_device_error) != cudaSuccess) return nullptr;
+    g_err_ptr[dev] = static_cast<unsigned*>(p);
+  }
+  return g_err_ptr[dev];
+}
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// Common dims checks. Returns GDN_OK or the status to report.
+int check_dims(const gdn_dims* d, bool chunked) {
+  if (!d) return GDN_ERR_INVALID_ARG;
+  if (d->B < 0 || d->T < 0 || d->H < 0) return GDN_ERR_INVALID_ARG;
+  if (d->dtype != GDN_F32 && d->dtype != GDN_BF16) return GDN_ERR_UNSUPPORTED;
+  if ((d->Dk != 64 && d->Dk != 128) || (d->Dv != 64 && d->Dv != 128)) return GDN_ERR_UNSUPPORTED;
+  if ((long long)d->B * d->H > 65535) return GDN_ERR_UNSUPPORTED;  // grid y limit
+  if (d->flags & ~GDN_FLAG_PAIRWISE_WITHIN_BLOCK) return GDN_ERR_INVALID_ARG;
+  if (chunked && d->Dk != d->Dv) return GDN_ERR_UNSUPPORTED;
+  if (chunked && d->T % GDN_CHUNK != 0) return GDN_ERR_SHAPE;
+  return GDN_OK;
+}
+
+int esize(const gdn_dims* d) { return d->dtype == GDN_BF16 ? 2 : 4; }
+
+// Required tensor: non-NULL and 16-byte aligned when the call has work.
+bool tensor_ok(const void* p, bool has_work) { return !has_work || (p && aligned(p, 16)); }
+bool optional_ok(const void* p) { return !p || aligned(p, 16); }
+// [B,T,H] gates: element alignment only.
+bool gate_ok(const void* p, bool has_work, int es) { return !has_work || (p && aligned(p, es)); }
+
+ResidualPtrs residual_ptrs(const gdn_dims* d, void* base) {
+  const ResidualLayout L = residual_layout(d->B, d->T, d->H, d->Dk, d->Dv, esize(d));
+  char* b = static_cast<char*>(base);
+  ResidualPtrs r;
+  r.aqk = b + L.aqk;
+  r.tmat = b + L.tmat;
+  r.wneg = b + L.wneg;
+  r.up = b + L.up;
+  r.qh = b + L.qh;
+  r.kt = b + L.kt;
+  r.gam = reinterpret_cast<float*>(b + L.gam);
+  r.state = b + L.state;
+  r.u = b + L.u;
+  return r;
+}
+
+BwdWorkspacePtrs workspace_ptrs(const gdn_dims* d, void* base) {
+  const BwdWorkspaceLayout L = bwd_workspace_layout(d->B, d->T, d->H, d->Dk, d->Dv, esize(d));
+  char* b = static_cast<char*>(base);
+  BwdWorkspacePtrs w;
+  w.du = b + L.du;
+  w.dstate = b + L.dstate;
+  w.dqh = b + L.dqh;
+  w.dw = b + L.dw;
+  w.dkt = b + L.dkt;
+  w.daqk = b + L.daqk;
+  w.dgam = reinterpret_cast<float*>(b + L.dgam);
+  return w;
+}
+
+int launch_status(cudaError_t e) { return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA; }
+
+// Per-launch timing: a pool of event pairs, recorded around each kernel launch while on.
+struct ProfRec {
+  int id;
+  cudaEvent_t a, b;
+};
+std::mutex g_prof_mutex;
+std::vector<ProfRec> g_prof;
+size_t g_prof_used = 0;
+bool g_prof_on = false;
+bool g_prof_failed = false;
+
+const char* kKernelNames[K_COUNT] = {"chunk_prep_kernel",    "chunk_scan_fwd_kernel",
+                                     "chunk_scan_bwd_kernel", "chunk_dstate_kernel",
+                                     "chunk_grads_kernel",    "recurrent_kernel"};
+
+}  // namespace
+
+void prof_mark(KernelId id, cudaStream_t s, bool begin) {
+  if (!g_prof_on) return;
+  std::lock_guard<std::mutex> lock(g_prof_mutex);
+  if (begin) {
+    if (g_prof_used == g_prof.size()) {
+      ProfRec r{};
+      if (cudaEventCreate(&r.a) != cudaSuccess || cudaEventCreate(&r.b) != cudaSuccess) {
+        g_prof_failed = true;
+        return;
+      }
+      g_prof.push_back(r);
+    }
+    g_prof[g_prof_used].id = (int)id;
+    if (cudaEventRecord(g_prof[g_prof_used].a, s) != cudaSuccess) g_prof_failed = true;
+  } else {
+    if (g_prof_used >= g_prof.size()) return;
+    if (cudaEventRecord(g_prof[g_prof_used].b, s) != cudaSuccess) g_prof_failed = true;
+    ++g_prof_used;
+  }
+}
+
+}  // namespace gdn
+
+using namespace gdn;
+
+extern "C" {
+
+size_t gdn_chunk_residual_bytes(const gdn_dims* d) {
+  if (check_dims(d, true) != GDN_OK) return 0;
+  return residual_layout(d->B, d->T, d->H, d->Dk, d->Dv, esize(d)).total;
+}
+
+size_t gdn_chunk_bwd_workspace_bytes(const gdn_dims* d) {
+  if (check_dims(d, true) != GDN_OK) return 0;
+  return bwd_workspace_layout(d->B, d->T, d->H, d->Dk, d->Dv, esize(d)).total;
+}
+
+int gdn_chunk_fwd(const gdn_dims* d, const void* q, const void* k, const void* v, const void* g,
+                  const void* beta, const float* h0, float scale, void* out, float* h_final,
+                  void* residuals, void* stream) {
+  int st = check_dims(d, true);
+  if (st != GDN_OK) return st;
+  if (!std::isfinite(scale)) return GDN_ERR_INVALID_ARG;
+  const bool work = (long long)d->B * d->H * d->T > 0;
+  const int es = esize(d);
+  if (!tensor_ok(q, work) || !tensor_ok(k, work) || !tensor_ok(v, work) || !tensor_ok(out, work))
+    return GDN_ERR_INVALID_ARG;
+  if (d->g_per_channel ? !tensor_ok(g, work) : !gate_ok(g, work, es)) return GDN_ERR_INVALID_ARG;
+  if (!gate_ok(beta, work, es)) return GDN_ERR_INVALID_ARG;
+  if (!optional_ok(h0) || !optional_ok(h_final)) return GDN_ERR_INVALID_ARG;
+  if (work && (!residuals || !aligned(residuals, 256))) return GDN_ERR_INVALID_ARG;
+  if ((long long)d->B * d->H == 0) return GDN_OK;
+  ChunkFwdArgs a{};
+  a.B = d->B; a.T = d->T; a.H = d->H; a.DK = d->Dk; a.DV = d->Dv;
+  a.per_channel = d->g_per_channel ? 1 : 0;
+  a.bf16 = d->dtype == GDN_BF16;
+  a.flags = d->flags;
+  a.q = q; a.k = k; a.v = v; a.g = g; a.beta = beta; a.h0 = h0; a.scale = scale;
+  a.out = out; a.h_final = h_final;
+  if (residuals) a.res = residual_ptrs(d, residuals);
+  a.err = device_error_word();
+  if (!a.err) return GDN_ERR_CUDA;
+  return launch_status(launch_chunk_fwd(a, static_cast<cudaStream_t>(stream)));
+}
+
+int gdn_chunk_bwd(const gdn_dims* d, const void* q, const void* k, const void* v, const void* g,
+                  const void* beta, const float* h0, float scale, const void* residuals,
+                  const void* dout, const float* dh_final, void* dq, void* dk, void* dv, void* dg,
+                  void* dbeta, float* dh0, void* workspace, void* stream) {
+  int st = check_dims(d, true);
+  if (st != GDN_OK) return st;
+  if (d->dtype != GDN_BF16) return GDN_ERR_UNSUPPORTED;
+  if (!std::isfinite(scale)) return GDN_ERR_INVALID_ARG;
+  const bool work = (long long)d->B * d->H * d->T > 0;
+  const int es = esize(d);
+  (void)h0;  // the chunk-start states in the residuals already carry h0
+  if (!tensor_ok(q, work) || !tensor_ok(k, work) || !tensor_ok(v, work) || !tensor_ok(dout, work) ||
+      !tensor_ok(dq, work) || !tensor_ok(dk, work) || !tensor_ok(dv, work))
+    return GDN_ERR_INVALID_ARG;
+  if (d->g_per_channel ? (!tensor_ok(g, work) || !tensor_ok(dg, work))
+                       : (!gate_ok(g, work, es) || !gate_ok(dg, work, es)))
+    return GDN_ERR_INVALID_ARG;
+  if (!gate_ok(beta, work, es) || !gate_ok(dbeta, work, es)) return GDN_ERR_INVALID_ARG;
+  if (!optional_ok(dh_final) || !optional_ok(dh0)) return GDN_ERR_INVALID_ARG;
+  if (work && (!residuals || !aligned(residuals, 256) || !workspace || !aligned(workspace, 256)))
+    return GDN_ERR_INVALID_ARG;
+  if ((long long)d->B * d->H == 0) return GDN_OK;
+  ChunkBwdArgs a{};
+  a.B = d->B; a.T = d->T; a.H = d->H; a.DK = d->Dk; a.DV = d->Dv;
+  a.per_channel = d->g_per_channel ? 1 : 0;
+  a.bf16 = 1;
+  a.flags = d->flags;
+  a.q = q; a.k = k; a.v = v; a.g = g; a.beta = beta; a.scale = scale;
+  if (residuals) a.res = residual_ptrs(d, const_cast<void*>(residuals));
+  a.dout = dout; a.dh_final = dh_final;
+  a.dq = dq; a.dk = dk; a.dv = dv; a.dg = dg; a.dbeta = dbeta; a.dh0 = dh0;
+  if (workspace) a.ws = workspace_ptrs(d, workspace);
+  a.err = device_error_word();
+  if (!a.err) return GDN_ERR_CUDA;
+  return launch_status(launch_chunk_bwd(a, static_cast<cudaStream_t>(stream)));
+}
+
+int gdn_recurrent(const gdn_dims* d, const void* q, const void* k, const void* v, const void* g,
+                  const void* beta, const float* h0, float scale, void* out, float* h_final,
+                  void* stream) {
+  int st = check_dims(d, false);
+  if (st != GDN_OK) return st;
+  if (!std::isfinite(scale)) return GDN_ERR_INVALID_ARG;
+  const bool work = (long long)d->B * d->H * d->T > 0;
+  const bool heads = (long long)d->B * d->H > 0;
+  const int es = esize(d);
+  if (!tensor_ok(q, work) || !tensor_ok(k, work) || !tensor_ok(v, work) || !tensor_ok(out, work))
+    return GDN_ERR_INVALID_ARG;
+  if (d->g_per_channel ? !tensor_ok(g, work) : !gate_ok(g, work, es)) return GDN_ERR_INVALID_ARG;
+  if (!gate_ok(beta, work, es)) return GDN_ERR_INVALID_ARG;
+  if (!optional_ok(h0) || !tensor_ok(h_final, heads)) return GDN_ERR_INVALID_ARG;
+  if (!heads) return GDN_OK;
+  RecurrentArgs a{};
+  a.B = d->B; a.T = d->T; a.H = d->H; a.DK = d->Dk; a.DV = d->Dv;
+  a.per_channel = d->g_per_channel ? 1 : 0;
+  a.bf16 = d->dtype == GDN_BF16;
+  a.q = q; a.k = k; a.v = v; a.g = g; a.beta = beta; a.h0 = h0; a.scale = scale;
+  a.out = out; a.h_final = h_final;
+  return launch_status(launch_recurrent(a, static_cast<cudaStream_t>(stream)));
+}
+
+int gdn_check_device_error(void) {
+  unsigned* p = device_error_word();
+  if (!p) return GDN_ERR_CUDA;
+  if (cudaDeviceSynchronize() != cudaSuccess) return GDN_ERR_CUDA;
+  unsigned v = 0;
+  if (cudaMemcpy(&v, p, sizeof(v), cudaMemcpyDeviceToHost) != cudaSuccess) return GDN_ERR_CUDA;
+  if (v) {
+    const unsigned zero = 0;
+    if (cudaMemcpy(p, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess) return GDN_ERR_CUDA;
+    return GDN_ERR_INTERNAL;
+  }
+  return GDN_OK;
+}
+
+const char* gdn_status_string(int s) {
+  switch (s) {
+    case GDN_OK: return "ok";
+    case GDN_ERR_INVALID_ARG: return "invalid argument (NULL or misaligned pointer, bad size or flag)";
+    case GDN_ERR_UNSUPPORTED: return "unsupported configuration (Dk, Dv in {64, 128}; chunked path Dk == Dv; bf16-only backward)";
+    case GDN_ERR_SHAPE: return "T must be a multiple of 64 on the chunked path";
+    case GDN_ERR_CUDA: return "CUDA launch or runtime error";
+    case GDN_ERR_INTERNAL: return "a kernel reported an internal error (bounded wait timed out)";
+    default: return "unknown status";
+  }
+}
+
+int gdn_version(void) { return 100; }
+
+int gdn_profile_enable(int on) {
+  std::lock_guard<std::mutex> lock(g_prof_mutex);
+  g_prof_on = on != 0;
+  g_prof_used = 0;
+  g_prof_failed = false;
+  return GDN_OK;
+}
+
+int gdn_profile_read(double* ms, int* launches, int n) {
+  if (!ms || !launches || n < 0) return GDN_ERR_INVALID_ARG;
+  std::lock_guard<std::mutex> lock(g_prof_mutex);
+  for (int i = 0; i < n; ++i) {
+    ms[i] = 0.0;
+    launches[i] = 0;
+  }
+  if (g_prof_failed) return GDN_ERR_CUDA;
+  for (size_t i = 0; i < g_prof_used; ++i) {
+    if (cudaEventSynchronize(g_prof[i].b) != cudaSuccess) return GDN_ERR_CUDA;
+    float t = 0.f;
+    if (cudaEventElapsedTime(&t, g_prof[i].a, g_prof[i].b) != cudaSuccess) return GDN_ERR_CUDA;
+    const int id = g_prof[i].id;
+    if (id < n) {
+      ms[id] += t;
+      launches[id] += 1;
+    }
+  }
+  g_prof_used = 0;
+  return GDN_OK;
+}
+
+const char* gdn_kernel_name(int id) { return (id >= 0 && id < K_COUNT) ? kKernelNames[id] : ""; }
+
+}  // extern "C"

@@ -1,0 +1,317 @@
+// Chunked backward of the gated delta rule (bf16 operands, fp32 state and accumulation).
+//
+// Hand-derived from the chunked forward (see chunk_fwd.cu). With dS1 the gradient of the
+// state leaving a chunk and dO the output gradient of its tokens:
+//   reverse scan   dU  = scale Aqk^T dO + K-tilde dS1
+//                  dS0 = diag(gam) dS1 + scale Q-hat^T dO - W^T dU
+//   chunk products dQ-hat = scale dO S0^T, dW = -dU S0^T, dK-tilde = U dS1^T,
+//                  dAqk = scale (dO U^T) masked j <= t, dgam = rowsum(dS1 * S0)
+//   chunk grads    dT = dW Bk^T + dU Bv^T (Bk = diag(beta) Gam*k, Bv = diag(beta) V),
+//                  dBk = T^T dW, dBv = T^T dU, dAkk = -(T^T dT T^T) masked j < t,
+//                  dbeta = rowsum(dBk * K-hat) + rowsum(dBv * V) + rowsum(dAkk * Pkk),
+//                  decay-weighted scores P[t,j] = sum_c x_tc y_jc exp(G_tc - G_jc) give
+//                  dx = (dP (*) E) y, dy = (dP^T (*) E) x and dG = x dx - y dy,
+//                  and dg is the reverse cumulative sum of dG inside the chunk.
+// atomic-ops 0.1.0 (sections Features and Limitations) describes a backward made of
+// stage kernels that reuse forward residuals, with the pairwise-decay score backward
+// as one of them; the staging here is this library's own.
+//
+// Kernels
+//   chunk_scan_bwd_kernel   grid (Dv/32, B*H), 128 threads, sequential over chunks in
+//                           reverse: dS in registers, writes dU and dS1 per chunk, dh0
+//   chunk_dstate_kernel     grid (chunks, B*H), 128 threads: the four products with the
+//                           chunk states (contractions over Dv) and dgam
+//   chunk_grads_kernel      (chunk_grads.cu) everything else
+#include "common.cuh"
+#include "kernels.h"
+
+namespace gdn {
+namespace {
+
+constexpr int RSCAN_THREADS = 128;
+constexpr int DST_THREADS = 128;
+
+
+// ------------------------------------------------------------------ reverse state scan
+template <int DK>
+struct RScanLayout {
+  static constexpr int ES = 2;
+  static constexpr int W = 0;                      // -W          [C][DK]
+  static constexpr int QH = W + C * DK * ES;       // scale Q-hat [C][DK]
+  static constexpr int KT = QH + C * DK * ES;      // K-tilde     [C][DK]
+  static constexpr int AQK = KT + C * DK * ES;     // scale Aqk   [C][C]
+  static constexpr int GAM = AQK + C * C * ES;     // float [DK]
+  static constexpr int DO = a1k(GAM + DK * 4);     // dO slice    [C][NT]
+  static constexpr int STAGE = a1k(DO + C * NT * ES);
+  static constexpr int DSS = 2 * STAGE;            // dS operand  [DK][NT]
+  static constexpr int DUS = a1k(DSS + DK * NT * ES);  // dU     [C][NT]
+  static constexpr int BAR = a1k(DUS + C * NT * ES);
+  static constexpr int BYTES = BAR + 64;
+  static constexpr uint32_t TX = (uint32_t)(3 * C * DK * ES + C * C * ES + DK * 4);
+};
+
+template <int DK, int DV>
+__global__ void __launch_bounds__(RSCAN_THREADS) chunk_scan_bwd_kernel(ChunkBwdArgs a) {
+  typedef bf16 T;
+  typedef RScanLayout<DK> L;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = align1024(smem_raw);
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int tile = blockIdx.x, bh = blockIdx.y, b = bh / a.H, h = bh % a.H;
+  const int N = a.T / C;
+  constexpr int NTILE = DV / NT, MTS = DK / 64, NTT = NT / 8, EPC = 8;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + L::BAR);
+  Tile<T, DK, NT> dSs{reinterpret_cast<T*>(sm + L::DSS)};
+  Tile<T, C, NT> dUs{reinterpret_cast<T*>(sm + L::DUS)};
+  const T* dout = static_cast<const T*>(a.dout);
+
+  float dS[MTS][NTT][4];
+  const size_t sb = (size_t)bh * DK * DV;
+#pragma unroll
+  for (int mt = 0; mt < MTS; ++mt)
+#pragma unroll
+    for (int nt = 0; nt < NTT; ++nt)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int r = warp * 16 * MTS + 16 * mt + frag_row(lane, e);
+        const int c = tile * NT + 8 * nt + frag_col(lane, e);
+        dS[mt][nt][e] = a.dh_final ? a.dh_final[sb + (size_t)r * DV + c] : 0.f;
+      }
+  if (tid == 0) {
+    mbar_init(&bars[0], 1);
+    mbar_init(&bars[1], 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+
+  auto issue = [&](int n, int s) {  // all threads: dO via cp.async; thread 0: records via bulk
+    uint8_t* st = sm + s * L::STAGE;
+    const size_t ch = (size_t)bh * N + n;
+    if (tid == 0) {
+      mbar_arrive_expect_tx(&bars[s], L::TX);
+      bulk_g2s(st + L::W, static_cast<const T*>(a.res.wneg) + ch * (C * DK), C * DK * 2, &bars[s]);
+      bulk_g2s(st + L::QH, static_cast<const T*>(a.res.qh) + ch * (C * DK), C * DK * 2, &bars[s]);
+      bulk_g2s(st + L::KT, static_cast<const T*>(a.res.kt) + ch * (C * DK), C * DK * 2, &bars[s]);
+      bulk_g2s(st + L::AQK, static_cast<const T*>(a.res.aqk) + ch * (C * C), C * C * 2, &bars[s]);
+      bulk_g2s(st + L::GAM, a.res.gam + ch * DK, DK * 4, &bars[s]);
+    }
+    Tile<T, C, NT> dOt{reinterpret_cast<T*>(st + L::DO)};
+    const size_t row0 = ((size_t)b * a.T + (size_t)n * C) * a.H + h;
+    for (int i = tid; i < C * NT / EPC; i += RSCAN_THREADS) {
+      const int r = i / (NT / EPC), c0 = (i % (NT / EPC)) * EPC;
+      cp_async16(dOt.ptr(r, c0), dout + (row0 + (size_t)r * a.H) * DV + tile * NT + c0);
+    }
+    cp_async_commit();
+  };
+  if (N > 0) issue(N - 1, 0);
+
+  for (int it = 0; it < N; ++it) {
+    const int n = N - 1 - it, s = it & 1;
+    const uint32_t par = (uint32_t)(it >> 1) & 1u;
+    const bool more = it + 1 < N;
+    if (more) issue(n - 1, s ^ 1);
+    uint8_t* st = sm + s * L::STAGE;
+    Tile<T, C, DK> Wt{reinterpret_cast<T*>(st + L::W)};
+    Tile<T, C, DK> Qt{reinterpret_cast<T*>(st + L::QH)};
+    Tile<T, C, DK> Kt{reinterpret_cast<T*>(st + L::KT)};
+    Tile<T, C, C> At{reinterpret_cast<T*>(st + L::AQK)};
+    Tile<T, C, NT> dOt{reinterpret_cast<T*>(st + L::DO)};
+    const float* gam = reinterpret_cast<const float*>(st + L::GAM);
+    const size_t ch = (size_t)bh * N + n;
+
+#pragma unroll
+    for (int mt = 0; mt < MTS; ++mt)
+#pragma unroll
+      for (int nt = 0; nt < NTT; ++nt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          dSs.at(warp * 16 * MTS + 16 * mt + frag_row(lane, e), 8 * nt + frag_col(lane, e)) =
+              from_f32<T>(dS[mt][nt][e]);
+    if (more) cp_async_wait<1>(); else cp_async_wait<0>();
+    mbar_wait(&bars[s], par, a.err);
+    __syncthreads();
+    {  // gradient of the state leaving chunk n
+      T* dst = static_cast<T*>(a.ws.dstate) + (ch * NTILE + tile) * (DK * NT);
+      for (int i = tid; i < DK * NT / EPC; i += RSCAN_THREADS) copy16(dst + i * EPC, dSs.p + i * EPC);
+    }
+    float du[1][NTT][4];
+    zero(du);
+    Gemm<T>::template run<1, NTT>(du, aview<true>(At), bview<true>(dOt), 16 * warp, 0, 0, C, lane);
+    Gemm<T>::template run<1, NTT>(du, aview<false>(Kt), bview<true>(dSs), 16 * warp, 0, 0, DK, lane);
+#pragma unroll
+    for (int nt = 0; nt < NTT; ++nt)
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
+        dUs.at(16 * warp + frag_row(lane, e), 8 * nt + frag_col(lane, e)) = from_f32<T>(du[0][nt][e]);
+    __syncthreads();
+    {
+      T* dst = static_cast<T*>(a.ws.du) + (ch * NTILE + tile) * (C * NT);
+      for (int i = tid; i < C * NT / EPC; i += RSCAN_THREADS) copy16(dst + i * EPC, dUs.p + i * EPC);
+    }
+#pragma unroll
+    for (int mt = 0; mt < MTS; ++mt)
+#pragma unroll
+      for (int nt = 0; nt < NTT; ++nt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) dS[mt][nt][e] *= gam[warp * 16 * MTS + 16 * mt + frag_row(lane, e)];
+    Gemm<T>::template run<MTS, NTT>(dS, aview<true>(Qt), bview<true>(dOt), warp * 16 * MTS, 0, 0, C, lane);
+    Gemm<T>::template run<MTS, NTT>(dS, aview<true>(Wt), bview<true>(dUs), warp * 16 * MTS, 0, 0, C, lane);
+    __syncthreads();
+  }
+  if (a.dh0) {
+#pragma unroll
+    for (int mt = 0; mt < MTS; ++mt)
+#pragma unroll
+      for (int nt = 0; nt < NTT; ++nt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int r = warp * 16 * MTS + 16 * mt + frag_row(lane, e);
+          const int c = tile * NT + 8 * nt + frag_col(lane, e);
+          a.dh0[sb + (size_t)r * DV + c] = dS[mt][nt][e];
+        }
+  }
+}
+
+// ------------------------------------------------------------------ state products
+template <int DK, int DV>
+struct DstLayout {
+  static constexpr int DO = 0;                      // dO   [C][DV]
+  static constexpr int U = a1k(DO + C * DV * 2);    // U    [C][DV] (NT slices)
+  static constexpr int DU = a1k(U + C * DV * 2);    // dU   [C][DV] (NT slices)
+  static constexpr int S0 = a1k(DU + C * DV * 2);   // S0   [DK][DV] (NT slices)
+  static constexpr int DS1 = a1k(S0 + DK * DV * 2); // dS1  [DK][DV] (NT slices)
+  static constexpr int BYTES = a1k(DS1 + DK * DV * 2);
+};
+
+template <int DK, int DV>
+__global__ void __launch_bounds__(DST_THREADS) chunk_dstate_kernel(ChunkBwdArgs a) {
+  typedef bf16 T;
+  typedef DstLayout<DK, DV> L;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = align1024(smem_raw);
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int n = blockIdx.x, bh = blockIdx.y, b = bh / a.H, h = bh % a.H;
+  const int N = a.T / C;
+  const size_t ch = (size_t)bh * N + n;
+  constexpr int EPC = 8;
+  Tile<T, C, DV> dOs{reinterpret_cast<T*>(sm + L::DO)};
+  TTile<T, C, DV, NT> Us{reinterpret_cast<T*>(sm + L::U)};
+  TTile<T, C, DV, NT> dUs{reinterpret_cast<T*>(sm + L::DU)};
+  TTile<T, DK, DV, NT> S0s{reinterpret_cast<T*>(sm + L::S0)};
+  TTile<T, DK, DV, NT> dS1s{reinterpret_cast<T*>(sm + L::DS1)};
+  const T* dout = static_cast<const T*>(a.dout);
+  const size_t row0 = ((size_t)b * a.T + (size_t)n * C) * a.H + h;
+  for (int i = tid; i < C * DV / EPC; i += DST_THREADS) {
+    const int r = i / (DV / EPC), c0 = (i % (DV / EPC)) * EPC;
+    cp_async16(dOs.ptr(r, c0), dout + (row0 + (size_t)r * a.H) * DV + c0);
+  }
+  {
+    const T* su = static_cast<const T*>(a.res.u) + ch * (C * DV);
+    const T* sdu = static_cast<const T*>(a.ws.du) + ch * (C * DV);
+    for (int i = tid; i < C * DV / EPC; i += DST_THREADS) {
+      cp_async16(Us.p + i * EPC, su + i * EPC);
+      cp_async16(dUs.p + i * EPC, sdu + i * EPC);
+    }
+    const T* ss = static_cast<const T*>(a.res.state) + ch * (DK * DV);
+    const T* sds = static_cast<const T*>(a.ws.dstate) + ch * (DK * DV);
+    for (int i = tid; i < DK * DV / EPC; i += DST_THREADS) {
+      cp_async16(S0s.p + i * EPC, ss + i * EPC);
+      cp_async16(dS1s.p + i * EPC, sds + i * EPC);
+    }
+  }
+  cp_async_commit();
+  cp_async_wait<0>();
+  __syncthreads();
+
+  // dgam_c = sum_v dS1[c][v] S0[c][v]
+  for (int c = tid; c < DK; c += DST_THREADS) {
+    float acc = 0.f;
+    for (int v = 0; v < DV; ++v) acc = fmaf(to_f32(dS1s.at(c, v)), to_f32(S0s.at(c, v)), acc);
+    static_cast<float*>(a.ws.dgam)[ch * DK + c] = acc;
+  }
+  // C x DK products, warp w rows 16 w; two halves of the columns at a time
+  constexpr int NH = DK / 16;  // n8 tiles per half
+  T* dqh = static_cast<T*>(a.ws.dqh) + ch * (C * DK);
+  T* dw = static_cast<T*>(a.ws.dw) + ch * (C * DK);
+  T* dkt = static_cast<T*>(a.ws.dkt) + ch * (C * DK);
+  for (int hf = 0; hf < 2; ++hf) {
+    const int n0 = hf * (DK / 2);
+    float acc[1][NH][4];
+    zero(acc);  // dQ-hat = scale dO S0^T
+    Gemm<T>::template run<1, NH>(acc, aview<false>(dOs), bview<false>(S0s), 16 * warp, n0, 0, DV, lane);
+#pragma unroll
+    for (int nt = 0; nt < NH; ++nt)
+#pragma unroll
+      for (int e = 0; e < 4; e += 2) {
+        const int r = 16 * warp + frag_row(lane, e), c = n0 + 8 * nt + frag_col(lane, e);
+        store2(dqh + Sw<T, C, DK>::off(r, c), a.scale * acc[0][nt][e], a.scale * acc[0][nt][e + 1]);
+      }
+    zero(acc);  // dW = -dU S0^T
+    Gemm<T>::template run<1, NH>(acc, aview<false>(dUs), bview<false>(S0s), 16 * warp, n0, 0, DV, lane);
+#pragma unroll
+    for (int nt = 0; nt < NH; ++nt)
+#pragma unroll
+      for (int e = 0; e < 4; e += 2) {
+        const int r = 16 * warp + frag_row(lane, e), c = n0 + 8 * nt + frag_col(lane, e);
+        store2(dw + Sw<T, C, DK>::off(r, c), -acc[0][nt][e], -acc[0][nt][e + 1]);
+      }
+    zero(acc);  // dK-tilde = U dS1^T
+    Gemm<T>::template run<1, NH>(acc, aview<false>(Us), bview<false>(dS1s), 16 * warp, n0, 0, DV, lane);
+#pragma unroll
+    for (int nt = 0; nt < NH; ++nt)
+#pragma unroll
+      for (int e = 0; e < 4; e += 2) {
+        const int r = 16 * warp + frag_row(lane, e), c = n0 + 8 * nt + frag_col(lane, e);
+        store2(dkt + Sw<T, C, DK>::off(r, c), acc[0][nt][e], acc[0][nt][e + 1]);
+      }
+  }
+  {  // dAqk = scale dO U^T, masked j <= t
+    float acc[1][8][4];
+    zero(acc);
+    Gemm<T>::template run<1, 8>(acc, aview<false>(dOs), bview<false>(Us), 16 * warp, 0, 0, DV, lane);
+    T* da = static_cast<T*>(a.ws.daqk) + ch * (C * C);
+#pragma unroll
+    for (int nt = 0; nt < 8; ++nt)
+#pragma unroll
+      for (int e = 0; e < 4; e += 2) {
+        const int r = 16 * warp + frag_row(lane, e), j = 8 * nt + frag_col(lane, e);
+        store2(da + Sw<T, C, C>::off(r, j), j <= r ? a.scale * acc[0][nt][e] : 0.f,
+               j + 1 <= r ? a.scale * acc[0][nt][e + 1] : 0.f);
+      }
+  }
+}
+
+template <int DK, int DV>
+cudaError_t launch_bwd_t(const ChunkBwdArgs& a, cudaStream_t s) {
+  const int N = a.T / C, BH = a.B * a.H;
+  cudaError_t e;
+  {
+    const int bytes = RScanLayout<DK>::BYTES + 1024;
+    auto kern = chunk_scan_bwd_kernel<DK, DV>;
+    if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes)) != cudaSuccess) return e;
+    prof_mark(K_SCAN_BWD, s, true);
+    kern<<<dim3(DV / NT, BH), RSCAN_THREADS, bytes, s>>>(a);
+    prof_mark(K_SCAN_BWD, s, false);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
+  if (N == 0) return cudaSuccess;
+  {
+    const int bytes = DstLayout<DK, DV>::BYTES + 1024;
+    auto kern = chunk_dstate_kernel<DK, DV>;
+    if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes)) != cudaSuccess) return e;
+    prof_mark(K_DSTATE, s, true);
+    kern<<<dim3(N, BH), DST_THREADS, bytes, s>>>(a);
+    prof_mark(K_DSTATE, s, false);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
+  return launch_chunk_grads(a, s);
+}
+
+}  // namespace
+
+cudaError_t launch_chunk_bwd(const ChunkBwdArgs& a, cudaStream_t s) {
+  if (a.B * a.H == 0) return cudaSuccess;
+  return a.DK == 64 ? launch_bwd_t<64, 64>(a, s) : launch_bwd_t<128, 128>(a, s);
+}
+
+}  // namespace gdn

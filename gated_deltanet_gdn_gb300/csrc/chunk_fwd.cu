@@ -1,0 +1,569 @@
+// Chunked forward of the gated delta rule: chunk-parallel preparation + sequential scan.
+//
+// Per chunk of C = 64 tokens (two 32-token blocks) and incoming state S0:
+//   G = cumsum(g) per key channel, Gam = exp(G), gam = Gam[C-1]
+//   Aqk[t,j] = sum_c q_tc k_jc exp(G_tc - G_jc) (j <= t),  Akk = diag(beta) (same, j < t, k for q)
+//   T = (I + Akk)^-1,  W = T diag(beta)(Gam * k),  U' = T diag(beta) V
+//   U = U' - W S0,  O = scale (Gam*q) S0 + scale Aqk U,  S1 = diag(gam) S0 + (exp(G_C - G) * k)^T U
+// This is the WY/UT chunked form of the token recurrence; atomic-ops 0.1.0 (section
+// Features) names the same four forward stages: chunk scores, WY block solve, recompute,
+// inter-chunk scan.
+//
+// Scores use the boundary-split decay factorisation of the marin.community note
+// "factoring GDN-2 decay on TPU" (section Approach): each query row and key row is
+// scaled by its decay relative to the last token of the first block, so the cross-block
+// tile is one tensor-core product with every factor <= 1. Rows of the first block use
+// the chunk start as reference and rows of the second block reuse the boundary, so the
+// in-block tiles are products too; their key factors are >= 1 and stay below
+// exp(SAFE_SPREAD) whenever the block's decay spread does. A block whose spread is
+// larger (or every block, with GDN_FLAG_PAIRWISE_WITHIN_BLOCK) gets its in-block
+// scores from the direct pairwise sum on CUDA cores instead (four lanes per pair,
+// reduced with warp shuffles), which is what the note's kernel does in every block.
+//
+// Kernels
+//   chunk_prep_kernel      grid (chunks, B*H), 256 threads: A1-A5, writes the residual
+//                          records (scaled Aqk, T, -W, U', scaled Q-hat, K-tilde, gam)
+//   chunk_scan_fwd_kernel  grid (Dv/32, B*H), 128 threads: A6, fp32 state slice in
+//                          registers; chunk records arrive by cp.async.bulk on mbarriers
+#include "common.cuh"
+#include "kernels.h"
+
+namespace gdn {
+namespace {
+
+constexpr int PREP_THREADS = 256;
+constexpr int SCAN_THREADS = 128;
+// (i, j) of pair p in the lower triangle (diagonal included), row-major order
+__device__ __forceinline__ void tri_index(int p, int& i, int& j) {
+  int r = (int)((sqrtf(8.f * p + 1.f) - 1.f) * 0.5f);
+  while (r * (r + 1) / 2 > p) --r;
+  while ((r + 1) * (r + 2) / 2 <= p) ++r;
+  i = r;
+  j = p - r * (r + 1) / 2;
+}
+
+// In-place inverse of the unit lower triangular L = I + A, A strictly lower in M.
+// Diagonal and upper part of M are never read (taken as 1 and 0); the strictly lower
+// part of M receives that of T = L^-1. Forward substitution on the four 16x16 diagonal
+// blocks, then two doubling steps T21 = -T22 A21 T11 (16 -> 32 -> 64). fp32 throughout.
+template <int NTHR>
+__device__ void unit_lower_inverse64(FTile<C, C> M, FTile<BLK, BLK> X, int tid) {
+  const int warp = tid >> 5, lane = tid & 31;
+  if (warp < 4) {
+    const int o = warp * 16;
+    for (int r = 1; r < 16; ++r) {
+      float val = 0.f;
+      const int c = lane;
+      if (c < r) {
+        val = M.at(o + r, o + c);
+        for (int j = c + 1; j < r; ++j) val = fmaf(M.at(o + r, o + j), M.at(o + j, o + c), val);
+        val = -val;
+      }
+      __syncwarp();
+      if (c < r) M.at(o + r, o + c) = val;
+      __syncwarp();
+    }
+  }
+  __syncthreads();
+  auto tval = [&](int i, int j) -> float { return i == j ? 1.f : (i > j ? M.at(i, j) : 0.f); };
+  // 16 -> 32, two independent 32-blocks at offsets 0 and 32
+  for (int e = tid; e < 2 * 256; e += NTHR) {
+    const int p = e >> 8, i = (e >> 4) & 15, c = e & 15, o = p * 32;
+    // X = A21 T11 (A21 rows o+16+i, cols o..o+15)
+    float acc = M.at(o + 16 + i, o + c);
+    for (int j = c + 1; j < 16; ++j) acc = fmaf(M.at(o + 16 + i, o + j), M.at(o + j, o + c), acc);
+    X.at(p * 16 + i, c) = acc;
+  }
+  __syncthreads();
+  for (int e = tid; e < 2 * 256; e += NTHR) {
+    const int p = e >> 8, i = (e >> 4) & 15, c = e & 15, o = p * 32;
+    float acc = X.at(p * 16 + i, c);
+    for (int j = 0; j < i; ++j) acc = fmaf(M.at(o + 16 + i, o + 16 + j), X.at(p * 16 + j, c), acc);
+    M.at(o + 16 + i, o + c) = -acc;
+  }
+  __syncthreads();
+  // 32 -> 64
+  for (int e = tid; e < 1024; e += NTHR) {
+    const int i = e >> 5, c = e & 31;
+    float acc = M.at(32 + i, c);
+    for (int j = c + 1; j < 32; ++j) acc = fmaf(M.at(32 + i, j), tval(j, c), acc);
+    X.at(i, c) = acc;
+  }
+  __syncthreads();
+  for (int e = tid; e < 1024; e += NTHR) {
+    const int i = e >> 5, c = e & 31;
+    float acc = X.at(i, c);
+    for (int j = 0; j < i; ++j) acc = fmaf(tval(32 + i, 32 + j), X.at(j, c), acc);
+    M.at(32 + i, c) = -acc;
+  }
+  __syncthreads();
+}
+
+template <class T, int DK, int DV>
+struct PrepLayout {
+  static constexpr int ES = (int)sizeof(T);
+  static constexpr int MX = DK > DV ? DK : DV;
+  static constexpr int G = 0;                             // float [C][DK]
+  static constexpr int Q = a1k(G + C * DK * 4);           // q, later -W staging
+  static constexpr int K = a1k(Q + C * DK * ES);          // k, later U' staging  [C][MX]
+  static constexpr int X = a1k(K + C * MX * ES);          // query-side scaled rows, later beta*Gam*k
+  static constexpr int Y1 = a1k(X + C * DK * ES);         // key rows of block 1 * exp(-G)
+  static constexpr int Y2 = a1k(Y1 + BLK * DK * ES);      // key rows * exp(G_b - G), later beta*v
+  static constexpr int AKK = a1k(Y2 + C * MX * ES);       // float [C][C]: Akk, then T
+  static constexpr int TMP = AKK + C * C * 4;             // float [32][32]
+  static constexpr int TST = a1k(TMP + BLK * BLK * 4);    // [C][C] op: Aqk staging, then T
+  static constexpr int BETA = a1k(TST + C * C * ES);      // float [C]
+  static constexpr int BYTES = BETA + C * 4;
+};
+
+template <class T, int DK, int DV, bool PC>
+__global__ void __launch_bounds__(PREP_THREADS) chunk_prep_kernel(ChunkFwdArgs a) {
+  typedef PrepLayout<T, DK, DV> L;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = align1024(smem_raw);
+  FTile<C, DK> Gs{reinterpret_cast<float*>(sm + L::G)};
+  Tile<T, C, DK> qs{reinterpret_cast<T*>(sm + L::Q)};
+  Tile<T, C, DK> ks{reinterpret_cast<T*>(sm + L::K)};
+  Tile<T, C, DK> Xs{reinterpret_cast<T*>(sm + L::X)};
+  Tile<T, BLK, DK> Y1{reinterpret_cast<T*>(sm + L::Y1)};
+  Tile<T, C, DK> Y2{reinterpret_cast<T*>(sm + L::Y2)};
+  FTile<C, C> Akk{reinterpret_cast<float*>(sm + L::AKK)};
+  FTile<BLK, BLK> tmp{reinterpret_cast<float*>(sm + L::TMP)};
+  Tile<T, C, C> Tst{reinterpret_cast<T*>(sm + L::TST)};
+  float* beta_s = reinterpret_cast<float*>(sm + L::BETA);
+
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int n = blockIdx.x, bh = blockIdx.y, b = bh / a.H, h = bh % a.H;
+  const int N = a.T / C;
+  const size_t ch = (size_t)bh * N + n;
+  const size_t row0 = ((size_t)b * a.T + (size_t)n * C) * a.H + h;
+  const size_t rs = a.H;
+  constexpr int EPC = 16 / (int)sizeof(T);
+  const T* q = static_cast<const T*>(a.q);
+  const T* k = static_cast<const T*>(a.k);
+  const T* v = static_cast<const T*>(a.v);
+  const T* g = static_cast<const T*>(a.g);
+  const T* beta = static_cast<const T*>(a.beta);
+
+  // ---- load q, k, g (as fp32 G), beta
+  for (int i = tid; i < C * DK / EPC; i += PREP_THREADS) {
+    const int r = i / (DK / EPC), c = (i % (DK / EPC)) * EPC;
+    const size_t gi = (row0 + r * rs) * DK + c;
+    copy16(qs.ptr(r, c), q + gi);
+    copy16(ks.ptr(r, c), k + gi);
+    if (PC) {
+      __align__(16) T gv[EPC];
+      copy16(gv, g + gi);
+#pragma unroll
+      for (int e = 0; e < EPC; ++e) Gs.at(r, c + e) = to_f32(gv[e]);
+    }
+  }
+  if (!PC)
+    for (int i = tid; i < C * DK; i += PREP_THREADS) Gs.at(i / DK, i % DK) = to_f32(g[row0 + (i / DK) * rs]);
+  if (tid < C) beta_s[tid] = to_f32(beta[row0 + tid * rs]);
+  __syncthreads();
+
+  // ---- A1: cumulative log-decay per channel (inclusive)
+  for (int c = tid; c < DK; c += PREP_THREADS) {
+    float s = 0.f;
+    for (int r = 0; r < C; ++r) {
+      s += Gs.at(r, c);
+      Gs.at(r, c) = s;
+    }
+  }
+  __syncthreads();
+  const bool force = (a.flags & 1) != 0;
+  bool u1 = false, u2 = false;
+  for (int c = tid; c < DK; c += PREP_THREADS) {
+    u1 |= !(-Gs.at(BLK - 1, c) <= SAFE_SPREAD);
+    u2 |= !(Gs.at(BLK - 1, c) - Gs.at(C - 1, c) <= SAFE_SPREAD);
+  }
+  const bool unsafe1 = __syncthreads_or(u1 || force) != 0;
+  const bool unsafe2 = __syncthreads_or(u2 || force) != 0;
+
+  // ---- A2: scaled rows; scan records Q-hat (times scale), K-tilde, gam
+  T* qh_g = static_cast<T*>(a.res.qh) + ch * (C * DK);
+  T* kt_g = static_cast<T*>(a.res.kt) + ch * (C * DK);
+  for (int i = tid; i < C * DK / EPC; i += PREP_THREADS) {
+    const int r = i / (DK / EPC), c0 = (i % (DK / EPC)) * EPC;
+    __align__(16) T qv[EPC], kv[EPC], o1[EPC], o2[EPC], xq[EPC], y1[EPC], y2[EPC];
+    copy16(qv, qs.ptr(r, c0));
+    copy16(kv, ks.ptr(r, c0));
+#pragma unroll
+    for (int e = 0; e < EPC; ++e) {
+      const int c = c0 + e;
+      const float G = Gs.at(r, c), Gb = Gs.at(BLK - 1, c), GC = Gs.at(C - 1, c);
+      const float qf = to_f32(qv[e]), kf = to_f32(kv[e]);
+      const float gamr = __expf(G);
+      o1[e] = from_f32<T>(a.scale * gamr * qf);
+      o2[e] = from_f32<T>(__expf(GC - G) * kf);
+      xq[e] = from_f32<T>(qf * (r < BLK ? gamr : __expf(G - Gb)));
+      y2[e] = from_f32<T>((r < BLK || !unsafe2) ? kf * __expf(Gb - G) : 0.f);
+      y1[e] = from_f32<T>(unsafe1 ? 0.f : kf * __expf(-G));
+    }
+    const int off = Sw<T, C, DK>::off(r, c0);
+    copy16(qh_g + off, o1);
+    copy16(kt_g + off, o2);
+    copy16(Xs.ptr(r, c0), xq);
+    copy16(Y2.ptr(r, c0), y2);
+    if (r < BLK) copy16(Y1.ptr(r, c0), y1);
+  }
+  for (int c = tid; c < DK; c += PREP_THREADS) a.res.gam[ch * DK + c] = __expf(Gs.at(C - 1, c));
+  for (int i = tid; i < C * C / EPC; i += PREP_THREADS) {
+    const uint4 z = make_uint4(0, 0, 0, 0);
+    *reinterpret_cast<uint4*>(Tst.p + i * EPC) = z;
+  }
+  __syncthreads();
+
+  // ---- A3: score products. Warp w: rows 16 (w & 3) .. +15; block-1 rows take key
+  // columns 16 (w >> 2) .. +15 against Y1, block-2 rows columns 32 (w >> 2) .. +31 against Y2.
+  const int rg = warp & 3, half = warp >> 2, m0 = 16 * rg;
+  auto score_pass = [&](bool is_qk) {
+    if (rg < 2) {
+      if (unsafe1) return;
+      float acc[1][2][4];
+      zero(acc);
+      Gemm<T>::template run<1, 2>(acc, aview<false>(Xs), bview<false>(Y1), m0, 16 * half, 0, DK, lane);
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int r = m0 + frag_row(lane, e), j = 16 * half + 8 * nt + frag_col(lane, e);
+          if (is_qk) Tst.at(r, j) = from_f32<T>(j <= r ? a.scale * acc[0][nt][e] : 0.f);
+          else Akk.at(r, j) = j < r ? beta_s[r] * acc[0][nt][e] : 0.f;
+        }
+    } else {
+      float acc[1][4][4];
+      zero(acc);
+      Gemm<T>::template run<1, 4>(acc, aview<false>(Xs), bview<false>(Y2), m0, 32 * half, 0, DK, lane);
+#pragma unroll
+      for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int r = m0 + frag_row(lane, e), j = 32 * half + 8 * nt + frag_col(lane, e);
+          if (is_qk) Tst.at(r, j) = from_f32<T>(j <= r ? a.scale * acc[0][nt][e] : 0.f);
+          else Akk.at(r, j) = j < r ? beta_s[r] * acc[0][nt][e] : 0.f;
+        }
+    }
+  };
+  score_pass(true);
+  __syncthreads();
+  // query side for Akk: the keys, scaled like the queries were
+  for (int i = tid; i < C * DK / EPC; i += PREP_THREADS) {
+    const int r = i / (DK / EPC), c0 = (i % (DK / EPC)) * EPC;
+    __align__(16) T kv[EPC], xk[EPC];
+    copy16(kv, ks.ptr(r, c0));
+#pragma unroll
+    for (int e = 0; e < EPC; ++e) {
+      const int c = c0 + e;
+      const float G = Gs.at(r, c);
+      xk[e] = from_f32<T>(to_f32(kv[e]) * __expf(r < BLK ? G : G - Gs.at(BLK - 1, c)));
+    }
+    copy16(Xs.ptr(r, c0), xk);
+  }
+  __syncthreads();
+  score_pass(false);
+
+  // ---- A4: pairwise in-block scores for blocks outside the safe range
+  if (unsafe1 || unsafe2) {
+    __syncthreads();
+    for (int blk = 0; blk < 2; ++blk) {
+      if (!(blk == 0 ? unsafe1 : unsafe2)) continue;
+      const int bs = blk * BLK;
+      constexpr int NPAIR = BLK * (BLK + 1) / 2;
+      for (int base = 0; base < NPAIR; base += 8 * (PREP_THREADS / 32)) {
+        const int p = base + warp * 8 + (lane >> 2), quarter = lane & 3;
+        const bool valid = p < NPAIR;
+        int i = 0, j = 0;
+        float sq = 0.f, sk = 0.f;
+        if (valid) {
+          tri_index(p, i, j);
+          for (int c = quarter * (DK / 4); c < (quarter + 1) * (DK / 4); ++c) {
+            const float e = __expf(Gs.at(bs + i, c) - Gs.at(bs + j, c));
+            const float kj = to_f32(ks.at(bs + j, c)) * e;
+            sq = fmaf(to_f32(qs.at(bs + i, c)), kj, sq);
+            sk = fmaf(to_f32(ks.at(bs + i, c)), kj, sk);
+          }
+        }
+        sq += __shfl_xor_sync(0xffffffffu, sq, 1);
+        sk += __shfl_xor_sync(0xffffffffu, sk, 1);
+        sq += __shfl_xor_sync(0xffffffffu, sq, 2);
+        sk += __shfl_xor_sync(0xffffffffu, sk, 2);
+        if (valid && quarter == 0) {
+          Tst.at(bs + i, bs + j) = from_f32<T>(a.scale * sq);
+          if (i > j) Akk.at(bs + i, bs + j) = beta_s[bs + i] * sk;
+        }
+      }
+    }
+  }
+  __syncthreads();
+
+  // ---- store the scaled Aqk record, then A5: T = (I + Akk)^-1
+  {
+    T* dst = static_cast<T*>(a.res.aqk) + ch * (C * C);
+    for (int i = tid; i < C * C / EPC; i += PREP_THREADS) copy16(dst + i * EPC, Tst.p + i * EPC);
+  }
+  unit_lower_inverse64<PREP_THREADS>(Akk, tmp, tid);  // ends with __syncthreads
+  for (int i = tid; i < C * C; i += PREP_THREADS) {
+    const int r = i / C, c = i % C;
+    Tst.at(r, c) = from_f32<T>(r == c ? 1.f : (r > c ? Akk.at(r, c) : 0.f));
+  }
+  // beta * Gam * k (A operand rows of W's right factor) and beta * v
+  for (int i = tid; i < C * DK / EPC; i += PREP_THREADS) {
+    const int r = i / (DK / EPC), c0 = (i % (DK / EPC)) * EPC;
+    __align__(16) T kv[EPC], bk[EPC];
+    copy16(kv, ks.ptr(r, c0));
+#pragma unroll
+    for (int e = 0; e < EPC; ++e)
+      bk[e] = from_f32<T>(beta_s[r] * __expf(Gs.at(r, c0 + e)) * to_f32(kv[e]));
+    copy16(Xs.ptr(r, c0), bk);
+  }
+  Tile<T, C, DV> Bv{reinterpret_cast<T*>(sm + L::Y2)};
+  for (int i = tid; i < C * DV / EPC; i += PREP_THREADS) {
+    const int r = i / (DV / EPC), c0 = (i % (DV / EPC)) * EPC;
+    __align__(16) T vv[EPC], bv[EPC];
+    copy16(vv, v + (row0 + r * rs) * DV + c0);
+#pragma unroll
+    for (int e = 0; e < EPC; ++e) bv[e] = from_f32<T>(beta_s[r] * to_f32(vv[e]));
+    copy16(Bv.ptr(r, c0), bv);
+  }
+  __syncthreads();
+  {
+    T* dst = static_cast<T*>(a.res.tmat) + ch * (C * C);
+    for (int i = tid; i < C * C / EPC; i += PREP_THREADS) copy16(dst + i * EPC, Tst.p + i * EPC);
+  }
+
+  // ---- W (stored negated) and U': warp w rows 16 (w & 3), half the columns
+  {
+    constexpr int NW = DK / 16;  // n8 tiles per warp
+    float acc[1][NW][4];
+    zero(acc);
+    Gemm<T>::template run<1, NW>(acc, aview<false>(Tst), bview<true>(Xs), m0, half * (DK / 2), 0, C, lane);
+    Tile<T, C, DK> wst{reinterpret_cast<T*>(sm + L::Q)};
+#pragma unroll
+    for (int nt = 0; nt < NW; ++nt)
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
+        wst.at(m0 + frag_row(lane, e), half * (DK / 2) + 8 * nt + frag_col(lane, e)) = from_f32<T>(-acc[0][nt][e]);
+  }
+  {
+    constexpr int NU = DV / 16;
+    float acc[1][NU][4];
+    zero(acc);
+    Gemm<T>::template run<1, NU>(acc, aview<false>(Tst), bview<true>(Bv), m0, half * (DV / 2), 0, C, lane);
+    T* ust = reinterpret_cast<T*>(sm + L::K);
+#pragma unroll
+    for (int nt = 0; nt < NU; ++nt)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int r = m0 + frag_row(lane, e), c = half * (DV / 2) + 8 * nt + frag_col(lane, e);
+        ust[(c / NT) * (C * NT) + Sw<T, C, NT>::off(r, c % NT)] = from_f32<T>(acc[0][nt][e]);
+      }
+  }
+  __syncthreads();
+  {
+    T* dw = static_cast<T*>(a.res.wneg) + ch * (C * DK);
+    const T* sw = reinterpret_cast<const T*>(sm + L::Q);
+    for (int i = tid; i < C * DK / EPC; i += PREP_THREADS) copy16(dw + i * EPC, sw + i * EPC);
+    T* du = static_cast<T*>(a.res.up) + ch * (C * DV);
+    const T* su = reinterpret_cast<const T*>(sm + L::K);
+    for (int i = tid; i < C * DV / EPC; i += PREP_THREADS) copy16(du + i * EPC, su + i * EPC);
+  }
+}
+
+// ------------------------------------------------------------------ state scan
+template <class T, int DK>
+struct ScanLayout {
+  static constexpr int ES = (int)sizeof(T);
+  static constexpr int W = 0;                      // -W        [C][DK]
+  static constexpr int QH = W + C * DK * ES;       // scale Q-hat [C][DK]
+  static constexpr int KT = QH + C * DK * ES;      // K-tilde   [C][DK]
+  static constexpr int AQK = KT + C * DK * ES;     // scale Aqk [C][C]
+  static constexpr int UP = AQK + C * C * ES;      // U' slice  [C][NT] (then the output tile)
+  static constexpr int GAM = UP + C * NT * ES;     // float [DK]
+  static constexpr int STAGE = a1k(GAM + DK * 4);
+  static constexpr int STAGES = ES == 2 ? 2 : 1;
+  static constexpr int SS = STAGES * STAGE;        // state operand [DK][NT]
+  static constexpr int US = a1k(SS + DK * NT * ES);  // U [C][NT]
+  static constexpr int BAR = a1k(US + C * NT * ES);
+  static constexpr int BYTES = BAR + 64;
+  static constexpr uint32_t TX = (uint32_t)(3 * C * DK * ES + C * C * ES + C * NT * ES + DK * 4);
+};
+
+template <class T, int DK, int DV>
+__global__ void __launch_bounds__(SCAN_THREADS) chunk_scan_fwd_kernel(ChunkFwdArgs a) {
+  typedef ScanLayout<T, DK> L;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = align1024(smem_raw);
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int tile = blockIdx.x, bh = blockIdx.y, b = bh / a.H, h = bh % a.H;
+  const int N = a.T / C;
+  constexpr int NTILE = DV / NT;
+  constexpr int MTS = DK / 64;  // m16 tiles of state rows per warp
+  constexpr int NTT = NT / 8;
+  constexpr int EPC = 16 / (int)sizeof(T);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + L::BAR);
+  Tile<T, DK, NT> Ss{reinterpret_cast<T*>(sm + L::SS)};
+  Tile<T, C, NT> Us{reinterpret_cast<T*>(sm + L::US)};
+
+  // state slice, fragment layout: rows warp*16*MTS + 16 mt + frag_row, cols 8 nt + frag_col
+  float S[MTS][NTT][4];
+  const size_t sb = (size_t)bh * DK * DV;
+#pragma unroll
+  for (int mt = 0; mt < MTS; ++mt)
+#pragma unroll
+    for (int nt = 0; nt < NTT; ++nt)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int r = warp * 16 * MTS + 16 * mt + frag_row(lane, e);
+        const int c = tile * NT + 8 * nt + frag_col(lane, e);
+        S[mt][nt][e] = a.h0 ? a.h0[sb + (size_t)r * DV + c] : 0.f;
+      }
+
+  if (tid == 0) {
+    for (int s = 0; s < L::STAGES; ++s) mbar_init(&bars[s], 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+
+  auto issue = [&](int n, int s) {
+    uint8_t* st = sm + s * L::STAGE;
+    const size_t ch = (size_t)bh * N + n;
+    mbar_arrive_expect_tx(&bars[s], L::TX);
+    bulk_g2s(st + L::W, static_cast<const T*>(a.res.wneg) + ch * (C * DK), C * DK * sizeof(T), &bars[s]);
+    bulk_g2s(st + L::QH, static_cast<const T*>(a.res.qh) + ch * (C * DK), C * DK * sizeof(T), &bars[s]);
+    bulk_g2s(st + L::KT, static_cast<const T*>(a.res.kt) + ch * (C * DK), C * DK * sizeof(T), &bars[s]);
+    bulk_g2s(st + L::AQK, static_cast<const T*>(a.res.aqk) + ch * (C * C), C * C * sizeof(T), &bars[s]);
+    bulk_g2s(st + L::UP, static_cast<const T*>(a.res.up) + (ch * NTILE + tile) * (C * NT),
+             C * NT * sizeof(T), &bars[s]);
+    bulk_g2s(st + L::GAM, a.res.gam + ch * DK, DK * 4, &bars[s]);
+  };
+  if (tid == 0 && N > 0) issue(0, 0);
+
+  for (int n = 0; n < N; ++n) {
+    const int s = n % L::STAGES;
+    const uint32_t par = (uint32_t)(n / L::STAGES) & 1u;
+    if (L::STAGES == 2 && tid == 0 && n + 1 < N) issue(n + 1, (n + 1) % 2);
+    uint8_t* st = sm + s * L::STAGE;
+    Tile<T, C, DK> Wt{reinterpret_cast<T*>(st + L::W)};
+    Tile<T, C, DK> Qt{reinterpret_cast<T*>(st + L::QH)};
+    Tile<T, C, DK> Kt{reinterpret_cast<T*>(st + L::KT)};
+    Tile<T, C, C> At{reinterpret_cast<T*>(st + L::AQK)};
+    Tile<T, C, NT> Up{reinterpret_cast<T*>(st + L::UP)};
+    const float* gam = reinterpret_cast<const float*>(st + L::GAM);
+    const size_t ch = (size_t)bh * N + n;
+
+    // chunk-start state -> MMA operand copy
+#pragma unroll
+    for (int mt = 0; mt < MTS; ++mt)
+#pragma unroll
+      for (int nt = 0; nt < NTT; ++nt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          Ss.at(warp * 16 * MTS + 16 * mt + frag_row(lane, e), 8 * nt + frag_col(lane, e)) =
+              from_f32<T>(S[mt][nt][e]);
+    mbar_wait(&bars[s], par, a.err);
+    __syncthreads();
+    {  // residual: chunk-start state
+      T* dst = static_cast<T*>(a.res.state) + (ch * NTILE + tile) * (DK * NT);
+      for (int i = tid; i < DK * NT / EPC; i += SCAN_THREADS) copy16(dst + i * EPC, Ss.p + i * EPC);
+    }
+    // U = U' + (-W) S ; O = (scale Q-hat) S + (scale Aqk) U
+    float ws[1][NTT][4], o[1][NTT][4];
+    zero(ws);
+    zero(o);
+    Gemm<T>::template run<1, NTT>(ws, aview<false>(Wt), bview<true>(Ss), 16 * warp, 0, 0, DK, lane);
+    Gemm<T>::template run<1, NTT>(o, aview<false>(Qt), bview<true>(Ss), 16 * warp, 0, 0, DK, lane);
+#pragma unroll
+    for (int nt = 0; nt < NTT; ++nt)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int r = 16 * warp + frag_row(lane, e), c = 8 * nt + frag_col(lane, e);
+        Us.at(r, c) = from_f32<T>(to_f32(Up.at(r, c)) + ws[0][nt][e]);
+      }
+    __syncthreads();
+    {  // residual: U
+      T* dst = static_cast<T*>(a.res.u) + (ch * NTILE + tile) * (C * NT);
+      for (int i = tid; i < C * NT / EPC; i += SCAN_THREADS) copy16(dst + i * EPC, Us.p + i * EPC);
+    }
+    Gemm<T>::template run<1, NTT>(o, aview<false>(At), bview<true>(Us), 16 * warp, 0, 0, C, lane);
+#pragma unroll
+    for (int nt = 0; nt < NTT; ++nt)
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
+        Up.at(16 * warp + frag_row(lane, e), 8 * nt + frag_col(lane, e)) = from_f32<T>(o[0][nt][e]);
+    // S = diag(gam) S + K-tilde^T U
+#pragma unroll
+    for (int mt = 0; mt < MTS; ++mt)
+#pragma unroll
+      for (int nt = 0; nt < NTT; ++nt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) S[mt][nt][e] *= gam[warp * 16 * MTS + 16 * mt + frag_row(lane, e)];
+    Gemm<T>::template run<MTS, NTT>(S, aview<true>(Kt), bview<true>(Us), warp * 16 * MTS, 0, 0, C, lane);
+    __syncthreads();
+    {  // output tile
+      T* out = static_cast<T*>(a.out);
+      const size_t row0 = ((size_t)b * a.T + (size_t)n * C) * a.H + h;
+      for (int i = tid; i < C * NT / EPC; i += SCAN_THREADS) {
+        const int r = i / (NT / EPC), c0 = (i % (NT / EPC)) * EPC;
+        copy16(out + (row0 + (size_t)r * a.H) * DV + tile * NT + c0, Up.ptr(r, c0));
+      }
+    }
+    __syncthreads();
+    if (L::STAGES == 1 && tid == 0 && n + 1 < N) issue(n + 1, 0);
+  }
+  if (a.h_final) {
+#pragma unroll
+    for (int mt = 0; mt < MTS; ++mt)
+#pragma unroll
+      for (int nt = 0; nt < NTT; ++nt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int r = warp * 16 * MTS + 16 * mt + frag_row(lane, e);
+          const int c = tile * NT + 8 * nt + frag_col(lane, e);
+          a.h_final[sb + (size_t)r * DV + c] = S[mt][nt][e];
+        }
+  }
+}
+
+template <class T, int DK, int DV>
+cudaError_t launch_fwd_t(const ChunkFwdArgs& a, cudaStream_t s) {
+  const int N = a.T / C, BH = a.B * a.H;
+  {
+    const int bytes = PrepLayout<T, DK, DV>::BYTES + 1024;
+    auto kern = a.per_channel ? chunk_prep_kernel<T, DK, DV, true> : chunk_prep_kernel<T, DK, DV, false>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e != cudaSuccess) return e;
+    if (N > 0) {
+      prof_mark(K_PREP, s, true);
+      kern<<<dim3(N, BH), PREP_THREADS, bytes, s>>>(a);
+      prof_mark(K_PREP, s, false);
+    }
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  {
+    const int bytes = ScanLayout<T, DK>::BYTES + 1024;
+    auto kern = chunk_scan_fwd_kernel<T, DK, DV>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e != cudaSuccess) return e;
+    prof_mark(K_SCAN_FWD, s, true);
+    kern<<<dim3(DV / NT, BH), SCAN_THREADS, bytes, s>>>(a);
+    prof_mark(K_SCAN_FWD, s, false);
+    return cudaGetLastError();
+  }
+}
+
+template <class T>
+cudaError_t launch_fwd_dims(const ChunkFwdArgs& a, cudaStream_t s) {
+  return a.DK == 64 ? launch_fwd_t<T, 64, 64>(a, s) : launch_fwd_t<T, 128, 128>(a, s);
+}
+
+}  // namespace
+
+cudaError_t launch_chunk_fwd(const ChunkFwdArgs& a, cudaStream_t s) {
+  if (a.B * a.H == 0) return cudaSuccess;
+  return a.bf16 ? launch_fwd_dims<bf16>(a, s) : launch_fwd_dims<float>(a, s);
+}
+
+}  // namespace gdn

@@ -1,0 +1,371 @@
+// Device helpers shared by the gated delta rule kernels (sm_103a).
+//
+//  * element types: the "operand type" T of a kernel is __nv_bfloat16 (bf16 inputs,
+//    fp32 state / accumulation) or float (fp32 everything; tensor-core products use
+//    a three-term TF32 split so that they keep ~fp32 accuracy);
+//  * swizzled shared-memory tiles whose byte layout equals what a TMA copy with the
+//    matching swizzle mode writes, so a tile can be filled by a bulk copy of an image
+//    written in the same layout;
+//  * warp-level tensor-core products (mma.sync m16n8k16 bf16, m16n8k8 tf32x3) on
+//    those tiles, with either operand read as stored or transposed;
+//  * bulk async copies (cp.async.bulk) completing on an mbarrier, with bounded waits.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace gdn {
+
+typedef __nv_bfloat16 bf16;
+
+// ------------------------------------------------------------------ conversions
+__device__ __forceinline__ float to_f32(float x) { return x; }
+__device__ __forceinline__ float to_f32(bf16 x) { return __bfloat162float(x); }
+template <class T> __device__ __forceinline__ T from_f32(float x);
+template <> __device__ __forceinline__ float from_f32<float>(float x) { return x; }
+template <> __device__ __forceinline__ bf16 from_f32<bf16>(float x) { return __float2bfloat16_rn(x); }
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+// ------------------------------------------------------------------ swizzled tiles
+// A ROWS x COLS tile of T stored as column panels of 128 bytes (fewer when a row is
+// shorter). Inside a panel, row r occupies PANB bytes and the 16-byte chunk index is
+// XORed with (r / rows-per-128B) like the TMA SWIZZLE_{128,64,32}B modes. Eight
+// consecutive rows at the same logical 16-byte chunk land in eight different bank
+// groups, so ldmatrix reads are conflict free. Tiles must start 1024-byte aligned.
+template <class T, int ROWS, int COLS>
+struct Sw {
+  static constexpr int ES = (int)sizeof(T);
+  static constexpr int ROWB = COLS * ES;
+  static constexpr int PANB = ROWB >= 128 ? 128 : ROWB;
+  static constexpr int PW = PANB / ES;  // panel width in elements
+  static constexpr int ELEMS = ROWS * COLS;
+  static constexpr int BYTES = ELEMS * ES;
+  static_assert(PANB == 128 || PANB == 64 || PANB == 32, "tile row must be 32, 64 or >=128 bytes");
+  static_assert(COLS % PW == 0, "whole panels only");
+  __device__ __host__ static __forceinline__ int off(int r, int c) {
+    const int panel = c / PW;
+    int a = r * PANB + (c % PW) * ES;  // byte offset inside the panel
+    if (PANB == 128) a ^= ((a >> 7) & 7) << 4;
+    else if (PANB == 64) a ^= ((a >> 7) & 3) << 4;
+    else a ^= ((a >> 7) & 1) << 4;
+    return panel * (ROWS * PW) + a / ES;
+  }
+};
+
+template <class T, int ROWS, int COLS>
+struct Tile {
+  T* p;
+  typedef Sw<T, ROWS, COLS> L;
+  __device__ __forceinline__ T& at(int r, int c) const { return p[L::off(r, c)]; }
+  __device__ __forceinline__ T* ptr(int r, int c) const { return p + L::off(r, c); }
+};
+
+// A ROWS x COLS tile stored as COLS / TW consecutive ROWS x TW swizzled sub-tiles (the
+// value-column slices the state scan works on).
+template <class T, int ROWS, int COLS, int TW>
+struct TTile {
+  T* p;
+  typedef Sw<T, ROWS, TW> L;
+  __device__ __forceinline__ static int off(int r, int c) { return (c / TW) * (ROWS * TW) + L::off(r, c % TW); }
+  __device__ __forceinline__ T& at(int r, int c) const { return p[off(r, c)]; }
+  __device__ __forceinline__ T* ptr(int r, int c) const { return p + off(r, c); }
+};
+
+// Plain row-major fp32 matrix in shared memory (elementwise work, no MMA reads).
+template <int ROWS, int COLS, int PAD = 0>
+struct FTile {
+  float* p;
+  static constexpr int LD = COLS + PAD;
+  static constexpr int BYTES = ROWS * LD * 4;
+  __device__ __forceinline__ float& at(int r, int c) const { return p[r * LD + c]; }
+};
+
+// ------------------------------------------------------------------ ldmatrix / mma
+__device__ __forceinline__ void ldsm_x4(uint32_t* r, const void* p) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(smem_u32(p)));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t* r, const void* p) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(smem_u32(p)));
+}
+__device__ __forceinline__ void ldsm_x2(uint32_t* r, const void* p) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x2.shared.b16 {%0,%1}, [%2];\n"
+               : "=r"(r[0]), "=r"(r[1])
+               : "r"(smem_u32(p)));
+}
+__device__ __forceinline__ void ldsm_x2_t(uint32_t* r, const void* p) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x2.trans.shared.b16 {%0,%1}, [%2];\n"
+               : "=r"(r[0]), "=r"(r[1])
+               : "r"(smem_u32(p)));
+}
+__device__ __forceinline__ void mma_bf16(float* d, const uint32_t* a, const uint32_t* b) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};\n"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
+}
+__device__ __forceinline__ void mma_tf32(float* d, const uint32_t* a, const uint32_t* b) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};\n"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
+}
+__device__ __forceinline__ uint32_t tf32_rna(float x) {
+  uint32_t r;
+  asm("cvt.rna.tf32.f32 %0, %1;\n" : "=r"(r) : "f"(x));
+  return r;
+}
+// x = hi + lo with hi, lo representable in tf32 (three-term split products keep
+// about 21 significant bits)
+__device__ __forceinline__ void tf32_split(float x, uint32_t& hi, uint32_t& lo) {
+  hi = tf32_rna(x);
+  lo = tf32_rna(x - __uint_as_float(hi));
+}
+
+// ------------------------------------------------------------------ operand views
+// An A operand (M x K) or B operand (K x N) read from a tile either as stored
+// (A: tile rows = m; B: tile rows = n, "col" operand) or transposed
+// (A: tile rows = k; B: tile rows = k). r0/c0 shift the window inside the tile.
+template <class TileT, bool TRANS>
+struct AView {
+  TileT t;
+  int r0, c0;
+};
+template <class TileT, bool KROWS>
+struct BView {
+  TileT t;
+  int r0, c0;
+};
+template <bool TRANS, class TileT>
+__device__ __forceinline__ AView<TileT, TRANS> aview(TileT t, int r0 = 0, int c0 = 0) {
+  return AView<TileT, TRANS>{t, r0, c0};
+}
+// KROWS = true: B[k][n] = tile(k, n); false: B[k][n] = tile(n, k)
+template <bool KROWS, class TileT>
+__device__ __forceinline__ BView<TileT, KROWS> bview(TileT t, int r0 = 0, int c0 = 0) {
+  return BView<TileT, KROWS>{t, r0, c0};
+}
+
+// bf16 fragments ------------------------------------------------------------
+template <class TileT>
+__device__ __forceinline__ void load_a(uint32_t* a, const AView<TileT, false>& v, int m0, int k0, int lane) {
+  ldsm_x4(a, v.t.ptr(v.r0 + m0 + (lane & 15), v.c0 + k0 + (lane >> 4) * 8));
+}
+template <class TileT>
+__device__ __forceinline__ void load_a(uint32_t* a, const AView<TileT, true>& v, int m0, int k0, int lane) {
+  ldsm_x4_t(a, v.t.ptr(v.r0 + k0 + (lane & 7) + (lane >> 4) * 8, v.c0 + m0 + ((lane >> 3) & 1) * 8));
+}
+// two n8 tiles (n0, n0 + 8): b[0..1] first, b[2..3] second
+template <class TileT>
+__device__ __forceinline__ void load_b2(uint32_t* b, const BView<TileT, false>& v, int n0, int k0, int lane) {
+  ldsm_x4(b, v.t.ptr(v.r0 + n0 + (lane & 7) + (lane >> 4) * 8, v.c0 + k0 + ((lane >> 3) & 1) * 8));
+}
+template <class TileT>
+__device__ __forceinline__ void load_b2(uint32_t* b, const BView<TileT, true>& v, int n0, int k0, int lane) {
+  ldsm_x4_t(b, v.t.ptr(v.r0 + k0 + (lane & 7) + ((lane >> 3) & 1) * 8, v.c0 + n0 + (lane >> 4) * 8));
+}
+template <class TileT>
+__device__ __forceinline__ void load_b1(uint32_t* b, const BView<TileT, false>& v, int n0, int k0, int lane) {
+  ldsm_x2(b, v.t.ptr(v.r0 + n0 + (lane & 7), v.c0 + k0 + ((lane >> 3) & 1) * 8));
+}
+template <class TileT>
+__device__ __forceinline__ void load_b1(uint32_t* b, const BView<TileT, true>& v, int n0, int k0, int lane) {
+  ldsm_x2_t(b, v.t.ptr(v.r0 + k0 + (lane & 7) + ((lane >> 3) & 1) * 8, v.c0 + n0));
+}
+
+// fp32 (tf32x3) fragments ---------------------------------------------------
+template <class TileT>
+__device__ __forceinline__ float a_elem(const AView<TileT, false>& v, int m, int k) { return v.t.at(v.r0 + m, v.c0 + k); }
+template <class TileT>
+__device__ __forceinline__ float a_elem(const AView<TileT, true>& v, int m, int k) { return v.t.at(v.r0 + k, v.c0 + m); }
+template <class TileT>
+__device__ __forceinline__ float b_elem(const BView<TileT, false>& v, int k, int n) { return v.t.at(v.r0 + n, v.c0 + k); }
+template <class TileT>
+__device__ __forceinline__ float b_elem(const BView<TileT, true>& v, int k, int n) { return v.t.at(v.r0 + k, v.c0 + n); }
+
+// ------------------------------------------------------------------ warp GEMM
+// acc[mt][nt][0..3] += A[m0 + 16 mt .., k] * B[k, n0 + 8 nt ..] for k in [k_begin, k_end).
+// Accumulator layout is the mma C fragment: element (row g or g + 8, col 2t or 2t + 1)
+// with g = lane / 4, t = lane % 4. NT must be even for bf16 (pairs of n-tiles per ldmatrix).
+template <int MT, int NT, class AV, class BV>
+__device__ __forceinline__ void warp_gemm_bf16(float (&acc)[MT][NT][4], const AV& A, const BV& B,
+                                               int m0, int n0, int k_begin, int k_end, int lane) {
+  for (int k0 = k_begin; k0 < k_end; k0 += 16) {
+    uint32_t a[MT][4];
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt) load_a(a[mt], A, m0 + 16 * mt, k0, lane);
+#pragma unroll
+    for (int nt = 0; nt + 1 < NT; nt += 2) {
+      uint32_t b[4];
+      load_b2(b, B, n0 + 8 * nt, k0, lane);
+#pragma unroll
+      for (int mt = 0; mt < MT; ++mt) {
+        mma_bf16(acc[mt][nt], a[mt], b);
+        mma_bf16(acc[mt][nt + 1], a[mt], b + 2);
+      }
+    }
+    if (NT & 1) {
+      uint32_t b[2];
+      load_b1(b, B, n0 + 8 * (NT - 1), k0, lane);
+#pragma unroll
+      for (int mt = 0; mt < MT; ++mt) mma_bf16(acc[mt][NT - 1], a[mt], b);
+    }
+  }
+}
+
+template <int MT, int NT, class AV, class BV>
+__device__ __forceinline__ void warp_gemm_tf32x3(float (&acc)[MT][NT][4], const AV& A, const BV& B,
+                                                 int m0, int n0, int k_begin, int k_end, int lane) {
+  const int g = lane >> 2, t = lane & 3;
+  for (int k0 = k_begin; k0 < k_end; k0 += 8) {
+    uint32_t ah[MT][4], al[MT][4];
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt) {
+      const int m = m0 + 16 * mt;
+      tf32_split(a_elem(A, m + g, k0 + t), ah[mt][0], al[mt][0]);
+      tf32_split(a_elem(A, m + g + 8, k0 + t), ah[mt][1], al[mt][1]);
+      tf32_split(a_elem(A, m + g, k0 + t + 4), ah[mt][2], al[mt][2]);
+      tf32_split(a_elem(A, m + g + 8, k0 + t + 4), ah[mt][3], al[mt][3]);
+    }
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      const int n = n0 + 8 * nt;
+      uint32_t bh[2], bl[2];
+      tf32_split(b_elem(B, k0 + t, n + g), bh[0], bl[0]);
+      tf32_split(b_elem(B, k0 + t + 4, n + g), bh[1], bl[1]);
+#pragma unroll
+      for (int mt = 0; mt < MT; ++mt) {
+        mma_tf32(acc[mt][nt], al[mt], bh);
+        mma_tf32(acc[mt][nt], ah[mt], bl);
+        mma_tf32(acc[mt][nt], ah[mt], bh);
+      }
+    }
+  }
+}
+
+template <class T> struct Gemm;
+template <> struct Gemm<bf16> {
+  static constexpr int KSTEP = 16;
+  template <int MT, int NT, class AV, class BV>
+  __device__ static __forceinline__ void run(float (&acc)[MT][NT][4], const AV& A, const BV& B, int m0,
+                                             int n0, int kb, int ke, int lane) {
+    warp_gemm_bf16<MT, NT>(acc, A, B, m0, n0, kb, ke, lane);
+  }
+};
+template <> struct Gemm<float> {
+  static constexpr int KSTEP = 8;
+  template <int MT, int NT, class AV, class BV>
+  __device__ static __forceinline__ void run(float (&acc)[MT][NT][4], const AV& A, const BV& B, int m0,
+                                             int n0, int kb, int ke, int lane) {
+    warp_gemm_tf32x3<MT, NT>(acc, A, B, m0, n0, kb, ke, lane);
+  }
+};
+
+template <int MT, int NT>
+__device__ __forceinline__ void zero(float (&acc)[MT][NT][4]) {
+#pragma unroll
+  for (int i = 0; i < MT; ++i)
+#pragma unroll
+    for (int j = 0; j < NT; ++j)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) acc[i][j][e] = 0.f;
+}
+
+// Row / column of accumulator element e (0..3) of an m16n8 fragment.
+__device__ __forceinline__ int frag_row(int lane, int e) { return (lane >> 2) + ((e >> 1) << 3); }
+__device__ __forceinline__ int frag_col(int lane, int e) { return ((lane & 3) << 1) + (e & 1); }
+
+// ------------------------------------------------------------------ bulk copies
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;\n" ::"r"(smem_u32(bar)), "r"(count));
+}
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+}
+__device__ __forceinline__ void fence_proxy_async() {
+  asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(smem_u32(bar)),
+               "r"(bytes)
+               : "memory");
+}
+// global -> shared bulk copy (16-byte aligned addresses, size a multiple of 16)
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n" ::"r"(
+          smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+// shared -> global bulk copy, completion tracked with bulk groups
+__device__ __forceinline__ void bulk_s2g(void* dst, const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;\n" ::"l"(dst),
+               "r"(smem_u32(src)), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;\n" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_read0() {
+  asm volatile("cp.async.bulk.wait_group.read 0;\n" ::: "memory");
+}
+__device__ __forceinline__ void bulk_wait0() { asm volatile("cp.async.bulk.wait_group 0;\n" ::: "memory"); }
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Error word bits written by a kernel that gave up on a wait.
+enum : unsigned { ERR_WAIT_TIMEOUT = 1u };
+
+// Bounded wait on an mbarrier phase. Each try_wait already suspends for a
+// hardware-defined time; 1 << 22 tries is far longer than any copy here needs.
+// On time-out the error word gets ERR_WAIT_TIMEOUT and false is returned.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, unsigned* err) {
+  for (uint32_t i = 0; i < (1u << 22); ++i)
+    if (mbar_try_wait(bar, parity)) return true;
+  if (err) atomicOr(err, ERR_WAIT_TIMEOUT);
+  return false;
+}
+
+// 16-byte vector copy helpers
+__device__ __forceinline__ void copy16(void* dst, const void* src) {
+  *reinterpret_cast<uint4*>(dst) = *reinterpret_cast<const uint4*>(src);
+}
+
+// ------------------------------------------------------------------ misc helpers
+__host__ __device__ constexpr int a1k(int x) { return (x + 1023) / 1024 * 1024; }
+__device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
+  return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
+}
+// Ampere-style 16-byte asynchronous copies (used where the destination is swizzled per 16 bytes)
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
+template <int NPEND>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;\n" ::"n"(NPEND) : "memory");
+}
+__device__ __forceinline__ void store2(bf16* p, float x, float y) {
+  *reinterpret_cast<__nv_bfloat162*>(p) = __floats2bfloat162_rn(x, y);
+}
+__device__ __forceinline__ void store2(float* p, float x, float y) {
+  *reinterpret_cast<float2*>(p) = make_float2(x, y);
+}
+
+}  // namespace gdn

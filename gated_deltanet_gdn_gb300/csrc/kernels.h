@@ -1,0 +1,150 @@
+// Internal launch interface between the C ABI (api.cu) and the kernel files.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace gdn {
+
+constexpr int C = 64;       // chunk length (tokens)
+constexpr int BLK = 32;     // block length inside a chunk
+constexpr int NT = 32;      // value columns per state-scan CTA
+constexpr float SAFE_SPREAD = 80.f;  // max decay spread (nats) for row-scaled in-block scores
+
+// Per (batch, head) and chunk, the forward writes these records. Byte sizes of one record
+// for operand element size es; every record starts 1024-byte aligned inside its region.
+struct ResidualLayout {
+  // region base offsets in bytes from the residual pointer
+  size_t aqk, tmat, wneg, up, qh, kt, gam, state, u, total;
+  // bytes of one chunk-head record
+  size_t aqk_b, tmat_b, w_b, up_b, qh_b, kt_b, gam_b, state_b, u_b;
+};
+
+struct BwdWorkspaceLayout {
+  size_t du, dstate, dqh, dw, dkt, daqk, dgam, total;
+  size_t du_b, dstate_b, dqh_b, dw_b, dkt_b, daqk_b, dgam_b;
+};
+
+inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+inline ResidualLayout residual_layout(int B, int T, int H, int DK, int DV, int es) {
+  ResidualLayout L{};
+  const size_t n = (size_t)B * H * (T / C);
+  L.aqk_b = (size_t)C * C * es;
+  L.tmat_b = (size_t)C * C * es;
+  L.w_b = (size_t)C * DK * es;
+  L.up_b = (size_t)C * DV * es;
+  L.qh_b = (size_t)C * DK * es;
+  L.kt_b = (size_t)C * DK * es;
+  L.gam_b = (size_t)DK * 4;
+  L.state_b = (size_t)DK * DV * es;
+  L.u_b = (size_t)C * DV * es;
+  size_t off = 0;
+  auto put = [&](size_t& field, size_t rec) {
+    field = off;
+    off = align_up(off + rec * n, 1024);
+  };
+  put(L.aqk, L.aqk_b);
+  put(L.tmat, L.tmat_b);
+  put(L.wneg, L.w_b);
+  put(L.up, L.up_b);
+  put(L.qh, L.qh_b);
+  put(L.kt, L.kt_b);
+  put(L.gam, L.gam_b);
+  put(L.state, L.state_b);
+  put(L.u, L.u_b);
+  L.total = off;
+  return L;
+}
+
+inline BwdWorkspaceLayout bwd_workspace_layout(int B, int T, int H, int DK, int DV, int es) {
+  BwdWorkspaceLayout L{};
+  const size_t n = (size_t)B * H * (T / C);
+  L.du_b = (size_t)C * DV * es;
+  L.dstate_b = (size_t)DK * DV * es;
+  L.dqh_b = (size_t)C * DK * es;
+  L.dw_b = (size_t)C * DK * es;
+  L.dkt_b = (size_t)C * DK * es;
+  L.daqk_b = (size_t)C * C * es;
+  L.dgam_b = (size_t)DK * 4;
+  size_t off = 0;
+  auto put = [&](size_t& field, size_t rec) {
+    field = off;
+    off = align_up(off + rec * n, 1024);
+  };
+  put(L.du, L.du_b);
+  put(L.dstate, L.dstate_b);
+  put(L.dqh, L.dqh_b);
+  put(L.dw, L.dw_b);
+  put(L.dkt, L.dkt_b);
+  put(L.daqk, L.daqk_b);
+  put(L.dgam, L.dgam_b);
+  L.total = off;
+  return L;
+}
+
+// Pointers into the residual buffer, resolved on the host.
+struct ResidualPtrs {
+  void *aqk, *tmat, *wneg, *up, *qh, *kt;
+  float* gam;
+  void *state, *u;
+};
+struct BwdWorkspacePtrs {
+  void *du, *dstate, *dqh, *dw, *dkt, *daqk;
+  float* dgam;
+};
+
+struct ChunkFwdArgs {
+  int B, T, H, DK, DV, per_channel, bf16, flags;
+  const void *q, *k, *v, *g, *beta;
+  const float* h0;
+  float scale;
+  void* out;
+  float* h_final;
+  ResidualPtrs res;
+  unsigned* err;
+};
+
+struct ChunkBwdArgs {
+  int B, T, H, DK, DV, per_channel, bf16, flags;
+  const void *q, *k, *v, *g, *beta;
+  float scale;
+  ResidualPtrs res;
+  const void* dout;
+  const float* dh_final;
+  void *dq, *dk, *dv, *dg, *dbeta;
+  float* dh0;
+  BwdWorkspacePtrs ws;
+  unsigned* err;
+};
+
+struct RecurrentArgs {
+  int B, T, H, DK, DV, per_channel, bf16;
+  const void *q, *k, *v, *g, *beta;
+  const float* h0;
+  float scale;
+  void* out;
+  float* h_final;
+};
+
+// Kernel identifiers for the optional per-launch timing (gdn_profile_* in the C ABI).
+enum KernelId {
+  K_PREP = 0,      // chunk_prep_kernel
+  K_SCAN_FWD = 1,  // chunk_scan_fwd_kernel
+  K_SCAN_BWD = 2,  // chunk_scan_bwd_kernel
+  K_DSTATE = 3,    // chunk_dstate_kernel
+  K_GRADS = 4,     // chunk_grads_kernel
+  K_RECURRENT = 5, // recurrent_kernel
+  K_COUNT = 6
+};
+// Records a CUDA event on s before (begin = true) or after a launch when timing is on.
+void prof_mark(KernelId id, cudaStream_t s, bool begin);
+
+// Each returns a cudaError_t from the launches (cudaSuccess when all were accepted).
+cudaError_t launch_chunk_fwd(const ChunkFwdArgs& a, cudaStream_t s);
+cudaError_t launch_chunk_bwd(const ChunkBwdArgs& a, cudaStream_t s);
+cudaError_t launch_recurrent(const RecurrentArgs& a, cudaStream_t s);
+cudaError_t launch_chunk_grads(const ChunkBwdArgs& a, cudaStream_t s);  // part of launch_chunk_bwd
+
+}  // namespace gdn

@@ -1,0 +1,191 @@
+// Token-recurrent gated delta rule (prefill and decode are the same kernel).
+//
+// "gated-deltanet" kernel card, section Method: per token a decay, a read, a delta
+// scaled by the write gate, a rank-one write and a read with the query; the state is
+// the whole cost, so it is read from memory once and written once per call.
+//
+// GB300 layout: one CTA owns a (batch, head, 32-column value slice) of the fp32 state.
+// The delta rule never mixes value columns (each column of S evolves with the same
+// k, g, beta and its own v), so slicing Dv multiplies the number of CTAs by Dv / 32
+// without any exchange. Inside a CTA, 16 threads share a group of 4 value columns and
+// each holds Dk / 16 key rows of those columns in registers; the two Dk reductions per
+// token (S^T k and S^T q) are 16-lane butterfly shuffles in a fixed order, so a
+// sequence split into several calls gives bit-identical results. Token inputs are
+// staged through shared memory in batches of TB tokens with cp.async double buffering.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace gdn {
+namespace {
+
+constexpr int REC_COLS = 32;                 // value columns per CTA
+constexpr int REC_VEC = 4;                   // value columns per thread
+constexpr int REC_TPC = 16;                  // threads sharing a column group
+constexpr int REC_THREADS = (REC_COLS / REC_VEC) * REC_TPC;  // 128
+constexpr int TB = 8;                        // tokens per staged batch (static smem <= 48 KB)
+
+
+template <class T, int DK>
+struct RecSmem {
+  T q[2][TB][DK];
+  T k[2][TB][DK];
+  T v[2][TB][REC_COLS];
+  T graw[2][TB][DK];  // per-channel g (scalar g uses gs)
+  float a[TB][DK];    // exp(g) of the batch being computed
+  float gs[2][TB];
+  float beta[2][TB];
+};
+
+template <class T, int DK, bool PC>
+__global__ void __launch_bounds__(REC_THREADS) recurrent_kernel(RecurrentArgs p) {
+  constexpr int RPT = DK / REC_TPC;  // key rows per thread
+  __shared__ __align__(16) RecSmem<T, DK> sm;
+  const int tid = threadIdx.x;
+  const int cg = tid / REC_TPC;    // column group 0..7
+  const int part = tid % REC_TPC;  // row interleave 0..15
+  const int bh = blockIdx.y, b = bh / p.H, h = bh % p.H;
+  const int col0 = blockIdx.x * REC_COLS + cg * REC_VEC;
+  const int DV = p.DV, H = p.H, T_ = p.T;
+
+  // state slice: rows part + 16 i, columns col0 .. col0 + 3
+  float S[RPT][REC_VEC];
+  const size_t sbase = (size_t)bh * DK * DV;
+#pragma unroll
+  for (int i = 0; i < RPT; ++i) {
+    const int r = part + REC_TPC * i;
+    if (p.h0) {
+      const float4 x = *reinterpret_cast<const float4*>(p.h0 + sbase + (size_t)r * DV + col0);
+      S[i][0] = x.x; S[i][1] = x.y; S[i][2] = x.z; S[i][3] = x.w;
+    } else {
+      S[i][0] = S[i][1] = S[i][2] = S[i][3] = 0.f;
+    }
+  }
+
+  const T* q = static_cast<const T*>(p.q);
+  const T* k = static_cast<const T*>(p.k);
+  const T* v = static_cast<const T*>(p.v);
+  const T* g = static_cast<const T*>(p.g);
+  const T* beta = static_cast<const T*>(p.beta);
+  constexpr int EPC = 16 / (int)sizeof(T);  // elements per 16-byte copy
+
+  auto stage = [&](int buf, int t0) {
+    const int nt = min(TB, T_ - t0);
+    // q, k (and per-channel g): rows of DK elements
+    constexpr int CPR = DK / EPC;  // copies per row
+    for (int i = tid; i < nt * CPR; i += REC_THREADS) {
+      const int tt = i / CPR, c = (i % CPR) * EPC;
+      const size_t row = ((size_t)b * T_ + t0 + tt) * H + h;
+      cp_async16(&sm.q[buf][tt][c], q + row * DK + c);
+      cp_async16(&sm.k[buf][tt][c], k + row * DK + c);
+      if (PC) cp_async16(&sm.graw[buf][tt][c], g + row * DK + c);
+    }
+    constexpr int VPR = REC_COLS / EPC;
+    for (int i = tid; i < nt * VPR; i += REC_THREADS) {
+      const int tt = i / VPR, c = (i % VPR) * EPC;
+      const size_t row = ((size_t)b * T_ + t0 + tt) * H + h;
+      cp_async16(&sm.v[buf][tt][c], v + row * DV + blockIdx.x * REC_COLS + c);
+    }
+    if (tid < nt) {
+      const size_t row = ((size_t)b * T_ + t0 + tid) * H + h;
+      sm.beta[buf][tid] = to_f32(beta[row]);
+      if (!PC) sm.gs[buf][tid] = to_f32(g[row]);
+    }
+    cp_async_commit();
+  };
+
+  const int nbatch = (T_ + TB - 1) / TB;
+  if (nbatch > 0) stage(0, 0);
+  for (int bi = 0; bi < nbatch; ++bi) {
+    const int buf = bi & 1, t0 = bi * TB, nt = min(TB, T_ - t0);
+    cp_async_wait<0>();
+    __syncthreads();  // batch bi visible; everyone finished batch bi-1 (its buffer is free)
+    if (bi + 1 < nbatch) stage(buf ^ 1, t0 + TB);
+    if (PC) {
+      for (int i = tid; i < nt * DK; i += REC_THREADS) {
+        const int tt = i / DK, c = i % DK;
+        sm.a[tt][c] = expf(to_f32(sm.graw[buf][tt][c]));
+      }
+      __syncthreads();
+    }
+    for (int tt = 0; tt < nt; ++tt) {
+      const float bt = sm.beta[buf][tt];
+      const float as = PC ? 1.f : expf(sm.gs[buf][tt]);
+      float pv[REC_VEC] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int i = 0; i < RPT; ++i) {
+        const int r = part + REC_TPC * i;
+        const float a = PC ? sm.a[tt][r] : as;
+        const float kr = to_f32(sm.k[buf][tt][r]);
+#pragma unroll
+        for (int j = 0; j < REC_VEC; ++j) {
+          S[i][j] *= a;
+          pv[j] = fmaf(S[i][j], kr, pv[j]);
+        }
+      }
+#pragma unroll
+      for (int off = 1; off < REC_TPC; off <<= 1)
+#pragma unroll
+        for (int j = 0; j < REC_VEC; ++j) pv[j] += __shfl_xor_sync(0xffffffffu, pv[j], off);
+      float d[REC_VEC];
+#pragma unroll
+      for (int j = 0; j < REC_VEC; ++j) d[j] = bt * (to_f32(sm.v[buf][tt][cg * REC_VEC + j]) - pv[j]);
+      float ov[REC_VEC] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int i = 0; i < RPT; ++i) {
+        const int r = part + REC_TPC * i;
+        const float kr = to_f32(sm.k[buf][tt][r]);
+        const float qr = to_f32(sm.q[buf][tt][r]);
+#pragma unroll
+        for (int j = 0; j < REC_VEC; ++j) {
+          S[i][j] = fmaf(kr, d[j], S[i][j]);
+          ov[j] = fmaf(S[i][j], qr, ov[j]);
+        }
+      }
+#pragma unroll
+      for (int off = 1; off < REC_TPC; off <<= 1)
+#pragma unroll
+        for (int j = 0; j < REC_VEC; ++j) ov[j] += __shfl_xor_sync(0xffffffffu, ov[j], off);
+      if (part == 0) {
+        const size_t row = ((size_t)b * T_ + t0 + tt) * H + h;
+        T* o = static_cast<T*>(p.out) + row * DV + col0;
+        if (sizeof(T) == 4) {
+          *reinterpret_cast<float4*>(o) =
+              make_float4(p.scale * ov[0], p.scale * ov[1], p.scale * ov[2], p.scale * ov[3]);
+        } else {
+          __align__(8) T tmp[4];
+#pragma unroll
+          for (int j = 0; j < 4; ++j) tmp[j] = from_f32<T>(p.scale * ov[j]);
+          *reinterpret_cast<uint2*>(o) = *reinterpret_cast<const uint2*>(tmp);
+        }
+      }
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < RPT; ++i) {
+    const int r = part + REC_TPC * i;
+    *reinterpret_cast<float4*>(p.h_final + sbase + (size_t)r * DV + col0) =
+        make_float4(S[i][0], S[i][1], S[i][2], S[i][3]);
+  }
+}
+
+template <class T, int DK>
+cudaError_t launch_rec_t(const RecurrentArgs& a, cudaStream_t s) {
+  dim3 grid(a.DV / REC_COLS, a.B * a.H);
+  prof_mark(K_RECURRENT, s, true);
+  if (a.per_channel)
+    recurrent_kernel<T, DK, true><<<grid, REC_THREADS, 0, s>>>(a);
+  else
+    recurrent_kernel<T, DK, false><<<grid, REC_THREADS, 0, s>>>(a);
+  prof_mark(K_RECURRENT, s, false);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_recurrent(const RecurrentArgs& a, cudaStream_t s) {
+  if (a.B * a.H == 0) return cudaSuccess;
+  if (a.bf16) return a.DK == 64 ? launch_rec_t<bf16, 64>(a, s) : launch_rec_t<bf16, 128>(a, s);
+  return a.DK == 64 ? launch_rec_t<float, 64>(a, s) : launch_rec_t<float, 128>(a, s);
+}
+
+}  // namespace gdn

@@ -1,0 +1,171 @@
+/*
+ * gdn.h - C ABI of the GB300 (sm_103a) gated delta rule library (libgdn.so).
+ *
+ * The operation. For every batch b and head h the state S (Dk x Dv, fp32, row =
+ * key channel) evolves token by token:
+ *
+ *     S   <- diag(exp(g_t)) S              per-key-channel log-decay g_t <= 0
+ *     d    = beta_t (v_t - S^T k_t)         delta, scaled by the write gate
+ *     S   <- S + k_t d^T                    rank-one write
+ *     o_t  = scale * S^T q_t                read after the write
+ *
+ * Sources: "gated-deltanet" kernel card (hf kernels hub), section Method (the
+ * per-token decay, read, delta, write, read, and the state carried between
+ * calls in section Usage); marin.community note "factoring GDN-2 decay on TPU",
+ * section Background (one decay rate per key channel; a scalar per head is the
+ * special case the kernel card uses); atomic-ops 0.1.0, sections Quick start and
+ * API (the (q, k, v, g, scale, h0) -> (out, h_final) training call whose
+ * backward reuses forward residuals, seq_len a multiple of the chunk size).
+ *
+ * Layouts (contiguous, row-major):
+ *   q, k              [B, T, H, Dk]
+ *   v, out, dout      [B, T, H, Dv]
+ *   g                 [B, T, H, Dk] if dims.g_per_channel, else [B, T, H]
+ *   beta              [B, T, H]
+ *   h0, h_final,
+ *   dh_final, dh0     [B, H, Dk, Dv]   always float32
+ *   dq, dk, dv, dg,
+ *   dbeta             same shapes as q, k, v, g, beta
+ * dims.dtype is the element type of q, k, v, g, beta, out, dout and of every
+ * gradient: GDN_F32 (float) or GDN_BF16 (bfloat16). The state and every
+ * accumulation are float32 in both cases.
+ *
+ * Ownership and execution. Every tensor pointer is a DEVICE pointer owned by
+ * the caller; the library never allocates or frees device memory. Each call
+ * only enqueues kernels on `stream` (a cudaStream_t; NULL = legacy default
+ * stream) and returns; results are ready when the stream reaches that point.
+ * Calls keep no state between them and may run concurrently on different
+ * streams with disjoint buffers. Outputs must not alias inputs, except
+ * h_final == h0 in gdn_recurrent (in-place state carry).
+ *
+ * Errors. Arguments are validated before anything is enqueued; a failed
+ * check returns a gdn_status and enqueues nothing:
+ *   GDN_ERR_INVALID_ARG  NULL dims or required pointer, negative sizes, a
+ *                        pointer not aligned to 16 bytes, scale not finite
+ *   GDN_ERR_UNSUPPORTED  Dk or Dv not in {64, 128}, Dk != Dv on the chunked
+ *                        path, unknown dtype, a float32 chunked backward (the
+ *                        chunked backward is bfloat16 only), B * H > 65535
+ *   GDN_ERR_SHAPE        chunked calls with T not a multiple of 64
+ *   GDN_ERR_CUDA         a launch was rejected (cudaGetLastError); faults that
+ *                        happen later surface at the caller's next
+ *                        synchronisation on the stream
+ * Inputs are not clipped: non-finite values propagate like the recurrence
+ * itself (the rule diverges when beta |k|^2 > 2).
+ */
+#ifndef GDN_H
+#define GDN_H
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  GDN_OK = 0,
+  GDN_ERR_INVALID_ARG = 1,
+  GDN_ERR_UNSUPPORTED = 2,
+  GDN_ERR_SHAPE = 3,
+  GDN_ERR_CUDA = 4,
+  GDN_ERR_INTERNAL = 5
+} gdn_status;
+
+typedef enum { GDN_F32 = 0, GDN_BF16 = 1 } gdn_dtype;
+
+/* dims.flags bits */
+/* Score tiles inside each 32-token block are always computed pairwise on CUDA
+ * cores instead of from row-scaled tensor-core products (the library already
+ * does so by itself for any block whose decay spread makes the row scaling
+ * leave the safe exponent range). Results agree to rounding. */
+#define GDN_FLAG_PAIRWISE_WITHIN_BLOCK 1
+
+typedef struct {
+  int B, T, H;       /* batch, tokens, heads */
+  int Dk, Dv;        /* key and value widths: 64 or 128 each */
+  int g_per_channel; /* 1: g is [B,T,H,Dk]; 0: g is [B,T,H] (one decay per head) */
+  int dtype;         /* gdn_dtype */
+  int flags;         /* GDN_FLAG_* */
+} gdn_dims;
+
+/* Chunk size of the chunked path (tokens) and its split into two blocks. */
+#define GDN_CHUNK 64
+#define GDN_BLOCK 32
+
+/* Bytes of the residual buffer that gdn_chunk_fwd fills and gdn_chunk_bwd
+ * reads: per 64-token chunk and head, the chunk-start state, the chunk's
+ * decay-weighted score tile, its WY factors and the per-token deltas. Returns 0
+ * for invalid dims. The content is private to the library. */
+size_t gdn_chunk_residual_bytes(const gdn_dims* dims);
+
+/* Bytes of scratch that gdn_chunk_bwd needs (reverse-scan outputs and the
+ * per-chunk state-gradient products). Returns 0 for invalid dims. */
+size_t gdn_chunk_bwd_workspace_bytes(const gdn_dims* dims);
+
+/* Chunked forward (training / prefill), T a multiple of 64.
+ *   h0        initial state, NULL = zeros
+ *   scale     output scale (the Python binding passes Dk^-0.5 by default)
+ *   out       [B,T,H,Dv] result
+ *   h_final   final state, may be NULL
+ *   residuals gdn_chunk_residual_bytes(dims) bytes, REQUIRED (also for
+ *             forward-only use: it holds the chunk products between kernels),
+ *             256-byte aligned
+ * Steps: per-chunk cumulative log-decay, boundary-split decay-factorised
+ * scores (marin.community note, section Approach), the WY/UT triangular solve
+ * (atomic-ops Features: chunk scores -> WY block solve -> recompute ->
+ * inter-chunk scan), then the sequential state scan over chunks. */
+int gdn_chunk_fwd(const gdn_dims* dims, const void* q, const void* k, const void* v,
+                  const void* g, const void* beta, const float* h0, float scale, void* out,
+                  float* h_final, void* residuals, void* stream);
+
+/* Chunked backward. Same inputs as the forward plus the residuals it wrote,
+ * dout [B,T,H,Dv] and dh_final (NULL = zeros). Writes dq, dk, dv, dg, dbeta
+ * and dh0 (may be NULL). workspace: gdn_chunk_bwd_workspace_bytes(dims) bytes,
+ * 256-byte aligned. bfloat16 only (dims.dtype == GDN_BF16). */
+int gdn_chunk_bwd(const gdn_dims* dims, const void* q, const void* k, const void* v,
+                  const void* g, const void* beta, const float* h0, float scale,
+                  const void* residuals, const void* dout, const float* dh_final, void* dq,
+                  void* dk, void* dv, void* dg, void* dbeta, float* dh0, void* workspace,
+                  void* stream);
+
+/* Token-recurrent prefill / decode ("gated-deltanet" kernel card, sections
+ * Usage and Method): the exact recurrence in fp32, token by token, any T >= 0.
+ * Each state slice is read once and written once per call, and the per-token
+ * arithmetic does not depend on how a sequence is split into calls, so a
+ * sequence run in several calls (carrying h_final -> h0) equals one call
+ * bitwise. h0 NULL = zeros; h_final may equal h0 (in place). T = 0 copies h0
+ * to h_final. */
+int gdn_recurrent(const gdn_dims* dims, const void* q, const void* k, const void* v,
+                  const void* g, const void* beta, const float* h0, float scale, void* out,
+                  float* h_final, void* stream);
+
+/* Reads and clears the library's device error word on the current device
+ * (bit 1: a kernel gave up waiting for one of its own asynchronous copies).
+ * Synchronises the device. Returns GDN_OK when the word was zero,
+ * GDN_ERR_INTERNAL when it was not, GDN_ERR_CUDA if the read failed. */
+int gdn_check_device_error(void);
+
+/* Static description of a status code (never NULL). */
+const char* gdn_status_string(int status);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+int gdn_version(void);
+
+/* Optional per-launch timing, off by default. While enabled, every kernel the
+ * library launches is bracketed by two CUDA events recorded on the launch
+ * stream (one host thread, one device at a time). gdn_profile_enable(1)
+ * starts a fresh record, gdn_profile_enable(0) stops recording.
+ * gdn_profile_read(ms, launches, n) waits for the recorded events, writes for
+ * each kernel id < n the summed milliseconds and the launch count, clears the
+ * record and returns GDN_OK (GDN_ERR_CUDA if an event failed). Kernel ids:
+ * 0 chunk preparation, 1 forward state scan, 2 reverse state scan, 3 state
+ * products, 4 chunk gradients, 5 recurrent; gdn_kernel_name(id) names them
+ * ("" for an unknown id). Not part of the paper's method: instrumentation. */
+int gdn_profile_enable(int on);
+int gdn_profile_read(double* ms, int* launches, int n);
+const char* gdn_kernel_name(int id);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GDN_H */

@@ -1,0 +1,117 @@
+"""Host-side checks of the C ABI: the library builds, loads and exports every
+symbol include/gdn.h declares, sizes are consistent, and invalid arguments are
+rejected with status codes before anything reaches a GPU. No kernel runs here."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import gated_deltanet_gdn_gb300 as gdn
+from gated_deltanet_gdn_gb300 import binding
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "gdn.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    return gdn.load()
+
+
+def _declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(gdn_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_and_binding_agree():
+    assert _declared_functions() == sorted(binding.EXPORTED)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in _declared_functions():
+        assert hasattr(lib, name), name
+    assert gdn.gdn_version() == 100
+    assert lib.gdn_status_string(0).decode() == "ok"
+    for s in range(6):
+        assert lib.gdn_status_string(s)
+    assert b"unknown" in lib.gdn_status_string(99)
+
+
+def _dims(**kw):
+    base = dict(B=2, T=128, H=3, Dk=128, Dv=128, g_per_channel=1, dtype=binding.GDN_BF16, flags=0)
+    base.update(kw)
+    return binding.GdnDims(**base)
+
+
+def test_size_queries(lib):
+    d = _dims()
+    r = lib.gdn_chunk_residual_bytes(ctypes.byref(d))
+    w = lib.gdn_chunk_bwd_workspace_bytes(ctypes.byref(d))
+    n = 2 * 3 * 2  # chunk-heads
+    C, D = 64, 128
+    # Aqk, T, -W, U', Q-hat, K-tilde, state, U in bf16 plus gam in fp32 (each region 1 KiB aligned)
+    want_r = n * (2 * C * C * 2 + 5 * C * D * 2 + D * D * 2 + D * 4)
+    assert want_r <= r <= want_r + 9 * 1024
+    assert r % 1024 == 0 and w % 1024 == 0
+    d32 = _dims(dtype=binding.GDN_F32)
+    assert lib.gdn_chunk_residual_bytes(ctypes.byref(d32)) > r
+    assert lib.gdn_chunk_residual_bytes(ctypes.byref(_dims(T=100))) == 0  # T % 64 != 0
+    assert lib.gdn_chunk_residual_bytes(ctypes.byref(_dims(Dk=96))) == 0
+    assert lib.gdn_chunk_residual_bytes(None) == 0
+    # linear in the number of chunk-heads
+    r2 = lib.gdn_chunk_residual_bytes(ctypes.byref(_dims(T=256)))
+    assert abs(r2 - 2 * r) <= 9 * 1024
+
+
+def _fake(addr=1 << 20):
+    return ctypes.c_void_p(addr)
+
+
+def test_invalid_arguments_are_rejected_on_the_host(lib):
+    p = _fake()
+    f = ctypes.c_float(0.1)
+    fwd = lib.gdn_chunk_fwd
+    # NULL dims
+    assert fwd(None, p, p, p, p, p, None, f, p, None, p, None) == binding.GDN_ERR_INVALID_ARG
+    # unsupported widths / dtype / flags / shape
+    assert fwd(ctypes.byref(_dims(Dk=96)), p, p, p, p, p, None, f, p, None, p, None) == binding.GDN_ERR_UNSUPPORTED
+    assert fwd(ctypes.byref(_dims(Dk=64, Dv=128)), p, p, p, p, p, None, f, p, None, p, None) == binding.GDN_ERR_UNSUPPORTED
+    assert fwd(ctypes.byref(_dims(dtype=7)), p, p, p, p, p, None, f, p, None, p, None) == binding.GDN_ERR_UNSUPPORTED
+    assert fwd(ctypes.byref(_dims(flags=8)), p, p, p, p, p, None, f, p, None, p, None) == binding.GDN_ERR_INVALID_ARG
+    assert fwd(ctypes.byref(_dims(T=100)), p, p, p, p, p, None, f, p, None, p, None) == binding.GDN_ERR_SHAPE
+    assert fwd(ctypes.byref(_dims(B=-1)), p, p, p, p, p, None, f, p, None, p, None) == binding.GDN_ERR_INVALID_ARG
+    # NULL and misaligned required pointers, missing residuals, non-finite scale
+    assert fwd(ctypes.byref(_dims()), None, p, p, p, p, None, f, p, None, p, None) == binding.GDN_ERR_INVALID_ARG
+    assert fwd(ctypes.byref(_dims()), _fake((1 << 20) + 8), p, p, p, p, None, f, p, None, p, None) == binding.GDN_ERR_INVALID_ARG
+    assert fwd(ctypes.byref(_dims()), p, p, p, p, p, None, f, p, None, None, None) == binding.GDN_ERR_INVALID_ARG
+    assert fwd(ctypes.byref(_dims()), p, p, p, p, p, None, f, p, None, _fake((1 << 20) + 64), None) == binding.GDN_ERR_INVALID_ARG
+    assert fwd(ctypes.byref(_dims()), p, p, p, p, p, None, ctypes.c_float(float("nan")), p, None, p, None) == binding.GDN_ERR_INVALID_ARG
+    # empty problems are accepted without touching the device
+    assert fwd(ctypes.byref(_dims(B=0)), None, None, None, None, None, None, f, None, None, None, None) == binding.GDN_OK
+    # backward: float32 is not supported; workspace required
+    bwd = lib.gdn_chunk_bwd
+    args = [p, p, p, p, p, None, f, p, p, None, p, p, p, p, p, None, p, None]
+    assert bwd(ctypes.byref(_dims(dtype=binding.GDN_F32)), *args) == binding.GDN_ERR_UNSUPPORTED
+    bad = list(args)
+    bad[16] = None  # workspace
+    assert bwd(ctypes.byref(_dims()), *bad) == binding.GDN_ERR_INVALID_ARG
+    bad = list(args)
+    bad[8] = None  # dout
+    assert bwd(ctypes.byref(_dims()), *bad) == binding.GDN_ERR_INVALID_ARG
+    # recurrent: any T, mixed widths allowed; still validated
+    rec = lib.gdn_recurrent
+    assert rec(ctypes.byref(_dims(Dk=96)), p, p, p, p, p, None, f, p, p, None) == binding.GDN_ERR_UNSUPPORTED
+    assert rec(ctypes.byref(_dims(T=13)), p, p, p, p, p, None, f, p, None, None) == binding.GDN_ERR_INVALID_ARG
+    assert rec(ctypes.byref(_dims(B=0, T=5)), None, None, None, None, None, None, f, None, None, None) == binding.GDN_OK
+    # scalar gates only need element alignment
+    assert rec(ctypes.byref(_dims(T=13, g_per_channel=0)), p, p, p, _fake((1 << 20) + 3), p, None, f, p, p,
+               None) == binding.GDN_ERR_INVALID_ARG
+
+
+def test_binding_rejects_cpu_tensors():
+    import torch
+
+    q = torch.zeros(1, 64, 1, 64)
+    with pytest.raises(gdn.GdnError):
+        gdn.gdn_chunk_fwd(q, q, q, q, torch.zeros(1, 64, 1))
