@@ -21,6 +21,8 @@ GDN_ERR_UNSUPPORTED = 2
 GDN_ERR_SHAPE = 3
 GDN_ERR_CUDA = 4
 GDN_ERR_INTERNAL = 5
+GDN_ERR_SCRATCH_LIMIT = 6
+GDN_NOALLOC_SCRATCH_BYTES = 32 << 20
 GDN_F32 = 0
 GDN_BF16 = 1
 GDN_FLAG_PAIRWISE_WITHIN_BLOCK = 1
@@ -29,7 +31,8 @@ GDN_CHUNK = 64
 # every symbol include/gdn.h declares
 EXPORTED = ("gdn_chunk_residual_bytes", "gdn_chunk_bwd_workspace_bytes", "gdn_chunk_fwd",
             "gdn_chunk_bwd", "gdn_recurrent", "gdn_check_device_error", "gdn_status_string",
-            "gdn_version", "gdn_profile_enable", "gdn_profile_read", "gdn_kernel_name")
+            "gdn_version", "gdn_profile_enable", "gdn_profile_read", "gdn_kernel_name",
+            "gdn_chunk_fwd_noalloc")
 KERNEL_COUNT = 6
 
 
@@ -84,6 +87,8 @@ def load(build_if_needed: bool = True) -> ctypes.CDLL:
             lib.gdn_profile_read.restype = i
             lib.gdn_kernel_name.argtypes = [i]
             lib.gdn_kernel_name.restype = ctypes.c_char_p
+            lib.gdn_chunk_fwd_noalloc.argtypes = [pd, vp, vp, vp, vp, vp, vp, f, vp, vp, vp]
+            lib.gdn_chunk_fwd_noalloc.restype = i
             _lib = lib
     return _lib
 
@@ -164,6 +169,24 @@ def gdn_chunk_fwd(q, k, v, g, beta, h0=None, scale: Optional[float] = None, *, o
                                   _stream(dev))
     _check("gdn_chunk_fwd", st)
     return out, h_final, residuals
+
+
+def gdn_chunk_fwd_noalloc(q, k, v, g, beta, h0=None, scale: Optional[float] = None, *, out,
+                          h_final, flags: int = 0) -> Tuple[torch.Tensor, torch.Tensor]:
+    """Chunked forward through the entry point that allocates nothing: the caller
+    passes the outputs, the library keeps the residual records in its static
+    device array (calls sharing it must not overlap on the GPU)."""
+    dev = q.device
+    _require(dict(q=q, k=k, v=v, g=g, beta=beta, h0=h0, out=out, h_final=h_final), dev)
+    dims = make_dims(q, v, g, flags)
+    if scale is None:
+        scale = dims.Dk ** -0.5
+    with torch.cuda.device(dev):
+        st = load().gdn_chunk_fwd_noalloc(ctypes.byref(dims), _ptr(q), _ptr(k), _ptr(v), _ptr(g),
+                                          _ptr(beta), _ptr(h0), float(scale), _ptr(out), _ptr(h_final),
+                                          _stream(dev))
+    _check("gdn_chunk_fwd_noalloc", st)
+    return out, h_final
 
 
 def gdn_chunk_bwd(q, k, v, g, beta, h0, residuals, dout, dh_final=None,

@@ -252,6 +252,7 @@ const char* gdn_status_string(int s) {
     case GDN_ERR_SHAPE: return "T must be a multiple of 64 on the chunked path";
     case GDN_ERR_CUDA: return "CUDA launch or runtime error";
     case GDN_ERR_INTERNAL: return "a kernel reported an internal error (bounded wait timed out)";
+    case GDN_ERR_SCRATCH_LIMIT: return "problem needs more residual scratch than the static GDN_NOALLOC_SCRATCH_BYTES array";
     default: return "unknown status";
   }
 }

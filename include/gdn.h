@@ -67,7 +67,9 @@ typedef enum {
   GDN_ERR_UNSUPPORTED = 2,
   GDN_ERR_SHAPE = 3,
   GDN_ERR_CUDA = 4,
-  GDN_ERR_INTERNAL = 5
+  GDN_ERR_INTERNAL = 5,
+  GDN_ERR_SCRATCH_LIMIT = 6 /* gdn_chunk_fwd_noalloc: problem needs more than
+                               GDN_NOALLOC_SCRATCH_BYTES of residual scratch */
 } gdn_status;
 
 typedef enum { GDN_F32 = 0, GDN_BF16 = 1 } gdn_dtype;
@@ -126,6 +128,35 @@ int gdn_chunk_bwd(const gdn_dims* dims, const void* q, const void* k, const void
                   const void* residuals, const void* dout, const float* dh_final, void* dq,
                   void* dk, void* dv, void* dg, void* dbeta, float* dh0, void* workspace,
                   void* stream);
+
+/* Chunked forward that allocates nothing and takes no residual buffer.
+ *
+ * The paper has no counterpart to this call; it exists for callers that cannot
+ * call cudaMalloc: code that runs where device memory is owned by someone else
+ * (an inference server or plugin host with a fixed memory pool, an embedded or
+ * real-time loop that forbids allocation after start-up, a runtime whose
+ * allocator would have to be re-entered from a callback). Inputs and outputs
+ * are the caller's, exactly as in gdn_chunk_fwd; only the residual records the
+ * forward passes between its kernels live in a static device array compiled
+ * into the library, GDN_NOALLOC_SCRATCH_BYTES (32 MiB) on every GPU that loads
+ * the library, held until the process exits. That fits up to 255 chunk-heads
+ * (B * H * T/64) at Dk = Dv = 128 in bf16 (127 in fp32), e.g. B=1, H=3,
+ * T=4096; larger problems return GDN_ERR_SCRATCH_LIMIT, before anything is
+ * enqueued, and must use gdn_chunk_fwd.
+ *
+ * The first call on a device resolves the array's device address there (with
+ * that device current); make that first call before any stream capture. Every
+ * call shares the one array: calls whose work overlaps on the GPU (on two
+ * streams, or from two threads) race on it and must be serialised by the
+ * caller. The array keeps the last call's contents; nothing in it needs to
+ * start at zero because each call writes every record before reading it. No
+ * cudaMalloc, cudaFree or allocating library routine is called. The residual
+ * records are not available afterwards, so this call cannot feed
+ * gdn_chunk_bwd. Arguments and other errors as gdn_chunk_fwd. */
+#define GDN_NOALLOC_SCRATCH_BYTES (32u << 20)
+int gdn_chunk_fwd_noalloc(const gdn_dims* dims, const void* q, const void* k, const void* v,
+                          const void* g, const void* beta, const float* h0, float scale,
+                          void* out, float* h_final, void* stream);
 
 /* Token-recurrent prefill / decode ("gated-deltanet" kernel card, sections
  * Usage and Method): the exact recurrence in fp32, token by token, any T >= 0.
