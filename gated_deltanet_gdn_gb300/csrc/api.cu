@@ -78,10 +78,14 @@ BwdWorkspacePtrs workspace_ptrs(const gdn_dims* d, void* base) {
   w.du = b + L.du;
   w.dstate = b + L.dstate;
   w.dqh = b + L.dqh;
-  w.dw = b + L.dw;
+  w.dbk = b + L.dbk;
   w.dkt = b + L.dkt;
   w.daqk = b + L.daqk;
+  w.dakk = b + L.dakk;
   w.dgam = reinterpret_cast<float*>(b + L.dgam);
+  w.dbv = reinterpret_cast<float*>(b + L.dbv);
+  w.dbpart = reinterpret_cast<float*>(b + L.dbpart);
+  w.dgpart = reinterpret_cast<float*>(b + L.dgpart);
   return w;
 }
 
@@ -100,7 +104,8 @@ bool g_prof_failed = false;
 
 const char* kKernelNames[K_COUNT] = {"chunk_prep_kernel",    "chunk_scan_fwd_kernel",
                                      "chunk_scan_bwd_kernel", "chunk_dstate_kernel",
-                                     "chunk_grads_kernel",    "recurrent_kernel"};
+                                     "chunk_grads_kernel",    "recurrent_kernel",
+                                     "chunk_bwd_finalize_kernel"};
 
 }  // namespace
 

@@ -29,7 +29,7 @@ namespace gdn {
 namespace {
 
 constexpr int RSCAN_THREADS = 128;
-constexpr int DST_THREADS = 128;
+constexpr int DST_THREADS = 256;
 
 
 // ------------------------------------------------------------------ reverse state scan
@@ -173,14 +173,22 @@ __global__ void __launch_bounds__(RSCAN_THREADS) chunk_scan_bwd_kernel(ChunkBwdA
 }
 
 // ------------------------------------------------------------------ state products
+// Per chunk: everything that contracts over the value columns. With Y = T^T dU:
+//   dv = beta Y, dbeta_v = rowsum(Y * V), dQ-hat = scale dO S0^T, dBk = -Y S0^T,
+//   dK-tilde = U dS1^T, dAqk = scale dO U^T (j <= t), dAkk = -Y U^T (j < t),
+//   dgam = rowsum(dS1 * S0).
 template <int DK, int DV>
 struct DstLayout {
-  static constexpr int DO = 0;                      // dO   [C][DV]
-  static constexpr int U = a1k(DO + C * DV * 2);    // U    [C][DV] (NT slices)
-  static constexpr int DU = a1k(U + C * DV * 2);    // dU   [C][DV] (NT slices)
-  static constexpr int S0 = a1k(DU + C * DV * 2);   // S0   [DK][DV] (NT slices)
-  static constexpr int DS1 = a1k(S0 + DK * DV * 2); // dS1  [DK][DV] (NT slices)
-  static constexpr int BYTES = a1k(DS1 + DK * DV * 2);
+  static constexpr int TM = 0;                       // T    [C][C]
+  static constexpr int DO = a1k(TM + C * C * 2);     // dO   [C][DV]
+  static constexpr int V = a1k(DO + C * DV * 2);     // v    [C][DV]
+  static constexpr int U = a1k(V + C * DV * 2);      // U    [C][DV] (NT slices)
+  static constexpr int DU = a1k(U + C * DV * 2);     // dU   [C][DV] (NT slices), then Y
+  static constexpr int S0 = a1k(DU + C * DV * 2);    // S0   [DK][DV] (NT slices)
+  static constexpr int DS1 = a1k(S0 + DK * DV * 2);  // dS1  [DK][DV] (NT slices)
+  static constexpr int BETA = a1k(DS1 + DK * DV * 2);
+  static constexpr int DB = BETA + C * 4;            // float [2][C]
+  static constexpr int BYTES = DB + 2 * C * 4;
 };
 
 template <int DK, int DV>
@@ -194,18 +202,27 @@ __global__ void __launch_bounds__(DST_THREADS) chunk_dstate_kernel(ChunkBwdArgs 
   const int N = a.T / C;
   const size_t ch = (size_t)bh * N + n;
   constexpr int EPC = 8;
+  Tile<T, C, C> Ts{reinterpret_cast<T*>(sm + L::TM)};
   Tile<T, C, DV> dOs{reinterpret_cast<T*>(sm + L::DO)};
+  Tile<T, C, DV> Vs{reinterpret_cast<T*>(sm + L::V)};
   TTile<T, C, DV, NT> Us{reinterpret_cast<T*>(sm + L::U)};
   TTile<T, C, DV, NT> dUs{reinterpret_cast<T*>(sm + L::DU)};
   TTile<T, DK, DV, NT> S0s{reinterpret_cast<T*>(sm + L::S0)};
   TTile<T, DK, DV, NT> dS1s{reinterpret_cast<T*>(sm + L::DS1)};
+  float* beta_s = reinterpret_cast<float*>(sm + L::BETA);
+  float* db_s = reinterpret_cast<float*>(sm + L::DB);
   const T* dout = static_cast<const T*>(a.dout);
+  const T* v = static_cast<const T*>(a.v);
   const size_t row0 = ((size_t)b * a.T + (size_t)n * C) * a.H + h;
+  const size_t rs = a.H;
   for (int i = tid; i < C * DV / EPC; i += DST_THREADS) {
     const int r = i / (DV / EPC), c0 = (i % (DV / EPC)) * EPC;
-    cp_async16(dOs.ptr(r, c0), dout + (row0 + (size_t)r * a.H) * DV + c0);
+    cp_async16(dOs.ptr(r, c0), dout + (row0 + r * rs) * DV + c0);
+    cp_async16(Vs.ptr(r, c0), v + (row0 + r * rs) * DV + c0);
   }
   {
+    const T* st = static_cast<const T*>(a.res.tmat) + ch * (C * C);
+    for (int i = tid; i < C * C / EPC; i += DST_THREADS) cp_async16(Ts.p + i * EPC, st + i * EPC);
     const T* su = static_cast<const T*>(a.res.u) + ch * (C * DV);
     const T* sdu = static_cast<const T*>(a.ws.du) + ch * (C * DV);
     for (int i = tid; i < C * DV / EPC; i += DST_THREADS) {
@@ -220,63 +237,103 @@ __global__ void __launch_bounds__(DST_THREADS) chunk_dstate_kernel(ChunkBwdArgs 
     }
   }
   cp_async_commit();
+  if (tid < C) beta_s[tid] = to_f32(static_cast<const T*>(a.beta)[row0 + tid * rs]);
   cp_async_wait<0>();
   __syncthreads();
 
-  // dgam_c = sum_v dS1[c][v] S0[c][v]
-  for (int c = tid; c < DK; c += DST_THREADS) {
+  const int m0 = 16 * (warp & 3), hf = warp >> 2;
+  // Y = T^T dU; dv = beta Y; dbeta_v = rowsum(Y * V)
+  constexpr int NWV = DV / 16;
+  float y[1][NWV][4];
+  zero(y);
+  Gemm<T>::template run<1, NWV>(y, aview<true>(Ts), bview<true>(dUs), m0, hf * (DV / 2), 0, C, lane);
+  {
+    float db[2] = {0.f, 0.f};
+    T* dv = static_cast<T*>(a.dv);
+#pragma unroll
+    for (int nt = 0; nt < NWV; ++nt)
+#pragma unroll
+      for (int e = 0; e < 4; e += 2) {
+        const int r = m0 + frag_row(lane, e), c = hf * (DV / 2) + 8 * nt + frag_col(lane, e);
+        db[e >> 1] += y[0][nt][e] * to_f32(Vs.at(r, c)) + y[0][nt][e + 1] * to_f32(Vs.at(r, c + 1));
+        store2(dv + (row0 + r * rs) * DV + c, beta_s[r] * y[0][nt][e], beta_s[r] * y[0][nt][e + 1]);
+      }
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      db[i] += __shfl_xor_sync(0xffffffffu, db[i], 1);
+      db[i] += __shfl_xor_sync(0xffffffffu, db[i], 2);
+    }
+    if ((lane & 3) == 0) {
+      db_s[hf * C + m0 + (lane >> 2)] = db[0];
+      db_s[hf * C + m0 + (lane >> 2) + 8] = db[1];
+    }
+  }
+  __syncthreads();  // dU consumed: Y takes its place
+  Tile<T, C, DV> Ys{reinterpret_cast<T*>(sm + L::DU)};
+#pragma unroll
+  for (int nt = 0; nt < NWV; ++nt)
+#pragma unroll
+    for (int e = 0; e < 4; ++e)
+      Ys.at(m0 + frag_row(lane, e), hf * (DV / 2) + 8 * nt + frag_col(lane, e)) = from_f32<T>(y[0][nt][e]);
+  if (tid < C) a.ws.dbv[ch * C + tid] = db_s[tid] + db_s[C + tid];
+  for (int c = tid; c < DK; c += DST_THREADS) {  // dgam_c = sum_v dS1[c][v] S0[c][v]
     float acc = 0.f;
-    for (int v = 0; v < DV; ++v) acc = fmaf(to_f32(dS1s.at(c, v)), to_f32(S0s.at(c, v)), acc);
-    static_cast<float*>(a.ws.dgam)[ch * DK + c] = acc;
+    for (int v2 = 0; v2 < DV; v2 += 2) {
+      const __nv_bfloat162 x = *reinterpret_cast<const __nv_bfloat162*>(dS1s.ptr(c, v2));
+      const __nv_bfloat162 z = *reinterpret_cast<const __nv_bfloat162*>(S0s.ptr(c, v2));
+      acc = fmaf(__low2float(x), __low2float(z), acc);
+      acc = fmaf(__high2float(x), __high2float(z), acc);
+    }
+    a.ws.dgam[ch * DK + c] = acc;
   }
-  // C x DK products, warp w rows 16 w; two halves of the columns at a time
-  constexpr int NH = DK / 16;  // n8 tiles per half
-  T* dqh = static_cast<T*>(a.ws.dqh) + ch * (C * DK);
-  T* dw = static_cast<T*>(a.ws.dw) + ch * (C * DK);
-  T* dkt = static_cast<T*>(a.ws.dkt) + ch * (C * DK);
-  for (int hf = 0; hf < 2; ++hf) {
-    const int n0 = hf * (DK / 2);
+  __syncthreads();
+
+  // C x DK products: warp rows m0, columns hf * DK / 2 .. + DK / 2
+  constexpr int NH = DK / 16;
+  const int n0 = hf * (DK / 2);
+  auto store_cdk = [&](void* base, const float (&acc)[1][NH][4], float mul) {
+    T* dst = static_cast<T*>(base) + ch * (C * DK);
+#pragma unroll
+    for (int nt = 0; nt < NH; ++nt)
+#pragma unroll
+      for (int e = 0; e < 4; e += 2) {
+        const int r = m0 + frag_row(lane, e), c = n0 + 8 * nt + frag_col(lane, e);
+        store2(dst + Sw<T, C, DK>::off(r, c), mul * acc[0][nt][e], mul * acc[0][nt][e + 1]);
+      }
+  };
+  {
     float acc[1][NH][4];
-    zero(acc);  // dQ-hat = scale dO S0^T
-    Gemm<T>::template run<1, NH>(acc, aview<false>(dOs), bview<false>(S0s), 16 * warp, n0, 0, DV, lane);
-#pragma unroll
-    for (int nt = 0; nt < NH; ++nt)
-#pragma unroll
-      for (int e = 0; e < 4; e += 2) {
-        const int r = 16 * warp + frag_row(lane, e), c = n0 + 8 * nt + frag_col(lane, e);
-        store2(dqh + Sw<T, C, DK>::off(r, c), a.scale * acc[0][nt][e], a.scale * acc[0][nt][e + 1]);
-      }
-    zero(acc);  // dW = -dU S0^T
-    Gemm<T>::template run<1, NH>(acc, aview<false>(dUs), bview<false>(S0s), 16 * warp, n0, 0, DV, lane);
-#pragma unroll
-    for (int nt = 0; nt < NH; ++nt)
-#pragma unroll
-      for (int e = 0; e < 4; e += 2) {
-        const int r = 16 * warp + frag_row(lane, e), c = n0 + 8 * nt + frag_col(lane, e);
-        store2(dw + Sw<T, C, DK>::off(r, c), -acc[0][nt][e], -acc[0][nt][e + 1]);
-      }
-    zero(acc);  // dK-tilde = U dS1^T
-    Gemm<T>::template run<1, NH>(acc, aview<false>(Us), bview<false>(dS1s), 16 * warp, n0, 0, DV, lane);
-#pragma unroll
-    for (int nt = 0; nt < NH; ++nt)
-#pragma unroll
-      for (int e = 0; e < 4; e += 2) {
-        const int r = 16 * warp + frag_row(lane, e), c = n0 + 8 * nt + frag_col(lane, e);
-        store2(dkt + Sw<T, C, DK>::off(r, c), acc[0][nt][e], acc[0][nt][e + 1]);
-      }
-  }
-  {  // dAqk = scale dO U^T, masked j <= t
-    float acc[1][8][4];
     zero(acc);
-    Gemm<T>::template run<1, 8>(acc, aview<false>(dOs), bview<false>(Us), 16 * warp, 0, 0, DV, lane);
+    Gemm<T>::template run<1, NH>(acc, aview<false>(dOs), bview<false>(S0s), m0, n0, 0, DV, lane);
+    store_cdk(a.ws.dqh, acc, a.scale);
+    zero(acc);
+    Gemm<T>::template run<1, NH>(acc, aview<false>(Ys), bview<false>(S0s), m0, n0, 0, DV, lane);
+    store_cdk(a.ws.dbk, acc, -1.f);
+    zero(acc);
+    Gemm<T>::template run<1, NH>(acc, aview<false>(Us), bview<false>(dS1s), m0, n0, 0, DV, lane);
+    store_cdk(a.ws.dkt, acc, 1.f);
+  }
+  // C x C products: warp rows m0, columns 32 hf .. +31 (block-1 rows see no block-2 columns)
+  {
+    const int c0 = 32 * hf;
+    const bool dead = m0 < BLK && hf == 1;
+    float aq[1][4][4], ak[1][4][4];
+    zero(aq);
+    zero(ak);
+    if (!dead) {
+      Gemm<T>::template run<1, 4>(aq, aview<false>(dOs), bview<false>(Us), m0, c0, 0, DV, lane);
+      Gemm<T>::template run<1, 4>(ak, aview<false>(Ys), bview<false>(Us), m0, c0, 0, DV, lane);
+    }
     T* da = static_cast<T*>(a.ws.daqk) + ch * (C * C);
+    T* dk = static_cast<T*>(a.ws.dakk) + ch * (C * C);
 #pragma unroll
-    for (int nt = 0; nt < 8; ++nt)
+    for (int nt = 0; nt < 4; ++nt)
 #pragma unroll
       for (int e = 0; e < 4; e += 2) {
-        const int r = 16 * warp + frag_row(lane, e), j = 8 * nt + frag_col(lane, e);
-        store2(da + Sw<T, C, C>::off(r, j), j <= r ? a.scale * acc[0][nt][e] : 0.f,
-               j + 1 <= r ? a.scale * acc[0][nt][e + 1] : 0.f);
+        const int r = m0 + frag_row(lane, e), j = c0 + 8 * nt + frag_col(lane, e);
+        const int off = Sw<T, C, C>::off(r, j);
+        store2(da + off, j <= r ? a.scale * aq[0][nt][e] : 0.f, j + 1 <= r ? a.scale * aq[0][nt][e + 1] : 0.f);
+        store2(dk + off, j < r ? -ak[0][nt][e] : 0.f, j + 1 < r ? -ak[0][nt][e + 1] : 0.f);
       }
   }
 }

@@ -103,18 +103,56 @@ template <class T, int DK, int DV>
 struct PrepLayout {
   static constexpr int ES = (int)sizeof(T);
   static constexpr int MX = DK > DV ? DK : DV;
-  static constexpr int G = 0;                             // float [C][DK]
-  static constexpr int Q = a1k(G + C * DK * 4);           // q, later -W staging
-  static constexpr int K = a1k(Q + C * DK * ES);          // k, later U' staging  [C][MX]
-  static constexpr int X = a1k(K + C * MX * ES);          // query-side scaled rows, later beta*Gam*k
-  static constexpr int Y1 = a1k(X + C * DK * ES);         // key rows of block 1 * exp(-G)
-  static constexpr int Y2 = a1k(Y1 + BLK * DK * ES);      // key rows * exp(G_b - G), later beta*v
-  static constexpr int AKK = a1k(Y2 + C * MX * ES);       // float [C][C]: Akk, then T
-  static constexpr int TMP = AKK + C * C * 4;             // float [32][32]
-  static constexpr int TST = a1k(TMP + BLK * BLK * 4);    // [C][C] op: Aqk staging, then T
-  static constexpr int BETA = a1k(TST + C * C * ES);      // float [C]
+  static constexpr int RK = C * MX * ES;
+  static constexpr int RX = C * MX * ES > C * C * 4 ? C * MX * ES : C * C * 4;
+  static constexpr int RY = C * MX * ES > BLK * BLK * 4 ? C * MX * ES : BLK * BLK * 4;
+  static constexpr int G = 0;                         // float [C][DK] cumulative log-decay
+  static constexpr int K = a1k(G + C * DK * 4);       // k; later -W staging
+  static constexpr int X = a1k(K + RK);               // q -> query-side rows; key-side k; Akk/T (fp32); beta*v
+  static constexpr int Y = a1k(X + RX);               // raw g; key-side rows; inverse scratch; beta*Gam*k; U' staging
+  static constexpr int TST = a1k(Y + RY);             // [C][C]: scale*Aqk staging, then T
+  static constexpr int BETA = a1k(TST + C * C * ES);  // float [C]
   static constexpr int BYTES = BETA + C * 4;
 };
+
+// In-block pairwise scores (A4) for the blocks flagged unsafe: 4 lanes per (i, j) pair,
+// each summing a quarter of the channels, reduced with two xor shuffles. Writes
+// scale * sum q k E into the Aqk staging tile and beta_i * sum k k E (i > j) into Akk.
+template <class T, int DK, int NTHR>
+__device__ __noinline__ void prep_pairwise(bool unsafe1, bool unsafe2, const T* q, size_t row0, size_t rs,
+                                           Tile<T, C, DK> ks, FTile<C, DK> Gs, Tile<T, C, C> Tst,
+                                           FTile<C, C> Akk, const float* beta_s, float scale, int tid) {
+  const int warp = tid >> 5, lane = tid & 31;
+  for (int blk = 0; blk < 2; ++blk) {
+    if (!(blk == 0 ? unsafe1 : unsafe2)) continue;
+    const int bs = blk * BLK;
+    constexpr int NPAIR = BLK * (BLK + 1) / 2;
+    for (int base = 0; base < NPAIR; base += 8 * (NTHR / 32)) {
+      const int p = base + warp * 8 + (lane >> 2), quarter = lane & 3;
+      const bool valid = p < NPAIR;
+      int i = 0, j = 0;
+      float sq = 0.f, sk = 0.f;
+      if (valid) {
+        tri_index(p, i, j);
+        const T* qi = q + (row0 + (size_t)(bs + i) * rs) * DK;
+        for (int c = quarter * (DK / 4); c < (quarter + 1) * (DK / 4); ++c) {
+          const float e = __expf(Gs.at(bs + i, c) - Gs.at(bs + j, c));
+          const float kj = to_f32(ks.at(bs + j, c)) * e;
+          sq = fmaf(to_f32(qi[c]), kj, sq);
+          sk = fmaf(to_f32(ks.at(bs + i, c)), kj, sk);
+        }
+      }
+      sq += __shfl_xor_sync(0xffffffffu, sq, 1);
+      sk += __shfl_xor_sync(0xffffffffu, sk, 1);
+      sq += __shfl_xor_sync(0xffffffffu, sq, 2);
+      sk += __shfl_xor_sync(0xffffffffu, sk, 2);
+      if (valid && quarter == 0) {
+        Tst.at(bs + i, bs + j) = from_f32<T>(scale * sq);
+        if (i > j) Akk.at(bs + i, bs + j) = beta_s[bs + i] * sk;
+      }
+    }
+  }
+}
 
 template <class T, int DK, int DV, bool PC>
 __global__ void __launch_bounds__(PREP_THREADS) chunk_prep_kernel(ChunkFwdArgs a) {
@@ -122,13 +160,9 @@ __global__ void __launch_bounds__(PREP_THREADS) chunk_prep_kernel(ChunkFwdArgs a
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = align1024(smem_raw);
   FTile<C, DK> Gs{reinterpret_cast<float*>(sm + L::G)};
-  Tile<T, C, DK> qs{reinterpret_cast<T*>(sm + L::Q)};
   Tile<T, C, DK> ks{reinterpret_cast<T*>(sm + L::K)};
   Tile<T, C, DK> Xs{reinterpret_cast<T*>(sm + L::X)};
-  Tile<T, BLK, DK> Y1{reinterpret_cast<T*>(sm + L::Y1)};
-  Tile<T, C, DK> Y2{reinterpret_cast<T*>(sm + L::Y2)};
-  FTile<C, C> Akk{reinterpret_cast<float*>(sm + L::AKK)};
-  FTile<BLK, BLK> tmp{reinterpret_cast<float*>(sm + L::TMP)};
+  Tile<T, C, DK> Ys{reinterpret_cast<T*>(sm + L::Y)};
   Tile<T, C, C> Tst{reinterpret_cast<T*>(sm + L::TST)};
   float* beta_s = reinterpret_cast<float*>(sm + L::BETA);
 
@@ -139,234 +173,208 @@ __global__ void __launch_bounds__(PREP_THREADS) chunk_prep_kernel(ChunkFwdArgs a
   const size_t row0 = ((size_t)b * a.T + (size_t)n * C) * a.H + h;
   const size_t rs = a.H;
   constexpr int EPC = 16 / (int)sizeof(T);
+  constexpr int CPR = DK / EPC;  // 16-byte chunks per row
   const T* q = static_cast<const T*>(a.q);
   const T* k = static_cast<const T*>(a.k);
   const T* v = static_cast<const T*>(a.v);
   const T* g = static_cast<const T*>(a.g);
   const T* beta = static_cast<const T*>(a.beta);
 
-  // ---- load q, k, g (as fp32 G), beta
-  for (int i = tid; i < C * DK / EPC; i += PREP_THREADS) {
-    const int r = i / (DK / EPC), c = (i % (DK / EPC)) * EPC;
+  // ---- asynchronous loads: k -> K, q -> X, per-channel g (raw) -> Y
+  T* graw = reinterpret_cast<T*>(sm + L::Y);
+  for (int i = tid; i < C * CPR; i += PREP_THREADS) {
+    const int r = i / CPR, c = (i % CPR) * EPC;
     const size_t gi = (row0 + r * rs) * DK + c;
-    copy16(qs.ptr(r, c), q + gi);
-    copy16(ks.ptr(r, c), k + gi);
-    if (PC) {
-      __align__(16) T gv[EPC];
-      copy16(gv, g + gi);
-#pragma unroll
-      for (int e = 0; e < EPC; ++e) Gs.at(r, c + e) = to_f32(gv[e]);
-    }
+    cp_async16(ks.ptr(r, c), k + gi);
+    cp_async16(Xs.ptr(r, c), q + gi);
+    if (PC) cp_async16(graw + r * DK + c, g + gi);
   }
+  cp_async_commit();
+  if (tid < C) beta_s[tid] = to_f32(beta[row0 + tid * rs]);
   if (!PC)
     for (int i = tid; i < C * DK; i += PREP_THREADS) Gs.at(i / DK, i % DK) = to_f32(g[row0 + (i / DK) * rs]);
-  if (tid < C) beta_s[tid] = to_f32(beta[row0 + tid * rs]);
+  cp_async_wait<0>();
+  __syncthreads();
+  if (PC)
+    for (int i = tid; i < C * DK; i += PREP_THREADS) Gs.at(i / DK, i % DK) = to_f32(graw[i]);
   __syncthreads();
 
-  // ---- A1: cumulative log-decay per channel (inclusive)
-  for (int c = tid; c < DK; c += PREP_THREADS) {
+  // ---- A1: inclusive cumulative log-decay per channel, two threads per channel
+  for (int u = tid; u < 2 * DK; u += PREP_THREADS) {
+    const int c = u % DK, r0 = (u / DK) * BLK;
     float s = 0.f;
-    for (int r = 0; r < C; ++r) {
+#pragma unroll 8
+    for (int r = r0; r < r0 + BLK; ++r) {
       s += Gs.at(r, c);
       Gs.at(r, c) = s;
     }
   }
   __syncthreads();
+  for (int u = tid; u < DK; u += PREP_THREADS) {
+    const float base = Gs.at(BLK - 1, u);
+#pragma unroll 8
+    for (int r = BLK; r < C; ++r) Gs.at(r, u) += base;
+  }
+  __syncthreads();
+  // Reference point for every row: the boundary b = last token of the first block.
+  // Factor ranges: block 1 queries exp(G_t - G_b) <= exp(G_0 - G_b); block 2 keys
+  // exp(G_b - G_j) <= exp(G_b - G_C-1). Each must stay inside the fp32/bf16 range.
   const bool force = (a.flags & 1) != 0;
   bool u1 = false, u2 = false;
   for (int c = tid; c < DK; c += PREP_THREADS) {
-    u1 |= !(-Gs.at(BLK - 1, c) <= SAFE_SPREAD);
+    u1 |= !(Gs.at(0, c) - Gs.at(BLK - 1, c) <= SAFE_SPREAD);
     u2 |= !(Gs.at(BLK - 1, c) - Gs.at(C - 1, c) <= SAFE_SPREAD);
   }
   const bool unsafe1 = __syncthreads_or(u1 || force) != 0;
   const bool unsafe2 = __syncthreads_or(u2 || force) != 0;
 
-  // ---- A2: scaled rows; scan records Q-hat (times scale), K-tilde, gam
+  // ---- A2: scan records (scale Q-hat, K-tilde, gam) and the row-scaled score operands
   T* qh_g = static_cast<T*>(a.res.qh) + ch * (C * DK);
   T* kt_g = static_cast<T*>(a.res.kt) + ch * (C * DK);
-  for (int i = tid; i < C * DK / EPC; i += PREP_THREADS) {
-    const int r = i / (DK / EPC), c0 = (i % (DK / EPC)) * EPC;
-    __align__(16) T qv[EPC], kv[EPC], o1[EPC], o2[EPC], xq[EPC], y1[EPC], y2[EPC];
-    copy16(qv, qs.ptr(r, c0));
+  for (int i = tid; i < C * CPR; i += PREP_THREADS) {
+    const int r = i / CPR, c0 = (i % CPR) * EPC;
+    const bool dead_q = r < BLK ? unsafe1 : false;   // query rows whose factor may overflow
+    const bool dead_k = r < BLK ? false : unsafe2;   // key rows whose factor may overflow
+    __align__(16) T qv[EPC], kv[EPC], o1[EPC], o2[EPC], xq[EPC], yk[EPC];
+    copy16(qv, Xs.ptr(r, c0));
     copy16(kv, ks.ptr(r, c0));
 #pragma unroll
     for (int e = 0; e < EPC; ++e) {
       const int c = c0 + e;
       const float G = Gs.at(r, c), Gb = Gs.at(BLK - 1, c), GC = Gs.at(C - 1, c);
       const float qf = to_f32(qv[e]), kf = to_f32(kv[e]);
-      const float gamr = __expf(G);
-      o1[e] = from_f32<T>(a.scale * gamr * qf);
+      o1[e] = from_f32<T>(a.scale * __expf(G) * qf);
       o2[e] = from_f32<T>(__expf(GC - G) * kf);
-      xq[e] = from_f32<T>(qf * (r < BLK ? gamr : __expf(G - Gb)));
-      y2[e] = from_f32<T>((r < BLK || !unsafe2) ? kf * __expf(Gb - G) : 0.f);
-      y1[e] = from_f32<T>(unsafe1 ? 0.f : kf * __expf(-G));
+      xq[e] = from_f32<T>(dead_q ? 0.f : qf * __expf(G - Gb));
+      yk[e] = from_f32<T>(dead_k ? 0.f : kf * __expf(Gb - G));
     }
     const int off = Sw<T, C, DK>::off(r, c0);
     copy16(qh_g + off, o1);
     copy16(kt_g + off, o2);
     copy16(Xs.ptr(r, c0), xq);
-    copy16(Y2.ptr(r, c0), y2);
-    if (r < BLK) copy16(Y1.ptr(r, c0), y1);
+    copy16(Ys.ptr(r, c0), yk);
   }
   for (int c = tid; c < DK; c += PREP_THREADS) a.res.gam[ch * DK + c] = __expf(Gs.at(C - 1, c));
-  for (int i = tid; i < C * C / EPC; i += PREP_THREADS) {
-    const uint4 z = make_uint4(0, 0, 0, 0);
-    *reinterpret_cast<uint4*>(Tst.p + i * EPC) = z;
-  }
   __syncthreads();
 
-  // ---- A3: score products. Warp w: rows 16 (w & 3) .. +15; block-1 rows take key
-  // columns 16 (w >> 2) .. +15 against Y1, block-2 rows columns 32 (w >> 2) .. +31 against Y2.
-  const int rg = warp & 3, half = warp >> 2, m0 = 16 * rg;
-  auto score_pass = [&](bool is_qk) {
-    if (rg < 2) {
-      if (unsafe1) return;
-      float acc[1][2][4];
-      zero(acc);
-      Gemm<T>::template run<1, 2>(acc, aview<false>(Xs), bview<false>(Y1), m0, 16 * half, 0, DK, lane);
+  // ---- A3: scores. Warp w: rows 16 (w & 3) .. +15, key columns 32 (w >> 2) .. +31.
+  // Block-1 rows never see block-2 keys; unsafe blocks leave their in-block tile to A4.
+  const int rg = warp & 3, hf = warp >> 2, m0 = 16 * rg, n0 = 32 * hf;
+  const bool skip = (m0 < BLK) && (hf == 1 || unsafe1);
+  float acc[1][4][4];
+  zero(acc);
+  if (!skip) Gemm<T>::template run<1, 4>(acc, aview<false>(Xs), bview<false>(Ys), m0, n0, 0, DK, lane);
 #pragma unroll
-      for (int nt = 0; nt < 2; ++nt)
+  for (int nt = 0; nt < 4; ++nt)
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int r = m0 + frag_row(lane, e), j = 16 * half + 8 * nt + frag_col(lane, e);
-          if (is_qk) Tst.at(r, j) = from_f32<T>(j <= r ? a.scale * acc[0][nt][e] : 0.f);
-          else Akk.at(r, j) = j < r ? beta_s[r] * acc[0][nt][e] : 0.f;
-        }
-    } else {
-      float acc[1][4][4];
-      zero(acc);
-      Gemm<T>::template run<1, 4>(acc, aview<false>(Xs), bview<false>(Y2), m0, 32 * half, 0, DK, lane);
-#pragma unroll
-      for (int nt = 0; nt < 4; ++nt)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int r = m0 + frag_row(lane, e), j = 32 * half + 8 * nt + frag_col(lane, e);
-          if (is_qk) Tst.at(r, j) = from_f32<T>(j <= r ? a.scale * acc[0][nt][e] : 0.f);
-          else Akk.at(r, j) = j < r ? beta_s[r] * acc[0][nt][e] : 0.f;
-        }
+    for (int e = 0; e < 4; ++e) {
+      const int r = m0 + frag_row(lane, e), j = n0 + 8 * nt + frag_col(lane, e);
+      Tst.at(r, j) = from_f32<T>(j <= r ? a.scale * acc[0][nt][e] : 0.f);
     }
-  };
-  score_pass(true);
   __syncthreads();
-  // query side for Akk: the keys, scaled like the queries were
-  for (int i = tid; i < C * DK / EPC; i += PREP_THREADS) {
-    const int r = i / (DK / EPC), c0 = (i % (DK / EPC)) * EPC;
+  for (int i = tid; i < C * CPR; i += PREP_THREADS) {  // query side for Akk: the keys
+    const int r = i / CPR, c0 = (i % CPR) * EPC;
+    const bool dead_q = r < BLK ? unsafe1 : false;
     __align__(16) T kv[EPC], xk[EPC];
     copy16(kv, ks.ptr(r, c0));
 #pragma unroll
-    for (int e = 0; e < EPC; ++e) {
-      const int c = c0 + e;
-      const float G = Gs.at(r, c);
-      xk[e] = from_f32<T>(to_f32(kv[e]) * __expf(r < BLK ? G : G - Gs.at(BLK - 1, c)));
-    }
+    for (int e = 0; e < EPC; ++e)
+      xk[e] = from_f32<T>(dead_q ? 0.f : to_f32(kv[e]) * __expf(Gs.at(r, c0 + e) - Gs.at(BLK - 1, c0 + e)));
     copy16(Xs.ptr(r, c0), xk);
   }
   __syncthreads();
-  score_pass(false);
-
-  // ---- A4: pairwise in-block scores for blocks outside the safe range
-  if (unsafe1 || unsafe2) {
-    __syncthreads();
-    for (int blk = 0; blk < 2; ++blk) {
-      if (!(blk == 0 ? unsafe1 : unsafe2)) continue;
-      const int bs = blk * BLK;
-      constexpr int NPAIR = BLK * (BLK + 1) / 2;
-      for (int base = 0; base < NPAIR; base += 8 * (PREP_THREADS / 32)) {
-        const int p = base + warp * 8 + (lane >> 2), quarter = lane & 3;
-        const bool valid = p < NPAIR;
-        int i = 0, j = 0;
-        float sq = 0.f, sk = 0.f;
-        if (valid) {
-          tri_index(p, i, j);
-          for (int c = quarter * (DK / 4); c < (quarter + 1) * (DK / 4); ++c) {
-            const float e = __expf(Gs.at(bs + i, c) - Gs.at(bs + j, c));
-            const float kj = to_f32(ks.at(bs + j, c)) * e;
-            sq = fmaf(to_f32(qs.at(bs + i, c)), kj, sq);
-            sk = fmaf(to_f32(ks.at(bs + i, c)), kj, sk);
-          }
-        }
-        sq += __shfl_xor_sync(0xffffffffu, sq, 1);
-        sk += __shfl_xor_sync(0xffffffffu, sk, 1);
-        sq += __shfl_xor_sync(0xffffffffu, sq, 2);
-        sk += __shfl_xor_sync(0xffffffffu, sk, 2);
-        if (valid && quarter == 0) {
-          Tst.at(bs + i, bs + j) = from_f32<T>(a.scale * sq);
-          if (i > j) Akk.at(bs + i, bs + j) = beta_s[bs + i] * sk;
-        }
-      }
+  zero(acc);
+  if (!skip) Gemm<T>::template run<1, 4>(acc, aview<false>(Xs), bview<false>(Ys), m0, n0, 0, DK, lane);
+  __syncthreads();  // every warp is done reading X: it becomes the fp32 Akk
+  FTile<C, C> Akk{reinterpret_cast<float*>(sm + L::X)};
+#pragma unroll
+  for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int r = m0 + frag_row(lane, e), j = n0 + 8 * nt + frag_col(lane, e);
+      Akk.at(r, j) = j < r ? beta_s[r] * acc[0][nt][e] : 0.f;
     }
-  }
   __syncthreads();
+  if (unsafe1 || unsafe2) {
+    prep_pairwise<T, DK, PREP_THREADS>(unsafe1, unsafe2, q, row0, rs, ks, Gs, Tst, Akk, beta_s, a.scale, tid);
+    __syncthreads();
+  }
 
-  // ---- store the scaled Aqk record, then A5: T = (I + Akk)^-1
+  // ---- scaled Aqk record; A5: T = (I + Akk)^-1 (inverse scratch in Y)
   {
     T* dst = static_cast<T*>(a.res.aqk) + ch * (C * C);
     for (int i = tid; i < C * C / EPC; i += PREP_THREADS) copy16(dst + i * EPC, Tst.p + i * EPC);
   }
-  unit_lower_inverse64<PREP_THREADS>(Akk, tmp, tid);  // ends with __syncthreads
+  unit_lower_inverse64<PREP_THREADS>(Akk, FTile<BLK, BLK>{reinterpret_cast<float*>(sm + L::Y)}, tid);
   for (int i = tid; i < C * C; i += PREP_THREADS) {
     const int r = i / C, c = i % C;
     Tst.at(r, c) = from_f32<T>(r == c ? 1.f : (r > c ? Akk.at(r, c) : 0.f));
   }
-  // beta * Gam * k (A operand rows of W's right factor) and beta * v
-  for (int i = tid; i < C * DK / EPC; i += PREP_THREADS) {
-    const int r = i / (DK / EPC), c0 = (i % (DK / EPC)) * EPC;
+  for (int i = tid; i < C * CPR; i += PREP_THREADS) {  // beta Gam k -> Y
+    const int r = i / CPR, c0 = (i % CPR) * EPC;
     __align__(16) T kv[EPC], bk[EPC];
     copy16(kv, ks.ptr(r, c0));
 #pragma unroll
-    for (int e = 0; e < EPC; ++e)
-      bk[e] = from_f32<T>(beta_s[r] * __expf(Gs.at(r, c0 + e)) * to_f32(kv[e]));
-    copy16(Xs.ptr(r, c0), bk);
+    for (int e = 0; e < EPC; ++e) bk[e] = from_f32<T>(beta_s[r] * __expf(Gs.at(r, c0 + e)) * to_f32(kv[e]));
+    copy16(Ys.ptr(r, c0), bk);
   }
-  Tile<T, C, DV> Bv{reinterpret_cast<T*>(sm + L::Y2)};
-  for (int i = tid; i < C * DV / EPC; i += PREP_THREADS) {
-    const int r = i / (DV / EPC), c0 = (i % (DV / EPC)) * EPC;
-    __align__(16) T vv[EPC], bv[EPC];
-    copy16(vv, v + (row0 + r * rs) * DV + c0);
-#pragma unroll
-    for (int e = 0; e < EPC; ++e) bv[e] = from_f32<T>(beta_s[r] * to_f32(vv[e]));
-    copy16(Bv.ptr(r, c0), bv);
+  __syncthreads();  // T in Tst; X (fp32 T) free: v arrives there
+  Tile<T, C, DV> Vs{reinterpret_cast<T*>(sm + L::X)};
+  constexpr int CPRV = DV / EPC;
+  for (int i = tid; i < C * CPRV; i += PREP_THREADS) {
+    const int r = i / CPRV, c = (i % CPRV) * EPC;
+    cp_async16(Vs.ptr(r, c), v + (row0 + r * rs) * DV + c);
   }
-  __syncthreads();
+  cp_async_commit();
   {
     T* dst = static_cast<T*>(a.res.tmat) + ch * (C * C);
     for (int i = tid; i < C * C / EPC; i += PREP_THREADS) copy16(dst + i * EPC, Tst.p + i * EPC);
   }
-
-  // ---- W (stored negated) and U': warp w rows 16 (w & 3), half the columns
+  // -W = -T (beta Gam k), staged in K (k is no longer needed)
   {
-    constexpr int NW = DK / 16;  // n8 tiles per warp
-    float acc[1][NW][4];
-    zero(acc);
-    Gemm<T>::template run<1, NW>(acc, aview<false>(Tst), bview<true>(Xs), m0, half * (DK / 2), 0, C, lane);
-    Tile<T, C, DK> wst{reinterpret_cast<T*>(sm + L::Q)};
+    constexpr int NW = DK / 16;
+    float accw[1][NW][4];
+    zero(accw);
+    Gemm<T>::template run<1, NW>(accw, aview<false>(Tst), bview<true>(Ys), m0, hf * (DK / 2), 0, C, lane);
+    cp_async_wait<0>();
+    __syncthreads();  // all warps done with k (B operand rows were Y) and v has landed
+    Tile<T, C, DK> wst{reinterpret_cast<T*>(sm + L::K)};
 #pragma unroll
     for (int nt = 0; nt < NW; ++nt)
 #pragma unroll
       for (int e = 0; e < 4; ++e)
-        wst.at(m0 + frag_row(lane, e), half * (DK / 2) + 8 * nt + frag_col(lane, e)) = from_f32<T>(-acc[0][nt][e]);
+        wst.at(m0 + frag_row(lane, e), hf * (DK / 2) + 8 * nt + frag_col(lane, e)) = from_f32<T>(-accw[0][nt][e]);
   }
+  for (int i = tid; i < C * CPRV; i += PREP_THREADS) {  // beta v in place
+    const int r = i / CPRV, c0 = (i % CPRV) * EPC;
+    __align__(16) T vv[EPC];
+    copy16(vv, Vs.ptr(r, c0));
+#pragma unroll
+    for (int e = 0; e < EPC; ++e) vv[e] = from_f32<T>(beta_s[r] * to_f32(vv[e]));
+    copy16(Vs.ptr(r, c0), vv);
+  }
+  __syncthreads();  // beta v complete; Y (beta Gam k) consumed: U' is staged there
   {
     constexpr int NU = DV / 16;
-    float acc[1][NU][4];
-    zero(acc);
-    Gemm<T>::template run<1, NU>(acc, aview<false>(Tst), bview<true>(Bv), m0, half * (DV / 2), 0, C, lane);
-    T* ust = reinterpret_cast<T*>(sm + L::K);
+    float accu[1][NU][4];
+    zero(accu);
+    Gemm<T>::template run<1, NU>(accu, aview<false>(Tst), bview<true>(Vs), m0, hf * (DV / 2), 0, C, lane);
+    T* ust = reinterpret_cast<T*>(sm + L::Y);
 #pragma unroll
     for (int nt = 0; nt < NU; ++nt)
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
-        const int r = m0 + frag_row(lane, e), c = half * (DV / 2) + 8 * nt + frag_col(lane, e);
-        ust[(c / NT) * (C * NT) + Sw<T, C, NT>::off(r, c % NT)] = from_f32<T>(acc[0][nt][e]);
+        const int r = m0 + frag_row(lane, e), c = hf * (DV / 2) + 8 * nt + frag_col(lane, e);
+        ust[(c / NT) * (C * NT) + Sw<T, C, NT>::off(r, c % NT)] = from_f32<T>(accu[0][nt][e]);
       }
   }
   __syncthreads();
   {
     T* dw = static_cast<T*>(a.res.wneg) + ch * (C * DK);
-    const T* sw = reinterpret_cast<const T*>(sm + L::Q);
+    const T* sw = reinterpret_cast<const T*>(sm + L::K);
     for (int i = tid; i < C * DK / EPC; i += PREP_THREADS) copy16(dw + i * EPC, sw + i * EPC);
     T* du = static_cast<T*>(a.res.up) + ch * (C * DV);
-    const T* su = reinterpret_cast<const T*>(sm + L::K);
+    const T* su = reinterpret_cast<const T*>(sm + L::Y);
     for (int i = tid; i < C * DV / EPC; i += PREP_THREADS) copy16(du + i * EPC, su + i * EPC);
   }
 }

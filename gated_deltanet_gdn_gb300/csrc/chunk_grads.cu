@@ -1,11 +1,21 @@
 // Chunk-parallel gradients of the chunked gated delta rule backward (bf16 operands).
 //
-// One CTA per (chunk, batch, head). Inputs: q, k, v, g, beta of the chunk, the WY
-// inverse T saved by the forward, and the reverse scan's dU plus the state products
-// dW, dQ-hat, dK-tilde, dAqk, dgam (chunk_bwd.cu). The algebra is listed at the top of
-// chunk_bwd.cu. Score gradients reuse the forward's row-scaled tiles (boundary-split
-// factorisation, marin.community note "factoring GDN-2 decay on TPU", section
-// Approach); blocks whose decay spread leaves the safe range take the pairwise sums.
+// One CTA per (64-channel group, chunk, batch*head). Inputs: q, k, g, beta of the
+// chunk and the state products dQ-hat, dBk, dK-tilde, dAqk, dAkk, dgam written by
+// chunk_dstate_kernel (chunk_bwd.cu). Decay-weighted scores
+//   P[t,j] = sum_c x_tc y_jc exp(G_tc - G_jc)
+// have the gradients dx = (dP (*) E) y, dy = (dP^T (*) E) x and dG = x dx - y dy.
+// Both products run on tensor cores with the rows scaled about one reference point,
+// the last token b of the first block (the boundary-split factorisation of the
+// marin.community note "factoring GDN-2 decay on TPU", section Approach): key rows
+// by exp(G_b - G_j), query rows by exp(G_t - G_b). A block whose decay spread would
+// push those factors out of range takes its in-block part from the pairwise sums.
+//   Aqk family: x = q, dP = dAqk (diagonal handled apart: its dG terms cancel)
+//   Akk family: x = k, dP = diag(beta) dAkk; sum_c k dx' gives the score part of dbeta
+// dG further collects dQ-hat * Q-hat + beta dBk * K-hat - dK-tilde * K-tilde, and at
+// the last row the K-tilde column sums and dgam * gam; dg is its reverse cumulative
+// sum. dbeta and scalar-decay dg need sums over all channels: each CTA writes its
+// channel group's partials and chunk_bwd_finalize_kernel adds them in a fixed order.
 #include "common.cuh"
 #include "kernels.h"
 
@@ -13,456 +23,390 @@ namespace gdn {
 namespace {
 
 constexpr int GR_THREADS = 256;
+constexpr int HC = 64;  // channels per CTA (one 128-byte panel of a bf16 C x Dk record)
 
-// ------------------------------------------------------------------ chunk gradients
-template <int DK, int DV>
 struct GrLayout {
-  static constexpr int MX = DK > DV ? DK : DV;
-  static constexpr int G = 0;                        // float [C][DK]
-  static constexpr int Q = a1k(G + C * DK * 4);      // q
-  static constexpr int K = a1k(Q + C * DK * 2);      // k
-  static constexpr int V = a1k(K + C * DK * 2);      // v
-  static constexpr int TM = a1k(V + C * DV * 2);     // T
-  static constexpr int DW = a1k(TM + C * C * 2);     // dW, later x-side scaled k
-  static constexpr int DU = a1k(DW + C * DK * 2);    // dU (NT slices), later Y1   [C][MX]
-  static constexpr int BUF = a1k(DU + C * MX * 2);   // Bk, Bv, later Y2   [C][MX]
-  static constexpr int DT = a1k(BUF + C * MX * 2);   // dT, X = T^T dT; later Pkk (fp32), Xq
-  static constexpr int XS = DT + C * C * 2;
-  static constexpr int DPKK = a1k(XS + C * C * 2);   // beta * dAkk
-  static constexpr int DAQK = a1k(DPKK + C * C * 2); // dAqk (scaled, masked)
-  static constexpr int BETA = a1k(DAQK + C * C * 2); // float [C]
-  static constexpr int DB = BETA + C * 4;            // float [2][C] dbeta halves
-  static constexpr int DIAG = DB + 2 * C * 4;        // float [C] diagonal of dAqk
-  static constexpr int BYTES = DIAG + C * 4;
-  static_assert(BUF - DW >= C * DK * 4, "dG staging spans the dW and dU regions");
+  static constexpr int GLD = HC + 8;                  // padded fp32 row
+  static constexpr int G = 0;                         // float [C][GLD]
+  static constexpr int Q = a1k(G + C * GLD * 4);      // q     [C][HC]
+  static constexpr int K = a1k(Q + C * HC * 2);       // k     [C][HC]
+  static constexpr int X = a1k(K + C * HC * 2);       // query-side rows; with Y: dG staging
+  static constexpr int Y = X + C * HC * 2;            // key-side rows
+  static constexpr int DQH = a1k(Y + C * HC * 2);     // dQ-hat   [C][HC]
+  static constexpr int DBK = a1k(DQH + C * HC * 2);   // dBk      [C][HC]
+  static constexpr int DKT = a1k(DBK + C * HC * 2);   // dK-tilde [C][HC]
+  static constexpr int DAQ = a1k(DKT + C * HC * 2);   // dAqk [C][C]
+  static constexpr int DAK = a1k(DAQ + C * C * 2);    // dAkk [C][C]
+  static constexpr int BETA = a1k(DAK + C * C * 2);   // float [C]
+  static constexpr int DIAG = BETA + C * 4;           // float [C] diagonal of dAqk
+  static constexpr int DBS = DIAG + C * 4;            // float [2][C] dbeta partials
+  static constexpr int COLS = DBS + 2 * C * 4;        // float [4][HC] K-tilde column partials
+  static constexpr int GCOL = COLS + 4 * HC * 4;      // float [HC] dgam * gam
+  static constexpr int BYTES = GCOL + HC * 4;
+  static_assert(Y - X == C * HC * 2, "dG staging spans X and Y");
 };
 
-template <int DK, int DV, bool PC>
-__global__ void __launch_bounds__(GR_THREADS) chunk_grads_kernel(ChunkBwdArgs a) {
+typedef Tile<bf16, C, HC> HTile;
+
+// sum over j in [j0, j1] of dP(r, j) y(j, c) exp(G(r,c) - G(j,c)) (in-block x side)
+__device__ __noinline__ float pw_dx(const Tile<bf16, C, C>* dP, const HTile* ys, const float* G, int r, int c,
+                                    int j0, int j1) {
+  constexpr int LD = GrLayout::GLD;
+  const float Gr = G[r * LD + c];
+  float s = 0.f;
+  for (int j = j0; j <= j1; ++j)
+    s = fmaf(to_f32(dP->at(r, j)) * to_f32(ys->at(j, c)), __expf(Gr - G[j * LD + c]), s);
+  return s;
+}
+// sum over t in [t0, t1] of dP(t, j) w_t x(t, c) exp(G(t,c) - G(j,c)) (in-block y side)
+__device__ __noinline__ float pw_dy(const Tile<bf16, C, C>* dP, const HTile* xs, const float* w, const float* G,
+                                    int j, int c, int t0, int t1) {
+  constexpr int LD = GrLayout::GLD;
+  const float Gj = G[j * LD + c];
+  float s = 0.f;
+  for (int t = t0; t <= t1; ++t) {
+    const float wt = w ? w[t] : 1.f;
+    s = fmaf(to_f32(dP->at(t, j)) * wt * to_f32(xs->at(t, c)), __expf(G[t * LD + c] - Gj), s);
+  }
+  return s;
+}
+
+template <bool PC>
+__global__ void __launch_bounds__(GR_THREADS, 2) chunk_grads_kernel(ChunkBwdArgs a) {
   typedef bf16 T;
-  typedef GrLayout<DK, DV> L;
+  typedef GrLayout L;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = align1024(smem_raw);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int n = blockIdx.x, bh = blockIdx.y, b = bh / a.H, h = bh % a.H;
-  const int N = a.T / C;
+  const int grp = blockIdx.x, n = blockIdx.y, bh = blockIdx.z, b = bh / a.H, h = bh % a.H;
+  const int N = a.T / C, DK = a.DK, NGRP = DK / HC;
   const size_t ch = (size_t)bh * N + n;
   const size_t row0 = ((size_t)b * a.T + (size_t)n * C) * a.H + h;
   const size_t rs = a.H;
+  const int cbase = grp * HC;  // first channel of this CTA
   constexpr int EPC = 8;
-  FTile<C, DK> Gs{reinterpret_cast<float*>(sm + L::G)};
-  Tile<T, C, DK> Qs{reinterpret_cast<T*>(sm + L::Q)};
-  Tile<T, C, DK> Ks{reinterpret_cast<T*>(sm + L::K)};
-  Tile<T, C, DV> Vs{reinterpret_cast<T*>(sm + L::V)};
-  Tile<T, C, C> Ts{reinterpret_cast<T*>(sm + L::TM)};
-  Tile<T, C, DK> dWs{reinterpret_cast<T*>(sm + L::DW)};
-  TTile<T, C, DV, NT> dUs{reinterpret_cast<T*>(sm + L::DU)};
-  Tile<T, C, C> dTs{reinterpret_cast<T*>(sm + L::DT)};
-  Tile<T, C, C> Xs{reinterpret_cast<T*>(sm + L::XS)};
-  Tile<T, C, C> dPs{reinterpret_cast<T*>(sm + L::DPKK)};
-  Tile<T, C, C> dAs{reinterpret_cast<T*>(sm + L::DAQK)};
+  float* Gp = reinterpret_cast<float*>(sm + L::G);
+  auto Gat = [&](int r, int c) -> float& { return Gp[r * L::GLD + c]; };
+  HTile Qs{reinterpret_cast<T*>(sm + L::Q)};
+  HTile Ks{reinterpret_cast<T*>(sm + L::K)};
+  HTile Xs{reinterpret_cast<T*>(sm + L::X)};
+  HTile Ys{reinterpret_cast<T*>(sm + L::Y)};
+  HTile dQh{reinterpret_cast<T*>(sm + L::DQH)};
+  HTile dBk{reinterpret_cast<T*>(sm + L::DBK)};
+  HTile dKt{reinterpret_cast<T*>(sm + L::DKT)};
+  Tile<T, C, C> dAq{reinterpret_cast<T*>(sm + L::DAQ)};
+  Tile<T, C, C> dAk{reinterpret_cast<T*>(sm + L::DAK)};
   float* beta_s = reinterpret_cast<float*>(sm + L::BETA);
-  float* db_s = reinterpret_cast<float*>(sm + L::DB);
   float* diag_s = reinterpret_cast<float*>(sm + L::DIAG);
+  float* db_s = reinterpret_cast<float*>(sm + L::DBS);
+  float* cols_s = reinterpret_cast<float*>(sm + L::COLS);
+  float* gcol_s = reinterpret_cast<float*>(sm + L::GCOL);
   const T* q = static_cast<const T*>(a.q);
   const T* k = static_cast<const T*>(a.k);
-  const T* v = static_cast<const T*>(a.v);
   const T* g = static_cast<const T*>(a.g);
   const T* beta = static_cast<const T*>(a.beta);
 
-  // ---- loads
-  for (int i = tid; i < C * DK / EPC; i += GR_THREADS) {
-    const int r = i / (DK / EPC), c = (i % (DK / EPC)) * EPC;
-    const size_t gi = (row0 + r * rs) * DK + c;
+  // ---- asynchronous loads (per-channel g lands raw in X first)
+  T* graw = reinterpret_cast<T*>(sm + L::X);
+  for (int i = tid; i < C * HC / EPC; i += GR_THREADS) {
+    const int r = i / (HC / EPC), c = (i % (HC / EPC)) * EPC;
+    const size_t gi = (row0 + r * rs) * DK + cbase + c;
     cp_async16(Qs.ptr(r, c), q + gi);
     cp_async16(Ks.ptr(r, c), k + gi);
-  }
-  for (int i = tid; i < C * DV / EPC; i += GR_THREADS) {
-    const int r = i / (DV / EPC), c = (i % (DV / EPC)) * EPC;
-    cp_async16(Vs.ptr(r, c), v + (row0 + r * rs) * DV + c);
+    if (PC) cp_async16(graw + r * HC + c, g + gi);
   }
   {
-    const T* st = static_cast<const T*>(a.res.tmat) + ch * (C * C);
-    const T* sa = static_cast<const T*>(a.ws.daqk) + ch * (C * C);
-    for (int i = tid; i < C * C / EPC; i += GR_THREADS) {
-      cp_async16(Ts.p + i * EPC, st + i * EPC);
-      cp_async16(dAs.p + i * EPC, sa + i * EPC);
+    // the C x Dk records are 64-column panels: this CTA's panel is contiguous
+    const size_t pan = ch * (C * (size_t)DK) + (size_t)grp * C * HC;
+    const T* s1 = static_cast<const T*>(a.ws.dqh) + pan;
+    const T* s2 = static_cast<const T*>(a.ws.dbk) + pan;
+    const T* s3 = static_cast<const T*>(a.ws.dkt) + pan;
+    for (int i = tid; i < C * HC / EPC; i += GR_THREADS) {
+      cp_async16(dQh.p + i * EPC, s1 + i * EPC);
+      cp_async16(dBk.p + i * EPC, s2 + i * EPC);
+      cp_async16(dKt.p + i * EPC, s3 + i * EPC);
     }
-    const T* sw = static_cast<const T*>(a.ws.dw) + ch * (C * DK);
-    for (int i = tid; i < C * DK / EPC; i += GR_THREADS) cp_async16(dWs.p + i * EPC, sw + i * EPC);
-    const T* su = static_cast<const T*>(a.ws.du) + ch * (C * DV);
-    for (int i = tid; i < C * DV / EPC; i += GR_THREADS) cp_async16(dUs.p + i * EPC, su + i * EPC);
+    const T* sa = static_cast<const T*>(a.ws.daqk) + ch * (C * C);
+    const T* sk = static_cast<const T*>(a.ws.dakk) + ch * (C * C);
+    for (int i = tid; i < C * C / EPC; i += GR_THREADS) {
+      cp_async16(dAq.p + i * EPC, sa + i * EPC);
+      cp_async16(dAk.p + i * EPC, sk + i * EPC);
+    }
   }
   cp_async_commit();
-  if (PC) {
-    for (int i = tid; i < C * DK / EPC; i += GR_THREADS) {
-      const int r = i / (DK / EPC), c = (i % (DK / EPC)) * EPC;
-      __align__(16) T gv[EPC];
-      copy16(gv, g + (row0 + r * rs) * DK + c);
-#pragma unroll
-      for (int e = 0; e < EPC; ++e) Gs.at(r, c + e) = to_f32(gv[e]);
-    }
-  } else {
-    for (int i = tid; i < C * DK; i += GR_THREADS) Gs.at(i / DK, i % DK) = to_f32(g[row0 + (i / DK) * rs]);
-  }
   if (tid < C) beta_s[tid] = to_f32(beta[row0 + tid * rs]);
+  if (!PC)
+    for (int i = tid; i < C * HC; i += GR_THREADS) Gat(i / HC, i % HC) = to_f32(g[row0 + (i / HC) * rs]);
   cp_async_wait<0>();
   __syncthreads();
-  // The diagonal of dAqk (decay factor 1) only feeds dq and dk: its two dG terms
-  // q_t dP_tt k_t and k_t dP_tt q_t cancel exactly, so it is taken out of the
-  // row-scaled products (where bf16 rounding would leave a residual) and added back below.
-  if (tid < C) {
-    diag_s[tid] = to_f32(dAs.at(tid, tid));
-    dAs.at(tid, tid) = from_f32<T>(0.f);
+  if (PC)
+    for (int i = tid; i < C * HC; i += GR_THREADS) Gat(i / HC, i % HC) = to_f32(graw[i]);
+  if (tid < C) {  // the diagonal of dAqk only feeds dq and dk (its dG terms cancel exactly)
+    diag_s[tid] = to_f32(dAq.at(tid, tid));
+    dAq.at(tid, tid) = from_f32<T>(0.f);
   }
-  for (int c = tid; c < DK; c += GR_THREADS) {
+  __syncthreads();
+  for (int u = tid; u < 2 * HC; u += GR_THREADS) {  // cumulative log-decay, two threads per channel
+    const int c = u % HC, r0 = (u / HC) * BLK;
     float s = 0.f;
-    for (int r = 0; r < C; ++r) {
-      s += Gs.at(r, c);
-      Gs.at(r, c) = s;
+#pragma unroll 8
+    for (int r = r0; r < r0 + BLK; ++r) {
+      s += Gat(r, c);
+      Gat(r, c) = s;
     }
+  }
+  __syncthreads();
+  for (int c = tid; c < HC; c += GR_THREADS) {
+    const float base = Gat(BLK - 1, c);
+#pragma unroll 8
+    for (int r = BLK; r < C; ++r) Gat(r, c) += base;
   }
   __syncthreads();
   const bool force = (a.flags & 1) != 0;
   bool u1 = false, u2 = false;
-  for (int c = tid; c < DK; c += GR_THREADS) {
-    u1 |= !(-Gs.at(BLK - 1, c) <= SAFE_SPREAD);
-    u2 |= !(Gs.at(BLK - 1, c) - Gs.at(C - 1, c) <= SAFE_SPREAD);
+  for (int c = tid; c < HC; c += GR_THREADS) {
+    u1 |= !(Gat(0, c) - Gat(BLK - 1, c) <= SAFE_SPREAD);
+    u2 |= !(Gat(BLK - 1, c) - Gat(C - 1, c) <= SAFE_SPREAD);
+    gcol_s[c] = a.ws.dgam[ch * DK + cbase + c] * __expf(Gat(C - 1, c));
   }
   const bool unsafe1 = __syncthreads_or(u1 || force) != 0;
   const bool unsafe2 = __syncthreads_or(u2 || force) != 0;
 
-  // warp partition: rows m0 .. m0 + 15, column half hf
-  const int m0 = 16 * (warp & 3), hf = warp >> 2;
-  constexpr int NWK = DK / 16, NWV = DV / 16;  // n8 tiles per warp for C x DK / C x DV outputs
-  const int ck0 = hf * (DK / 2), cv0 = hf * (DV / 2), cc0 = hf * 32;
-  float db[2] = {0.f, 0.f};  // dbeta partials for rows m0 + g and m0 + g + 8
-
-  // ---- Bk = beta Gam k
-  Tile<T, C, DK> Bk{reinterpret_cast<T*>(sm + L::BUF)};
-  Tile<T, C, DV> Bv{reinterpret_cast<T*>(sm + L::BUF)};
-  for (int i = tid; i < C * DK; i += GR_THREADS) {
-    const int r = i / DK, c = i % DK;
-    Bk.at(r, c) = from_f32<T>(beta_s[r] * __expf(Gs.at(r, c)) * to_f32(Ks.at(r, c)));
-  }
-  __syncthreads();
-  float dT[1][4][4];
-  zero(dT);
-  Gemm<T>::template run<1, 4>(dT, aview<false>(dWs), bview<false>(Bk), m0, cc0, 0, DK, lane);
-  __syncthreads();
-  for (int i = tid; i < C * DV; i += GR_THREADS) {
-    const int r = i / DV, c = i % DV;
-    Bv.at(r, c) = from_f32<T>(beta_s[r] * to_f32(Vs.at(r, c)));
-  }
-  __syncthreads();
-  Gemm<T>::template run<1, 4>(dT, aview<false>(dUs), bview<false>(Bv), m0, cc0, 0, DV, lane);
+  // row-scaled operands: X (query side, x = beta k first) and Y (key side)
+  for (int i = tid; i < C * HC / EPC; i += GR_THREADS) {
+    const int r = i / (HC / EPC), c0 = (i % (HC / EPC)) * EPC;
+    __align__(16) T kv[EPC], xb[EPC], yk[EPC];
+    copy16(kv, Ks.ptr(r, c0));
+    const bool dead_x = r < BLK && unsafe1, dead_y = r >= BLK && unsafe2;
 #pragma unroll
-  for (int nt = 0; nt < 4; ++nt)
-#pragma unroll
-    for (int e = 0; e < 4; ++e)
-      dTs.at(m0 + frag_row(lane, e), cc0 + 8 * nt + frag_col(lane, e)) = from_f32<T>(dT[0][nt][e]);
-
-  // ---- dv = beta (T^T dU)
-  {
-    float acc[1][NWV][4];
-    zero(acc);
-    Gemm<T>::template run<1, NWV>(acc, aview<true>(Ts), bview<true>(dUs), m0, cv0, 0, C, lane);
-    T* dv = static_cast<T*>(a.dv);
-#pragma unroll
-    for (int nt = 0; nt < NWV; ++nt)
-#pragma unroll
-      for (int e = 0; e < 4; e += 2) {
-        const int r = m0 + frag_row(lane, e), c = cv0 + 8 * nt + frag_col(lane, e);
-        db[e >> 1] += acc[0][nt][e] * to_f32(Vs.at(r, c)) + acc[0][nt][e + 1] * to_f32(Vs.at(r, c + 1));
-        store2(dv + (row0 + r * rs) * DV + c, beta_s[r] * acc[0][nt][e], beta_s[r] * acc[0][nt][e + 1]);
-      }
-  }
-  // ---- dBk = T^T dW: dK-hat = beta dBk; dk += dK-hat Gam; dG += dK-hat K-hat
-  float dq_acc[NWK][4], dk_acc[NWK][4], dG_acc[NWK][4];
-  {
-    float acc[1][NWK][4];
-    zero(acc);
-    Gemm<T>::template run<1, NWK>(acc, aview<true>(Ts), bview<true>(dWs), m0, ck0, 0, C, lane);
-#pragma unroll
-    for (int nt = 0; nt < NWK; ++nt)
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int r = m0 + frag_row(lane, e), c = ck0 + 8 * nt + frag_col(lane, e);
-        const float gm = __expf(Gs.at(r, c));
-        const float khat = gm * to_f32(Ks.at(r, c));
-        db[e >> 1] += acc[0][nt][e] * khat;
-        const float dkh = beta_s[r] * acc[0][nt][e];
-        dq_acc[nt][e] = 0.f;
-        dk_acc[nt][e] = dkh * gm;
-        dG_acc[nt][e] = dkh * khat;
-      }
-  }
-  __syncthreads();  // dT complete; dW and dU no longer needed after this point except dUs reads done
-  // ---- X = T^T dT ; dAkk = -(X T^T) masked strict
-  {
-    float acc[1][4][4];
-    zero(acc);
-    Gemm<T>::template run<1, 4>(acc, aview<true>(Ts), bview<true>(dTs), m0, cc0, 0, C, lane);
-#pragma unroll
-    for (int nt = 0; nt < 4; ++nt)
-#pragma unroll
-      for (int e = 0; e < 4; ++e)
-        Xs.at(m0 + frag_row(lane, e), cc0 + 8 * nt + frag_col(lane, e)) = from_f32<T>(acc[0][nt][e]);
-  }
-  // x-side scaled keys (into dW), Y1 (into dU), Y2 (into BUF)
-  Tile<T, C, DK> Xk{reinterpret_cast<T*>(sm + L::DW)};
-  Tile<T, BLK, DK> Y1{reinterpret_cast<T*>(sm + L::DU)};
-  Tile<T, C, DK> Y2{reinterpret_cast<T*>(sm + L::BUF)};
-  __syncthreads();
-  float dAkk[1][4][4];
-  zero(dAkk);
-  Gemm<T>::template run<1, 4>(dAkk, aview<false>(Xs), bview<false>(Ts), m0, cc0, 0, C, lane);
-  for (int i = tid; i < C * DK; i += GR_THREADS) {
-    const int r = i / DK, c = i % DK;
-    const float G = Gs.at(r, c), Gb = Gs.at(BLK - 1, c), kf = to_f32(Ks.at(r, c));
-    Xk.at(r, c) = from_f32<T>(kf * __expf(r < BLK ? G : G - Gb));
-    Y2.at(r, c) = from_f32<T>((r < BLK || !unsafe2) ? kf * __expf(Gb - G) : 0.f);
-    if (r < BLK) Y1.at(r, c) = from_f32<T>(unsafe1 ? 0.f : kf * __expf(-G));
-  }
-  __syncthreads();  // X consumed; DT/XS region becomes Pkk
-  FTile<C, C> Pk{reinterpret_cast<float*>(sm + L::DT)};
-  {
-    float acc[1][4][4];
-    zero(acc);
-    const bool blk1 = m0 < BLK;
-    if (!(blk1 && (unsafe1 || hf == 1))) {
-      if (blk1) Gemm<T>::template run<1, 4>(acc, aview<false>(Xk), bview<false>(Y1), m0, 0, 0, DK, lane);
-      else Gemm<T>::template run<1, 4>(acc, aview<false>(Xk), bview<false>(Y2), m0, cc0, 0, DK, lane);
+    for (int e = 0; e < EPC; ++e) {
+      const float G = Gat(r, c0 + e), Gb = Gat(BLK - 1, c0 + e), kf = to_f32(kv[e]);
+      xb[e] = from_f32<T>(dead_x ? 0.f : beta_s[r] * kf * __expf(G - Gb));
+      yk[e] = from_f32<T>(dead_y ? 0.f : kf * __expf(Gb - G));
     }
-#pragma unroll
-    for (int nt = 0; nt < 4; ++nt)
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int r = m0 + frag_row(lane, e), j = cc0 + 8 * nt + frag_col(lane, e);
-        Pk.at(r, j) = j < r ? acc[0][nt][e] : 0.f;
-      }
-  }
-  __syncthreads();
-  if (unsafe1 || unsafe2) {  // pairwise in-block scores, four lanes per pair
-    for (int blk = 0; blk < 2; ++blk) {
-      if (!(blk == 0 ? unsafe1 : unsafe2)) continue;
-      const int bs = blk * BLK;
-      constexpr int NPAIR = BLK * (BLK - 1) / 2;  // strict triangle
-      for (int base = 0; base < NPAIR; base += 8 * (GR_THREADS / 32)) {
-        const int p = base + warp * 8 + (lane >> 2), quarter = lane & 3;
-        const bool valid = p < NPAIR;
-        int i = 1, j = 0;
-        float sk = 0.f;
-        if (valid) {
-          int r = (int)((sqrtf(8.f * p + 1.f) + 1.f) * 0.5f);  // strict: p = i(i-1)/2 + j
-          while (r * (r - 1) / 2 > p) --r;
-          while ((r + 1) * r / 2 <= p) ++r;
-          i = r;
-          j = p - r * (r - 1) / 2;
-          for (int c = quarter * (DK / 4); c < (quarter + 1) * (DK / 4); ++c)
-            sk = fmaf(to_f32(Ks.at(bs + i, c)), to_f32(Ks.at(bs + j, c)) * __expf(Gs.at(bs + i, c) - Gs.at(bs + j, c)), sk);
-        }
-        sk += __shfl_xor_sync(0xffffffffu, sk, 1);
-        sk += __shfl_xor_sync(0xffffffffu, sk, 2);
-        if (valid && quarter == 0) Pk.at(bs + i, bs + j) = sk;
-      }
-    }
-    __syncthreads();
-  }
-  // dbeta += rowsum(dAkk * Pkk); dPkk = beta dAkk
-#pragma unroll
-  for (int nt = 0; nt < 4; ++nt)
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const int r = m0 + frag_row(lane, e), j = cc0 + 8 * nt + frag_col(lane, e);
-      const float d = j < r ? -dAkk[0][nt][e] : 0.f;
-      db[e >> 1] += d * Pk.at(r, j);
-      dPs.at(r, j) = from_f32<T>(beta_s[r] * d);
-    }
-  __syncthreads();  // Pkk consumed: DT/XS region becomes the query-side scaled q
-  Tile<T, C, DK> Xq{reinterpret_cast<T*>(sm + L::DT)};
-  for (int i = tid; i < C * DK; i += GR_THREADS) {
-    const int r = i / DK, c = i % DK;
-    const float G = Gs.at(r, c);
-    Xq.at(r, c) = from_f32<T>(to_f32(Qs.at(r, c)) * __expf(r < BLK ? G : G - Gs.at(BLK - 1, c)));
+    copy16(Xs.ptr(r, c0), xb);
+    copy16(Ys.ptr(r, c0), yk);
   }
   __syncthreads();
 
-  // ---- score backward. x side: dx_t = f_t * sum_j dP[t,j] Y_j ; y side: dy_j = sum over
-  // query blocks of f'_j * sum_t dP[t,j] X_t (row-scaled tiles as in the forward).
-  auto score_bwd = [&](const Tile<T, C, C>& dP, const Tile<T, C, DK>& Xx, bool x_is_q, bool strict) {
-    float acc[1][NWK][4];
-    // dx
-    zero(acc);
-    const bool blk1 = m0 < BLK;
-    if (blk1) {
-      if (!unsafe1) Gemm<T>::template run<1, NWK>(acc, aview<false>(dP), bview<true>(Y1), m0, ck0, 0, BLK, lane);
-    } else {
-      Gemm<T>::template run<1, NWK>(acc, aview<false>(dP), bview<true>(Y2), m0, ck0, 0, C, lane);
-    }
-#pragma unroll
-    for (int nt = 0; nt < NWK; ++nt)
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int r = m0 + frag_row(lane, e), c = ck0 + 8 * nt + frag_col(lane, e);
-        const float G = Gs.at(r, c);
-        float dx = acc[0][nt][e] * __expf(blk1 ? G : G - Gs.at(BLK - 1, c));
-        if (blk1 ? unsafe1 : unsafe2) {  // in-block part, pairwise
-          const int bs = blk1 ? 0 : BLK, jmax = strict ? r - 1 : r;
-#pragma unroll 1
-          for (int j = bs; j <= jmax; ++j)
-            dx = fmaf(to_f32(dP.at(r, j)) * to_f32(Ks.at(j, c)), __expf(G - Gs.at(j, c)), dx);
-        }
-        const float xv = to_f32(x_is_q ? Qs.at(r, c) : Ks.at(r, c));
-        if (x_is_q) dq_acc[nt][e] += dx; else dk_acc[nt][e] += dx;
-        dG_acc[nt][e] += xv * dx;
-      }
-    // dy: part from second-block queries (t in 32..63), then first-block queries (t < 32)
-    zero(acc);
-    if (!(m0 >= BLK && unsafe2))
-      Gemm<T>::template run<1, NWK>(acc, aview<true>(dP), bview<true>(Xx), m0, ck0, BLK, C, lane);
-    float acc1[1][NWK][4];
-    zero(acc1);
-    if (m0 < BLK && !unsafe1)
-      Gemm<T>::template run<1, NWK>(acc1, aview<true>(dP), bview<true>(Xx), m0, ck0, 0, BLK, lane);
-#pragma unroll
-    for (int nt = 0; nt < NWK; ++nt)
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int j = m0 + frag_row(lane, e), c = ck0 + 8 * nt + frag_col(lane, e);
-        const float G = Gs.at(j, c), Gb = Gs.at(BLK - 1, c);
-        float dy = 0.f;
-        if (!(j >= BLK && unsafe2)) dy = acc[0][nt][e] * __expf(Gb - G);
-        if (j < BLK && !unsafe1) dy = fmaf(acc1[0][nt][e], __expf(-G), dy);
-        const bool up = j < BLK ? unsafe1 : unsafe2;
-        if (up) {
-          const int be = j < BLK ? BLK : C, tmin = strict ? j + 1 : j;
-#pragma unroll 1
-          for (int t = tmin; t < be; ++t) {
-            const float xv = to_f32(x_is_q ? Qs.at(t, c) : Ks.at(t, c));
-            dy = fmaf(to_f32(dP.at(t, j)) * xv, __expf(Gs.at(t, c) - G), dy);
-          }
-        }
-        dk_acc[nt][e] += dy;
-        dG_acc[nt][e] -= to_f32(Ks.at(j, c)) * dy;
-      }
+  // warp w: rows m0 .. m0 + 15, channels c0 .. c0 + 31 of this group
+  const int m0 = 16 * (warp & 3), cq = warp >> 2, c0 = 32 * cq;
+  const bool blk1 = m0 < BLK;
+  const bool pw_rows = blk1 ? unsafe1 : unsafe2;  // in-block part of these rows is pairwise
+  float dk_acc[4][4], dG_acc[4][4], dbp[2] = {0.f, 0.f};
+
+  // x-side GEMM over key columns [0, C) ([0, BLK) for block-1 rows), y-side over query rows
+  auto products = [&](const Tile<T, C, C>& dP, float (&ax)[1][4][4], float (&ay)[1][4][4]) {
+    zero(ax);
+    zero(ay);
+    if (!(blk1 && unsafe1))
+      Gemm<T>::template run<1, 4>(ax, aview<false>(dP), bview<true>(Ys), m0, c0, 0, blk1 ? BLK : C, lane);
+    if (!(!blk1 && unsafe2))
+      Gemm<T>::template run<1, 4>(ay, aview<true>(dP), bview<true>(Xs), m0, c0, blk1 ? 0 : BLK, C, lane);
   };
-  score_bwd(dAs, Xq, true, false);
-  score_bwd(dPs, Xk, false, true);
-#pragma unroll
-  for (int nt = 0; nt < NWK; ++nt)
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const int r = m0 + frag_row(lane, e), c = ck0 + 8 * nt + frag_col(lane, e);
-      dq_acc[nt][e] = fmaf(diag_s[r], to_f32(Ks.at(r, c)), dq_acc[nt][e]);
-      dk_acc[nt][e] = fmaf(diag_s[r], to_f32(Qs.at(r, c)), dk_acc[nt][e]);
-    }
 
-  // ---- elementwise terms of Q-hat and K-tilde
-  {
-    const T* dqh = static_cast<const T*>(a.ws.dqh) + ch * (C * DK);
-    const T* dkt = static_cast<const T*>(a.ws.dkt) + ch * (C * DK);
+  {  // ---- Akk family (x = k, weights beta on the query side)
+    float ax[1][4][4], ay[1][4][4];
+    products(dAk, ax, ay);
 #pragma unroll
-    for (int nt = 0; nt < NWK; ++nt)
+    for (int nt = 0; nt < 4; ++nt)
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
-        const int r = m0 + frag_row(lane, e), c = ck0 + 8 * nt + frag_col(lane, e);
-        const int off = Sw<T, C, DK>::off(r, c);
-        const float G = Gs.at(r, c), GC = Gs.at(C - 1, c);
-        const float gm = __expf(G), kdec = __expf(GC - G);
-        const float a1 = to_f32(dqh[off]), a2 = to_f32(dkt[off]);
-        const float kf = to_f32(Ks.at(r, c));
-        dq_acc[nt][e] += a1 * gm;
-        dk_acc[nt][e] += a2 * kdec;
-        dG_acc[nt][e] += a1 * gm * to_f32(Qs.at(r, c)) - a2 * kdec * kf;
+        const int r = m0 + frag_row(lane, e), c = c0 + 8 * nt + frag_col(lane, e);
+        const float G = Gat(r, c), Gb = Gat(BLK - 1, c), kf = to_f32(Ks.at(r, c));
+        float dxp = (blk1 && unsafe1) ? 0.f : ax[0][nt][e] * __expf(G - Gb);
+        float dy = (!blk1 && unsafe2) ? 0.f : ay[0][nt][e] * __expf(Gb - G);
+        if (pw_rows) {
+          const int bs = blk1 ? 0 : BLK;
+          dxp += pw_dx(&dAk, &Ks, Gp, r, c, bs, r);
+          dy += pw_dy(&dAk, &Ks, beta_s, Gp, r, c, r, bs + BLK - 1);
+        }
+        const float dx = beta_s[r] * dxp;
+        dbp[e >> 1] += kf * dxp;
+        dk_acc[nt][e] = dx + dy;
+        dG_acc[nt][e] = kf * (dx - dy);
       }
   }
-  // ---- dq, dk out; dbeta reduce
-  {
-    T* dq = static_cast<T*>(a.dq);
-    T* dk = static_cast<T*>(a.dk);
+  __syncthreads();  // X consumed: rebuild it with the queries
+  for (int i = tid; i < C * HC / EPC; i += GR_THREADS) {
+    const int r = i / (HC / EPC), cc = (i % (HC / EPC)) * EPC;
+    __align__(16) T qv[EPC], xq[EPC];
+    copy16(qv, Qs.ptr(r, cc));
+    const bool dead_x = r < BLK && unsafe1;
 #pragma unroll
-    for (int nt = 0; nt < NWK; ++nt)
+    for (int e = 0; e < EPC; ++e)
+      xq[e] = from_f32<T>(dead_x ? 0.f : to_f32(qv[e]) * __expf(Gat(r, cc + e) - Gat(BLK - 1, cc + e)));
+    copy16(Xs.ptr(r, cc), xq);
+  }
+  __syncthreads();
+  {  // ---- Aqk family (x = q); dq is complete after this block
+    float ax[1][4][4], ay[1][4][4];
+    products(dAq, ax, ay);
+    T* dq = static_cast<T*>(a.dq);
+#pragma unroll
+    for (int nt = 0; nt < 4; ++nt)
 #pragma unroll
       for (int e = 0; e < 4; e += 2) {
-        const int r = m0 + frag_row(lane, e), c = ck0 + 8 * nt + frag_col(lane, e);
-        const size_t gi = (row0 + r * rs) * DK + c;
-        store2(dq + gi, dq_acc[nt][e], dq_acc[nt][e + 1]);
-        store2(dk + gi, dk_acc[nt][e], dk_acc[nt][e + 1]);
+        float out[2];
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+          const int r = m0 + frag_row(lane, e + u), c = c0 + 8 * nt + frag_col(lane, e + u);
+          const float G = Gat(r, c), Gb = Gat(BLK - 1, c);
+          const float qf = to_f32(Qs.at(r, c)), kf = to_f32(Ks.at(r, c));
+          float dx = (blk1 && unsafe1) ? 0.f : ax[0][nt][e + u] * __expf(G - Gb);
+          float dy = (!blk1 && unsafe2) ? 0.f : ay[0][nt][e + u] * __expf(Gb - G);
+          if (pw_rows) {
+            const int bs = blk1 ? 0 : BLK;
+            dx += pw_dx(&dAq, &Ks, Gp, r, c, bs, r);
+            dy += pw_dy(&dAq, &Qs, nullptr, Gp, r, c, r, bs + BLK - 1);
+          }
+          const float gm = __expf(G), a1 = to_f32(dQh.at(r, c));
+          out[u] = a1 * gm + dx + diag_s[r] * kf;
+          dk_acc[nt][e + u] += dy + diag_s[r] * qf;
+          dG_acc[nt][e + u] += qf * dx - kf * dy + a1 * gm * qf;
+        }
+        const int r = m0 + frag_row(lane, e), c = c0 + 8 * nt + frag_col(lane, e);
+        store2(dq + (row0 + r * rs) * DK + cbase + c, out[0], out[1]);
+      }
+  }
+  // ---- elementwise terms of K-hat (via dBk) and K-tilde; dk out
+  {
+    T* dk = static_cast<T*>(a.dk);
+    float colp[4][2];
+#pragma unroll
+    for (int nt = 0; nt < 4; ++nt) {
+      colp[nt][0] = colp[nt][1] = 0.f;
+#pragma unroll
+      for (int e = 0; e < 4; e += 2) {
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+          const int r = m0 + frag_row(lane, e + u), c = c0 + 8 * nt + frag_col(lane, e + u);
+          const float G = Gat(r, c), GC = Gat(C - 1, c), kf = to_f32(Ks.at(r, c));
+          const float gm = __expf(G), kdec = __expf(GC - G);
+          const float bk = to_f32(dBk.at(r, c)), kt = to_f32(dKt.at(r, c));
+          const float khat = gm * kf, ktil = kdec * kf, dkh = beta_s[r] * bk;
+          dbp[e >> 1] += bk * khat;
+          dk_acc[nt][e + u] += dkh * gm + kt * kdec;
+          dG_acc[nt][e + u] += dkh * khat - kt * ktil;
+          colp[nt][u] += kt * ktil;
+        }
+        const int r = m0 + frag_row(lane, e), c = c0 + 8 * nt + frag_col(lane, e);
+        store2(dk + (row0 + r * rs) * DK + cbase + c, dk_acc[nt][e], dk_acc[nt][e + 1]);
+      }
+    }
+    // column sums over this warp's 16 rows (lanes sharing a column differ in bits 2..4)
+#pragma unroll
+    for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        float x = colp[nt][u];
+        x += __shfl_xor_sync(0xffffffffu, x, 4);
+        x += __shfl_xor_sync(0xffffffffu, x, 8);
+        x += __shfl_xor_sync(0xffffffffu, x, 16);
+        if (lane < 4) cols_s[(warp & 3) * HC + c0 + 8 * nt + 2 * lane + u] = x;
       }
 #pragma unroll
     for (int i = 0; i < 2; ++i) {
-      db[i] += __shfl_xor_sync(0xffffffffu, db[i], 1);
-      db[i] += __shfl_xor_sync(0xffffffffu, db[i], 2);
+      dbp[i] += __shfl_xor_sync(0xffffffffu, dbp[i], 1);
+      dbp[i] += __shfl_xor_sync(0xffffffffu, dbp[i], 2);
     }
     if ((lane & 3) == 0) {
-      db_s[hf * C + m0 + (lane >> 2)] = db[0];
-      db_s[hf * C + m0 + (lane >> 2) + 8] = db[1];
+      db_s[cq * C + m0 + (lane >> 2)] = dbp[0];
+      db_s[cq * C + m0 + (lane >> 2) + 8] = dbp[1];
     }
   }
-  __syncthreads();  // all score tiles consumed: dW/dU region becomes the dG staging
-  FTile<C, DK> dGs{reinterpret_cast<float*>(sm + L::DW)};
+  __syncthreads();  // X and Y free: dG staging (fp32 [C][HC])
+  float* dGs = reinterpret_cast<float*>(sm + L::X);
 #pragma unroll
-  for (int nt = 0; nt < NWK; ++nt)
+  for (int nt = 0; nt < 4; ++nt)
 #pragma unroll
     for (int e = 0; e < 4; ++e)
-      dGs.at(m0 + frag_row(lane, e), ck0 + 8 * nt + frag_col(lane, e)) = dG_acc[nt][e];
-  if (tid < C) {
-    T* dbeta = static_cast<T*>(a.dbeta);
-    dbeta[row0 + tid * rs] = from_f32<T>(db_s[tid] + db_s[C + tid]);
+      dGs[(m0 + frag_row(lane, e)) * HC + c0 + 8 * nt + frag_col(lane, e)] = dG_acc[nt][e];
+  if (tid < C) a.ws.dbpart[(ch * 2 + grp) * C + tid] = db_s[tid] + db_s[C + tid];
+  __syncthreads();
+  // reverse cumulative sum per channel; the last row also gets the K-tilde column sum and
+  // dgam * gam (both are derivatives with respect to G at the chunk's last token)
+  for (int u = tid; u < 2 * HC; u += GR_THREADS) {
+    const int c = u % HC, hi = u / HC;
+    float s = hi ? (cols_s[c] + cols_s[HC + c] + cols_s[2 * HC + c] + cols_s[3 * HC + c] + gcol_s[c]) : 0.f;
+    const int r1 = hi ? C - 1 : BLK - 1;
+#pragma unroll 8
+    for (int r = r1; r > r1 - BLK; --r) {
+      s += dGs[r * HC + c];
+      dGs[r * HC + c] = s;
+    }
   }
   __syncthreads();
-  // reverse cumulative sum per channel; the last row also collects the K-tilde column
-  // sums and dgam * gam (both depend on G at the chunk's last token)
-  for (int c = tid; c < DK; c += GR_THREADS) {
-    const T* dkt = static_cast<const T*>(a.ws.dkt) + ch * (C * DK);
-    const float GC = Gs.at(C - 1, c);
-    float extra = static_cast<const float*>(a.ws.dgam)[ch * DK + c] * __expf(GC);
-    for (int t = 0; t < C; ++t)
-      extra = fmaf(to_f32(dkt[Sw<T, C, DK>::off(t, c)]), __expf(GC - Gs.at(t, c)) * to_f32(Ks.at(t, c)), extra);
-    float s = extra;
-    for (int t = C - 1; t >= 0; --t) {
-      s += dGs.at(t, c);
-      dGs.at(t, c) = s;
-    }
+  for (int c = tid; c < HC; c += GR_THREADS) {
+    const float top = dGs[BLK * HC + c];  // rows >= BLK summed (with the extras)
+#pragma unroll 8
+    for (int r = 0; r < BLK; ++r) dGs[r * HC + c] += top;
   }
   __syncthreads();
   T* dg = static_cast<T*>(a.dg);
   if (PC) {
-    for (int i = tid; i < C * DK / 2; i += GR_THREADS) {
-      const int r = i / (DK / 2), c = (i % (DK / 2)) * 2;
-      store2(dg + (row0 + r * rs) * DK + c, dGs.at(r, c), dGs.at(r, c + 1));
+    for (int i = tid; i < C * HC / EPC; i += GR_THREADS) {
+      const int r = i / (HC / EPC), cc = (i % (HC / EPC)) * EPC;
+      __align__(16) T o[EPC];
+#pragma unroll
+      for (int e = 0; e < EPC; ++e) o[e] = from_f32<T>(dGs[r * HC + cc + e]);
+      copy16(dg + (row0 + r * rs) * DK + cbase + cc, o);
     }
   } else {
     for (int r = warp; r < C; r += GR_THREADS / 32) {
-      float s = 0.f;
-      for (int c = lane; c < DK; c += 32) s += dGs.at(r, c);
+      float s = dGs[r * HC + lane] + dGs[r * HC + lane + 32];
 #pragma unroll
       for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
-      if (lane == 0) dg[row0 + r * rs] = from_f32<T>(s);
+      if (lane == 0) a.ws.dgpart[(ch * 2 + grp) * C + r] = s;
     }
   }
+  (void)NGRP;
 }
 
-
-template <int DK, int DV>
-cudaError_t launch_grads_t(const ChunkBwdArgs& a, cudaStream_t s) {
-  const int N = a.T / C, BH = a.B * a.H;
-  const int bytes = GrLayout<DK, DV>::BYTES + 1024;
-  auto kern = a.per_channel ? chunk_grads_kernel<DK, DV, true> : chunk_grads_kernel<DK, DV, false>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
-  if (e != cudaSuccess) return e;
-  prof_mark(K_GRADS, s, true);
-  kern<<<dim3(N, BH), GR_THREADS, bytes, s>>>(a);
-  prof_mark(K_GRADS, s, false);
-  return cudaGetLastError();
+// dbeta = dbeta_v + the channel groups' partials (and scalar-decay dg), fixed order.
+template <bool PC>
+__global__ void chunk_bwd_finalize_kernel(ChunkBwdArgs a) {
+  const size_t total = (size_t)a.B * a.H * a.T;
+  const int N = a.T / C, NGRP = a.DK / HC;
+  for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (size_t)gridDim.x * blockDim.x) {
+    const int t = (int)(i % C);
+    const size_t ch = i / C;  // (bh, n) record
+    const int n = (int)(ch % N);
+    const int bh = (int)(ch / N), b = bh / a.H, h = bh % a.H;
+    const size_t row = ((size_t)b * a.T + (size_t)n * C + t) * a.H + h;
+    float db = a.ws.dbv[ch * C + t] + a.ws.dbpart[(ch * 2) * C + t];
+    if (NGRP > 1) db += a.ws.dbpart[(ch * 2 + 1) * C + t];
+    static_cast<bf16*>(a.dbeta)[row] = from_f32<bf16>(db);
+    if (!PC) {
+      float s = a.ws.dgpart[(ch * 2) * C + t];
+      if (NGRP > 1) s += a.ws.dgpart[(ch * 2 + 1) * C + t];
+      static_cast<bf16*>(a.dg)[row] = from_f32<bf16>(s);
+    }
+  }
 }
 
 }  // namespace
 
 cudaError_t launch_chunk_grads(const ChunkBwdArgs& a, cudaStream_t s) {
   if (a.B * a.H == 0 || a.T == 0) return cudaSuccess;
-  return a.DK == 64 ? launch_grads_t<64, 64>(a, s) : launch_grads_t<128, 128>(a, s);
+  const int N = a.T / C, BH = a.B * a.H;
+  const int bytes = GrLayout::BYTES + 1024;
+  auto kern = a.per_channel ? chunk_grads_kernel<true> : chunk_grads_kernel<false>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e != cudaSuccess) return e;
+  prof_mark(K_GRADS, s, true);
+  kern<<<dim3(a.DK / HC, N, BH), GR_THREADS, bytes, s>>>(a);
+  prof_mark(K_GRADS, s, false);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  const size_t total = (size_t)BH * a.T;
+  const int blocks = (int)((total + 255) / 256 < 4096 ? (total + 255) / 256 : 4096);
+  prof_mark(K_FINALIZE, s, true);
+  if (a.per_channel)
+    chunk_bwd_finalize_kernel<true><<<blocks, 256, 0, s>>>(a);
+  else
+    chunk_bwd_finalize_kernel<false><<<blocks, 256, 0, s>>>(a);
+  prof_mark(K_FINALIZE, s, false);
+  return cudaGetLastError();
 }
 
 }  // namespace gdn

@@ -22,8 +22,8 @@ struct ResidualLayout {
 };
 
 struct BwdWorkspaceLayout {
-  size_t du, dstate, dqh, dw, dkt, daqk, dgam, total;
-  size_t du_b, dstate_b, dqh_b, dw_b, dkt_b, daqk_b, dgam_b;
+  size_t du, dstate, dqh, dbk, dkt, daqk, dakk, dgam, dbv, dbpart, dgpart, total;
+  size_t du_b, dstate_b, dqh_b, dbk_b, dkt_b, daqk_b, dakk_b, dgam_b, dbv_b, dbpart_b, dgpart_b;
 };
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -64,10 +64,14 @@ inline BwdWorkspaceLayout bwd_workspace_layout(int B, int T, int H, int DK, int 
   L.du_b = (size_t)C * DV * es;
   L.dstate_b = (size_t)DK * DV * es;
   L.dqh_b = (size_t)C * DK * es;
-  L.dw_b = (size_t)C * DK * es;
+  L.dbk_b = (size_t)C * DK * es;
   L.dkt_b = (size_t)C * DK * es;
   L.daqk_b = (size_t)C * C * es;
+  L.dakk_b = (size_t)C * C * es;
   L.dgam_b = (size_t)DK * 4;
+  L.dbv_b = (size_t)C * 4;
+  L.dbpart_b = (size_t)2 * C * 4;
+  L.dgpart_b = (size_t)2 * C * 4;
   size_t off = 0;
   auto put = [&](size_t& field, size_t rec) {
     field = off;
@@ -76,10 +80,14 @@ inline BwdWorkspaceLayout bwd_workspace_layout(int B, int T, int H, int DK, int 
   put(L.du, L.du_b);
   put(L.dstate, L.dstate_b);
   put(L.dqh, L.dqh_b);
-  put(L.dw, L.dw_b);
+  put(L.dbk, L.dbk_b);
   put(L.dkt, L.dkt_b);
   put(L.daqk, L.daqk_b);
+  put(L.dakk, L.dakk_b);
   put(L.dgam, L.dgam_b);
+  put(L.dbv, L.dbv_b);
+  put(L.dbpart, L.dbpart_b);
+  put(L.dgpart, L.dgpart_b);
   L.total = off;
   return L;
 }
@@ -91,8 +99,8 @@ struct ResidualPtrs {
   void *state, *u;
 };
 struct BwdWorkspacePtrs {
-  void *du, *dstate, *dqh, *dw, *dkt, *daqk;
-  float* dgam;
+  void *du, *dstate, *dqh, *dbk, *dkt, *daqk, *dakk;
+  float *dgam, *dbv, *dbpart, *dgpart;
 };
 
 struct ChunkFwdArgs {
@@ -136,7 +144,8 @@ enum KernelId {
   K_DSTATE = 3,    // chunk_dstate_kernel
   K_GRADS = 4,     // chunk_grads_kernel
   K_RECURRENT = 5, // recurrent_kernel
-  K_COUNT = 6
+  K_FINALIZE = 6,  // chunk_bwd_finalize_kernel
+  K_COUNT = 7
 };
 // Records a CUDA event on s before (begin = true) or after a launch when timing is on.
 void prof_mark(KernelId id, cudaStream_t s, bool begin);

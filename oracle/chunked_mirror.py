@@ -24,8 +24,10 @@ marin.community note "factoring GDN-2 decay on TPU", section Approach: the
 chunk is cut into two consecutive blocks and the decay of a pair that spans
 the cut is split at the last token of the first block, so each query row and
 key row is scaled once and the cross-block tile is one product Q K^T.
-``scores_factored`` also applies one reference point per query block inside
-the block (the block's start for the first block, the cut for the second);
+``scores_factored`` uses that same split point as the reference for every row:
+query rows are scaled by exp(G_t - G_b) and key rows by exp(G_b - G_j), so the
+whole chunk is one masked product; factors across the cut are <= 1 and the
+in-block factors are bounded by exp(decay spread of the block).
 ``scores_pairwise`` is the direct definition.
 """
 from __future__ import annotations
@@ -50,17 +52,15 @@ def scores_pairwise(x: np.ndarray, y: np.ndarray, G: np.ndarray, inclusive: bool
 
 def scores_factored(x: np.ndarray, y: np.ndarray, G: np.ndarray, inclusive: bool,
                     block: int = BLOCK) -> np.ndarray:
-    """Same scores as ``scores_pairwise`` from row-scaled products.
+    """Same scores as ``scores_pairwise`` from one row-scaled product.
 
-    Rows of the first block use the chunk start as reference (query factor
-    exp(G_t) <= 1, key factor exp(-G_j) >= 1); rows of the second block use the
-    last token b of the first block (query factor exp(G_t - G_b) <= 1, key factor
-    exp(G_b - G_j): <= 1 across the cut, >= 1 inside the second block)."""
+    b is the last token of the first block. Query rows are scaled by
+    exp(G_t - G_b) (<= 1 in the second block, >= 1 in the first) and key rows by
+    exp(G_b - G_j) (<= 1 in the first block, >= 1 in the second), so each pair
+    gets exp(G_t - G_j); pairs across the cut use two factors <= 1."""
     C = x.shape[0]
-    P = np.zeros((C, C))
     b = block - 1
-    P[:block, :block] = (x[:block] * np.exp(G[:block])) @ (y[:block] * np.exp(-G[:block])).T
-    P[block:, :] = (x[block:] * np.exp(G[block:] - G[b])) @ (y * np.exp(G[b] - G)).T
+    P = (x * np.exp(G - G[b])) @ (y * np.exp(G[b] - G)).T
     mask = np.tril(np.ones((C, C)), 0 if inclusive else -1)
     return P * mask
 
@@ -138,30 +138,36 @@ def fwd(q, k, v, g, beta, h0=None, scale=None, chunk: int = CHUNK, factored: boo
 def chunk_grads(q, k, v, beta, L, S0, U, dO, dS1, dU, scale):
     """Chunk-parallel gradients of one chunk given the reverse scan's dU and the
     gradient dS1 of the state leaving the chunk. Returns dq, dk, dv, dG, dbeta
-    (dG is the gradient of the chunk-local cumulative log-decay G)."""
+    (dG is the gradient of the chunk-local cumulative log-decay G).
+
+    With Bk = diag(beta) K-hat, Bv = diag(beta) V, W = T Bk, U' = T Bv and
+    U = U' - W S0 = T (Bv - Bk S0), the WY factors' gradients collapse:
+      dT = dW Bk^T + dU Bv^T = dU ((I + Akk) U)^T, so with Y = T^T dU
+      dBv = Y,  dBk = -Y S0^T,  dAkk = -(T^T dT T^T) = -Y U^T  (masked j < t).
+    The score term of dbeta, sum_j dAkk[t,j] Pkk[t,j], equals sum_c k_tc dx'_tc
+    where dx' is the x-side score gradient taken with dAkk itself."""
     C = q.shape[0]
     incl = np.tril(np.ones((C, C)))
     strict = np.tril(np.ones((C, C)), -1)
-    Tm, W = L["T"], L["W"]
+    G, Gam = L["G"], L["Gam"]
     dQh = scale * dO @ S0.T
     dAqk = scale * (dO @ U.T) * incl
     dKt = U @ dS1.T
     dgam = np.sum(dS1 * S0, axis=1)
-    dW = -dU @ S0.T
-    dT = dW @ L["Bk"].T + dU @ L["Bv"].T
-    dBk = Tm.T @ dW
-    dBv = Tm.T @ dU
-    dAkk = -(Tm.T @ dT @ Tm.T) * strict
-    dbeta = np.sum(dBk * L["Kh"], 1) + np.sum(dBv * v, 1) + np.sum(dAkk * L["Pkk"], 1)
-    dPkk = beta[:, None] * dAkk
-    dq_s, dk_s, dG_qk = score_backward(q, k, L["G"], dAqk)
-    dk_x, dk_y, dG_kk = score_backward(k, k, L["G"], dPkk)
+    Y = L["T"].T @ dU
+    dv = beta[:, None] * Y
+    dBk = -Y @ S0.T
+    dAkk = -(Y @ U.T) * strict
+    dq_s, dk_s, dG_qk = score_backward(q, k, G, dAqk)
+    dxb, dyb, _ = score_backward(k, k, G, dAkk)          # with dP = dAkk
+    _, dyb_beta, _ = score_backward(beta[:, None] * k, k, G, dAkk)  # dy of dP = diag(beta) dAkk
     dKh = beta[:, None] * dBk
-    G, Gam = L["G"], L["Gam"]
+    dbeta = np.sum(Y * v, 1) + np.sum(dBk * L["Kh"], 1) + np.sum(k * dxb, 1)
+    dx_kk = beta[:, None] * dxb
     dq = dQh * Gam + dq_s
-    dk = dKh * Gam + dKt * np.exp(G[-1] - G) + dk_s + dk_x + dk_y
-    dv = beta[:, None] * dBv
-    dG = dQh * L["Qh"] + dKh * L["Kh"] - dKt * L["Kt"] + dG_qk + dG_kk
+    dk = dKh * Gam + dKt * np.exp(G[-1] - G) + dk_s + dx_kk + dyb_beta
+    dG = (dQh * L["Qh"] + dKh * L["Kh"] - dKt * L["Kt"] + dG_qk
+          + k * dx_kk - k * dyb_beta)
     dG[-1] += np.sum(dKt * L["Kt"], 0) + dgam * L["gam"]
     return dq, dk, dv, dG, dbeta
 
