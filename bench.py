@@ -161,17 +161,22 @@ def kernel_work(B, T, H, D, es=2):
     CD, CC, DD = C * D * es, C * C * es, D * D * es
     gam = D * 4
     per = {
+        # reads q, k, v, g, beta; writes scale*Aqk, T, -W, U', scale*Q-hat, K-tilde, gam
         "chunk_prep_kernel": (4 * CD + C * es + 2 * CC + 4 * CD + gam,
-                              2 * (32 * 32 + 32 * 64) * D * 2 + 2 * C * C * D * 2),
-        "chunk_scan_fwd_kernel": (3 * CD + CC + CD + gam + DD + CD + CD,
-                                  2 * C * D * D * 2 + C * C * D * 2 + D * C * D * 2),
-        "chunk_scan_bwd_kernel": (CD + CC + 3 * CD + gam + CD + DD,
-                                  C * C * D * 2 + 3 * C * D * D * 2),
-        "chunk_dstate_kernel": (3 * CD + 2 * DD + 3 * CD + CC + gam,
-                                3 * C * D * D * 2 + C * C * D * 2),
-        "chunk_grads_kernel": (4 * CD + C * es + CC + 2 * CD + CC + 2 * CD + gam + 4 * CD + C * es,
-                               2 * C * C * D * 2 + 2 * C * C * D * 2 + 2 * C * C * C * 2
-                               + (32 * 32 + 32 * 64) * D * 2 + 2 * (2 * C * C * D * 2)),
+                              2 * C * C * D * 2 + 2 * C * C * D * 2),
+        # reads -W, K-tilde, U', gam; writes the chunk-start state and U
+        "chunk_scan_fwd_kernel": (3 * CD + gam + DD + CD, 2 * C * D * D * 2),
+        # reads scale*Q-hat, scale*Aqk, state, U; writes out
+        "chunk_out_kernel": (CD + CC + DD + CD + CD, C * D * D * 2 + C * C * D * 2),
+        # reads dout, scale*Aqk, K-tilde, scale*Q-hat, -W, gam; writes dU, dS
+        "chunk_scan_bwd_kernel": (CD + CC + 3 * CD + gam + CD + DD, C * C * D * 2 + 3 * C * D * D * 2),
+        # reads T, dout, v, U, dU, state, dS, beta; writes dv, dQ-hat, dBk, dK-tilde, dAqk, dAkk, dgam, dbeta_v
+        "chunk_dstate_kernel": (CC + 4 * CD + 2 * DD + C * es + 4 * CD + 2 * CC + gam + C * 4,
+                                C * C * D * 2 + 3 * C * D * D * 2 + 2 * C * C * D * 2),
+        # reads q, k, g, beta, dQ-hat, dBk, dK-tilde, dAqk, dAkk, dgam; writes dq, dk, dg and partials
+        "chunk_grads_kernel": (3 * CD + C * es + 3 * CD + 2 * CC + gam + 3 * CD + 2 * 2 * C * 4,
+                               4 * C * C * D * 2),
+        "chunk_bwd_finalize_kernel": (C * 4 + 2 * 2 * C * 4 + C * es, 0),
     }
     return {k: (b * n, f * n) for k, (b, f) in per.items()}
 
@@ -301,7 +306,7 @@ def run_gdn(args, world, rank, local):
                    "l2": "inputs larger than L2 (q,k,v,g,dout %.0f MB + residuals %.0f MB > 129 MB)" % (
                        5 * d["q"].numel() * 2 / 1e6, res.numel() / 1e6),
                    "parallelism": f"replicas x{world} (no collective)"},
-        "gpu_launches": 5 * args.steps,
+        "gpu_launches": 7 * args.steps,
         "roofline": roofline,
         "tensor": tensor,
         "kernels": kernels,

@@ -17,7 +17,7 @@
 // as one of them; the staging here is this library's own.
 //
 // Kernels
-//   chunk_scan_bwd_kernel   grid (Dv/32, B*H), 128 threads, sequential over chunks in
+//   chunk_scan_bwd_kernel   grid (Dv/64, B*H), 256 threads, sequential over chunks in
 //                           reverse: dS in registers, writes dU and dS1 per chunk, dh0
 //   chunk_dstate_kernel     grid (chunks, B*H), 128 threads: the four products with the
 //                           chunk states (contractions over Dv) and dgam
@@ -28,11 +28,13 @@
 namespace gdn {
 namespace {
 
-constexpr int RSCAN_THREADS = 128;
+constexpr int RSCAN_THREADS = 256;
 constexpr int DST_THREADS = 256;
 
 
 // ------------------------------------------------------------------ reverse state scan
+// One CTA per (batch*head, NTS = 64 value columns), 8 warps; warp w owns gradient rows
+// (w & 3) * Dk/4 .. + Dk/4 and columns 32 (w >> 2) .. + 31 of the slice.
 template <int DK>
 struct RScanLayout {
   static constexpr int ES = 2;
@@ -41,11 +43,11 @@ struct RScanLayout {
   static constexpr int KT = QH + C * DK * ES;      // K-tilde     [C][DK]
   static constexpr int AQK = KT + C * DK * ES;     // scale Aqk   [C][C]
   static constexpr int GAM = AQK + C * C * ES;     // float [DK]
-  static constexpr int DO = a1k(GAM + DK * 4);     // dO slice    [C][NT]
-  static constexpr int STAGE = a1k(DO + C * NT * ES);
-  static constexpr int DSS = 2 * STAGE;            // dS operand  [DK][NT]
-  static constexpr int DUS = a1k(DSS + DK * NT * ES);  // dU     [C][NT]
-  static constexpr int BAR = a1k(DUS + C * NT * ES);
+  static constexpr int DO = a1k(GAM + DK * 4);     // dO slice    [C][NTS]
+  static constexpr int STAGE = a1k(DO + C * NTS * ES);
+  static constexpr int DSS = 2 * STAGE;            // dS operand  [DK][NTS] (NT slices)
+  static constexpr int DUS = a1k(DSS + DK * NTS * ES);  // dU     [C][NTS] (NT slices)
+  static constexpr int BAR = a1k(DUS + C * NTS * ES);
   static constexpr int BYTES = BAR + 64;
   static constexpr uint32_t TX = (uint32_t)(3 * C * DK * ES + C * C * ES + DK * 4);
 };
@@ -59,22 +61,24 @@ __global__ void __launch_bounds__(RSCAN_THREADS) chunk_scan_bwd_kernel(ChunkBwdA
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int tile = blockIdx.x, bh = blockIdx.y, b = bh / a.H, h = bh % a.H;
   const int N = a.T / C;
-  constexpr int NTILE = DV / NT, MTS = DK / 64, NTT = NT / 8, EPC = 8;
+  constexpr int NTILE = DV / NT, MTS = DK / 64, EPC = 8;
+  const int rg = warp & 3, cg = warp >> 2;
+  const int srow = rg * 16 * MTS, col0 = 32 * cg;
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + L::BAR);
-  Tile<T, DK, NT> dSs{reinterpret_cast<T*>(sm + L::DSS)};
-  Tile<T, C, NT> dUs{reinterpret_cast<T*>(sm + L::DUS)};
+  TTile<T, DK, NTS, NT> dSs{reinterpret_cast<T*>(sm + L::DSS)};
+  TTile<T, C, NTS, NT> dUs{reinterpret_cast<T*>(sm + L::DUS)};
   const T* dout = static_cast<const T*>(a.dout);
 
-  float dS[MTS][NTT][4];
+  float dS[MTS][4][4];
   const size_t sb = (size_t)bh * DK * DV;
 #pragma unroll
   for (int mt = 0; mt < MTS; ++mt)
 #pragma unroll
-    for (int nt = 0; nt < NTT; ++nt)
+    for (int nt = 0; nt < 4; ++nt)
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
-        const int r = warp * 16 * MTS + 16 * mt + frag_row(lane, e);
-        const int c = tile * NT + 8 * nt + frag_col(lane, e);
+        const int r = srow + 16 * mt + frag_row(lane, e);
+        const int c = tile * NTS + col0 + 8 * nt + frag_col(lane, e);
         dS[mt][nt][e] = a.dh_final ? a.dh_final[sb + (size_t)r * DV + c] : 0.f;
       }
   if (tid == 0) {
@@ -95,11 +99,11 @@ __global__ void __launch_bounds__(RSCAN_THREADS) chunk_scan_bwd_kernel(ChunkBwdA
       bulk_g2s(st + L::AQK, static_cast<const T*>(a.res.aqk) + ch * (C * C), C * C * 2, &bars[s]);
       bulk_g2s(st + L::GAM, a.res.gam + ch * DK, DK * 4, &bars[s]);
     }
-    Tile<T, C, NT> dOt{reinterpret_cast<T*>(st + L::DO)};
+    Tile<T, C, NTS> dOt{reinterpret_cast<T*>(st + L::DO)};
     const size_t row0 = ((size_t)b * a.T + (size_t)n * C) * a.H + h;
-    for (int i = tid; i < C * NT / EPC; i += RSCAN_THREADS) {
-      const int r = i / (NT / EPC), c0 = (i % (NT / EPC)) * EPC;
-      cp_async16(dOt.ptr(r, c0), dout + (row0 + (size_t)r * a.H) * DV + tile * NT + c0);
+    for (int i = tid; i < C * NTS / EPC; i += RSCAN_THREADS) {
+      const int r = i / (NTS / EPC), c0 = (i % (NTS / EPC)) * EPC;
+      cp_async16(dOt.ptr(r, c0), dout + (row0 + (size_t)r * a.H) * DV + tile * NTS + c0);
     }
     cp_async_commit();
   };
@@ -115,58 +119,57 @@ __global__ void __launch_bounds__(RSCAN_THREADS) chunk_scan_bwd_kernel(ChunkBwdA
     Tile<T, C, DK> Qt{reinterpret_cast<T*>(st + L::QH)};
     Tile<T, C, DK> Kt{reinterpret_cast<T*>(st + L::KT)};
     Tile<T, C, C> At{reinterpret_cast<T*>(st + L::AQK)};
-    Tile<T, C, NT> dOt{reinterpret_cast<T*>(st + L::DO)};
+    Tile<T, C, NTS> dOt{reinterpret_cast<T*>(st + L::DO)};
     const float* gam = reinterpret_cast<const float*>(st + L::GAM);
     const size_t ch = (size_t)bh * N + n;
 
 #pragma unroll
     for (int mt = 0; mt < MTS; ++mt)
 #pragma unroll
-      for (int nt = 0; nt < NTT; ++nt)
+      for (int nt = 0; nt < 4; ++nt)
 #pragma unroll
         for (int e = 0; e < 4; ++e)
-          dSs.at(warp * 16 * MTS + 16 * mt + frag_row(lane, e), 8 * nt + frag_col(lane, e)) =
-              from_f32<T>(dS[mt][nt][e]);
+          dSs.at(srow + 16 * mt + frag_row(lane, e), col0 + 8 * nt + frag_col(lane, e)) = from_f32<T>(dS[mt][nt][e]);
     if (more) cp_async_wait<1>(); else cp_async_wait<0>();
     mbar_wait(&bars[s], par, a.err);
     __syncthreads();
     {  // gradient of the state leaving chunk n
-      T* dst = static_cast<T*>(a.ws.dstate) + (ch * NTILE + tile) * (DK * NT);
-      for (int i = tid; i < DK * NT / EPC; i += RSCAN_THREADS) copy16(dst + i * EPC, dSs.p + i * EPC);
+      T* dst = static_cast<T*>(a.ws.dstate) + (ch * NTILE + tile * (NTS / NT)) * (DK * NT);
+      for (int i = tid; i < DK * NTS / EPC; i += RSCAN_THREADS) copy16(dst + i * EPC, dSs.p + i * EPC);
     }
-    float du[1][NTT][4];
+    float du[1][4][4];
     zero(du);
-    Gemm<T>::template run<1, NTT>(du, aview<true>(At), bview<true>(dOt), 16 * warp, 0, 0, C, lane);
-    Gemm<T>::template run<1, NTT>(du, aview<false>(Kt), bview<true>(dSs), 16 * warp, 0, 0, DK, lane);
+    Gemm<T>::template run<1, 4>(du, aview<true>(At), bview<true>(dOt), 16 * rg, col0, 0, C, lane);
+    Gemm<T>::template run<1, 4>(du, aview<false>(Kt), bview<true>(dSs), 16 * rg, col0, 0, DK, lane);
 #pragma unroll
-    for (int nt = 0; nt < NTT; ++nt)
+    for (int nt = 0; nt < 4; ++nt)
 #pragma unroll
       for (int e = 0; e < 4; ++e)
-        dUs.at(16 * warp + frag_row(lane, e), 8 * nt + frag_col(lane, e)) = from_f32<T>(du[0][nt][e]);
+        dUs.at(16 * rg + frag_row(lane, e), col0 + 8 * nt + frag_col(lane, e)) = from_f32<T>(du[0][nt][e]);
     __syncthreads();
     {
-      T* dst = static_cast<T*>(a.ws.du) + (ch * NTILE + tile) * (C * NT);
-      for (int i = tid; i < C * NT / EPC; i += RSCAN_THREADS) copy16(dst + i * EPC, dUs.p + i * EPC);
+      T* dst = static_cast<T*>(a.ws.du) + (ch * NTILE + tile * (NTS / NT)) * (C * NT);
+      for (int i = tid; i < C * NTS / EPC; i += RSCAN_THREADS) copy16(dst + i * EPC, dUs.p + i * EPC);
     }
 #pragma unroll
     for (int mt = 0; mt < MTS; ++mt)
 #pragma unroll
-      for (int nt = 0; nt < NTT; ++nt)
+      for (int nt = 0; nt < 4; ++nt)
 #pragma unroll
-        for (int e = 0; e < 4; ++e) dS[mt][nt][e] *= gam[warp * 16 * MTS + 16 * mt + frag_row(lane, e)];
-    Gemm<T>::template run<MTS, NTT>(dS, aview<true>(Qt), bview<true>(dOt), warp * 16 * MTS, 0, 0, C, lane);
-    Gemm<T>::template run<MTS, NTT>(dS, aview<true>(Wt), bview<true>(dUs), warp * 16 * MTS, 0, 0, C, lane);
+        for (int e = 0; e < 4; ++e) dS[mt][nt][e] *= gam[srow + 16 * mt + frag_row(lane, e)];
+    Gemm<T>::template run<MTS, 4>(dS, aview<true>(Qt), bview<true>(dOt), srow, col0, 0, C, lane);
+    Gemm<T>::template run<MTS, 4>(dS, aview<true>(Wt), bview<true>(dUs), srow, col0, 0, C, lane);
     __syncthreads();
   }
   if (a.dh0) {
 #pragma unroll
     for (int mt = 0; mt < MTS; ++mt)
 #pragma unroll
-      for (int nt = 0; nt < NTT; ++nt)
+      for (int nt = 0; nt < 4; ++nt)
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-          const int r = warp * 16 * MTS + 16 * mt + frag_row(lane, e);
-          const int c = tile * NT + 8 * nt + frag_col(lane, e);
+          const int r = srow + 16 * mt + frag_row(lane, e);
+          const int c = tile * NTS + col0 + 8 * nt + frag_col(lane, e);
           a.dh0[sb + (size_t)r * DV + c] = dS[mt][nt][e];
         }
   }
@@ -347,7 +350,7 @@ cudaError_t launch_bwd_t(const ChunkBwdArgs& a, cudaStream_t s) {
     auto kern = chunk_scan_bwd_kernel<DK, DV>;
     if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes)) != cudaSuccess) return e;
     prof_mark(K_SCAN_BWD, s, true);
-    kern<<<dim3(DV / NT, BH), RSCAN_THREADS, bytes, s>>>(a);
+    kern<<<dim3(DV / NTS, BH), RSCAN_THREADS, bytes, s>>>(a);
     prof_mark(K_SCAN_BWD, s, false);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }

@@ -23,8 +23,9 @@
 // Kernels
 //   chunk_prep_kernel      grid (chunks, B*H), 256 threads: A1-A5, writes the residual
 //                          records (scaled Aqk, T, -W, U', scaled Q-hat, K-tilde, gam)
-//   chunk_scan_fwd_kernel  grid (Dv/32, B*H), 128 threads: A6, fp32 state slice in
+//   chunk_scan_fwd_kernel  grid (Dv/64, B*H), 256 threads: A6, fp32 state slice in
 //                          registers; chunk records arrive by cp.async.bulk on mbarriers
+//   chunk_out_kernel       grid (chunks, B*H), 256 threads: outputs from stored states
 #include "common.cuh"
 #include "kernels.h"
 
@@ -32,7 +33,7 @@ namespace gdn {
 namespace {
 
 constexpr int PREP_THREADS = 256;
-constexpr int SCAN_THREADS = 128;
+constexpr int SCAN_THREADS = 256;
 // (i, j) of pair p in the lower triangle (diagonal included), row-major order
 __device__ __forceinline__ void tri_index(int p, int& i, int& j) {
   int r = (int)((sqrtf(8.f * p + 1.f) - 1.f) * 0.5f);
@@ -380,51 +381,54 @@ __global__ void __launch_bounds__(PREP_THREADS) chunk_prep_kernel(ChunkFwdArgs a
 }
 
 // ------------------------------------------------------------------ state scan
+// Only the recurrence is sequential: U = U' + (-W) S and S <- diag(gam) S + K-tilde^T U.
+// The outputs O = (scale Q-hat) S + (scale Aqk) U need no sequential order and are
+// produced afterwards by chunk_out_kernel from the states and U this scan stores.
 template <class T, int DK>
 struct ScanLayout {
   static constexpr int ES = (int)sizeof(T);
-  static constexpr int W = 0;                      // -W        [C][DK]
-  static constexpr int QH = W + C * DK * ES;       // scale Q-hat [C][DK]
-  static constexpr int KT = QH + C * DK * ES;      // K-tilde   [C][DK]
-  static constexpr int AQK = KT + C * DK * ES;     // scale Aqk [C][C]
-  static constexpr int UP = AQK + C * C * ES;      // U' slice  [C][NT] (then the output tile)
-  static constexpr int GAM = UP + C * NT * ES;     // float [DK]
+  static constexpr int W = 0;                        // -W        [C][DK]
+  static constexpr int KT = W + C * DK * ES;         // K-tilde   [C][DK]
+  static constexpr int UP = KT + C * DK * ES;        // U' slices [C][NTS]
+  static constexpr int GAM = UP + C * NTS * ES;      // float [DK]
   static constexpr int STAGE = a1k(GAM + DK * 4);
-  static constexpr int STAGES = ES == 2 ? 2 : 1;
-  static constexpr int SS = STAGES * STAGE;        // state operand [DK][NT]
-  static constexpr int US = a1k(SS + DK * NT * ES);  // U [C][NT]
-  static constexpr int BAR = a1k(US + C * NT * ES);
+  static constexpr int STAGES = ES == 2 ? 3 : 1;
+  static constexpr int SS = STAGES * STAGE;          // state operand [DK][NTS] (NT slices)
+  static constexpr int US = a1k(SS + DK * NTS * ES); // U [C][NTS] (NT slices)
+  static constexpr int BAR = a1k(US + C * NTS * ES);
   static constexpr int BYTES = BAR + 64;
-  static constexpr uint32_t TX = (uint32_t)(3 * C * DK * ES + C * C * ES + C * NT * ES + DK * 4);
+  static constexpr uint32_t TX = (uint32_t)(2 * C * DK * ES + C * NTS * ES + DK * 4);
 };
 
+// One CTA per (batch*head, NTS = 64 value columns), 8 warps. Warp w owns state rows
+// (w & 3) * Dk/4 .. + Dk/4 and columns 32 (w >> 2) .. + 31 of the slice.
 template <class T, int DK, int DV>
 __global__ void __launch_bounds__(SCAN_THREADS) chunk_scan_fwd_kernel(ChunkFwdArgs a) {
   typedef ScanLayout<T, DK> L;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = align1024(smem_raw);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int tile = blockIdx.x, bh = blockIdx.y, b = bh / a.H, h = bh % a.H;
+  const int tile = blockIdx.x, bh = blockIdx.y;
   const int N = a.T / C;
-  constexpr int NTILE = DV / NT;
-  constexpr int MTS = DK / 64;  // m16 tiles of state rows per warp
-  constexpr int NTT = NT / 8;
+  constexpr int NTILE = DV / NT;  // NT-column record slices per row
+  constexpr int MTS = DK / 64;    // m16 tiles of state rows per warp
   constexpr int EPC = 16 / (int)sizeof(T);
+  const int rg = warp & 3, cg = warp >> 2;
+  const int srow = rg * 16 * MTS, col0 = 32 * cg;
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + L::BAR);
-  Tile<T, DK, NT> Ss{reinterpret_cast<T*>(sm + L::SS)};
-  Tile<T, C, NT> Us{reinterpret_cast<T*>(sm + L::US)};
+  TTile<T, DK, NTS, NT> Ss{reinterpret_cast<T*>(sm + L::SS)};
+  TTile<T, C, NTS, NT> Us{reinterpret_cast<T*>(sm + L::US)};
 
-  // state slice, fragment layout: rows warp*16*MTS + 16 mt + frag_row, cols 8 nt + frag_col
-  float S[MTS][NTT][4];
+  float S[MTS][4][4];
   const size_t sb = (size_t)bh * DK * DV;
 #pragma unroll
   for (int mt = 0; mt < MTS; ++mt)
 #pragma unroll
-    for (int nt = 0; nt < NTT; ++nt)
+    for (int nt = 0; nt < 4; ++nt)
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
-        const int r = warp * 16 * MTS + 16 * mt + frag_row(lane, e);
-        const int c = tile * NT + 8 * nt + frag_col(lane, e);
+        const int r = srow + 16 * mt + frag_row(lane, e);
+        const int c = tile * NTS + col0 + 8 * nt + frag_col(lane, e);
         S[mt][nt][e] = a.h0 ? a.h0[sb + (size_t)r * DV + c] : 0.f;
       }
 
@@ -434,113 +438,154 @@ __global__ void __launch_bounds__(SCAN_THREADS) chunk_scan_fwd_kernel(ChunkFwdAr
   }
   __syncthreads();
 
-  auto issue = [&](int n, int s) {
+  auto issue = [&](int n) {
+    const int s = n % L::STAGES;
     uint8_t* st = sm + s * L::STAGE;
     const size_t ch = (size_t)bh * N + n;
     mbar_arrive_expect_tx(&bars[s], L::TX);
     bulk_g2s(st + L::W, static_cast<const T*>(a.res.wneg) + ch * (C * DK), C * DK * sizeof(T), &bars[s]);
-    bulk_g2s(st + L::QH, static_cast<const T*>(a.res.qh) + ch * (C * DK), C * DK * sizeof(T), &bars[s]);
     bulk_g2s(st + L::KT, static_cast<const T*>(a.res.kt) + ch * (C * DK), C * DK * sizeof(T), &bars[s]);
-    bulk_g2s(st + L::AQK, static_cast<const T*>(a.res.aqk) + ch * (C * C), C * C * sizeof(T), &bars[s]);
-    bulk_g2s(st + L::UP, static_cast<const T*>(a.res.up) + (ch * NTILE + tile) * (C * NT),
-             C * NT * sizeof(T), &bars[s]);
+    bulk_g2s(st + L::UP, static_cast<const T*>(a.res.up) + (ch * NTILE + tile * (NTS / NT)) * (C * NT),
+             C * NTS * sizeof(T), &bars[s]);
     bulk_g2s(st + L::GAM, a.res.gam + ch * DK, DK * 4, &bars[s]);
   };
-  if (tid == 0 && N > 0) issue(0, 0);
+  if (tid == 0)
+    for (int n = 0; n < L::STAGES - 1 && n < N; ++n) issue(n);
 
   for (int n = 0; n < N; ++n) {
     const int s = n % L::STAGES;
     const uint32_t par = (uint32_t)(n / L::STAGES) & 1u;
-    if (L::STAGES == 2 && tid == 0 && n + 1 < N) issue(n + 1, (n + 1) % 2);
+    // refill the stage freed at the end of the previous step
+    if (tid == 0 && n + L::STAGES - 1 < N) issue(n + L::STAGES - 1);
     uint8_t* st = sm + s * L::STAGE;
     Tile<T, C, DK> Wt{reinterpret_cast<T*>(st + L::W)};
-    Tile<T, C, DK> Qt{reinterpret_cast<T*>(st + L::QH)};
     Tile<T, C, DK> Kt{reinterpret_cast<T*>(st + L::KT)};
-    Tile<T, C, C> At{reinterpret_cast<T*>(st + L::AQK)};
-    Tile<T, C, NT> Up{reinterpret_cast<T*>(st + L::UP)};
+    TTile<T, C, NTS, NT> Up{reinterpret_cast<T*>(st + L::UP)};
     const float* gam = reinterpret_cast<const float*>(st + L::GAM);
     const size_t ch = (size_t)bh * N + n;
 
-    // chunk-start state -> MMA operand copy
 #pragma unroll
     for (int mt = 0; mt < MTS; ++mt)
 #pragma unroll
-      for (int nt = 0; nt < NTT; ++nt)
+      for (int nt = 0; nt < 4; ++nt)
 #pragma unroll
         for (int e = 0; e < 4; ++e)
-          Ss.at(warp * 16 * MTS + 16 * mt + frag_row(lane, e), 8 * nt + frag_col(lane, e)) =
-              from_f32<T>(S[mt][nt][e]);
+          Ss.at(srow + 16 * mt + frag_row(lane, e), col0 + 8 * nt + frag_col(lane, e)) = from_f32<T>(S[mt][nt][e]);
     mbar_wait(&bars[s], par, a.err);
     __syncthreads();
-    {  // residual: chunk-start state
-      T* dst = static_cast<T*>(a.res.state) + (ch * NTILE + tile) * (DK * NT);
-      for (int i = tid; i < DK * NT / EPC; i += SCAN_THREADS) copy16(dst + i * EPC, Ss.p + i * EPC);
+    {  // residual: chunk-start state (this CTA's two record slices are adjacent)
+      T* dst = static_cast<T*>(a.res.state) + (ch * NTILE + tile * (NTS / NT)) * (DK * NT);
+      for (int i = tid; i < DK * NTS / EPC; i += SCAN_THREADS) copy16(dst + i * EPC, Ss.p + i * EPC);
     }
-    // U = U' + (-W) S ; O = (scale Q-hat) S + (scale Aqk) U
-    float ws[1][NTT][4], o[1][NTT][4];
+    float ws[1][4][4];
     zero(ws);
-    zero(o);
-    Gemm<T>::template run<1, NTT>(ws, aview<false>(Wt), bview<true>(Ss), 16 * warp, 0, 0, DK, lane);
-    Gemm<T>::template run<1, NTT>(o, aview<false>(Qt), bview<true>(Ss), 16 * warp, 0, 0, DK, lane);
+    Gemm<T>::template run<1, 4>(ws, aview<false>(Wt), bview<true>(Ss), 16 * rg, col0, 0, DK, lane);
 #pragma unroll
-    for (int nt = 0; nt < NTT; ++nt)
+    for (int nt = 0; nt < 4; ++nt)
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
-        const int r = 16 * warp + frag_row(lane, e), c = 8 * nt + frag_col(lane, e);
+        const int r = 16 * rg + frag_row(lane, e), c = col0 + 8 * nt + frag_col(lane, e);
         Us.at(r, c) = from_f32<T>(to_f32(Up.at(r, c)) + ws[0][nt][e]);
       }
     __syncthreads();
     {  // residual: U
-      T* dst = static_cast<T*>(a.res.u) + (ch * NTILE + tile) * (C * NT);
-      for (int i = tid; i < C * NT / EPC; i += SCAN_THREADS) copy16(dst + i * EPC, Us.p + i * EPC);
+      T* dst = static_cast<T*>(a.res.u) + (ch * NTILE + tile * (NTS / NT)) * (C * NT);
+      for (int i = tid; i < C * NTS / EPC; i += SCAN_THREADS) copy16(dst + i * EPC, Us.p + i * EPC);
     }
-    Gemm<T>::template run<1, NTT>(o, aview<false>(At), bview<true>(Us), 16 * warp, 0, 0, C, lane);
-#pragma unroll
-    for (int nt = 0; nt < NTT; ++nt)
-#pragma unroll
-      for (int e = 0; e < 4; ++e)
-        Up.at(16 * warp + frag_row(lane, e), 8 * nt + frag_col(lane, e)) = from_f32<T>(o[0][nt][e]);
-    // S = diag(gam) S + K-tilde^T U
 #pragma unroll
     for (int mt = 0; mt < MTS; ++mt)
 #pragma unroll
-      for (int nt = 0; nt < NTT; ++nt)
+      for (int nt = 0; nt < 4; ++nt)
 #pragma unroll
-        for (int e = 0; e < 4; ++e) S[mt][nt][e] *= gam[warp * 16 * MTS + 16 * mt + frag_row(lane, e)];
-    Gemm<T>::template run<MTS, NTT>(S, aview<true>(Kt), bview<true>(Us), warp * 16 * MTS, 0, 0, C, lane);
+        for (int e = 0; e < 4; ++e) S[mt][nt][e] *= gam[srow + 16 * mt + frag_row(lane, e)];
+    Gemm<T>::template run<MTS, 4>(S, aview<true>(Kt), bview<true>(Us), srow, col0, 0, C, lane);
     __syncthreads();
-    {  // output tile
-      T* out = static_cast<T*>(a.out);
-      const size_t row0 = ((size_t)b * a.T + (size_t)n * C) * a.H + h;
-      for (int i = tid; i < C * NT / EPC; i += SCAN_THREADS) {
-        const int r = i / (NT / EPC), c0 = (i % (NT / EPC)) * EPC;
-        copy16(out + (row0 + (size_t)r * a.H) * DV + tile * NT + c0, Up.ptr(r, c0));
-      }
-    }
-    __syncthreads();
-    if (L::STAGES == 1 && tid == 0 && n + 1 < N) issue(n + 1, 0);
   }
   if (a.h_final) {
 #pragma unroll
     for (int mt = 0; mt < MTS; ++mt)
 #pragma unroll
-      for (int nt = 0; nt < NTT; ++nt)
+      for (int nt = 0; nt < 4; ++nt)
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-          const int r = warp * 16 * MTS + 16 * mt + frag_row(lane, e);
-          const int c = tile * NT + 8 * nt + frag_col(lane, e);
+          const int r = srow + 16 * mt + frag_row(lane, e);
+          const int c = tile * NTS + col0 + 8 * nt + frag_col(lane, e);
           a.h_final[sb + (size_t)r * DV + c] = S[mt][nt][e];
         }
+  }
+}
+
+// ------------------------------------------------------------------ outputs
+// O = (scale Q-hat) S0 + (scale Aqk) U per chunk, from the scan's chunk-start states and U.
+constexpr int OUT_THREADS = 256;
+
+template <class T, int DK, int DV>
+struct OutLayout {
+  static constexpr int ES = (int)sizeof(T);
+  static constexpr int QH = 0;                         // [C][DK]
+  static constexpr int AQ = a1k(QH + C * DK * ES);     // [C][C]
+  static constexpr int S0 = a1k(AQ + C * C * ES);      // [DK][DV] (NT slices)
+  static constexpr int U = a1k(S0 + DK * DV * ES);     // [C][DV] (NT slices), then the output tile
+  static constexpr int BYTES = a1k(U + C * DV * ES);
+};
+
+template <class T, int DK, int DV>
+__global__ void __launch_bounds__(OUT_THREADS) chunk_out_kernel(ChunkFwdArgs a) {
+  typedef OutLayout<T, DK, DV> L;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = align1024(smem_raw);
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int n = blockIdx.x, bh = blockIdx.y, b = bh / a.H, h = bh % a.H;
+  const int N = a.T / C;
+  const size_t ch = (size_t)bh * N + n;
+  constexpr int EPC = 16 / (int)sizeof(T);
+  Tile<T, C, DK> Qs{reinterpret_cast<T*>(sm + L::QH)};
+  Tile<T, C, C> As{reinterpret_cast<T*>(sm + L::AQ)};
+  TTile<T, DK, DV, NT> S0s{reinterpret_cast<T*>(sm + L::S0)};
+  TTile<T, C, DV, NT> Us{reinterpret_cast<T*>(sm + L::U)};
+  {
+    const T* s1 = static_cast<const T*>(a.res.qh) + ch * (C * DK);
+    for (int i = tid; i < C * DK / EPC; i += OUT_THREADS) cp_async16(Qs.p + i * EPC, s1 + i * EPC);
+    const T* s2 = static_cast<const T*>(a.res.aqk) + ch * (C * C);
+    for (int i = tid; i < C * C / EPC; i += OUT_THREADS) cp_async16(As.p + i * EPC, s2 + i * EPC);
+    const T* s3 = static_cast<const T*>(a.res.state) + ch * (DK * DV);
+    for (int i = tid; i < DK * DV / EPC; i += OUT_THREADS) cp_async16(S0s.p + i * EPC, s3 + i * EPC);
+    const T* s4 = static_cast<const T*>(a.res.u) + ch * (C * DV);
+    for (int i = tid; i < C * DV / EPC; i += OUT_THREADS) cp_async16(Us.p + i * EPC, s4 + i * EPC);
+  }
+  cp_async_commit();
+  cp_async_wait<0>();
+  __syncthreads();
+  const int m0 = 16 * (warp & 3), n0 = (warp >> 2) * (DV / 2);
+  constexpr int NW = DV / 16;
+  float o[1][NW][4];
+  zero(o);
+  Gemm<T>::template run<1, NW>(o, aview<false>(Qs), bview<true>(S0s), m0, n0, 0, DK, lane);
+  Gemm<T>::template run<1, NW>(o, aview<false>(As), bview<true>(Us), m0, n0, 0, C, lane);
+  __syncthreads();  // U consumed: stage the output tile in its place
+  Tile<T, C, DV> Os{reinterpret_cast<T*>(sm + L::U)};
+#pragma unroll
+  for (int nt = 0; nt < NW; ++nt)
+#pragma unroll
+    for (int e = 0; e < 4; ++e)
+      Os.at(m0 + frag_row(lane, e), n0 + 8 * nt + frag_col(lane, e)) = from_f32<T>(o[0][nt][e]);
+  __syncthreads();
+  T* out = static_cast<T*>(a.out);
+  const size_t row0 = ((size_t)b * a.T + (size_t)n * C) * a.H + h;
+  for (int i = tid; i < C * DV / EPC; i += OUT_THREADS) {
+    const int r = i / (DV / EPC), c0 = (i % (DV / EPC)) * EPC;
+    copy16(out + (row0 + (size_t)r * a.H) * DV + c0, Os.ptr(r, c0));
   }
 }
 
 template <class T, int DK, int DV>
 cudaError_t launch_fwd_t(const ChunkFwdArgs& a, cudaStream_t s) {
   const int N = a.T / C, BH = a.B * a.H;
+  cudaError_t e;
   {
     const int bytes = PrepLayout<T, DK, DV>::BYTES + 1024;
     auto kern = a.per_channel ? chunk_prep_kernel<T, DK, DV, true> : chunk_prep_kernel<T, DK, DV, false>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
     if (e != cudaSuccess) return e;
     if (N > 0) {
       prof_mark(K_PREP, s, true);
@@ -553,13 +598,23 @@ cudaError_t launch_fwd_t(const ChunkFwdArgs& a, cudaStream_t s) {
   {
     const int bytes = ScanLayout<T, DK>::BYTES + 1024;
     auto kern = chunk_scan_fwd_kernel<T, DK, DV>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
     if (e != cudaSuccess) return e;
     prof_mark(K_SCAN_FWD, s, true);
-    kern<<<dim3(DV / NT, BH), SCAN_THREADS, bytes, s>>>(a);
+    kern<<<dim3(DV / NTS, BH), SCAN_THREADS, bytes, s>>>(a);
     prof_mark(K_SCAN_FWD, s, false);
-    return cudaGetLastError();
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
+  if (N > 0) {
+    const int bytes = OutLayout<T, DK, DV>::BYTES + 1024;
+    auto kern = chunk_out_kernel<T, DK, DV>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e != cudaSuccess) return e;
+    prof_mark(K_OUT, s, true);
+    kern<<<dim3(N, BH), OUT_THREADS, bytes, s>>>(a);
+    prof_mark(K_OUT, s, false);
+  }
+  return cudaGetLastError();
 }
 
 template <class T>

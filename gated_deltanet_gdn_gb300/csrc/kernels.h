@@ -9,7 +9,8 @@ namespace gdn {
 
 constexpr int C = 64;       // chunk length (tokens)
 constexpr int BLK = 32;     // block length inside a chunk
-constexpr int NT = 32;      // value columns per state-scan CTA
+constexpr int NT = 32;      // value columns per record slice (state, U, U', dU, dS records)
+constexpr int NTS = 64;     // value columns per state-scan CTA (two record slices)
 constexpr float SAFE_SPREAD = 80.f;  // max decay spread (nats) for row-scaled in-block scores
 
 // Per (batch, head) and chunk, the forward writes these records. Byte sizes of one record
@@ -145,7 +146,8 @@ enum KernelId {
   K_GRADS = 4,     // chunk_grads_kernel
   K_RECURRENT = 5, // recurrent_kernel
   K_FINALIZE = 6,  // chunk_bwd_finalize_kernel
-  K_COUNT = 7
+  K_OUT = 7,       // chunk_out_kernel
+  K_COUNT = 8
 };
 // Records a CUDA event on s before (begin = true) or after a launch when timing is on.
 void prof_mark(KernelId id, cudaStream_t s, bool begin);

@@ -189,7 +189,8 @@ int gdn_version(void);
  * each kernel id < n the summed milliseconds and the launch count, clears the
  * record and returns GDN_OK (GDN_ERR_CUDA if an event failed). Kernel ids:
  * 0 chunk preparation, 1 forward state scan, 2 reverse state scan, 3 state
- * products, 4 chunk gradients, 5 recurrent, 6 backward finalisation;
+ * products, 4 chunk gradients, 5 recurrent, 6 backward finalisation,
+ * 7 chunk outputs;
  * gdn_kernel_name(id) names them
  * ("" for an unknown id). Not part of the paper's method: instrumentation. */
 int gdn_profile_enable(int on);
