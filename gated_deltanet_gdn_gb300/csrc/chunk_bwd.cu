@@ -130,26 +130,29 @@ __global__ void __launch_bounds__(RSCAN_THREADS) chunk_scan_bwd_kernel(ChunkBwdA
 #pragma unroll
         for (int e = 0; e < 4; ++e)
           dSs.at(srow + 16 * mt + frag_row(lane, e), col0 + 8 * nt + frag_col(lane, e)) = from_f32<T>(dS[mt][nt][e]);
+    fence_proxy_async();  // read by the bulk store below
     if (more) cp_async_wait<1>(); else cp_async_wait<0>();
     mbar_wait(&bars[s], par, a.err);
     __syncthreads();
-    {  // gradient of the state leaving chunk n
-      T* dst = static_cast<T*>(a.ws.dstate) + (ch * NTILE + tile * (NTS / NT)) * (DK * NT);
-      for (int i = tid; i < DK * NTS / EPC; i += RSCAN_THREADS) copy16(dst + i * EPC, dSs.p + i * EPC);
+    if (tid == 0) {  // gradient of the state leaving chunk n
+      bulk_s2g(static_cast<T*>(a.ws.dstate) + (ch * NTILE + tile * (NTS / NT)) * (DK * NT), dSs.p,
+               DK * NTS * 2);
+      bulk_commit();
     }
     float du[1][4][4];
     zero(du);
-    Gemm<T>::template run<1, 4>(du, aview<true>(At), bview<true>(dOt), 16 * rg, col0, 0, C, lane);
-    Gemm<T>::template run<1, 4>(du, aview<false>(Kt), bview<true>(dSs), 16 * rg, col0, 0, DK, lane);
+    Gemm<T>::template runk<1, 4, 0, C>(du, aview<true>(At), bview<true>(dOt), 16 * rg, col0, lane);
+    Gemm<T>::template runk<1, 4, 0, DK>(du, aview<false>(Kt), bview<true>(dSs), 16 * rg, col0, lane);
 #pragma unroll
     for (int nt = 0; nt < 4; ++nt)
 #pragma unroll
       for (int e = 0; e < 4; ++e)
         dUs.at(16 * rg + frag_row(lane, e), col0 + 8 * nt + frag_col(lane, e)) = from_f32<T>(du[0][nt][e]);
+    fence_proxy_async();
     __syncthreads();
-    {
-      T* dst = static_cast<T*>(a.ws.du) + (ch * NTILE + tile * (NTS / NT)) * (C * NT);
-      for (int i = tid; i < C * NTS / EPC; i += RSCAN_THREADS) copy16(dst + i * EPC, dUs.p + i * EPC);
+    if (tid == 0) {
+      bulk_s2g(static_cast<T*>(a.ws.du) + (ch * NTILE + tile * (NTS / NT)) * (C * NT), dUs.p, C * NTS * 2);
+      bulk_commit();
     }
 #pragma unroll
     for (int mt = 0; mt < MTS; ++mt)
@@ -157,10 +160,12 @@ __global__ void __launch_bounds__(RSCAN_THREADS) chunk_scan_bwd_kernel(ChunkBwdA
       for (int nt = 0; nt < 4; ++nt)
 #pragma unroll
         for (int e = 0; e < 4; ++e) dS[mt][nt][e] *= gam[srow + 16 * mt + frag_row(lane, e)];
-    Gemm<T>::template run<MTS, 4>(dS, aview<true>(Qt), bview<true>(dOt), srow, col0, 0, C, lane);
-    Gemm<T>::template run<MTS, 4>(dS, aview<true>(Wt), bview<true>(dUs), srow, col0, 0, C, lane);
+    Gemm<T>::template runk<MTS, 4, 0, C>(dS, aview<true>(Qt), bview<true>(dOt), srow, col0, lane);
+    Gemm<T>::template runk<MTS, 4, 0, C>(dS, aview<true>(Wt), bview<true>(dUs), srow, col0, lane);
+    if (tid == 0) bulk_wait_read0();  // the bulk stores have read dSs and dUs before they are rewritten
     __syncthreads();
   }
+  if (tid == 0) bulk_wait0();  // residual stores complete before the CTA retires
   if (a.dh0) {
 #pragma unroll
     for (int mt = 0; mt < MTS; ++mt)
@@ -249,7 +254,7 @@ __global__ void __launch_bounds__(DST_THREADS) chunk_dstate_kernel(ChunkBwdArgs 
   constexpr int NWV = DV / 16;
   float y[1][NWV][4];
   zero(y);
-  Gemm<T>::template run<1, NWV>(y, aview<true>(Ts), bview<true>(dUs), m0, hf * (DV / 2), 0, C, lane);
+  Gemm<T>::template runk<1, NWV, 0, C>(y, aview<true>(Ts), bview<true>(dUs), m0, hf * (DV / 2), lane);
   {
     float db[2] = {0.f, 0.f};
     T* dv = static_cast<T*>(a.dv);
@@ -307,13 +312,13 @@ __global__ void __launch_bounds__(DST_THREADS) chunk_dstate_kernel(ChunkBwdArgs 
   {
     float acc[1][NH][4];
     zero(acc);
-    Gemm<T>::template run<1, NH>(acc, aview<false>(dOs), bview<false>(S0s), m0, n0, 0, DV, lane);
+    Gemm<T>::template runk<1, NH, 0, DV>(acc, aview<false>(dOs), bview<false>(S0s), m0, n0, lane);
     store_cdk(a.ws.dqh, acc, a.scale);
     zero(acc);
-    Gemm<T>::template run<1, NH>(acc, aview<false>(Ys), bview<false>(S0s), m0, n0, 0, DV, lane);
+    Gemm<T>::template runk<1, NH, 0, DV>(acc, aview<false>(Ys), bview<false>(S0s), m0, n0, lane);
     store_cdk(a.ws.dbk, acc, -1.f);
     zero(acc);
-    Gemm<T>::template run<1, NH>(acc, aview<false>(Us), bview<false>(dS1s), m0, n0, 0, DV, lane);
+    Gemm<T>::template runk<1, NH, 0, DV>(acc, aview<false>(Us), bview<false>(dS1s), m0, n0, lane);
     store_cdk(a.ws.dkt, acc, 1.f);
   }
   // C x C products: warp rows m0, columns 32 hf .. +31 (block-1 rows see no block-2 columns)
@@ -324,8 +329,8 @@ __global__ void __launch_bounds__(DST_THREADS) chunk_dstate_kernel(ChunkBwdArgs 
     zero(aq);
     zero(ak);
     if (!dead) {
-      Gemm<T>::template run<1, 4>(aq, aview<false>(dOs), bview<false>(Us), m0, c0, 0, DV, lane);
-      Gemm<T>::template run<1, 4>(ak, aview<false>(Ys), bview<false>(Us), m0, c0, 0, DV, lane);
+      Gemm<T>::template runk<1, 4, 0, DV>(aq, aview<false>(dOs), bview<false>(Us), m0, c0, lane);
+      Gemm<T>::template runk<1, 4, 0, DV>(ak, aview<false>(Ys), bview<false>(Us), m0, c0, lane);
     }
     T* da = static_cast<T*>(a.ws.daqk) + ch * (C * C);
     T* dk = static_cast<T*>(a.ws.dakk) + ch * (C * C);

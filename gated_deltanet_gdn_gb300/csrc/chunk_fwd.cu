@@ -43,59 +43,79 @@ __device__ __forceinline__ void tri_index(int p, int& i, int& j) {
   j = p - r * (r + 1) / 2;
 }
 
-// In-place inverse of the unit lower triangular L = I + A, A strictly lower in M.
-// Diagonal and upper part of M are never read (taken as 1 and 0); the strictly lower
-// part of M receives that of T = L^-1. Forward substitution on the four 16x16 diagonal
-// blocks, then two doubling steps T21 = -T22 A21 T11 (16 -> 32 -> 64). fp32 throughout.
+// In-place inverse of the unit lower triangular L = I + A. On entry M holds A (strictly
+// lower, zeros on and above the diagonal); on exit it holds T = L^-1 with its unit
+// diagonal and zero upper part stored explicitly. Doubling: if T11, T22 invert the
+// diagonal blocks of size s, the inverse of the 2s block is [[T11, 0], [-T22 A21 T11, T22]].
+// Blocks of size 1..8 use dense fp32 loops; the 16 and 32 levels run on tensor cores with
+// the three-term TF32 split (about 21 significant bits, far below the bf16 operand error).
+typedef FTile<C, C, 4> MTile;        // padded rows: fragment loads are conflict free
+typedef FTile<BLK, BLK, 4> XTile;
+
+template <int S, int NTHR>
+__device__ __forceinline__ void inv_level_simt(MTile M, XTile X, int tid) {
+  constexpr int NB = C / (2 * S), OUT = NB * S * S;
+  for (int e = tid; e < OUT; e += NTHR) {  // X_b = A21_b T11_b
+    const int b = e / (S * S), i = (e / S) % S, c = e % S, o = b * 2 * S;
+    float acc = 0.f;
+#pragma unroll
+    for (int j = 0; j < S; ++j) acc = fmaf(M.at(o + S + i, o + j), M.at(o + j, o + c), acc);
+    X.p[e] = acc;
+  }
+  __syncthreads();
+  for (int e = tid; e < OUT; e += NTHR) {  // T21_b = -T22_b X_b
+    const int b = e / (S * S), i = (e / S) % S, c = e % S, o = b * 2 * S;
+    float acc = 0.f;
+#pragma unroll
+    for (int j = 0; j < S; ++j) acc = fmaf(M.at(o + S + i, o + S + j), X.p[b * S * S + j * S + c], acc);
+    M.at(o + S + i, o + c) = -acc;
+  }
+  __syncthreads();
+}
+
 template <int NTHR>
-__device__ void unit_lower_inverse64(FTile<C, C> M, FTile<BLK, BLK> X, int tid) {
+__device__ void unit_lower_inverse64(MTile M, XTile X, int tid) {
+  static_assert(NTHR == 256, "tensor-core levels assume 8 warps");
   const int warp = tid >> 5, lane = tid & 31;
+  for (int i = tid; i < C; i += NTHR) M.at(i, i) = 1.f;
+  __syncthreads();
+  inv_level_simt<1, NTHR>(M, X, tid);
+  inv_level_simt<2, NTHR>(M, X, tid);
+  inv_level_simt<4, NTHR>(M, X, tid);
+  inv_level_simt<8, NTHR>(M, X, tid);
+  // s = 16: two blocks (rows/cols offset o = 0, 32); warps 0..3: block w >> 1, columns 8 (w & 1)
   if (warp < 4) {
-    const int o = warp * 16;
-    for (int r = 1; r < 16; ++r) {
-      float val = 0.f;
-      const int c = lane;
-      if (c < r) {
-        val = M.at(o + r, o + c);
-        for (int j = c + 1; j < r; ++j) val = fmaf(M.at(o + r, o + j), M.at(o + j, o + c), val);
-        val = -val;
-      }
-      __syncwarp();
-      if (c < r) M.at(o + r, o + c) = val;
-      __syncwarp();
-    }
+    const int o = (warp >> 1) * 32, n0 = (warp & 1) * 8;
+    float acc[1][1][4];
+    zero(acc);
+    Gemm<float>::runk<1, 1, 0, 16>(acc, aview<false>(M, o + 16, o), bview<true>(M, o, o), 0, n0, lane);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) X.at((warp >> 1) * 16 + frag_row(lane, e), n0 + frag_col(lane, e)) = acc[0][0][e];
   }
   __syncthreads();
-  auto tval = [&](int i, int j) -> float { return i == j ? 1.f : (i > j ? M.at(i, j) : 0.f); };
-  // 16 -> 32, two independent 32-blocks at offsets 0 and 32
-  for (int e = tid; e < 2 * 256; e += NTHR) {
-    const int p = e >> 8, i = (e >> 4) & 15, c = e & 15, o = p * 32;
-    // X = A21 T11 (A21 rows o+16+i, cols o..o+15)
-    float acc = M.at(o + 16 + i, o + c);
-    for (int j = c + 1; j < 16; ++j) acc = fmaf(M.at(o + 16 + i, o + j), M.at(o + j, o + c), acc);
-    X.at(p * 16 + i, c) = acc;
+  if (warp < 4) {
+    const int o = (warp >> 1) * 32, n0 = (warp & 1) * 8;
+    float acc[1][1][4];
+    zero(acc);
+    Gemm<float>::runk<1, 1, 0, 16>(acc, aview<false>(M, o + 16, o + 16), bview<true>(X, (warp >> 1) * 16, 0), 0, n0,
+                                   lane);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) M.at(o + 16 + frag_row(lane, e), o + n0 + frag_col(lane, e)) = -acc[0][0][e];
   }
   __syncthreads();
-  for (int e = tid; e < 2 * 256; e += NTHR) {
-    const int p = e >> 8, i = (e >> 4) & 15, c = e & 15, o = p * 32;
-    float acc = X.at(p * 16 + i, c);
-    for (int j = 0; j < i; ++j) acc = fmaf(M.at(o + 16 + i, o + 16 + j), X.at(p * 16 + j, c), acc);
-    M.at(o + 16 + i, o + c) = -acc;
-  }
-  __syncthreads();
-  // 32 -> 64
-  for (int e = tid; e < 1024; e += NTHR) {
-    const int i = e >> 5, c = e & 31;
-    float acc = M.at(32 + i, c);
-    for (int j = c + 1; j < 32; ++j) acc = fmaf(M.at(32 + i, j), tval(j, c), acc);
-    X.at(i, c) = acc;
-  }
-  __syncthreads();
-  for (int e = tid; e < 1024; e += NTHR) {
-    const int i = e >> 5, c = e & 31;
-    float acc = X.at(i, c);
-    for (int j = 0; j < i; ++j) acc = fmaf(tval(32 + i, 32 + j), X.at(j, c), acc);
-    M.at(32 + i, c) = -acc;
+  // s = 32: one block; warp w: rows 16 (w & 1), columns 8 (w >> 1)
+  {
+    const int m0 = 16 * (warp & 1), n0 = 8 * (warp >> 1);
+    float acc[1][1][4];
+    zero(acc);
+    Gemm<float>::runk<1, 1, 0, 32>(acc, aview<false>(M, 32, 0), bview<true>(M, 0, 0), m0, n0, lane);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) X.at(m0 + frag_row(lane, e), n0 + frag_col(lane, e)) = acc[0][0][e];
+    __syncthreads();
+    zero(acc);
+    Gemm<float>::runk<1, 1, 0, 32>(acc, aview<false>(M, 32, 32), bview<true>(X, 0, 0), m0, n0, lane);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) M.at(32 + m0 + frag_row(lane, e), n0 + frag_col(lane, e)) = -acc[0][0][e];
   }
   __syncthreads();
 }
@@ -105,24 +125,25 @@ struct PrepLayout {
   static constexpr int ES = (int)sizeof(T);
   static constexpr int MX = DK > DV ? DK : DV;
   static constexpr int RK = C * MX * ES;
-  static constexpr int RX = C * MX * ES > C * C * 4 ? C * MX * ES : C * C * 4;
-  static constexpr int RY = C * MX * ES > BLK * BLK * 4 ? C * MX * ES : BLK * BLK * 4;
+  static constexpr int RX = C * MX * ES > MTile::BYTES ? C * MX * ES : MTile::BYTES;
+  static constexpr int RY = C * MX * ES > XTile::BYTES ? C * MX * ES : XTile::BYTES;
   static constexpr int G = 0;                         // float [C][DK] cumulative log-decay
-  static constexpr int K = a1k(G + C * DK * 4);       // k; later -W staging
-  static constexpr int X = a1k(K + RK);               // q -> query-side rows; key-side k; Akk/T (fp32); beta*v
-  static constexpr int Y = a1k(X + RX);               // raw g; key-side rows; inverse scratch; beta*Gam*k; U' staging
+  static constexpr int K = a1k(G + C * DK * 4);       // k, then beta Gam k in place
+  static constexpr int X = a1k(K + RK);               // q, then q e1; then Akk / T (fp32); then beta v
+  static constexpr int X2 = a1k(X + RX);              // k e1 (query side of Akk); then -W staging
+  static constexpr int Y = a1k(X2 + RK);              // raw g; k e2 (key side); inverse scratch; U' staging
   static constexpr int TST = a1k(Y + RY);             // [C][C]: scale*Aqk staging, then T
-  static constexpr int BETA = a1k(TST + C * C * ES);  // float [C]
-  static constexpr int BYTES = BETA + C * 4;
+  static constexpr int BETA = a1k(TST + C * C * ES);  // float [C] beta, float [C] scalar decay
+  static constexpr int BYTES = BETA + 2 * C * 4;
 };
 
 // In-block pairwise scores (A4) for the blocks flagged unsafe: 4 lanes per (i, j) pair,
 // each summing a quarter of the channels, reduced with two xor shuffles. Writes
 // scale * sum q k E into the Aqk staging tile and beta_i * sum k k E (i > j) into Akk.
 template <class T, int DK, int NTHR>
-__device__ __noinline__ void prep_pairwise(bool unsafe1, bool unsafe2, const T* q, size_t row0, size_t rs,
-                                           Tile<T, C, DK> ks, FTile<C, DK> Gs, Tile<T, C, C> Tst,
-                                           FTile<C, C> Akk, const float* beta_s, float scale, int tid) {
+__device__ __noinline__ void prep_pairwise(bool unsafe1, bool unsafe2, const T* q, const T* k, size_t row0,
+                                           size_t rs, FTile<C, DK> Gs, Tile<T, C, C> Tst, FTile<C, C, 4> Akk,
+                                           const float* beta_s, float scale, int tid) {
   const int warp = tid >> 5, lane = tid & 31;
   for (int blk = 0; blk < 2; ++blk) {
     if (!(blk == 0 ? unsafe1 : unsafe2)) continue;
@@ -136,11 +157,13 @@ __device__ __noinline__ void prep_pairwise(bool unsafe1, bool unsafe2, const T* 
       if (valid) {
         tri_index(p, i, j);
         const T* qi = q + (row0 + (size_t)(bs + i) * rs) * DK;
+        const T* ki = k + (row0 + (size_t)(bs + i) * rs) * DK;
+        const T* kj = k + (row0 + (size_t)(bs + j) * rs) * DK;
         for (int c = quarter * (DK / 4); c < (quarter + 1) * (DK / 4); ++c) {
           const float e = __expf(Gs.at(bs + i, c) - Gs.at(bs + j, c));
-          const float kj = to_f32(ks.at(bs + j, c)) * e;
-          sq = fmaf(to_f32(qi[c]), kj, sq);
-          sk = fmaf(to_f32(ks.at(bs + i, c)), kj, sk);
+          const float kje = to_f32(kj[c]) * e;
+          sq = fmaf(to_f32(qi[c]), kje, sq);
+          sk = fmaf(to_f32(ki[c]), kje, sk);
         }
       }
       sq += __shfl_xor_sync(0xffffffffu, sq, 1);
@@ -191,22 +214,21 @@ __global__ void __launch_bounds__(PREP_THREADS) chunk_prep_kernel(ChunkFwdArgs a
     if (PC) cp_async16(graw + r * DK + c, g + gi);
   }
   cp_async_commit();
-  if (tid < C) beta_s[tid] = to_f32(beta[row0 + tid * rs]);
-  if (!PC)
-    for (int i = tid; i < C * DK; i += PREP_THREADS) Gs.at(i / DK, i % DK) = to_f32(g[row0 + (i / DK) * rs]);
+  float* gsc = reinterpret_cast<float*>(sm + L::BETA) + C;  // scalar decay per token
+  if (tid < C) {
+    beta_s[tid] = to_f32(beta[row0 + tid * rs]);
+    if (!PC) gsc[tid] = to_f32(g[row0 + tid * rs]);
+  }
   cp_async_wait<0>();
   __syncthreads();
-  if (PC)
-    for (int i = tid; i < C * DK; i += PREP_THREADS) Gs.at(i / DK, i % DK) = to_f32(graw[i]);
-  __syncthreads();
 
-  // ---- A1: inclusive cumulative log-decay per channel, two threads per channel
+  // ---- A1: inclusive cumulative log-decay per channel (fp32), two threads per channel
   for (int u = tid; u < 2 * DK; u += PREP_THREADS) {
     const int c = u % DK, r0 = (u / DK) * BLK;
     float s = 0.f;
 #pragma unroll 8
     for (int r = r0; r < r0 + BLK; ++r) {
-      s += Gs.at(r, c);
+      s += PC ? to_f32(graw[r * DK + c]) : gsc[r];
       Gs.at(r, c) = s;
     }
   }
@@ -229,31 +251,42 @@ __global__ void __launch_bounds__(PREP_THREADS) chunk_prep_kernel(ChunkFwdArgs a
   const bool unsafe1 = __syncthreads_or(u1 || force) != 0;
   const bool unsafe2 = __syncthreads_or(u2 || force) != 0;
 
-  // ---- A2: scan records (scale Q-hat, K-tilde, gam) and the row-scaled score operands
+  // ---- A2, one pass with four exponentials per element: the scan records (scale Q-hat,
+  // K-tilde), the row-scaled score operands about the block boundary b (q e1 and k e1 on
+  // the query side, k e2 on the key side; e1 = exp(G - G_b), e2 = exp(G_b - G)) and
+  // beta Gam k for W, written over k
+  Tile<T, C, DK> X2s{reinterpret_cast<T*>(sm + L::X2)};
   T* qh_g = static_cast<T*>(a.res.qh) + ch * (C * DK);
   T* kt_g = static_cast<T*>(a.res.kt) + ch * (C * DK);
-  for (int i = tid; i < C * CPR; i += PREP_THREADS) {
-    const int r = i / CPR, c0 = (i % CPR) * EPC;
+  for (int i = tid; i < C * (DK / 4); i += PREP_THREADS) {
+    const int r = i / (DK / 4), c0 = (i % (DK / 4)) * 4;
     const bool dead_q = r < BLK ? unsafe1 : false;   // query rows whose factor may overflow
     const bool dead_k = r < BLK ? false : unsafe2;   // key rows whose factor may overflow
-    __align__(16) T qv[EPC], kv[EPC], o1[EPC], o2[EPC], xq[EPC], yk[EPC];
-    copy16(qv, Xs.ptr(r, c0));
-    copy16(kv, ks.ptr(r, c0));
+    float qv[4], kv[4], G[4], Gb[4], GC[4], o1[4], o2[4], xq[4], xk[4], yk[4], bk[4];
+    ld4(qv, Xs.ptr(r, c0));
+    ld4(kv, ks.ptr(r, c0));
+    ld4(G, &Gs.at(r, c0));
+    ld4(Gb, &Gs.at(BLK - 1, c0));
+    ld4(GC, &Gs.at(C - 1, c0));
+    const float br = beta_s[r];
 #pragma unroll
-    for (int e = 0; e < EPC; ++e) {
-      const int c = c0 + e;
-      const float G = Gs.at(r, c), Gb = Gs.at(BLK - 1, c), GC = Gs.at(C - 1, c);
-      const float qf = to_f32(qv[e]), kf = to_f32(kv[e]);
-      o1[e] = from_f32<T>(a.scale * __expf(G) * qf);
-      o2[e] = from_f32<T>(__expf(GC - G) * kf);
-      xq[e] = from_f32<T>(dead_q ? 0.f : qf * __expf(G - Gb));
-      yk[e] = from_f32<T>(dead_k ? 0.f : kf * __expf(Gb - G));
+    for (int e = 0; e < 4; ++e) {
+      const float gm = __expf(G[e]), kd = __expf(GC[e] - G[e]);
+      const float e1 = dead_q ? 0.f : __expf(G[e] - Gb[e]), e2 = dead_k ? 0.f : __expf(Gb[e] - G[e]);
+      o1[e] = a.scale * gm * qv[e];
+      o2[e] = kd * kv[e];
+      xq[e] = qv[e] * e1;
+      xk[e] = kv[e] * e1;
+      yk[e] = kv[e] * e2;
+      bk[e] = br * gm * kv[e];
     }
     const int off = Sw<T, C, DK>::off(r, c0);
-    copy16(qh_g + off, o1);
-    copy16(kt_g + off, o2);
-    copy16(Xs.ptr(r, c0), xq);
-    copy16(Ys.ptr(r, c0), yk);
+    st4(qh_g + off, o1);
+    st4(kt_g + off, o2);
+    st4(Xs.ptr(r, c0), xq);
+    st4(X2s.ptr(r, c0), xk);
+    st4(Ys.ptr(r, c0), yk);
+    st4(ks.ptr(r, c0), bk);
   }
   for (int c = tid; c < DK; c += PREP_THREADS) a.res.gam[ch * DK + c] = __expf(Gs.at(C - 1, c));
   __syncthreads();
@@ -262,42 +295,26 @@ __global__ void __launch_bounds__(PREP_THREADS) chunk_prep_kernel(ChunkFwdArgs a
   // Block-1 rows never see block-2 keys; unsafe blocks leave their in-block tile to A4.
   const int rg = warp & 3, hf = warp >> 2, m0 = 16 * rg, n0 = 32 * hf;
   const bool skip = (m0 < BLK) && (hf == 1 || unsafe1);
-  float acc[1][4][4];
-  zero(acc);
-  if (!skip) Gemm<T>::template run<1, 4>(acc, aview<false>(Xs), bview<false>(Ys), m0, n0, 0, DK, lane);
-#pragma unroll
-  for (int nt = 0; nt < 4; ++nt)
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const int r = m0 + frag_row(lane, e), j = n0 + 8 * nt + frag_col(lane, e);
-      Tst.at(r, j) = from_f32<T>(j <= r ? a.scale * acc[0][nt][e] : 0.f);
-    }
-  __syncthreads();
-  for (int i = tid; i < C * CPR; i += PREP_THREADS) {  // query side for Akk: the keys
-    const int r = i / CPR, c0 = (i % CPR) * EPC;
-    const bool dead_q = r < BLK ? unsafe1 : false;
-    __align__(16) T kv[EPC], xk[EPC];
-    copy16(kv, ks.ptr(r, c0));
-#pragma unroll
-    for (int e = 0; e < EPC; ++e)
-      xk[e] = from_f32<T>(dead_q ? 0.f : to_f32(kv[e]) * __expf(Gs.at(r, c0 + e) - Gs.at(BLK - 1, c0 + e)));
-    copy16(Xs.ptr(r, c0), xk);
+  float aq[1][4][4], ak[1][4][4];
+  zero(aq);
+  zero(ak);
+  if (!skip) {
+    Gemm<T>::template runk<1, 4, 0, DK>(aq, aview<false>(Xs), bview<false>(Ys), m0, n0, lane);
+    Gemm<T>::template runk<1, 4, 0, DK>(ak, aview<false>(X2s), bview<false>(Ys), m0, n0, lane);
   }
-  __syncthreads();
-  zero(acc);
-  if (!skip) Gemm<T>::template run<1, 4>(acc, aview<false>(Xs), bview<false>(Ys), m0, n0, 0, DK, lane);
   __syncthreads();  // every warp is done reading X: it becomes the fp32 Akk
-  FTile<C, C> Akk{reinterpret_cast<float*>(sm + L::X)};
+  MTile Akk{reinterpret_cast<float*>(sm + L::X)};
 #pragma unroll
   for (int nt = 0; nt < 4; ++nt)
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
       const int r = m0 + frag_row(lane, e), j = n0 + 8 * nt + frag_col(lane, e);
-      Akk.at(r, j) = j < r ? beta_s[r] * acc[0][nt][e] : 0.f;
+      Tst.at(r, j) = from_f32<T>(j <= r ? a.scale * aq[0][nt][e] : 0.f);
+      Akk.at(r, j) = j < r ? beta_s[r] * ak[0][nt][e] : 0.f;
     }
   __syncthreads();
   if (unsafe1 || unsafe2) {
-    prep_pairwise<T, DK, PREP_THREADS>(unsafe1, unsafe2, q, row0, rs, ks, Gs, Tst, Akk, beta_s, a.scale, tid);
+    prep_pairwise<T, DK, PREP_THREADS>(unsafe1, unsafe2, q, k, row0, rs, Gs, Tst, Akk, beta_s, a.scale, tid);
     __syncthreads();
   }
 
@@ -306,18 +323,10 @@ __global__ void __launch_bounds__(PREP_THREADS) chunk_prep_kernel(ChunkFwdArgs a
     T* dst = static_cast<T*>(a.res.aqk) + ch * (C * C);
     for (int i = tid; i < C * C / EPC; i += PREP_THREADS) copy16(dst + i * EPC, Tst.p + i * EPC);
   }
-  unit_lower_inverse64<PREP_THREADS>(Akk, FTile<BLK, BLK>{reinterpret_cast<float*>(sm + L::Y)}, tid);
+  unit_lower_inverse64<PREP_THREADS>(Akk, XTile{reinterpret_cast<float*>(sm + L::Y)}, tid);
   for (int i = tid; i < C * C; i += PREP_THREADS) {
     const int r = i / C, c = i % C;
-    Tst.at(r, c) = from_f32<T>(r == c ? 1.f : (r > c ? Akk.at(r, c) : 0.f));
-  }
-  for (int i = tid; i < C * CPR; i += PREP_THREADS) {  // beta Gam k -> Y
-    const int r = i / CPR, c0 = (i % CPR) * EPC;
-    __align__(16) T kv[EPC], bk[EPC];
-    copy16(kv, ks.ptr(r, c0));
-#pragma unroll
-    for (int e = 0; e < EPC; ++e) bk[e] = from_f32<T>(beta_s[r] * __expf(Gs.at(r, c0 + e)) * to_f32(kv[e]));
-    copy16(Ys.ptr(r, c0), bk);
+    Tst.at(r, c) = from_f32<T>(r >= c ? Akk.at(r, c) : 0.f);
   }
   __syncthreads();  // T in Tst; X (fp32 T) free: v arrives there
   Tile<T, C, DV> Vs{reinterpret_cast<T*>(sm + L::X)};
@@ -331,15 +340,15 @@ __global__ void __launch_bounds__(PREP_THREADS) chunk_prep_kernel(ChunkFwdArgs a
     T* dst = static_cast<T*>(a.res.tmat) + ch * (C * C);
     for (int i = tid; i < C * C / EPC; i += PREP_THREADS) copy16(dst + i * EPC, Tst.p + i * EPC);
   }
-  // -W = -T (beta Gam k), staged in K (k is no longer needed)
+  // -W = -T (beta Gam k), staged in X2
   {
     constexpr int NW = DK / 16;
     float accw[1][NW][4];
     zero(accw);
-    Gemm<T>::template run<1, NW>(accw, aview<false>(Tst), bview<true>(Ys), m0, hf * (DK / 2), 0, C, lane);
+    Gemm<T>::template runk<1, NW, 0, C>(accw, aview<false>(Tst), bview<true>(ks), m0, hf * (DK / 2), lane);
     cp_async_wait<0>();
-    __syncthreads();  // all warps done with k (B operand rows were Y) and v has landed
-    Tile<T, C, DK> wst{reinterpret_cast<T*>(sm + L::K)};
+    __syncthreads();  // v has landed
+    Tile<T, C, DK> wst{reinterpret_cast<T*>(sm + L::X2)};
 #pragma unroll
     for (int nt = 0; nt < NW; ++nt)
 #pragma unroll
@@ -354,12 +363,12 @@ __global__ void __launch_bounds__(PREP_THREADS) chunk_prep_kernel(ChunkFwdArgs a
     for (int e = 0; e < EPC; ++e) vv[e] = from_f32<T>(beta_s[r] * to_f32(vv[e]));
     copy16(Vs.ptr(r, c0), vv);
   }
-  __syncthreads();  // beta v complete; Y (beta Gam k) consumed: U' is staged there
+  __syncthreads();  // beta v complete; U' is staged in Y
   {
     constexpr int NU = DV / 16;
     float accu[1][NU][4];
     zero(accu);
-    Gemm<T>::template run<1, NU>(accu, aview<false>(Tst), bview<true>(Vs), m0, hf * (DV / 2), 0, C, lane);
+    Gemm<T>::template runk<1, NU, 0, C>(accu, aview<false>(Tst), bview<true>(Vs), m0, hf * (DV / 2), lane);
     T* ust = reinterpret_cast<T*>(sm + L::Y);
 #pragma unroll
     for (int nt = 0; nt < NU; ++nt)
@@ -372,7 +381,7 @@ __global__ void __launch_bounds__(PREP_THREADS) chunk_prep_kernel(ChunkFwdArgs a
   __syncthreads();
   {
     T* dw = static_cast<T*>(a.res.wneg) + ch * (C * DK);
-    const T* sw = reinterpret_cast<const T*>(sm + L::K);
+    const T* sw = reinterpret_cast<const T*>(sm + L::X2);
     for (int i = tid; i < C * DK / EPC; i += PREP_THREADS) copy16(dw + i * EPC, sw + i * EPC);
     T* du = static_cast<T*>(a.res.up) + ch * (C * DV);
     const T* su = reinterpret_cast<const T*>(sm + L::Y);
@@ -392,7 +401,7 @@ struct ScanLayout {
   static constexpr int UP = KT + C * DK * ES;        // U' slices [C][NTS]
   static constexpr int GAM = UP + C * NTS * ES;      // float [DK]
   static constexpr int STAGE = a1k(GAM + DK * 4);
-  static constexpr int STAGES = ES == 2 ? 3 : 1;
+  static constexpr int STAGES = ES == 2 ? 4 : 1;
   static constexpr int SS = STAGES * STAGE;          // state operand [DK][NTS] (NT slices)
   static constexpr int US = a1k(SS + DK * NTS * ES); // U [C][NTS] (NT slices)
   static constexpr int BAR = a1k(US + C * NTS * ES);
@@ -471,15 +480,17 @@ __global__ void __launch_bounds__(SCAN_THREADS) chunk_scan_fwd_kernel(ChunkFwdAr
 #pragma unroll
         for (int e = 0; e < 4; ++e)
           Ss.at(srow + 16 * mt + frag_row(lane, e), col0 + 8 * nt + frag_col(lane, e)) = from_f32<T>(S[mt][nt][e]);
+    fence_proxy_async();  // the state copy is read by the bulk store below
     mbar_wait(&bars[s], par, a.err);
     __syncthreads();
-    {  // residual: chunk-start state (this CTA's two record slices are adjacent)
-      T* dst = static_cast<T*>(a.res.state) + (ch * NTILE + tile * (NTS / NT)) * (DK * NT);
-      for (int i = tid; i < DK * NTS / EPC; i += SCAN_THREADS) copy16(dst + i * EPC, Ss.p + i * EPC);
+    if (tid == 0) {  // residual: chunk-start state (this CTA's two record slices are adjacent)
+      bulk_s2g(static_cast<T*>(a.res.state) + (ch * NTILE + tile * (NTS / NT)) * (DK * NT), Ss.p,
+               DK * NTS * sizeof(T));
+      bulk_commit();
     }
     float ws[1][4][4];
     zero(ws);
-    Gemm<T>::template run<1, 4>(ws, aview<false>(Wt), bview<true>(Ss), 16 * rg, col0, 0, DK, lane);
+    Gemm<T>::template runk<1, 4, 0, DK>(ws, aview<false>(Wt), bview<true>(Ss), 16 * rg, col0, lane);
 #pragma unroll
     for (int nt = 0; nt < 4; ++nt)
 #pragma unroll
@@ -487,10 +498,11 @@ __global__ void __launch_bounds__(SCAN_THREADS) chunk_scan_fwd_kernel(ChunkFwdAr
         const int r = 16 * rg + frag_row(lane, e), c = col0 + 8 * nt + frag_col(lane, e);
         Us.at(r, c) = from_f32<T>(to_f32(Up.at(r, c)) + ws[0][nt][e]);
       }
+    fence_proxy_async();
     __syncthreads();
-    {  // residual: U
-      T* dst = static_cast<T*>(a.res.u) + (ch * NTILE + tile * (NTS / NT)) * (C * NT);
-      for (int i = tid; i < C * NTS / EPC; i += SCAN_THREADS) copy16(dst + i * EPC, Us.p + i * EPC);
+    if (tid == 0) {  // residual: U
+      bulk_s2g(static_cast<T*>(a.res.u) + (ch * NTILE + tile * (NTS / NT)) * (C * NT), Us.p, C * NTS * sizeof(T));
+      bulk_commit();
     }
 #pragma unroll
     for (int mt = 0; mt < MTS; ++mt)
@@ -498,9 +510,11 @@ __global__ void __launch_bounds__(SCAN_THREADS) chunk_scan_fwd_kernel(ChunkFwdAr
       for (int nt = 0; nt < 4; ++nt)
 #pragma unroll
         for (int e = 0; e < 4; ++e) S[mt][nt][e] *= gam[srow + 16 * mt + frag_row(lane, e)];
-    Gemm<T>::template run<MTS, 4>(S, aview<true>(Kt), bview<true>(Us), srow, col0, 0, C, lane);
+    Gemm<T>::template runk<MTS, 4, 0, C>(S, aview<true>(Kt), bview<true>(Us), srow, col0, lane);
+    if (tid == 0) bulk_wait_read0();  // the bulk stores have read Ss and Us before they are rewritten
     __syncthreads();
   }
+  if (tid == 0) bulk_wait0();  // residual stores complete before the CTA retires
   if (a.h_final) {
 #pragma unroll
     for (int mt = 0; mt < MTS; ++mt)
@@ -560,8 +574,8 @@ __global__ void __launch_bounds__(OUT_THREADS) chunk_out_kernel(ChunkFwdArgs a) 
   constexpr int NW = DV / 16;
   float o[1][NW][4];
   zero(o);
-  Gemm<T>::template run<1, NW>(o, aview<false>(Qs), bview<true>(S0s), m0, n0, 0, DK, lane);
-  Gemm<T>::template run<1, NW>(o, aview<false>(As), bview<true>(Us), m0, n0, 0, C, lane);
+  Gemm<T>::template runk<1, NW, 0, DK>(o, aview<false>(Qs), bview<true>(S0s), m0, n0, lane);
+  Gemm<T>::template runk<1, NW, 0, C>(o, aview<false>(As), bview<true>(Us), m0, n0, lane);
   __syncthreads();  // U consumed: stage the output tile in its place
   Tile<T, C, DV> Os{reinterpret_cast<T*>(sm + L::U)};
 #pragma unroll

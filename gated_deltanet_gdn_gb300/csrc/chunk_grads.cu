@@ -30,8 +30,9 @@ struct GrLayout {
   static constexpr int G = 0;                         // float [C][GLD]
   static constexpr int Q = a1k(G + C * GLD * 4);      // q     [C][HC]
   static constexpr int K = a1k(Q + C * HC * 2);       // k     [C][HC]
-  static constexpr int X = a1k(K + C * HC * 2);       // query-side rows; with Y: dG staging
-  static constexpr int Y = X + C * HC * 2;            // key-side rows
+  static constexpr int X = a1k(K + C * HC * 2);       // query-side rows q e1
+  static constexpr int XB = X + C * HC * 2;           // query-side rows beta k e1
+  static constexpr int Y = a1k(XB + C * HC * 2);      // key-side rows k e2
   static constexpr int DQH = a1k(Y + C * HC * 2);     // dQ-hat   [C][HC]
   static constexpr int DBK = a1k(DQH + C * HC * 2);   // dBk      [C][HC]
   static constexpr int DKT = a1k(DBK + C * HC * 2);   // dK-tilde [C][HC]
@@ -42,8 +43,10 @@ struct GrLayout {
   static constexpr int DBS = DIAG + C * 4;            // float [2][C] dbeta partials
   static constexpr int COLS = DBS + 2 * C * 4;        // float [4][HC] K-tilde column partials
   static constexpr int GCOL = COLS + 4 * HC * 4;      // float [HC] dgam * gam
-  static constexpr int BYTES = GCOL + HC * 4;
-  static_assert(Y - X == C * HC * 2, "dG staging spans X and Y");
+  static constexpr int GSC = GCOL + HC * 4;           // float [C] scalar decay per token
+  static constexpr int BYTES = GSC + C * 4;
+  static constexpr int DG = X;                        // float [C][HC] dG staging over X and XB
+  static_assert(XB - X == C * HC * 2, "dG staging spans X and XB");
 };
 
 typedef Tile<bf16, C, HC> HTile;
@@ -134,24 +137,23 @@ __global__ void __launch_bounds__(GR_THREADS, 2) chunk_grads_kernel(ChunkBwdArgs
     }
   }
   cp_async_commit();
-  if (tid < C) beta_s[tid] = to_f32(beta[row0 + tid * rs]);
-  if (!PC)
-    for (int i = tid; i < C * HC; i += GR_THREADS) Gat(i / HC, i % HC) = to_f32(g[row0 + (i / HC) * rs]);
+  float* gsc = reinterpret_cast<float*>(sm + L::GSC);
+  if (tid < C) {
+    beta_s[tid] = to_f32(beta[row0 + tid * rs]);
+    if (!PC) gsc[tid] = to_f32(g[row0 + tid * rs]);
+  }
   cp_async_wait<0>();
   __syncthreads();
-  if (PC)
-    for (int i = tid; i < C * HC; i += GR_THREADS) Gat(i / HC, i % HC) = to_f32(graw[i]);
   if (tid < C) {  // the diagonal of dAqk only feeds dq and dk (its dG terms cancel exactly)
     diag_s[tid] = to_f32(dAq.at(tid, tid));
     dAq.at(tid, tid) = from_f32<T>(0.f);
   }
-  __syncthreads();
-  for (int u = tid; u < 2 * HC; u += GR_THREADS) {  // cumulative log-decay, two threads per channel
+  for (int u = tid; u < 2 * HC; u += GR_THREADS) {  // cumulative log-decay (fp32), two threads per channel
     const int c = u % HC, r0 = (u / HC) * BLK;
     float s = 0.f;
 #pragma unroll 8
     for (int r = r0; r < r0 + BLK; ++r) {
-      s += Gat(r, c);
+      s += PC ? to_f32(graw[r * HC + c]) : gsc[r];
       Gat(r, c) = s;
     }
   }
@@ -172,20 +174,29 @@ __global__ void __launch_bounds__(GR_THREADS, 2) chunk_grads_kernel(ChunkBwdArgs
   const bool unsafe1 = __syncthreads_or(u1 || force) != 0;
   const bool unsafe2 = __syncthreads_or(u2 || force) != 0;
 
-  // row-scaled operands: X (query side, x = beta k first) and Y (key side)
-  for (int i = tid; i < C * HC / EPC; i += GR_THREADS) {
-    const int r = i / (HC / EPC), c0 = (i % (HC / EPC)) * EPC;
-    __align__(16) T kv[EPC], xb[EPC], yk[EPC];
-    copy16(kv, Ks.ptr(r, c0));
+  // row-scaled operands, one pass: X = q e1, XB = beta k e1 (query side), Y = k e2 (key side),
+  // with e1 = exp(G - G_b), e2 = exp(G_b - G) about the block boundary b
+  HTile XBs{reinterpret_cast<T*>(sm + L::XB)};
+  for (int i = tid; i < C * (HC / 4); i += GR_THREADS) {
+    const int r = i / (HC / 4), c0 = (i % (HC / 4)) * 4;
+    float kv[4], qv[4], G[4], Gb[4], xq[4], xb[4], yk[4];
+    ld4(kv, Ks.ptr(r, c0));
+    ld4(qv, Qs.ptr(r, c0));
+    ld4(G, &Gat(r, c0));
+    ld4(Gb, &Gat(BLK - 1, c0));
     const bool dead_x = r < BLK && unsafe1, dead_y = r >= BLK && unsafe2;
+    const float br = beta_s[r];
 #pragma unroll
-    for (int e = 0; e < EPC; ++e) {
-      const float G = Gat(r, c0 + e), Gb = Gat(BLK - 1, c0 + e), kf = to_f32(kv[e]);
-      xb[e] = from_f32<T>(dead_x ? 0.f : beta_s[r] * kf * __expf(G - Gb));
-      yk[e] = from_f32<T>(dead_y ? 0.f : kf * __expf(Gb - G));
+    for (int e = 0; e < 4; ++e) {
+      const float d = G[e] - Gb[e];
+      const float e1 = dead_x ? 0.f : __expf(d);
+      xq[e] = qv[e] * e1;
+      xb[e] = br * kv[e] * e1;
+      yk[e] = dead_y ? 0.f : kv[e] * __expf(-d);
     }
-    copy16(Xs.ptr(r, c0), xb);
-    copy16(Ys.ptr(r, c0), yk);
+    st4(Xs.ptr(r, c0), xq);
+    st4(XBs.ptr(r, c0), xb);
+    st4(Ys.ptr(r, c0), yk);
   }
   __syncthreads();
 
@@ -193,137 +204,109 @@ __global__ void __launch_bounds__(GR_THREADS, 2) chunk_grads_kernel(ChunkBwdArgs
   const int m0 = 16 * (warp & 3), cq = warp >> 2, c0 = 32 * cq;
   const bool blk1 = m0 < BLK;
   const bool pw_rows = blk1 ? unsafe1 : unsafe2;  // in-block part of these rows is pairwise
-  float dk_acc[4][4], dG_acc[4][4], dbp[2] = {0.f, 0.f};
+  // x side: dP Y over key columns [0, BLK) for block-1 rows, [0, C) otherwise;
+  // y side: dP^T X over query rows [0, C) for block-1 rows, [BLK, C) otherwise
+  float axB[1][4][4], ayB[1][4][4], axA[1][4][4], ayA[1][4][4];
+  zero(axB);
+  zero(ayB);
+  zero(axA);
+  zero(ayA);
+  if (blk1) {
+    if (!unsafe1) {
+      Gemm<T>::template runk<1, 4, 0, BLK>(axB, aview<false>(dAk), bview<true>(Ys), m0, c0, lane);
+      Gemm<T>::template runk<1, 4, 0, BLK>(axA, aview<false>(dAq), bview<true>(Ys), m0, c0, lane);
+    }
+    Gemm<T>::template runk<1, 4, 0, C>(ayB, aview<true>(dAk), bview<true>(XBs), m0, c0, lane);
+    Gemm<T>::template runk<1, 4, 0, C>(ayA, aview<true>(dAq), bview<true>(Xs), m0, c0, lane);
+  } else {
+    Gemm<T>::template runk<1, 4, 0, C>(axB, aview<false>(dAk), bview<true>(Ys), m0, c0, lane);
+    Gemm<T>::template runk<1, 4, 0, C>(axA, aview<false>(dAq), bview<true>(Ys), m0, c0, lane);
+    if (!unsafe2) {
+      Gemm<T>::template runk<1, 4, BLK, C>(ayB, aview<true>(dAk), bview<true>(XBs), m0, c0, lane);
+      Gemm<T>::template runk<1, 4, BLK, C>(ayA, aview<true>(dAq), bview<true>(Xs), m0, c0, lane);
+    }
+  }
 
-  // x-side GEMM over key columns [0, C) ([0, BLK) for block-1 rows), y-side over query rows
-  auto products = [&](const Tile<T, C, C>& dP, float (&ax)[1][4][4], float (&ay)[1][4][4]) {
-    zero(ax);
-    zero(ay);
-    if (!(blk1 && unsafe1))
-      Gemm<T>::template run<1, 4>(ax, aview<false>(dP), bview<true>(Ys), m0, c0, 0, blk1 ? BLK : C, lane);
-    if (!(!blk1 && unsafe2))
-      Gemm<T>::template run<1, 4>(ay, aview<true>(dP), bview<true>(Xs), m0, c0, blk1 ? 0 : BLK, C, lane);
-  };
-
-  {  // ---- Akk family (x = k, weights beta on the query side)
-    float ax[1][4][4], ay[1][4][4];
-    products(dAk, ax, ay);
-#pragma unroll
-    for (int nt = 0; nt < 4; ++nt)
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int r = m0 + frag_row(lane, e), c = c0 + 8 * nt + frag_col(lane, e);
-        const float G = Gat(r, c), Gb = Gat(BLK - 1, c), kf = to_f32(Ks.at(r, c));
-        float dxp = (blk1 && unsafe1) ? 0.f : ax[0][nt][e] * __expf(G - Gb);
-        float dy = (!blk1 && unsafe2) ? 0.f : ay[0][nt][e] * __expf(Gb - G);
-        if (pw_rows) {
-          const int bs = blk1 ? 0 : BLK;
-          dxp += pw_dx(&dAk, &Ks, Gp, r, c, bs, r);
-          dy += pw_dy(&dAk, &Ks, beta_s, Gp, r, c, r, bs + BLK - 1);
-        }
-        const float dx = beta_s[r] * dxp;
-        dbp[e >> 1] += kf * dxp;
-        dk_acc[nt][e] = dx + dy;
-        dG_acc[nt][e] = kf * (dx - dy);
-      }
-  }
-  __syncthreads();  // X consumed: rebuild it with the queries
-  for (int i = tid; i < C * HC / EPC; i += GR_THREADS) {
-    const int r = i / (HC / EPC), cc = (i % (HC / EPC)) * EPC;
-    __align__(16) T qv[EPC], xq[EPC];
-    copy16(qv, Qs.ptr(r, cc));
-    const bool dead_x = r < BLK && unsafe1;
-#pragma unroll
-    for (int e = 0; e < EPC; ++e)
-      xq[e] = from_f32<T>(dead_x ? 0.f : to_f32(qv[e]) * __expf(Gat(r, cc + e) - Gat(BLK - 1, cc + e)));
-    copy16(Xs.ptr(r, cc), xq);
-  }
-  __syncthreads();
-  {  // ---- Aqk family (x = q); dq is complete after this block
-    float ax[1][4][4], ay[1][4][4];
-    products(dAq, ax, ay);
-    T* dq = static_cast<T*>(a.dq);
-#pragma unroll
-    for (int nt = 0; nt < 4; ++nt)
-#pragma unroll
-      for (int e = 0; e < 4; e += 2) {
-        float out[2];
-#pragma unroll
-        for (int u = 0; u < 2; ++u) {
-          const int r = m0 + frag_row(lane, e + u), c = c0 + 8 * nt + frag_col(lane, e + u);
-          const float G = Gat(r, c), Gb = Gat(BLK - 1, c);
-          const float qf = to_f32(Qs.at(r, c)), kf = to_f32(Ks.at(r, c));
-          float dx = (blk1 && unsafe1) ? 0.f : ax[0][nt][e + u] * __expf(G - Gb);
-          float dy = (!blk1 && unsafe2) ? 0.f : ay[0][nt][e + u] * __expf(Gb - G);
-          if (pw_rows) {
-            const int bs = blk1 ? 0 : BLK;
-            dx += pw_dx(&dAq, &Ks, Gp, r, c, bs, r);
-            dy += pw_dy(&dAq, &Qs, nullptr, Gp, r, c, r, bs + BLK - 1);
-          }
-          const float gm = __expf(G), a1 = to_f32(dQh.at(r, c));
-          out[u] = a1 * gm + dx + diag_s[r] * kf;
-          dk_acc[nt][e + u] += dy + diag_s[r] * qf;
-          dG_acc[nt][e + u] += qf * dx - kf * dy + a1 * gm * qf;
-        }
-        const int r = m0 + frag_row(lane, e), c = c0 + 8 * nt + frag_col(lane, e);
-        store2(dq + (row0 + r * rs) * DK + cbase + c, out[0], out[1]);
-      }
-  }
-  // ---- elementwise terms of K-hat (via dBk) and K-tilde; dk out
+  __syncthreads();  // every warp is done reading X and XB: dG is staged there
+  // one epilogue per element pair: every gradient term of (r, c) and (r, c + 1)
+  float* dGs = reinterpret_cast<float*>(sm + L::DG);
+  float dbp[2] = {0.f, 0.f}, colp[4][2];
   {
+    T* dq = static_cast<T*>(a.dq);
     T* dk = static_cast<T*>(a.dk);
-    float colp[4][2];
+    const int bs = blk1 ? 0 : BLK;
+    const bool skip_x = blk1 && unsafe1, skip_y = !blk1 && unsafe2;
 #pragma unroll
     for (int nt = 0; nt < 4; ++nt) {
+      const int c = c0 + 8 * nt + 2 * (lane & 3);
+      const float2 gb = *reinterpret_cast<const float2*>(&Gat(BLK - 1, c));
+      const float2 gc = *reinterpret_cast<const float2*>(&Gat(C - 1, c));
       colp[nt][0] = colp[nt][1] = 0.f;
 #pragma unroll
       for (int e = 0; e < 4; e += 2) {
+        const int r = m0 + frag_row(lane, e);
+        const float2 G2 = *reinterpret_cast<const float2*>(&Gat(r, c));
+        const __nv_bfloat162 k2 = *reinterpret_cast<const __nv_bfloat162*>(Ks.ptr(r, c));
+        const __nv_bfloat162 q2 = *reinterpret_cast<const __nv_bfloat162*>(Qs.ptr(r, c));
+        const __nv_bfloat162 h2 = *reinterpret_cast<const __nv_bfloat162*>(dQh.ptr(r, c));
+        const __nv_bfloat162 b2 = *reinterpret_cast<const __nv_bfloat162*>(dBk.ptr(r, c));
+        const __nv_bfloat162 t2 = *reinterpret_cast<const __nv_bfloat162*>(dKt.ptr(r, c));
+        const float br = beta_s[r], dg = diag_s[r];
+        float oq[2], ok[2];
 #pragma unroll
         for (int u = 0; u < 2; ++u) {
-          const int r = m0 + frag_row(lane, e + u), c = c0 + 8 * nt + frag_col(lane, e + u);
-          const float G = Gat(r, c), GC = Gat(C - 1, c), kf = to_f32(Ks.at(r, c));
-          const float gm = __expf(G), kdec = __expf(GC - G);
-          const float bk = to_f32(dBk.at(r, c)), kt = to_f32(dKt.at(r, c));
-          const float khat = gm * kf, ktil = kdec * kf, dkh = beta_s[r] * bk;
-          dbp[e >> 1] += bk * khat;
-          dk_acc[nt][e + u] += dkh * gm + kt * kdec;
-          dG_acc[nt][e + u] += dkh * khat - kt * ktil;
-          colp[nt][u] += kt * ktil;
+          const float G = u ? G2.y : G2.x, Gb = u ? gb.y : gb.x, GC = u ? gc.y : gc.x;
+          const float kf = u ? __high2float(k2) : __low2float(k2);
+          const float qf = u ? __high2float(q2) : __low2float(q2);
+          const float dqh = u ? __high2float(h2) : __low2float(h2);
+          const float dbk = u ? __high2float(b2) : __low2float(b2);
+          const float dkt = u ? __high2float(t2) : __low2float(t2);
+          const float e1 = __expf(G - Gb), e2 = __expf(Gb - G), gm = __expf(G), kd = __expf(GC - G);
+          float dxb = skip_x ? 0.f : axB[0][nt][e + u] * e1;  // Akk family, dP = dAkk
+          float dyb = skip_y ? 0.f : ayB[0][nt][e + u] * e2;
+          float dxa = skip_x ? 0.f : axA[0][nt][e + u] * e1;  // Aqk family
+          float dya = skip_y ? 0.f : ayA[0][nt][e + u] * e2;
+          if (pw_rows) {
+            dxb += pw_dx(&dAk, &Ks, Gp, r, c + u, bs, r);
+            dyb += pw_dy(&dAk, &Ks, beta_s, Gp, r, c + u, r, bs + BLK - 1);
+            dxa += pw_dx(&dAq, &Ks, Gp, r, c + u, bs, r);
+            dya += pw_dy(&dAq, &Qs, nullptr, Gp, r, c + u, r, bs + BLK - 1);
+          }
+          const float khat = gm * kf, ktil = kd * kf, dkh = br * dbk;
+          oq[u] = dqh * gm + dxa + dg * kf;
+          ok[u] = br * dxb + dyb + dya + dg * qf + dkh * gm + dkt * kd;
+          dGs[r * HC + c + u] = kf * (br * dxb - dyb - dya) + qf * (dxa + dqh * gm) + dkh * khat - dkt * ktil;
+          dbp[e >> 1] += kf * dxb + dbk * khat;
+          colp[nt][u] += dkt * ktil;
         }
-        const int r = m0 + frag_row(lane, e), c = c0 + 8 * nt + frag_col(lane, e);
-        store2(dk + (row0 + r * rs) * DK + cbase + c, dk_acc[nt][e], dk_acc[nt][e + 1]);
+        const size_t gi = (row0 + r * rs) * DK + cbase + c;
+        store2(dq + gi, oq[0], oq[1]);
+        store2(dk + gi, ok[0], ok[1]);
       }
-    }
-    // column sums over this warp's 16 rows (lanes sharing a column differ in bits 2..4)
-#pragma unroll
-    for (int nt = 0; nt < 4; ++nt)
-#pragma unroll
-      for (int u = 0; u < 2; ++u) {
-        float x = colp[nt][u];
-        x += __shfl_xor_sync(0xffffffffu, x, 4);
-        x += __shfl_xor_sync(0xffffffffu, x, 8);
-        x += __shfl_xor_sync(0xffffffffu, x, 16);
-        if (lane < 4) cols_s[(warp & 3) * HC + c0 + 8 * nt + 2 * lane + u] = x;
-      }
-#pragma unroll
-    for (int i = 0; i < 2; ++i) {
-      dbp[i] += __shfl_xor_sync(0xffffffffu, dbp[i], 1);
-      dbp[i] += __shfl_xor_sync(0xffffffffu, dbp[i], 2);
-    }
-    if ((lane & 3) == 0) {
-      db_s[cq * C + m0 + (lane >> 2)] = dbp[0];
-      db_s[cq * C + m0 + (lane >> 2) + 8] = dbp[1];
     }
   }
-  __syncthreads();  // X and Y free: dG staging (fp32 [C][HC])
-  float* dGs = reinterpret_cast<float*>(sm + L::X);
+  // column sums over this warp's 16 rows (lanes sharing a column differ in bits 2..4)
 #pragma unroll
   for (int nt = 0; nt < 4; ++nt)
 #pragma unroll
-    for (int e = 0; e < 4; ++e)
-      dGs[(m0 + frag_row(lane, e)) * HC + c0 + 8 * nt + frag_col(lane, e)] = dG_acc[nt][e];
+    for (int u = 0; u < 2; ++u) {
+      float x = colp[nt][u];
+      x += __shfl_xor_sync(0xffffffffu, x, 4);
+      x += __shfl_xor_sync(0xffffffffu, x, 8);
+      x += __shfl_xor_sync(0xffffffffu, x, 16);
+      if (lane < 4) cols_s[(warp & 3) * HC + c0 + 8 * nt + 2 * lane + u] = x;
+    }
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    dbp[i] += __shfl_xor_sync(0xffffffffu, dbp[i], 1);
+    dbp[i] += __shfl_xor_sync(0xffffffffu, dbp[i], 2);
+  }
+  if ((lane & 3) == 0) {
+    db_s[cq * C + m0 + (lane >> 2)] = dbp[0];
+    db_s[cq * C + m0 + (lane >> 2) + 8] = dbp[1];
+  }
+  __syncthreads();  // dG, column and dbeta partials complete
   if (tid < C) a.ws.dbpart[(ch * 2 + grp) * C + tid] = db_s[tid] + db_s[C + tid];
-  __syncthreads();
   // reverse cumulative sum per channel; the last row also gets the K-tilde column sum and
   // dgam * gam (both are derivatives with respect to G at the chunk's last token)
   for (int u = tid; u < 2 * HC; u += GR_THREADS) {

@@ -252,6 +252,35 @@ __device__ __forceinline__ void warp_gemm_tf32x3(float (&acc)[MT][NT][4], const 
   }
 }
 
+// Same products with the k range fixed at compile time: the loop unrolls, so the
+// fragment loads of step k + 1 overlap the MMAs of step k.
+template <int MT, int NT, int K0, int K1, class AV, class BV>
+__device__ __forceinline__ void warp_gemm_bf16_k(float (&acc)[MT][NT][4], const AV& A, const BV& B, int m0,
+                                                 int n0, int lane) {
+#pragma unroll
+  for (int k0 = K0; k0 < K1; k0 += 16) {
+    uint32_t a[MT][4];
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt) load_a(a[mt], A, m0 + 16 * mt, k0, lane);
+#pragma unroll
+    for (int nt = 0; nt + 1 < NT; nt += 2) {
+      uint32_t b[4];
+      load_b2(b, B, n0 + 8 * nt, k0, lane);
+#pragma unroll
+      for (int mt = 0; mt < MT; ++mt) {
+        mma_bf16(acc[mt][nt], a[mt], b);
+        mma_bf16(acc[mt][nt + 1], a[mt], b + 2);
+      }
+    }
+    if (NT & 1) {
+      uint32_t b[2];
+      load_b1(b, B, n0 + 8 * (NT - 1), k0, lane);
+#pragma unroll
+      for (int mt = 0; mt < MT; ++mt) mma_bf16(acc[mt][NT - 1], a[mt], b);
+    }
+  }
+}
+
 template <class T> struct Gemm;
 template <> struct Gemm<bf16> {
   static constexpr int KSTEP = 16;
@@ -260,6 +289,11 @@ template <> struct Gemm<bf16> {
                                              int n0, int kb, int ke, int lane) {
     warp_gemm_bf16<MT, NT>(acc, A, B, m0, n0, kb, ke, lane);
   }
+  template <int MT, int NT, int K0, int K1, class AV, class BV>
+  __device__ static __forceinline__ void runk(float (&acc)[MT][NT][4], const AV& A, const BV& B, int m0,
+                                              int n0, int lane) {
+    warp_gemm_bf16_k<MT, NT, K0, K1>(acc, A, B, m0, n0, lane);
+  }
 };
 template <> struct Gemm<float> {
   static constexpr int KSTEP = 8;
@@ -267,6 +301,11 @@ template <> struct Gemm<float> {
   __device__ static __forceinline__ void run(float (&acc)[MT][NT][4], const AV& A, const BV& B, int m0,
                                              int n0, int kb, int ke, int lane) {
     warp_gemm_tf32x3<MT, NT>(acc, A, B, m0, n0, kb, ke, lane);
+  }
+  template <int MT, int NT, int K0, int K1, class AV, class BV>
+  __device__ static __forceinline__ void runk(float (&acc)[MT][NT][4], const AV& A, const BV& B, int m0,
+                                              int n0, int lane) {
+    warp_gemm_tf32x3<MT, NT>(acc, A, B, m0, n0, K0, K1, lane);
   }
 };
 
@@ -345,6 +384,26 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, unsign
 // 16-byte vector copy helpers
 __device__ __forceinline__ void copy16(void* dst, const void* src) {
   *reinterpret_cast<uint4*>(dst) = *reinterpret_cast<const uint4*>(src);
+}
+// Four consecutive elements (8 bytes of bf16, 16 bytes of fp32) as floats.
+__device__ __forceinline__ void ld4(float (&x)[4], const bf16* p) {
+  const uint2 u = *reinterpret_cast<const uint2*>(p);
+  const __nv_bfloat162 a = *reinterpret_cast<const __nv_bfloat162*>(&u.x);
+  const __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162*>(&u.y);
+  x[0] = __low2float(a); x[1] = __high2float(a); x[2] = __low2float(b); x[3] = __high2float(b);
+}
+__device__ __forceinline__ void ld4(float (&x)[4], const float* p) {
+  const float4 u = *reinterpret_cast<const float4*>(p);
+  x[0] = u.x; x[1] = u.y; x[2] = u.z; x[3] = u.w;
+}
+__device__ __forceinline__ void st4(bf16* p, const float (&x)[4]) {
+  uint2 u;
+  *reinterpret_cast<__nv_bfloat162*>(&u.x) = __floats2bfloat162_rn(x[0], x[1]);
+  *reinterpret_cast<__nv_bfloat162*>(&u.y) = __floats2bfloat162_rn(x[2], x[3]);
+  *reinterpret_cast<uint2*>(p) = u;
+}
+__device__ __forceinline__ void st4(float* p, const float (&x)[4]) {
+  *reinterpret_cast<float4*>(p) = make_float4(x[0], x[1], x[2], x[3]);
 }
 
 // ------------------------------------------------------------------ misc helpers
