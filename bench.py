@@ -39,6 +39,8 @@ def parse_args():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="gdn", choices=["gdn", "reference"])
     ap.add_argument("--no-extras", action="store_true", help="skip decode, e2e and cpu baseline legs")
+    ap.add_argument("--batch", type=int, default=None,
+                    help="override the batch size (small profiling cases only; the JSON line says so)")
     return ap.parse_args()
 
 
@@ -220,6 +222,8 @@ def run_gdn(args, world, rank, local):
     gdn.load(build_if_needed=True)
     dev = torch.device("cuda", local)
     w = WORKLOADS[WORKLOAD]
+    if args.batch:
+        w = w.with_(B=args.batch)
     host = make_inputs(w)
     d = {k: (None if v is None else v.to(dev)) for k, v in host.items()}
     dims = gdn.make_dims(d["q"], d["v"], d["g"])
@@ -300,8 +304,8 @@ def run_gdn(args, world, rank, local):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_max, 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic",
-        "config": {"workload": "chunked fwd+bwd, B8 T4096 H6 Dk=Dv=128, bf16 inputs / fp32 state, "
-                               "per-channel decay, chunk 64",
+        "config": {"workload": "chunked fwd+bwd, B%d T4096 H6 Dk=Dv=128, bf16 inputs / fp32 state, "
+                               "per-channel decay, chunk 64" % w.B,
                    "B": w.B, "T": w.T, "H": w.H, "Dk": w.Dk, "Dv": w.Dv, "tokens_per_step_per_gpu": tokens,
                    "l2": "inputs larger than L2 (q,k,v,g,dout %.0f MB + residuals %.0f MB > 129 MB)" % (
                        5 * d["q"].numel() * 2 / 1e6, res.numel() / 1e6),
@@ -365,7 +369,7 @@ def e2e_leg(args, host, d, step, outputs, world):
 
 def decode_leg(dev):
     """Recurrent kernel: decode steps (T = 1) with the state read and written once,
-    L2 flushed between timed steps; a batch whose state exceeds L2; and the
+    L2 flushed between timed steps (a buffer twice the L2 size is read); a batch whose state exceeds L2; and the
     2048-token prefill of the same geometry."""
     import torch
 
@@ -373,7 +377,8 @@ def decode_leg(dev):
     from gated_deltanet_gdn_gb300.synthetic import WORKLOADS, make_inputs
 
     res = {}
-    flush = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=dev)
+    # read (not written) between steps, so no dirty lines are written back inside a timed step
+    flush = torch.ones(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
     for B, label in ((2, "B2 H48 Dk=Dv=128 fp32 (L2 flushed between steps)"),
                      (32, "B32 H48 Dk=Dv=128 fp32 (state 201 MB > L2)")):
         w = WORKLOADS["recurrent"].with_(B=B, T=1, h0_std=0.01)
@@ -389,7 +394,7 @@ def decode_leg(dev):
         times = []
         for _ in range(30):
             if B == 2:
-                flush.zero_()
+                flush.sum()
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             e0.record()
             one()
