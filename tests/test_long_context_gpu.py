@@ -65,13 +65,35 @@ def _divergence_check(o_gpu, o_ref, tol):
     return checked, nonfinite
 
 
+def _perturbation_envelope(args, norms, rel, trials=8, seed=0):
+    """How far the exact rule itself moves on this slice when q, k, v and the
+    incoming state get i.i.d. relative perturbations of size `rel` (the rounding
+    of a bf16 operand): the largest per-row |log10 norm ratio| and the largest
+    aggregate relative error over `trials` seeded draws."""
+    rng = np.random.default_rng(seed)
+    ref, _ = oracle.fwd(*args)
+    worst_ratio = worst_agg = 0.0
+    for _ in range(trials):
+        b = list(args)
+        for i in (0, 1, 2, 5):
+            b[i] = args[i] * (1 + rng.uniform(-rel, rel, args[i].shape))
+        p, _ = oracle.fwd(*b)
+        ok = np.isfinite(ref).all(-1) & (norms < 1e30) & np.isfinite(p).all(-1)
+        worst_ratio = max(worst_ratio, np.abs(np.log10(np.linalg.norm(p, axis=-1)[ok] / norms[ok])).max())
+        worst_agg = max(worst_agg, np.linalg.norm((p - ref)[ok]) / np.linalg.norm(ref[ok]))
+    return worst_ratio, worst_agg
+
+
 def test_out_of_region_slice_diverges_like_the_oracle(long_run):
     """The recurrent kernel follows the oracle row by row (bf16 output tolerance).
-    The chunked path follows it to 1e-4 per row with fp32 inputs; with bf16 inputs
-    its operands are rounded to bf16 and then amplified by |k| ~ 11 (single rows
-    measured up to ~0.3 off), so it must reproduce the divergence itself: every
-    row's norm within a factor 10^0.2 of the oracle's and the slice as a whole
-    within 2e-2 (the pages give no accuracy for a chunked form in this regime)."""
+    The chunked path follows it to 1e-4 per row with fp32 inputs. With bf16 inputs
+    its intermediate operands are rounded to bf16, and on this slice the rule is so
+    ill-conditioned that bf16-sized perturbations of the inputs alone move single
+    rows by up to ~10x in norm (the pages give no accuracy for any form of the rule
+    in this regime). So the chunked bf16 path must reproduce the divergence itself
+    (growth by > 1e6 over the chunk) and stay within the envelope that such
+    perturbations give the exact rule: per-row log10 norm ratio and aggregate
+    relative error no larger than the worst of eight seeded perturbed oracle runs."""
     w, host, out, hT, ro, rh, o_ref, h_ref = long_run
     h0 = torch.from_numpy(h_ref).to(torch.float32)  # the oracle's state after the region
     for dtype in ("bf16", "f32"):
@@ -91,9 +113,12 @@ def test_out_of_region_slice_diverges_like_the_oracle(long_run):
         else:
             finite = np.isfinite(so_ref).all(axis=-1) & (norms < 1e30)
             co = c_out.double().cpu().numpy()
-            ratio = np.log10(np.linalg.norm(co, axis=-1)[finite] / norms[finite])
-            assert np.abs(ratio).max() <= 0.2, np.abs(ratio).max()
+            cn = np.linalg.norm(co, axis=-1)
+            assert cn[finite].max() > 1e6 * cn[:, :2].max()  # the chunked path diverges too
+            env_ratio, env_agg = _perturbation_envelope(args, norms, 2.0 ** -9)
+            ratio = np.abs(np.log10(cn[finite] / norms[finite])).max()
+            assert ratio <= env_ratio, (ratio, env_ratio)
             err = np.linalg.norm((co - so_ref)[finite]) / np.linalg.norm(so_ref[finite])
-            assert err <= TOL["bf16"], err
+            assert err <= env_agg, (err, env_agg)
             checked = int(finite.sum())
         assert checked > 0
