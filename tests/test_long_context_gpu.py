@@ -46,9 +46,48 @@ def test_long_context_recurrent(long_run):
     assert rel(head_slice(rh, PAIRS, state=True), h_ref) <= 1e-4  # fp32 state, exact recurrence
 
 
-def _divergence_check(o_gpu, o_ref, tol):
-    """Per-row rule: within tol while the oracle row norm stays below 1e30;
-    non-finite once the oracle row leaves the fp32 range."""
+def _perturbed_runs(args, rel, trials=8, seed=0):
+    """The exact rule on this slice with q, k, v and the incoming state given
+    i.i.d. relative perturbations of size `rel`, over `trials` seeded draws."""
+    rng = np.random.default_rng(seed)
+    runs = []
+    for _ in range(trials):
+        b = list(args)
+        for i in (0, 1, 2, 5):
+            b[i] = args[i] * (1 + rng.uniform(-rel, rel, args[i].shape))
+        runs.append(oracle.fwd(*b)[0])
+    return runs
+
+
+def _row_envelope(args, ref, rel):
+    """Per output row, the largest relative deviation of a perturbed run: how far
+    the exact rule itself moves when its inputs carry errors of size `rel`."""
+    norms = np.linalg.norm(ref, axis=-1)
+    env = np.zeros_like(norms)
+    with np.errstate(all="ignore"):
+        for p in _perturbed_runs(args, rel):
+            dev = np.linalg.norm(p - ref, axis=-1) / np.maximum(norms, 1e-30)
+            env = np.maximum(env, np.where(np.isfinite(dev), dev, 0.0))
+    return env
+
+
+def _aggregate_envelope(args, ref, rel):
+    """Largest per-row |log10 norm ratio| and largest aggregate relative error of
+    a perturbed run over the rows where the exact result is finite."""
+    norms = np.linalg.norm(ref, axis=-1)
+    worst_ratio = worst_agg = 0.0
+    with np.errstate(all="ignore"):
+        for p in _perturbed_runs(args, rel):
+            ok = np.isfinite(ref).all(-1) & (norms < 1e30) & np.isfinite(p).all(-1)
+            worst_ratio = max(worst_ratio, np.abs(np.log10(np.linalg.norm(p, axis=-1)[ok] / norms[ok])).max())
+            worst_agg = max(worst_agg, np.linalg.norm((p - ref)[ok]) / np.linalg.norm(ref[ok]))
+    return worst_ratio, worst_agg
+
+
+def _divergence_check(o_gpu, o_ref, tol, env):
+    """Per-row rule: within max(tol, the row's perturbation envelope) while the
+    oracle row norm stays below 1e30; non-finite once the oracle row leaves the
+    fp32 range."""
     o = o_gpu.double().numpy()
     checked = nonfinite = 0
     for t in range(o.shape[1]):
@@ -57,7 +96,7 @@ def _divergence_check(o_gpu, o_ref, tol):
             nrm = np.linalg.norm(ref)
             if nrm < 1e30:
                 err = np.linalg.norm(o[0, t, h] - ref) / max(nrm, 1e-30)
-                assert err <= tol, (t, h, err)
+                assert err <= max(tol, env[0, t, h]), (t, h, err, env[0, t, h])
                 checked += 1
             elif not np.isfinite(nrm) or nrm > 3.4e38:
                 assert not np.all(np.isfinite(o[0, t, h])), (t, h)
@@ -65,35 +104,16 @@ def _divergence_check(o_gpu, o_ref, tol):
     return checked, nonfinite
 
 
-def _perturbation_envelope(args, norms, rel, trials=8, seed=0):
-    """How far the exact rule itself moves on this slice when q, k, v and the
-    incoming state get i.i.d. relative perturbations of size `rel` (the rounding
-    of a bf16 operand): the largest per-row |log10 norm ratio| and the largest
-    aggregate relative error over `trials` seeded draws."""
-    rng = np.random.default_rng(seed)
-    ref, _ = oracle.fwd(*args)
-    worst_ratio = worst_agg = 0.0
-    for _ in range(trials):
-        b = list(args)
-        for i in (0, 1, 2, 5):
-            b[i] = args[i] * (1 + rng.uniform(-rel, rel, args[i].shape))
-        p, _ = oracle.fwd(*b)
-        ok = np.isfinite(ref).all(-1) & (norms < 1e30) & np.isfinite(p).all(-1)
-        worst_ratio = max(worst_ratio, np.abs(np.log10(np.linalg.norm(p, axis=-1)[ok] / norms[ok])).max())
-        worst_agg = max(worst_agg, np.linalg.norm((p - ref)[ok]) / np.linalg.norm(ref[ok]))
-    return worst_ratio, worst_agg
-
-
 def test_out_of_region_slice_diverges_like_the_oracle(long_run):
-    """The recurrent kernel follows the oracle row by row (bf16 output tolerance).
-    The chunked path follows it to 1e-4 per row with fp32 inputs. With bf16 inputs
-    its intermediate operands are rounded to bf16, and on this slice the rule is so
-    ill-conditioned that bf16-sized perturbations of the inputs alone move single
-    rows by up to ~10x in norm (the pages give no accuracy for any form of the rule
-    in this regime). So the chunked bf16 path must reproduce the divergence itself
-    (growth by > 1e6 over the chunk) and stay within the envelope that such
-    perturbations give the exact rule: per-row log10 norm ratio and aggregate
-    relative error no larger than the worst of eight seeded perturbed oracle runs."""
+    """The pages give no accuracy for any form of the rule in this regime, and on
+    this slice the rule is badly conditioned: relative input perturbations of one
+    fp32 unit roundoff already move single rows by ~5e-4, bf16-sized ones by ~10x
+    in norm. So each tolerance is the output's tolerance or the spread of eight
+    seeded perturbed oracle runs, whichever is larger, with the perturbation set
+    by the arithmetic: Dk * 2^-24 (the dot-product rounding bound in fp32) for the
+    recurrent kernel and the fp32 chunked path, checked row by row; 2^-9 (bf16
+    operands) for the bf16 chunked path, checked by per-row norm ratio and in
+    aggregate, after it has reproduced the divergence (growth by > 1e6)."""
     w, host, out, hT, ro, rh, o_ref, h_ref = long_run
     h0 = torch.from_numpy(h_ref).to(torch.float32)  # the oracle's state after the region
     for dtype in ("bf16", "f32"):
@@ -106,16 +126,17 @@ def test_out_of_region_slice_diverges_like_the_oracle(long_run):
         r_out, _ = gdn.gdn_recurrent(d["q"], d["k"], d["v"], d["g"], d["beta"], d["h0"])
         c_out, _, _ = gdn.gdn_chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], d["h0"])
         torch.cuda.synchronize()
-        checked, _ = _divergence_check(r_out.cpu(), so_ref, TOL[dtype])
+        env = _row_envelope(args, so_ref, w.Dk * 2.0 ** -24)
+        checked, _ = _divergence_check(r_out.cpu(), so_ref, TOL[dtype], env)
         assert checked > 0
         if dtype == "f32":
-            checked, _ = _divergence_check(c_out.cpu(), so_ref, TOL["f32"])
+            checked, _ = _divergence_check(c_out.cpu(), so_ref, TOL["f32"], env)
         else:
             finite = np.isfinite(so_ref).all(axis=-1) & (norms < 1e30)
             co = c_out.double().cpu().numpy()
             cn = np.linalg.norm(co, axis=-1)
             assert cn[finite].max() > 1e6 * cn[:, :2].max()  # the chunked path diverges too
-            env_ratio, env_agg = _perturbation_envelope(args, norms, 2.0 ** -9)
+            env_ratio, env_agg = _aggregate_envelope(args, so_ref, 2.0 ** -9)
             ratio = np.abs(np.log10(cn[finite] / norms[finite])).max()
             assert ratio <= env_ratio, (ratio, env_ratio)
             err = np.linalg.norm((co - so_ref)[finite]) / np.linalg.norm(so_ref[finite])
