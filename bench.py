@@ -35,7 +35,7 @@ L2_BYTES = 129 * 1024 * 1024
 def parse_args():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="gdn", choices=["gdn", "reference"])
     ap.add_argument("--no-extras", action="store_true", help="skip decode, e2e and cpu baseline legs")
@@ -270,8 +270,9 @@ def run_gdn(args, world, rank, local):
     value = job_tokens_per_s(world, tokens, ms_max)
 
     # per-kernel launch durations: events on the launch stream around every kernel
+    prof_steps = min(args.steps, 50)
     gdn.gdn_profile_enable(True)
-    for _ in range(args.steps):
+    for _ in range(prof_steps):
         step()
     prof = gdn.gdn_profile_read()
     gdn.gdn_profile_enable(False)
@@ -283,7 +284,7 @@ def run_gdn(args, world, rank, local):
     for name, (tms, nl) in prof.items():
         avg = tms / nl
         b, f = work.get(name, (None, None))
-        kernels[name] = {"launches_per_step": nl // args.steps, "avg_ms": round(avg, 4),
+        kernels[name] = {"launches_per_step": nl // prof_steps, "avg_ms": round(avg, 4),
                          "share": round(tms / total, 4)}
         if b:
             kernels[name]["gbs"] = round(b / (avg / 1e3) / 1e9, 1)
@@ -352,7 +353,7 @@ def e2e_leg(args, host, d, step, outputs, world):
         full_step()
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    n = max(3, args.steps // 2)
+    n = max(3, min(50, args.steps // 2))
     barrier(world)
     torch.cuda.synchronize()
     e0.record()
