@@ -180,6 +180,8 @@ def kernel_work(B, T, H, D, es=2):
                                4 * C * C * D * 2),
         "chunk_bwd_finalize_kernel": (C * 4 + 2 * 2 * C * 4 + C * es, 0),
     }
+    per["chunk_scan_fwd_tc_kernel"] = per["chunk_scan_fwd_kernel"]
+    per["chunk_scan_bwd_tc_kernel"] = per["chunk_scan_bwd_kernel"]
     return {k: (b * n, f * n) for k, (b, f) in per.items()}
 
 

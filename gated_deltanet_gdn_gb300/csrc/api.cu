@@ -105,7 +105,8 @@ bool g_prof_failed = false;
 const char* kKernelNames[K_COUNT] = {"chunk_prep_kernel",    "chunk_scan_fwd_kernel",
                                      "chunk_scan_bwd_kernel", "chunk_dstate_kernel",
                                      "chunk_grads_kernel",    "recurrent_kernel",
-                                     "chunk_bwd_finalize_kernel", "chunk_out_kernel"};
+                                     "chunk_bwd_finalize_kernel", "chunk_out_kernel",
+                                     "chunk_scan_fwd_tc_kernel", "chunk_scan_bwd_tc_kernel"};
 
 }  // namespace
 

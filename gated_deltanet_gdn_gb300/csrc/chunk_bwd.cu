@@ -45,8 +45,8 @@ struct RScanLayout {
   static constexpr int GAM = AQK + C * C * ES;     // float [DK]
   static constexpr int DO = a1k(GAM + DK * 4);     // dO slice    [C][NTS]
   static constexpr int STAGE = a1k(DO + C * NTS * ES);
-  static constexpr int DSS = 2 * STAGE;            // dS operand  [DK][NTS] (NT slices)
-  static constexpr int DUS = a1k(DSS + DK * NTS * ES);  // dU     [C][NTS] (NT slices)
+  static constexpr int DSS = 2 * STAGE;            // dS operand, transposed [NTS][DK]
+  static constexpr int DUS = a1k(DSS + DK * NTS * ES);  // dU, transposed  [NTS][C]
   static constexpr int BAR = a1k(DUS + C * NTS * ES);
   static constexpr int BYTES = BAR + 64;
   static constexpr uint32_t TX = (uint32_t)(3 * C * DK * ES + C * C * ES + DK * 4);
@@ -65,8 +65,8 @@ __global__ void __launch_bounds__(RSCAN_THREADS) chunk_scan_bwd_kernel(ChunkBwdA
   const int rg = warp & 3, cg = warp >> 2;
   const int srow = rg * 16 * MTS, col0 = 32 * cg;
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + L::BAR);
-  TTile<T, DK, NTS, NT> dSs{reinterpret_cast<T*>(sm + L::DSS)};
-  TTile<T, C, NTS, NT> dUs{reinterpret_cast<T*>(sm + L::DUS)};
+  Tile<T, NTS, DK> dSs{reinterpret_cast<T*>(sm + L::DSS)};  // dS^T rows of this slice
+  Tile<T, NTS, C> dUs{reinterpret_cast<T*>(sm + L::DUS)};   // dU^T rows of this slice
   const T* dout = static_cast<const T*>(a.dout);
 
   float dS[MTS][4][4];
@@ -129,29 +129,28 @@ __global__ void __launch_bounds__(RSCAN_THREADS) chunk_scan_bwd_kernel(ChunkBwdA
       for (int nt = 0; nt < 4; ++nt)
 #pragma unroll
         for (int e = 0; e < 4; ++e)
-          dSs.at(srow + 16 * mt + frag_row(lane, e), col0 + 8 * nt + frag_col(lane, e)) = from_f32<T>(dS[mt][nt][e]);
+          dSs.at(col0 + 8 * nt + frag_col(lane, e), srow + 16 * mt + frag_row(lane, e)) = from_f32<T>(dS[mt][nt][e]);
     fence_proxy_async();  // read by the bulk store below
     if (more) cp_async_wait<1>(); else cp_async_wait<0>();
     mbar_wait(&bars[s], par, a.err);
     __syncthreads();
     if (tid == 0) {  // gradient of the state leaving chunk n
-      bulk_s2g(static_cast<T*>(a.ws.dstate) + (ch * NTILE + tile * (NTS / NT)) * (DK * NT), dSs.p,
-               DK * NTS * 2);
+      store_row_block<T, DV, DK>(static_cast<T*>(a.ws.dstate) + ch * (DK * DV), dSs.p, tile * NTS, NTS);
       bulk_commit();
     }
     float du[1][4][4];
     zero(du);
     Gemm<T>::template runk<1, 4, 0, C>(du, aview<true>(At), bview<true>(dOt), 16 * rg, col0, lane);
-    Gemm<T>::template runk<1, 4, 0, DK>(du, aview<false>(Kt), bview<true>(dSs), 16 * rg, col0, lane);
+    Gemm<T>::template runk<1, 4, 0, DK>(du, aview<false>(Kt), bview<false>(dSs), 16 * rg, col0, lane);
 #pragma unroll
     for (int nt = 0; nt < 4; ++nt)
 #pragma unroll
       for (int e = 0; e < 4; ++e)
-        dUs.at(16 * rg + frag_row(lane, e), col0 + 8 * nt + frag_col(lane, e)) = from_f32<T>(du[0][nt][e]);
+        dUs.at(col0 + 8 * nt + frag_col(lane, e), 16 * rg + frag_row(lane, e)) = from_f32<T>(du[0][nt][e]);
     fence_proxy_async();
     __syncthreads();
     if (tid == 0) {
-      bulk_s2g(static_cast<T*>(a.ws.du) + (ch * NTILE + tile * (NTS / NT)) * (C * NT), dUs.p, C * NTS * 2);
+      store_row_block<T, DV, C>(static_cast<T*>(a.ws.du) + ch * (C * DV), dUs.p, tile * NTS, NTS);
       bulk_commit();
     }
 #pragma unroll
@@ -161,7 +160,7 @@ __global__ void __launch_bounds__(RSCAN_THREADS) chunk_scan_bwd_kernel(ChunkBwdA
 #pragma unroll
         for (int e = 0; e < 4; ++e) dS[mt][nt][e] *= gam[srow + 16 * mt + frag_row(lane, e)];
     Gemm<T>::template runk<MTS, 4, 0, C>(dS, aview<true>(Qt), bview<true>(dOt), srow, col0, lane);
-    Gemm<T>::template runk<MTS, 4, 0, C>(dS, aview<true>(Wt), bview<true>(dUs), srow, col0, lane);
+    Gemm<T>::template runk<MTS, 4, 0, C>(dS, aview<true>(Wt), bview<false>(dUs), srow, col0, lane);
     if (tid == 0) bulk_wait_read0();  // the bulk stores have read dSs and dUs before they are rewritten
     __syncthreads();
   }
@@ -190,10 +189,10 @@ struct DstLayout {
   static constexpr int TM = 0;                       // T    [C][C]
   static constexpr int DO = a1k(TM + C * C * 2);     // dO   [C][DV]
   static constexpr int V = a1k(DO + C * DV * 2);     // v    [C][DV]
-  static constexpr int U = a1k(V + C * DV * 2);      // U    [C][DV] (NT slices)
-  static constexpr int DU = a1k(U + C * DV * 2);     // dU   [C][DV] (NT slices), then Y
-  static constexpr int S0 = a1k(DU + C * DV * 2);    // S0   [DK][DV] (NT slices)
-  static constexpr int DS1 = a1k(S0 + DK * DV * 2);  // dS1  [DK][DV] (NT slices)
+  static constexpr int U = a1k(V + C * DV * 2);      // U^T   [DV][C]
+  static constexpr int DU = a1k(U + C * DV * 2);     // dU^T  [DV][C], then Y [C][DV]
+  static constexpr int S0 = a1k(DU + C * DV * 2);    // S0^T  [DV][DK]
+  static constexpr int DS1 = a1k(S0 + DK * DV * 2);  // dS1^T [DV][DK]
   static constexpr int BETA = a1k(DS1 + DK * DV * 2);
   static constexpr int DB = BETA + C * 4;            // float [2][C]
   static constexpr int BYTES = DB + 2 * C * 4;
@@ -213,10 +212,10 @@ __global__ void __launch_bounds__(DST_THREADS) chunk_dstate_kernel(ChunkBwdArgs 
   Tile<T, C, C> Ts{reinterpret_cast<T*>(sm + L::TM)};
   Tile<T, C, DV> dOs{reinterpret_cast<T*>(sm + L::DO)};
   Tile<T, C, DV> Vs{reinterpret_cast<T*>(sm + L::V)};
-  TTile<T, C, DV, NT> Us{reinterpret_cast<T*>(sm + L::U)};
-  TTile<T, C, DV, NT> dUs{reinterpret_cast<T*>(sm + L::DU)};
-  TTile<T, DK, DV, NT> S0s{reinterpret_cast<T*>(sm + L::S0)};
-  TTile<T, DK, DV, NT> dS1s{reinterpret_cast<T*>(sm + L::DS1)};
+  Tile<T, DV, C> Us{reinterpret_cast<T*>(sm + L::U)};       // U^T
+  Tile<T, DV, C> dUs{reinterpret_cast<T*>(sm + L::DU)};      // dU^T
+  Tile<T, DV, DK> S0s{reinterpret_cast<T*>(sm + L::S0)};     // S0^T
+  Tile<T, DV, DK> dS1s{reinterpret_cast<T*>(sm + L::DS1)};   // dS1^T
   float* beta_s = reinterpret_cast<float*>(sm + L::BETA);
   float* db_s = reinterpret_cast<float*>(sm + L::DB);
   const T* dout = static_cast<const T*>(a.dout);
@@ -254,7 +253,7 @@ __global__ void __launch_bounds__(DST_THREADS) chunk_dstate_kernel(ChunkBwdArgs 
   constexpr int NWV = DV / 16;
   float y[1][NWV][4];
   zero(y);
-  Gemm<T>::template runk<1, NWV, 0, C>(y, aview<true>(Ts), bview<true>(dUs), m0, hf * (DV / 2), lane);
+  Gemm<T>::template runk<1, NWV, 0, C>(y, aview<true>(Ts), bview<false>(dUs), m0, hf * (DV / 2), lane);
   {
     float db[2] = {0.f, 0.f};
     T* dv = static_cast<T*>(a.dv);
@@ -284,15 +283,16 @@ __global__ void __launch_bounds__(DST_THREADS) chunk_dstate_kernel(ChunkBwdArgs 
     for (int e = 0; e < 4; ++e)
       Ys.at(m0 + frag_row(lane, e), hf * (DV / 2) + 8 * nt + frag_col(lane, e)) = from_f32<T>(y[0][nt][e]);
   if (tid < C) a.ws.dbv[ch * C + tid] = db_s[tid] + db_s[C + tid];
-  for (int c = tid; c < DK; c += DST_THREADS) {  // dgam_c = sum_v dS1[c][v] S0[c][v]
-    float acc = 0.f;
-    for (int v2 = 0; v2 < DV; v2 += 2) {
-      const __nv_bfloat162 x = *reinterpret_cast<const __nv_bfloat162*>(dS1s.ptr(c, v2));
-      const __nv_bfloat162 z = *reinterpret_cast<const __nv_bfloat162*>(S0s.ptr(c, v2));
-      acc = fmaf(__low2float(x), __low2float(z), acc);
-      acc = fmaf(__high2float(x), __high2float(z), acc);
+  for (int c = 2 * tid; c < DK; c += 2 * DST_THREADS) {  // dgam_c = sum_v dS1[c][v] S0[c][v]
+    float acc0 = 0.f, acc1 = 0.f;
+    for (int v2 = 0; v2 < DV; ++v2) {
+      const __nv_bfloat162 x = *reinterpret_cast<const __nv_bfloat162*>(dS1s.ptr(v2, c));
+      const __nv_bfloat162 z = *reinterpret_cast<const __nv_bfloat162*>(S0s.ptr(v2, c));
+      acc0 = fmaf(__low2float(x), __low2float(z), acc0);
+      acc1 = fmaf(__high2float(x), __high2float(z), acc1);
     }
-    a.ws.dgam[ch * DK + c] = acc;
+    a.ws.dgam[ch * DK + c] = acc0;
+    a.ws.dgam[ch * DK + c + 1] = acc1;
   }
   __syncthreads();
 
@@ -312,13 +312,13 @@ __global__ void __launch_bounds__(DST_THREADS) chunk_dstate_kernel(ChunkBwdArgs 
   {
     float acc[1][NH][4];
     zero(acc);
-    Gemm<T>::template runk<1, NH, 0, DV>(acc, aview<false>(dOs), bview<false>(S0s), m0, n0, lane);
+    Gemm<T>::template runk<1, NH, 0, DV>(acc, aview<false>(dOs), bview<true>(S0s), m0, n0, lane);
     store_cdk(a.ws.dqh, acc, a.scale);
     zero(acc);
-    Gemm<T>::template runk<1, NH, 0, DV>(acc, aview<false>(Ys), bview<false>(S0s), m0, n0, lane);
+    Gemm<T>::template runk<1, NH, 0, DV>(acc, aview<false>(Ys), bview<true>(S0s), m0, n0, lane);
     store_cdk(a.ws.dbk, acc, -1.f);
     zero(acc);
-    Gemm<T>::template runk<1, NH, 0, DV>(acc, aview<false>(Us), bview<false>(dS1s), m0, n0, lane);
+    Gemm<T>::template runk<1, NH, 0, DV>(acc, aview<true>(Us), bview<true>(dS1s), m0, n0, lane);
     store_cdk(a.ws.dkt, acc, 1.f);
   }
   // C x C products: warp rows m0, columns 32 hf .. +31 (block-1 rows see no block-2 columns)
@@ -329,8 +329,8 @@ __global__ void __launch_bounds__(DST_THREADS) chunk_dstate_kernel(ChunkBwdArgs 
     zero(aq);
     zero(ak);
     if (!dead) {
-      Gemm<T>::template runk<1, 4, 0, DV>(aq, aview<false>(dOs), bview<false>(Us), m0, c0, lane);
-      Gemm<T>::template runk<1, 4, 0, DV>(ak, aview<false>(Ys), bview<false>(Us), m0, c0, lane);
+      Gemm<T>::template runk<1, 4, 0, DV>(aq, aview<false>(dOs), bview<true>(Us), m0, c0, lane);
+      Gemm<T>::template runk<1, 4, 0, DV>(ak, aview<false>(Ys), bview<true>(Us), m0, c0, lane);
     }
     T* da = static_cast<T*>(a.ws.daqk) + ch * (C * C);
     T* dk = static_cast<T*>(a.ws.dakk) + ch * (C * C);
@@ -350,7 +350,9 @@ template <int DK, int DV>
 cudaError_t launch_bwd_t(const ChunkBwdArgs& a, cudaStream_t s) {
   const int N = a.T / C, BH = a.B * a.H;
   cudaError_t e;
-  {
+  if (scan_tc_applies(1, DK, DV)) {
+    if ((e = launch_scan_bwd_tc(a, s)) != cudaSuccess) return e;
+  } else {
     const int bytes = RScanLayout<DK>::BYTES + 1024;
     auto kern = chunk_scan_bwd_kernel<DK, DV>;
     if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes)) != cudaSuccess) return e;

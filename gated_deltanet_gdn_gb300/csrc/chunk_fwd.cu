@@ -375,7 +375,7 @@ __global__ void __launch_bounds__(PREP_THREADS) chunk_prep_kernel(ChunkFwdArgs a
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         const int r = m0 + frag_row(lane, e), c = hf * (DV / 2) + 8 * nt + frag_col(lane, e);
-        ust[(c / NT) * (C * NT) + Sw<T, C, NT>::off(r, c % NT)] = from_f32<T>(accu[0][nt][e]);
+        ust[Sw<T, C, DV>::off(r, c)] = from_f32<T>(accu[0][nt][e]);
       }
   }
   __syncthreads();
@@ -398,19 +398,21 @@ struct ScanLayout {
   static constexpr int ES = (int)sizeof(T);
   static constexpr int W = 0;                        // -W        [C][DK]
   static constexpr int KT = W + C * DK * ES;         // K-tilde   [C][DK]
-  static constexpr int UP = KT + C * DK * ES;        // U' slices [C][NTS]
+  static constexpr int UP = KT + C * DK * ES;        // U' columns of this slice [C][NTS]
   static constexpr int GAM = UP + C * NTS * ES;      // float [DK]
   static constexpr int STAGE = a1k(GAM + DK * 4);
   static constexpr int STAGES = ES == 2 ? 4 : 1;
-  static constexpr int SS = STAGES * STAGE;          // state operand [DK][NTS] (NT slices)
-  static constexpr int US = a1k(SS + DK * NTS * ES); // U [C][NTS] (NT slices)
+  static constexpr int SS = STAGES * STAGE;          // state operand, transposed [NTS][DK]
+  static constexpr int US = a1k(SS + DK * NTS * ES); // U, transposed [NTS][C]
   static constexpr int BAR = a1k(US + C * NTS * ES);
   static constexpr int BYTES = BAR + 64;
   static constexpr uint32_t TX = (uint32_t)(2 * C * DK * ES + C * NTS * ES + DK * 4);
 };
 
 // One CTA per (batch*head, NTS = 64 value columns), 8 warps. Warp w owns state rows
-// (w & 3) * Dk/4 .. + Dk/4 and columns 32 (w >> 2) .. + 31 of the slice.
+// (w & 3) * Dk/4 .. + Dk/4 and columns 32 (w >> 2) .. + 31 of the slice. The state and U
+// records are stored transposed (value rows): S^T [Dv][Dk] and U^T [Dv][C]; this CTA
+// writes their rows tile * NTS .. + NTS - 1.
 template <class T, int DK, int DV>
 __global__ void __launch_bounds__(SCAN_THREADS) chunk_scan_fwd_kernel(ChunkFwdArgs a) {
   typedef ScanLayout<T, DK> L;
@@ -419,14 +421,13 @@ __global__ void __launch_bounds__(SCAN_THREADS) chunk_scan_fwd_kernel(ChunkFwdAr
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int tile = blockIdx.x, bh = blockIdx.y;
   const int N = a.T / C;
-  constexpr int NTILE = DV / NT;  // NT-column record slices per row
   constexpr int MTS = DK / 64;    // m16 tiles of state rows per warp
   constexpr int EPC = 16 / (int)sizeof(T);
   const int rg = warp & 3, cg = warp >> 2;
   const int srow = rg * 16 * MTS, col0 = 32 * cg;
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + L::BAR);
-  TTile<T, DK, NTS, NT> Ss{reinterpret_cast<T*>(sm + L::SS)};
-  TTile<T, C, NTS, NT> Us{reinterpret_cast<T*>(sm + L::US)};
+  Tile<T, NTS, DK> Ss{reinterpret_cast<T*>(sm + L::SS)};  // S^T rows of this slice
+  Tile<T, NTS, C> Us{reinterpret_cast<T*>(sm + L::US)};   // U^T rows of this slice
 
   float S[MTS][4][4];
   const size_t sb = (size_t)bh * DK * DV;
@@ -454,7 +455,7 @@ __global__ void __launch_bounds__(SCAN_THREADS) chunk_scan_fwd_kernel(ChunkFwdAr
     mbar_arrive_expect_tx(&bars[s], L::TX);
     bulk_g2s(st + L::W, static_cast<const T*>(a.res.wneg) + ch * (C * DK), C * DK * sizeof(T), &bars[s]);
     bulk_g2s(st + L::KT, static_cast<const T*>(a.res.kt) + ch * (C * DK), C * DK * sizeof(T), &bars[s]);
-    bulk_g2s(st + L::UP, static_cast<const T*>(a.res.up) + (ch * NTILE + tile * (NTS / NT)) * (C * NT),
+    bulk_g2s(st + L::UP, static_cast<const T*>(a.res.up) + ch * (C * DV) + tile * (C * NTS),
              C * NTS * sizeof(T), &bars[s]);
     bulk_g2s(st + L::GAM, a.res.gam + ch * DK, DK * 4, &bars[s]);
   };
@@ -469,7 +470,7 @@ __global__ void __launch_bounds__(SCAN_THREADS) chunk_scan_fwd_kernel(ChunkFwdAr
     uint8_t* st = sm + s * L::STAGE;
     Tile<T, C, DK> Wt{reinterpret_cast<T*>(st + L::W)};
     Tile<T, C, DK> Kt{reinterpret_cast<T*>(st + L::KT)};
-    TTile<T, C, NTS, NT> Up{reinterpret_cast<T*>(st + L::UP)};
+    Tile<T, C, NTS> Up{reinterpret_cast<T*>(st + L::UP)};  // this slice's panels of the U' tile
     const float* gam = reinterpret_cast<const float*>(st + L::GAM);
     const size_t ch = (size_t)bh * N + n;
 
@@ -479,29 +480,28 @@ __global__ void __launch_bounds__(SCAN_THREADS) chunk_scan_fwd_kernel(ChunkFwdAr
       for (int nt = 0; nt < 4; ++nt)
 #pragma unroll
         for (int e = 0; e < 4; ++e)
-          Ss.at(srow + 16 * mt + frag_row(lane, e), col0 + 8 * nt + frag_col(lane, e)) = from_f32<T>(S[mt][nt][e]);
+          Ss.at(col0 + 8 * nt + frag_col(lane, e), srow + 16 * mt + frag_row(lane, e)) = from_f32<T>(S[mt][nt][e]);
     fence_proxy_async();  // the state copy is read by the bulk store below
     mbar_wait(&bars[s], par, a.err);
     __syncthreads();
-    if (tid == 0) {  // residual: chunk-start state (this CTA's two record slices are adjacent)
-      bulk_s2g(static_cast<T*>(a.res.state) + (ch * NTILE + tile * (NTS / NT)) * (DK * NT), Ss.p,
-               DK * NTS * sizeof(T));
+    if (tid == 0) {  // residual: chunk-start state
+      store_row_block<T, DV, DK>(static_cast<T*>(a.res.state) + ch * (DK * DV), Ss.p, tile * NTS, NTS);
       bulk_commit();
     }
     float ws[1][4][4];
     zero(ws);
-    Gemm<T>::template runk<1, 4, 0, DK>(ws, aview<false>(Wt), bview<true>(Ss), 16 * rg, col0, lane);
+    Gemm<T>::template runk<1, 4, 0, DK>(ws, aview<false>(Wt), bview<false>(Ss), 16 * rg, col0, lane);
 #pragma unroll
     for (int nt = 0; nt < 4; ++nt)
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         const int r = 16 * rg + frag_row(lane, e), c = col0 + 8 * nt + frag_col(lane, e);
-        Us.at(r, c) = from_f32<T>(to_f32(Up.at(r, c)) + ws[0][nt][e]);
+        Us.at(c, r) = from_f32<T>(to_f32(Up.at(r, c)) + ws[0][nt][e]);
       }
     fence_proxy_async();
     __syncthreads();
     if (tid == 0) {  // residual: U
-      bulk_s2g(static_cast<T*>(a.res.u) + (ch * NTILE + tile * (NTS / NT)) * (C * NT), Us.p, C * NTS * sizeof(T));
+      store_row_block<T, DV, C>(static_cast<T*>(a.res.u) + ch * (C * DV), Us.p, tile * NTS, NTS);
       bulk_commit();
     }
 #pragma unroll
@@ -510,7 +510,7 @@ __global__ void __launch_bounds__(SCAN_THREADS) chunk_scan_fwd_kernel(ChunkFwdAr
       for (int nt = 0; nt < 4; ++nt)
 #pragma unroll
         for (int e = 0; e < 4; ++e) S[mt][nt][e] *= gam[srow + 16 * mt + frag_row(lane, e)];
-    Gemm<T>::template runk<MTS, 4, 0, C>(S, aview<true>(Kt), bview<true>(Us), srow, col0, lane);
+    Gemm<T>::template runk<MTS, 4, 0, C>(S, aview<true>(Kt), bview<false>(Us), srow, col0, lane);
     if (tid == 0) bulk_wait_read0();  // the bulk stores have read Ss and Us before they are rewritten
     __syncthreads();
   }
@@ -538,8 +538,8 @@ struct OutLayout {
   static constexpr int ES = (int)sizeof(T);
   static constexpr int QH = 0;                         // [C][DK]
   static constexpr int AQ = a1k(QH + C * DK * ES);     // [C][C]
-  static constexpr int S0 = a1k(AQ + C * C * ES);      // [DK][DV] (NT slices)
-  static constexpr int U = a1k(S0 + DK * DV * ES);     // [C][DV] (NT slices), then the output tile
+  static constexpr int S0 = a1k(AQ + C * C * ES);      // S0^T [DV][DK]
+  static constexpr int U = a1k(S0 + DK * DV * ES);     // U^T [DV][C], then the output tile
   static constexpr int BYTES = a1k(U + C * DV * ES);
 };
 
@@ -555,8 +555,8 @@ __global__ void __launch_bounds__(OUT_THREADS) chunk_out_kernel(ChunkFwdArgs a) 
   constexpr int EPC = 16 / (int)sizeof(T);
   Tile<T, C, DK> Qs{reinterpret_cast<T*>(sm + L::QH)};
   Tile<T, C, C> As{reinterpret_cast<T*>(sm + L::AQ)};
-  TTile<T, DK, DV, NT> S0s{reinterpret_cast<T*>(sm + L::S0)};
-  TTile<T, C, DV, NT> Us{reinterpret_cast<T*>(sm + L::U)};
+  Tile<T, DV, DK> S0s{reinterpret_cast<T*>(sm + L::S0)};
+  Tile<T, DV, C> Us{reinterpret_cast<T*>(sm + L::U)};
   {
     const T* s1 = static_cast<const T*>(a.res.qh) + ch * (C * DK);
     for (int i = tid; i < C * DK / EPC; i += OUT_THREADS) cp_async16(Qs.p + i * EPC, s1 + i * EPC);
@@ -574,8 +574,8 @@ __global__ void __launch_bounds__(OUT_THREADS) chunk_out_kernel(ChunkFwdArgs a) 
   constexpr int NW = DV / 16;
   float o[1][NW][4];
   zero(o);
-  Gemm<T>::template runk<1, NW, 0, DK>(o, aview<false>(Qs), bview<true>(S0s), m0, n0, lane);
-  Gemm<T>::template runk<1, NW, 0, C>(o, aview<false>(As), bview<true>(Us), m0, n0, lane);
+  Gemm<T>::template runk<1, NW, 0, DK>(o, aview<false>(Qs), bview<false>(S0s), m0, n0, lane);
+  Gemm<T>::template runk<1, NW, 0, C>(o, aview<false>(As), bview<false>(Us), m0, n0, lane);
   __syncthreads();  // U consumed: stage the output tile in its place
   Tile<T, C, DV> Os{reinterpret_cast<T*>(sm + L::U)};
 #pragma unroll
@@ -609,7 +609,9 @@ cudaError_t launch_fwd_t(const ChunkFwdArgs& a, cudaStream_t s) {
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
-  {
+  if (scan_tc_applies(a.bf16, DK, DV)) {
+    if ((e = launch_scan_fwd_tc(a, s)) != cudaSuccess) return e;
+  } else {
     const int bytes = ScanLayout<T, DK>::BYTES + 1024;
     auto kern = chunk_scan_fwd_kernel<T, DK, DV>;
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);

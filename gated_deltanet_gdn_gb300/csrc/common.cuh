@@ -356,6 +356,19 @@ __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.comm
 __device__ __forceinline__ void bulk_wait_read0() {
   asm volatile("cp.async.bulk.wait_group.read 0;\n" ::: "memory");
 }
+
+// Copies rows row0 .. row0 + rows - 1 of a swizzled ROWS x COLS record tile held in
+// shared memory as its own rows x COLS tile (row0 a multiple of 8, so the swizzle
+// phase of every row is the same in both) to the record in global memory: one bulk
+// copy per column panel. Issued by one thread.
+template <class T, int ROWS, int COLS>
+__device__ __forceinline__ void store_row_block(T* rec, const T* tile, int row0, int rows) {
+  constexpr int PW = Sw<T, ROWS, COLS>::PW;
+  for (int p = 0; p < COLS / PW; ++p)
+    bulk_s2g(rec + (size_t)p * ROWS * PW + (size_t)row0 * PW, tile + (size_t)p * rows * PW,
+             (uint32_t)(rows * PW * sizeof(T)));
+}
+
 __device__ __forceinline__ void bulk_wait0() { asm volatile("cp.async.bulk.wait_group 0;\n" ::: "memory"); }
 
 __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {

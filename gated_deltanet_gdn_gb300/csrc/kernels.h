@@ -9,12 +9,16 @@ namespace gdn {
 
 constexpr int C = 64;       // chunk length (tokens)
 constexpr int BLK = 32;     // block length inside a chunk
-constexpr int NT = 32;      // value columns per record slice (state, U, U', dU, dS records)
+constexpr int NT = 32;      // value columns per warp column group of the mma.sync scans
 constexpr int NTS = 64;     // value columns per state-scan CTA (two record slices)
 constexpr float SAFE_SPREAD = 80.f;  // max decay spread (nats) for row-scaled in-block scores
 
 // Per (batch, head) and chunk, the forward writes these records. Byte sizes of one record
 // for operand element size es; every record starts 1024-byte aligned inside its region.
+// Each record is a swizzled tile (Sw in common.cuh): Aqk, T [C][C]; -W, Q-hat, K-tilde
+// [C][Dk]; U' [C][Dv]; the chunk-start state and U transposed,
+// S^T [Dv][Dk] and U^T [Dv][C]. The backward's dS and dU records are likewise
+// dS^T [Dv][Dk] and dU^T [Dv][C].
 struct ResidualLayout {
   // region base offsets in bytes from the residual pointer
   size_t aqk, tmat, wneg, up, qh, kt, gam, state, u, total;
@@ -147,7 +151,9 @@ enum KernelId {
   K_RECURRENT = 5, // recurrent_kernel
   K_FINALIZE = 6,  // chunk_bwd_finalize_kernel
   K_OUT = 7,       // chunk_out_kernel
-  K_COUNT = 8
+  K_SCAN_FWD_TC = 8,  // chunk_scan_fwd_tc_kernel
+  K_SCAN_BWD_TC = 9,  // chunk_scan_bwd_tc_kernel
+  K_COUNT = 10
 };
 // Records a CUDA event on s before (begin = true) or after a launch when timing is on.
 void prof_mark(KernelId id, cudaStream_t s, bool begin);
@@ -157,5 +163,9 @@ cudaError_t launch_chunk_fwd(const ChunkFwdArgs& a, cudaStream_t s);
 cudaError_t launch_chunk_bwd(const ChunkBwdArgs& a, cudaStream_t s);
 cudaError_t launch_recurrent(const RecurrentArgs& a, cudaStream_t s);
 cudaError_t launch_chunk_grads(const ChunkBwdArgs& a, cudaStream_t s);  // part of launch_chunk_bwd
+// The tensor-core (tcgen05) state scans, used when scan_tc_applies(bf16, Dk, Dv).
+bool scan_tc_applies(int bf16_operands, int DK, int DV);
+cudaError_t launch_scan_fwd_tc(const ChunkFwdArgs& a, cudaStream_t s);
+cudaError_t launch_scan_bwd_tc(const ChunkBwdArgs& a, cudaStream_t s);
 
 }  // namespace gdn

@@ -190,7 +190,9 @@ int gdn_version(void);
  * record and returns GDN_OK (GDN_ERR_CUDA if an event failed). Kernel ids:
  * 0 chunk preparation, 1 forward state scan, 2 reverse state scan, 3 state
  * products, 4 chunk gradients, 5 recurrent, 6 backward finalisation,
- * 7 chunk outputs;
+ * 7 chunk outputs, 8 forward state scan on tcgen05 tensor cores, 9 reverse
+ * state scan on tcgen05 tensor cores (8 and 9 replace 1 and 2 for bf16
+ * operands with Dk = Dv = 128);
  * gdn_kernel_name(id) names them
  * ("" for an unknown id). Not part of the paper's method: instrumentation. */
 int gdn_profile_enable(int on);
