@@ -375,7 +375,7 @@ __global__ void __launch_bounds__(PREP_THREADS) chunk_prep_kernel(ChunkFwdArgs a
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         const int r = m0 + frag_row(lane, e), c = hf * (DV / 2) + 8 * nt + frag_col(lane, e);
-        ust[Sw<T, C, DV>::off(r, c)] = from_f32<T>(accu[0][nt][e]);
+        ust[Sw<T, DV, C>::off(c, r)] = from_f32<T>(accu[0][nt][e]);  // U'^T [Dv][C]
       }
   }
   __syncthreads();
@@ -398,7 +398,7 @@ struct ScanLayout {
   static constexpr int ES = (int)sizeof(T);
   static constexpr int W = 0;                        // -W        [C][DK]
   static constexpr int KT = W + C * DK * ES;         // K-tilde   [C][DK]
-  static constexpr int UP = KT + C * DK * ES;        // U' columns of this slice [C][NTS]
+  static constexpr int UP = KT + C * DK * ES;        // U'^T rows of this slice [NTS][C]
   static constexpr int GAM = UP + C * NTS * ES;      // float [DK]
   static constexpr int STAGE = a1k(GAM + DK * 4);
   static constexpr int STAGES = ES == 2 ? 4 : 1;
@@ -455,8 +455,13 @@ __global__ void __launch_bounds__(SCAN_THREADS) chunk_scan_fwd_kernel(ChunkFwdAr
     mbar_arrive_expect_tx(&bars[s], L::TX);
     bulk_g2s(st + L::W, static_cast<const T*>(a.res.wneg) + ch * (C * DK), C * DK * sizeof(T), &bars[s]);
     bulk_g2s(st + L::KT, static_cast<const T*>(a.res.kt) + ch * (C * DK), C * DK * sizeof(T), &bars[s]);
-    bulk_g2s(st + L::UP, static_cast<const T*>(a.res.up) + ch * (C * DV) + tile * (C * NTS),
-             C * NTS * sizeof(T), &bars[s]);
+    {  // rows tile * NTS .. + NTS - 1 of U'^T: one piece per column panel
+      constexpr int PW = Sw<T, DV, C>::PW;
+      const T* src = static_cast<const T*>(a.res.up) + ch * (C * DV);
+      for (int p = 0; p < C / PW; ++p)
+        bulk_g2s(st + L::UP + p * NTS * PW * sizeof(T), src + (size_t)p * DV * PW + (size_t)tile * NTS * PW,
+                 NTS * PW * sizeof(T), &bars[s]);
+    }
     bulk_g2s(st + L::GAM, a.res.gam + ch * DK, DK * 4, &bars[s]);
   };
   if (tid == 0)
@@ -470,7 +475,7 @@ __global__ void __launch_bounds__(SCAN_THREADS) chunk_scan_fwd_kernel(ChunkFwdAr
     uint8_t* st = sm + s * L::STAGE;
     Tile<T, C, DK> Wt{reinterpret_cast<T*>(st + L::W)};
     Tile<T, C, DK> Kt{reinterpret_cast<T*>(st + L::KT)};
-    Tile<T, C, NTS> Up{reinterpret_cast<T*>(st + L::UP)};  // this slice's panels of the U' tile
+    Tile<T, NTS, C> Up{reinterpret_cast<T*>(st + L::UP)};  // this slice's rows of U'^T
     const float* gam = reinterpret_cast<const float*>(st + L::GAM);
     const size_t ch = (size_t)bh * N + n;
 
@@ -496,7 +501,7 @@ __global__ void __launch_bounds__(SCAN_THREADS) chunk_scan_fwd_kernel(ChunkFwdAr
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         const int r = 16 * rg + frag_row(lane, e), c = col0 + 8 * nt + frag_col(lane, e);
-        Us.at(c, r) = from_f32<T>(to_f32(Up.at(r, c)) + ws[0][nt][e]);
+        Us.at(c, r) = from_f32<T>(to_f32(Up.at(c, r)) + ws[0][nt][e]);
       }
     fence_proxy_async();
     __syncthreads();

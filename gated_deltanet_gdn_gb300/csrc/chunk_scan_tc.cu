@@ -17,10 +17,10 @@
 // TMA tensor load for dO) as soon as the tensor cores release a stage. Thread 0 issues
 // every tcgen05.mma (bf16 x bf16 -> fp32 in TMEM) on 128-byte swizzled tiles: the
 // records exactly as the preparation kernel stored them (K-major or MN-major operands,
-// no transposition) and the bf16 copies of S^T / U^T the compute warps write from TMEM,
-// which are also the chunk-start state and U records the later kernels read. U' enters
-// the forward accumulator through a product with the identity. Every wait is bounded
-// and sets the device error word.
+// no transposition) and the bf16 copies of S^T / U^T the compute warps write from TMEM
+// (double-buffered), which bulk copies also store as the chunk-start state and U records
+// the later kernels read. The compute warps add U' to the forward's U^T. Every wait is
+// bounded and sets the device error word.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -130,14 +130,13 @@ __device__ __forceinline__ void umma_commit_to(uint64_t* bar) { umma_commit(bar)
 struct TcFwdLayout {
   static constexpr int W = 0;                    // -W      [C][Dk]  (K-major B of U^T)
   static constexpr int KT = W + C * TD * 2;      // K-tilde [C][Dk]  (MN-major B of S^T)
-  static constexpr int UP = KT + C * TD * 2;     // U'      [C][Dv]  (MN-major A of U^T)
+  static constexpr int UP = KT + C * TD * 2;     // U'^T    [Dv][C]  (added by the threads)
   static constexpr int GAM = UP + C * TD * 2;    // gam     [Dk] fp32
   static constexpr int STAGE = a1k(GAM + TD * 4);
-  static constexpr int STAGES = 3;
-  static constexpr int SA = STAGES * STAGE;      // S^T bf16 [Dv][Dk]
-  static constexpr int UA = SA + TD * TD * 2;    // U^T bf16 [Dv][C]
-  static constexpr int ID = UA + TD * C * 2;     // identity [C][C] (K-major B)
-  static constexpr int BAR = ID + C * C * 2;     // full[STAGES], empty[STAGES], u, s
+  static constexpr int STAGES = 2;
+  static constexpr int SA = STAGES * STAGE;        // S^T bf16 [Dv][Dk], two buffers
+  static constexpr int UA = SA + 2 * TD * TD * 2;  // U^T bf16 [Dv][C], two buffers
+  static constexpr int BAR = UA + 2 * TD * C * 2;  // full[STAGES], empty[STAGES], u, s
   static constexpr int TSLOT = BAR + 8 * (2 * STAGES + 2);
   static constexpr int BYTES = TSLOT + 16;
   static constexpr uint32_t TX = (uint32_t)(3 * C * TD * 2 + TD * 4);
@@ -155,9 +154,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_scan_fwd_tc_kernel(ChunkF
   uint64_t* bar_u = empty + L::STAGES;
   uint64_t* bar_s = bar_u + 1;
   uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + L::TSLOT);
-  Tile<bf16, TD, TD> Sa{reinterpret_cast<bf16*>(sm + L::SA)};
-  Tile<bf16, TD, C> Ua{reinterpret_cast<bf16*>(sm + L::UA)};
-  Tile<bf16, C, C> Id{reinterpret_cast<bf16*>(sm + L::ID)};
+  bf16* const sa_buf = reinterpret_cast<bf16*>(sm + L::SA);
+  bf16* const ua_buf = reinterpret_cast<bf16*>(sm + L::UA);
 
   if (tid == 0) {
     for (int s = 0; s < L::STAGES; ++s) {
@@ -172,8 +170,6 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_scan_fwd_tc_kernel(ChunkF
     tmem_alloc(tslot, TMEM_COLS);
     tmem_relinquish();
   }
-  for (int i = tid; i < C * C; i += TC_THREADS) Id.at(i / C, i % C) = __float2bfloat16(i / C == i % C ? 1.f : 0.f);
-  fence_proxy_async();
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -210,15 +206,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_scan_fwd_tc_kernel(ChunkF
     tmem_st32(tl + 64 * half + 32, hi);
     tmem_wait_st();
   }
-  uint64_t dSa = 0, dUa = 0, dId = 0;
-  constexpr uint32_t id_u = umma_idesc_bf16(128, C, true, false);   // U'^T I
   constexpr uint32_t id_1 = umma_idesc_bf16(128, C, false, false);  // S^T (-W)^T
   constexpr uint32_t id_2 = umma_idesc_bf16(128, TD, false, true);  // U^T K-tilde
-  if (tid == 0) {
-    dSa = desc_k(Sa.p);
-    dUa = desc_k(Ua.p);
-    dId = desc_k(Id.p);
-  }
   bf16* state_rec = static_cast<bf16*>(a.res.state);
   bf16* u_rec = static_cast<bf16*>(a.res.u);
   uint32_t ph_u = 0, ph_s = 0;
@@ -227,6 +216,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_scan_fwd_tc_kernel(ChunkF
     const int s = n % L::STAGES;
     uint8_t* st = sm + s * L::STAGE;
     const size_t ch = (size_t)bh * N + n;
+    Tile<bf16, TD, TD> Sa{sa_buf + (n & 1) * (TD * TD)};
+    Tile<bf16, TD, C> Ua{ua_buf + (n & 1) * (TD * C)};
     if (n > 0) {  // the previous chunk's S^T update is done
       mbar_wait(bar_s, ph_s, a.err);
       ph_s ^= 1u;
@@ -237,37 +228,47 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_scan_fwd_tc_kernel(ChunkF
     state_slice_out(tl + 64 * half, Sa, row, 64 * half, reinterpret_cast<const float*>(st + L::GAM));
     fence_proxy_async();
     tc_fence_before();
-    if (tid == 0) bulk_wait_read0();  // the previous U record store has read Ua
     compute_sync();
     if (tid == 0) {
       tc_fence_after();
       bulk_s2g(state_rec + ch * (TD * TD), Sa.p, TD * TD * 2);
       bulk_commit();
-      const uint64_t dUp = desc_mn(st + L::UP, PANEL_C), dW = desc_k(st + L::W);
-#pragma unroll
-      for (int ks = 0; ks < C / 16; ++ks) umma_bf16(tm + 128, kstep_mn(dUp, ks), kstep_k(dId, ks, 0), id_u, ks > 0);
+      const uint64_t dW = desc_k(st + L::W), dSa = desc_k(Sa.p);
 #pragma unroll
       for (int ks = 0; ks < TD / 16; ++ks)
-        umma_bf16(tm + 128, kstep_k(dSa, ks, PANEL_D), kstep_k(dW, ks, PANEL_C), id_1, 1u);
+        umma_bf16(tm + 128, kstep_k(dSa, ks, PANEL_D), kstep_k(dW, ks, PANEL_C), id_1, ks > 0);
       umma_commit_to(bar_u);
     }
     mbar_wait(bar_u, ph_u, a.err);
     ph_u ^= 1u;
     tc_fence_after();
-    {  // U^T row -> bf16 operand (the U record)
+    {  // U^T row = U'^T row + (S^T (-W)^T) row -> bf16 operand (the U record)
       float x[32];
       tmem_ld32(tl + 128 + 32 * half, x);
+      const bf16* up = reinterpret_cast<const bf16*>(st + L::UP);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const uint4 u = *reinterpret_cast<const uint4*>(up + Sw<bf16, TD, C>::off(row, 32 * half + 8 * q));
+        const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&u);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float2 f = __bfloat1622float2(h2[e]);
+          x[8 * q + 2 * e] += f.x;
+          x[8 * q + 2 * e + 1] += f.y;
+        }
+      }
       store_row32(Ua, row, 32 * half, x);
     }
     fence_proxy_async();
     tc_fence_before();
-    if (tid == 0) bulk_wait_read0();  // the state record store has read Sa
+    // the record stores of the previous chunk have read the buffers the next chunk writes
+    if (tid == 0) bulk_wait_read1();
     compute_sync();
     if (tid == 0) {
       tc_fence_after();
       bulk_s2g(u_rec + ch * (C * TD), Ua.p, C * TD * 2);
       bulk_commit();
-      const uint64_t dKt = desc_mn(st + L::KT, PANEL_C);
+      const uint64_t dKt = desc_mn(st + L::KT, PANEL_C), dUa = desc_k(Ua.p);
 #pragma unroll
       for (int ks = 0; ks < C / 16; ++ks) umma_bf16(tm, kstep_k(dUa, ks, PANEL_D), kstep_mn(dKt, ks), id_2, 1u);
       umma_commit_to(&empty[s]);
@@ -297,12 +298,12 @@ struct TcBwdLayout {
   static constexpr int KT = QH + C * TD * 2;     // K-tilde     [C][Dk] (K-major B of dU^T)
   static constexpr int DO = KT + C * TD * 2;     // dO          [C][Dv] (MN-major A)
   static constexpr int AQK = DO + C * TD * 2;    // scale Aqk   [C][C]  (MN-major B of dU^T)
-  static constexpr int GAM = AQK + C * C * 2;    // gam         [Dk] fp32
-  static constexpr int STAGE = a1k(GAM + TD * 4);
+  static constexpr int STAGE = AQK + C * C * 2;
   static constexpr int STAGES = 2;
-  static constexpr int SA = STAGES * STAGE;      // dS^T bf16 [Dv][Dk]
-  static constexpr int UA = SA + TD * TD * 2;    // dU^T bf16 [Dv][C]
-  static constexpr int BAR = UA + TD * C * 2;    // full[STAGES], empty[STAGES], u, s
+  static constexpr int GAM = STAGES * STAGE;     // gam [STAGES][Dk] fp32
+  static constexpr int SA = a1k(GAM + STAGES * TD * 4);  // dS^T bf16 [Dv][Dk], two buffers
+  static constexpr int UA = SA + 2 * TD * TD * 2;  // dU^T bf16 [Dv][C]
+  static constexpr int BAR = UA + TD * C * 2;      // full[STAGES], empty[STAGES], u, s
   static constexpr int TSLOT = BAR + 8 * (2 * STAGES + 2);
   static constexpr int BYTES = TSLOT + 16;
   static constexpr uint32_t TX = (uint32_t)(4 * C * TD * 2 + C * C * 2 + TD * 4);
@@ -331,8 +332,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
   uint64_t* bar_u = empty + L::STAGES;
   uint64_t* bar_s = bar_u + 1;
   uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + L::TSLOT);
-  Tile<bf16, TD, TD> Sa{reinterpret_cast<bf16*>(sm + L::SA)};
+  bf16* const sa_buf = reinterpret_cast<bf16*>(sm + L::SA);
   Tile<bf16, TD, C> Ua{reinterpret_cast<bf16*>(sm + L::UA)};
+  float* const gams = reinterpret_cast<float*>(sm + L::GAM);
 
   if (tid == 0) {
     for (int s = 0; s < L::STAGES; ++s) {
@@ -364,7 +366,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         bulk_g2s(st + L::QH, static_cast<const bf16*>(a.res.qh) + ch * (C * TD), C * TD * 2, &full[s]);
         bulk_g2s(st + L::KT, static_cast<const bf16*>(a.res.kt) + ch * (C * TD), C * TD * 2, &full[s]);
         bulk_g2s(st + L::AQK, static_cast<const bf16*>(a.res.aqk) + ch * (C * C), C * C * 2, &full[s]);
-        bulk_g2s(st + L::GAM, a.res.gam + ch * TD, TD * 4, &full[s]);
+        bulk_g2s(gams + s * TD, a.res.gam + ch * TD, TD * 4, &full[s]);
         const int tok = b * a.T + n * C;
         tma_load_3d(st + L::DO, &dout_map, 0, h, tok, &full[s]);
         tma_load_3d(st + L::DO + PANEL_C, &dout_map, 64, h, tok, &full[s]);
@@ -387,15 +389,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     tmem_st32(tl + 64 * half + 32, hi);
     tmem_wait_st();
   }
-  uint64_t dSa = 0, dUa = 0;
   constexpr uint32_t id_a = umma_idesc_bf16(128, C, true, true);    // dO^T Aqk
   constexpr uint32_t id_b = umma_idesc_bf16(128, C, false, false);  // dS^T K-tilde^T
   constexpr uint32_t id_c = umma_idesc_bf16(128, TD, true, true);   // dO^T Q-hat
   constexpr uint32_t id_d = umma_idesc_bf16(128, TD, false, true);  // dU^T (-W)
-  if (tid == 0) {
-    dSa = desc_k(Sa.p);
-    dUa = desc_k(Ua.p);
-  }
   bf16* dstate_rec = static_cast<bf16*>(a.ws.dstate);
   bf16* du_rec = static_cast<bf16*>(a.ws.du);
   uint32_t ph_u = 0, ph_s = 0;
@@ -404,6 +401,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     const int n = N - 1 - it, s = it % L::STAGES;
     uint8_t* st = sm + s * L::STAGE;
     const size_t ch = (size_t)bh * N + n;
+    Tile<bf16, TD, TD> Sa{sa_buf + (it & 1) * (TD * TD)};
     if (it > 0) {
       mbar_wait(bar_s, ph_s, a.err);
       ph_s ^= 1u;
@@ -411,7 +409,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     }
     mbar_wait(&full[s], (uint32_t)(it / L::STAGES) & 1u, a.err);
     // dS^T -> bf16 operand (the record of the gradient leaving chunk n); scale by gam
-    state_slice_out(tl + 64 * half, Sa, row, 64 * half, reinterpret_cast<const float*>(st + L::GAM));
+    state_slice_out(tl + 64 * half, Sa, row, 64 * half, gams + s * TD);
     fence_proxy_async();
     tc_fence_before();
     if (tid == 0) bulk_wait_read0();  // the previous dU record store has read Ua
@@ -420,6 +418,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       tc_fence_after();
       bulk_s2g(dstate_rec + ch * (TD * TD), Sa.p, TD * TD * 2);
       bulk_commit();
+      const uint64_t dSa = desc_k(Sa.p);
       const uint64_t dDo = desc_mn(st + L::DO, PANEL_C), dAq = desc_mn(st + L::AQK, PANEL_C);
       const uint64_t dKt = desc_k(st + L::KT), dQh = desc_mn(st + L::QH, PANEL_C);
 #pragma unroll
@@ -441,13 +440,14 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     }
     fence_proxy_async();
     tc_fence_before();
-    if (tid == 0) bulk_wait_read0();  // the dS record store has read Sa
+    // the dS record store of the previous chunk has read the buffer the next one writes
+    if (tid == 0) bulk_wait_read1();
     compute_sync();
     if (tid == 0) {
       tc_fence_after();
       bulk_s2g(du_rec + ch * (C * TD), Ua.p, C * TD * 2);
       bulk_commit();
-      const uint64_t dW = desc_mn(st + L::W, PANEL_C);
+      const uint64_t dW = desc_mn(st + L::W, PANEL_C), dUa = desc_k(Ua.p);
 #pragma unroll
       for (int ks = 0; ks < C / 16; ++ks) umma_bf16(tm, kstep_k(dUa, ks, PANEL_D), kstep_mn(dW, ks), id_d, 1u);
       umma_commit_to(&empty[s]);

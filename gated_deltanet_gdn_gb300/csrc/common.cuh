@@ -356,6 +356,10 @@ __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.comm
 __device__ __forceinline__ void bulk_wait_read0() {
   asm volatile("cp.async.bulk.wait_group.read 0;\n" ::: "memory");
 }
+// all but the most recently committed bulk group have finished reading shared memory
+__device__ __forceinline__ void bulk_wait_read1() {
+  asm volatile("cp.async.bulk.wait_group.read 1;\n" ::: "memory");
+}
 
 // Copies rows row0 .. row0 + rows - 1 of a swizzled ROWS x COLS record tile held in
 // shared memory as its own rows x COLS tile (row0 a multiple of 8, so the swizzle

@@ -16,7 +16,7 @@ constexpr float SAFE_SPREAD = 80.f;  // max decay spread (nats) for row-scaled i
 // Per (batch, head) and chunk, the forward writes these records. Byte sizes of one record
 // for operand element size es; every record starts 1024-byte aligned inside its region.
 // Each record is a swizzled tile (Sw in common.cuh): Aqk, T [C][C]; -W, Q-hat, K-tilde
-// [C][Dk]; U' [C][Dv]; the chunk-start state and U transposed,
+// [C][Dk]; U', the chunk-start state and U transposed: U'^T [Dv][C],
 // S^T [Dv][Dk] and U^T [Dv][C]. The backward's dS and dU records are likewise
 // dS^T [Dv][Dk] and dU^T [Dv][C].
 struct ResidualLayout {
