@@ -193,9 +193,15 @@ struct DstLayout {
   static constexpr int DU = a1k(U + C * DV * 2);     // dU^T  [DV][C], then Y [C][DV]
   static constexpr int S0 = a1k(DU + C * DV * 2);    // S0^T  [DV][DK]
   static constexpr int DS1 = a1k(S0 + DK * DV * 2);  // dS1^T [DV][DK]
-  static constexpr int BETA = a1k(DS1 + DK * DV * 2);
+  static constexpr int OQH = a1k(DS1 + DK * DV * 2);  // output records staged as tiles:
+  static constexpr int OBK = OQH + C * DK * 2;         //   dQ-hat, dBk, dK-tilde [C][DK]
+  static constexpr int OKT = OBK + C * DK * 2;
+  static constexpr int OAQ = OKT + C * DK * 2;         //   dAqk, dAkk [C][C]
+  static constexpr int OAK = OAQ + C * C * 2;
+  static constexpr int BETA = OAK + C * C * 2;
   static constexpr int DB = BETA + C * 4;            // float [2][C]
-  static constexpr int BYTES = DB + 2 * C * 4;
+  static constexpr int GQ = DB + 2 * C * 4;          // float [quarters][DK] dgam partials
+  static constexpr int BYTES = GQ + (DST_THREADS / (DK / 2)) * DK * 4;
 };
 
 template <int DK, int DV>
@@ -256,14 +262,14 @@ __global__ void __launch_bounds__(DST_THREADS) chunk_dstate_kernel(ChunkBwdArgs 
   Gemm<T>::template runk<1, NWV, 0, C>(y, aview<true>(Ts), bview<false>(dUs), m0, hf * (DV / 2), lane);
   {
     float db[2] = {0.f, 0.f};
-    T* dv = static_cast<T*>(a.dv);
 #pragma unroll
     for (int nt = 0; nt < NWV; ++nt)
 #pragma unroll
       for (int e = 0; e < 4; e += 2) {
         const int r = m0 + frag_row(lane, e), c = hf * (DV / 2) + 8 * nt + frag_col(lane, e);
         db[e >> 1] += y[0][nt][e] * to_f32(Vs.at(r, c)) + y[0][nt][e + 1] * to_f32(Vs.at(r, c + 1));
-        store2(dv + (row0 + r * rs) * DV + c, beta_s[r] * y[0][nt][e], beta_s[r] * y[0][nt][e + 1]);
+        // dv staged over this thread's own v elements, stored row-wise below
+        store2(Vs.ptr(r, c), beta_s[r] * y[0][nt][e], beta_s[r] * y[0][nt][e + 1]);
       }
 #pragma unroll
     for (int i = 0; i < 2; ++i) {
@@ -283,24 +289,43 @@ __global__ void __launch_bounds__(DST_THREADS) chunk_dstate_kernel(ChunkBwdArgs 
     for (int e = 0; e < 4; ++e)
       Ys.at(m0 + frag_row(lane, e), hf * (DV / 2) + 8 * nt + frag_col(lane, e)) = from_f32<T>(y[0][nt][e]);
   if (tid < C) a.ws.dbv[ch * C + tid] = db_s[tid] + db_s[C + tid];
-  for (int c = 2 * tid; c < DK; c += 2 * DST_THREADS) {  // dgam_c = sum_v dS1[c][v] S0[c][v]
+  {
+    T* dv = static_cast<T*>(a.dv);
+    for (int i = tid; i < C * DV / EPC; i += DST_THREADS) {
+      const int r = i / (DV / EPC), c0 = (i % (DV / EPC)) * EPC;
+      copy16(dv + (row0 + r * rs) * DV + c0, Vs.ptr(r, c0));
+    }
+  }
+  {  // dgam_c = sum_v dS1[c][v] S0[c][v]: thread (channel pair, quarter of v), then the quarters
+    constexpr int NQ = DST_THREADS / (DK / 2), VQ = DV / NQ;
+    const int c = 2 * (tid % (DK / 2)), vq = tid / (DK / 2);
     float acc0 = 0.f, acc1 = 0.f;
-    for (int v2 = 0; v2 < DV; ++v2) {
+#pragma unroll 8
+    for (int v2 = vq * VQ; v2 < (vq + 1) * VQ; ++v2) {
       const __nv_bfloat162 x = *reinterpret_cast<const __nv_bfloat162*>(dS1s.ptr(v2, c));
       const __nv_bfloat162 z = *reinterpret_cast<const __nv_bfloat162*>(S0s.ptr(v2, c));
       acc0 = fmaf(__low2float(x), __low2float(z), acc0);
       acc1 = fmaf(__high2float(x), __high2float(z), acc1);
     }
-    a.ws.dgam[ch * DK + c] = acc0;
-    a.ws.dgam[ch * DK + c + 1] = acc1;
+    float* part = reinterpret_cast<float*>(sm + L::GQ);
+    part[vq * DK + c] = acc0;
+    part[vq * DK + c + 1] = acc1;
   }
   __syncthreads();
+  for (int c = tid; c < DK; c += DST_THREADS) {
+    constexpr int NQ = DST_THREADS / (DK / 2);
+    const float* part = reinterpret_cast<const float*>(sm + L::GQ);
+    float acc = 0.f;
+#pragma unroll
+    for (int i = 0; i < NQ; ++i) acc += part[i * DK + c];
+    a.ws.dgam[ch * DK + c] = acc;
+  }
 
   // C x DK products: warp rows m0, columns hf * DK / 2 .. + DK / 2
   constexpr int NH = DK / 16;
   const int n0 = hf * (DK / 2);
-  auto store_cdk = [&](void* base, const float (&acc)[1][NH][4], float mul) {
-    T* dst = static_cast<T*>(base) + ch * (C * DK);
+  auto store_cdk = [&](int region, const float (&acc)[1][NH][4], float mul) {
+    T* dst = reinterpret_cast<T*>(sm + region);
 #pragma unroll
     for (int nt = 0; nt < NH; ++nt)
 #pragma unroll
@@ -313,13 +338,13 @@ __global__ void __launch_bounds__(DST_THREADS) chunk_dstate_kernel(ChunkBwdArgs 
     float acc[1][NH][4];
     zero(acc);
     Gemm<T>::template runk<1, NH, 0, DV>(acc, aview<false>(dOs), bview<true>(S0s), m0, n0, lane);
-    store_cdk(a.ws.dqh, acc, a.scale);
+    store_cdk(L::OQH, acc, a.scale);
     zero(acc);
     Gemm<T>::template runk<1, NH, 0, DV>(acc, aview<false>(Ys), bview<true>(S0s), m0, n0, lane);
-    store_cdk(a.ws.dbk, acc, -1.f);
+    store_cdk(L::OBK, acc, -1.f);
     zero(acc);
     Gemm<T>::template runk<1, NH, 0, DV>(acc, aview<true>(Us), bview<true>(dS1s), m0, n0, lane);
-    store_cdk(a.ws.dkt, acc, 1.f);
+    store_cdk(L::OKT, acc, 1.f);
   }
   // C x C products: warp rows m0, columns 32 hf .. +31 (block-1 rows see no block-2 columns)
   {
@@ -332,8 +357,8 @@ __global__ void __launch_bounds__(DST_THREADS) chunk_dstate_kernel(ChunkBwdArgs 
       Gemm<T>::template runk<1, 4, 0, DV>(aq, aview<false>(dOs), bview<true>(Us), m0, c0, lane);
       Gemm<T>::template runk<1, 4, 0, DV>(ak, aview<false>(Ys), bview<true>(Us), m0, c0, lane);
     }
-    T* da = static_cast<T*>(a.ws.daqk) + ch * (C * C);
-    T* dk = static_cast<T*>(a.ws.dakk) + ch * (C * C);
+    T* da = reinterpret_cast<T*>(sm + L::OAQ);
+    T* dk = reinterpret_cast<T*>(sm + L::OAK);
 #pragma unroll
     for (int nt = 0; nt < 4; ++nt)
 #pragma unroll
@@ -343,6 +368,17 @@ __global__ void __launch_bounds__(DST_THREADS) chunk_dstate_kernel(ChunkBwdArgs 
         store2(da + off, j <= r ? a.scale * aq[0][nt][e] : 0.f, j + 1 <= r ? a.scale * aq[0][nt][e + 1] : 0.f);
         store2(dk + off, j < r ? -ak[0][nt][e] : 0.f, j + 1 < r ? -ak[0][nt][e + 1] : 0.f);
       }
+  }
+  fence_proxy_async();  // the staged records are read by the bulk copies below
+  __syncthreads();
+  if (tid == 0) {
+    bulk_s2g(static_cast<T*>(a.ws.dqh) + ch * (C * DK), sm + L::OQH, C * DK * 2);
+    bulk_s2g(static_cast<T*>(a.ws.dbk) + ch * (C * DK), sm + L::OBK, C * DK * 2);
+    bulk_s2g(static_cast<T*>(a.ws.dkt) + ch * (C * DK), sm + L::OKT, C * DK * 2);
+    bulk_s2g(static_cast<T*>(a.ws.daqk) + ch * (C * C), sm + L::OAQ, C * C * 2);
+    bulk_s2g(static_cast<T*>(a.ws.dakk) + ch * (C * C), sm + L::OAK, C * C * 2);
+    bulk_commit();
+    bulk_wait_read0();  // the staged tiles are read before the CTA releases its shared memory
   }
 }
 

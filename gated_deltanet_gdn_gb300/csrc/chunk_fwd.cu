@@ -222,21 +222,20 @@ __global__ void __launch_bounds__(PREP_THREADS) chunk_prep_kernel(ChunkFwdArgs a
   cp_async_wait<0>();
   __syncthreads();
 
-  // ---- A1: inclusive cumulative log-decay per channel (fp32), two threads per channel
+  // ---- A1: inclusive cumulative log-decay per channel (fp32): lanes 2c and 2c + 1 take
+  // channel c, one 32-row block each in registers; the second block adds the first
+  // block's total (from its partner lane)
+  static_assert((2 * DK) % 32 == 0, "whole warps per pass");
   for (int u = tid; u < 2 * DK; u += PREP_THREADS) {
-    const int c = u % DK, r0 = (u / DK) * BLK;
-    float s = 0.f;
-#pragma unroll 8
-    for (int r = r0; r < r0 + BLK; ++r) {
-      s += PC ? to_f32(graw[r * DK + c]) : gsc[r];
-      Gs.at(r, c) = s;
-    }
-  }
-  __syncthreads();
-  for (int u = tid; u < DK; u += PREP_THREADS) {
-    const float base = Gs.at(BLK - 1, u);
-#pragma unroll 8
-    for (int r = BLK; r < C; ++r) Gs.at(r, u) += base;
+    const int c = u >> 1, hb = u & 1, r0 = hb * BLK;
+    float v[BLK];
+#pragma unroll
+    for (int i = 0; i < BLK; ++i) v[i] = PC ? to_f32(graw[(r0 + i) * DK + c]) : gsc[r0 + i];
+#pragma unroll
+    for (int i = 1; i < BLK; ++i) v[i] += v[i - 1];
+    const float base = __shfl_sync(0xffffffffu, v[BLK - 1], lane & ~1);
+#pragma unroll
+    for (int i = 0; i < BLK; ++i) Gs.at(r0 + i, c) = hb ? v[i] + base : v[i];
   }
   __syncthreads();
   // Reference point for every row: the boundary b = last token of the first block.
@@ -258,6 +257,24 @@ __global__ void __launch_bounds__(PREP_THREADS) chunk_prep_kernel(ChunkFwdArgs a
   Tile<T, C, DK> X2s{reinterpret_cast<T*>(sm + L::X2)};
   T* qh_g = static_cast<T*>(a.res.qh) + ch * (C * DK);
   T* kt_g = static_cast<T*>(a.res.kt) + ch * (C * DK);
+  // Each thread always takes the same four channels c0 .. c0 + 3. When both blocks are
+  // safe (spreads <= SAFE_SPREAD, so exp(G_b), exp(G_C - G_b), e1 and e2 are all in fp32
+  // range), Gam = exp(G_b) e1 and exp(G_C - G) = exp(G_C - G_b) e2 save two exponentials
+  // per element; otherwise every factor is its own exponential.
+  const bool fast = !(unsafe1 || unsafe2);
+  float eGb[4], eCb[4];
+  {
+    const int c0 = (tid % (DK / 4)) * 4;
+    float Gb[4], GC[4];
+    ld4(Gb, &Gs.at(BLK - 1, c0));
+    ld4(GC, &Gs.at(C - 1, c0));
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      eGb[e] = __expf(Gb[e]);
+      eCb[e] = __expf(GC[e] - Gb[e]);
+    }
+  }
+  static_assert(PREP_THREADS % (DK / 4) == 0, "fixed channels per thread");
   for (int i = tid; i < C * (DK / 4); i += PREP_THREADS) {
     const int r = i / (DK / 4), c0 = (i % (DK / 4)) * 4;
     const bool dead_q = r < BLK ? unsafe1 : false;   // query rows whose factor may overflow
@@ -271,8 +288,18 @@ __global__ void __launch_bounds__(PREP_THREADS) chunk_prep_kernel(ChunkFwdArgs a
     const float br = beta_s[r];
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
-      const float gm = __expf(G[e]), kd = __expf(GC[e] - G[e]);
-      const float e1 = dead_q ? 0.f : __expf(G[e] - Gb[e]), e2 = dead_k ? 0.f : __expf(Gb[e] - G[e]);
+      float gm, kd, e1, e2;
+      if (fast) {
+        e1 = __expf(G[e] - Gb[e]);
+        e2 = __expf(Gb[e] - G[e]);
+        gm = eGb[e] * e1;
+        kd = eCb[e] * e2;
+      } else {
+        gm = __expf(G[e]);
+        kd = __expf(GC[e] - G[e]);
+        e1 = dead_q ? 0.f : __expf(G[e] - Gb[e]);
+        e2 = dead_k ? 0.f : __expf(Gb[e] - G[e]);
+      }
       o1[e] = a.scale * gm * qv[e];
       o2[e] = kd * kv[e];
       xq[e] = qv[e] * e1;

@@ -148,20 +148,19 @@ __global__ void __launch_bounds__(GR_THREADS, 2) chunk_grads_kernel(ChunkBwdArgs
     diag_s[tid] = to_f32(dAq.at(tid, tid));
     dAq.at(tid, tid) = from_f32<T>(0.f);
   }
-  for (int u = tid; u < 2 * HC; u += GR_THREADS) {  // cumulative log-decay (fp32), two threads per channel
-    const int c = u % HC, r0 = (u / HC) * BLK;
-    float s = 0.f;
-#pragma unroll 8
-    for (int r = r0; r < r0 + BLK; ++r) {
-      s += PC ? to_f32(graw[r * HC + c]) : gsc[r];
-      Gat(r, c) = s;
-    }
-  }
-  __syncthreads();
-  for (int c = tid; c < HC; c += GR_THREADS) {
-    const float base = Gat(BLK - 1, c);
-#pragma unroll 8
-    for (int r = BLK; r < C; ++r) Gat(r, c) += base;
+  // cumulative log-decay (fp32): lanes 2c and 2c + 1 take channel c, one 32-row block
+  // each in registers; the second block adds the first block's total (from its partner)
+  static_assert(2 * HC <= GR_THREADS, "two threads per channel");
+  if (tid < 2 * HC) {
+    const int c = tid >> 1, hb = tid & 1, r0 = hb * BLK;
+    float v[BLK];
+#pragma unroll
+    for (int i = 0; i < BLK; ++i) v[i] = PC ? to_f32(graw[(r0 + i) * HC + c]) : gsc[r0 + i];
+#pragma unroll
+    for (int i = 1; i < BLK; ++i) v[i] += v[i - 1];
+    const float base = __shfl_sync(0xffffffffu, v[BLK - 1], lane & ~1);
+#pragma unroll
+    for (int i = 0; i < BLK; ++i) Gat(r0 + i, c) = hb ? v[i] + base : v[i];
   }
   __syncthreads();
   const bool force = (a.flags & 1) != 0;
@@ -232,15 +231,18 @@ __global__ void __launch_bounds__(GR_THREADS, 2) chunk_grads_kernel(ChunkBwdArgs
   float* dGs = reinterpret_cast<float*>(sm + L::DG);
   float dbp[2] = {0.f, 0.f}, colp[4][2];
   {
-    T* dq = static_cast<T*>(a.dq);
-    T* dk = static_cast<T*>(a.dk);
     const int bs = blk1 ? 0 : BLK;
     const bool skip_x = blk1 && unsafe1, skip_y = !blk1 && unsafe2;
+    // with both blocks safe, Gam = exp(G_b) e1 and exp(G_C - G) = exp(G_C - G_b) e2 (all
+    // factors in fp32 range) save two exponentials per element
+    const bool fast = !(unsafe1 || unsafe2);
 #pragma unroll
     for (int nt = 0; nt < 4; ++nt) {
       const int c = c0 + 8 * nt + 2 * (lane & 3);
       const float2 gb = *reinterpret_cast<const float2*>(&Gat(BLK - 1, c));
       const float2 gc = *reinterpret_cast<const float2*>(&Gat(C - 1, c));
+      const float eb[2] = {__expf(gb.x), __expf(gb.y)};
+      const float ecb[2] = {__expf(gc.x - gb.x), __expf(gc.y - gb.y)};
       colp[nt][0] = colp[nt][1] = 0.f;
 #pragma unroll
       for (int e = 0; e < 4; e += 2) {
@@ -261,7 +263,8 @@ __global__ void __launch_bounds__(GR_THREADS, 2) chunk_grads_kernel(ChunkBwdArgs
           const float dqh = u ? __high2float(h2) : __low2float(h2);
           const float dbk = u ? __high2float(b2) : __low2float(b2);
           const float dkt = u ? __high2float(t2) : __low2float(t2);
-          const float e1 = __expf(G - Gb), e2 = __expf(Gb - G), gm = __expf(G), kd = __expf(GC - G);
+          const float e1 = __expf(G - Gb), e2 = __expf(Gb - G);
+          const float gm = fast ? eb[u] * e1 : __expf(G), kd = fast ? ecb[u] * e2 : __expf(GC - G);
           float dxb = skip_x ? 0.f : axB[0][nt][e + u] * e1;  // Akk family, dP = dAkk
           float dyb = skip_y ? 0.f : ayB[0][nt][e + u] * e2;
           float dxa = skip_x ? 0.f : axA[0][nt][e + u] * e1;  // Aqk family
@@ -279,9 +282,9 @@ __global__ void __launch_bounds__(GR_THREADS, 2) chunk_grads_kernel(ChunkBwdArgs
           dbp[e >> 1] += kf * dxb + dbk * khat;
           colp[nt][u] += dkt * ktil;
         }
-        const size_t gi = (row0 + r * rs) * DK + cbase + c;
-        store2(dq + gi, oq[0], oq[1]);
-        store2(dk + gi, ok[0], ok[1]);
+        // staged over this thread's own dQ-hat / dBk elements, stored row-wise below
+        store2(dQh.ptr(r, c), oq[0], oq[1]);
+        store2(dBk.ptr(r, c), ok[0], ok[1]);
       }
     }
   }
@@ -305,25 +308,36 @@ __global__ void __launch_bounds__(GR_THREADS, 2) chunk_grads_kernel(ChunkBwdArgs
     db_s[cq * C + m0 + (lane >> 2)] = dbp[0];
     db_s[cq * C + m0 + (lane >> 2) + 8] = dbp[1];
   }
-  __syncthreads();  // dG, column and dbeta partials complete
+  __syncthreads();  // dG, column and dbeta partials, dq and dk tiles complete
   if (tid < C) a.ws.dbpart[(ch * 2 + grp) * C + tid] = db_s[tid] + db_s[C + tid];
-  // reverse cumulative sum per channel; the last row also gets the K-tilde column sum and
-  // dgam * gam (both are derivatives with respect to G at the chunk's last token)
-  for (int u = tid; u < 2 * HC; u += GR_THREADS) {
-    const int c = u % HC, hi = u / HC;
-    float s = hi ? (cols_s[c] + cols_s[HC + c] + cols_s[2 * HC + c] + cols_s[3 * HC + c] + gcol_s[c]) : 0.f;
-    const int r1 = hi ? C - 1 : BLK - 1;
-#pragma unroll 8
-    for (int r = r1; r > r1 - BLK; --r) {
-      s += dGs[r * HC + c];
-      dGs[r * HC + c] = s;
+  {
+    T* dq = static_cast<T*>(a.dq);
+    T* dk = static_cast<T*>(a.dk);
+    for (int i = tid; i < C * HC / EPC; i += GR_THREADS) {
+      const int r = i / (HC / EPC), cc = (i % (HC / EPC)) * EPC;
+      const size_t gi = (row0 + r * rs) * DK + cbase + cc;
+      copy16(dq + gi, dQh.ptr(r, cc));
+      copy16(dk + gi, dBk.ptr(r, cc));
     }
   }
-  __syncthreads();
-  for (int c = tid; c < HC; c += GR_THREADS) {
-    const float top = dGs[BLK * HC + c];  // rows >= BLK summed (with the extras)
-#pragma unroll 8
-    for (int r = 0; r < BLK; ++r) dGs[r * HC + c] += top;
+  // reverse cumulative sum per channel; the last row also gets the K-tilde column sum and
+  // dgam * gam (both are derivatives with respect to G at the chunk's last token). Lanes
+  // 2c and 2c + 1 take channel c, one 32-row block each; the first block adds the
+  // second block's total (from its partner)
+  if (tid < 2 * HC) {
+    const int c = tid >> 1, hi = tid & 1, r0 = hi * BLK;
+    float v[BLK];
+#pragma unroll
+    for (int i = 0; i < BLK; ++i) v[i] = dGs[(r0 + i) * HC + c];
+    float s = hi ? (cols_s[c] + cols_s[HC + c] + cols_s[2 * HC + c] + cols_s[3 * HC + c] + gcol_s[c]) : 0.f;
+#pragma unroll
+    for (int i = BLK - 1; i >= 0; --i) {
+      s += v[i];
+      v[i] = s;
+    }
+    const float top = __shfl_sync(0xffffffffu, v[0], lane | 1);  // rows >= BLK summed (with the extras)
+#pragma unroll
+    for (int i = 0; i < BLK; ++i) dGs[(r0 + i) * HC + c] = hi ? v[i] : v[i] + top;
   }
   __syncthreads();
   T* dg = static_cast<T*>(a.dg);
