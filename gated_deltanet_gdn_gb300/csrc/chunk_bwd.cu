@@ -30,6 +30,7 @@ namespace {
 
 constexpr int RSCAN_THREADS = 256;
 constexpr int DST_THREADS = 256;
+constexpr int DST_CG = DST_THREADS / 128;  // column groups of the state-products warps (4 row groups each)
 
 
 // ------------------------------------------------------------------ reverse state scan
@@ -61,7 +62,7 @@ __global__ void __launch_bounds__(RSCAN_THREADS) chunk_scan_bwd_kernel(ChunkBwdA
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int tile = blockIdx.x, bh = blockIdx.y, b = bh / a.H, h = bh % a.H;
   const int N = a.T / C;
-  constexpr int NTILE = DV / NT, MTS = DK / 64, EPC = 8;
+  constexpr int MTS = DK / 64, EPC = 8;
   const int rg = warp & 3, cg = warp >> 2;
   const int srow = rg * 16 * MTS, col0 = 32 * cg;
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + L::BAR);
@@ -186,28 +187,27 @@ __global__ void __launch_bounds__(RSCAN_THREADS) chunk_scan_bwd_kernel(ChunkBwdA
 //   dgam = rowsum(dS1 * S0).
 template <int DK, int DV>
 struct DstLayout {
-  static constexpr int TM = 0;                       // T    [C][C]
-  static constexpr int DO = a1k(TM + C * C * 2);     // dO   [C][DV]
-  static constexpr int V = a1k(DO + C * DV * 2);     // v    [C][DV]
+  static constexpr int TM = 0;                       // T     [C][C]
+  static constexpr int DO = a1k(TM + C * C * 2);     // dO    [C][DV]
+  static constexpr int V = a1k(DO + C * DV * 2);     // v     [C][DV], then dv; then S0^T panel 1
   static constexpr int U = a1k(V + C * DV * 2);      // U^T   [DV][C]
   static constexpr int DU = a1k(U + C * DV * 2);     // dU^T  [DV][C], then Y [C][DV]
-  static constexpr int S0 = a1k(DU + C * DV * 2);    // S0^T  [DV][DK]
-  static constexpr int DS1 = a1k(S0 + DK * DV * 2);  // dS1^T [DV][DK]
-  static constexpr int OQH = a1k(DS1 + DK * DV * 2);  // output records staged as tiles:
-  static constexpr int OBK = OQH + C * DK * 2;         //   dQ-hat, dBk, dK-tilde [C][DK]
-  static constexpr int OKT = OBK + C * DK * 2;
-  static constexpr int OAQ = OKT + C * DK * 2;         //   dAqk, dAkk [C][C]
-  static constexpr int OAK = OAQ + C * C * 2;
-  static constexpr int BETA = OAK + C * C * 2;
-  static constexpr int DB = BETA + C * 4;            // float [2][C]
-  static constexpr int GQ = DB + 2 * C * 4;          // float [quarters][DK] dgam partials
-  static constexpr int BYTES = GQ + (DST_THREADS / (DK / 2)) * DK * 4;
+  static constexpr int S0P = a1k(DU + C * DV * 2);   // S0^T  [DV][64], one 64-channel panel
+  static constexpr int DSP = a1k(S0P + DV * 64 * 2); // dS1^T [DV][64], one 64-channel panel
+  static constexpr int BETA = a1k(DSP + DV * 64 * 2);
+  static constexpr int DB = BETA + C * 4;            // float [DST_CG][C]
+  static constexpr int GQ = DB + DST_CG * C * 4;     // float [DST_THREADS / 32][DK] dgam partials
+  static constexpr int BYTES = GQ + (DST_THREADS / 32) * DK * 4;
 };
 
+// Two CTAs per SM: while one computes, the other's loads are in flight. The state and
+// state-gradient records are taken one 64-channel panel (16 KiB each) at a time; the
+// second S0^T panel is prefetched into v's buffer as soon as dv has left it.
 template <int DK, int DV>
-__global__ void __launch_bounds__(DST_THREADS) chunk_dstate_kernel(ChunkBwdArgs a) {
+__global__ void __launch_bounds__(DST_THREADS, 2) chunk_dstate_kernel(ChunkBwdArgs a) {
   typedef bf16 T;
   typedef DstLayout<DK, DV> L;
+  constexpr int NPAN = DK / 64;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = align1024(smem_raw);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -218,55 +218,63 @@ __global__ void __launch_bounds__(DST_THREADS) chunk_dstate_kernel(ChunkBwdArgs 
   Tile<T, C, C> Ts{reinterpret_cast<T*>(sm + L::TM)};
   Tile<T, C, DV> dOs{reinterpret_cast<T*>(sm + L::DO)};
   Tile<T, C, DV> Vs{reinterpret_cast<T*>(sm + L::V)};
-  Tile<T, DV, C> Us{reinterpret_cast<T*>(sm + L::U)};       // U^T
-  Tile<T, DV, C> dUs{reinterpret_cast<T*>(sm + L::DU)};      // dU^T
-  Tile<T, DV, DK> S0s{reinterpret_cast<T*>(sm + L::S0)};     // S0^T
-  Tile<T, DV, DK> dS1s{reinterpret_cast<T*>(sm + L::DS1)};   // dS1^T
+  Tile<T, DV, C> Us{reinterpret_cast<T*>(sm + L::U)};    // U^T
+  Tile<T, DV, C> dUs{reinterpret_cast<T*>(sm + L::DU)};  // dU^T
   float* beta_s = reinterpret_cast<float*>(sm + L::BETA);
   float* db_s = reinterpret_cast<float*>(sm + L::DB);
+  float* gq = reinterpret_cast<float*>(sm + L::GQ);
   const T* dout = static_cast<const T*>(a.dout);
   const T* v = static_cast<const T*>(a.v);
+  const T* s0rec = static_cast<const T*>(a.res.state) + ch * (DK * DV);
+  const T* ds1rec = static_cast<const T*>(a.ws.dstate) + ch * (DK * DV);
   const size_t row0 = ((size_t)b * a.T + (size_t)n * C) * a.H + h;
   const size_t rs = a.H;
-  for (int i = tid; i < C * DV / EPC; i += DST_THREADS) {
-    const int r = i / (DV / EPC), c0 = (i % (DV / EPC)) * EPC;
-    cp_async16(dOs.ptr(r, c0), dout + (row0 + r * rs) * DV + c0);
-    cp_async16(Vs.ptr(r, c0), v + (row0 + r * rs) * DV + c0);
-  }
+  auto load_panel = [&](T* dst, const T* rec, int p) {  // columns 64p .. 64p + 63 of an S^T record
+    const T* src = rec + (size_t)p * DV * 64;
+    for (int i = tid; i < DV * 64 / EPC; i += DST_THREADS) cp_async16(dst + i * EPC, src + i * EPC);
+  };
+  // group 0: what Y, dv and dbeta_v need
   {
     const T* st = static_cast<const T*>(a.res.tmat) + ch * (C * C);
     for (int i = tid; i < C * C / EPC; i += DST_THREADS) cp_async16(Ts.p + i * EPC, st + i * EPC);
-    const T* su = static_cast<const T*>(a.res.u) + ch * (C * DV);
     const T* sdu = static_cast<const T*>(a.ws.du) + ch * (C * DV);
     for (int i = tid; i < C * DV / EPC; i += DST_THREADS) {
-      cp_async16(Us.p + i * EPC, su + i * EPC);
+      const int r = i / (DV / EPC), c0 = (i % (DV / EPC)) * EPC;
       cp_async16(dUs.p + i * EPC, sdu + i * EPC);
-    }
-    const T* ss = static_cast<const T*>(a.res.state) + ch * (DK * DV);
-    const T* sds = static_cast<const T*>(a.ws.dstate) + ch * (DK * DV);
-    for (int i = tid; i < DK * DV / EPC; i += DST_THREADS) {
-      cp_async16(S0s.p + i * EPC, ss + i * EPC);
-      cp_async16(dS1s.p + i * EPC, sds + i * EPC);
+      cp_async16(Vs.ptr(r, c0), v + (row0 + r * rs) * DV + c0);
     }
   }
   cp_async_commit();
+  // group 1: the products with U, S0 and dS1 (first channel panel)
+  {
+    const T* su = static_cast<const T*>(a.res.u) + ch * (C * DV);
+    for (int i = tid; i < C * DV / EPC; i += DST_THREADS) {
+      const int r = i / (DV / EPC), c0 = (i % (DV / EPC)) * EPC;
+      cp_async16(Us.p + i * EPC, su + i * EPC);
+      cp_async16(dOs.ptr(r, c0), dout + (row0 + r * rs) * DV + c0);
+    }
+    load_panel(reinterpret_cast<T*>(sm + L::S0P), s0rec, 0);
+    load_panel(reinterpret_cast<T*>(sm + L::DSP), ds1rec, 0);
+  }
+  cp_async_commit();
   if (tid < C) beta_s[tid] = to_f32(static_cast<const T*>(a.beta)[row0 + tid * rs]);
-  cp_async_wait<0>();
+  cp_async_wait<1>();
   __syncthreads();
 
+  // warp w: rows 16 (w % 4) .. + 15 and column group w / 4 of every product
   const int m0 = 16 * (warp & 3), hf = warp >> 2;
   // Y = T^T dU; dv = beta Y; dbeta_v = rowsum(Y * V)
-  constexpr int NWV = DV / 16;
+  constexpr int NWV = DV / (8 * DST_CG);
   float y[1][NWV][4];
   zero(y);
-  Gemm<T>::template runk<1, NWV, 0, C>(y, aview<true>(Ts), bview<false>(dUs), m0, hf * (DV / 2), lane);
+  Gemm<T>::template runk<1, NWV, 0, C>(y, aview<true>(Ts), bview<false>(dUs), m0, hf * (DV / DST_CG), lane);
   {
     float db[2] = {0.f, 0.f};
 #pragma unroll
     for (int nt = 0; nt < NWV; ++nt)
 #pragma unroll
       for (int e = 0; e < 4; e += 2) {
-        const int r = m0 + frag_row(lane, e), c = hf * (DV / 2) + 8 * nt + frag_col(lane, e);
+        const int r = m0 + frag_row(lane, e), c = hf * (DV / DST_CG) + 8 * nt + frag_col(lane, e);
         db[e >> 1] += y[0][nt][e] * to_f32(Vs.at(r, c)) + y[0][nt][e + 1] * to_f32(Vs.at(r, c + 1));
         // dv staged over this thread's own v elements, stored row-wise below
         store2(Vs.ptr(r, c), beta_s[r] * y[0][nt][e], beta_s[r] * y[0][nt][e + 1]);
@@ -281,14 +289,19 @@ __global__ void __launch_bounds__(DST_THREADS) chunk_dstate_kernel(ChunkBwdArgs 
       db_s[hf * C + m0 + (lane >> 2) + 8] = db[1];
     }
   }
-  __syncthreads();  // dU consumed: Y takes its place
+  __syncthreads();  // dU consumed: Y takes its place; dv complete
   Tile<T, C, DV> Ys{reinterpret_cast<T*>(sm + L::DU)};
 #pragma unroll
   for (int nt = 0; nt < NWV; ++nt)
 #pragma unroll
     for (int e = 0; e < 4; ++e)
-      Ys.at(m0 + frag_row(lane, e), hf * (DV / 2) + 8 * nt + frag_col(lane, e)) = from_f32<T>(y[0][nt][e]);
-  if (tid < C) a.ws.dbv[ch * C + tid] = db_s[tid] + db_s[C + tid];
+      Ys.at(m0 + frag_row(lane, e), hf * (DV / DST_CG) + 8 * nt + frag_col(lane, e)) = from_f32<T>(y[0][nt][e]);
+  if (tid < C) {
+    float sdb = 0.f;
+#pragma unroll
+    for (int i = 0; i < DST_CG; ++i) sdb += db_s[i * C + tid];
+    a.ws.dbv[ch * C + tid] = sdb;
+  }
   {
     T* dv = static_cast<T*>(a.dv);
     for (int i = tid; i < C * DV / EPC; i += DST_THREADS) {
@@ -296,71 +309,33 @@ __global__ void __launch_bounds__(DST_THREADS) chunk_dstate_kernel(ChunkBwdArgs 
       copy16(dv + (row0 + r * rs) * DV + c0, Vs.ptr(r, c0));
     }
   }
-  {  // dgam_c = sum_v dS1[c][v] S0[c][v]: thread (channel pair, quarter of v), then the quarters
-    constexpr int NQ = DST_THREADS / (DK / 2), VQ = DV / NQ;
-    const int c = 2 * (tid % (DK / 2)), vq = tid / (DK / 2);
-    float acc0 = 0.f, acc1 = 0.f;
-#pragma unroll 8
-    for (int v2 = vq * VQ; v2 < (vq + 1) * VQ; ++v2) {
-      const __nv_bfloat162 x = *reinterpret_cast<const __nv_bfloat162*>(dS1s.ptr(v2, c));
-      const __nv_bfloat162 z = *reinterpret_cast<const __nv_bfloat162*>(S0s.ptr(v2, c));
-      acc0 = fmaf(__low2float(x), __low2float(z), acc0);
-      acc1 = fmaf(__high2float(x), __high2float(z), acc1);
-    }
-    float* part = reinterpret_cast<float*>(sm + L::GQ);
-    part[vq * DK + c] = acc0;
-    part[vq * DK + c + 1] = acc1;
+  __syncthreads();  // v's buffer free: prefetch the second S0^T panel there
+  if (NPAN > 1) {
+    load_panel(reinterpret_cast<T*>(sm + L::V), s0rec, 1);
+    cp_async_commit();
+    cp_async_wait<1>();  // group 1 (first panels, U, dO) complete
+  } else {
+    cp_async_wait<0>();
   }
   __syncthreads();
-  for (int c = tid; c < DK; c += DST_THREADS) {
-    constexpr int NQ = DST_THREADS / (DK / 2);
-    const float* part = reinterpret_cast<const float*>(sm + L::GQ);
-    float acc = 0.f;
-#pragma unroll
-    for (int i = 0; i < NQ; ++i) acc += part[i * DK + c];
-    a.ws.dgam[ch * DK + c] = acc;
-  }
 
-  // C x DK products: warp rows m0, columns hf * DK / 2 .. + DK / 2
-  constexpr int NH = DK / 16;
-  const int n0 = hf * (DK / 2);
-  auto store_cdk = [&](int region, const float (&acc)[1][NH][4], float mul) {
-    T* dst = reinterpret_cast<T*>(sm + region);
-#pragma unroll
-    for (int nt = 0; nt < NH; ++nt)
-#pragma unroll
-      for (int e = 0; e < 4; e += 2) {
-        const int r = m0 + frag_row(lane, e), c = n0 + 8 * nt + frag_col(lane, e);
-        store2(dst + Sw<T, C, DK>::off(r, c), mul * acc[0][nt][e], mul * acc[0][nt][e + 1]);
-      }
-  };
+  // C x C products: warp rows m0, columns hf * C / DST_CG .. (block-1 rows see no block-2
+  // columns); stored straight into the records (swizzled tile images)
   {
-    float acc[1][NH][4];
-    zero(acc);
-    Gemm<T>::template runk<1, NH, 0, DV>(acc, aview<false>(dOs), bview<true>(S0s), m0, n0, lane);
-    store_cdk(L::OQH, acc, a.scale);
-    zero(acc);
-    Gemm<T>::template runk<1, NH, 0, DV>(acc, aview<false>(Ys), bview<true>(S0s), m0, n0, lane);
-    store_cdk(L::OBK, acc, -1.f);
-    zero(acc);
-    Gemm<T>::template runk<1, NH, 0, DV>(acc, aview<true>(Us), bview<true>(dS1s), m0, n0, lane);
-    store_cdk(L::OKT, acc, 1.f);
-  }
-  // C x C products: warp rows m0, columns 32 hf .. +31 (block-1 rows see no block-2 columns)
-  {
-    const int c0 = 32 * hf;
-    const bool dead = m0 < BLK && hf == 1;
-    float aq[1][4][4], ak[1][4][4];
+    constexpr int NCC = C / (8 * DST_CG);
+    const int c0 = hf * (C / DST_CG);
+    const bool dead = m0 < BLK && c0 >= BLK;
+    float aq[1][NCC][4], ak[1][NCC][4];
     zero(aq);
     zero(ak);
     if (!dead) {
-      Gemm<T>::template runk<1, 4, 0, DV>(aq, aview<false>(dOs), bview<true>(Us), m0, c0, lane);
-      Gemm<T>::template runk<1, 4, 0, DV>(ak, aview<false>(Ys), bview<true>(Us), m0, c0, lane);
+      Gemm<T>::template runk<1, NCC, 0, DV>(aq, aview<false>(dOs), bview<true>(Us), m0, c0, lane);
+      Gemm<T>::template runk<1, NCC, 0, DV>(ak, aview<false>(Ys), bview<true>(Us), m0, c0, lane);
     }
-    T* da = reinterpret_cast<T*>(sm + L::OAQ);
-    T* dk = reinterpret_cast<T*>(sm + L::OAK);
+    T* da = static_cast<T*>(a.ws.daqk) + ch * (C * C);
+    T* dk = static_cast<T*>(a.ws.dakk) + ch * (C * C);
 #pragma unroll
-    for (int nt = 0; nt < 4; ++nt)
+    for (int nt = 0; nt < NCC; ++nt)
 #pragma unroll
       for (int e = 0; e < 4; e += 2) {
         const int r = m0 + frag_row(lane, e), j = c0 + 8 * nt + frag_col(lane, e);
@@ -369,16 +344,64 @@ __global__ void __launch_bounds__(DST_THREADS) chunk_dstate_kernel(ChunkBwdArgs 
         store2(dk + off, j < r ? -ak[0][nt][e] : 0.f, j + 1 < r ? -ak[0][nt][e + 1] : 0.f);
       }
   }
-  fence_proxy_async();  // the staged records are read by the bulk copies below
+
+  // C x 64 products per channel panel: warp rows m0, columns hf * 64 / DST_CG ..
+  constexpr int NH = 64 / (8 * DST_CG);
+  const int n0 = hf * (64 / DST_CG);
+  auto store_cdk = [&](void* base, int p, const float (&acc)[1][NH][4], float mul) {
+    T* dst = static_cast<T*>(base) + ch * (C * DK);
+#pragma unroll
+    for (int nt = 0; nt < NH; ++nt)
+#pragma unroll
+      for (int e = 0; e < 4; e += 2) {
+        const int r = m0 + frag_row(lane, e), c = 64 * p + n0 + 8 * nt + frag_col(lane, e);
+        store2(dst + Sw<T, C, DK>::off(r, c), mul * acc[0][nt][e], mul * acc[0][nt][e + 1]);
+      }
+  };
+  // dgam over one panel: thread (channel pair, 1/16 of the value rows), partials in gq
+  auto dgam_part = [&](Tile<T, DV, 64> s0, Tile<T, DV, 64> ds1, int p) {
+    constexpr int NQ = DST_THREADS / 32, VQ = DV / NQ;
+    const int c = 2 * (tid % 32), vq = tid / 32;
+    float acc0 = 0.f, acc1 = 0.f;
+#pragma unroll
+    for (int v2 = vq * VQ; v2 < (vq + 1) * VQ; ++v2) {
+      const __nv_bfloat162 x = *reinterpret_cast<const __nv_bfloat162*>(ds1.ptr(v2, c));
+      const __nv_bfloat162 z = *reinterpret_cast<const __nv_bfloat162*>(s0.ptr(v2, c));
+      acc0 = fmaf(__low2float(x), __low2float(z), acc0);
+      acc1 = fmaf(__high2float(x), __high2float(z), acc1);
+    }
+    gq[vq * DK + 64 * p + c] = acc0;
+    gq[vq * DK + 64 * p + c + 1] = acc1;
+  };
+#pragma unroll 1
+  for (int p = 0; p < NPAN; ++p) {
+    Tile<T, DV, 64> S0p{reinterpret_cast<T*>(sm + (p == 0 ? L::S0P : L::V))};
+    Tile<T, DV, 64> dS1p{reinterpret_cast<T*>(sm + L::DSP)};
+    float acc[1][NH][4];
+    zero(acc);
+    Gemm<T>::template runk<1, NH, 0, DV>(acc, aview<false>(dOs), bview<true>(S0p), m0, n0, lane);
+    store_cdk(a.ws.dqh, p, acc, a.scale);
+    zero(acc);
+    Gemm<T>::template runk<1, NH, 0, DV>(acc, aview<false>(Ys), bview<true>(S0p), m0, n0, lane);
+    store_cdk(a.ws.dbk, p, acc, -1.f);
+    zero(acc);
+    Gemm<T>::template runk<1, NH, 0, DV>(acc, aview<true>(Us), bview<true>(dS1p), m0, n0, lane);
+    store_cdk(a.ws.dkt, p, acc, 1.f);
+    dgam_part(S0p, dS1p, p);
+    if (p + 1 < NPAN) {
+      __syncthreads();  // the first dS1^T panel is consumed: load the second in its place
+      load_panel(reinterpret_cast<T*>(sm + L::DSP), ds1rec, p + 1);
+      cp_async_commit();
+      cp_async_wait<0>();
+      __syncthreads();
+    }
+  }
   __syncthreads();
-  if (tid == 0) {
-    bulk_s2g(static_cast<T*>(a.ws.dqh) + ch * (C * DK), sm + L::OQH, C * DK * 2);
-    bulk_s2g(static_cast<T*>(a.ws.dbk) + ch * (C * DK), sm + L::OBK, C * DK * 2);
-    bulk_s2g(static_cast<T*>(a.ws.dkt) + ch * (C * DK), sm + L::OKT, C * DK * 2);
-    bulk_s2g(static_cast<T*>(a.ws.daqk) + ch * (C * C), sm + L::OAQ, C * C * 2);
-    bulk_s2g(static_cast<T*>(a.ws.dakk) + ch * (C * C), sm + L::OAK, C * C * 2);
-    bulk_commit();
-    bulk_wait_read0();  // the staged tiles are read before the CTA releases its shared memory
+  for (int c = tid; c < DK; c += DST_THREADS) {
+    float acc = 0.f;
+#pragma unroll
+    for (int i = 0; i < DST_THREADS / 32; ++i) acc += gq[i * DK + c];
+    a.ws.dgam[ch * DK + c] = acc;
   }
 }
 
