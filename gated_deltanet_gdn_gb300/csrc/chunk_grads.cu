@@ -51,6 +51,11 @@ struct GrLayout {
 
 typedef Tile<bf16, C, HC> HTile;
 
+template <bool B>
+struct BoolTag {
+  static constexpr bool value = B;
+};
+
 // sum over j in [j0, j1] of dP(r, j) y(j, c) exp(G(r,c) - G(j,c)) (in-block x side)
 __device__ __noinline__ float pw_dx(const Tile<bf16, C, C>* dP, const HTile* ys, const float* G, int r, int c,
                                     int j0, int j1) {
@@ -230,19 +235,24 @@ __global__ void __launch_bounds__(GR_THREADS, 2) chunk_grads_kernel(ChunkBwdArgs
   // one epilogue per element pair: every gradient term of (r, c) and (r, c + 1)
   float* dGs = reinterpret_cast<float*>(sm + L::DG);
   float dbp[2] = {0.f, 0.f}, colp[4][2];
-  {
+  // FAST (both blocks safe): no pairwise rows, and Gam = exp(G_b) e1, exp(G_C - G) =
+  // exp(G_C - G_b) e2 with every factor in fp32 range, two exponentials per element fewer
+  auto epilogue = [&](auto fast_tag) {
+    constexpr bool FAST = decltype(fast_tag)::value;
     const int bs = blk1 ? 0 : BLK;
-    const bool skip_x = blk1 && unsafe1, skip_y = !blk1 && unsafe2;
-    // with both blocks safe, Gam = exp(G_b) e1 and exp(G_C - G) = exp(G_C - G_b) e2 (all
-    // factors in fp32 range) save two exponentials per element
-    const bool fast = !(unsafe1 || unsafe2);
+    const bool skip_x = !FAST && blk1 && unsafe1, skip_y = !FAST && !blk1 && unsafe2;
 #pragma unroll
     for (int nt = 0; nt < 4; ++nt) {
       const int c = c0 + 8 * nt + 2 * (lane & 3);
       const float2 gb = *reinterpret_cast<const float2*>(&Gat(BLK - 1, c));
       const float2 gc = *reinterpret_cast<const float2*>(&Gat(C - 1, c));
-      const float eb[2] = {__expf(gb.x), __expf(gb.y)};
-      const float ecb[2] = {__expf(gc.x - gb.x), __expf(gc.y - gb.y)};
+      float eb[2] = {0.f, 0.f}, ecb[2] = {0.f, 0.f};
+      if (FAST) {
+        eb[0] = __expf(gb.x);
+        eb[1] = __expf(gb.y);
+        ecb[0] = __expf(gc.x - gb.x);
+        ecb[1] = __expf(gc.y - gb.y);
+      }
       colp[nt][0] = colp[nt][1] = 0.f;
 #pragma unroll
       for (int e = 0; e < 4; e += 2) {
@@ -264,12 +274,12 @@ __global__ void __launch_bounds__(GR_THREADS, 2) chunk_grads_kernel(ChunkBwdArgs
           const float dbk = u ? __high2float(b2) : __low2float(b2);
           const float dkt = u ? __high2float(t2) : __low2float(t2);
           const float e1 = __expf(G - Gb), e2 = __expf(Gb - G);
-          const float gm = fast ? eb[u] * e1 : __expf(G), kd = fast ? ecb[u] * e2 : __expf(GC - G);
+          const float gm = FAST ? eb[u] * e1 : __expf(G), kd = FAST ? ecb[u] * e2 : __expf(GC - G);
           float dxb = skip_x ? 0.f : axB[0][nt][e + u] * e1;  // Akk family, dP = dAkk
           float dyb = skip_y ? 0.f : ayB[0][nt][e + u] * e2;
           float dxa = skip_x ? 0.f : axA[0][nt][e + u] * e1;  // Aqk family
           float dya = skip_y ? 0.f : ayA[0][nt][e + u] * e2;
-          if (pw_rows) {
+          if (!FAST && pw_rows) {
             dxb += pw_dx(&dAk, &Ks, Gp, r, c + u, bs, r);
             dyb += pw_dy(&dAk, &Ks, beta_s, Gp, r, c + u, r, bs + BLK - 1);
             dxa += pw_dx(&dAq, &Ks, Gp, r, c + u, bs, r);
@@ -287,7 +297,11 @@ __global__ void __launch_bounds__(GR_THREADS, 2) chunk_grads_kernel(ChunkBwdArgs
         store2(dBk.ptr(r, c), ok[0], ok[1]);
       }
     }
-  }
+  };
+  if (!(unsafe1 || unsafe2))
+    epilogue(BoolTag<true>{});
+  else
+    epilogue(BoolTag<false>{});
   // column sums over this warp's 16 rows (lanes sharing a column differ in bits 2..4)
 #pragma unroll
   for (int nt = 0; nt < 4; ++nt)
