@@ -257,64 +257,58 @@ __global__ void __launch_bounds__(PREP_THREADS) chunk_prep_kernel(ChunkFwdArgs a
   Tile<T, C, DK> X2s{reinterpret_cast<T*>(sm + L::X2)};
   T* qh_g = static_cast<T*>(a.res.qh) + ch * (C * DK);
   T* kt_g = static_cast<T*>(a.res.kt) + ch * (C * DK);
-  // Each thread always takes the same four channels c0 .. c0 + 3. When both blocks are
-  // safe (spreads <= SAFE_SPREAD, so exp(G_b), exp(G_C - G_b), e1 and e2 are all in fp32
-  // range), Gam = exp(G_b) e1 and exp(G_C - G) = exp(G_C - G_b) e2 save two exponentials
-  // per element; otherwise every factor is its own exponential.
-  const bool fast = !(unsafe1 || unsafe2);
-  float eGb[4], eCb[4];
-  {
-    const int c0 = (tid % (DK / 4)) * 4;
-    float Gb[4], GC[4];
-    ld4(Gb, &Gs.at(BLK - 1, c0));
-    ld4(GC, &Gs.at(C - 1, c0));
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      eGb[e] = __expf(Gb[e]);
-      eCb[e] = __expf(GC[e] - Gb[e]);
-    }
-  }
+  // Each thread always takes the same four channels. When both blocks are safe (spreads
+  // <= SAFE_SPREAD, so exp(G_b), exp(G_C - G_b), e1 and e2 are all in fp32 range),
+  // Gam = exp(G_b) e1 and exp(G_C - G) = exp(G_C - G_b) e2 save two exponentials per
+  // element (the pass is compiled for that case); otherwise every factor is its own
+  // exponential.
   static_assert(PREP_THREADS % (DK / 4) == 0, "fixed channels per thread");
-  for (int i = tid; i < C * (DK / 4); i += PREP_THREADS) {
-    const int r = i / (DK / 4), c0 = (i % (DK / 4)) * 4;
-    const bool dead_q = r < BLK ? unsafe1 : false;   // query rows whose factor may overflow
-    const bool dead_k = r < BLK ? false : unsafe2;   // key rows whose factor may overflow
-    float qv[4], kv[4], G[4], Gb[4], GC[4], o1[4], o2[4], xq[4], xk[4], yk[4], bk[4];
-    ld4(qv, Xs.ptr(r, c0));
-    ld4(kv, ks.ptr(r, c0));
-    ld4(G, &Gs.at(r, c0));
-    ld4(Gb, &Gs.at(BLK - 1, c0));
-    ld4(GC, &Gs.at(C - 1, c0));
-    const float br = beta_s[r];
+  auto a2_pass = [&](auto fast_tag) {
+    constexpr bool FAST = decltype(fast_tag)::value;
+    const int cc = (tid % (DK / 4)) * 4;
+    float Gb[4], GC[4], eGb[4], eCb[4];
+    ld4(Gb, &Gs.at(BLK - 1, cc));
+    ld4(GC, &Gs.at(C - 1, cc));
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
-      float gm, kd, e1, e2;
-      if (fast) {
-        e1 = __expf(G[e] - Gb[e]);
-        e2 = __expf(Gb[e] - G[e]);
-        gm = eGb[e] * e1;
-        kd = eCb[e] * e2;
-      } else {
-        gm = __expf(G[e]);
-        kd = __expf(GC[e] - G[e]);
-        e1 = dead_q ? 0.f : __expf(G[e] - Gb[e]);
-        e2 = dead_k ? 0.f : __expf(Gb[e] - G[e]);
-      }
-      o1[e] = a.scale * gm * qv[e];
-      o2[e] = kd * kv[e];
-      xq[e] = qv[e] * e1;
-      xk[e] = kv[e] * e1;
-      yk[e] = kv[e] * e2;
-      bk[e] = br * gm * kv[e];
+      eGb[e] = FAST ? __expf(Gb[e]) : 0.f;
+      eCb[e] = FAST ? __expf(GC[e] - Gb[e]) : 0.f;
     }
-    const int off = Sw<T, C, DK>::off(r, c0);
-    st4(qh_g + off, o1);
-    st4(kt_g + off, o2);
-    st4(Xs.ptr(r, c0), xq);
-    st4(X2s.ptr(r, c0), xk);
-    st4(Ys.ptr(r, c0), yk);
-    st4(ks.ptr(r, c0), bk);
-  }
+    for (int i = tid; i < C * (DK / 4); i += PREP_THREADS) {
+      const int r = i / (DK / 4), c0 = cc;
+      const bool dead_q = !FAST && r < BLK && unsafe1;  // query rows whose factor may overflow
+      const bool dead_k = !FAST && r >= BLK && unsafe2;  // key rows whose factor may overflow
+      float qv[4], kv[4], G[4], o1[4], o2[4], xq[4], xk[4], yk[4], bk[4];
+      ld4(qv, Xs.ptr(r, c0));
+      ld4(kv, ks.ptr(r, c0));
+      ld4(G, &Gs.at(r, c0));
+      const float br = beta_s[r];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float e1 = dead_q ? 0.f : __expf(G[e] - Gb[e]);
+        const float e2 = dead_k ? 0.f : __expf(Gb[e] - G[e]);
+        const float gm = FAST ? eGb[e] * e1 : __expf(G[e]);
+        const float kd = FAST ? eCb[e] * e2 : __expf(GC[e] - G[e]);
+        o1[e] = a.scale * gm * qv[e];
+        o2[e] = kd * kv[e];
+        xq[e] = qv[e] * e1;
+        xk[e] = kv[e] * e1;
+        yk[e] = kv[e] * e2;
+        bk[e] = br * gm * kv[e];
+      }
+      const int off = Sw<T, C, DK>::off(r, c0);
+      st4(qh_g + off, o1);
+      st4(kt_g + off, o2);
+      st4(Xs.ptr(r, c0), xq);
+      st4(X2s.ptr(r, c0), xk);
+      st4(Ys.ptr(r, c0), yk);
+      st4(ks.ptr(r, c0), bk);
+    }
+  };
+  if (!(unsafe1 || unsafe2))
+    a2_pass(BoolTag<true>{});
+  else
+    a2_pass(BoolTag<false>{});
   for (int c = tid; c < DK; c += PREP_THREADS) a.res.gam[ch * DK + c] = __expf(Gs.at(C - 1, c));
   __syncthreads();
 

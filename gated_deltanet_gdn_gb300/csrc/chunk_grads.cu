@@ -51,11 +51,6 @@ struct GrLayout {
 
 typedef Tile<bf16, C, HC> HTile;
 
-template <bool B>
-struct BoolTag {
-  static constexpr bool value = B;
-};
-
 // sum over j in [j0, j1] of dP(r, j) y(j, c) exp(G(r,c) - G(j,c)) (in-block x side)
 __device__ __noinline__ float pw_dx(const Tile<bf16, C, C>* dP, const HTile* ys, const float* G, int r, int c,
                                     int j0, int j1) {

@@ -30,6 +30,12 @@ __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return (uint32_t)__cvta_generic_to_shared(p);
 }
 
+// Compile-time flag for generic lambdas that are specialised on a condition.
+template <bool B>
+struct BoolTag {
+  static constexpr bool value = B;
+};
+
 // ------------------------------------------------------------------ swizzled tiles
 // A ROWS x COLS tile of T stored as column panels of 128 bytes (fewer when a row is
 // shorter). Inside a panel, row r occupies PANB bytes and the 16-byte chunk index is
