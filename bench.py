@@ -399,9 +399,11 @@ def e2e_leg(args, host, d, step, outputs, world):
 
 
 def decode_leg(dev):
-    """Recurrent kernel: decode steps (T = 1) with the state read and written once,
-    L2 flushed between timed steps (a buffer twice the L2 size is read); a batch whose state exceeds L2; and the
-    2048-token prefill of the same geometry."""
+    """Recurrent kernel: decode steps (T = 1) with the state read and written once.
+    B2 H48: L2 flushed before every step (a buffer twice the L2 size is read), the
+    kernel timed alone by the library's per-launch events (no host launch gap inside
+    the measurement). B32 H48 (state 201 MB > L2): 30 steps back to back between two
+    CUDA events. Then the 2048-token prefill of the same geometry."""
     import torch
 
     import gated_deltanet_gdn_gb300 as gdn
@@ -410,8 +412,8 @@ def decode_leg(dev):
     res = {}
     # read (not written) between steps, so no dirty lines are written back inside a timed step
     flush = torch.ones(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
-    for B, label in ((2, "B2 H48 Dk=Dv=128 fp32 (L2 flushed between steps)"),
-                     (32, "B32 H48 Dk=Dv=128 fp32 (state 201 MB > L2)")):
+    for B, label in ((2, "B2 H48 Dk=Dv=128 fp32 (L2 flushed before each step, kernel events)"),
+                     (32, "B32 H48 Dk=Dv=128 fp32 (state 201 MB > L2, 30 steps back to back)")):
         w = WORKLOADS["recurrent"].with_(B=B, T=1, h0_std=0.01)
         d = {k: (None if v is None else v.to(dev)) for k, v in make_inputs(w).items()}
         state = d["h0"].clone()
@@ -422,17 +424,25 @@ def decode_leg(dev):
 
         for _ in range(5):
             one()
-        times = []
-        for _ in range(30):
-            if B == 2:
+        torch.cuda.synchronize()
+        if B == 2:
+            times = []
+            for _ in range(30):
                 flush.sum()
+                gdn.gdn_profile_enable(True)
+                one()
+                prof = gdn.gdn_profile_read()
+                gdn.gdn_profile_enable(False)
+                times.append(sum(v[0] for v in prof.values()))
+            ms = statistics.median(times)
+        else:
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             e0.record()
-            one()
+            for _ in range(30):
+                one()
             e1.record()
             torch.cuda.synchronize()
-            times.append(e0.elapsed_time(e1))
-        ms = statistics.median(times)
+            ms = e0.elapsed_time(e1) / 30
         sb = w.B * w.H * w.Dk * w.Dv * 4
         io_b = w.B * w.H * (2 * w.Dk + 2 * w.Dv + 2) * 4
         b = 2 * sb + io_b

@@ -33,7 +33,7 @@ EXPORTED = ("gdn_chunk_residual_bytes", "gdn_chunk_bwd_workspace_bytes", "gdn_ch
             "gdn_chunk_bwd", "gdn_recurrent", "gdn_check_device_error", "gdn_status_string",
             "gdn_version", "gdn_profile_enable", "gdn_profile_read", "gdn_kernel_name",
             "gdn_chunk_fwd_noalloc")
-KERNEL_COUNT = 10
+KERNEL_COUNT = 11
 
 
 class GdnDims(ctypes.Structure):

@@ -106,7 +106,8 @@ const char* kKernelNames[K_COUNT] = {"chunk_prep_kernel",    "chunk_scan_fwd_ker
                                      "chunk_scan_bwd_kernel", "chunk_dstate_kernel",
                                      "chunk_grads_kernel",    "recurrent_kernel",
                                      "chunk_bwd_finalize_kernel", "chunk_out_kernel",
-                                     "chunk_scan_fwd_tc_kernel", "chunk_scan_bwd_tc_kernel"};
+                                     "chunk_scan_fwd_tc_kernel", "chunk_scan_bwd_tc_kernel",
+                                     "decode_kernel"};
 
 }  // namespace
 
@@ -233,6 +234,8 @@ int gdn_recurrent(const gdn_dims* d, const void* q, const void* k, const void* v
   a.bf16 = d->dtype == GDN_BF16;
   a.q = q; a.k = k; a.v = v; a.g = g; a.beta = beta; a.h0 = h0; a.scale = scale;
   a.out = out; a.h_final = h_final;
+  a.err = device_error_word();
+  if (!a.err) return GDN_ERR_CUDA;
   return launch_status(launch_recurrent(a, static_cast<cudaStream_t>(stream)));
 }
 

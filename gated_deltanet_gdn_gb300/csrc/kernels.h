@@ -139,6 +139,7 @@ struct RecurrentArgs {
   float scale;
   void* out;
   float* h_final;
+  unsigned* err;
 };
 
 // Kernel identifiers for the optional per-launch timing (gdn_profile_* in the C ABI).
@@ -153,7 +154,8 @@ enum KernelId {
   K_OUT = 7,       // chunk_out_kernel
   K_SCAN_FWD_TC = 8,  // chunk_scan_fwd_tc_kernel
   K_SCAN_BWD_TC = 9,  // chunk_scan_bwd_tc_kernel
-  K_COUNT = 10
+  K_DECODE = 10,      // decode_kernel
+  K_COUNT = 11
 };
 // Records a CUDA event on s before (begin = true) or after a launch when timing is on.
 void prof_mark(KernelId id, cudaStream_t s, bool begin);
@@ -167,5 +169,7 @@ cudaError_t launch_chunk_grads(const ChunkBwdArgs& a, cudaStream_t s);  // part 
 bool scan_tc_applies(int bf16_operands, int DK, int DV);
 cudaError_t launch_scan_fwd_tc(const ChunkFwdArgs& a, cudaStream_t s);
 cudaError_t launch_scan_bwd_tc(const ChunkBwdArgs& a, cudaStream_t s);
+// The single-token decode kernel (decode.cu), used by launch_recurrent when T == 1.
+cudaError_t launch_decode(const RecurrentArgs& a, cudaStream_t s);
 
 }  // namespace gdn

@@ -22,10 +22,11 @@ constexpr int REC_COLS = 32;                 // value columns per CTA
 constexpr int REC_VEC = 4;                   // value columns per thread
 constexpr int REC_TPC = 16;                  // threads sharing a column group
 constexpr int REC_THREADS = (REC_COLS / REC_VEC) * REC_TPC;  // 128
-constexpr int TB = 8;                        // tokens per staged batch (static smem <= 48 KB)
+// Tokens per staged batch: 8 for prefill (static smem <= 48 KB); 1 for single-token
+// decode, which keeps the CTA's shared memory to a few KB so that 16 CTAs (the thread
+// limit) share an SM and the state loads of many CTAs are in flight at once.
 
-
-template <class T, int DK>
+template <class T, int DK, int TB>
 struct RecSmem {
   T q[2][TB][DK];
   T k[2][TB][DK];
@@ -36,10 +37,10 @@ struct RecSmem {
   float beta[2][TB];
 };
 
-template <class T, int DK, bool PC>
+template <class T, int DK, bool PC, int TB>
 __global__ void __launch_bounds__(REC_THREADS) recurrent_kernel(RecurrentArgs p) {
   constexpr int RPT = DK / REC_TPC;  // key rows per thread
-  __shared__ __align__(16) RecSmem<T, DK> sm;
+  __shared__ __align__(16) RecSmem<T, DK, TB> sm;
   const int tid = threadIdx.x;
   const int cg = tid / REC_TPC;    // column group 0..7
   const int part = tid % REC_TPC;  // row interleave 0..15
@@ -168,14 +169,22 @@ __global__ void __launch_bounds__(REC_THREADS) recurrent_kernel(RecurrentArgs p)
   }
 }
 
+template <class T, int DK, int TB>
+void launch_rec_tb(const RecurrentArgs& a, cudaStream_t s) {
+  dim3 grid(a.DV / REC_COLS, a.B * a.H);
+  if (a.per_channel)
+    recurrent_kernel<T, DK, true, TB><<<grid, REC_THREADS, 0, s>>>(a);
+  else
+    recurrent_kernel<T, DK, false, TB><<<grid, REC_THREADS, 0, s>>>(a);
+}
+
 template <class T, int DK>
 cudaError_t launch_rec_t(const RecurrentArgs& a, cudaStream_t s) {
-  dim3 grid(a.DV / REC_COLS, a.B * a.H);
   prof_mark(K_RECURRENT, s, true);
-  if (a.per_channel)
-    recurrent_kernel<T, DK, true><<<grid, REC_THREADS, 0, s>>>(a);
+  if (a.T == 1)
+    launch_rec_tb<T, DK, 1>(a, s);
   else
-    recurrent_kernel<T, DK, false><<<grid, REC_THREADS, 0, s>>>(a);
+    launch_rec_tb<T, DK, 8>(a, s);
   prof_mark(K_RECURRENT, s, false);
   return cudaGetLastError();
 }
@@ -184,6 +193,7 @@ cudaError_t launch_rec_t(const RecurrentArgs& a, cudaStream_t s) {
 
 cudaError_t launch_recurrent(const RecurrentArgs& a, cudaStream_t s) {
   if (a.B * a.H == 0) return cudaSuccess;
+  if (a.T == 1) return launch_decode(a, s);  // same arithmetic, shaped for one token
   if (a.bf16) return a.DK == 64 ? launch_rec_t<bf16, 64>(a, s) : launch_rec_t<bf16, 128>(a, s);
   return a.DK == 64 ? launch_rec_t<float, 64>(a, s) : launch_rec_t<float, 128>(a, s);
 }

@@ -192,7 +192,7 @@ int gdn_version(void);
  * products, 4 chunk gradients, 5 recurrent, 6 backward finalisation,
  * 7 chunk outputs, 8 forward state scan on tcgen05 tensor cores, 9 reverse
  * state scan on tcgen05 tensor cores (8 and 9 replace 1 and 2 for bf16
- * operands with Dk = Dv = 128);
+ * operands with Dk = Dv = 128), 10 single-token decode (replaces 5 when T = 1);
  * gdn_kernel_name(id) names them
  * ("" for an unknown id). Not part of the paper's method: instrumentation. */
 int gdn_profile_enable(int on);

@@ -76,6 +76,30 @@ def test_prefill_decode_workload_bitwise_and_parity():
     assert rel(h_full, h_ref) <= TOL["f32"]
 
 
+@pytest.mark.parametrize("dtype,dims,per_channel", [("bf16", (128, 128), True), ("f32", (64, 128), True),
+                                                   ("f32", (128, 64), False), ("bf16", (64, 64), False)])
+def test_single_token_calls_equal_one_call(dtype, dims, per_channel):
+    """A sequence decoded one token per call (the single-token decode kernel, state
+    carried in place) equals one prefill call bitwise, for every head geometry, both
+    gate shapes and both input types; with more heads than SMs each decode CTA takes
+    several heads."""
+    w = WORKLOADS["tiny_fwd"].with_(B=2, T=24, H=100, Dk=dims[0], Dv=dims[1], dtype=dtype,
+                                    g_per_channel=per_channel, h0_std=0.1)
+    d = cuda_inputs(make_inputs(w))
+    out_full, h_full = _run(d)
+    state = d["h0"].clone()
+    outs = []
+    for t in range(w.T):
+        sl = slice(t, t + 1)
+        o, _ = gdn.gdn_recurrent(d["q"][:, sl].contiguous(), d["k"][:, sl].contiguous(), d["v"][:, sl].contiguous(),
+                                 d["g"][:, sl].contiguous(), d["beta"][:, sl].contiguous(), state, h_final=state)
+        outs.append(o)
+    torch.cuda.synchronize()
+    assert torch.equal(torch.cat(outs, 1), out_full)
+    assert torch.equal(state, h_full)
+    assert gdn.gdn_check_device_error() == 0  # no bounded wait ran out
+
+
 def test_in_place_state_carry_and_determinism():
     w = WORKLOADS["recurrent"].with_(B=1, T=100, H=4, h0_std=0.2)
     d = cuda_inputs(make_inputs(w))
