@@ -401,8 +401,8 @@ def e2e_leg(args, host, d, step, outputs, world):
 def decode_leg(dev):
     """Recurrent kernel: decode steps (T = 1) with the state read and written once.
     B2 H48: L2 flushed before every step (a buffer twice the L2 size is read), the
-    kernel timed alone by the library's per-launch events (no host launch gap inside
-    the measurement). B32 H48 (state 201 MB > L2): 30 steps back to back between two
+    kernel timed alone by the library's per-launch events, queued behind a spin
+    kernel so that no host launch gap falls inside the measurement. B32 H48 (state 201 MB > L2): 30 steps back to back between two
     CUDA events. Then the 2048-token prefill of the same geometry."""
     import torch
 
@@ -429,6 +429,9 @@ def decode_leg(dev):
             times = []
             for _ in range(30):
                 flush.sum()
+                # a spin kernel keeps the GPU busy while the host submits the step, so the
+                # library's begin event and the kernel run back to back (no launch gap)
+                torch.cuda._sleep(200_000)
                 gdn.gdn_profile_enable(True)
                 one()
                 prof = gdn.gdn_profile_read()

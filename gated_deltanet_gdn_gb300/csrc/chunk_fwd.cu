@@ -274,6 +274,7 @@ __global__ void __launch_bounds__(PREP_THREADS) chunk_prep_kernel(ChunkFwdArgs a
       eGb[e] = FAST ? __expf(Gb[e]) : 0.f;
       eCb[e] = FAST ? __expf(GC[e] - Gb[e]) : 0.f;
     }
+#pragma unroll 2
     for (int i = tid; i < C * (DK / 4); i += PREP_THREADS) {
       const int r = i / (DK / 4), c0 = cc;
       const bool dead_q = !FAST && r < BLK && unsafe1;  // query rows whose factor may overflow

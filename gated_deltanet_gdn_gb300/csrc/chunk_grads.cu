@@ -129,6 +129,7 @@ __global__ void __launch_bounds__(GR_THREADS, 2) chunk_grads_kernel(ChunkBwdArgs
       cp_async16(dBk.p + i * EPC, s2 + i * EPC);
       cp_async16(dKt.p + i * EPC, s3 + i * EPC);
     }
+    if (tid < HC / 4) cp_async16(gcol_s + 4 * tid, a.ws.dgam + ch * DK + cbase + 4 * tid);  // dgam, scaled below
     const T* sa = static_cast<const T*>(a.ws.daqk) + ch * (C * C);
     const T* sk = static_cast<const T*>(a.ws.dakk) + ch * (C * C);
     for (int i = tid; i < C * C / EPC; i += GR_THREADS) {
@@ -168,7 +169,7 @@ __global__ void __launch_bounds__(GR_THREADS, 2) chunk_grads_kernel(ChunkBwdArgs
   for (int c = tid; c < HC; c += GR_THREADS) {
     u1 |= !(Gat(0, c) - Gat(BLK - 1, c) <= SAFE_SPREAD);
     u2 |= !(Gat(BLK - 1, c) - Gat(C - 1, c) <= SAFE_SPREAD);
-    gcol_s[c] = a.ws.dgam[ch * DK + cbase + c] * __expf(Gat(C - 1, c));
+    gcol_s[c] *= __expf(Gat(C - 1, c));  // dgam * gam
   }
   const bool unsafe1 = __syncthreads_or(u1 || force) != 0;
   const bool unsafe2 = __syncthreads_or(u2 || force) != 0;
@@ -176,6 +177,8 @@ __global__ void __launch_bounds__(GR_THREADS, 2) chunk_grads_kernel(ChunkBwdArgs
   // row-scaled operands, one pass: X = q e1, XB = beta k e1 (query side), Y = k e2 (key side),
   // with e1 = exp(G - G_b), e2 = exp(G_b - G) about the block boundary b
   HTile XBs{reinterpret_cast<T*>(sm + L::XB)};
+  static_assert(C * (HC / 4) % GR_THREADS == 0, "whole passes");
+#pragma unroll
   for (int i = tid; i < C * (HC / 4); i += GR_THREADS) {
     const int r = i / (HC / 4), c0 = (i % (HC / 4)) * 4;
     float kv[4], qv[4], G[4], Gb[4], xq[4], xb[4], yk[4];
