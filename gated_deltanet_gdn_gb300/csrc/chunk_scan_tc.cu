@@ -84,14 +84,15 @@ __device__ __forceinline__ void tmem_ld64(uint32_t taddr, float* v) {
   for (int i = 0; i < 64; ++i) v[i] = __uint_as_float(r[i]);
 }
 
-// S^T row slice (64 fp32 columns of this thread's lane from `col`): write its bf16 copy
-// into the operand tile and put it back into TMEM scaled column-wise by gam.
-__device__ __forceinline__ void state_slice_out(uint32_t taddr, Tile<bf16, TD, TD> Sa, int row, int col,
-                                                const float* gam) {
-  float x[64];
+// S^T row slice (64 fp32 columns of this thread's lane from `col`): load it from TMEM
+// into x and write its bf16 copy into the operand tile.
+__device__ __forceinline__ void state_copy_out(uint32_t taddr, Tile<bf16, TD, TD> Sa, int row, int col, float* x) {
   tmem_ld64(taddr, x);
   store_row32(Sa, row, col, x);
   store_row32(Sa, row, col + 32, x + 32);
+}
+// Put the slice back into TMEM scaled column-wise by gam (the decay of the state).
+__device__ __forceinline__ void state_scale_back(uint32_t taddr, int col, const float* gam, float* x) {
 #pragma unroll
   for (int i = 0; i < 64; i += 4) {
     const float4 g = *reinterpret_cast<const float4*>(gam + col + i);
@@ -224,8 +225,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_scan_fwd_tc_kernel(ChunkF
       tc_fence_after();
     }
     mbar_wait(&full[s], (uint32_t)(n / L::STAGES) & 1u, a.err);
-    // S^T -> bf16 operand (the chunk-start state record); S^T <- S^T diag(gam)
-    state_slice_out(tl + 64 * half, Sa, row, 64 * half, reinterpret_cast<const float*>(st + L::GAM));
+    // S^T -> bf16 operand (the chunk-start state record)
+    float xs[64];
+    state_copy_out(tl + 64 * half, Sa, row, 64 * half, xs);
     fence_proxy_async();
     tc_fence_before();
     compute_sync();
@@ -239,6 +241,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_scan_fwd_tc_kernel(ChunkF
         umma_bf16(tm + 128, kstep_k(dSa, ks, PANEL_D), kstep_k(dW, ks, PANEL_C), id_1, ks > 0);
       umma_commit_to(bar_u);
     }
+    // S^T <- S^T diag(gam) while the tensor cores form U^T (the S^T update comes after
+    // the next barrier)
+    state_scale_back(tl + 64 * half, 64 * half, reinterpret_cast<const float*>(st + L::GAM), xs);
     mbar_wait(bar_u, ph_u, a.err);
     ph_u ^= 1u;
     tc_fence_after();
@@ -408,8 +413,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       tc_fence_after();
     }
     mbar_wait(&full[s], (uint32_t)(it / L::STAGES) & 1u, a.err);
-    // dS^T -> bf16 operand (the record of the gradient leaving chunk n); scale by gam
-    state_slice_out(tl + 64 * half, Sa, row, 64 * half, gams + s * TD);
+    // dS^T -> bf16 operand (the record of the gradient leaving chunk n)
+    float xs[64];
+    state_copy_out(tl + 64 * half, Sa, row, 64 * half, xs);
     fence_proxy_async();
     tc_fence_before();
     if (tid == 0) bulk_wait_read0();  // the previous dU record store has read Ua
@@ -420,16 +426,17 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       bulk_commit();
       const uint64_t dSa = desc_k(Sa.p);
       const uint64_t dDo = desc_mn(st + L::DO, PANEL_C), dAq = desc_mn(st + L::AQK, PANEL_C);
-      const uint64_t dKt = desc_k(st + L::KT), dQh = desc_mn(st + L::QH, PANEL_C);
+      const uint64_t dKt = desc_k(st + L::KT);
 #pragma unroll
       for (int ks = 0; ks < C / 16; ++ks) umma_bf16(tm + 128, kstep_mn(dDo, ks), kstep_mn(dAq, ks), id_a, ks > 0);
 #pragma unroll
       for (int ks = 0; ks < TD / 16; ++ks)
         umma_bf16(tm + 128, kstep_k(dSa, ks, PANEL_D), kstep_k(dKt, ks, PANEL_C), id_b, 1u);
       umma_commit_to(bar_u);
-#pragma unroll
-      for (int ks = 0; ks < C / 16; ++ks) umma_bf16(tm, kstep_mn(dDo, ks), kstep_mn(dQh, ks), id_c, 1u);
     }
+    // dS^T <- dS^T diag(gam) while the tensor cores form dU^T; every product into dS^T
+    // comes after the next barrier
+    state_scale_back(tl + 64 * half, 64 * half, gams + s * TD, xs);
     mbar_wait(bar_u, ph_u, a.err);
     ph_u ^= 1u;
     tc_fence_after();
@@ -448,6 +455,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       bulk_s2g(du_rec + ch * (C * TD), Ua.p, C * TD * 2);
       bulk_commit();
       const uint64_t dW = desc_mn(st + L::W, PANEL_C), dUa = desc_k(Ua.p);
+      const uint64_t dDo = desc_mn(st + L::DO, PANEL_C), dQh = desc_mn(st + L::QH, PANEL_C);
+#pragma unroll
+      for (int ks = 0; ks < C / 16; ++ks) umma_bf16(tm, kstep_mn(dDo, ks), kstep_mn(dQh, ks), id_c, 1u);
 #pragma unroll
       for (int ks = 0; ks < C / 16; ++ks) umma_bf16(tm, kstep_k(dUa, ks, PANEL_D), kstep_mn(dW, ks), id_d, 1u);
       umma_commit_to(&empty[s]);
