@@ -15,7 +15,8 @@ Contents
 
 Parity status: both entry points are pinned by tests in
 ``tests/test_oracle_pins.py`` (closed forms, gate semantics, the decay
-factorisation worked example, finite differences, brute force).
+factorisation worked example, finite differences, brute force), the optional
+q/k L2 normalisation by finite differences and its scale invariance.
 """
 from __future__ import annotations
 
@@ -75,9 +76,37 @@ def _c64(a):
     return np.ascontiguousarray(np.asarray(a, dtype=np.float64))
 
 
-def fwd(q, k, v, g, beta, h0=None, scale: Optional[float] = None, nthreads: int = 0):
+# The "gated-deltanet" kernel card (sections Usage and Correctness) offers an
+# in-kernel L2 normalisation of q and k (use_qk_l2norm) without stating its
+# guard for a zero vector; this oracle takes x / sqrt(sum_c x_c^2 + eps) per
+# (token, head) with eps = 1e-6.
+QK_L2NORM_EPS = 1e-6
+
+
+def l2norm(x, eps: float = QK_L2NORM_EPS):
+    """x / sqrt(sum over the last axis of x^2 + eps), float64."""
+    x = np.asarray(x, dtype=np.float64)
+    return x / np.sqrt(np.sum(x * x, axis=-1, keepdims=True) + eps)
+
+
+def l2norm_backward(x, dxhat, eps: float = QK_L2NORM_EPS):
+    """Gradient with respect to x of the normalisation above, given the gradient
+    dxhat with respect to its output: with r = (|x|^2 + eps)^(-1/2) and
+    xhat = r x, dx = r (dxhat - xhat <xhat, dxhat>)."""
+    x = np.asarray(x, dtype=np.float64)
+    dxhat = np.asarray(dxhat, dtype=np.float64)
+    r = 1.0 / np.sqrt(np.sum(x * x, axis=-1, keepdims=True) + eps)
+    xhat = x * r
+    return r * (dxhat - xhat * np.sum(xhat * dxhat, axis=-1, keepdims=True))
+
+
+def fwd(q, k, v, g, beta, h0=None, scale: Optional[float] = None, nthreads: int = 0,
+        qk_l2norm: bool = False):
     """Token-serial forward. Arrays as in the C ABI layouts, any float dtype
-    (converted to float64). Returns (out [B,T,H,Dv], h_final [B,H,Dk,Dv])."""
+    (converted to float64). With qk_l2norm, q and k are first normalised per
+    (token, head) by ``l2norm``. Returns (out [B,T,H,Dv], h_final [B,H,Dk,Dv])."""
+    if qk_l2norm:
+        q, k = l2norm(q), l2norm(k)
     q, k, v, g, beta, h0 = map(_c64, (q, k, v, g, beta, h0))
     B, T, H, Dk = q.shape
     Dv = v.shape[-1]
@@ -95,8 +124,16 @@ def fwd(q, k, v, g, beta, h0=None, scale: Optional[float] = None, nthreads: int 
 
 
 def bwd(q, k, v, g, beta, h0, dout, dh_final=None, scale: Optional[float] = None,
-        nthreads: int = 0) -> Dict[str, np.ndarray]:
-    """Hand-derived reverse pass. Returns dq, dk, dv, dg, dbeta, dh0."""
+        nthreads: int = 0, qk_l2norm: bool = False) -> Dict[str, np.ndarray]:
+    """Hand-derived reverse pass. Returns dq, dk, dv, dg, dbeta, dh0. With
+    qk_l2norm the reverse pass runs on the normalised q, k and dq, dk are then
+    taken back through ``l2norm_backward``."""
+    if qk_l2norm:
+        q_raw, k_raw = _c64(q), _c64(k)
+        res = bwd(l2norm(q_raw), l2norm(k_raw), v, g, beta, h0, dout, dh_final, scale, nthreads)
+        res["dq"] = l2norm_backward(q_raw, res["dq"])
+        res["dk"] = l2norm_backward(k_raw, res["dk"])
+        return res
     q, k, v, g, beta, h0, dout, dh_final = map(_c64, (q, k, v, g, beta, h0, dout, dh_final))
     B, T, H, Dk = q.shape
     Dv = v.shape[-1]

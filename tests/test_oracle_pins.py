@@ -266,6 +266,56 @@ def test_reverse_pass_matches_finite_differences(per_channel):
         assert err < 1e-6, (name, err)
 
 
+def test_qk_l2norm_reverse_pass_matches_finite_differences():
+    """With the q/k L2 normalisation, the gradients of q and k (taken back through the
+    normalisation) match central differences of the normalised forward."""
+    rng = np.random.default_rng(21)
+    q, k, v, g, beta, S0 = _rand_problem(rng, B=1, T=6, H=1, Dk=4, Dv=3, per_channel=True, norm=False)
+    dO = rng.standard_normal(v.shape)
+    dhT = rng.standard_normal(S0.shape)
+    grads = oracle.bwd(q, k, v, g, beta, S0, dO, dhT, scale=0.7, qk_l2norm=True)
+
+    def loss():
+        out, hT = oracle.fwd(q, k, v, g, beta, S0, scale=0.7, qk_l2norm=True)
+        return float(np.sum(out * dO) + np.sum(hT * dhT))
+
+    eps = 1e-6
+    for arr, name in ((q, "dq"), (k, "dk"), (v, "dv"), (g, "dg"), (beta, "dbeta")):
+        fd = np.zeros_like(arr)
+        it = np.nditer(arr, flags=["multi_index"])
+        for _ in it:
+            idx = it.multi_index
+            orig = arr[idx]
+            arr[idx] = orig + eps
+            lp = loss()
+            arr[idx] = orig - eps
+            lm = loss()
+            arr[idx] = orig
+            fd[idx] = (lp - lm) / (2 * eps)
+        err = np.linalg.norm(grads[name] - fd) / max(np.linalg.norm(fd), 1e-30)
+        assert err < 1e-6, (name, err)
+
+
+def test_qk_l2norm_is_scale_invariant_and_unit_rows_pass_through():
+    """Scaling each q and k row by a positive factor does not change the normalised
+    forward (up to the eps guard); rows that already have unit norm give the same
+    result with or without the normalisation; a zero row stays zero."""
+    rng = np.random.default_rng(22)
+    q, k, v, g, beta, S0 = _rand_problem(rng, B=1, T=20, H=2, Dk=8, Dv=5, per_channel=False, norm=False)
+    o1, h1 = oracle.fwd(q, k, v, g, beta, S0, qk_l2norm=True)
+    cq = rng.uniform(0.5, 3.0, q.shape[:-1] + (1,))
+    ck = rng.uniform(0.5, 3.0, k.shape[:-1] + (1,))
+    o2, h2 = oracle.fwd(q * cq, k * ck, v, g, beta, S0, qk_l2norm=True)
+    assert oracle.rel_l2(o2, o1) < 1e-5 and oracle.rel_l2(h2, h1) < 1e-5
+    qu = q / np.linalg.norm(q, axis=-1, keepdims=True)
+    ku = k / np.linalg.norm(k, axis=-1, keepdims=True)
+    o3, h3 = oracle.fwd(qu, ku, v, g, beta, S0)
+    o4, h4 = oracle.fwd(qu, ku, v, g, beta, S0, qk_l2norm=True)
+    assert oracle.rel_l2(o4, o3) < 1e-5 and oracle.rel_l2(h4, h3) < 1e-5
+    z = np.zeros((2, 8))
+    assert np.array_equal(oracle.l2norm(z), z)
+
+
 def test_reverse_pass_chunk_split_consistency():
     """The reverse pass of a sequence equals the reverse passes of its two halves
     chained through dh (the segment checkpointing must not leak)."""
