@@ -26,6 +26,7 @@ GDN_NOALLOC_SCRATCH_BYTES = 32 << 20
 GDN_F32 = 0
 GDN_BF16 = 1
 GDN_FLAG_PAIRWISE_WITHIN_BLOCK = 1
+GDN_FLAG_QK_L2NORM = 2
 GDN_CHUNK = 64
 
 # every symbol include/gdn.h declares
@@ -33,7 +34,7 @@ EXPORTED = ("gdn_chunk_residual_bytes", "gdn_chunk_bwd_workspace_bytes", "gdn_ch
             "gdn_chunk_bwd", "gdn_recurrent", "gdn_check_device_error", "gdn_status_string",
             "gdn_version", "gdn_profile_enable", "gdn_profile_read", "gdn_kernel_name",
             "gdn_chunk_fwd_noalloc")
-KERNEL_COUNT = 11
+KERNEL_COUNT = 13
 
 
 class GdnDims(ctypes.Structure):
@@ -220,11 +221,11 @@ def gdn_chunk_bwd(q, k, v, g, beta, h0, residuals, dout, dh_final=None,
 
 
 def gdn_recurrent(q, k, v, g, beta, h0=None, scale: Optional[float] = None, *, out=None,
-                  h_final=None) -> Tuple[torch.Tensor, torch.Tensor]:
+                  h_final=None, flags: int = 0) -> Tuple[torch.Tensor, torch.Tensor]:
     """Token-recurrent prefill / decode. h_final may be h0 (in-place carry)."""
     dev = q.device
     _require(dict(q=q, k=k, v=v, g=g, beta=beta, h0=h0, out=out, h_final=h_final), dev)
-    dims = make_dims(q, v, g)
+    dims = make_dims(q, v, g, flags)
     if scale is None:
         scale = dims.Dk ** -0.5
     if out is None:

@@ -41,7 +41,7 @@ int check_dims(const gdn_dims* d, bool chunked) {
   if (d->dtype != GDN_F32 && d->dtype != GDN_BF16) return GDN_ERR_UNSUPPORTED;
   if ((d->Dk != 64 && d->Dk != 128) || (d->Dv != 64 && d->Dv != 128)) return GDN_ERR_UNSUPPORTED;
   if ((long long)d->B * d->H > 65535) return GDN_ERR_UNSUPPORTED;  // grid y limit
-  if (d->flags & ~GDN_FLAG_PAIRWISE_WITHIN_BLOCK) return GDN_ERR_INVALID_ARG;
+  if (d->flags & ~(GDN_FLAG_PAIRWISE_WITHIN_BLOCK | GDN_FLAG_QK_L2NORM)) return GDN_ERR_INVALID_ARG;
   if (chunked && d->Dk != d->Dv) return GDN_ERR_UNSUPPORTED;
   if (chunked && d->T % GDN_CHUNK != 0) return GDN_ERR_SHAPE;
   return GDN_OK;
@@ -55,8 +55,10 @@ bool optional_ok(const void* p) { return !p || aligned(p, 16); }
 // [B,T,H] gates: element alignment only.
 bool gate_ok(const void* p, bool has_work, int es) { return !has_work || (p && aligned(p, es)); }
 
+bool qk_norm(const gdn_dims* d) { return (d->flags & GDN_FLAG_QK_L2NORM) != 0; }
+
 ResidualPtrs residual_ptrs(const gdn_dims* d, void* base) {
-  const ResidualLayout L = residual_layout(d->B, d->T, d->H, d->Dk, d->Dv, esize(d));
+  const ResidualLayout L = residual_layout(d->B, d->T, d->H, d->Dk, d->Dv, esize(d), qk_norm(d));
   char* b = static_cast<char*>(base);
   ResidualPtrs r;
   r.aqk = b + L.aqk;
@@ -68,6 +70,12 @@ ResidualPtrs residual_ptrs(const gdn_dims* d, void* base) {
   r.gam = reinterpret_cast<float*>(b + L.gam);
   r.state = b + L.state;
   r.u = b + L.u;
+  if (qk_norm(d)) {
+    r.qn = b + L.qn;
+    r.kn = b + L.kn;
+    r.qinv = reinterpret_cast<float*>(b + L.qinv);
+    r.kinv = reinterpret_cast<float*>(b + L.kinv);
+  }
   return r;
 }
 
@@ -107,7 +115,7 @@ const char* kKernelNames[K_COUNT] = {"chunk_prep_kernel",    "chunk_scan_fwd_ker
                                      "chunk_grads_kernel",    "recurrent_kernel",
                                      "chunk_bwd_finalize_kernel", "chunk_out_kernel",
                                      "chunk_scan_fwd_tc_kernel", "chunk_scan_bwd_tc_kernel",
-                                     "decode_kernel"};
+                                     "decode_kernel", "l2norm_rows_kernel", "l2norm_bwd_kernel"};
 
 }  // namespace
 
@@ -140,7 +148,7 @@ extern "C" {
 
 size_t gdn_chunk_residual_bytes(const gdn_dims* d) {
   if (check_dims(d, true) != GDN_OK) return 0;
-  return residual_layout(d->B, d->T, d->H, d->Dk, d->Dv, esize(d)).total;
+  return residual_layout(d->B, d->T, d->H, d->Dk, d->Dv, esize(d), qk_norm(d)).total;
 }
 
 size_t gdn_chunk_bwd_workspace_bytes(const gdn_dims* d) {
@@ -173,7 +181,15 @@ int gdn_chunk_fwd(const gdn_dims* d, const void* q, const void* k, const void* v
   if (residuals) a.res = residual_ptrs(d, residuals);
   a.err = device_error_word();
   if (!a.err) return GDN_ERR_CUDA;
-  return launch_status(launch_chunk_fwd(a, static_cast<cudaStream_t>(stream)));
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (qk_norm(d) && work) {  // every chunk kernel reads the normalised rows
+    const cudaError_t e = launch_l2norm_rows(q, k, a.res.qn, a.res.kn, a.res.qinv, a.res.kinv,
+                                             (size_t)d->B * d->T * d->H, d->Dk, a.bf16, s);
+    if (e != cudaSuccess) return launch_status(e);
+    a.q = a.res.qn;
+    a.k = a.res.kn;
+  }
+  return launch_status(launch_chunk_fwd(a, s));
 }
 
 int gdn_chunk_bwd(const gdn_dims* d, const void* q, const void* k, const void* v, const void* g,
@@ -210,7 +226,17 @@ int gdn_chunk_bwd(const gdn_dims* d, const void* q, const void* k, const void* v
   if (workspace) a.ws = workspace_ptrs(d, workspace);
   a.err = device_error_word();
   if (!a.err) return GDN_ERR_CUDA;
-  return launch_status(launch_chunk_bwd(a, static_cast<cudaStream_t>(stream)));
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const bool norm = qk_norm(d) && work;
+  if (norm) {  // the gradients come out with respect to the normalised rows first
+    a.q = a.res.qn;
+    a.k = a.res.kn;
+  }
+  cudaError_t e = launch_chunk_bwd(a, s);
+  if (e == cudaSuccess && norm)
+    e = launch_l2norm_bwd(dq, dk, a.res.qn, a.res.kn, a.res.qinv, a.res.kinv, (size_t)d->B * d->T * d->H, d->Dk,
+                          1, s);
+  return launch_status(e);
 }
 
 int gdn_recurrent(const gdn_dims* d, const void* q, const void* k, const void* v, const void* g,
@@ -232,6 +258,7 @@ int gdn_recurrent(const gdn_dims* d, const void* q, const void* k, const void* v
   a.B = d->B; a.T = d->T; a.H = d->H; a.DK = d->Dk; a.DV = d->Dv;
   a.per_channel = d->g_per_channel ? 1 : 0;
   a.bf16 = d->dtype == GDN_BF16;
+  a.qk_norm = qk_norm(d) ? 1 : 0;
   a.q = q; a.k = k; a.v = v; a.g = g; a.beta = beta; a.h0 = h0; a.scale = scale;
   a.out = out; a.h_final = h_final;
   a.err = device_error_word();

@@ -36,6 +36,26 @@ struct BoolTag {
   static constexpr bool value = B;
 };
 
+// q/k L2 normalisation: the guard added to the sum of squares.
+constexpr float QK_NORM_EPS = 1e-6f;
+
+// Inverse L2 norm 1 / sqrt(sum_c x_c^2 + QK_NORM_EPS) of a row x[0 .. N-1] (N a multiple
+// of 32), read by one full warp: lane l sums x[l + 32 j]^2 over ascending j with fmaf,
+// then the lanes are added by a butterfly (xor 16, 8, 4, 2, 1). Every kernel that
+// normalises q or k uses this one definition, so they agree bitwise.
+template <int N, class T>
+__device__ __forceinline__ float warp_row_inv_norm(const T* x, int lane) {
+  float s = 0.f;
+#pragma unroll
+  for (int j = 0; j < N / 32; ++j) {
+    const float v = to_f32(x[lane + 32 * j]);
+    s = fmaf(v, v, s);
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
+  return rsqrtf(s + QK_NORM_EPS);
+}
+
 // ------------------------------------------------------------------ swizzled tiles
 // A ROWS x COLS tile of T stored as column panels of 128 bytes (fewer when a row is
 // shorter). Inside a panel, row r occupies PANB bytes and the 16-byte chunk index is

@@ -37,7 +37,8 @@ struct DecLayout {
   static constexpr int STAGES = 3;
   static constexpr int RED = STAGES * STAGE;           // float [2][4][DV]: pv and ov partials
   static constexpr int A = RED + 2 * 4 * DV * 4;       // float [DK] exp(g)
-  static constexpr int BAR = A + DK * 4;               // full[STAGES], computed[STAGES]
+  static constexpr int NINV = A + DK * 4;              // float [2]: q, k inverse norms
+  static constexpr int BAR = NINV + 16;                // full[STAGES], computed[STAGES]
   static constexpr int BYTES = BAR + 16 * STAGES;
   static constexpr int COMPUTE = DV / 4 * 16;          // threads: 4 columns x 16 row parts each
   static constexpr int THREADS = COMPUTE + 32;         // + the producer warp
@@ -58,6 +59,7 @@ __global__ void __launch_bounds__(DecLayout<T, DK, DV>::THREADS, 1) decode_kerne
   uint64_t* computed = full + L::STAGES;
   float* red = reinterpret_cast<float*>(sm + L::RED);
   float* aexp = reinterpret_cast<float*>(sm + L::A);
+  float* ninv = reinterpret_cast<float*>(sm + L::NINV);
   const int nunits = (BH - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x;  // heads of this CTA
 
   if (tid == 0) {
@@ -122,11 +124,18 @@ __global__ void __launch_bounds__(DecLayout<T, DK, DV>::THREADS, 1) decode_kerne
     const float bt = to_f32(beta[row]);
     const float as = PC ? 1.f : expf(to_f32(g[row]));
     mbar_wait(&full[s], (uint32_t)(m / L::STAGES) & 1u, p.err);
-    if (PC) {
-      const T* gs = reinterpret_cast<const T*>(st + L::G);
-      for (int c = tid; c < DK; c += L::COMPUTE) aexp[c] = expf(to_f32(gs[c]));
+    if (PC || p.qk_norm) {
+      if (PC) {
+        const T* gs = reinterpret_cast<const T*>(st + L::G);
+        for (int c = tid; c < DK; c += L::COMPUTE) aexp[c] = expf(to_f32(gs[c]));
+      }
+      if (p.qk_norm && warp < 2) {  // warp 0: the q row, warp 1: the k row
+        const float inv = warp_row_inv_norm<DK>(warp ? ks : qs, lane);
+        if (lane == 0) ninv[warp] = inv;
+      }
       decode_sync(L::COMPUTE);
     }
+    const float nq = p.qk_norm ? ninv[0] : 1.f, nk = p.qk_norm ? ninv[1] : 1.f;
     float S[RPT][4];
     float pv[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
@@ -139,7 +148,7 @@ __global__ void __launch_bounds__(DecLayout<T, DK, DV>::THREADS, 1) decode_kerne
         S[i][0] = S[i][1] = S[i][2] = S[i][3] = 0.f;
       }
       const float a = PC ? aexp[r] : as;
-      const float kr = to_f32(ks[r]);
+      const float kr = to_f32(ks[r]) * nk;
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         S[i][e] *= a;
@@ -169,8 +178,8 @@ __global__ void __launch_bounds__(DecLayout<T, DK, DV>::THREADS, 1) decode_kerne
 #pragma unroll
     for (int i = 0; i < RPT; ++i) {
       const int r = part + 16 * i;
-      const float kr = to_f32(ks[r]);
-      const float qr = to_f32(qs[r]);
+      const float kr = to_f32(ks[r]) * nk;
+      const float qr = to_f32(qs[r]) * nq;
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         S[i][e] = fmaf(kr, d[e], S[i][e]);

@@ -20,8 +20,9 @@ constexpr float SAFE_SPREAD = 80.f;  // max decay spread (nats) for row-scaled i
 // S^T [Dv][Dk] and U^T [Dv][C]. The backward's dS and dU records are likewise
 // dS^T [Dv][Dk] and dU^T [Dv][C].
 struct ResidualLayout {
-  // region base offsets in bytes from the residual pointer
-  size_t aqk, tmat, wneg, up, qh, kt, gam, state, u, total;
+  // region base offsets in bytes from the residual pointer (qn, kn, qinv, kinv: only with
+  // the q/k L2 normalisation, the normalised rows and their inverse norms)
+  size_t aqk, tmat, wneg, up, qh, kt, gam, state, u, qn, kn, qinv, kinv, total;
   // bytes of one chunk-head record
   size_t aqk_b, tmat_b, w_b, up_b, qh_b, kt_b, gam_b, state_b, u_b;
 };
@@ -33,7 +34,7 @@ struct BwdWorkspaceLayout {
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-inline ResidualLayout residual_layout(int B, int T, int H, int DK, int DV, int es) {
+inline ResidualLayout residual_layout(int B, int T, int H, int DK, int DV, int es, bool qk_norm = false) {
   ResidualLayout L{};
   const size_t n = (size_t)B * H * (T / C);
   L.aqk_b = (size_t)C * C * es;
@@ -59,6 +60,17 @@ inline ResidualLayout residual_layout(int B, int T, int H, int DK, int DV, int e
   put(L.gam, L.gam_b);
   put(L.state, L.state_b);
   put(L.u, L.u_b);
+  if (qk_norm) {
+    const size_t rows = (size_t)B * T * H;
+    L.qn = off;
+    off = align_up(off + (size_t)DK * es * rows, 1024);
+    L.kn = off;
+    off = align_up(off + (size_t)DK * es * rows, 1024);
+    L.qinv = off;
+    off = align_up(off + rows * 4, 1024);
+    L.kinv = off;
+    off = align_up(off + rows * 4, 1024);
+  }
   L.total = off;
   return L;
 }
@@ -102,6 +114,8 @@ struct ResidualPtrs {
   void *aqk, *tmat, *wneg, *up, *qh, *kt;
   float* gam;
   void *state, *u;
+  void *qn, *kn;  // normalised q, k rows (q/k L2 normalisation only)
+  float *qinv, *kinv;
 };
 struct BwdWorkspacePtrs {
   void *du, *dstate, *dqh, *dbk, *dkt, *daqk, *dakk;
@@ -133,7 +147,7 @@ struct ChunkBwdArgs {
 };
 
 struct RecurrentArgs {
-  int B, T, H, DK, DV, per_channel, bf16;
+  int B, T, H, DK, DV, per_channel, bf16, qk_norm;
   const void *q, *k, *v, *g, *beta;
   const float* h0;
   float scale;
@@ -155,7 +169,9 @@ enum KernelId {
   K_SCAN_FWD_TC = 8,  // chunk_scan_fwd_tc_kernel
   K_SCAN_BWD_TC = 9,  // chunk_scan_bwd_tc_kernel
   K_DECODE = 10,      // decode_kernel
-  K_COUNT = 11
+  K_L2NORM = 11,      // l2norm_rows_kernel
+  K_L2NORM_BWD = 12,  // l2norm_bwd_kernel
+  K_COUNT = 13
 };
 // Records a CUDA event on s before (begin = true) or after a launch when timing is on.
 void prof_mark(KernelId id, cudaStream_t s, bool begin);
@@ -171,5 +187,10 @@ cudaError_t launch_scan_fwd_tc(const ChunkFwdArgs& a, cudaStream_t s);
 cudaError_t launch_scan_bwd_tc(const ChunkBwdArgs& a, cudaStream_t s);
 // The single-token decode kernel (decode.cu), used by launch_recurrent when T == 1.
 cudaError_t launch_decode(const RecurrentArgs& a, cudaStream_t s);
+// q/k L2 normalisation for the chunked path (l2norm.cu): rows = B * T * H.
+cudaError_t launch_l2norm_rows(const void* q, const void* k, void* qn, void* kn, float* qinv, float* kinv,
+                               size_t rows, int DK, int bf16, cudaStream_t s);
+cudaError_t launch_l2norm_bwd(void* dq, void* dk, const void* qn, const void* kn, const float* qinv,
+                              const float* kinv, size_t rows, int DK, int bf16, cudaStream_t s);
 
 }  // namespace gdn

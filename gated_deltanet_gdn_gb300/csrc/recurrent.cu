@@ -22,9 +22,7 @@ constexpr int REC_COLS = 32;                 // value columns per CTA
 constexpr int REC_VEC = 4;                   // value columns per thread
 constexpr int REC_TPC = 16;                  // threads sharing a column group
 constexpr int REC_THREADS = (REC_COLS / REC_VEC) * REC_TPC;  // 128
-// Tokens per staged batch: 8 for prefill (static smem <= 48 KB); 1 for single-token
-// decode, which keeps the CTA's shared memory to a few KB so that 16 CTAs (the thread
-// limit) share an SM and the state loads of many CTAs are in flight at once.
+// Tokens per staged batch (TB): 8 (static smem <= 48 KB).
 
 template <class T, int DK, int TB>
 struct RecSmem {
@@ -35,6 +33,7 @@ struct RecSmem {
   float a[TB][DK];    // exp(g) of the batch being computed
   float gs[2][TB];
   float beta[2][TB];
+  float inv[2][TB];   // q/k L2 normalisation: inverse norms of the batch's q and k rows
 };
 
 template <class T, int DK, bool PC, int TB>
@@ -101,22 +100,31 @@ __global__ void __launch_bounds__(REC_THREADS) recurrent_kernel(RecurrentArgs p)
     cp_async_wait<0>();
     __syncthreads();  // batch bi visible; everyone finished batch bi-1 (its buffer is free)
     if (bi + 1 < nbatch) stage(buf ^ 1, t0 + TB);
-    if (PC) {
-      for (int i = tid; i < nt * DK; i += REC_THREADS) {
-        const int tt = i / DK, c = i % DK;
-        sm.a[tt][c] = expf(to_f32(sm.graw[buf][tt][c]));
+    if (PC || p.qk_norm) {
+      if (PC)
+        for (int i = tid; i < nt * DK; i += REC_THREADS) {
+          const int tt = i / DK, c = i % DK;
+          sm.a[tt][c] = expf(to_f32(sm.graw[buf][tt][c]));
+        }
+      if (p.qk_norm) {  // one warp per q or k row of the batch
+        const int warp = tid >> 5, lane = tid & 31;
+        for (int rr = warp; rr < 2 * nt; rr += REC_THREADS / 32) {
+          const float inv = warp_row_inv_norm<DK>((rr & 1) ? sm.k[buf][rr >> 1] : sm.q[buf][rr >> 1], lane);
+          if (lane == 0) sm.inv[rr & 1][rr >> 1] = inv;
+        }
       }
       __syncthreads();
     }
     for (int tt = 0; tt < nt; ++tt) {
       const float bt = sm.beta[buf][tt];
       const float as = PC ? 1.f : expf(sm.gs[buf][tt]);
+      const float nq = p.qk_norm ? sm.inv[0][tt] : 1.f, nk = p.qk_norm ? sm.inv[1][tt] : 1.f;
       float pv[REC_VEC] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int i = 0; i < RPT; ++i) {
         const int r = part + REC_TPC * i;
         const float a = PC ? sm.a[tt][r] : as;
-        const float kr = to_f32(sm.k[buf][tt][r]);
+        const float kr = to_f32(sm.k[buf][tt][r]) * nk;
 #pragma unroll
         for (int j = 0; j < REC_VEC; ++j) {
           S[i][j] *= a;
@@ -134,8 +142,8 @@ __global__ void __launch_bounds__(REC_THREADS) recurrent_kernel(RecurrentArgs p)
 #pragma unroll
       for (int i = 0; i < RPT; ++i) {
         const int r = part + REC_TPC * i;
-        const float kr = to_f32(sm.k[buf][tt][r]);
-        const float qr = to_f32(sm.q[buf][tt][r]);
+        const float kr = to_f32(sm.k[buf][tt][r]) * nk;
+        const float qr = to_f32(sm.q[buf][tt][r]) * nq;
 #pragma unroll
         for (int j = 0; j < REC_VEC; ++j) {
           S[i][j] = fmaf(kr, d[j], S[i][j]);
@@ -181,10 +189,7 @@ void launch_rec_tb(const RecurrentArgs& a, cudaStream_t s) {
 template <class T, int DK>
 cudaError_t launch_rec_t(const RecurrentArgs& a, cudaStream_t s) {
   prof_mark(K_RECURRENT, s, true);
-  if (a.T == 1)
-    launch_rec_tb<T, DK, 1>(a, s);
-  else
-    launch_rec_tb<T, DK, 8>(a, s);
+  launch_rec_tb<T, DK, 8>(a, s);  // single-token calls go to decode_kernel (decode.cu)
   prof_mark(K_RECURRENT, s, false);
   return cudaGetLastError();
 }

@@ -80,6 +80,15 @@ typedef enum { GDN_F32 = 0, GDN_BF16 = 1 } gdn_dtype;
  * does so by itself for any block whose decay spread makes the row scaling
  * leave the safe exponent range). Results agree to rounding. */
 #define GDN_FLAG_PAIRWISE_WITHIN_BLOCK 1
+/* q and k are L2-normalised per (token, head) before the rule sees them, the
+ * use_qk_l2norm option of the "gated-deltanet" kernel card (sections Usage and
+ * Correctness): x / sqrt(sum_c x_c^2 + 1e-6) (the card states no guard for a
+ * zero row; 1e-6 is this library's). Accepted by gdn_chunk_fwd, gdn_chunk_bwd
+ * (pass the same flags as to the forward that filled the residuals: dq and dk
+ * are then gradients with respect to the raw q and k) and gdn_recurrent. With
+ * it the residual buffer also holds the normalised rows, so
+ * gdn_chunk_residual_bytes depends on the flag. */
+#define GDN_FLAG_QK_L2NORM 2
 
 typedef struct {
   int B, T, H;       /* batch, tokens, heads */
@@ -192,7 +201,8 @@ int gdn_version(void);
  * products, 4 chunk gradients, 5 recurrent, 6 backward finalisation,
  * 7 chunk outputs, 8 forward state scan on tcgen05 tensor cores, 9 reverse
  * state scan on tcgen05 tensor cores (8 and 9 replace 1 and 2 for bf16
- * operands with Dk = Dv = 128), 10 single-token decode (replaces 5 when T = 1);
+ * operands with Dk = Dv = 128), 10 single-token decode (replaces 5 when T = 1),
+ * 11 q/k L2 normalisation, 12 its reverse (GDN_FLAG_QK_L2NORM only);
  * gdn_kernel_name(id) names them
  * ("" for an unknown id). Not part of the paper's method: instrumentation. */
 int gdn_profile_enable(int on);

@@ -25,22 +25,22 @@ def head_slice(t: Optional[torch.Tensor], pairs: Iterable[Tuple[int, int]], stat
     return torch.stack([t[b, :, h] for b, h in pairs], 1)[None]
 
 
-def oracle_fwd(d, pairs: Optional[List[Tuple[int, int]]] = None, scale=None):
+def oracle_fwd(d, pairs: Optional[List[Tuple[int, int]]] = None, scale=None, qk_l2norm: bool = False):
     """float64 oracle forward of the whole problem, or of the listed (b, h) pairs."""
     if pairs is None:
         args = [to_f64(d[n]) for n in ("q", "k", "v", "g", "beta", "h0")]
     else:
         args = [to_f64(head_slice(d[n], pairs, state=(n == "h0"))) for n in ("q", "k", "v", "g", "beta", "h0")]
-    return oracle.fwd(*args, scale=scale)
+    return oracle.fwd(*args, scale=scale, qk_l2norm=qk_l2norm)
 
 
-def oracle_bwd(d, pairs: Optional[List[Tuple[int, int]]] = None, scale=None):
+def oracle_bwd(d, pairs: Optional[List[Tuple[int, int]]] = None, scale=None, qk_l2norm: bool = False):
     names = ("q", "k", "v", "g", "beta", "h0", "dout", "dh_final")
     if pairs is None:
         args = [to_f64(d[n]) for n in names]
     else:
         args = [to_f64(head_slice(d[n], pairs, state=(n in ("h0", "dh_final")))) for n in names]
-    return oracle.bwd(*args, scale=scale)
+    return oracle.bwd(*args, scale=scale, qk_l2norm=qk_l2norm)
 
 
 def rel(x: torch.Tensor, y: np.ndarray) -> float:

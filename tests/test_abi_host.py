@@ -62,6 +62,10 @@ def test_size_queries(lib):
     # linear in the number of chunk-heads
     r2 = lib.gdn_chunk_residual_bytes(ctypes.byref(_dims(T=256)))
     assert abs(r2 - 2 * r) <= 9 * 1024
+    # the q/k L2 normalisation adds the normalised q, k rows (bf16) and their inverse norms
+    rn = lib.gdn_chunk_residual_bytes(ctypes.byref(_dims(flags=binding.GDN_FLAG_QK_L2NORM)))
+    rows = 2 * 128 * 3
+    assert r + rows * (2 * D * 2 + 2 * 4) <= rn <= r + rows * (2 * D * 2 + 2 * 4) + 4 * 1024
 
 
 def _fake(addr=1 << 20):

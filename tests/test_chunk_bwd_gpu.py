@@ -99,3 +99,19 @@ def test_training_shape_fwd_bwd_workload():
         assert rel(got, ref[n]) <= TOL["bf16"], (n, rel(got, ref[n]))
     for n in GRADS:  # the heads not sampled are finite
         assert bool(torch.isfinite(grads[n].float()).all()), n
+
+
+@pytest.mark.parametrize("D", [64, 128])
+def test_qk_l2norm_forward_and_backward(D):
+    """q and k drawn without normalisation (norms ~ sqrt(D)); with GDN_FLAG_QK_L2NORM the
+    chunked forward and backward follow the oracle's normalised rule, and dq, dk are
+    gradients with respect to the raw q, k."""
+    w = WORKLOADS["train_fwdbwd"].with_(B=2, T=128, H=3, Dk=D, Dv=D, normalize_qk=False, h0_std=0.2)
+    host = make_inputs(w)
+    flags = gdn.GDN_FLAG_QK_L2NORM
+    out, hT, grads = _fwd_bwd(cuda_inputs(host), flags)
+    o_ref, h_ref = oracle_fwd(host, qk_l2norm=True)
+    assert rel(out, o_ref) <= TOL["bf16"] and rel(hT, h_ref) <= TOL["bf16"]
+    ref = oracle_bwd(host, qk_l2norm=True)
+    for n in GRADS:
+        assert rel(grads[n], ref[n]) <= TOL["bf16"], (n, rel(grads[n], ref[n]))

@@ -100,3 +100,17 @@ def test_training_shape_forward_workload(dtype):
     o_ref, h_ref = oracle_fwd(host)
     assert rel(out, o_ref) <= TOL[dtype], rel(out, o_ref)
     assert rel(hT, h_ref) <= TOL[dtype], rel(hT, h_ref)
+
+
+def test_qk_l2norm_forward_fp32():
+    """GDN_FLAG_QK_L2NORM with fp32 inputs: within the fp32 tolerance of the oracle's
+    normalised forward; the residual buffer grows by the normalised rows."""
+    w = WORKLOADS["train_fwd_f32"].with_(B=1, T=192, H=2, normalize_qk=False, h0_std=0.1)
+    host = make_inputs(w)
+    d = cuda_inputs(host)
+    flags = gdn.GDN_FLAG_QK_L2NORM
+    out, hT, res = gdn.gdn_chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], d["h0"], flags=flags)
+    o_ref, h_ref = oracle_fwd(host, qk_l2norm=True)
+    assert rel(out, o_ref) <= TOL["f32"] and rel(hT, h_ref) <= TOL["f32"]
+    plain = gdn.gdn_chunk_residual_bytes(gdn.make_dims(d["q"], d["v"], d["g"]))
+    assert res.numel() > plain

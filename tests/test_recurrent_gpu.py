@@ -182,3 +182,29 @@ def test_divergence_is_reproduced():
             elif np.linalg.norm(ref) > 3.4e38 or not np.isfinite(np.linalg.norm(ref)):
                 assert not np.all(np.isfinite(o[0, t, h])), (t, h)
     assert checked > 0
+
+
+@pytest.mark.parametrize("dtype,per_channel", [("f32", False), ("bf16", True)])
+def test_qk_l2norm_recurrent_and_decode(dtype, per_channel):
+    """GDN_FLAG_QK_L2NORM in the recurrent kernel and the single-token decode kernel:
+    within tolerance of the oracle's normalised rule, and one token per call (decode,
+    state carried in place) equals one prefill call bitwise."""
+    w = WORKLOADS["tiny_fwd"].with_(B=2, T=40, H=5, Dk=128, Dv=128, dtype=dtype, g_per_channel=per_channel,
+                                    normalize_qk=False, h0_std=0.1)
+    host = make_inputs(w)
+    d = cuda_inputs(host)
+    flags = gdn.GDN_FLAG_QK_L2NORM
+    out_full, h_full = _run(d, flags=flags)
+    o_ref, h_ref = oracle_fwd(host, qk_l2norm=True)
+    assert rel(out_full, o_ref) <= TOL[dtype] and rel(h_full, h_ref) <= 1e-4
+    state = d["h0"].clone()
+    outs = []
+    for t in range(w.T):
+        sl = slice(t, t + 1)
+        o, _ = gdn.gdn_recurrent(d["q"][:, sl].contiguous(), d["k"][:, sl].contiguous(), d["v"][:, sl].contiguous(),
+                                 d["g"][:, sl].contiguous(), d["beta"][:, sl].contiguous(), state, h_final=state,
+                                 flags=flags)
+        outs.append(o)
+    torch.cuda.synchronize()
+    assert torch.equal(torch.cat(outs, 1), out_full)
+    assert torch.equal(state, h_full)
