@@ -321,6 +321,7 @@ def run_gdn(args, world, rank, local):
         "kernels": kernels,
         "clocks": clk.summary(),
         "correctness_gate": {"chunked_vs_recurrent_rel_l2": round(gate, 6), "finite": finite},
+        "variants": variants_leg(args, w, host, dev),
     }
     if not args.no_extras:
         outputs = dict(grads, out=out, h_final=hT)
@@ -331,6 +332,47 @@ def run_gdn(args, world, rank, local):
             result["cpu_baseline"] = cpu_baseline(w, host)
     if rank == 0:
         print(json.dumps(result), flush=True)
+
+
+def variants_leg(args, w, host, dev):
+    """The same fwd+bwd step for the two input variants the library also supports:
+    q/k L2-normalised in the library (GDN_FLAG_QK_L2NORM, raw q and k of norm ~ sqrt(Dk))
+    and one scalar decay per head (g [B,T,H]). CUDA events around N steps each."""
+    import torch
+
+    import gated_deltanet_gdn_gb300 as gdn
+    from gated_deltanet_gdn_gb300.synthetic import make_inputs
+
+    res = {}
+    n = max(3, min(100, args.steps))
+    for name, wv, flags in (("qk_l2norm", w.with_(normalize_qk=False), gdn.GDN_FLAG_QK_L2NORM),
+                            ("scalar_decay", w.with_(g_per_channel=False, g_kind="logsigmoid", g_mu=2.0), 0)):
+        d = {k: (None if v is None else v.to(dev)) for k, v in make_inputs(wv).items()}
+        dims = gdn.make_dims(d["q"], d["v"], d["g"], flags)
+        res_buf = torch.empty(gdn.gdn_chunk_residual_bytes(dims), dtype=torch.uint8, device=dev)
+        ws = torch.empty(gdn.gdn_chunk_bwd_workspace_bytes(dims), dtype=torch.uint8, device=dev)
+
+        def step():
+            gdn.gdn_chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], d["h0"], residuals=res_buf, flags=flags)
+            gdn.gdn_chunk_bwd(d["q"], d["k"], d["v"], d["g"], d["beta"], d["h0"], res_buf, d["dout"],
+                              d["dh_final"], workspace=ws, flags=flags)
+
+        for _ in range(3):
+            step()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(n):
+            step()
+        e1.record()
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / n
+        res[name] = {"ms_per_step": round(ms, 4), "tokens_per_s": round(wv.B * wv.T / (ms / 1e3), 1), "steps": n,
+                     "workload": "B%d T%d H%d D%d bf16, %s" % (wv.B, wv.T, wv.H, wv.Dk,
+                                                              "raw q/k normalised in the library" if flags else
+                                                              "scalar decay logsigmoid(N(2,1)) per head")}
+        del d, res_buf, ws
+    return res
 
 
 def e2e_leg(args, host, d, step, outputs, world):
