@@ -39,18 +39,46 @@ struct BoolTag {
 // q/k L2 normalisation: the guard added to the sum of squares.
 constexpr float QK_NORM_EPS = 1e-6f;
 
-// Inverse L2 norm 1 / sqrt(sum_c x_c^2 + QK_NORM_EPS) of a row x[0 .. N-1] (N a multiple
-// of 32), read by one full warp: lane l sums x[l + 32 j]^2 over ascending j with fmaf,
-// then the lanes are added by a butterfly (xor 16, 8, 4, 2, 1). Every kernel that
-// normalises q or k uses this one definition, so they agree bitwise.
+// V consecutive elements (V = 2 or 4) as floats with one vector load; p aligned to V
+// elements.
+template <int V>
+__device__ __forceinline__ void load_vec(const float* p, float (&x)[V]) {
+  static_assert(V == 2 || V == 4, "two or four elements");
+  if constexpr (V == 4) {
+    const float4 u = *reinterpret_cast<const float4*>(p);
+    x[0] = u.x; x[1] = u.y; x[2] = u.z; x[3] = u.w;
+  } else {
+    const float2 u = *reinterpret_cast<const float2*>(p);
+    x[0] = u.x; x[1] = u.y;
+  }
+}
+template <int V>
+__device__ __forceinline__ void load_vec(const bf16* p, float (&x)[V]) {
+  static_assert(V == 2 || V == 4, "two or four elements");
+  if constexpr (V == 4) {
+    const uint2 u = *reinterpret_cast<const uint2*>(p);
+    const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.x));
+    const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.y));
+    x[0] = a.x; x[1] = a.y; x[2] = b.x; x[3] = b.y;
+  } else {
+    const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(p));
+    x[0] = a.x; x[1] = a.y;
+  }
+}
+
+// Inverse L2 norm 1 / sqrt(sum_c x_c^2 + QK_NORM_EPS) of a row x[0 .. N-1] (N = 64 or
+// 128), read by one full warp: lane l takes the N/32 consecutive elements from
+// l N/32 and sums their squares in ascending order with fmaf, then the lanes are
+// added by a butterfly (xor 16, 8, 4, 2, 1). Every kernel that normalises q or k uses
+// this one definition, so they agree bitwise.
 template <int N, class T>
 __device__ __forceinline__ float warp_row_inv_norm(const T* x, int lane) {
+  constexpr int V = N / 32;
+  float v[V];
+  load_vec<V>(x + V * lane, v);
   float s = 0.f;
 #pragma unroll
-  for (int j = 0; j < N / 32; ++j) {
-    const float v = to_f32(x[lane + 32 * j]);
-    s = fmaf(v, v, s);
-  }
+  for (int j = 0; j < V; ++j) s = fmaf(v[j], v[j], s);
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
   return rsqrtf(s + QK_NORM_EPS);

@@ -26,9 +26,12 @@ __global__ void __launch_bounds__(NORM_THREADS) l2norm_rows_kernel(const T* q, c
   const bool isk = (w & 1) != 0;
   const T* x = (isk ? k : q) + row * DK;
   T* y = (isk ? kn : qn) + row * DK;
+  constexpr int V = DK / 32;  // consecutive elements per lane
   const float inv = warp_row_inv_norm<DK>(x, lane);
+  float xv[V];
+  load_vec<V>(x + V * lane, xv);
 #pragma unroll
-  for (int j = 0; j < DK / 32; ++j) y[lane + 32 * j] = from_f32<T>(to_f32(x[lane + 32 * j]) * inv);
+  for (int j = 0; j < V; j += 2) store2(y + V * lane + j, xv[j] * inv, xv[j + 1] * inv);
   if (lane == 0) (isk ? kinv : qinv)[row] = inv;
 }
 
@@ -44,17 +47,16 @@ __global__ void __launch_bounds__(NORM_THREADS) l2norm_bwd_kernel(T* dq, T* dk, 
   T* dx = (isk ? dk : dq) + row * DK;
   const T* xh = (isk ? kn : qn) + row * DK;
   const float r = (isk ? kinv : qinv)[row];
-  float g[DK / 32], xv[DK / 32], dot = 0.f;
+  constexpr int V = DK / 32;  // consecutive elements per lane
+  float g[V], xv[V], dot = 0.f;
+  load_vec<V>(dx + V * lane, g);
+  load_vec<V>(xh + V * lane, xv);
 #pragma unroll
-  for (int j = 0; j < DK / 32; ++j) {
-    g[j] = to_f32(dx[lane + 32 * j]);
-    xv[j] = to_f32(xh[lane + 32 * j]);
-    dot = fmaf(xv[j], g[j], dot);
-  }
+  for (int j = 0; j < V; ++j) dot = fmaf(xv[j], g[j], dot);
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, off);
 #pragma unroll
-  for (int j = 0; j < DK / 32; ++j) dx[lane + 32 * j] = from_f32<T>(r * (g[j] - xv[j] * dot));
+  for (int j = 0; j < V; j += 2) store2(dx + V * lane + j, r * (g[j] - xv[j] * dot), r * (g[j + 1] - xv[j + 1] * dot));
 }
 
 template <class T, int DK>
