@@ -374,27 +374,31 @@ __global__ void __launch_bounds__(DST_THREADS, 2) chunk_dstate_kernel(ChunkBwdAr
     gq[vq * DK + 64 * p + c + 1] = acc1;
   };
 #pragma unroll 1
+  // per panel: the products with dS1^T first, so that the next dS1^T panel streams in
+  // behind this panel's products with S0^T
   for (int p = 0; p < NPAN; ++p) {
     Tile<T, DV, 64> S0p{reinterpret_cast<T*>(sm + (p == 0 ? L::S0P : L::V))};
     Tile<T, DV, 64> dS1p{reinterpret_cast<T*>(sm + L::DSP)};
     float acc[1][NH][4];
+    if (p > 0) {
+      cp_async_wait<0>();  // this dS1^T panel
+      __syncthreads();
+    }
+    zero(acc);
+    Gemm<T>::template runk<1, NH, 0, DV>(acc, aview<true>(Us), bview<true>(dS1p), m0, n0, lane);
+    store_cdk(a.ws.dkt, p, acc, 1.f);
+    dgam_part(S0p, dS1p, p);
+    if (p + 1 < NPAN) {
+      __syncthreads();  // this dS1^T panel is consumed: the next one loads in its place
+      load_panel(reinterpret_cast<T*>(sm + L::DSP), ds1rec, p + 1);
+      cp_async_commit();
+    }
     zero(acc);
     Gemm<T>::template runk<1, NH, 0, DV>(acc, aview<false>(dOs), bview<true>(S0p), m0, n0, lane);
     store_cdk(a.ws.dqh, p, acc, a.scale);
     zero(acc);
     Gemm<T>::template runk<1, NH, 0, DV>(acc, aview<false>(Ys), bview<true>(S0p), m0, n0, lane);
     store_cdk(a.ws.dbk, p, acc, -1.f);
-    zero(acc);
-    Gemm<T>::template runk<1, NH, 0, DV>(acc, aview<true>(Us), bview<true>(dS1p), m0, n0, lane);
-    store_cdk(a.ws.dkt, p, acc, 1.f);
-    dgam_part(S0p, dS1p, p);
-    if (p + 1 < NPAN) {
-      __syncthreads();  // the first dS1^T panel is consumed: load the second in its place
-      load_panel(reinterpret_cast<T*>(sm + L::DSP), ds1rec, p + 1);
-      cp_async_commit();
-      cp_async_wait<0>();
-      __syncthreads();
-    }
   }
   __syncthreads();
   for (int c = tid; c < DK; c += DST_THREADS) {
