@@ -47,42 +47,34 @@ __device__ __forceinline__ void tri_index(int p, int& i, int& j) {
 // lower, zeros on and above the diagonal); on exit it holds T = L^-1 with its unit
 // diagonal and zero upper part stored explicitly. Doubling: if T11, T22 invert the
 // diagonal blocks of size s, the inverse of the 2s block is [[T11, 0], [-T22 A21 T11, T22]].
-// Blocks of size 1..8 use dense fp32 loops; the 16 and 32 levels run on tensor cores with
+// The 16 x 16 diagonal blocks are inverted by forward substitution (a lane per column,
+// in registers), and the 32 and 64 levels run on tensor cores with
 // the three-term TF32 split (about 21 significant bits, far below the bf16 operand error).
 typedef FTile<C, C, 4> MTile;        // padded rows: fragment loads are conflict free
 typedef FTile<BLK, BLK, 4> XTile;
-
-template <int S, int NTHR>
-__device__ __forceinline__ void inv_level_simt(MTile M, XTile X, int tid) {
-  constexpr int NB = C / (2 * S), OUT = NB * S * S;
-  for (int e = tid; e < OUT; e += NTHR) {  // X_b = A21_b T11_b
-    const int b = e / (S * S), i = (e / S) % S, c = e % S, o = b * 2 * S;
-    float acc = 0.f;
-#pragma unroll
-    for (int j = 0; j < S; ++j) acc = fmaf(M.at(o + S + i, o + j), M.at(o + j, o + c), acc);
-    X.p[e] = acc;
-  }
-  __syncthreads();
-  for (int e = tid; e < OUT; e += NTHR) {  // T21_b = -T22_b X_b
-    const int b = e / (S * S), i = (e / S) % S, c = e % S, o = b * 2 * S;
-    float acc = 0.f;
-#pragma unroll
-    for (int j = 0; j < S; ++j) acc = fmaf(M.at(o + S + i, o + S + j), X.p[b * S * S + j * S + c], acc);
-    M.at(o + S + i, o + c) = -acc;
-  }
-  __syncthreads();
-}
 
 template <int NTHR>
 __device__ void unit_lower_inverse64(MTile M, XTile X, int tid) {
   static_assert(NTHR == 256, "tensor-core levels assume 8 warps");
   const int warp = tid >> 5, lane = tid & 31;
-  for (int i = tid; i < C; i += NTHR) M.at(i, i) = 1.f;
+  // 16 x 16 diagonal blocks by forward substitution: each lane of warps 0 and 1 keeps one
+  // column of one block's inverse in registers, T[i][j] = -sum_{k<i} A[i][k] T[k][j]
+  if (warp < 2) {
+    const int o = 16 * (2 * warp + (lane >> 4)), j = lane & 15;
+    float t[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) t[i] = i == j ? 1.f : 0.f;
+#pragma unroll
+    for (int i = 1; i < 16; ++i) {
+      float acc = 0.f;
+#pragma unroll
+      for (int kk = 0; kk < i; ++kk) acc = fmaf(M.at(o + i, o + kk), t[kk], acc);
+      if (i > j) t[i] = -acc;
+    }
+#pragma unroll
+    for (int i = 0; i < 16; ++i) M.at(o + i, o + j) = t[i];
+  }
   __syncthreads();
-  inv_level_simt<1, NTHR>(M, X, tid);
-  inv_level_simt<2, NTHR>(M, X, tid);
-  inv_level_simt<4, NTHR>(M, X, tid);
-  inv_level_simt<8, NTHR>(M, X, tid);
   // s = 16: two blocks (rows/cols offset o = 0, 32); warps 0..3: block w >> 1, columns 8 (w & 1)
   if (warp < 4) {
     const int o = (warp >> 1) * 32, n0 = (warp & 1) * 8;
