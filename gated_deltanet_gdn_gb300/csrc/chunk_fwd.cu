@@ -233,12 +233,16 @@ __global__ void __launch_bounds__(PREP_THREADS) chunk_prep_kernel(ChunkFwdArgs a
   // Reference point for every row: the boundary b = last token of the first block.
   // Factor ranges: block 1 queries exp(G_t - G_b) <= exp(G_0 - G_b); block 2 keys
   // exp(G_b - G_j) <= exp(G_b - G_C-1). Each must stay inside the fp32/bf16 range.
+  // With one decay per head (PC false) the scores are the raw products times the C x C
+  // factor exp(G_t - G_j) <= 1, which never leaves the fp32 range: no range check (the
+  // mask form; GDN_FLAG_PAIRWISE_WITHIN_BLOCK still makes every in-block tile pairwise).
   const bool force = (a.flags & 1) != 0;
   bool u1 = false, u2 = false;
-  for (int c = tid; c < DK; c += PREP_THREADS) {
-    u1 |= !(Gs.at(0, c) - Gs.at(BLK - 1, c) <= SAFE_SPREAD);
-    u2 |= !(Gs.at(BLK - 1, c) - Gs.at(C - 1, c) <= SAFE_SPREAD);
-  }
+  if (PC)
+    for (int c = tid; c < DK; c += PREP_THREADS) {
+      u1 |= !(Gs.at(0, c) - Gs.at(BLK - 1, c) <= SAFE_SPREAD);
+      u2 |= !(Gs.at(BLK - 1, c) - Gs.at(C - 1, c) <= SAFE_SPREAD);
+    }
   const bool unsafe1 = __syncthreads_or(u1 || force) != 0;
   const bool unsafe2 = __syncthreads_or(u2 || force) != 0;
 
@@ -298,7 +302,33 @@ __global__ void __launch_bounds__(PREP_THREADS) chunk_prep_kernel(ChunkFwdArgs a
       st4(ks.ptr(r, c0), bk);
     }
   };
-  if (!(unsafe1 || unsafe2))
+  // one decay per head: the score operands are q and k themselves (the decay enters the
+  // scores as a C x C factor), and Gam, exp(G_C - G) are one exponential per row
+  auto a2_scalar = [&]() {
+    for (int i = tid; i < C * (DK / 4); i += PREP_THREADS) {
+      const int r = i / (DK / 4), c0 = (i % (DK / 4)) * 4;
+      const float Gr = Gs.at(r, 0);
+      const float gm = __expf(Gr), kd = __expf(Gs.at(C - 1, 0) - Gr), br = beta_s[r];
+      float qv[4], kv[4], o1[4], o2[4], bk[4];
+      ld4(qv, Xs.ptr(r, c0));
+      ld4(kv, ks.ptr(r, c0));
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        o1[e] = a.scale * gm * qv[e];
+        o2[e] = kd * kv[e];
+        bk[e] = br * gm * kv[e];
+      }
+      const int off = Sw<T, C, DK>::off(r, c0);
+      st4(qh_g + off, o1);
+      st4(kt_g + off, o2);
+      st4(X2s.ptr(r, c0), kv);
+      st4(Ys.ptr(r, c0), kv);
+      st4(ks.ptr(r, c0), bk);
+    }
+  };
+  if (!PC && !force)
+    a2_scalar();
+  else if (!(unsafe1 || unsafe2))
     a2_pass(BoolTag<true>{});
   else
     a2_pass(BoolTag<false>{});
@@ -323,8 +353,10 @@ __global__ void __launch_bounds__(PREP_THREADS) chunk_prep_kernel(ChunkFwdArgs a
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
       const int r = m0 + frag_row(lane, e), j = n0 + 8 * nt + frag_col(lane, e);
-      Tst.at(r, j) = from_f32<T>(j <= r ? a.scale * aq[0][nt][e] : 0.f);
-      Akk.at(r, j) = j < r ? beta_s[r] * ak[0][nt][e] : 0.f;
+      // one decay per head (mask form): exp(G_r - G_j) on the raw products
+      const float dec = PC || force || j > r ? 1.f : __expf(Gs.at(r, 0) - Gs.at(j, 0));
+      Tst.at(r, j) = from_f32<T>(j <= r ? a.scale * aq[0][nt][e] * dec : 0.f);
+      Akk.at(r, j) = j < r ? beta_s[r] * ak[0][nt][e] * dec : 0.f;
     }
   __syncthreads();
   if (unsafe1 || unsafe2) {

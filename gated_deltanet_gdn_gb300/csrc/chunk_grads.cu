@@ -164,13 +164,21 @@ __global__ void __launch_bounds__(GR_THREADS, 2) chunk_grads_kernel(ChunkBwdArgs
     for (int i = 0; i < BLK; ++i) Gat(r0 + i, c) = hb ? v[i] + base : v[i];
   }
   __syncthreads();
+  // One decay per head (PC false) without the pairwise flag: the mask form. The score
+  // gradients are (dP (*) E) y and (dP (*) E)^T x with E[t][j] = exp(G_t - G_j) <= 1,
+  // applied to the dP tiles, and the operands are q, beta k and k themselves.
   const bool force = (a.flags & 1) != 0;
+  const bool mask_form = !PC && !force;
   bool u1 = false, u2 = false;
   for (int c = tid; c < HC; c += GR_THREADS) {
-    u1 |= !(Gat(0, c) - Gat(BLK - 1, c) <= SAFE_SPREAD);
-    u2 |= !(Gat(BLK - 1, c) - Gat(C - 1, c) <= SAFE_SPREAD);
+    if (PC) {
+      u1 |= !(Gat(0, c) - Gat(BLK - 1, c) <= SAFE_SPREAD);
+      u2 |= !(Gat(BLK - 1, c) - Gat(C - 1, c) <= SAFE_SPREAD);
+    }
     gcol_s[c] *= __expf(Gat(C - 1, c));  // dgam * gam
   }
+  if (!PC && tid < C) gsc[tid] = Gat(tid, 0);  // one decay per head: G per token, read by the mask form
+  auto gsc_cum = [&](int r) { return gsc[r]; };
   const bool unsafe1 = __syncthreads_or(u1 || force) != 0;
   const bool unsafe2 = __syncthreads_or(u2 || force) != 0;
 
@@ -191,14 +199,29 @@ __global__ void __launch_bounds__(GR_THREADS, 2) chunk_grads_kernel(ChunkBwdArgs
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
       const float d = G[e] - Gb[e];
-      const float e1 = dead_x ? 0.f : __expf(d);
+      const float e1 = mask_form ? 1.f : dead_x ? 0.f : __expf(d);
+      const float e2 = mask_form ? 1.f : dead_y ? 0.f : __expf(-d);
       xq[e] = qv[e] * e1;
       xb[e] = br * kv[e] * e1;
-      yk[e] = dead_y ? 0.f : kv[e] * __expf(-d);
+      yk[e] = kv[e] * e2;
     }
     st4(Xs.ptr(r, c0), xq);
     st4(XBs.ptr(r, c0), xb);
     st4(Ys.ptr(r, c0), yk);
+  }
+  if (mask_form) {  // dP (*) E on both score tiles (strictly lower part; the diagonal has E = 1)
+    for (int i = tid; i < C * C / 2; i += GR_THREADS) {
+      const int t = i / (C / 2), j = 2 * (i % (C / 2));
+      if (j < t) {
+        const float Gt = Gat(t, 0);
+        const float e0 = __expf(Gt - gsc_cum(j)), e1 = j + 1 < t ? __expf(Gt - gsc_cum(j + 1)) : 0.f;
+        __nv_bfloat162* pq = reinterpret_cast<__nv_bfloat162*>(dAq.ptr(t, j));
+        __nv_bfloat162* pk = reinterpret_cast<__nv_bfloat162*>(dAk.ptr(t, j));
+        const float2 fq = __bfloat1622float2(*pq), fk = __bfloat1622float2(*pk);
+        *pq = __floats2bfloat162_rn(fq.x * e0, j + 1 < t ? fq.y * e1 : fq.y);
+        *pk = __floats2bfloat162_rn(fk.x * e0, j + 1 < t ? fk.y * e1 : fk.y);
+      }
+    }
   }
   __syncthreads();
 
@@ -235,17 +258,26 @@ __global__ void __launch_bounds__(GR_THREADS, 2) chunk_grads_kernel(ChunkBwdArgs
   float dbp[2] = {0.f, 0.f}, colp[4][2];
   // FAST (both blocks safe): no pairwise rows, and Gam = exp(G_b) e1, exp(G_C - G) =
   // exp(G_C - G_b) e2 with every factor in fp32 range, two exponentials per element fewer
-  auto epilogue = [&](auto fast_tag) {
+  auto epilogue = [&](auto fast_tag, auto mask_tag) {
     constexpr bool FAST = decltype(fast_tag)::value;
+    constexpr bool MASK = decltype(mask_tag)::value;  // scalar decay: E already in dP
     const int bs = blk1 ? 0 : BLK;
     const bool skip_x = !FAST && blk1 && unsafe1, skip_y = !FAST && !blk1 && unsafe2;
+    float rgm[2] = {0.f, 0.f}, rkd[2] = {0.f, 0.f};  // MASK: Gam and exp(G_C - G) of this thread's two rows
+    if (MASK)
+#pragma unroll
+      for (int h2 = 0; h2 < 2; ++h2) {
+        const float Gr = Gat(m0 + frag_row(lane, 2 * h2), 0);
+        rgm[h2] = __expf(Gr);
+        rkd[h2] = __expf(Gat(C - 1, 0) - Gr);
+      }
 #pragma unroll
     for (int nt = 0; nt < 4; ++nt) {
       const int c = c0 + 8 * nt + 2 * (lane & 3);
       const float2 gb = *reinterpret_cast<const float2*>(&Gat(BLK - 1, c));
       const float2 gc = *reinterpret_cast<const float2*>(&Gat(C - 1, c));
       float eb[2] = {0.f, 0.f}, ecb[2] = {0.f, 0.f};
-      if (FAST) {
+      if (FAST && !MASK) {
         eb[0] = __expf(gb.x);
         eb[1] = __expf(gb.y);
         ecb[0] = __expf(gc.x - gb.x);
@@ -271,8 +303,9 @@ __global__ void __launch_bounds__(GR_THREADS, 2) chunk_grads_kernel(ChunkBwdArgs
           const float dqh = u ? __high2float(h2) : __low2float(h2);
           const float dbk = u ? __high2float(b2) : __low2float(b2);
           const float dkt = u ? __high2float(t2) : __low2float(t2);
-          const float e1 = __expf(G - Gb), e2 = __expf(Gb - G);
-          const float gm = FAST ? eb[u] * e1 : __expf(G), kd = FAST ? ecb[u] * e2 : __expf(GC - G);
+          const float e1 = MASK ? 1.f : __expf(G - Gb), e2 = MASK ? 1.f : __expf(Gb - G);
+          const float gm = MASK ? rgm[e >> 1] : FAST ? eb[u] * e1 : __expf(G);
+          const float kd = MASK ? rkd[e >> 1] : FAST ? ecb[u] * e2 : __expf(GC - G);
           float dxb = skip_x ? 0.f : axB[0][nt][e + u] * e1;  // Akk family, dP = dAkk
           float dyb = skip_y ? 0.f : ayB[0][nt][e + u] * e2;
           float dxa = skip_x ? 0.f : axA[0][nt][e + u] * e1;  // Aqk family
@@ -296,10 +329,12 @@ __global__ void __launch_bounds__(GR_THREADS, 2) chunk_grads_kernel(ChunkBwdArgs
       }
     }
   };
-  if (!(unsafe1 || unsafe2))
-    epilogue(BoolTag<true>{});
+  if (mask_form)
+    epilogue(BoolTag<true>{}, BoolTag<true>{});
+  else if (!(unsafe1 || unsafe2))
+    epilogue(BoolTag<true>{}, BoolTag<false>{});
   else
-    epilogue(BoolTag<false>{});
+    epilogue(BoolTag<false>{}, BoolTag<false>{});
   // column sums over this warp's 16 rows (lanes sharing a column differ in bits 2..4)
 #pragma unroll
   for (int nt = 0; nt < 4; ++nt)

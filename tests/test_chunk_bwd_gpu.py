@@ -115,3 +115,19 @@ def test_qk_l2norm_forward_and_backward(D):
     ref = oracle_bwd(host, qk_l2norm=True)
     for n in GRADS:
         assert rel(grads[n], ref[n]) <= TOL["bf16"], (n, rel(grads[n], ref[n]))
+
+
+@pytest.mark.parametrize("flags", [0, gdn.GDN_FLAG_PAIRWISE_WITHIN_BLOCK])
+def test_scalar_decay_with_wipes(flags):
+    """One decay per head with g = -20 wipes inside chunks (every 50 tokens): the scalar
+    decay's mask form (decay as a C x C factor on the raw products) and the forced pairwise
+    path both follow the oracle, forward and backward."""
+    w = WORKLOADS["train_fwdbwd"].with_(B=1, T=256, H=3, g_per_channel=False, g_kind="logsigmoid",
+                                        g_mu=2.0, wipe_every=50, h0_std=0.3)
+    host = make_inputs(w)
+    out, hT, grads = _fwd_bwd(cuda_inputs(host), flags)
+    o_ref, h_ref = oracle_fwd(host)
+    assert rel(out, o_ref) <= TOL["bf16"] and rel(hT, h_ref) <= TOL["bf16"]
+    ref = oracle_bwd(host)
+    for n in GRADS:
+        assert rel(grads[n], ref[n]) <= TOL["bf16"], (n, rel(grads[n], ref[n]))
