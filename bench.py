@@ -493,6 +493,7 @@ def decode_leg(dev):
         b = 2 * sb + io_b
         res["B%d" % B] = {"workload": label, "ms_per_step": round(ms, 5), "bytes_per_step": b,
                           "hbm_gbs": round(b / (ms / 1e3) / 1e9, 1)}
+    res["replay_B32"] = replay_leg(dev, res["B32"]["ms_per_step"])
     w = WORKLOADS["recurrent"]
     d = {k: (None if v is None else v.to(dev)) for k, v in make_inputs(w).items()}
     gdn.gdn_recurrent(d["q"], d["k"], d["v"], d["g"], d["beta"], None)
@@ -508,6 +509,46 @@ def decode_leg(dev):
     peaks = load_peaks()
     res["hbm_peak_gbs"] = peaks["hbm_gbs"]
     return res
+
+
+def replay_leg(dev, recurrent_ms, L=16):
+    """Replay decode (checkpoint + L-token buffer) on the B32 H48 Dk=Dv=128 fp32 decode
+    batch: 2 L warm-up steps reach the steady fill cycle, then 4 L steps (4 folds) back to
+    back between two CUDA events. Bytes per step are averaged over the cycle: the
+    checkpoint read, (L + 1) / 2 buffer slots read, one slot written, the checkpoint
+    written once per L steps, the token row in and the output out."""
+    import torch
+
+    import gated_deltanet_gdn_gb300 as gdn
+    from gated_deltanet_gdn_gb300.synthetic import WORKLOADS, make_inputs
+
+    w = WORKLOADS["recurrent"].with_(B=32, T=1, h0_std=0.01)
+    d = {k: (None if v is None else v.to(dev)) for k, v in make_inputs(w).items()}
+    ckpt, buffer, fill = gdn.replay_init(d["h0"], L)
+    out = torch.empty_like(d["v"])
+
+    def one():
+        gdn.gdn_replay_decode(d["q"], d["k"], d["v"], d["g"], d["beta"], ckpt, buffer, fill, L, out=out)
+
+    for _ in range(2 * L):
+        one()
+    torch.cuda.synchronize()
+    steps = 4 * L
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(steps):
+        one()
+    e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / steps
+    heads = w.B * w.H
+    sb = w.Dk * w.Dv * 4
+    slot = (2 * w.Dk + w.Dv) * 4
+    io = (2 * w.Dk + 2 * w.Dv + 2) * 4
+    b = heads * (sb + (L + 1) / 2 * slot + slot + sb / L + io)
+    return {"workload": "B32 H48 Dk=Dv=128 fp32, buffer L=%d, %d steps back to back" % (L, steps),
+            "ms_per_step": round(ms, 5), "bytes_per_step": int(b), "hbm_gbs": round(b / (ms / 1e3) / 1e9, 1),
+            "speedup_vs_recurrent_decode": round(recurrent_ms / ms, 3)}
 
 
 def oracle_sample(w, host, pairs):

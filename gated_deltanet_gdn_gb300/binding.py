@@ -33,8 +33,10 @@ GDN_CHUNK = 64
 EXPORTED = ("gdn_chunk_residual_bytes", "gdn_chunk_bwd_workspace_bytes", "gdn_chunk_fwd",
             "gdn_chunk_bwd", "gdn_recurrent", "gdn_check_device_error", "gdn_status_string",
             "gdn_version", "gdn_profile_enable", "gdn_profile_read", "gdn_kernel_name",
-            "gdn_chunk_fwd_noalloc")
-KERNEL_COUNT = 13
+            "gdn_chunk_fwd_noalloc", "gdn_replay_buffer_bytes", "gdn_replay_decode",
+            "gdn_replay_state")
+KERNEL_COUNT = 15
+GDN_REPLAY_MAX_TOKENS = 16
 
 
 class GdnDims(ctypes.Structure):
@@ -90,6 +92,12 @@ def load(build_if_needed: bool = True) -> ctypes.CDLL:
             lib.gdn_kernel_name.restype = ctypes.c_char_p
             lib.gdn_chunk_fwd_noalloc.argtypes = [pd, vp, vp, vp, vp, vp, vp, f, vp, vp, vp]
             lib.gdn_chunk_fwd_noalloc.restype = i
+            lib.gdn_replay_buffer_bytes.argtypes = [pd, i]
+            lib.gdn_replay_buffer_bytes.restype = sz
+            lib.gdn_replay_decode.argtypes = [pd, i, vp, vp, vp, vp, vp, f, vp, vp, vp, vp, vp]
+            lib.gdn_replay_decode.restype = i
+            lib.gdn_replay_state.argtypes = [pd, i, vp, vp, vp, vp, vp]
+            lib.gdn_replay_state.restype = i
             _lib = lib
     return _lib
 
@@ -237,6 +245,58 @@ def gdn_recurrent(q, k, v, g, beta, h0=None, scale: Optional[float] = None, *, o
                                   _ptr(h0), float(scale), _ptr(out), _ptr(h_final), _stream(dev))
     _check("gdn_recurrent", st)
     return out, h_final
+
+
+def gdn_replay_buffer_bytes(dims: GdnDims, L: int) -> int:
+    return int(load().gdn_replay_buffer_bytes(ctypes.byref(dims), int(L)))
+
+
+def replay_init(h0: torch.Tensor, L: int):
+    """(ckpt, buffer, fill) for replay decode starting from state h0 [B,H,Dk,Dv] fp32:
+    the checkpoint is a copy of h0, the buffer is empty (fill = 0)."""
+    B, H, Dk, Dv = h0.shape
+    dims = GdnDims(B, 1, H, Dk, Dv, 1, GDN_F32, 0)
+    nbytes = gdn_replay_buffer_bytes(dims, L)
+    if nbytes == 0 and B * H > 0:
+        raise GdnError("gdn_replay_buffer_bytes", GDN_ERR_INVALID_ARG, f"bad dims or L={L}")
+    ckpt = h0.detach().to(torch.float32).contiguous().clone()
+    buffer = torch.empty(max(nbytes // 4, 4), dtype=torch.float32, device=h0.device)
+    fill = torch.zeros((B, H), dtype=torch.int32, device=h0.device)
+    return ckpt, buffer, fill
+
+
+def gdn_replay_decode(q, k, v, g, beta, ckpt, buffer, fill, L: int, scale: Optional[float] = None, *,
+                      out=None, flags: int = 0) -> torch.Tensor:
+    """One decode step (T = 1) against checkpoint + buffer; advances fill, folds the
+    buffer into ckpt when it is full. Returns out [B,1,H,Dv]."""
+    dev = q.device
+    _require(dict(q=q, k=k, v=v, g=g, beta=beta, ckpt=ckpt, buffer=buffer, fill=fill, out=out), dev)
+    dims = make_dims(q, v, g, flags)
+    if scale is None:
+        scale = dims.Dk ** -0.5
+    if out is None:
+        out = torch.empty(v.shape, dtype=v.dtype, device=dev)
+    with torch.cuda.device(dev):
+        st = load().gdn_replay_decode(ctypes.byref(dims), int(L), _ptr(q), _ptr(k), _ptr(v), _ptr(g),
+                                      _ptr(beta), float(scale), _ptr(ckpt), _ptr(buffer), _ptr(fill),
+                                      _ptr(out), _stream(dev))
+    _check("gdn_replay_decode", st)
+    return out
+
+
+def gdn_replay_state(ckpt, buffer, fill, L: int, *, h_out=None) -> torch.Tensor:
+    """The full state [B,H,Dk,Dv] fp32 that checkpoint + buffer stand for."""
+    dev = ckpt.device
+    _require(dict(ckpt=ckpt, buffer=buffer, fill=fill, h_out=h_out), dev)
+    B, H, Dk, Dv = ckpt.shape
+    dims = GdnDims(B, 1, H, Dk, Dv, 1, GDN_F32, 0)
+    if h_out is None:
+        h_out = torch.empty_like(ckpt)
+    with torch.cuda.device(dev):
+        st = load().gdn_replay_state(ctypes.byref(dims), int(L), _ptr(ckpt), _ptr(buffer), _ptr(fill),
+                                     _ptr(h_out), _stream(dev))
+    _check("gdn_replay_state", st)
+    return h_out
 
 
 def gdn_check_device_error() -> int:

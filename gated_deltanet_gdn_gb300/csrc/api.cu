@@ -115,7 +115,8 @@ const char* kKernelNames[K_COUNT] = {"chunk_prep_kernel",    "chunk_scan_fwd_ker
                                      "chunk_grads_kernel",    "recurrent_kernel",
                                      "chunk_bwd_finalize_kernel", "chunk_out_kernel",
                                      "chunk_scan_fwd_tc_kernel", "chunk_scan_bwd_tc_kernel",
-                                     "decode_kernel", "l2norm_rows_kernel", "l2norm_bwd_kernel"};
+                                     "decode_kernel", "l2norm_rows_kernel", "l2norm_bwd_kernel",
+                                     "replay_decode_kernel", "replay_state_kernel"};
 
 }  // namespace
 
@@ -266,6 +267,55 @@ int gdn_recurrent(const gdn_dims* d, const void* q, const void* k, const void* v
   return launch_status(launch_recurrent(a, static_cast<cudaStream_t>(stream)));
 }
 
+size_t gdn_replay_buffer_bytes(const gdn_dims* d, int L) {
+  if (check_dims(d, false) != GDN_OK || L < 1 || L > GDN_REPLAY_MAX_TOKENS) return 0;
+  return (size_t)d->B * d->H * L * (2 * d->Dk + d->Dv) * sizeof(float);
+}
+
+int gdn_replay_decode(const gdn_dims* d, int L, const void* q, const void* k, const void* v,
+                      const void* g, const void* beta, float scale, float* ckpt, void* buffer,
+                      int* fill, void* out, void* stream) {
+  int st = check_dims(d, false);
+  if (st != GDN_OK) return st;
+  if (L < 1 || L > GDN_REPLAY_MAX_TOKENS || !std::isfinite(scale)) return GDN_ERR_INVALID_ARG;
+  if (d->T != 1) return GDN_ERR_SHAPE;
+  const bool work = (long long)d->B * d->H > 0;
+  const int es = esize(d);
+  if (!tensor_ok(q, work) || !tensor_ok(k, work) || !tensor_ok(v, work) || !tensor_ok(out, work))
+    return GDN_ERR_INVALID_ARG;
+  if (d->g_per_channel ? !tensor_ok(g, work) : !gate_ok(g, work, es)) return GDN_ERR_INVALID_ARG;
+  if (!gate_ok(beta, work, es)) return GDN_ERR_INVALID_ARG;
+  if (!tensor_ok(ckpt, work) || !tensor_ok(buffer, work) || !gate_ok(fill, work, 4)) return GDN_ERR_INVALID_ARG;
+  if (!work) return GDN_OK;
+  ReplayArgs a{};
+  a.B = d->B; a.H = d->H; a.DK = d->Dk; a.DV = d->Dv; a.L = L;
+  a.per_channel = d->g_per_channel ? 1 : 0;
+  a.bf16 = d->dtype == GDN_BF16;
+  a.qk_norm = qk_norm(d) ? 1 : 0;
+  a.q = q; a.k = k; a.v = v; a.g = g; a.beta = beta; a.scale = scale;
+  a.ckpt = ckpt; a.buffer = static_cast<float*>(buffer); a.fill = fill; a.out = out;
+  a.err = device_error_word();
+  if (!a.err) return GDN_ERR_CUDA;
+  return launch_status(launch_replay_decode(a, static_cast<cudaStream_t>(stream)));
+}
+
+int gdn_replay_state(const gdn_dims* d, int L, const float* ckpt, const void* buffer, const int* fill,
+                     float* h_out, void* stream) {
+  int st = check_dims(d, false);
+  if (st != GDN_OK) return st;
+  if (L < 1 || L > GDN_REPLAY_MAX_TOKENS) return GDN_ERR_INVALID_ARG;
+  const bool work = (long long)d->B * d->H > 0;
+  if (!tensor_ok(ckpt, work) || !tensor_ok(buffer, work) || !gate_ok(fill, work, 4) || !tensor_ok(h_out, work))
+    return GDN_ERR_INVALID_ARG;
+  if (!work) return GDN_OK;
+  ReplayStateArgs a{};
+  a.B = d->B; a.H = d->H; a.DK = d->Dk; a.DV = d->Dv; a.L = L;
+  a.ckpt = ckpt; a.buffer = static_cast<const float*>(buffer); a.fill = fill; a.h_out = h_out;
+  a.err = device_error_word();
+  if (!a.err) return GDN_ERR_CUDA;
+  return launch_status(launch_replay_state(a, static_cast<cudaStream_t>(stream)));
+}
+
 int gdn_check_device_error(void) {
   unsigned* p = device_error_word();
   if (!p) return GDN_ERR_CUDA;
@@ -287,7 +337,7 @@ const char* gdn_status_string(int s) {
     case GDN_ERR_UNSUPPORTED: return "unsupported configuration (Dk, Dv in {64, 128}; chunked path Dk == Dv; bf16-only backward)";
     case GDN_ERR_SHAPE: return "T must be a multiple of 64 on the chunked path";
     case GDN_ERR_CUDA: return "CUDA launch or runtime error";
-    case GDN_ERR_INTERNAL: return "a kernel reported an internal error (bounded wait timed out)";
+    case GDN_ERR_INTERNAL: return "a kernel reported an error (a bounded wait timed out, or a replay fill count out of range)";
     case GDN_ERR_SCRATCH_LIMIT: return "problem needs more residual scratch than the static GDN_NOALLOC_SCRATCH_BYTES array";
     default: return "unknown status";
   }

@@ -156,6 +156,28 @@ struct RecurrentArgs {
   unsigned* err;
 };
 
+// Replay decode (replay.cu): checkpoint [B,H,DK,DV] fp32, buffer [B,H,L][2 DK + DV] fp32
+// slots (k, cumulative log-decay G, delta d), fill [B,H] slots in use.
+constexpr int REPLAY_MAX_TOKENS = 16;
+struct ReplayArgs {
+  int B, H, DK, DV, L, per_channel, bf16, qk_norm;
+  const void *q, *k, *v, *g, *beta;
+  float scale;
+  float* ckpt;
+  float* buffer;
+  int* fill;
+  void* out;
+  unsigned* err;
+};
+struct ReplayStateArgs {
+  int B, H, DK, DV, L;
+  const float* ckpt;
+  const float* buffer;
+  const int* fill;
+  float* h_out;
+  unsigned* err;
+};
+
 // Kernel identifiers for the optional per-launch timing (gdn_profile_* in the C ABI).
 enum KernelId {
   K_PREP = 0,      // chunk_prep_kernel
@@ -171,7 +193,9 @@ enum KernelId {
   K_DECODE = 10,      // decode_kernel
   K_L2NORM = 11,      // l2norm_rows_kernel
   K_L2NORM_BWD = 12,  // l2norm_bwd_kernel
-  K_COUNT = 13
+  K_REPLAY = 13,      // replay_decode_kernel
+  K_REPLAY_STATE = 14,  // replay_state_kernel
+  K_COUNT = 15
 };
 // Records a CUDA event on s before (begin = true) or after a launch when timing is on.
 void prof_mark(KernelId id, cudaStream_t s, bool begin);
@@ -192,5 +216,9 @@ cudaError_t launch_l2norm_rows(const void* q, const void* k, void* qn, void* kn,
                                size_t rows, int DK, int bf16, cudaStream_t s);
 cudaError_t launch_l2norm_bwd(void* dq, void* dk, const void* qn, const void* kn, const float* qinv,
                               const float* kinv, size_t rows, int DK, int bf16, cudaStream_t s);
+// Replay decode (replay.cu): one token per (batch, head) against checkpoint + buffer,
+// and the fold of a buffer into a full state.
+cudaError_t launch_replay_decode(const ReplayArgs& a, cudaStream_t s);
+cudaError_t launch_replay_state(const ReplayStateArgs& a, cudaStream_t s);
 
 }  // namespace gdn

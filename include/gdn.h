@@ -178,8 +178,48 @@ int gdn_recurrent(const gdn_dims* dims, const void* q, const void* k, const void
                   const void* g, const void* beta, const float* h0, float scale, void* out,
                   float* h_final, void* stream);
 
+/* Replay decode: the state of each (batch, head) held as a checkpoint plus a
+ * buffer of its last few tokens, after the ReplaySSM summary on the ai4snews
+ * "Gated DeltaNet" topic page (item "SSM decoding stops writing state every
+ * step"): each step reads the checkpoint, computes the token's output directly
+ * from it and the buffered tokens, and appends the token to the buffer; the
+ * checkpoint is written only when a step finds the buffer full (it is folded in
+ * first). A decode step therefore reads the state but rarely writes it, where
+ * gdn_recurrent reads and writes it every step. Outputs equal the recurrence to
+ * rounding (not bitwise: the sums run in another order).
+ *
+ *   L       buffer length in tokens, 1 .. GDN_REPLAY_MAX_TOKENS, fixed for the
+ *           life of a buffer
+ *   ckpt    [B,H,Dk,Dv] float32 checkpoint, read and (on a fold) written in
+ *           place. Start a sequence with ckpt = its state (zeros, or h_final of
+ *           a prefill) and fill = 0.
+ *   buffer  gdn_replay_buffer_bytes(dims, L) bytes, 16-byte aligned: per (b, h)
+ *           L slots of (k, cumulative log-decay since the checkpoint, delta), fp32;
+ *           private layout, no initialisation needed
+ *   fill    [B,H] int32, slots in use; advanced by each step (to 1 after a
+ *           fold). Rolling back the last r <= fill tokens of a sequence (a
+ *           rejected speculative draft) is lowering its fill by r before the
+ *           next call. A count outside [0, L] sets bit 2 (value 2) of the device
+ *           error word and is clamped.
+ * gdn_replay_decode processes one token per (b, h): dims.T must be 1, inputs
+ * and out as gdn_recurrent with T = 1; dims.flags may hold
+ * GDN_FLAG_QK_L2NORM. gdn_replay_state writes the full state the buffer stands
+ * for, h_out = fold(ckpt, the fill slots) [B,H,Dk,Dv] (dims.T is ignored); it
+ * does not change ckpt, buffer or fill. h_out may be ckpt itself, in which case
+ * the caller sets fill to 0 afterwards. Errors as gdn_recurrent, plus
+ * GDN_ERR_SHAPE for dims.T != 1 in gdn_replay_decode and GDN_ERR_INVALID_ARG
+ * for L out of range. Returns 0 bytes for invalid dims or L. */
+#define GDN_REPLAY_MAX_TOKENS 16
+size_t gdn_replay_buffer_bytes(const gdn_dims* dims, int L);
+int gdn_replay_decode(const gdn_dims* dims, int L, const void* q, const void* k, const void* v,
+                      const void* g, const void* beta, float scale, float* ckpt, void* buffer,
+                      int* fill, void* out, void* stream);
+int gdn_replay_state(const gdn_dims* dims, int L, const float* ckpt, const void* buffer,
+                     const int* fill, float* h_out, void* stream);
+
 /* Reads and clears the library's device error word on the current device
- * (bit 1: a kernel gave up waiting for one of its own asynchronous copies).
+ * (bits, OR-ed: 1 = a kernel gave up waiting for one of its own asynchronous
+ * copies; 2 = a replay fill count was outside [0, L]).
  * Synchronises the device. Returns GDN_OK when the word was zero,
  * GDN_ERR_INTERNAL when it was not, GDN_ERR_CUDA if the read failed. */
 int gdn_check_device_error(void);
@@ -202,7 +242,8 @@ int gdn_version(void);
  * 7 chunk outputs, 8 forward state scan on tcgen05 tensor cores, 9 reverse
  * state scan on tcgen05 tensor cores (8 and 9 replace 1 and 2 for bf16
  * operands with Dk = Dv = 128), 10 single-token decode (replaces 5 when T = 1),
- * 11 q/k L2 normalisation, 12 its reverse (GDN_FLAG_QK_L2NORM only);
+ * 11 q/k L2 normalisation, 12 its reverse (GDN_FLAG_QK_L2NORM only),
+ * 13 replay decode, 14 replay state fold;
  * gdn_kernel_name(id) names them
  * ("" for an unknown id). Not part of the paper's method: instrumentation. */
 int gdn_profile_enable(int on);

@@ -119,3 +119,35 @@ def test_binding_rejects_cpu_tensors():
     q = torch.zeros(1, 64, 1, 64)
     with pytest.raises(gdn.GdnError):
         gdn.gdn_chunk_fwd(q, q, q, q, torch.zeros(1, 64, 1))
+
+
+def test_replay_sizes_and_validation(lib):
+    d = _dims(T=1, dtype=binding.GDN_F32)
+    # per (b, h): L slots of k, cumulative log-decay and delta, fp32
+    assert lib.gdn_replay_buffer_bytes(ctypes.byref(d), 16) == 2 * 3 * 16 * (2 * 128 + 128) * 4
+    assert lib.gdn_replay_buffer_bytes(ctypes.byref(_dims(T=1, Dk=64, Dv=128)), 1) == 2 * 3 * (2 * 64 + 128) * 4
+    assert lib.gdn_replay_buffer_bytes(ctypes.byref(d), 0) == 0
+    assert lib.gdn_replay_buffer_bytes(ctypes.byref(d), binding.GDN_REPLAY_MAX_TOKENS + 1) == 0
+    assert lib.gdn_replay_buffer_bytes(ctypes.byref(_dims(T=1, Dk=96)), 4) == 0
+    p, f = _fake(), ctypes.c_float(0.1)
+    dec = lib.gdn_replay_decode
+    ok_args = [p, p, p, p, p, f, p, p, p, p, None]
+    assert dec(ctypes.byref(_dims(T=2)), 4, *ok_args) == binding.GDN_ERR_SHAPE
+    assert dec(ctypes.byref(d), 0, *ok_args) == binding.GDN_ERR_INVALID_ARG
+    assert dec(ctypes.byref(d), 17, *ok_args) == binding.GDN_ERR_INVALID_ARG
+    assert dec(ctypes.byref(_dims(T=1, Dk=96)), 4, *ok_args) == binding.GDN_ERR_UNSUPPORTED
+    bad = list(ok_args)
+    bad[6] = None  # ckpt
+    assert dec(ctypes.byref(d), 4, *bad) == binding.GDN_ERR_INVALID_ARG
+    bad = list(ok_args)
+    bad[8] = _fake((1 << 20) + 2)  # fill not 4-byte aligned
+    assert dec(ctypes.byref(d), 4, *bad) == binding.GDN_ERR_INVALID_ARG
+    bad = list(ok_args)
+    bad[5] = ctypes.c_float(float("inf"))
+    assert dec(ctypes.byref(d), 4, *bad) == binding.GDN_ERR_INVALID_ARG
+    assert dec(ctypes.byref(_dims(B=0, T=1)), 4, None, None, None, None, None, f, None, None, None, None,
+               None) == binding.GDN_OK
+    sta = lib.gdn_replay_state
+    assert sta(ctypes.byref(d), 0, p, p, p, p, None) == binding.GDN_ERR_INVALID_ARG
+    assert sta(ctypes.byref(d), 4, p, p, p, None, None) == binding.GDN_ERR_INVALID_ARG
+    assert sta(ctypes.byref(_dims(B=0)), 4, None, None, None, None, None) == binding.GDN_OK
