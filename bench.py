@@ -444,8 +444,10 @@ def decode_leg(dev):
     """Recurrent kernel: decode steps (T = 1) with the state read and written once.
     B2 H48: L2 flushed before every step (a buffer twice the L2 size is read), the
     kernel timed alone by the library's per-launch events, queued behind a spin
-    kernel so that no host launch gap falls inside the measurement. B32 H48 (state 201 MB > L2): 30 steps back to back between two
-    CUDA events. Then the 2048-token prefill of the same geometry."""
+    kernel so that no host launch gap falls inside the measurement. B32 H48 (state
+    201 MB > L2): 30 steps back to back between two CUDA events, all queued behind a
+    spin kernel first. Then replay decode on the B32 batch and the 2048-token prefill
+    of the same geometry."""
     import torch
 
     import gated_deltanet_gdn_gb300 as gdn
@@ -482,6 +484,7 @@ def decode_leg(dev):
             ms = statistics.median(times)
         else:
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            torch.cuda._sleep(4_000_000)  # every step is queued before the timed region starts
             e0.record()
             for _ in range(30):
                 one()
@@ -511,10 +514,10 @@ def decode_leg(dev):
     return res
 
 
-def replay_leg(dev, recurrent_ms, L=16):
+def replay_leg(dev, recurrent_ms, L=8):
     """Replay decode (checkpoint + L-token buffer) on the B32 H48 Dk=Dv=128 fp32 decode
     batch: 2 L warm-up steps reach the steady fill cycle, then 4 L steps (4 folds) back to
-    back between two CUDA events. Bytes per step are averaged over the cycle: the
+    back between two CUDA events, queued behind a spin kernel. Bytes per step are averaged over the cycle: the
     checkpoint read, (L + 1) / 2 buffer slots read, one slot written, the checkpoint
     written once per L steps, the token row in and the output out."""
     import torch
@@ -535,6 +538,7 @@ def replay_leg(dev, recurrent_ms, L=16):
     torch.cuda.synchronize()
     steps = 4 * L
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda._sleep(4_000_000)  # every step is queued before the timed region starts
     e0.record()
     for _ in range(steps):
         one()

@@ -158,7 +158,7 @@ struct RecurrentArgs {
 
 // Replay decode (replay.cu): checkpoint [B,H,DK,DV] fp32, buffer [B,H,L][2 DK + DV] fp32
 // slots (k, cumulative log-decay G, delta d), fill [B,H] slots in use.
-constexpr int REPLAY_MAX_TOKENS = 16;
+constexpr int REPLAY_MAX_TOKENS = 8;
 struct ReplayArgs {
   int B, H, DK, DV, L, per_channel, bf16, qk_norm;
   const void *q, *k, *v, *g, *beta;

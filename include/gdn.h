@@ -209,7 +209,7 @@ int gdn_recurrent(const gdn_dims* dims, const void* q, const void* k, const void
  * the caller sets fill to 0 afterwards. Errors as gdn_recurrent, plus
  * GDN_ERR_SHAPE for dims.T != 1 in gdn_replay_decode and GDN_ERR_INVALID_ARG
  * for L out of range. Returns 0 bytes for invalid dims or L. */
-#define GDN_REPLAY_MAX_TOKENS 16
+#define GDN_REPLAY_MAX_TOKENS 8
 size_t gdn_replay_buffer_bytes(const gdn_dims* dims, int L);
 int gdn_replay_decode(const gdn_dims* dims, int L, const void* q, const void* k, const void* v,
                       const void* g, const void* beta, float scale, float* ckpt, void* buffer,

@@ -124,7 +124,7 @@ def test_binding_rejects_cpu_tensors():
 def test_replay_sizes_and_validation(lib):
     d = _dims(T=1, dtype=binding.GDN_F32)
     # per (b, h): L slots of k, cumulative log-decay and delta, fp32
-    assert lib.gdn_replay_buffer_bytes(ctypes.byref(d), 16) == 2 * 3 * 16 * (2 * 128 + 128) * 4
+    assert lib.gdn_replay_buffer_bytes(ctypes.byref(d), 8) == 2 * 3 * 8 * (2 * 128 + 128) * 4
     assert lib.gdn_replay_buffer_bytes(ctypes.byref(_dims(T=1, Dk=64, Dv=128)), 1) == 2 * 3 * (2 * 64 + 128) * 4
     assert lib.gdn_replay_buffer_bytes(ctypes.byref(d), 0) == 0
     assert lib.gdn_replay_buffer_bytes(ctypes.byref(d), binding.GDN_REPLAY_MAX_TOKENS + 1) == 0
@@ -134,7 +134,7 @@ def test_replay_sizes_and_validation(lib):
     ok_args = [p, p, p, p, p, f, p, p, p, p, None]
     assert dec(ctypes.byref(_dims(T=2)), 4, *ok_args) == binding.GDN_ERR_SHAPE
     assert dec(ctypes.byref(d), 0, *ok_args) == binding.GDN_ERR_INVALID_ARG
-    assert dec(ctypes.byref(d), 17, *ok_args) == binding.GDN_ERR_INVALID_ARG
+    assert dec(ctypes.byref(d), binding.GDN_REPLAY_MAX_TOKENS + 1, *ok_args) == binding.GDN_ERR_INVALID_ARG
     assert dec(ctypes.byref(_dims(T=1, Dk=96)), 4, *ok_args) == binding.GDN_ERR_UNSUPPORTED
     bad = list(ok_args)
     bad[6] = None  # ckpt

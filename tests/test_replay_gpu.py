@@ -31,7 +31,7 @@ def _decode(d, t0, t1, state, L, flags=0):
     return torch.cat(outs, 1), fills
 
 
-@pytest.mark.parametrize("L", [1, 5, 16])
+@pytest.mark.parametrize("L", [1, 5, 8])
 @pytest.mark.parametrize("dtype,dims,per_channel", [("f32", (128, 128), True), ("f32", (64, 128), False),
                                                    ("bf16", (128, 64), True), ("bf16", (64, 64), False)])
 def test_replay_decode_matches_oracle(L, dtype, dims, per_channel):
@@ -48,6 +48,21 @@ def test_replay_decode_matches_oracle(L, dtype, dims, per_channel):
     assert rel(h, h_ref) <= TOL["f32"]
     for t, f in enumerate(fills):  # the step that finds the buffer full folds it, then holds one token
         assert bool((f == (t % L) + 1).all()), t
+    assert gdn.gdn_check_device_error() == gdn.binding.GDN_OK
+
+
+def test_replay_several_heads_per_cta():
+    """B8 H48 (384 heads on at most 152 persistent CTAs, so each CTA runs its rings over
+    two or three heads) over 20 tokens with L = 8: every head against the oracle."""
+    L = 8
+    w = WORKLOADS["recurrent"].with_(B=8, T=20, h0_std=0.01)
+    host = make_inputs(w)
+    d = cuda_inputs(host)
+    state = gdn.replay_init(d["h0"], L)
+    out, _ = _decode(d, 0, w.T, state, L)
+    o_ref, h_ref = oracle_fwd(host)
+    assert rel(out, o_ref) <= TOL["f32"]
+    assert rel(gdn.gdn_replay_state(*state, L), h_ref) <= TOL["f32"]
     assert gdn.gdn_check_device_error() == gdn.binding.GDN_OK
 
 
@@ -72,7 +87,7 @@ def test_replay_state_is_the_next_checkpoint_bitwise():
 def test_replay_rollback_of_a_rejected_draft():
     """Decode 7 tokens, reject the last 3 (fill -= 3), decode 3 others: the outputs and the
     state are the oracle's for the accepted 4 tokens followed by the 3 new ones."""
-    L = 16
+    L = 8
     w = WORKLOADS["tiny_fwd"].with_(B=2, T=10, H=3, Dk=128, Dv=128, h0_std=0.3)
     host = make_inputs(w)
     d = cuda_inputs(host)
@@ -89,9 +104,9 @@ def test_replay_rollback_of_a_rejected_draft():
 
 def test_replay_scalar_decay_with_wipes_and_recurrent_agreement():
     """The scalar-decay decode geometry (B2 H48 Dk=Dv=128 fp32, g = logsigmoid(N(2,1)), a
-    -20 wipe at token 255) over 300 tokens with L = 16: within 1e-4 of the oracle and of
+    -20 wipe at token 255) over 300 tokens with L = 8: within 1e-4 of the oracle and of
     the token-recurrent decode of the same tokens."""
-    L = 16
+    L = 8
     w = WORKLOADS["recurrent"].with_(T=300, h0_std=0.01)
     host = make_inputs(w)
     d = cuda_inputs(host)
