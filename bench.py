@@ -172,9 +172,11 @@ def kernel_work(B, T, H, D, es=2):
         "chunk_out_kernel": (CD + CC + DD + CD + CD, C * D * D * 2 + C * C * D * 2),
         # reads dout, scale*Aqk, K-tilde, scale*Q-hat, -W, gam; writes dU, dS
         "chunk_scan_bwd_kernel": (CD + CC + 3 * CD + gam + CD + DD, C * C * D * 2 + 3 * C * D * D * 2),
-        # reads T, dout, v, U, dU, state, dS, beta; writes dv, dQ-hat, dBk, dK-tilde, dAqk, dAkk, dgam, dbeta_v
-        "chunk_dstate_kernel": (CC + 4 * CD + 2 * DD + C * es + 4 * CD + 2 * CC + gam + C * 4,
-                                C * C * D * 2 + 3 * C * D * D * 2 + 2 * C * C * D * 2),
+        # reads dout, U, state; writes dQ-hat, dAqk (beside the reverse scan, on a second stream)
+        "chunk_dqa_kernel": (2 * CD + DD + CD + CC, C * C * D * 2 + C * D * D * 2),
+        # reads T, v, U, dU, state, dS, beta; writes dv, dBk, dK-tilde, dAkk, dgam, dbeta_v
+        "chunk_dstate_kernel": (CC + 3 * CD + 2 * DD + C * es + 3 * CD + CC + gam + C * 4,
+                                2 * C * C * D * 2 + 2 * C * D * D * 2),
         # reads q, k, g, beta, dQ-hat, dBk, dK-tilde, dAqk, dAkk, dgam; writes dq, dk, dg and partials
         "chunk_grads_kernel": (3 * CD + C * es + 3 * CD + 2 * CC + gam + 3 * CD + 2 * 2 * C * 4,
                                4 * C * C * D * 2),
@@ -315,7 +317,7 @@ def run_gdn(args, world, rank, local):
                    "l2": "inputs larger than L2 (q,k,v,g,dout %.0f MB + residuals %.0f MB > 129 MB)" % (
                        5 * d["q"].numel() * 2 / 1e6, res.numel() / 1e6),
                    "parallelism": f"replicas x{world} (no collective)"},
-        "gpu_launches": 7 * args.steps,
+        "gpu_launches": 8 * args.steps,
         "roofline": roofline,
         "tensor": tensor,
         "kernels": kernels,

@@ -116,9 +116,38 @@ const char* kKernelNames[K_COUNT] = {"chunk_prep_kernel",    "chunk_scan_fwd_ker
                                      "chunk_bwd_finalize_kernel", "chunk_out_kernel",
                                      "chunk_scan_fwd_tc_kernel", "chunk_scan_bwd_tc_kernel",
                                      "decode_kernel", "l2norm_rows_kernel", "l2norm_bwd_kernel",
-                                     "replay_decode_kernel", "replay_state_kernel"};
+                                     "replay_decode_kernel", "replay_state_kernel", "chunk_dqa_kernel"};
 
 }  // namespace
+
+static std::mutex g_side_mutex;
+static cudaStream_t g_side_stream[64] = {};
+static cudaEvent_t g_fork_ev[64] = {}, g_join_ev[64] = {};
+
+cudaError_t side_fork(cudaStream_t s, SideStream* side) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  side->lock = std::unique_lock<std::mutex>(g_side_mutex);
+  if (!g_side_stream[dev]) {
+    if ((e = cudaEventCreateWithFlags(&g_fork_ev[dev], cudaEventDisableTiming)) != cudaSuccess) return e;
+    if ((e = cudaEventCreateWithFlags(&g_join_ev[dev], cudaEventDisableTiming)) != cudaSuccess) return e;
+    if ((e = cudaStreamCreateWithFlags(&g_side_stream[dev], cudaStreamNonBlocking)) != cudaSuccess) return e;
+  }
+  if ((e = cudaEventRecord(g_fork_ev[dev], s)) != cudaSuccess) return e;
+  if ((e = cudaStreamWaitEvent(g_side_stream[dev], g_fork_ev[dev], 0)) != cudaSuccess) return e;
+  side->stream = g_side_stream[dev];
+  side->join_ev = g_join_ev[dev];
+  return cudaSuccess;
+}
+
+cudaError_t side_join(cudaStream_t s, SideStream* side) {
+  cudaError_t e = cudaEventRecord(side->join_ev, side->stream);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(s, side->join_ev, 0);
+  side->lock.unlock();
+  return e;
+}
 
 void prof_mark(KernelId id, cudaStream_t s, bool begin) {
   if (!g_prof_on) return;
