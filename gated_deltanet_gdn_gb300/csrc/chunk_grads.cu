@@ -109,7 +109,9 @@ __global__ void __launch_bounds__(GR_THREADS, 2) chunk_grads_kernel(ChunkBwdArgs
   const T* g = static_cast<const T*>(a.g);
   const T* beta = static_cast<const T*>(a.beta);
 
-  // ---- asynchronous loads (per-channel g lands raw in X first)
+  // ---- asynchronous loads in two groups: what the cumulative decay, the row-scaled
+  // operands and the score products need (per-channel g lands raw in X first), then the
+  // state-product tiles that only the epilogue reads, which arrive during those phases
   T* graw = reinterpret_cast<T*>(sm + L::X);
   for (int i = tid; i < C * HC / EPC; i += GR_THREADS) {
     const int r = i / (HC / EPC), c = (i % (HC / EPC)) * EPC;
@@ -118,6 +120,16 @@ __global__ void __launch_bounds__(GR_THREADS, 2) chunk_grads_kernel(ChunkBwdArgs
     cp_async16(Ks.ptr(r, c), k + gi);
     if (PC) cp_async16(graw + r * HC + c, g + gi);
   }
+  {
+    if (tid < HC / 4) cp_async16(gcol_s + 4 * tid, a.ws.dgam + ch * DK + cbase + 4 * tid);  // dgam, scaled below
+    const T* sa = static_cast<const T*>(a.ws.daqk) + ch * (C * C);
+    const T* sk = static_cast<const T*>(a.ws.dakk) + ch * (C * C);
+    for (int i = tid; i < C * C / EPC; i += GR_THREADS) {
+      cp_async16(dAq.p + i * EPC, sa + i * EPC);
+      cp_async16(dAk.p + i * EPC, sk + i * EPC);
+    }
+  }
+  cp_async_commit();
   {
     // the C x Dk records are 64-column panels: this CTA's panel is contiguous
     const size_t pan = ch * (C * (size_t)DK) + (size_t)grp * C * HC;
@@ -129,13 +141,6 @@ __global__ void __launch_bounds__(GR_THREADS, 2) chunk_grads_kernel(ChunkBwdArgs
       cp_async16(dBk.p + i * EPC, s2 + i * EPC);
       cp_async16(dKt.p + i * EPC, s3 + i * EPC);
     }
-    if (tid < HC / 4) cp_async16(gcol_s + 4 * tid, a.ws.dgam + ch * DK + cbase + 4 * tid);  // dgam, scaled below
-    const T* sa = static_cast<const T*>(a.ws.daqk) + ch * (C * C);
-    const T* sk = static_cast<const T*>(a.ws.dakk) + ch * (C * C);
-    for (int i = tid; i < C * C / EPC; i += GR_THREADS) {
-      cp_async16(dAq.p + i * EPC, sa + i * EPC);
-      cp_async16(dAk.p + i * EPC, sk + i * EPC);
-    }
   }
   cp_async_commit();
   float* gsc = reinterpret_cast<float*>(sm + L::GSC);
@@ -143,7 +148,7 @@ __global__ void __launch_bounds__(GR_THREADS, 2) chunk_grads_kernel(ChunkBwdArgs
     beta_s[tid] = to_f32(beta[row0 + tid * rs]);
     if (!PC) gsc[tid] = to_f32(g[row0 + tid * rs]);
   }
-  cp_async_wait<0>();
+  cp_async_wait<1>();
   __syncthreads();
   if (tid < C) {  // the diagonal of dAqk only feeds dq and dk (its dG terms cancel exactly)
     diag_s[tid] = to_f32(dAq.at(tid, tid));
@@ -252,6 +257,7 @@ __global__ void __launch_bounds__(GR_THREADS, 2) chunk_grads_kernel(ChunkBwdArgs
     }
   }
 
+  cp_async_wait<0>();  // the state-product tiles
   __syncthreads();  // every warp is done reading X and XB: dG is staged there
   // one epilogue per element pair: every gradient term of (r, c) and (r, c + 1)
   float* dGs = reinterpret_cast<float*>(sm + L::DG);
