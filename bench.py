@@ -436,9 +436,28 @@ def e2e_leg(args, host, d, step, outputs, world):
     torch.cuda.synchronize()
     barrier(world)
     ms = max_over_ranks(e0.elapsed_time(e1) / n, world)
+    # the same copies with no compute: the host link's share of the step
+    e2, e3 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e2.record(s_in)
+    s_out.wait_event(e2)
+    for i in range(n):
+        b = i % 2
+        with torch.cuda.stream(s_in):
+            for k, v in pin_in.items():
+                dev_in[b][k].copy_(v, non_blocking=True)
+        with torch.cuda.stream(s_out):
+            for k, v in pin_out.items():
+                v.copy_(dev_out[b][k], non_blocking=True)
+    s_in.wait_stream(s_out)
+    e3.record(s_in)
+    torch.cuda.synchronize()
+    copy_ms = e2.elapsed_time(e3) / n
     tokens = host["q"].shape[0] * host["q"].shape[1]
     return {"value": round(world * tokens / (ms / 1e3), 1), "unit": "tokens/s", "ms_per_step": round(ms, 4),
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": n,
+            "copies_only_ms_per_step": round(copy_ms, 4),
+            "link_gbs_per_direction": round(max(h2d, d2h) / (copy_ms / 1e3) / 1e9, 1),
             "overlap": "inputs and results copied on their own streams, double-buffered against compute"}
 
 
