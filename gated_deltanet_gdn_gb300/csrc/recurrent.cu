@@ -36,7 +36,9 @@ struct RecSmem {
   float inv[2][TB];   // q/k L2 normalisation: inverse norms of the batch's q and k rows
 };
 
-template <class T, int DK, bool PC, int TB>
+// QK: q/k L2 normalisation (GDN_FLAG_QK_L2NORM) is compiled in only when asked for, so
+// the plain per-token chain carries no extra multiplies.
+template <class T, int DK, bool PC, int TB, bool QK>
 __global__ void __launch_bounds__(REC_THREADS) recurrent_kernel(RecurrentArgs p) {
   constexpr int RPT = DK / REC_TPC;  // key rows per thread
   __shared__ __align__(16) RecSmem<T, DK, TB> sm;
@@ -100,13 +102,13 @@ __global__ void __launch_bounds__(REC_THREADS) recurrent_kernel(RecurrentArgs p)
     cp_async_wait<0>();
     __syncthreads();  // batch bi visible; everyone finished batch bi-1 (its buffer is free)
     if (bi + 1 < nbatch) stage(buf ^ 1, t0 + TB);
-    if (PC || p.qk_norm) {
+    if (PC || QK) {
       if (PC)
         for (int i = tid; i < nt * DK; i += REC_THREADS) {
           const int tt = i / DK, c = i % DK;
           sm.a[tt][c] = expf(to_f32(sm.graw[buf][tt][c]));
         }
-      if (p.qk_norm) {  // one warp per q or k row of the batch
+      if (QK) {  // one warp per q or k row of the batch
         const int warp = tid >> 5, lane = tid & 31;
         for (int rr = warp; rr < 2 * nt; rr += REC_THREADS / 32) {
           const float inv = warp_row_inv_norm<DK>((rr & 1) ? sm.k[buf][rr >> 1] : sm.q[buf][rr >> 1], lane);
@@ -118,7 +120,7 @@ __global__ void __launch_bounds__(REC_THREADS) recurrent_kernel(RecurrentArgs p)
     for (int tt = 0; tt < nt; ++tt) {
       const float bt = sm.beta[buf][tt];
       const float as = PC ? 1.f : expf(sm.gs[buf][tt]);
-      const float nq = p.qk_norm ? sm.inv[0][tt] : 1.f, nk = p.qk_norm ? sm.inv[1][tt] : 1.f;
+      const float nq = QK ? sm.inv[0][tt] : 1.f, nk = QK ? sm.inv[1][tt] : 1.f;
       float pv[REC_VEC] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int i = 0; i < RPT; ++i) {
@@ -180,10 +182,17 @@ __global__ void __launch_bounds__(REC_THREADS) recurrent_kernel(RecurrentArgs p)
 template <class T, int DK, int TB>
 void launch_rec_tb(const RecurrentArgs& a, cudaStream_t s) {
   dim3 grid(a.DV / REC_COLS, a.B * a.H);
-  if (a.per_channel)
-    recurrent_kernel<T, DK, true, TB><<<grid, REC_THREADS, 0, s>>>(a);
-  else
-    recurrent_kernel<T, DK, false, TB><<<grid, REC_THREADS, 0, s>>>(a);
+  if (a.qk_norm) {
+    if (a.per_channel)
+      recurrent_kernel<T, DK, true, TB, true><<<grid, REC_THREADS, 0, s>>>(a);
+    else
+      recurrent_kernel<T, DK, false, TB, true><<<grid, REC_THREADS, 0, s>>>(a);
+  } else {
+    if (a.per_channel)
+      recurrent_kernel<T, DK, true, TB, false><<<grid, REC_THREADS, 0, s>>>(a);
+    else
+      recurrent_kernel<T, DK, false, TB, false><<<grid, REC_THREADS, 0, s>>>(a);
+  }
 }
 
 template <class T, int DK>
