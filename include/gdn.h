@@ -35,7 +35,10 @@
  * only enqueues kernels on `stream` (a cudaStream_t; NULL = legacy default
  * stream) and returns; results are ready when the stream reaches that point.
  * Calls keep no state between them and may run concurrently on different
- * streams with disjoint buffers. Outputs must not alias inputs, except
+ * streams with disjoint buffers. gdn_chunk_bwd forks part of its work onto a
+ * stream the library owns (one per device, created on first use) and joins it
+ * back onto `stream` before its last kernel, so the caller sees one ordered
+ * sequence on `stream`; under stream capture, make one call before capturing. Outputs must not alias inputs, except
  * h_final == h0 in gdn_recurrent (in-place state carry).
  *
  * Errors. Arguments are validated before anything is enqueued; a failed
