@@ -187,12 +187,16 @@ def kernel_work(B, T, H, D, es=2):
     return {k: (b * n, f * n) for k, (b, f) in per.items()}
 
 
+# the files the chunk kernels (the ones profiles/traffic.json covers) are compiled from
+CHUNK_KERNEL_SOURCES = ("chunk_fwd.cu", "chunk_bwd.cu", "chunk_grads.cu", "chunk_scan_tc.cu",
+                        "common.cuh", "umma.cuh", "kernels.h")
+
+
 def kernel_source_hash():
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "gated_deltanet_gdn_gb300", "csrc")
-    for f in sorted(os.listdir(csrc)):
-        if f.endswith((".cu", ".cuh", ".h")):
-            h.update(open(os.path.join(csrc, f), "rb").read())
+    for f in CHUNK_KERNEL_SOURCES:
+        h.update(open(os.path.join(csrc, f), "rb").read())
     return h.hexdigest()[:16]
 
 

@@ -34,7 +34,7 @@ EXPORTED = ("gdn_chunk_residual_bytes", "gdn_chunk_bwd_workspace_bytes", "gdn_ch
             "gdn_chunk_bwd", "gdn_recurrent", "gdn_check_device_error", "gdn_status_string",
             "gdn_version", "gdn_profile_enable", "gdn_profile_read", "gdn_kernel_name",
             "gdn_chunk_fwd_noalloc", "gdn_replay_buffer_bytes", "gdn_replay_decode",
-            "gdn_replay_state")
+            "gdn_replay_state", "gdn_selftest_wait_timeout")
 KERNEL_COUNT = 16
 GDN_REPLAY_MAX_TOKENS = 8
 
@@ -98,6 +98,8 @@ def load(build_if_needed: bool = True) -> ctypes.CDLL:
             lib.gdn_replay_decode.restype = i
             lib.gdn_replay_state.argtypes = [pd, i, vp, vp, vp, vp, vp]
             lib.gdn_replay_state.restype = i
+            lib.gdn_selftest_wait_timeout.argtypes = [ctypes.c_uint, vp]
+            lib.gdn_selftest_wait_timeout.restype = i
             _lib = lib
     return _lib
 
@@ -297,6 +299,14 @@ def gdn_replay_state(ckpt, buffer, fill, L: int, *, h_out=None) -> torch.Tensor:
                                      _ptr(h_out), _stream(dev))
     _check("gdn_replay_state", st)
     return h_out
+
+
+def gdn_selftest_wait_timeout(max_tries: int = 1024, device: Optional[torch.device] = None) -> None:
+    """Launch the library's wait-timeout self-test kernel (see include/gdn.h)."""
+    dev = device if device is not None else torch.device("cuda", torch.cuda.current_device())
+    with torch.cuda.device(dev):
+        st = load().gdn_selftest_wait_timeout(int(max_tries), _stream(dev))
+    _check("gdn_selftest_wait_timeout", st)
 
 
 def gdn_check_device_error() -> int:

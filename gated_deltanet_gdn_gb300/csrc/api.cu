@@ -6,6 +6,7 @@
 #include <vector>
 
 #include "../../include/gdn.h"
+#include "common.cuh"
 #include "kernels.h"
 
 namespace gdn {
@@ -33,6 +34,18 @@ unsigned* device_error_word() {
 }
 
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// One thread waits on an mbarrier that nothing ever arrives on, giving up after max_tries
+// tries exactly as the kernels' own bounded waits do: the error word gets
+// ERR_WAIT_TIMEOUT and the kernel returns normally.
+__global__ void wait_timeout_selftest_kernel(unsigned* err, unsigned max_tries) {
+  __shared__ uint64_t bar;
+  mbar_init(&bar, 1);
+  fence_mbar_init();
+  for (unsigned i = 0; i < max_tries; ++i)
+    if (mbar_try_wait(&bar, 0u)) return;
+  atomicOr(err, ERR_WAIT_TIMEOUT);
+}
 
 // Common dims checks. Returns GDN_OK or the status to report.
 int check_dims(const gdn_dims* d, bool chunked) {
@@ -343,6 +356,14 @@ int gdn_replay_state(const gdn_dims* d, int L, const float* ckpt, const void* bu
   a.err = device_error_word();
   if (!a.err) return GDN_ERR_CUDA;
   return launch_status(launch_replay_state(a, static_cast<cudaStream_t>(stream)));
+}
+
+int gdn_selftest_wait_timeout(unsigned max_tries, void* stream) {
+  if (max_tries == 0 || max_tries > (1u << 16)) return GDN_ERR_INVALID_ARG;
+  unsigned* err = device_error_word();
+  if (!err) return GDN_ERR_CUDA;
+  wait_timeout_selftest_kernel<<<1, 1, 0, static_cast<cudaStream_t>(stream)>>>(err, max_tries);
+  return launch_status(cudaGetLastError());
 }
 
 int gdn_check_device_error(void) {

@@ -220,6 +220,14 @@ int gdn_replay_decode(const gdn_dims* dims, int L, const void* q, const void* k,
 int gdn_replay_state(const gdn_dims* dims, int L, const float* ckpt, const void* buffer,
                      const int* fill, float* h_out, void* stream);
 
+/* Self-test of the failure path: launches a one-thread kernel that waits on an
+ * mbarrier nothing arrives on and gives up after max_tries tries (1 .. 65536),
+ * like every wait in the library's kernels. The kernel then sets bit 1 of the
+ * device error word and returns, and the context stays usable. The next
+ * gdn_check_device_error returns GDN_ERR_INTERNAL. Not part of the method:
+ * it lets a caller or a test see the error path work without a GPU fault. */
+int gdn_selftest_wait_timeout(unsigned max_tries, void* stream);
+
 /* Reads and clears the library's device error word on the current device
  * (bits, OR-ed: 1 = a kernel gave up waiting for one of its own asynchronous
  * copies; 2 = a replay fill count was outside [0, L]).
