@@ -295,6 +295,8 @@ struct DstLayout {
 // second S0^T panel is prefetched into v's buffer as soon as dv has left it.
 template <int DK, int DV>
 __global__ void __launch_bounds__(DST_THREADS, 2) chunk_dstate_kernel(ChunkBwdArgs a) {
+  pdl_wait();
+  pdl_trigger();
   typedef bf16 T;
   typedef DstLayout<DK, DV> L;
   constexpr int NPAN = DK / 64;
@@ -526,9 +528,8 @@ cudaError_t launch_bwd_t(const ChunkBwdArgs& a, cudaStream_t s) {
     auto kern = chunk_dstate_kernel<DK, DV>;
     if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes)) != cudaSuccess) return e;
     prof_mark(K_DSTATE, s, true);
-    kern<<<dim3(N, BH), DST_THREADS, bytes, s>>>(a);
+    if ((e = launch_pdl(kern, dim3(N, BH), dim3(DST_THREADS), bytes, s, a)) != cudaSuccess) return e;
     prof_mark(K_DSTATE, s, false);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   if ((e = side_join(s, &side)) != cudaSuccess) return e;
   return launch_chunk_grads(a, s);

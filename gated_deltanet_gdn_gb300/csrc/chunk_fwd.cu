@@ -172,6 +172,8 @@ __device__ __noinline__ void prep_pairwise(bool unsafe1, bool unsafe2, const T* 
 
 template <class T, int DK, int DV, bool PC>
 __global__ void __launch_bounds__(PREP_THREADS) chunk_prep_kernel(ChunkFwdArgs a) {
+  pdl_wait();
+  pdl_trigger();
   typedef PrepLayout<T, DK, DV> L;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = align1024(smem_raw);
@@ -596,6 +598,8 @@ struct OutLayout {
 
 template <class T, int DK, int DV>
 __global__ void __launch_bounds__(OUT_THREADS) chunk_out_kernel(ChunkFwdArgs a) {
+  pdl_wait();
+  pdl_trigger();
   typedef OutLayout<T, DK, DV> L;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = align1024(smem_raw);
@@ -654,11 +658,9 @@ cudaError_t launch_fwd_t(const ChunkFwdArgs& a, cudaStream_t s) {
     if (e != cudaSuccess) return e;
     if (N > 0) {
       prof_mark(K_PREP, s, true);
-      kern<<<dim3(N, BH), PREP_THREADS, bytes, s>>>(a);
+      if ((e = launch_pdl(kern, dim3(N, BH), dim3(PREP_THREADS), bytes, s, a)) != cudaSuccess) return e;
       prof_mark(K_PREP, s, false);
     }
-    e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
   }
   if (scan_tc_applies(a.bf16, DK, DV)) {
     if ((e = launch_scan_fwd_tc(a, s)) != cudaSuccess) return e;
@@ -678,10 +680,10 @@ cudaError_t launch_fwd_t(const ChunkFwdArgs& a, cudaStream_t s) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
     if (e != cudaSuccess) return e;
     prof_mark(K_OUT, s, true);
-    kern<<<dim3(N, BH), OUT_THREADS, bytes, s>>>(a);
+    if ((e = launch_pdl(kern, dim3(N, BH), dim3(OUT_THREADS), bytes, s, a)) != cudaSuccess) return e;
     prof_mark(K_OUT, s, false);
   }
-  return cudaGetLastError();
+  return cudaSuccess;
 }
 
 template <class T>

@@ -76,6 +76,8 @@ __device__ __noinline__ float pw_dy(const Tile<bf16, C, C>* dP, const HTile* xs,
 
 template <bool PC>
 __global__ void __launch_bounds__(GR_THREADS, 2) chunk_grads_kernel(ChunkBwdArgs a) {
+  pdl_wait();
+  pdl_trigger();
   typedef bf16 T;
   typedef GrLayout L;
   extern __shared__ uint8_t smem_raw[];
@@ -416,6 +418,8 @@ __global__ void __launch_bounds__(GR_THREADS, 2) chunk_grads_kernel(ChunkBwdArgs
 // dbeta = dbeta_v + the channel groups' partials (and scalar-decay dg), fixed order.
 template <bool PC>
 __global__ void chunk_bwd_finalize_kernel(ChunkBwdArgs a) {
+  pdl_wait();
+  pdl_trigger();
   const size_t total = (size_t)a.B * a.H * a.T;
   const int N = a.T / C, NGRP = a.DK / HC;
   for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (size_t)gridDim.x * blockDim.x) {
@@ -445,18 +449,15 @@ cudaError_t launch_chunk_grads(const ChunkBwdArgs& a, cudaStream_t s) {
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
   if (e != cudaSuccess) return e;
   prof_mark(K_GRADS, s, true);
-  kern<<<dim3(a.DK / HC, N, BH), GR_THREADS, bytes, s>>>(a);
+  if ((e = launch_pdl(kern, dim3(a.DK / HC, N, BH), dim3(GR_THREADS), bytes, s, a)) != cudaSuccess) return e;
   prof_mark(K_GRADS, s, false);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
   const size_t total = (size_t)BH * a.T;
   const int blocks = (int)((total + 255) / 256 < 4096 ? (total + 255) / 256 : 4096);
   prof_mark(K_FINALIZE, s, true);
-  if (a.per_channel)
-    chunk_bwd_finalize_kernel<true><<<blocks, 256, 0, s>>>(a);
-  else
-    chunk_bwd_finalize_kernel<false><<<blocks, 256, 0, s>>>(a);
+  e = launch_pdl(a.per_channel ? chunk_bwd_finalize_kernel<true> : chunk_bwd_finalize_kernel<false>, dim3(blocks),
+                 dim3(256), 0, s, a);
   prof_mark(K_FINALIZE, s, false);
-  return cudaGetLastError();
+  return e;
 }
 
 }  // namespace gdn

@@ -144,6 +144,7 @@ struct TcFwdLayout {
 };
 
 __global__ void __launch_bounds__(TC_THREADS, 1) chunk_scan_fwd_tc_kernel(ChunkFwdArgs a) {
+  pdl_wait();  // no early trigger: one wave for the whole scan, successors must not park beside it
   typedef TcFwdLayout L;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = align1024(smem_raw);
@@ -326,6 +327,7 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, i
 
 __global__ void __launch_bounds__(TC_THREADS, 1)
     chunk_scan_bwd_tc_kernel(ChunkBwdArgs a, const __grid_constant__ CUtensorMap dout_map) {
+  pdl_wait();  // no early trigger: one wave for the whole scan, successors must not park beside it
   typedef TcBwdLayout L;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = align1024(smem_raw);
@@ -503,9 +505,9 @@ cudaError_t launch_scan_fwd_tc(const ChunkFwdArgs& a, cudaStream_t s) {
   cudaError_t e = cudaFuncSetAttribute(chunk_scan_fwd_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
   if (e != cudaSuccess) return e;
   prof_mark(K_SCAN_FWD_TC, s, true);
-  chunk_scan_fwd_tc_kernel<<<a.B * a.H, TC_THREADS, bytes, s>>>(a);
+  e = launch_pdl(chunk_scan_fwd_tc_kernel, dim3(a.B * a.H), dim3(TC_THREADS), bytes, s, a);
   prof_mark(K_SCAN_FWD_TC, s, false);
-  return cudaGetLastError();
+  return e;
 }
 
 cudaError_t launch_scan_bwd_tc(const ChunkBwdArgs& a, cudaStream_t s) {
@@ -526,9 +528,9 @@ cudaError_t launch_scan_bwd_tc(const ChunkBwdArgs& a, cudaStream_t s) {
   cudaError_t e = cudaFuncSetAttribute(chunk_scan_bwd_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
   if (e != cudaSuccess) return e;
   prof_mark(K_SCAN_BWD_TC, s, true);
-  chunk_scan_bwd_tc_kernel<<<a.B * a.H, TC_THREADS, bytes, s>>>(a, map);
+  e = launch_pdl(chunk_scan_bwd_tc_kernel, dim3(a.B * a.H), dim3(TC_THREADS), bytes, s, a, map);
   prof_mark(K_SCAN_BWD_TC, s, false);
-  return cudaGetLastError();
+  return e;
 }
 
 }  // namespace gdn

@@ -480,6 +480,34 @@ __device__ __forceinline__ void st4(float* p, const float (&x)[4]) {
   *reinterpret_cast<float4*>(p) = make_float4(x[0], x[1], x[2], x[3]);
 }
 
+// ------------------------------------------------------------------ programmatic dependent launch
+// The chunk kernels are launched with programmatic stream serialisation: a kernel's grid
+// may be scheduled while the previous kernel in the stream is still finishing. Every such
+// kernel calls pdl_wait() before it touches global memory (it returns once the previous
+// grid has completed and its writes are visible). Kernels of many waves also call
+// pdl_trigger() at the start, so the next kernel is scheduled while their last wave runs;
+// the single-wave state scans do not, or the next kernel's CTAs would occupy the SMs the
+// scans leave free for the whole scan. Both are no-ops for a grid launched without the
+// attribute.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;\n" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory"); }
+
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                              Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, args...);
+}
+
 // ------------------------------------------------------------------ misc helpers
 __host__ __device__ constexpr int a1k(int x) { return (x + 1023) / 1024 * 1024; }
 __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
