@@ -95,6 +95,24 @@ __global__ void __launch_bounds__(REC_THREADS) recurrent_kernel(RecurrentArgs p)
     cp_async_commit();
   };
 
+  // The loop is software-pipelined by one token: token t's output partials are reduced in
+  // the same butterfly as token t + 1's S^T k, and written then.
+  float ovp[REC_VEC] = {0.f, 0.f, 0.f, 0.f};
+  size_t rowp = 0;
+  bool pend = false;
+  auto write_out = [&](size_t row, const float (&ov)[REC_VEC]) {
+    if (part != 0) return;
+    T* o = static_cast<T*>(p.out) + row * DV + col0;
+    if (sizeof(T) == 4) {
+      *reinterpret_cast<float4*>(o) = make_float4(p.scale * ov[0], p.scale * ov[1], p.scale * ov[2], p.scale * ov[3]);
+    } else {
+      __align__(8) T tmp[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) tmp[j] = from_f32<T>(p.scale * ov[j]);
+      *reinterpret_cast<uint2*>(o) = *reinterpret_cast<const uint2*>(tmp);
+    }
+  };
+
   const int nbatch = (T_ + TB - 1) / TB;
   if (nbatch > 0) stage(0, 0);
   for (int bi = 0; bi < nbatch; ++bi) {
@@ -133,14 +151,21 @@ __global__ void __launch_bounds__(REC_THREADS) recurrent_kernel(RecurrentArgs p)
           pv[j] = fmaf(S[i][j], kr, pv[j]);
         }
       }
+      // one butterfly for this token's S^T k and the previous token's output partials:
+      // the two reductions are independent, and each keeps its own order (xor 1, 2, 4, 8)
 #pragma unroll
       for (int off = 1; off < REC_TPC; off <<= 1)
 #pragma unroll
-        for (int j = 0; j < REC_VEC; ++j) pv[j] += __shfl_xor_sync(0xffffffffu, pv[j], off);
+        for (int j = 0; j < REC_VEC; ++j) {
+          pv[j] += __shfl_xor_sync(0xffffffffu, pv[j], off);
+          ovp[j] += __shfl_xor_sync(0xffffffffu, ovp[j], off);
+        }
+      if (pend) write_out(rowp, ovp);
       float d[REC_VEC];
 #pragma unroll
       for (int j = 0; j < REC_VEC; ++j) d[j] = bt * (to_f32(sm.v[buf][tt][cg * REC_VEC + j]) - pv[j]);
-      float ov[REC_VEC] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int j = 0; j < REC_VEC; ++j) ovp[j] = 0.f;
 #pragma unroll
       for (int i = 0; i < RPT; ++i) {
         const int r = part + REC_TPC * i;
@@ -149,27 +174,19 @@ __global__ void __launch_bounds__(REC_THREADS) recurrent_kernel(RecurrentArgs p)
 #pragma unroll
         for (int j = 0; j < REC_VEC; ++j) {
           S[i][j] = fmaf(kr, d[j], S[i][j]);
-          ov[j] = fmaf(S[i][j], qr, ov[j]);
+          ovp[j] = fmaf(S[i][j], qr, ovp[j]);
         }
       }
-#pragma unroll
-      for (int off = 1; off < REC_TPC; off <<= 1)
-#pragma unroll
-        for (int j = 0; j < REC_VEC; ++j) ov[j] += __shfl_xor_sync(0xffffffffu, ov[j], off);
-      if (part == 0) {
-        const size_t row = ((size_t)b * T_ + t0 + tt) * H + h;
-        T* o = static_cast<T*>(p.out) + row * DV + col0;
-        if (sizeof(T) == 4) {
-          *reinterpret_cast<float4*>(o) =
-              make_float4(p.scale * ov[0], p.scale * ov[1], p.scale * ov[2], p.scale * ov[3]);
-        } else {
-          __align__(8) T tmp[4];
-#pragma unroll
-          for (int j = 0; j < 4; ++j) tmp[j] = from_f32<T>(p.scale * ov[j]);
-          *reinterpret_cast<uint2*>(o) = *reinterpret_cast<const uint2*>(tmp);
-        }
-      }
+      rowp = ((size_t)b * T_ + t0 + tt) * H + h;
+      pend = true;
     }
+  }
+  if (pend) {  // the last token's output
+#pragma unroll
+    for (int off = 1; off < REC_TPC; off <<= 1)
+#pragma unroll
+      for (int j = 0; j < REC_VEC; ++j) ovp[j] += __shfl_xor_sync(0xffffffffu, ovp[j], off);
+    write_out(rowp, ovp);
   }
 #pragma unroll
   for (int i = 0; i < RPT; ++i) {
