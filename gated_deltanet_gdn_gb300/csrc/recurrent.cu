@@ -31,7 +31,7 @@ struct RecSmem {
   T v[2][TB][REC_COLS];
   T graw[2][TB][DK];  // per-channel g (scalar g uses gs)
   float a[TB][DK];    // exp(g) of the batch being computed
-  float gs[2][TB];
+  float gs[2][TB];    // scalar decay: exp(g) per token
   float beta[2][TB];
   float inv[2][TB];   // q/k L2 normalisation: inverse norms of the batch's q and k rows
 };
@@ -90,7 +90,7 @@ __global__ void __launch_bounds__(REC_THREADS) recurrent_kernel(RecurrentArgs p)
     if (tid < nt) {
       const size_t row = ((size_t)b * T_ + t0 + tid) * H + h;
       sm.beta[buf][tid] = to_f32(beta[row]);
-      if (!PC) sm.gs[buf][tid] = to_f32(g[row]);
+      if (!PC) sm.gs[buf][tid] = expf(to_f32(g[row]));  // the decay factor, off the token chain
     }
     cp_async_commit();
   };
@@ -137,7 +137,7 @@ __global__ void __launch_bounds__(REC_THREADS) recurrent_kernel(RecurrentArgs p)
     }
     for (int tt = 0; tt < nt; ++tt) {
       const float bt = sm.beta[buf][tt];
-      const float as = PC ? 1.f : expf(sm.gs[buf][tt]);
+      const float as = PC ? 1.f : sm.gs[buf][tt];
       const float nq = QK ? sm.inv[0][tt] : 1.f, nk = QK ? sm.inv[1][tt] : 1.f;
       float pv[REC_VEC] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
