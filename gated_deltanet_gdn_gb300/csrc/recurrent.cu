@@ -22,7 +22,8 @@ constexpr int REC_COLS = 32;                 // value columns per CTA
 constexpr int REC_VEC = 4;                   // value columns per thread
 constexpr int REC_TPC = 16;                  // threads sharing a column group
 constexpr int REC_THREADS = (REC_COLS / REC_VEC) * REC_TPC;  // 128
-// Tokens per staged batch (TB): 8 (static smem <= 48 KB).
+// Tokens per staged batch (TB): 16, in dynamic shared memory (about 61 KB at Dk = 128 fp32,
+// three CTAs per SM); a batch boundary costs one wait and one barrier.
 
 template <class T, int DK, int TB>
 struct RecSmem {
@@ -41,7 +42,8 @@ struct RecSmem {
 template <class T, int DK, bool PC, int TB, bool QK>
 __global__ void __launch_bounds__(REC_THREADS) recurrent_kernel(RecurrentArgs p) {
   constexpr int RPT = DK / REC_TPC;  // key rows per thread
-  __shared__ __align__(16) RecSmem<T, DK, TB> sm;
+  extern __shared__ __align__(16) uint8_t rec_smem[];
+  RecSmem<T, DK, TB>& sm = *reinterpret_cast<RecSmem<T, DK, TB>*>(rec_smem);
   const int tid = threadIdx.x;
   const int cg = tid / REC_TPC;    // column group 0..7
   const int part = tid % REC_TPC;  // row interleave 0..15
@@ -196,28 +198,29 @@ __global__ void __launch_bounds__(REC_THREADS) recurrent_kernel(RecurrentArgs p)
   }
 }
 
+template <class T, int DK, int TB, bool PC, bool QK>
+cudaError_t launch_rec_one(const RecurrentArgs& a, cudaStream_t s) {
+  auto kern = recurrent_kernel<T, DK, PC, TB, QK>;
+  const int bytes = (int)sizeof(RecSmem<T, DK, TB>);
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e != cudaSuccess) return e;
+  kern<<<dim3(a.DV / REC_COLS, a.B * a.H), REC_THREADS, bytes, s>>>(a);
+  return cudaGetLastError();
+}
+
 template <class T, int DK, int TB>
-void launch_rec_tb(const RecurrentArgs& a, cudaStream_t s) {
-  dim3 grid(a.DV / REC_COLS, a.B * a.H);
-  if (a.qk_norm) {
-    if (a.per_channel)
-      recurrent_kernel<T, DK, true, TB, true><<<grid, REC_THREADS, 0, s>>>(a);
-    else
-      recurrent_kernel<T, DK, false, TB, true><<<grid, REC_THREADS, 0, s>>>(a);
-  } else {
-    if (a.per_channel)
-      recurrent_kernel<T, DK, true, TB, false><<<grid, REC_THREADS, 0, s>>>(a);
-    else
-      recurrent_kernel<T, DK, false, TB, false><<<grid, REC_THREADS, 0, s>>>(a);
-  }
+cudaError_t launch_rec_tb(const RecurrentArgs& a, cudaStream_t s) {
+  if (a.qk_norm)
+    return a.per_channel ? launch_rec_one<T, DK, TB, true, true>(a, s) : launch_rec_one<T, DK, TB, false, true>(a, s);
+  return a.per_channel ? launch_rec_one<T, DK, TB, true, false>(a, s) : launch_rec_one<T, DK, TB, false, false>(a, s);
 }
 
 template <class T, int DK>
 cudaError_t launch_rec_t(const RecurrentArgs& a, cudaStream_t s) {
   prof_mark(K_RECURRENT, s, true);
-  launch_rec_tb<T, DK, 8>(a, s);  // single-token calls go to decode_kernel (decode.cu)
+  const cudaError_t e = launch_rec_tb<T, DK, 16>(a, s);  // single-token calls go to decode_kernel (decode.cu)
   prof_mark(K_RECURRENT, s, false);
-  return cudaGetLastError();
+  return e;
 }
 
 }  // namespace
