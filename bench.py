@@ -634,7 +634,8 @@ def run_reference(args, world, rank):
     pairs = cpu_pairs(w)
     tokens = len(pairs) * w.T / w.H
     steps = max(1, min(args.steps, 10))
-    for _ in range(max(0, min(args.warmup, 1))):
+    warm = max(3, min(args.warmup, 5))  # at least three, and bounded: each step is seconds of CPU
+    for _ in range(warm):
         oracle_sample(w, host, pairs)
     t0 = time.perf_counter()
     for _ in range(steps):
@@ -642,7 +643,7 @@ def run_reference(args, world, rank):
     sec = (time.perf_counter() - t0) / steps
     value = tokens / sec
     line = {"impl": "reference", "metric": METRIC, "value": round(value, 1), "unit": "tokens/s",
-            "n_gpus": world, "steps": steps, "warmup": min(args.warmup, 1), "ms_per_step": round(sec * 1e3, 2),
+            "n_gpus": world, "steps": steps, "warmup": warm, "ms_per_step": round(sec * 1e3, 2),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": {"workload": "chunked fwd+bwd, B8 T4096 H6 Dk=Dv=128 (bounded sample, see cpu_baseline)"},
             "cpu_baseline": {"value": round(value, 1), "unit": "tokens/s", "cores": len(pairs), "kind": "oracle",
