@@ -371,3 +371,41 @@ def test_input_generator_recipe():
     assert d2["q"].dtype.is_floating_point and str(d2["q"].dtype) == "torch.bfloat16"
     assert d2["h0"].dtype == d2["dh_final"].dtype
     assert float(d2["g"].double().max()) <= 0.0
+
+
+@pytest.mark.parametrize("L,per_channel", [(1, True), (3, True), (8, True), (5, False)])
+def test_replay_form_equals_token_serial(L, per_channel):
+    """The checkpoint + buffer form the replay decode kernel follows (outputs from reads
+    of the checkpoint, lazy fold when the buffer is full) equals the token-serial oracle,
+    across several folds and with a -20 wipe inside the buffer."""
+    from oracle import replay_mirror as rm
+
+    w = WORKLOADS["tiny_fwd"].with_(T=23, H=2, Dk=8, Dv=6, h0_std=0.5, g_per_channel=per_channel)
+    a = _arrays(w)
+    a["g"][:, 11] = -20.0  # a wipe while tokens are buffered
+    out, hT = oracle.fwd(a["q"], a["k"], a["v"], a["g"], a["beta"], a["h0"])
+    o2, h2, fills = rm.decode(a["q"], a["k"], a["v"], a["g"], a["beta"], a["h0"], L)
+    assert oracle.rel_l2(o2, out) < 1e-12 and oracle.rel_l2(h2, hT) < 1e-12
+    assert (fills == (w.T - 1) % L + 1).all()
+
+
+def test_replay_rollback_forgets_the_rejected_tokens():
+    """Lowering the fill count by r forgets exactly the last r tokens: decoding 7 tokens,
+    rolling back 3 and decoding 3 others equals the oracle on the accepted sequence."""
+    from oracle import replay_mirror as rm
+
+    w = WORKLOADS["tiny_fwd"].with_(T=10, H=1, Dk=8, Dv=6, h0_std=0.5)
+    a = _arrays(w)
+    scale = w.Dk ** -0.5
+    ckpt, slots, fill, outs = a["h0"][0, 0].copy(), [], 0, []
+    for t in list(range(7)) + [7, 8, 9]:
+        if t == 7:
+            fill -= 3  # tokens 4, 5, 6 rejected
+        o, ckpt, slots, fill = rm.step(ckpt, slots, fill, 8, a["q"][0, t, 0], a["k"][0, t, 0], a["v"][0, t, 0],
+                                       a["g"][0, t, 0], float(a["beta"][0, t, 0]), scale)
+        outs.append(o)
+    keep = [0, 1, 2, 3, 7, 8, 9]
+    sub = {n: (a[n][:, keep] if a[n] is not None and n not in ("h0", "dh_final") else a[n]) for n in a}
+    out, hT = oracle.fwd(sub["q"], sub["k"], sub["v"], sub["g"], sub["beta"], sub["h0"])
+    assert oracle.rel_l2(np.stack(outs[7:]), out[0, 4:, 0]) < 1e-12
+    assert oracle.rel_l2(rm.fold(ckpt, slots, fill), hT[0, 0]) < 1e-12
