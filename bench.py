@@ -279,6 +279,30 @@ def run_gdn(args, world, rank, local):
     tokens = w.B * w.T
     value = job_tokens_per_s(world, tokens, ms_max)
 
+    # forward alone and backward alone (the backward re-reads one forward's residuals)
+    def timed(fn, n):
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a0.record()
+        for _ in range(n):
+            fn()
+        a1.record()
+        torch.cuda.synchronize()
+        return a0.elapsed_time(a1) / n
+
+    def fwd_only():
+        gdn.gdn_chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], d["h0"], out=out, h_final=hT, residuals=res)
+
+    def bwd_only():
+        gdn.gdn_chunk_bwd(d["q"], d["k"], d["v"], d["g"], d["beta"], d["h0"], res, d["dout"], d["dh_final"],
+                          workspace=ws, grads={k: grads[k] for k in ("dq", "dk", "dv", "dg", "dbeta", "dh0")})
+
+    split_n = min(args.steps, 200)
+    split = {"fwd_ms": round(timed(fwd_only, split_n), 4), "bwd_ms": round(timed(bwd_only, split_n), 4),
+             "steps": split_n}
+
     # per-kernel launch durations: events on the launch stream around every kernel
     prof_steps = min(args.steps, 50)
     gdn.gdn_profile_enable(True)
@@ -325,6 +349,7 @@ def run_gdn(args, world, rank, local):
         "roofline": roofline,
         "tensor": tensor,
         "kernels": kernels,
+        "fwd_bwd_split": split,
         "clocks": clk.summary(),
         "correctness_gate": {"chunked_vs_recurrent_rel_l2": round(gate, 6), "finite": finite},
         "variants": variants_leg(args, w, host, dev),
