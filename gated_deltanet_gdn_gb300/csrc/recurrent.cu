@@ -37,6 +37,28 @@ struct RecSmem {
   float inv[2][TB];   // q/k L2 normalisation: inverse norms of the batch's q and k rows
 };
 
+// Packed fp32 pairs (Blackwell f32x2 arithmetic): one instruction does the fp32 operation
+// on both halves with the same rounding as the scalar one, so the state update below is
+// element for element the scalar arithmetic of decode_kernel, in half the instructions.
+__device__ __forceinline__ uint64_t f2_pack(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void f2_unpack(uint64_t r, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(r));
+}
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+
 // QK: q/k L2 normalisation (GDN_FLAG_QK_L2NORM) is compiled in only when asked for, so
 // the plain per-token chain carries no extra multiplies.
 template <class T, int DK, bool PC, int TB, bool QK>
@@ -51,17 +73,19 @@ __global__ void __launch_bounds__(REC_THREADS) recurrent_kernel(RecurrentArgs p)
   const int col0 = blockIdx.x * REC_COLS + cg * REC_VEC;
   const int DV = p.DV, H = p.H, T_ = p.T;
 
-  // state slice: rows part + 16 i, columns col0 .. col0 + 3
-  float S[RPT][REC_VEC];
+  // state slice: rows part + 16 i, columns col0 .. col0 + 3, as two packed pairs per row
+  static_assert(REC_VEC == 4, "two packed pairs per row");
+  uint64_t S[RPT][2];
   const size_t sbase = (size_t)bh * DK * DV;
 #pragma unroll
   for (int i = 0; i < RPT; ++i) {
     const int r = part + REC_TPC * i;
     if (p.h0) {
       const float4 x = *reinterpret_cast<const float4*>(p.h0 + sbase + (size_t)r * DV + col0);
-      S[i][0] = x.x; S[i][1] = x.y; S[i][2] = x.z; S[i][3] = x.w;
+      S[i][0] = f2_pack(x.x, x.y);
+      S[i][1] = f2_pack(x.z, x.w);
     } else {
-      S[i][0] = S[i][1] = S[i][2] = S[i][3] = 0.f;
+      S[i][0] = S[i][1] = f2_pack(0.f, 0.f);
     }
   }
 
@@ -141,18 +165,22 @@ __global__ void __launch_bounds__(REC_THREADS) recurrent_kernel(RecurrentArgs p)
       const float bt = sm.beta[buf][tt];
       const float as = PC ? 1.f : sm.gs[buf][tt];
       const float nq = QK ? sm.inv[0][tt] : 1.f, nk = QK ? sm.inv[1][tt] : 1.f;
-      float pv[REC_VEC] = {0.f, 0.f, 0.f, 0.f};
+      uint64_t pv2[2] = {f2_pack(0.f, 0.f), f2_pack(0.f, 0.f)};
 #pragma unroll
       for (int i = 0; i < RPT; ++i) {
         const int r = part + REC_TPC * i;
         const float a = PC ? sm.a[tt][r] : as;
         const float kr = to_f32(sm.k[buf][tt][r]) * nk;
+        const uint64_t a2 = f2_pack(a, a), k2 = f2_pack(kr, kr);
 #pragma unroll
-        for (int j = 0; j < REC_VEC; ++j) {
-          S[i][j] *= a;
-          pv[j] = fmaf(S[i][j], kr, pv[j]);
+        for (int h2 = 0; h2 < 2; ++h2) {
+          S[i][h2] = f2_mul(S[i][h2], a2);
+          pv2[h2] = f2_fma(S[i][h2], k2, pv2[h2]);
         }
       }
+      float pv[REC_VEC];
+      f2_unpack(pv2[0], pv[0], pv[1]);
+      f2_unpack(pv2[1], pv[2], pv[3]);
       // one butterfly for this token's S^T k and the previous token's output partials:
       // the two reductions are independent, and each keeps its own order (xor 1, 2, 4, 8)
 #pragma unroll
@@ -166,19 +194,22 @@ __global__ void __launch_bounds__(REC_THREADS) recurrent_kernel(RecurrentArgs p)
       float d[REC_VEC];
 #pragma unroll
       for (int j = 0; j < REC_VEC; ++j) d[j] = bt * (to_f32(sm.v[buf][tt][cg * REC_VEC + j]) - pv[j]);
-#pragma unroll
-      for (int j = 0; j < REC_VEC; ++j) ovp[j] = 0.f;
+      const uint64_t d2[2] = {f2_pack(d[0], d[1]), f2_pack(d[2], d[3])};
+      uint64_t ov2[2] = {f2_pack(0.f, 0.f), f2_pack(0.f, 0.f)};
 #pragma unroll
       for (int i = 0; i < RPT; ++i) {
         const int r = part + REC_TPC * i;
         const float kr = to_f32(sm.k[buf][tt][r]) * nk;
         const float qr = to_f32(sm.q[buf][tt][r]) * nq;
+        const uint64_t k2 = f2_pack(kr, kr), q2 = f2_pack(qr, qr);
 #pragma unroll
-        for (int j = 0; j < REC_VEC; ++j) {
-          S[i][j] = fmaf(kr, d[j], S[i][j]);
-          ovp[j] = fmaf(S[i][j], qr, ovp[j]);
+        for (int h2 = 0; h2 < 2; ++h2) {
+          S[i][h2] = f2_fma(k2, d2[h2], S[i][h2]);
+          ov2[h2] = f2_fma(S[i][h2], q2, ov2[h2]);
         }
       }
+      f2_unpack(ov2[0], ovp[0], ovp[1]);
+      f2_unpack(ov2[1], ovp[2], ovp[3]);
       rowp = ((size_t)b * T_ + t0 + tt) * H + h;
       pend = true;
     }
@@ -193,8 +224,10 @@ __global__ void __launch_bounds__(REC_THREADS) recurrent_kernel(RecurrentArgs p)
 #pragma unroll
   for (int i = 0; i < RPT; ++i) {
     const int r = part + REC_TPC * i;
-    *reinterpret_cast<float4*>(p.h_final + sbase + (size_t)r * DV + col0) =
-        make_float4(S[i][0], S[i][1], S[i][2], S[i][3]);
+    float4 x;
+    f2_unpack(S[i][0], x.x, x.y);
+    f2_unpack(S[i][1], x.z, x.w);
+    *reinterpret_cast<float4*>(p.h_final + sbase + (size_t)r * DV + col0) = x;
   }
 }
 
