@@ -151,3 +151,9 @@ def test_replay_sizes_and_validation(lib):
     assert sta(ctypes.byref(d), 0, p, p, p, p, None) == binding.GDN_ERR_INVALID_ARG
     assert sta(ctypes.byref(d), 4, p, p, p, None, None) == binding.GDN_ERR_INVALID_ARG
     assert sta(ctypes.byref(_dims(B=0)), 4, None, None, None, None, None) == binding.GDN_OK
+
+
+def test_selftest_rejects_bad_bounds_on_the_host(lib):
+    # validated before anything touches a device
+    assert lib.gdn_selftest_wait_timeout(0, None) == binding.GDN_ERR_INVALID_ARG
+    assert lib.gdn_selftest_wait_timeout(1 << 20, None) == binding.GDN_ERR_INVALID_ARG
