@@ -153,6 +153,24 @@ def test_delta_rule_recalls_the_written_value():
     np.testing.assert_allclose(kk @ hT3[0, 0], v[0, 2, 0], rtol=1e-12, atol=1e-12)
 
 
+def test_delta_identity_for_any_key_norm_and_gate():
+    """Card, section Method, in general: after the write, k_t^T S_t = (1 - beta |k|^2) k_t^T S'
+    + beta |k|^2 v_t, where S' is the decayed previous state (unnormalised keys)."""
+    rng = np.random.default_rng(14)
+    for per_channel in (True, False):
+        q, k, v, g, beta, S0 = _rand_problem(rng, B=1, T=7, H=1, Dk=5, Dv=3, per_channel=per_channel,
+                                             norm=False)
+        t = 6
+        _, h_prev = oracle.fwd(q[:, :t], k[:, :t], v[:, :t], g[:, :t], beta[:, :t], S0)
+        _, h_t = oracle.fwd(q[:, :t + 1], k[:, :t + 1], v[:, :t + 1], g[:, :t + 1], beta[:, :t + 1], S0)
+        a = np.exp(g[0, t, 0]) * np.ones(5)
+        S_dec = a[:, None] * h_prev[0, 0]
+        kt, bt = k[0, t, 0], beta[0, t, 0]
+        nk = float(kt @ kt)
+        want = (1.0 - bt * nk) * (kt @ S_dec) + bt * nk * v[0, t, 0]
+        np.testing.assert_allclose(kt @ h_t[0, 0], want, rtol=1e-12, atol=1e-12)
+
+
 def test_householder_product_form():
     """Independent formulation: S_t = (I - beta k k^T) diag(exp g) S_{t-1} + beta k v^T,
     o_t = scale S_t^T q_t, evaluated with plain matrix products."""
