@@ -330,9 +330,14 @@ def run_gdn(args, world, rank, local):
     roofline = {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
                 "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
                 "traffic": traffic.get(dom), "algorithmic_bytes": b, "peak_source": peaks["source"]}
-    flops_step = sum(v[1] for v in work.values())
+    # whole-step work: the kernels that actually ran, each per launch times its launches per step
+    ran = {k: prof[k][1] // prof_steps for k in prof if k in work}
+    flops_step = sum(work[k][1] * n for k, n in ran.items())
+    bytes_step = sum(work[k][0] * n for k, n in ran.items())
     tensor = {"step_tflops": round(flops_step / (ms / 1e3) / 1e12, 2),
               "frac_of_sustained_bf16": round(flops_step / (ms / 1e3) / 1e12 / peaks["bf16_tflops_sustained"], 4)}
+    hbm = {"step_algorithmic_bytes": int(bytes_step), "step_gbs": round(bytes_step / (ms / 1e3) / 1e9, 1),
+           "frac_of_measured": round(bytes_step / (ms / 1e3) / 1e9 / peaks["hbm_gbs"], 4)}
 
     result = {
         "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world,
@@ -348,6 +353,7 @@ def run_gdn(args, world, rank, local):
         "gpu_launches": 8 * args.steps,
         "roofline": roofline,
         "tensor": tensor,
+        "hbm_whole_step": hbm,
         "kernels": kernels,
         "fwd_bwd_split": split,
         "clocks": clk.summary(),
