@@ -84,14 +84,18 @@ def score_backward(x, y, G, dP):
     return dx, dy, x * dx - y * dy
 
 
-def chunk_local(q, k, v, g, beta, factored: bool = True) -> Dict[str, np.ndarray]:
-    """Everything in one chunk that does not depend on the incoming state."""
+def chunk_local(q, k, v, g, beta, factored: bool = True, block: int = BLOCK) -> Dict[str, np.ndarray]:
+    """Everything in one chunk that does not depend on the incoming state. ``block``
+    is the length of the chunk's first block (the factored scores' split point)."""
     C = q.shape[0]
     G = np.cumsum(g, axis=0)
     Gam = np.exp(G)
-    sc = scores_factored if factored else scores_pairwise
-    Pqk = sc(q, k, G, True)
-    Pkk = sc(k, k, G, False)
+    if factored:
+        Pqk = scores_factored(q, k, G, True, block)
+        Pkk = scores_factored(k, k, G, False, block)
+    else:
+        Pqk = scores_pairwise(q, k, G, True)
+        Pkk = scores_pairwise(k, k, G, False)
     Akk = beta[:, None] * Pkk
     Tm = np.linalg.inv(np.eye(C) + Akk)
     Kh = Gam * k
@@ -105,7 +109,8 @@ def _expand_g(g, Dk):
     return g if g.ndim == 4 else np.repeat(g[..., None], Dk, axis=-1)
 
 
-def fwd(q, k, v, g, beta, h0=None, scale=None, chunk: int = CHUNK, factored: bool = True):
+def fwd(q, k, v, g, beta, h0=None, scale=None, chunk: int = CHUNK, factored: bool = True,
+        block: Optional[int] = None):
     """Chunked forward. Returns (out, h_final, residual chunk-start states
     [B,H,N,Dk,Dv], per-chunk U [B,H,N,C,Dv])."""
     q, k, v, beta = (np.asarray(a, np.float64) for a in (q, k, v, beta))
@@ -125,7 +130,7 @@ def fwd(q, k, v, g, beta, h0=None, scale=None, chunk: int = CHUNK, factored: boo
             for n in range(N):
                 sl = slice(n * chunk, (n + 1) * chunk)
                 L = chunk_local(q[b, sl, h], k[b, sl, h], v[b, sl, h], gx[b, sl, h],
-                                beta[b, sl, h], factored)
+                                beta[b, sl, h], factored, chunk // 2 if block is None else block)
                 states[b, h, n] = S
                 U = L["Up"] - L["W"] @ S
                 Us[b, h, n] = U
@@ -172,7 +177,7 @@ def chunk_grads(q, k, v, beta, L, S0, U, dO, dS1, dU, scale):
     return dq, dk, dv, dG, dbeta
 
 
-def bwd(q, k, v, g, beta, h0, dout, dh_final=None, scale=None, chunk: int = CHUNK):
+def bwd(q, k, v, g, beta, h0, dout, dh_final=None, scale=None, chunk: int = CHUNK, block: Optional[int] = None):
     """Chunked backward: reverse state scan plus chunk-parallel gradients."""
     q, k, v, beta, dout = (np.asarray(a, np.float64) for a in (q, k, v, beta, dout))
     B, T, H, Dk = q.shape
@@ -193,7 +198,8 @@ def bwd(q, k, v, g, beta, h0, dout, dh_final=None, scale=None, chunk: int = CHUN
             dS = np.zeros((Dk, Dv)) if dh_final is None else np.asarray(dh_final, np.float64)[b, h].copy()
             for n in reversed(range(N)):
                 sl = slice(n * chunk, (n + 1) * chunk)
-                L = chunk_local(q[b, sl, h], k[b, sl, h], v[b, sl, h], gx[b, sl, h], beta[b, sl, h])
+                L = chunk_local(q[b, sl, h], k[b, sl, h], v[b, sl, h], gx[b, sl, h], beta[b, sl, h], True,
+                                chunk // 2 if block is None else block)
                 dO = dout[b, sl, h]
                 dU = scale * L["Aqk"].T @ dO + L["Kt"] @ dS
                 cq, ck, cv, cG, cb = chunk_grads(q[b, sl, h], k[b, sl, h], v[b, sl, h],

@@ -371,6 +371,22 @@ def test_chunked_form_equals_token_serial(per_channel):
         assert oracle.rel_l2(gm[n], gr[n]) < 1e-11, n
 
 
+@pytest.mark.parametrize("per_channel", [True, False])
+def test_chunked_form_with_128_token_chunks_equals_token_serial(per_channel):
+    """The same chunked form with 128-token chunks cut into two 64-token blocks (the
+    marin note's 64 x 64 score tile, atomic-ops' bt = 2 bc), forward and backward, equals
+    the token-serial oracle: the algebra a C = 128 kernel would follow."""
+    w = WORKLOADS["tiny_fwd"].with_(T=256, H=1, Dk=8, Dv=6, h0_std=0.5, g_per_channel=per_channel)
+    a = _arrays(w)
+    out, hT = oracle.fwd(a["q"], a["k"], a["v"], a["g"], a["beta"], a["h0"])
+    o2, h2, _, _ = cm.fwd(a["q"], a["k"], a["v"], a["g"], a["beta"], a["h0"], chunk=128)
+    assert oracle.rel_l2(o2, out) < 1e-12 and oracle.rel_l2(h2, hT) < 1e-12
+    gr = oracle.bwd(a["q"], a["k"], a["v"], a["g"], a["beta"], a["h0"], a["dout"], a["dh_final"])
+    gm = cm.bwd(a["q"], a["k"], a["v"], a["g"], a["beta"], a["h0"], a["dout"], a["dh_final"], chunk=128)
+    for n in gr:
+        assert oracle.rel_l2(gm[n], gr[n]) < 1e-10, n
+
+
 def test_input_generator_recipe():
     """The generator follows the workload recipes (no method arithmetic)."""
     w = WORKLOADS["recurrent"].with_(B=1, T=512, H=2, Dk=8, Dv=8)
