@@ -140,6 +140,36 @@ def fwd(q, k, v, g, beta, h0=None, scale=None, chunk: int = CHUNK, factored: boo
     return out, hT, states, Us
 
 
+def fwd_transition(q, k, v, g, beta, h0=None, scale=None, chunk: int = CHUNK):
+    """The same forward with the state recurrence written as one affine map per chunk,
+        S1 = diag(gam) S0 + P S0 + C,   P = -K~^T W,   C = K~^T U',
+    (substitute U = U' - W S0 into S1 = diag(gam) S0 + K~^T U), the outputs taken from the
+    chunk-start states as before. A scan in this form has one product per chunk on its
+    sequential chain instead of two. Returns (out, h_final)."""
+    q, k, v, beta = (np.asarray(a, np.float64) for a in (q, k, v, beta))
+    B, T, H, Dk = q.shape
+    Dv = v.shape[-1]
+    gx = _expand_g(np.asarray(g, np.float64), Dk)
+    N = T // chunk
+    scale = Dk ** -0.5 if scale is None else scale
+    out = np.zeros((B, T, H, Dv))
+    hT = np.zeros((B, H, Dk, Dv))
+    for b in range(B):
+        for h in range(H):
+            S = np.zeros((Dk, Dv)) if h0 is None else np.asarray(h0, np.float64)[b, h].copy()
+            for n in range(N):
+                sl = slice(n * chunk, (n + 1) * chunk)
+                L = chunk_local(q[b, sl, h], k[b, sl, h], v[b, sl, h], gx[b, sl, h], beta[b, sl, h], True,
+                                chunk // 2)
+                P = -L["Kt"].T @ L["W"]
+                Cm = L["Kt"].T @ L["Up"]
+                U = L["Up"] - L["W"] @ S
+                out[b, sl, h] = scale * (L["Qh"] @ S + L["Aqk"] @ U)
+                S = L["gam"][:, None] * S + P @ S + Cm
+            hT[b, h] = S
+    return out, hT
+
+
 def chunk_grads(q, k, v, beta, L, S0, U, dO, dS1, dU, scale):
     """Chunk-parallel gradients of one chunk given the reverse scan's dU and the
     gradient dS1 of the state leaving the chunk. Returns dq, dk, dv, dG, dbeta

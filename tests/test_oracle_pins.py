@@ -387,6 +387,16 @@ def test_chunked_form_with_128_token_chunks_equals_token_serial(per_channel):
         assert oracle.rel_l2(gm[n], gr[n]) < 1e-10, n
 
 
+def test_transition_matrix_form_equals_token_serial():
+    """The chunk recurrence as one affine map, S1 = diag(gam) S0 - K~^T W S0 + K~^T U',
+    equals the token-serial oracle (the alternative scan form of the next-steps list)."""
+    w = WORKLOADS["tiny_fwd"].with_(T=192, H=2, Dk=8, Dv=6, h0_std=0.5)
+    a = _arrays(w)
+    out, hT = oracle.fwd(a["q"], a["k"], a["v"], a["g"], a["beta"], a["h0"])
+    o2, h2 = cm.fwd_transition(a["q"], a["k"], a["v"], a["g"], a["beta"], a["h0"])
+    assert oracle.rel_l2(o2, out) < 1e-12 and oracle.rel_l2(h2, hT) < 1e-12
+
+
 def test_input_generator_recipe():
     """The generator follows the workload recipes (no method arithmetic)."""
     w = WORKLOADS["recurrent"].with_(B=1, T=512, H=2, Dk=8, Dv=8)
