@@ -37,14 +37,27 @@ bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) %
 
 // One thread waits on an mbarrier that nothing ever arrives on, giving up after max_tries
 // tries exactly as the kernels' own bounded waits do: the error word gets
-// ERR_WAIT_TIMEOUT and the kernel returns normally.
-__global__ void wait_timeout_selftest_kernel(unsigned* err, unsigned max_tries) {
+// ERR_WAIT_TIMEOUT and the kernel returns normally. Then it runs SELFTEST_LATER_WAITS
+// of the kernels' own waits (mbar_wait) on the same barrier, which must give up soon
+// after WAIT_BAIL_TRIES tries because the error word is now set. With `cycles` non-NULL
+// it records the clock cycles of the first wait and of the later ones together.
+constexpr int SELFTEST_LATER_WAITS = 4;
+__global__ void wait_timeout_selftest_kernel(unsigned* err, unsigned max_tries, unsigned long long* cycles) {
   __shared__ uint64_t bar;
   mbar_init(&bar, 1);
   fence_mbar_init();
+  const long long t0 = clock64();
   for (unsigned i = 0; i < max_tries; ++i)
     if (mbar_try_wait(&bar, 0u)) return;
   atomicOr(err, ERR_WAIT_TIMEOUT);
+  __threadfence();
+  const long long t1 = clock64();
+  for (int w = 0; w < SELFTEST_LATER_WAITS; ++w) (void)mbar_wait(&bar, 0u, err);
+  const long long t2 = clock64();
+  if (cycles) {
+    cycles[0] = (unsigned long long)(t1 - t0);
+    cycles[1] = (unsigned long long)(t2 - t1);
+  }
 }
 
 // Common dims checks. Returns GDN_OK or the status to report.
@@ -132,35 +145,6 @@ const char* kKernelNames[K_COUNT] = {"chunk_prep_kernel",    "chunk_scan_fwd_ker
                                      "replay_decode_kernel", "replay_state_kernel", "chunk_dqa_kernel"};
 
 }  // namespace
-
-static std::mutex g_side_mutex;
-static cudaStream_t g_side_stream[64] = {};
-static cudaEvent_t g_fork_ev[64] = {}, g_join_ev[64] = {};
-
-cudaError_t side_fork(cudaStream_t s, SideStream* side) {
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  side->lock = std::unique_lock<std::mutex>(g_side_mutex);
-  if (!g_side_stream[dev]) {
-    if ((e = cudaEventCreateWithFlags(&g_fork_ev[dev], cudaEventDisableTiming)) != cudaSuccess) return e;
-    if ((e = cudaEventCreateWithFlags(&g_join_ev[dev], cudaEventDisableTiming)) != cudaSuccess) return e;
-    if ((e = cudaStreamCreateWithFlags(&g_side_stream[dev], cudaStreamNonBlocking)) != cudaSuccess) return e;
-  }
-  if ((e = cudaEventRecord(g_fork_ev[dev], s)) != cudaSuccess) return e;
-  if ((e = cudaStreamWaitEvent(g_side_stream[dev], g_fork_ev[dev], 0)) != cudaSuccess) return e;
-  side->stream = g_side_stream[dev];
-  side->join_ev = g_join_ev[dev];
-  return cudaSuccess;
-}
-
-cudaError_t side_join(cudaStream_t s, SideStream* side) {
-  cudaError_t e = cudaEventRecord(side->join_ev, side->stream);
-  if (e == cudaSuccess) e = cudaStreamWaitEvent(s, side->join_ev, 0);
-  side->lock.unlock();
-  return e;
-}
 
 void prof_mark(KernelId id, cudaStream_t s, bool begin) {
   if (!g_prof_on) return;
@@ -358,11 +342,12 @@ int gdn_replay_state(const gdn_dims* d, int L, const float* ckpt, const void* bu
   return launch_status(launch_replay_state(a, static_cast<cudaStream_t>(stream)));
 }
 
-int gdn_selftest_wait_timeout(unsigned max_tries, void* stream) {
+int gdn_selftest_wait_timeout(unsigned max_tries, unsigned long long* cycles, void* stream) {
   if (max_tries == 0 || max_tries > (1u << 16)) return GDN_ERR_INVALID_ARG;
+  if (!optional_ok(cycles)) return GDN_ERR_INVALID_ARG;
   unsigned* err = device_error_word();
   if (!err) return GDN_ERR_CUDA;
-  wait_timeout_selftest_kernel<<<1, 1, 0, static_cast<cudaStream_t>(stream)>>>(err, max_tries);
+  wait_timeout_selftest_kernel<<<1, 1, 0, static_cast<cudaStream_t>(stream)>>>(err, max_tries, cycles);
   return launch_status(cudaGetLastError());
 }
 

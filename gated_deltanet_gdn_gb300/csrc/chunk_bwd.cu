@@ -26,6 +26,7 @@
 //   chunk_dstate_kernel     grid (chunks, B*H), 256 threads: the products with dU and dS1
 //                           (contractions over Dv) and dgam
 //   chunk_grads_kernel      (chunk_grads.cu) everything else
+#include "chunk_dqa.cuh"
 #include "common.cuh"
 #include "kernels.h"
 
@@ -169,7 +170,11 @@ __global__ void __launch_bounds__(RSCAN_THREADS) chunk_scan_bwd_kernel(ChunkBwdA
     if (tid == 0) bulk_wait_read0();  // the bulk stores have read dSs and dUs before they are rewritten
     __syncthreads();
   }
-  if (tid == 0) bulk_wait0();  // residual stores complete before the CTA retires
+  cp_async_wait<0>();
+  if (tid == 0) {  // every load landed and the residual stores complete before the CTA retires
+    drain_ring(bars, 2, N);
+    bulk_wait0();
+  }
   if (a.dh0) {
 #pragma unroll
     for (int mt = 0; mt < MTS; ++mt)
@@ -189,91 +194,14 @@ __global__ void __launch_bounds__(RSCAN_THREADS) chunk_scan_bwd_kernel(ChunkBwdA
 // scan's results (chunk_dqa_kernel): dQ-hat = scale dO S0^T, dAqk = scale dO U^T
 // (j <= t). With Y = T^T dU (chunk_dstate_kernel): dv = beta Y, dbeta_v = rowsum(Y * V),
 // dBk = -Y S0^T, dK-tilde = U dS1^T, dAkk = -Y U^T (j < t), dgam = rowsum(dS1 * S0).
+// The products without the reverse scan's results, after the CUDA-core scan (the
+// tensor-core scan runs them as extra CTAs of its own launch).
 template <int DK, int DV>
-struct DqaLayout {
-  static constexpr int DO = 0;                       // dO    [C][DV]
-  static constexpr int U = a1k(DO + C * DV * 2);     // U^T   [DV][C]
-  static constexpr int S0 = a1k(U + C * DV * 2);     // S0^T  [DV][DK], as 64-channel panels
-  static constexpr int BYTES = a1k(S0 + DV * DK * 2);
-};
-
-// Persistent over the chunk-heads (unit = blockIdx.x, + gridDim.x, ...): launched with
-// about one CTA per SM that the reverse scan leaves free, so that its HBM traffic spreads
-// over the scan's duration instead of competing with the scan's loads in one burst.
-template <int DK, int DV>
-__global__ void __launch_bounds__(DST_THREADS, 2) chunk_dqa_kernel(ChunkBwdArgs a) {
-  typedef bf16 T;
-  typedef DqaLayout<DK, DV> L;
-  constexpr int NPAN = DK / 64;
-  constexpr int EPC = 8;
+__global__ void __launch_bounds__(DQA_THREADS, 2) chunk_dqa_kernel(ChunkBwdArgs a) {
+  pdl_wait();
+  pdl_trigger();
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* sm = align1024(smem_raw);
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int N = a.T / C, units = N * a.B * a.H;
-#pragma unroll 1
-  for (int unit = blockIdx.x; unit < units; unit += gridDim.x) {
-    const int n = unit % N, bh = unit / N, b = bh / a.H, h = bh % a.H;
-    const size_t ch = (size_t)bh * N + n;
-    Tile<T, C, DV> dOs{reinterpret_cast<T*>(sm + L::DO)};
-    Tile<T, DV, C> Us{reinterpret_cast<T*>(sm + L::U)};  // U^T
-    const T* dout = static_cast<const T*>(a.dout);
-    const T* s0rec = static_cast<const T*>(a.res.state) + ch * (DK * DV);
-    const size_t row0 = ((size_t)b * a.T + (size_t)n * C) * a.H + h;
-    const size_t rs = a.H;
-    {  // group 0: dO and U^T (dAqk); group 1: the S0^T record (dQ-hat)
-      const T* su = static_cast<const T*>(a.res.u) + ch * (C * DV);
-      for (int i = tid; i < C * DV / EPC; i += DST_THREADS) {
-        const int r = i / (DV / EPC), c0 = (i % (DV / EPC)) * EPC;
-        cp_async16(Us.p + i * EPC, su + i * EPC);
-        cp_async16(dOs.ptr(r, c0), dout + (row0 + r * rs) * DV + c0);
-      }
-      cp_async_commit();
-      T* s0 = reinterpret_cast<T*>(sm + L::S0);
-      for (int i = tid; i < DV * DK / EPC; i += DST_THREADS) cp_async16(s0 + i * EPC, s0rec + i * EPC);
-      cp_async_commit();
-    }
-    cp_async_wait<1>();
-    __syncthreads();
-    // warp w: rows 16 (w % 4) .. + 15 and column group w / 4 of every product
-    const int m0 = 16 * (warp & 3), hf = warp >> 2;
-    {
-      constexpr int NCC = C / (8 * DST_CG);
-      const int c0 = hf * (C / DST_CG);
-      float aq[1][NCC][4];
-      zero(aq);
-      if (!(m0 < BLK && c0 >= BLK))  // block-1 rows see no block-2 columns
-        Gemm<T>::template runk<1, NCC, 0, DV>(aq, aview<false>(dOs), bview<true>(Us), m0, c0, lane);
-      T* da = static_cast<T*>(a.ws.daqk) + ch * (C * C);
-#pragma unroll
-      for (int nt = 0; nt < NCC; ++nt)
-#pragma unroll
-        for (int e = 0; e < 4; e += 2) {
-          const int r = m0 + frag_row(lane, e), j = c0 + 8 * nt + frag_col(lane, e);
-          store2(da + Sw<T, C, C>::off(r, j), j <= r ? a.scale * aq[0][nt][e] : 0.f,
-                 j + 1 <= r ? a.scale * aq[0][nt][e + 1] : 0.f);
-        }
-    }
-    cp_async_wait<0>();
-    __syncthreads();
-    constexpr int NH = 64 / (8 * DST_CG);
-    const int n0 = hf * (64 / DST_CG);
-    T* dst = static_cast<T*>(a.ws.dqh) + ch * (C * DK);
-#pragma unroll 1
-    for (int p = 0; p < NPAN; ++p) {
-      Tile<T, DV, 64> S0p{reinterpret_cast<T*>(sm + L::S0) + (size_t)p * DV * 64};
-      float acc[1][NH][4];
-      zero(acc);
-      Gemm<T>::template runk<1, NH, 0, DV>(acc, aview<false>(dOs), bview<true>(S0p), m0, n0, lane);
-#pragma unroll
-      for (int nt = 0; nt < NH; ++nt)
-#pragma unroll
-        for (int e = 0; e < 4; e += 2) {
-          const int r = m0 + frag_row(lane, e), c = 64 * p + n0 + 8 * nt + frag_col(lane, e);
-          store2(dst + Sw<T, C, DK>::off(r, c), a.scale * acc[0][nt][e], a.scale * acc[0][nt][e + 1]);
-        }
-    }
-    __syncthreads();  // the tiles are refilled for the next unit
-  }
+  dqa_units<DK, DV>(a, align1024(smem_raw), blockIdx.x, gridDim.x, threadIdx.x);
 }
 
 template <int DK, int DV>
@@ -489,13 +417,11 @@ template <int DK, int DV>
 cudaError_t launch_bwd_t(const ChunkBwdArgs& a, cudaStream_t s) {
   const int N = a.T / C, BH = a.B * a.H;
   cudaError_t e;
-  // chunk_dqa_kernel needs only the forward's records and dO: it is forked onto the
-  // library's side stream before the reverse scan is launched and joined before the
-  // chunk gradients, so it runs on the SMs the scan leaves free
-  SideStream side;
-  const bool fork = N > 0;
-  if (fork && (e = side_fork(s, &side)) != cudaSuccess) return e;
-  if (scan_tc_applies(1, DK, DV)) {
+  // The products that need only the forward's records and dO (dQ-hat, dAqk) run as
+  // extra CTAs of the tensor-core reverse scan's launch, on the SMs the scan leaves free;
+  // after the CUDA-core scan they are a kernel of their own.
+  const bool tc = scan_tc_applies(1, DK, DV);
+  if (tc) {
     if ((e = launch_scan_bwd_tc(a, s)) != cudaSuccess) return e;
   } else {
     const int bytes = RScanLayout<DK>::BYTES + 1024;
@@ -507,21 +433,13 @@ cudaError_t launch_bwd_t(const ChunkBwdArgs& a, cudaStream_t s) {
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   if (N == 0) return cudaSuccess;
-  {
+  if (!tc) {
     const int bytes = DqaLayout<DK, DV>::BYTES + 1024;
     auto kern = chunk_dqa_kernel<DK, DV>;
     if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes)) != cudaSuccess) return e;
-    int dev = 0, nsm = 0;
-    if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
-    if ((e = cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
-    // the SMs the reverse scan leaves free (the tensor-core scan runs one CTA per (b, h))
-    const int scan_ctas = scan_tc_applies(1, DK, DV) ? BH : 0;
-    const int free_sms = nsm - scan_ctas > nsm / 2 ? nsm - scan_ctas : nsm / 2;
-    const int grid = N * BH < free_sms ? N * BH : free_sms;
-    prof_mark(K_DQA, side.stream, true);
-    kern<<<grid, DST_THREADS, bytes, side.stream>>>(a);
-    prof_mark(K_DQA, side.stream, false);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    prof_mark(K_DQA, s, true);
+    if ((e = launch_pdl(kern, dim3(N * BH), dim3(DQA_THREADS), bytes, s, a)) != cudaSuccess) return e;
+    prof_mark(K_DQA, s, false);
   }
   {
     const int bytes = DstLayout<DK, DV>::BYTES + 1024;
@@ -531,7 +449,6 @@ cudaError_t launch_bwd_t(const ChunkBwdArgs& a, cudaStream_t s) {
     if ((e = launch_pdl(kern, dim3(N, BH), dim3(DST_THREADS), bytes, s, a)) != cudaSuccess) return e;
     prof_mark(K_DSTATE, s, false);
   }
-  if ((e = side_join(s, &side)) != cudaSuccess) return e;
   return launch_chunk_grads(a, s);
 }
 

@@ -567,7 +567,10 @@ __global__ void __launch_bounds__(SCAN_THREADS) chunk_scan_fwd_kernel(ChunkFwdAr
     if (tid == 0) bulk_wait_read0();  // the bulk stores have read Ss and Us before they are rewritten
     __syncthreads();
   }
-  if (tid == 0) bulk_wait0();  // residual stores complete before the CTA retires
+  if (tid == 0) {  // every load landed and the residual stores complete before the CTA retires
+    drain_ring(bars, L::STAGES, N);
+    bulk_wait0();
+  }
   if (a.h_final) {
 #pragma unroll
     for (int mt = 0; mt < MTS; ++mt)

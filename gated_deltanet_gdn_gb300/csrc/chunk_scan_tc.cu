@@ -26,6 +26,7 @@
 
 #include <mutex>
 
+#include "chunk_dqa.cuh"
 #include "common.cuh"
 #include "kernels.h"
 #include "umma.cuh"
@@ -127,6 +128,12 @@ __device__ __forceinline__ uint64_t kstep_mn(uint64_t d, int ks) { return d + (u
 
 __device__ __forceinline__ void umma_commit_to(uint64_t* bar) { umma_commit(bar); }
 
+// Every MMA this thread issued has completed (one commit on a barrier used only here).
+__device__ __forceinline__ void drain_mma(uint64_t* bar) {
+  umma_commit(bar);
+  mbar_drain(bar, 0u);
+}
+
 // ------------------------------------------------------------------ forward
 struct TcFwdLayout {
   static constexpr int W = 0;                    // -W      [C][Dk]  (K-major B of U^T)
@@ -137,8 +144,8 @@ struct TcFwdLayout {
   static constexpr int STAGES = 2;
   static constexpr int SA = STAGES * STAGE;        // S^T bf16 [Dv][Dk], two buffers
   static constexpr int UA = SA + 2 * TD * TD * 2;  // U^T bf16 [Dv][C], two buffers
-  static constexpr int BAR = UA + 2 * TD * C * 2;  // full[STAGES], empty[STAGES], u, s
-  static constexpr int TSLOT = BAR + 8 * (2 * STAGES + 2);
+  static constexpr int BAR = UA + 2 * TD * C * 2;  // full[STAGES], empty[STAGES], u, s, drain
+  static constexpr int TSLOT = BAR + 8 * (2 * STAGES + 3);
   static constexpr int BYTES = TSLOT + 16;
   static constexpr uint32_t TX = (uint32_t)(3 * C * TD * 2 + TD * 4);
 };
@@ -155,6 +162,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_scan_fwd_tc_kernel(ChunkF
   uint64_t* empty = full + L::STAGES;
   uint64_t* bar_u = empty + L::STAGES;
   uint64_t* bar_s = bar_u + 1;
+  uint64_t* bar_d = bar_s + 1;
   uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + L::TSLOT);
   bf16* const sa_buf = reinterpret_cast<bf16*>(sm + L::SA);
   bf16* const ua_buf = reinterpret_cast<bf16*>(sm + L::UA);
@@ -166,6 +174,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_scan_fwd_tc_kernel(ChunkF
     }
     mbar_init(bar_u, 1);
     mbar_init(bar_s, 1);
+    mbar_init(bar_d, 1);
     fence_mbar_init();
   }
   if (warp == 0) {
@@ -190,6 +199,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_scan_fwd_tc_kernel(ChunkF
         bulk_g2s(st + L::UP, static_cast<const bf16*>(a.res.up) + ch * (C * TD), C * TD * 2, &full[s]);
         bulk_g2s(st + L::GAM, a.res.gam + ch * TD, TD * 4, &full[s]);
       }
+      drain_ring(full, L::STAGES, N);
     }
     return;
   }
@@ -291,9 +301,13 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_scan_fwd_tc_kernel(ChunkF
 #pragma unroll
     for (int i = 0; i < 64; ++i) a.h_final[sb + (size_t)(64 * half + i) * TD + row] = x[i];
   }
-  if (tid == 0) bulk_wait0();  // record stores complete before the CTA retires
+  if (tid == 0) {  // record stores and every issued MMA complete before TMEM is freed
+    bulk_wait0();
+    drain_mma(bar_d);
+  }
   tc_fence_before();
   compute_sync();
+  tc_fence_after();
   if (warp == 0) tmem_dealloc(tm, TMEM_COLS);
 }
 
@@ -309,8 +323,8 @@ struct TcBwdLayout {
   static constexpr int GAM = STAGES * STAGE;     // gam [STAGES][Dk] fp32
   static constexpr int SA = a1k(GAM + STAGES * TD * 4);  // dS^T bf16 [Dv][Dk], two buffers
   static constexpr int UA = SA + 2 * TD * TD * 2;  // dU^T bf16 [Dv][C]
-  static constexpr int BAR = UA + TD * C * 2;      // full[STAGES], empty[STAGES], u, s
-  static constexpr int TSLOT = BAR + 8 * (2 * STAGES + 2);
+  static constexpr int BAR = UA + TD * C * 2;      // full[STAGES], empty[STAGES], u, s, drain
+  static constexpr int TSLOT = BAR + 8 * (2 * STAGES + 3);
   static constexpr int BYTES = TSLOT + 16;
   static constexpr uint32_t TX = (uint32_t)(4 * C * TD * 2 + C * C * 2 + TD * 4);
 };
@@ -325,12 +339,19 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, i
       : "memory");
 }
 
+// Blocks 0 .. B*H - 1 scan one (batch, head) each; the blocks after them compute the
+// products that need no scan result (chunk_dqa.cuh) on the SMs the scan leaves free.
 __global__ void __launch_bounds__(TC_THREADS, 1)
     chunk_scan_bwd_tc_kernel(ChunkBwdArgs a, const __grid_constant__ CUtensorMap dout_map) {
   pdl_wait();  // no early trigger: one wave for the whole scan, successors must not park beside it
   typedef TcBwdLayout L;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = align1024(smem_raw);
+  if ((int)blockIdx.x >= a.B * a.H) {
+    if ((int)threadIdx.x < DQA_THREADS)
+      dqa_units<TD, TD>(a, sm, (int)blockIdx.x - a.B * a.H, (int)gridDim.x - a.B * a.H, (int)threadIdx.x);
+    return;
+  }
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int bh = blockIdx.x, b = bh / a.H, h = bh % a.H;
   const int N = a.T / C;
@@ -338,6 +359,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
   uint64_t* empty = full + L::STAGES;
   uint64_t* bar_u = empty + L::STAGES;
   uint64_t* bar_s = bar_u + 1;
+  uint64_t* bar_d = bar_s + 1;
   uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + L::TSLOT);
   bf16* const sa_buf = reinterpret_cast<bf16*>(sm + L::SA);
   Tile<bf16, TD, C> Ua{reinterpret_cast<bf16*>(sm + L::UA)};
@@ -350,6 +372,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     }
     mbar_init(bar_u, 1);
     mbar_init(bar_s, 1);
+    mbar_init(bar_d, 1);
     fence_mbar_init();
   }
   if (warp == 0) {
@@ -378,6 +401,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         tma_load_3d(st + L::DO, &dout_map, 0, h, tok, &full[s]);
         tma_load_3d(st + L::DO + PANEL_C, &dout_map, 64, h, tok, &full[s]);
       }
+      drain_ring(full, L::STAGES, N);
     }
     return;
   }
@@ -476,9 +500,13 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
 #pragma unroll
     for (int i = 0; i < 64; ++i) a.dh0[sb + (size_t)(64 * half + i) * TD + row] = x[i];
   }
-  if (tid == 0) bulk_wait0();
+  if (tid == 0) {  // record stores and every issued MMA complete before TMEM is freed
+    bulk_wait0();
+    drain_mma(bar_d);
+  }
   tc_fence_before();
   compute_sync();
+  tc_fence_after();
   if (warp == 0) tmem_dealloc(tm, TMEM_COLS);
 }
 
@@ -524,11 +552,20 @@ cudaError_t launch_scan_bwd_tc(const ChunkBwdArgs& a, cudaStream_t s) {
              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
     return cudaErrorInvalidValue;
+  static_assert(TcBwdLayout::BYTES >= DqaLayout<TD, TD>::BYTES, "the products' CTAs share the scan's shared memory");
   const int bytes = TcBwdLayout::BYTES + 1024;
   cudaError_t e = cudaFuncSetAttribute(chunk_scan_bwd_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
   if (e != cudaSuccess) return e;
+  int dev = 0, nsm = 0;
+  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+  if ((e = cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+  // one scan CTA per (b, h), then one products CTA per SM the scans leave free (at least
+  // half the SMs), never more than there are chunk-heads
+  const int BH = a.B * a.H, units = (a.T / C) * BH;
+  const int free_sms = nsm - BH > nsm / 2 ? nsm - BH : nsm / 2;
+  const int extra = units < free_sms ? units : free_sms;
   prof_mark(K_SCAN_BWD_TC, s, true);
-  e = launch_pdl(chunk_scan_bwd_tc_kernel, dim3(a.B * a.H), dim3(TC_THREADS), bytes, s, a, map);
+  e = launch_pdl(chunk_scan_bwd_tc_kernel, dim3(BH + extra), dim3(TC_THREADS), bytes, s, a, map);
   prof_mark(K_SCAN_BWD_TC, s, false);
   return e;
 }

@@ -448,11 +448,46 @@ enum : unsigned { ERR_WAIT_TIMEOUT = 1u };
 // Bounded wait on an mbarrier phase. Each try_wait already suspends for a
 // hardware-defined time; 1 << 22 tries is far longer than any copy here needs.
 // On time-out the error word gets ERR_WAIT_TIMEOUT and false is returned.
+//
+// After a time-out no result of the call is valid, and the barriers of the CTA that
+// gave up no longer follow their phases, so every later wait there would also run its
+// full count. Hence a wait that has already tried WAIT_BAIL_TRIES times gives up at
+// once when the error word holds ERR_WAIT_TIMEOUT (set by any CTA of any kernel, until
+// the host reads and clears it). Waits of normal operation end within microseconds, far
+// below that count, so they never look at the word. Kernels do not leave their loops
+// when a wait fails: every thread still reaches every named barrier and the loop runs
+// to its end without waiting, and before a CTA frees its tensor memory or exits it
+// drains what it issued (mbar_drain below).
+constexpr uint32_t WAIT_MAX_TRIES = 1u << 22;
+constexpr uint32_t WAIT_BAIL_TRIES = 1u << 12;
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, unsigned* err) {
-  for (uint32_t i = 0; i < (1u << 22); ++i)
+  for (uint32_t i = 0; i < WAIT_MAX_TRIES; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
+    if (i >= WAIT_BAIL_TRIES && (i & 255u) == 0 && err &&
+        (*reinterpret_cast<volatile unsigned*>(err) & ERR_WAIT_TIMEOUT))
+      return false;
+  }
   if (err) atomicOr(err, ERR_WAIT_TIMEOUT);
   return false;
+}
+
+// Bounded wait used only to drain: the completion of copies or tensor-core operations
+// this CTA issued itself, before it frees tensor memory or retires. It does not give up
+// early on the error word (operations already issued complete on their own) and
+// reports nothing; in normal operation the phase has completed long before.
+__device__ __forceinline__ bool mbar_drain(uint64_t* bar, uint32_t parity) {
+  for (uint32_t i = 0; i < (1u << 20); ++i)
+    if (mbar_try_wait(bar, parity)) return true;
+  return false;
+}
+
+// Producer exit: the last (up to `stages`) of the `count` loads issued on a ring of
+// single-arrival barriers (load i on barrier i % stages, phase i / stages) have landed.
+// In normal operation the consumers waited for them long ago; after a failed wait they
+// may not have, and a CTA must not retire with copies into its shared memory in flight.
+__device__ __forceinline__ void drain_ring(uint64_t* bars, int stages, int count) {
+  for (int i = count > stages ? count - stages : 0; i < count; ++i)
+    mbar_drain(&bars[i % stages], (uint32_t)(i / stages) & 1u);
 }
 
 // 16-byte vector copy helpers

@@ -103,6 +103,7 @@ __global__ void __launch_bounds__(DecLayout<T, DK, DV>::THREADS, 1) decode_kerne
         if (PC) bulk_g2s(st + L::G, g + row * DK, DK * sizeof(T), &full[s]);
       }
       for (int m = nunits > L::STAGES ? nunits - L::STAGES : 0; m < nunits; ++m) store_back(m);
+      drain_ring(full, L::STAGES, nunits);
       bulk_wait0();
     }
     return;

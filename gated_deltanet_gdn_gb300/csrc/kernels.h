@@ -2,7 +2,6 @@
 #pragma once
 
 #include <cuda_runtime.h>
-#include <mutex>
 #include <stddef.h>
 #include <stdint.h>
 
@@ -196,23 +195,12 @@ enum KernelId {
   K_L2NORM_BWD = 12,  // l2norm_bwd_kernel
   K_REPLAY = 13,      // replay_decode_kernel
   K_REPLAY_STATE = 14,  // replay_state_kernel
-  K_DQA = 15,           // chunk_dqa_kernel
+  K_DQA = 15,           // chunk_dqa_kernel (after the CUDA-core reverse scan; the tensor-core
+                        // reverse scan's launch includes these products)
   K_COUNT = 16
 };
 // Records a CUDA event on s before (begin = true) or after a launch when timing is on.
 void prof_mark(KernelId id, cudaStream_t s, bool begin);
-
-// A library-owned second stream per device, for kernels that can run beside the ones
-// queued on the caller's stream s. side_fork makes it wait for everything queued on s so
-// far; side_join makes s wait for everything queued on it since. The pair holds a
-// process-wide lock, so fork/join sequences of concurrent calls do not interleave.
-struct SideStream {
-  cudaStream_t stream = nullptr;
-  cudaEvent_t join_ev = nullptr;
-  std::unique_lock<std::mutex> lock;
-};
-cudaError_t side_fork(cudaStream_t s, SideStream* side);
-cudaError_t side_join(cudaStream_t s, SideStream* side);
 
 // Each returns a cudaError_t from the launches (cudaSuccess when all were accepted).
 cudaError_t launch_chunk_fwd(const ChunkFwdArgs& a, cudaStream_t s);

@@ -256,6 +256,8 @@ __global__ void __launch_bounds__(RepLayout<T, DK, DV>::THREADS, 1) replay_decod
           break;
         }
       }
+      drain_ring(full_s, L::SSTAGES, ms);
+      drain_ring(full_a, L::ASTAGES, ma);
     }
     return;
   }

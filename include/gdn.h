@@ -34,12 +34,11 @@
  * the caller; the library never allocates or frees device memory. Each call
  * only enqueues kernels on `stream` (a cudaStream_t; NULL = legacy default
  * stream) and returns; results are ready when the stream reaches that point.
- * Calls keep no state between them and may run concurrently on different
- * streams with disjoint buffers. gdn_chunk_bwd forks part of its work onto a
- * stream the library owns (one per device, created on first use) and joins it
- * back onto `stream` before its last kernel, so the caller sees one ordered
- * sequence on `stream`; under stream capture, make one call before capturing. Outputs must not alias inputs, except
- * h_final == h0 in gdn_recurrent (in-place state carry).
+ * Every kernel of a call runs on `stream` (the library owns no stream, event or
+ * lock), so calls keep no state between them and may run concurrently on
+ * different streams with disjoint buffers (gdn_chunk_fwd_noalloc excepted: see
+ * there). Outputs must not alias inputs, except h_final == h0 in gdn_recurrent
+ * (in-place state carry).
  *
  * Errors. Arguments are validated before anything is enqueued; a failed
  * check returns a gdn_status and enqueues nothing:
@@ -108,11 +107,21 @@ typedef struct {
 /* Bytes of the residual buffer that gdn_chunk_fwd fills and gdn_chunk_bwd
  * reads: per 64-token chunk and head, the chunk-start state, the chunk's
  * decay-weighted score tile, its WY factors and the per-token deltas. Returns 0
- * for invalid dims. The content is private to the library. */
+ * for invalid dims. The content is private to the library.
+ * Source: atomic-ops 0.1.0, section API (a forward variant that returns its
+ * residuals for the backward, gdn2_pallas_forward_with_residuals) and section
+ * Features (the backward stages reuse forward residuals instead of recomputing
+ * them); the records themselves are this library's. It plays the part of the
+ * memory estimate that page's API offers (estimate_memory): the caller sizes
+ * and owns the buffer. */
 size_t gdn_chunk_residual_bytes(const gdn_dims* dims);
 
 /* Bytes of scratch that gdn_chunk_bwd needs (reverse-scan outputs and the
- * per-chunk state-gradient products). Returns 0 for invalid dims. */
+ * per-chunk state-gradient products). Returns 0 for invalid dims.
+ * Source: atomic-ops 0.1.0, sections Features and Limitations (the backward is
+ * a chain of stage kernels whose intermediate results are passed between
+ * them, one of them the pairwise-decay score backward); this buffer holds what
+ * this library's stages pass. Caller-owned, like the residual buffer. */
 size_t gdn_chunk_bwd_workspace_bytes(const gdn_dims* dims);
 
 /* Chunked forward (training / prefill), T a multiple of 64.
@@ -131,10 +140,19 @@ int gdn_chunk_fwd(const gdn_dims* dims, const void* q, const void* k, const void
                   const void* g, const void* beta, const float* h0, float scale, void* out,
                   float* h_final, void* residuals, void* stream);
 
-/* Chunked backward. Same inputs as the forward plus the residuals it wrote,
- * dout [B,T,H,Dv] and dh_final (NULL = zeros). Writes dq, dk, dv, dg, dbeta
- * and dh0 (may be NULL). workspace: gdn_chunk_bwd_workspace_bytes(dims) bytes,
- * 256-byte aligned. bfloat16 only (dims.dtype == GDN_BF16). */
+/* Chunked backward: the gradients of the training call of atomic-ops 0.1.0
+ * (sections Quick start and API: gdn2_forward_trainable(q, k, v, ..., g, scale,
+ * h0) -> (out, h_final) is differentiable with respect to its inputs and h0,
+ * and section Features: a fused backward that reuses forward residuals). The
+ * reverse pass itself is hand-derived from the chunked forward (the pages
+ * print no formula for it): a reverse scan of the state gradient over the
+ * chunks, then chunk-parallel products and the decay gradients (dg is a
+ * reverse cumulative sum inside each chunk).
+ * Same inputs as the forward plus the residuals it wrote, dout [B,T,H,Dv] and
+ * dh_final (NULL = zeros). Writes dq, dk, dv, dg, dbeta and dh0 (may be NULL).
+ * workspace: gdn_chunk_bwd_workspace_bytes(dims) bytes, 256-byte aligned,
+ * caller-owned, overwritten. bfloat16 only (dims.dtype == GDN_BF16); errors as
+ * listed at the top of this file. */
 int gdn_chunk_bwd(const gdn_dims* dims, const void* q, const void* k, const void* v,
                   const void* g, const void* beta, const float* h0, float scale,
                   const void* residuals, const void* dout, const float* dh_final, void* dq,
@@ -157,7 +175,10 @@ int gdn_chunk_bwd(const gdn_dims* dims, const void* q, const void* k, const void
  * enqueued, and must use gdn_chunk_fwd.
  *
  * The first call on a device resolves the array's device address there (with
- * that device current); make that first call before any stream capture. Every
+ * that device current) and keeps it for the life of the process; make that
+ * first call before any stream capture, and make no call after a
+ * cudaDeviceReset (or any other teardown of the device's primary context) in
+ * the same process, because the kept address would then be stale. Every
  * call shares the one array: calls whose work overlaps on the GPU (on two
  * streams, or from two threads) race on it and must be serialised by the
  * caller. The array keeps the last call's contents; nothing in it needs to
@@ -223,10 +244,16 @@ int gdn_replay_state(const gdn_dims* dims, int L, const float* ckpt, const void*
 /* Self-test of the failure path: launches a one-thread kernel that waits on an
  * mbarrier nothing arrives on and gives up after max_tries tries (1 .. 65536),
  * like every wait in the library's kernels. The kernel then sets bit 1 of the
- * device error word and returns, and the context stays usable. The next
- * gdn_check_device_error returns GDN_ERR_INTERNAL. Not part of the method:
- * it lets a caller or a test see the error path work without a GPU fault. */
-int gdn_selftest_wait_timeout(unsigned max_tries, void* stream);
+ * device error word, runs four more of the kernels' own bounded waits on the same
+ * barrier (each must give up after 4096 tries or a little more, because the
+ * error word is set: after one time-out the library's later waits end early
+ * instead of running their full count), and returns; the context stays usable.
+ * The next gdn_check_device_error returns GDN_ERR_INTERNAL. cycles: NULL, or a
+ * 16-byte aligned device buffer of two unsigned 64-bit words that receives the
+ * clock cycles of the first wait and of the four later waits together. Not
+ * part of the method: it lets a caller or a test see the error path work
+ * without a GPU fault. */
+int gdn_selftest_wait_timeout(unsigned max_tries, unsigned long long* cycles, void* stream);
 
 /* Reads and clears the library's device error word on the current device
  * (bits, OR-ed: 1 = a kernel gave up waiting for one of its own asynchronous

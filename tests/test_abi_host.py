@@ -155,5 +155,5 @@ def test_replay_sizes_and_validation(lib):
 
 def test_selftest_rejects_bad_bounds_on_the_host(lib):
     # validated before anything touches a device
-    assert lib.gdn_selftest_wait_timeout(0, None) == binding.GDN_ERR_INVALID_ARG
-    assert lib.gdn_selftest_wait_timeout(1 << 20, None) == binding.GDN_ERR_INVALID_ARG
+    assert lib.gdn_selftest_wait_timeout(0, None, None) == binding.GDN_ERR_INVALID_ARG
+    assert lib.gdn_selftest_wait_timeout(1 << 20, None, None) == binding.GDN_ERR_INVALID_ARG

@@ -2,17 +2,17 @@
 hand-derived float64 reverse pass (rel-L2 <= 2e-2 per gradient, bf16 inputs).
 
 Includes the training-shape fwd+bwd workload (B8 T4096 H6 D128 bf16) at full
-size with the same launch the benchmark times; the oracle checks a sample of
-(batch, head) pairs there (heads never interact, so a pair's gradients are those
-of the pair alone).
+size with the same launch the benchmark times; the oracle checks every
+(batch, head) pair there.
 """
+import numpy as np
 import pytest
 import torch
 
 import gated_deltanet_gdn_gb300 as gdn
 from gated_deltanet_gdn_gb300.synthetic import WORKLOADS, make_inputs
 
-from helpers import TOL, cuda_inputs, head_slice, oracle_bwd, oracle_fwd, rel
+from helpers import TOL, cuda_inputs, oracle_bwd, oracle_fwd, rel
 
 pytestmark = pytest.mark.gpu
 GRADS = ("dq", "dk", "dv", "dg", "dbeta", "dh0")
@@ -84,21 +84,41 @@ def test_autograd_wrapper():
         assert rel(leaves[n].grad, ref[gn]) <= TOL["bf16"], (n, rel(leaves[n].grad, ref[gn]))
 
 
+def _per_head_rel(got, ref, state=False):
+    """rel-L2 of every (batch, head) pair: [B, T, H, ...] tensors ([B, H, ...] states)."""
+    g = got.detach().double().cpu().numpy()
+    B, H = (g.shape[0], g.shape[1]) if state else (g.shape[0], g.shape[2])
+    out = np.zeros((B, H))
+    for b in range(B):
+        for h in range(H):
+            x, y = (g[b, h], ref[b, h]) if state else (g[b, :, h], ref[b, :, h])
+            out[b, h] = np.linalg.norm(x - y) / max(np.linalg.norm(y), 1e-300)
+    return out
+
+
 def test_training_shape_fwd_bwd_workload():
-    """B8 T4096 H6 D128 bf16: the benchmark's launch; oracle on sampled heads."""
+    """B8 T4096 H6 D128 bf16: the benchmark's launch, every one of the 48 (batch, head)
+    pairs against the oracle, element by element: rel-L2 <= 2e-2 per tensor over all
+    elements and per pair. The measured margins are printed."""
     w = WORKLOADS["train_fwdbwd"]
     host = make_inputs(w)
     out, hT, grads = _fwd_bwd(cuda_inputs(host))
-    pairs = [(0, 0), (3, 5), (7, 2)]
-    o_ref, h_ref = oracle_fwd(host, pairs)
-    assert rel(head_slice(out.cpu(), pairs), o_ref) <= TOL["bf16"]
-    assert rel(head_slice(hT.cpu(), pairs, state=True), h_ref) <= TOL["bf16"]
-    ref = oracle_bwd(host, pairs)
-    for n in GRADS:
-        got = head_slice(grads[n].cpu(), pairs, state=(n == "dh0"))
-        assert rel(got, ref[n]) <= TOL["bf16"], (n, rel(got, ref[n]))
-    for n in GRADS:  # the heads not sampled are finite
-        assert bool(torch.isfinite(grads[n].float()).all()), n
+    torch.cuda.synchronize()
+    o_ref, h_ref = oracle_fwd(host)
+    ref = oracle_bwd(host)
+    got = dict(grads, out=out, h_final=hT)
+    refs = dict(ref, out=o_ref, h_final=h_ref)
+    report = {}
+    for n in ("out", "h_final") + GRADS:
+        state = n in ("h_final", "dh0")
+        whole = rel(got[n], refs[n])
+        per = _per_head_rel(got[n], refs[n], state)
+        report[n] = (whole, float(per.max()), tuple(int(i) for i in np.unravel_index(per.argmax(), per.shape)))
+        assert whole <= TOL["bf16"], (n, whole)
+        assert per.max() <= TOL["bf16"], (n, per.max(), report[n][2])
+    print("\ntraining shape B8 T4096 H6 D128 bf16, rel-L2 vs oracle (all 48 heads; worst pair):")
+    for n, (whole, worst, at) in report.items():
+        print(f"  {n:8s} {whole:.3e}  worst pair {worst:.3e} at (b, h) = {at}")
 
 
 @pytest.mark.parametrize("D", [64, 128])
@@ -131,3 +151,26 @@ def test_scalar_decay_with_wipes(flags):
     ref = oracle_bwd(host)
     for n in GRADS:
         assert rel(grads[n], ref[n]) <= TOL["bf16"], (n, rel(grads[n], ref[n]))
+
+
+def test_concurrent_backward_calls_on_two_streams():
+    """The library owns no stream, event or lock: two backward calls on two streams at
+    the same time (different problems, disjoint buffers) both match the oracle."""
+    ws_ = [WORKLOADS["train_fwdbwd"].with_(B=2, T=1024, H=6, h0_std=0.2),
+           WORKLOADS["train_fwdbwd"].with_(B=3, T=512, H=4, h0_std=0.1)]
+    hosts = [make_inputs(w, seed=i) for i, w in enumerate(ws_)]
+    ds = [cuda_inputs(h) for h in hosts]
+    fwd = [gdn.gdn_chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], d["h0"]) for d in ds]
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    main = torch.cuda.current_stream()
+    results = []
+    for d, (out, hT, res), s in zip(ds, fwd, streams):
+        s.wait_stream(main)
+        with torch.cuda.stream(s):
+            results.append(gdn.gdn_chunk_bwd(d["q"], d["k"], d["v"], d["g"], d["beta"], d["h0"], res,
+                                             d["dout"], d["dh_final"]))
+    torch.cuda.synchronize()
+    for host, grads in zip(hosts, results):
+        ref = oracle_bwd(host)
+        for n in GRADS:
+            assert rel(grads[n], ref[n]) <= TOL["bf16"], (n, rel(grads[n], ref[n]))

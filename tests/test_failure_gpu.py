@@ -25,6 +25,21 @@ def test_wait_timeout_is_reported_and_the_context_stays_usable():
     assert gdn.gdn_check_device_error() == gdn.binding.GDN_OK
 
 
+def test_waits_after_a_timeout_give_up_early():
+    """Once a wait has timed out (error word set), the kernels' later waits give up after
+    about 4096 tries instead of running their full count of 4194304: the self-test's four
+    later waits together take a few times the cycles of its first 4096-try wait, where
+    four full waits would take about a thousand times as many."""
+    assert gdn.gdn_check_device_error() == gdn.binding.GDN_OK
+    cycles = torch.zeros(2, dtype=torch.int64, device="cuda")
+    gdn.gdn_selftest_wait_timeout(4096, cycles=cycles)
+    first, later = (int(x) for x in cycles.cpu())
+    assert gdn.gdn_check_device_error() == gdn.binding.GDN_ERR_INTERNAL
+    print(f"first wait {first} cycles, four later waits {later} cycles")
+    assert first > 0 and later > 0
+    assert later < 4 * 4 * first, (first, later)
+
+
 def test_selftest_rejects_unbounded_requests():
     with pytest.raises(gdn.GdnError):
         gdn.gdn_selftest_wait_timeout(0)

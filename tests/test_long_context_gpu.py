@@ -1,10 +1,10 @@
 """Long-context workload: B=1, T=32768, H=16, Dk=Dv=128, bf16 inputs, fp32 state.
 
 The chunked forward and the recurrent kernel run the whole problem on the GPU;
-the oracle checks three sampled heads over all 32768 tokens (heads never
-interact). Then the out-of-region slice: one 64-token chunk whose keys are not
-normalised (beta |k|^2 ~ beta Dk >> 2, the regime where the "gated-deltanet"
-card says the rule diverges), started from the oracle's own final state.
+the oracle checks all 16 heads over all 32768 tokens. Then the out-of-region
+slice: one 64-token chunk whose keys are not normalised (beta |k|^2 ~ beta Dk
+>> 2, the regime where the "gated-deltanet" card says the rule diverges),
+started from the oracle's own final state, for all 16 heads.
 """
 import numpy as np
 import pytest
@@ -17,7 +17,7 @@ from gated_deltanet_gdn_gb300.synthetic import WORKLOADS, make_inputs, out_of_re
 from helpers import TOL, head_slice, rel
 
 pytestmark = pytest.mark.gpu
-PAIRS = [(0, 0), (0, 7), (0, 15)]
+PAIRS = [(0, h) for h in range(16)]  # every head of the B1 H16 workload
 
 
 @pytest.fixture(scope="module")
@@ -33,17 +33,32 @@ def long_run():
     return w, host, out.cpu(), hT.cpu(), ro.cpu(), rh.cpu(), o_ref, h_ref
 
 
+def _report(label, out, hT, o_ref, h_ref):
+    o = head_slice(out, PAIRS).double().numpy()
+    h = head_slice(hT, PAIRS, state=True).double().numpy()
+    per_o = [np.linalg.norm(o[0, :, i] - o_ref[0, :, i]) / np.linalg.norm(o_ref[0, :, i]) for i in range(len(PAIRS))]
+    per_h = [np.linalg.norm(h[0, i] - h_ref[0, i]) / np.linalg.norm(h_ref[0, i]) for i in range(len(PAIRS))]
+    whole_o, whole_h = rel(head_slice(out, PAIRS), o_ref), rel(head_slice(hT, PAIRS, state=True), h_ref)
+    print(f"\n{label}: out {whole_o:.3e} (worst head {max(per_o):.3e}), "
+          f"h_final {whole_h:.3e} (worst head {max(per_h):.3e})")
+    return whole_o, whole_h, max(per_o), max(per_h)
+
+
 def test_long_context_chunked_forward(long_run):
+    """Every head, rel-L2 <= 2e-2 over the whole tensor and per head."""
     w, host, out, hT, ro, rh, o_ref, h_ref = long_run
-    assert rel(head_slice(out, PAIRS), o_ref) <= TOL["bf16"]
-    assert rel(head_slice(hT, PAIRS, state=True), h_ref) <= TOL["bf16"]
+    whole_o, whole_h, head_o, head_h = _report("long context chunked bf16", out, hT, o_ref, h_ref)
+    assert max(whole_o, head_o) <= TOL["bf16"] and max(whole_h, head_h) <= TOL["bf16"]
     assert bool(torch.isfinite(out.float()).all()) and bool(torch.isfinite(hT).all())
 
 
 def test_long_context_recurrent(long_run):
+    """Every head: out within the bf16 tolerance (bf16 output), the fp32 final state
+    within 1e-4 (exact recurrence in fp32), per head."""
     w, host, out, hT, ro, rh, o_ref, h_ref = long_run
-    assert rel(head_slice(ro, PAIRS), o_ref) <= TOL["bf16"]
-    assert rel(head_slice(rh, PAIRS, state=True), h_ref) <= 1e-4  # fp32 state, exact recurrence
+    whole_o, whole_h, head_o, head_h = _report("long context recurrent", ro, rh, o_ref, h_ref)
+    assert max(whole_o, head_o) <= TOL["bf16"]
+    assert max(whole_h, head_h) <= 1e-4
 
 
 def _perturbed_runs(args, rel, trials=8, seed=0):
@@ -87,21 +102,45 @@ def _aggregate_envelope(args, ref, rel):
 def _divergence_check(o_gpu, o_ref, tol, env):
     """Per-row rule: within max(tol, the row's perturbation envelope) while the
     oracle row norm stays below 1e30; non-finite once the oracle row leaves the
-    fp32 range."""
+    fp32 range. Returns the rows checked, the rows required non-finite, the largest
+    bound used and how many rows the envelope widened beyond tol."""
     o = o_gpu.double().numpy()
-    checked = nonfinite = 0
+    checked = nonfinite = widened = 0
+    largest = tol
     for t in range(o.shape[1]):
         for h in range(o.shape[2]):
             ref = o_ref[0, t, h]
             nrm = np.linalg.norm(ref)
             if nrm < 1e30:
                 err = np.linalg.norm(o[0, t, h] - ref) / max(nrm, 1e-30)
-                assert err <= max(tol, env[0, t, h]), (t, h, err, env[0, t, h])
+                bound = max(tol, env[0, t, h])
+                assert err <= bound, (t, h, err, env[0, t, h])
                 checked += 1
+                widened += int(bound > tol)
+                largest = max(largest, bound)
             elif not np.isfinite(nrm) or nrm > 3.4e38:
                 assert not np.all(np.isfinite(o[0, t, h])), (t, h)
                 nonfinite += 1
-    return checked, nonfinite
+    return checked, nonfinite, largest, widened
+
+
+def _early_rows_check(o_gpu, o_ref, tol, growth=1e3):
+    """The rows of each head before the oracle's output norm first grows past
+    `growth` times its first row's: per-row rel-L2 within tol. Returns (rows, worst)."""
+    o = o_gpu.double().numpy()
+    rows, worst = 0, 0.0
+    for h in range(o.shape[2]):
+        n0 = np.linalg.norm(o_ref[0, 0, h])
+        for t in range(o.shape[1]):
+            ref = o_ref[0, t, h]
+            nrm = np.linalg.norm(ref)
+            if not nrm < growth * n0:
+                break
+            err = np.linalg.norm(o[0, t, h] - ref) / nrm
+            worst = max(worst, err)
+            rows += 1
+            assert err <= tol, (t, h, err)
+    return rows, worst
 
 
 def test_out_of_region_slice_diverges_like_the_oracle(long_run):
@@ -113,7 +152,10 @@ def test_out_of_region_slice_diverges_like_the_oracle(long_run):
     by the arithmetic: Dk * 2^-24 (the dot-product rounding bound in fp32) for the
     recurrent kernel and the fp32 chunked path, checked row by row; 2^-9 (bf16
     operands) for the bf16 chunked path, checked by per-row norm ratio and in
-    aggregate, after it has reproduced the divergence (growth by > 1e6)."""
+    aggregate, after it has reproduced the divergence (growth by > 1e6), and row by
+    row at the bf16 tolerance itself on every head's rows before the oracle's output
+    has grown a thousandfold. The largest bound used and the number of rows whose
+    bound the envelope widened are printed."""
     w, host, out, hT, ro, rh, o_ref, h_ref = long_run
     h0 = torch.from_numpy(h_ref).to(torch.float32)  # the oracle's state after the region
     for dtype in ("bf16", "f32"):
@@ -127,19 +169,28 @@ def test_out_of_region_slice_diverges_like_the_oracle(long_run):
         c_out, _, _ = gdn.gdn_chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], d["h0"])
         torch.cuda.synchronize()
         env = _row_envelope(args, so_ref, w.Dk * 2.0 ** -24)
-        checked, _ = _divergence_check(r_out.cpu(), so_ref, TOL[dtype], env)
+        checked, nonfin, largest, widened = _divergence_check(r_out.cpu(), so_ref, TOL[dtype], env)
+        print(f"\nout-of-region {dtype} recurrent: {checked} rows checked ({widened} with the bound widened "
+              f"beyond {TOL[dtype]:g}, largest bound {largest:.3e}), {nonfin} rows non-finite as required")
         assert checked > 0
         if dtype == "f32":
-            checked, _ = _divergence_check(c_out.cpu(), so_ref, TOL["f32"], env)
+            checked, nonfin, largest, widened = _divergence_check(c_out.cpu(), so_ref, TOL["f32"], env)
+            print(f"out-of-region f32 chunked: {checked} rows checked ({widened} widened beyond 1e-4, "
+                  f"largest bound {largest:.3e}), {nonfin} rows non-finite as required")
         else:
             finite = np.isfinite(so_ref).all(axis=-1) & (norms < 1e30)
             co = c_out.double().cpu().numpy()
             cn = np.linalg.norm(co, axis=-1)
             assert cn[finite].max() > 1e6 * cn[:, :2].max()  # the chunked path diverges too
+            rows, worst = _early_rows_check(c_out.cpu(), so_ref, TOL["bf16"])
             env_ratio, env_agg = _aggregate_envelope(args, so_ref, 2.0 ** -9)
             ratio = np.abs(np.log10(cn[finite] / norms[finite])).max()
-            assert ratio <= env_ratio, (ratio, env_ratio)
             err = np.linalg.norm((co - so_ref)[finite]) / np.linalg.norm(so_ref[finite])
+            print(f"out-of-region bf16 chunked: {rows} early rows, worst rel-L2 {worst:.3e} (<= 2e-2); "
+                  f"norm ratio {ratio:.3f} decades (envelope {env_ratio:.3f}); aggregate {err:.3e} "
+                  f"(envelope {env_agg:.3e})")
+            assert rows > 0
+            assert ratio <= env_ratio, (ratio, env_ratio)
             assert err <= env_agg, (err, env_agg)
             checked = int(finite.sum())
         assert checked > 0
