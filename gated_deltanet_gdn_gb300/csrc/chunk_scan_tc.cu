@@ -511,7 +511,13 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(tensor_map_encode_fn());
+}
+
+}  // namespace
+
+void* tensor_map_encode_fn() {
+  static void* fn = nullptr;
   static std::once_flag once;
   std::call_once(once, [] {
     void* p = nullptr;
@@ -519,12 +525,10 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
     if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
             cudaSuccess &&
         q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+      fn = p;
   });
   return fn;
 }
-
-}  // namespace
 
 bool scan_tc_applies(int bf16_operands, int DK, int DV) { return bf16_operands && DK == TD && DV == TD; }
 

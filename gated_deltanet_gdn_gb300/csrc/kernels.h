@@ -211,6 +211,9 @@ cudaError_t launch_chunk_grads(const ChunkBwdArgs& a, cudaStream_t s);  // part 
 bool scan_tc_applies(int bf16_operands, int DK, int DV);
 cudaError_t launch_scan_fwd_tc(const ChunkFwdArgs& a, cudaStream_t s);
 cudaError_t launch_scan_bwd_tc(const ChunkBwdArgs& a, cudaStream_t s);
+// cuTensorMapEncodeTiled through the runtime's driver entry point, resolved once (NULL if
+// the driver does not provide it); callers cast it to PFN_cuTensorMapEncodeTiled_v12000.
+void* tensor_map_encode_fn();
 // The single-token decode kernel (decode.cu), used by launch_recurrent when T == 1.
 cudaError_t launch_decode(const RecurrentArgs& a, cudaStream_t s);
 // q/k L2 normalisation for the chunked path (l2norm.cu): rows = B * T * H.

@@ -76,14 +76,16 @@ def test_prefill_decode_workload_bitwise_and_parity():
     assert rel(h_full, h_ref) <= TOL["f32"]
 
 
+@pytest.mark.parametrize("H", [100, 3])
 @pytest.mark.parametrize("dtype,dims,per_channel", [("bf16", (128, 128), True), ("f32", (64, 128), True),
                                                    ("f32", (128, 64), False), ("bf16", (64, 64), False)])
-def test_single_token_calls_equal_one_call(dtype, dims, per_channel):
+def test_single_token_calls_equal_one_call(dtype, dims, per_channel, H):
     """A sequence decoded one token per call (the single-token decode kernel, state
     carried in place) equals one prefill call bitwise, for every head geometry, both
-    gate shapes and both input types; with more heads than SMs each decode CTA takes
-    several heads."""
-    w = WORKLOADS["tiny_fwd"].with_(B=2, T=24, H=100, Dk=dims[0], Dv=dims[1], dtype=dtype,
+    gate shapes and both input types. With H = 100 (200 heads, more than SMs) each
+    decode CTA takes several whole heads; with H = 3 (fewer heads than SMs) each CTA
+    takes a 32-column slice of one head."""
+    w = WORKLOADS["tiny_fwd"].with_(B=2, T=24, H=H, Dk=dims[0], Dv=dims[1], dtype=dtype,
                                     g_per_channel=per_channel, h0_std=0.1)
     d = cuda_inputs(make_inputs(w))
     out_full, h_full = _run(d)
