@@ -206,6 +206,11 @@ def kernel_work(B, T, H, D, es=2):
         "chunk_grads_kernel": (3 * CD + C * es + 3 * CD + 2 * CC + gam + 3 * CD + 2 * 2 * C * 4,
                                4 * C * C * D * 2),
         "chunk_bwd_finalize_kernel": (C * 4 + 2 * 2 * C * 4 + C * es, 0),
+        # fused chunk gradients on tcgen05: reads T, dU, U, state, dS, dout, q, k, v, g, beta;
+        # writes dq, dk, dv, dg, dbeta (no intermediate records)
+        "chunk_bwd_tc_kernel": (CC + 3 * CD + 2 * DD + CD + 4 * CD + C * es + 4 * CD + C * es,
+                                2 * D * C * C + 2 * 2 * C * D * D + 2 * D * D * 2 * C + 2 * D * C * D
+                                + 2 * D * 2 * C * C + 2 * D * C * 2 * C),
     }
     per["chunk_scan_fwd_tc_kernel"] = per["chunk_scan_fwd_kernel"]
     # the tensor-core reverse scan's launch also runs the dQ-hat / dAqk products
@@ -356,7 +361,7 @@ def run_gdn(args, world, rank, local):
             kernels[name]["gbs"] = round(b / (avg / 1e3) / 1e9, 1)
             kernels[name]["tflops"] = round(f / (avg / 1e3) / 1e12, 2)
     dom = max(prof, key=lambda k: prof[k][0])
-    b, f = work[dom]
+    b, f = work.get(dom, (0, 0))
     avg = prof[dom][0] / prof[dom][1]
     # The roofline of the whole pass (the chunked fwd + bwd is HBM-bound as a whole): the
     # method's bytes per step with fp32 chunk-start states between the passes, over the

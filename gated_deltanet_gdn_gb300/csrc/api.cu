@@ -142,7 +142,8 @@ const char* kKernelNames[K_COUNT] = {"chunk_prep_kernel",    "chunk_scan_fwd_ker
                                      "chunk_bwd_finalize_kernel", "chunk_out_kernel",
                                      "chunk_scan_fwd_tc_kernel", "chunk_scan_bwd_tc_kernel",
                                      "decode_kernel", "l2norm_rows_kernel", "l2norm_bwd_kernel",
-                                     "replay_decode_kernel", "replay_state_kernel", "chunk_dqa_kernel"};
+                                     "replay_decode_kernel", "replay_state_kernel", "chunk_dqa_kernel",
+                                     "chunk_bwd_tc_kernel"};
 
 }  // namespace
 

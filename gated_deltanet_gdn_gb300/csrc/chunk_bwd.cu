@@ -417,9 +417,10 @@ template <int DK, int DV>
 cudaError_t launch_bwd_t(const ChunkBwdArgs& a, cudaStream_t s) {
   const int N = a.T / C, BH = a.B * a.H;
   cudaError_t e;
-  // The products that need only the forward's records and dO (dQ-hat, dAqk) run as
-  // extra CTAs of the tensor-core reverse scan's launch, on the SMs the scan leaves free;
-  // after the CUDA-core scan they are a kernel of their own.
+  // Dk = Dv = 128: the tensor-core reverse scan, then one fused tensor-core kernel for
+  // every chunk product and gradient (chunk_bwd_tc.cu). Dk = 64: the CUDA-core scan, then
+  // the products that need no scan result (chunk_dqa.cuh), the state products, the score
+  // gradients and the channel-group sums.
   const bool tc = scan_tc_applies(1, DK, DV);
   if (tc) {
     if ((e = launch_scan_bwd_tc(a, s)) != cudaSuccess) return e;
@@ -433,6 +434,7 @@ cudaError_t launch_bwd_t(const ChunkBwdArgs& a, cudaStream_t s) {
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   if (N == 0) return cudaSuccess;
+  if (bwd_tc_applies(DK, DV)) return launch_chunk_bwd_tc(a, s);
   if (!tc) {
     const int bytes = DqaLayout<DK, DV>::BYTES + 1024;
     auto kern = chunk_dqa_kernel<DK, DV>;

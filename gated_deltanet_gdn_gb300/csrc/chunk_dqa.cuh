@@ -1,9 +1,8 @@
 // The chunk products of the backward that need only forward records and dO:
 //   dQ-hat = scale dO S0^T  and  dAqk = scale (dO U^T) masked j <= t
-// (chunked WY backward, see chunk_bwd.cu). They run beside the reverse state scan:
-// as extra CTAs of the tensor-core reverse scan's own launch (chunk_scan_tc.cu), which
-// holds one CTA per (batch, head) and leaves most SMs free, and as a kernel of their
-// own after the CUDA-core scan (chunk_bwd.cu). Included by both translation units.
+// (chunked WY backward, see chunk_bwd.cu), as a kernel of their own after the CUDA-core
+// reverse scan (Dk = 64; at Dk = Dv = 128 the fused tensor-core kernel of chunk_bwd_tc.cu
+// computes them with the other chunk products).
 #pragma once
 
 #include "common.cuh"
@@ -15,8 +14,7 @@ namespace {
 constexpr int DQA_THREADS = 256;
 constexpr int DQA_CG = DQA_THREADS / 128;  // column groups (4 row groups of warps each)
 
-// The DQA_THREADS threads of this role synchronise on named barrier 2 (the tensor-core
-// scan's launch has one more warp, which takes no part).
+// The DQA_THREADS threads of the kernel synchronise on named barrier 2.
 __device__ __forceinline__ void dqa_sync() { asm volatile("bar.sync 2, 256;\n" ::: "memory"); }
 
 template <int DK, int DV>
@@ -27,10 +25,8 @@ struct DqaLayout {
   static constexpr int BYTES = a1k(S0 + DV * DK * 2);
 };
 
-// Chunk-heads unit0, unit0 + stride, ... (persistent: the launch gives about one CTA per
-// SM that the reverse scan leaves free, so the HBM traffic of these products spreads over
-// the scan's duration instead of competing with the scan's loads in one burst). Called by
-// threads 0 .. DQA_THREADS - 1 of a CTA; sm is its 1024-byte aligned shared memory.
+// Chunk-heads unit0, unit0 + stride, ... Called by threads 0 .. DQA_THREADS - 1 of a CTA;
+// sm is its 1024-byte aligned shared memory.
 template <int DK, int DV>
 __device__ __forceinline__ void dqa_units(const ChunkBwdArgs& a, uint8_t* sm, int unit0, int stride, int tid) {
   typedef bf16 T;

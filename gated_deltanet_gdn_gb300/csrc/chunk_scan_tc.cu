@@ -26,7 +26,6 @@
 
 #include <mutex>
 
-#include "chunk_dqa.cuh"
 #include "common.cuh"
 #include "kernels.h"
 #include "umma.cuh"
@@ -339,19 +338,12 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, i
       : "memory");
 }
 
-// Blocks 0 .. B*H - 1 scan one (batch, head) each; the blocks after them compute the
-// products that need no scan result (chunk_dqa.cuh) on the SMs the scan leaves free.
 __global__ void __launch_bounds__(TC_THREADS, 1)
     chunk_scan_bwd_tc_kernel(ChunkBwdArgs a, const __grid_constant__ CUtensorMap dout_map) {
   pdl_wait();  // no early trigger: one wave for the whole scan, successors must not park beside it
   typedef TcBwdLayout L;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = align1024(smem_raw);
-  if ((int)blockIdx.x >= a.B * a.H) {
-    if ((int)threadIdx.x < DQA_THREADS)
-      dqa_units<TD, TD>(a, sm, (int)blockIdx.x - a.B * a.H, (int)gridDim.x - a.B * a.H, (int)threadIdx.x);
-    return;
-  }
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int bh = blockIdx.x, b = bh / a.H, h = bh % a.H;
   const int N = a.T / C;
@@ -556,20 +548,11 @@ cudaError_t launch_scan_bwd_tc(const ChunkBwdArgs& a, cudaStream_t s) {
              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
     return cudaErrorInvalidValue;
-  static_assert(TcBwdLayout::BYTES >= DqaLayout<TD, TD>::BYTES, "the products' CTAs share the scan's shared memory");
   const int bytes = TcBwdLayout::BYTES + 1024;
   cudaError_t e = cudaFuncSetAttribute(chunk_scan_bwd_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
   if (e != cudaSuccess) return e;
-  int dev = 0, nsm = 0;
-  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
-  if ((e = cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
-  // one scan CTA per (b, h), then one products CTA per SM the scans leave free (at least
-  // half the SMs), never more than there are chunk-heads
-  const int BH = a.B * a.H, units = (a.T / C) * BH;
-  const int free_sms = nsm - BH > nsm / 2 ? nsm - BH : nsm / 2;
-  const int extra = units < free_sms ? units : free_sms;
   prof_mark(K_SCAN_BWD_TC, s, true);
-  e = launch_pdl(chunk_scan_bwd_tc_kernel, dim3(BH + extra), dim3(TC_THREADS), bytes, s, a, map);
+  e = launch_pdl(chunk_scan_bwd_tc_kernel, dim3(a.B * a.H), dim3(TC_THREADS), bytes, s, a, map);
   prof_mark(K_SCAN_BWD_TC, s, false);
   return e;
 }

@@ -12,6 +12,7 @@ constexpr int BLK = 32;     // block length inside a chunk
 constexpr int NT = 32;      // value columns per warp column group of the mma.sync scans
 constexpr int NTS = 64;     // value columns per state-scan CTA (two record slices)
 constexpr float SAFE_SPREAD = 80.f;  // max decay spread (nats) for row-scaled in-block scores
+constexpr int FLAG_PAIRWISE = 1;     // dims.flags bit: in-block scores always pairwise
 
 // Per (batch, head) and chunk, the forward writes these records. Byte sizes of one record
 // for operand element size es; every record starts 1024-byte aligned inside its region.
@@ -96,6 +97,12 @@ inline BwdWorkspaceLayout bwd_workspace_layout(int B, int T, int H, int DK, int 
   };
   put(L.du, L.du_b);
   put(L.dstate, L.dstate_b);
+  // Dk = Dv = 128 runs the fused chunk-gradient kernel (chunk_bwd_tc.cu), which needs only
+  // dU and dS from the reverse scan; the other regions serve the Dk = 64 kernels
+  if (DK == 128 && DV == 128) {
+    L.total = off;
+    return L;
+  }
   put(L.dqh, L.dqh_b);
   put(L.dbk, L.dbk_b);
   put(L.dkt, L.dkt_b);
@@ -195,9 +202,9 @@ enum KernelId {
   K_L2NORM_BWD = 12,  // l2norm_bwd_kernel
   K_REPLAY = 13,      // replay_decode_kernel
   K_REPLAY_STATE = 14,  // replay_state_kernel
-  K_DQA = 15,           // chunk_dqa_kernel (after the CUDA-core reverse scan; the tensor-core
-                        // reverse scan's launch includes these products)
-  K_COUNT = 16
+  K_DQA = 15,           // chunk_dqa_kernel (Dk = 64 path)
+  K_BWD_TC = 16,        // chunk_bwd_tc_kernel: every chunk product of the backward, fused, tcgen05
+  K_COUNT = 17
 };
 // Records a CUDA event on s before (begin = true) or after a launch when timing is on.
 void prof_mark(KernelId id, cudaStream_t s, bool begin);
@@ -211,6 +218,10 @@ cudaError_t launch_chunk_grads(const ChunkBwdArgs& a, cudaStream_t s);  // part 
 bool scan_tc_applies(int bf16_operands, int DK, int DV);
 cudaError_t launch_scan_fwd_tc(const ChunkFwdArgs& a, cudaStream_t s);
 cudaError_t launch_scan_bwd_tc(const ChunkBwdArgs& a, cudaStream_t s);
+// The fused chunk-gradient kernel on tcgen05 (chunk_bwd_tc.cu), for Dk = Dv = 128 (bf16);
+// it needs only the du and dstate parts of the backward workspace.
+bool bwd_tc_applies(int DK, int DV);
+cudaError_t launch_chunk_bwd_tc(const ChunkBwdArgs& a, cudaStream_t s);
 // cuTensorMapEncodeTiled through the runtime's driver entry point, resolved once (NULL if
 // the driver does not provide it); callers cast it to PFN_cuTensorMapEncodeTiled_v12000.
 void* tensor_map_encode_fn();

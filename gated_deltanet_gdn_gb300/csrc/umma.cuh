@@ -104,4 +104,57 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32]) 
 }
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;\n" ::: "memory"); }
 
+// 8 / 16 consecutive fp32 columns of the calling thread's TMEM lane, without the
+// completion wait (several loads may be in flight; tmem_wait_ld() before using them).
+__device__ __forceinline__ void tmem_ld4_nowait(uint32_t taddr, uint32_t (&r)[4]) {
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0,%1,%2,%3}, [%4];\n"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(taddr)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_ld8_nowait(uint32_t taddr, uint32_t (&r)[8]) {
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];\n"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+               : "r"(taddr)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_ld16_nowait(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];\n"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr)
+      : "memory");
+}
+__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;\n" ::: "memory"); }
+// 16 consecutive 32-bit columns of the calling thread's TMEM lane (tmem_wait_st() after).
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};\n" ::"r"(
+          taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),
+      "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+      : "memory");
+}
+
+// Shared-memory descriptors of the swizzled tiles of common.cuh (bf16, 64-element =
+// 128-byte panels, 1024-byte aligned). A tile stores ROWS rows of COLS elements as
+// COLS / 64 column panels, each ROWS x 128 bytes; `panel` below is that panel stride in
+// bytes (ROWS * 128).
+//  * K-major operand: tile rows are the M (or N) index, tile columns the K index.
+//    Eight-row groups are 1024 bytes apart; a K step of 16 elements advances 32 bytes
+//    inside a panel and a whole panel every four steps.
+//  * MN-major operand: tile rows are the K index, tile columns the M (or N) index.
+//    Consecutive 64-element M chunks are one panel apart (leading byte offset), eight
+//    K rows are 1024 bytes apart, and a K step of 16 rows advances 2048 bytes.
+// The start address field holds address / 16, so stepping inside a tile is an add.
+__device__ __forceinline__ uint64_t desc_kmajor(const void* base) { return umma_desc_sw128(smem_u32(base), 16, 1024); }
+__device__ __forceinline__ uint64_t desc_mnmajor(const void* base, int panel) {
+  return umma_desc_sw128(smem_u32(base), (uint32_t)panel, 1024);
+}
+__device__ __forceinline__ uint64_t kstep_kmajor(uint64_t d, int ks, int panel) {
+  return d + (uint64_t)(((ks >> 2) * panel + (ks & 3) * 32) >> 4);
+}
+__device__ __forceinline__ uint64_t kstep_mnmajor(uint64_t d, int ks) { return d + (uint64_t)((ks * 2048) >> 4); }
+
 }  // namespace gdn
