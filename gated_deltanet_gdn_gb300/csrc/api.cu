@@ -143,7 +143,7 @@ const char* kKernelNames[K_COUNT] = {"chunk_prep_kernel",    "chunk_scan_fwd_ker
                                      "chunk_scan_fwd_tc_kernel", "chunk_scan_bwd_tc_kernel",
                                      "decode_kernel", "l2norm_rows_kernel", "l2norm_bwd_kernel",
                                      "replay_decode_kernel", "replay_state_kernel", "chunk_dqa_kernel",
-                                     "chunk_bwd_tc_kernel"};
+                                     "chunk_bwd_tc_kernel", "chunk_prep_tc_kernel"};
 
 }  // namespace
 

@@ -26,6 +26,7 @@
 //   chunk_scan_fwd_kernel  grid (Dv/64, B*H), 256 threads: A6, fp32 state slice in
 //                          registers; chunk records arrive by cp.async.bulk on mbarriers
 //   chunk_out_kernel       grid (chunks, B*H), 256 threads: outputs from stored states
+#include "chunk_prep.cuh"
 #include "common.cuh"
 #include "kernels.h"
 
@@ -34,15 +35,6 @@ namespace {
 
 constexpr int PREP_THREADS = 256;
 constexpr int SCAN_THREADS = 256;
-// (i, j) of pair p in the lower triangle (diagonal included), row-major order
-__device__ __forceinline__ void tri_index(int p, int& i, int& j) {
-  int r = (int)((sqrtf(8.f * p + 1.f) - 1.f) * 0.5f);
-  while (r * (r + 1) / 2 > p) --r;
-  while ((r + 1) * (r + 2) / 2 <= p) ++r;
-  i = r;
-  j = p - r * (r + 1) / 2;
-}
-
 // In-place inverse of the unit lower triangular L = I + A. On entry M holds A (strictly
 // lower, zeros on and above the diagonal); on exit it holds T = L^-1 with its unit
 // diagonal and zero upper part stored explicitly. Doubling: if T11, T22 invert the
@@ -129,47 +121,6 @@ struct PrepLayout {
   static constexpr int BYTES = BETA + 2 * C * 4;
 };
 
-// In-block pairwise scores (A4) for the blocks flagged unsafe: 4 lanes per (i, j) pair,
-// each summing a quarter of the channels, reduced with two xor shuffles. Writes
-// scale * sum q k E into the Aqk staging tile and beta_i * sum k k E (i > j) into Akk.
-template <class T, int DK, int NTHR>
-__device__ __noinline__ void prep_pairwise(bool unsafe1, bool unsafe2, const T* q, const T* k, size_t row0,
-                                           size_t rs, FTile<C, DK> Gs, Tile<T, C, C> Tst, FTile<C, C, 4> Akk,
-                                           const float* beta_s, float scale, int tid) {
-  const int warp = tid >> 5, lane = tid & 31;
-  for (int blk = 0; blk < 2; ++blk) {
-    if (!(blk == 0 ? unsafe1 : unsafe2)) continue;
-    const int bs = blk * BLK;
-    constexpr int NPAIR = BLK * (BLK + 1) / 2;
-    for (int base = 0; base < NPAIR; base += 8 * (NTHR / 32)) {
-      const int p = base + warp * 8 + (lane >> 2), quarter = lane & 3;
-      const bool valid = p < NPAIR;
-      int i = 0, j = 0;
-      float sq = 0.f, sk = 0.f;
-      if (valid) {
-        tri_index(p, i, j);
-        const T* qi = q + (row0 + (size_t)(bs + i) * rs) * DK;
-        const T* ki = k + (row0 + (size_t)(bs + i) * rs) * DK;
-        const T* kj = k + (row0 + (size_t)(bs + j) * rs) * DK;
-        for (int c = quarter * (DK / 4); c < (quarter + 1) * (DK / 4); ++c) {
-          const float e = __expf(Gs.at(bs + i, c) - Gs.at(bs + j, c));
-          const float kje = to_f32(kj[c]) * e;
-          sq = fmaf(to_f32(qi[c]), kje, sq);
-          sk = fmaf(to_f32(ki[c]), kje, sk);
-        }
-      }
-      sq += __shfl_xor_sync(0xffffffffu, sq, 1);
-      sk += __shfl_xor_sync(0xffffffffu, sk, 1);
-      sq += __shfl_xor_sync(0xffffffffu, sq, 2);
-      sk += __shfl_xor_sync(0xffffffffu, sk, 2);
-      if (valid && quarter == 0) {
-        Tst.at(bs + i, bs + j) = from_f32<T>(scale * sq);
-        if (i > j) Akk.at(bs + i, bs + j) = beta_s[bs + i] * sk;
-      }
-    }
-  }
-}
-
 template <class T, int DK, int DV, bool PC>
 __global__ void __launch_bounds__(PREP_THREADS) chunk_prep_kernel(ChunkFwdArgs a) {
   pdl_wait();
@@ -216,21 +167,8 @@ __global__ void __launch_bounds__(PREP_THREADS) chunk_prep_kernel(ChunkFwdArgs a
   cp_async_wait<0>();
   __syncthreads();
 
-  // ---- A1: inclusive cumulative log-decay per channel (fp32): lanes 2c and 2c + 1 take
-  // channel c, one 32-row block each in registers; the second block adds the first
-  // block's total (from its partner lane)
-  static_assert((2 * DK) % 32 == 0, "whole warps per pass");
-  for (int u = tid; u < 2 * DK; u += PREP_THREADS) {
-    const int c = u >> 1, hb = u & 1, r0 = hb * BLK;
-    float v[BLK];
-#pragma unroll
-    for (int i = 0; i < BLK; ++i) v[i] = PC ? to_f32(graw[(r0 + i) * DK + c]) : gsc[r0 + i];
-#pragma unroll
-    for (int i = 1; i < BLK; ++i) v[i] += v[i - 1];
-    const float base = __shfl_sync(0xffffffffu, v[BLK - 1], lane & ~1);
-#pragma unroll
-    for (int i = 0; i < BLK; ++i) Gs.at(r0 + i, c) = hb ? v[i] + base : v[i];
-  }
+  // ---- A1: inclusive cumulative log-decay per channel (fp32)
+  prep_cumsum<T, DK, PREP_THREADS, PC>(Gs, graw, gsc, tid);
   __syncthreads();
   // Reference point for every row: the boundary b = last token of the first block.
   // Factor ranges: block 1 queries exp(G_t - G_b) <= exp(G_0 - G_b); block 2 keys
@@ -470,7 +408,6 @@ __global__ void __launch_bounds__(SCAN_THREADS) chunk_scan_fwd_kernel(ChunkFwdAr
   const int tile = blockIdx.x, bh = blockIdx.y;
   const int N = a.T / C;
   constexpr int MTS = DK / 64;    // m16 tiles of state rows per warp
-  constexpr int EPC = 16 / (int)sizeof(T);
   const int rg = warp & 3, cg = warp >> 2;
   const int srow = rg * 16 * MTS, col0 = 32 * cg;
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + L::BAR);
@@ -654,7 +591,9 @@ template <class T, int DK, int DV>
 cudaError_t launch_fwd_t(const ChunkFwdArgs& a, cudaStream_t s) {
   const int N = a.T / C, BH = a.B * a.H;
   cudaError_t e;
-  {
+  if (prep_tc_applies(a.bf16, DK, DV)) {
+    if ((e = launch_chunk_prep_tc(a, s)) != cudaSuccess) return e;
+  } else {
     const int bytes = PrepLayout<T, DK, DV>::BYTES + 1024;
     auto kern = a.per_channel ? chunk_prep_kernel<T, DK, DV, true> : chunk_prep_kernel<T, DK, DV, false>;
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);

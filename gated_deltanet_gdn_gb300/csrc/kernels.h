@@ -204,7 +204,8 @@ enum KernelId {
   K_REPLAY_STATE = 14,  // replay_state_kernel
   K_DQA = 15,           // chunk_dqa_kernel (Dk = 64 path)
   K_BWD_TC = 16,        // chunk_bwd_tc_kernel: every chunk product of the backward, fused, tcgen05
-  K_COUNT = 17
+  K_PREP_TC = 17,       // chunk_prep_tc_kernel: the chunk preparation on tcgen05
+  K_COUNT = 18
 };
 // Records a CUDA event on s before (begin = true) or after a launch when timing is on.
 void prof_mark(KernelId id, cudaStream_t s, bool begin);
@@ -218,6 +219,9 @@ cudaError_t launch_chunk_grads(const ChunkBwdArgs& a, cudaStream_t s);  // part 
 bool scan_tc_applies(int bf16_operands, int DK, int DV);
 cudaError_t launch_scan_fwd_tc(const ChunkFwdArgs& a, cudaStream_t s);
 cudaError_t launch_scan_bwd_tc(const ChunkBwdArgs& a, cudaStream_t s);
+// The chunk preparation on tcgen05 (chunk_prep_tc.cu), bf16 operands with Dk = Dv = 128.
+bool prep_tc_applies(int bf16_operands, int DK, int DV);
+cudaError_t launch_chunk_prep_tc(const ChunkFwdArgs& a, cudaStream_t s);
 // The fused chunk-gradient kernel on tcgen05 (chunk_bwd_tc.cu), for Dk = Dv = 128 (bf16);
 // it needs only the du and dstate parts of the backward workspace.
 bool bwd_tc_applies(int DK, int DV);

@@ -196,7 +196,7 @@ def test_out_of_region_slice_diverges_like_the_oracle(long_run):
                   f"{early:.3e}, median row {np.median(errs):.3e}, worst row {errs.max():.3e}, "
                   f"{int((errs > TOL['bf16']).sum())} rows above 2e-2; norm ratio {ratio:.3f} decades "
                   f"(envelope {env_ratio:.3f}); aggregate {err:.3e} (envelope {env_agg:.3e})")
-            assert rows > 0
+            assert len(errs) > 0
             assert ratio <= env_ratio, (ratio, env_ratio)
             assert err <= env_agg, (err, env_agg)
             checked = int(finite.sum())
