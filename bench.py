@@ -212,15 +212,16 @@ def kernel_work(B, T, H, D, es=2):
                                 2 * D * C * C + 2 * 2 * C * D * D + 2 * D * D * 2 * C + 2 * D * C * D
                                 + 2 * D * 2 * C * C + 2 * D * C * 2 * C),
     }
+    # the tensor-core kernels keep the record contracts of the CUDA-core ones they replace
+    per["chunk_prep_tc_kernel"] = per["chunk_prep_kernel"]
     per["chunk_scan_fwd_tc_kernel"] = per["chunk_scan_fwd_kernel"]
-    # the tensor-core reverse scan's launch also runs the dQ-hat / dAqk products
-    per["chunk_scan_bwd_tc_kernel"] = tuple(a + b for a, b in zip(per["chunk_scan_bwd_kernel"],
-                                                                   per["chunk_dqa_kernel"]))
+    per["chunk_scan_bwd_tc_kernel"] = per["chunk_scan_bwd_kernel"]
     return {k: (b * n, f * n) for k, (b, f) in per.items()}
 
 
 # the files the chunk kernels (the ones profiles/traffic.json covers) are compiled from
 CHUNK_KERNEL_SOURCES = ("chunk_fwd.cu", "chunk_bwd.cu", "chunk_grads.cu", "chunk_scan_tc.cu",
+                        "chunk_prep_tc.cu", "chunk_bwd_tc.cu", "chunk_prep.cuh", "chunk_dqa.cuh",
                         "common.cuh", "umma.cuh", "kernels.h")
 
 
