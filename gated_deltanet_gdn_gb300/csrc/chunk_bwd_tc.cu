@@ -95,16 +95,6 @@ static_assert(BtLayout::CTOT + NTG * BD * 4 <= BtLayout::COLP, "the dG totals fi
 
 __device__ __forceinline__ void epi_sync() { asm volatile("bar.sync 1, 512;\n" ::: "memory"); }
 
-// dO box (64 value columns x 1 head x 64 tokens), 3-D TMA tensor load
-__device__ __forceinline__ void tma_load_3d_bt(void* dst, const CUtensorMap* map, int c0, int c1, int c2,
-                                               uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], "
-      "[%5];\n" ::"r"(smem_u32(dst)),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(bar))
-      : "memory");
-}
-
 __device__ __forceinline__ float u2f(uint32_t x) { return __uint_as_float(x); }
 // Input element through the read-only path: the compiler may move these loads ahead of
 // the kernel's stores, so each loop below issues its loads as one batch.
@@ -114,11 +104,6 @@ __device__ __forceinline__ float ldg_bf16(const bf16* p) {
 __device__ __forceinline__ uint32_t pack2_bf16(float x, float y) {
   __nv_bfloat162 h = __floats2bfloat162_rn(x, y);
   return *reinterpret_cast<uint32_t*>(&h);
-}
-
-// Bulk prefetch of `bytes` (a multiple of 16, 16-byte aligned) at p into L2.
-__device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
-  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;\n" ::"l"(p), "r"(bytes) : "memory");
 }
 
 // Sums over the 32 lanes of a warp of TPT = 16 values per lane at once (recursive
@@ -238,8 +223,8 @@ __global__ void __launch_bounds__(BT_THREADS, 1)
     bulk_g2s(sm + L::TM, static_cast<const bf16*>(a.res.tmat) + ch * (C * C), C * C * 2, fullA);
     bulk_g2s(sm + L::DUT, static_cast<const bf16*>(a.ws.du) + ch * (C * BD), BD * C * 2, fullA);
     const int b = bh / a.H, h = bh % a.H, tok = b * a.T + n * C;
-    tma_load_3d_bt(sm + L::VT, &v_map, 0, h, tok, fullA);                // v, columns 0-63
-    tma_load_3d_bt(sm + L::VT + C * 128, &v_map, 64, h, tok, fullA);     // columns 64-127
+    tma_load_3d(sm + L::VT, &v_map, 0, h, tok, fullA);                // v, columns 0-63
+    tma_load_3d(sm + L::VT + C * 128, &v_map, 64, h, tok, fullA);     // columns 64-127
   };
   auto load_b = [&](int m) {
     int n, bh;
@@ -247,8 +232,8 @@ __global__ void __launch_bounds__(BT_THREADS, 1)
     const size_t ch = (size_t)bh * N + n;
     mbar_arrive_expect_tx(fullB, L::TXB);
     const int b = bh / a.H, h = bh % a.H, tok = b * a.T + n * C;
-    tma_load_3d_bt(sm + L::DY, &dout_map, 0, h, tok, fullB);                 // dO, columns 0-63
-    tma_load_3d_bt(sm + L::DY + 2 * C * 128, &dout_map, 64, h, tok, fullB);  // columns 64-127
+    tma_load_3d(sm + L::DY, &dout_map, 0, h, tok, fullB);                 // dO, columns 0-63
+    tma_load_3d(sm + L::DY + 2 * C * 128, &dout_map, 64, h, tok, fullB);  // columns 64-127
     bulk_g2s(sm + L::UT, static_cast<const bf16*>(a.res.u) + ch * (C * BD), BD * C * 2, fullB);
     bulk_g2s(sm + L::S0T, static_cast<const bf16*>(a.res.state) + ch * (BD * BD), BD * BD * 2, fullB);
     bulk_g2s(sm + L::DS1T, static_cast<const bf16*>(a.ws.dstate) + ch * (BD * BD), BD * BD * 2, fullB);

@@ -328,16 +328,6 @@ struct TcBwdLayout {
   static constexpr uint32_t TX = (uint32_t)(4 * C * TD * 2 + C * C * 2 + TD * 4);
 };
 
-// dO box (64 value columns x 64 tokens of one head) by a 3-D TMA tensor load
-__device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, int c0, int c1, int c2,
-                                            uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], "
-      "[%5];\n" ::"r"(smem_u32(dst)),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(bar))
-      : "memory");
-}
-
 __global__ void __launch_bounds__(TC_THREADS, 1)
     chunk_scan_bwd_tc_kernel(ChunkBwdArgs a, const __grid_constant__ CUtensorMap dout_map) {
   pdl_wait();  // no early trigger: one wave for the whole scan, successors must not park beside it
