@@ -80,7 +80,7 @@ struct BtLayout {
   static constexpr int DGP = DBP + 4 * C * 4;      // [4][C] scalar dg partials
   static constexpr int GX = DGP + 4 * C * 4;       // [NTG][Dk] token-group totals of g
   static constexpr int COLP = GX + NTG * BD * 4;   // [NTG][Dk] K-tilde column partials
-  static constexpr int DGAM = COLP + NTG * BD * 4; // [NTG][Dk] dgam partials
+  static constexpr int DGAM = COLP + NTG * BD * 4; // [Dk] dgam (room for [NTG][Dk])
   static constexpr int CTOT = GX;                  // [NTG][Dk] token-group totals of dG (final
                                                    // epilogue only; GX is read before it)
   static constexpr int FLAGS = DGAM + NTG * BD * 4;  // int [4]: unsafe1, unsafe2
@@ -124,6 +124,22 @@ __device__ __forceinline__ float warp_sum16(float (&x)[16], int lane) {
   return x[0] + __shfl_xor_sync(0xffffffffu, x[0], 1);
 }
 
+// Sums over the 32 lanes of a warp of 8 values per lane (recursive halving, 4 + 2 + 1
+// shuffles, then two more). On return lane l holds the warp total of value (l >> 2) & 7.
+__device__ __forceinline__ float warp_sum8(float (&x)[8], int lane) {
+#pragma unroll
+  for (int h = 4; h >= 1; h >>= 1) {
+    const bool up = (lane & (4 * h)) != 0;  // this lane keeps the upper half of its values
+#pragma unroll
+    for (int i = 0; i < h; ++i) {
+      const float send = up ? x[i] : x[i + h];
+      const float keep = up ? x[i + h] : x[i];
+      x[i] = keep + __shfl_xor_sync(0xffffffffu, send, 4 * h);
+    }
+  }
+  float r = x[0] + __shfl_xor_sync(0xffffffffu, x[0], 2);
+  return r + __shfl_xor_sync(0xffffffffu, r, 1);
+}
 
 // In-block score gradients summed pairwise (blocks whose row factors would leave the fp32
 // range, or every block with GDN_FLAG_PAIRWISE_WITHIN_BLOCK): for token t of block
@@ -255,7 +271,6 @@ __global__ void __launch_bounds__(BT_THREADS, 1)
   const bool mask_form = !PC && !force;
   const bf16* qg = static_cast<const bf16*>(a.q);
   const bf16* kg = static_cast<const bf16*>(a.k);
-  const bf16* vg = static_cast<const bf16*>(a.v);
   const bf16* gg = static_cast<const bf16*>(a.g);
   const bf16* bg = static_cast<const bf16*>(a.beta);
   const size_t rs = (size_t)a.H;  // token stride in rows
@@ -291,17 +306,6 @@ __global__ void __launch_bounds__(BT_THREADS, 1)
     if (cur && tid < C) {
       const size_t r = ((size_t)(bh / a.H) * a.T + (size_t)n * C + tid) * a.H + (bh % a.H);
       beta_pre = ldg_bf16(bg + r);
-    }
-    // The next chunk's q, k, v and (per-channel) g rows go to L2 now, so that the
-    // epilogues' element loads of that chunk find them there: thread i < 256 takes row
-    // i % 64 of tensor i / 64 (one 256-byte row of one head).
-    if (m + 1 < nunits && tid < 4 * C) {
-      int n1, bh1;
-      unit_of(m + 1, n1, bh1);
-      const int tsel = tid >> 6, j = tid & (C - 1);
-      const size_t r1 = ((size_t)(bh1 / a.H) * a.T + (size_t)n1 * C + j) * a.H + (bh1 % a.H);
-      const bf16* base = tsel == 0 ? qg : tsel == 1 ? kg : tsel == 2 ? vg : gg;
-      if (tsel < 3 || PC) prefetch_l2(base + r1 * BD, BD * 2);  // (v: for its TMA load)
     }
     // (a) P1 of this chunk: Y^T = dU^T T
     if (cur && tid == 0) {
@@ -409,7 +413,7 @@ __global__ void __launch_bounds__(BT_THREADS, 1)
       epi_sync();
       {
         float suffix = ((colp_s[c] + colp_s[BD + c]) + (colp_s[2 * BD + c] + colp_s[3 * BD + c])) +
-                       ((dgam_s[c] + dgam_s[BD + c]) + (dgam_s[2 * BD + c] + dgam_s[3 * BD + c])) * __expf(GC);
+                       dgam_s[c] * __expf(GC);
         for (int g2 = NTG - 1; g2 > tg; --g2) suffix += ctot_s[g2 * BD + c];
 #pragma unroll
         for (int i = 0; i < TPT; ++i) dGr[i] += suffix;
@@ -521,13 +525,26 @@ __global__ void __launch_bounds__(BT_THREADS, 1)
       gx_s[tg * BD + c] = s;
     }
     mbar_wait(fullB, par, a.err);
-    {
+    {  // dgam_c = sum_v dS1[c][v] S0[c][v]: warp w takes channels 8 w .. + 7 (one 16-byte
+       // piece of a row of S0^T and dS1^T), lane l rows l + 32 i; then a warp sum
       typedef Sw<bf16, BD, BD> SL;
-      float acc = 0.f;
-#pragma unroll 8
-      for (int v = 2 * TPT * tg; v < 2 * TPT * tg + 2 * TPT; ++v)
-        acc = fmaf(__bfloat162float(DS1T[SL::off(v, c)]), __bfloat162float(S0T[SL::off(v, c)]), acc);
-      dgam_s[tg * BD + c] = acc;
+      float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int i = 0; i < BD / 32; ++i) {
+        const int off = SL::off(lane + 32 * i, 8 * warp);
+        const uint4 s4 = *reinterpret_cast<const uint4*>(S0T + off);
+        const uint4 d4 = *reinterpret_cast<const uint4*>(DS1T + off);
+        const uint32_t sw[4] = {s4.x, s4.y, s4.z, s4.w}, dw[4] = {d4.x, d4.y, d4.z, d4.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float2 sf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&sw[e]));
+          const float2 df = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&dw[e]));
+          acc[2 * e] = fmaf(df.x, sf.x, acc[2 * e]);
+          acc[2 * e + 1] = fmaf(df.y, sf.y, acc[2 * e + 1]);
+        }
+      }
+      const float tot = warp_sum8(acc, lane);
+      if ((lane & 3) == 0) dgam_s[8 * warp + (lane >> 2)] = tot;
     }
     if (tid == 0) {
       flags_s[0] = 0;
