@@ -84,11 +84,13 @@ struct BtLayout {
   static constexpr int CTOT = GX;                  // [NTG][Dk] token-group totals of dG (final
                                                    // epilogue only; GX is read before it)
   static constexpr int FLAGS = DGAM + NTG * BD * 4;  // int [4]: unsafe1, unsafe2
-  static constexpr int BAR = FLAGS + 16;           // 7 mbarriers
-  static constexpr int TSLOT = BAR + 7 * 8;
+  static constexpr int BAR = FLAGS + 16;           // 8 mbarriers
+  static constexpr int TSLOT = BAR + 8 * 8;
   static constexpr int BYTES = TSLOT + 16;
   static constexpr uint32_t TXA = (uint32_t)(C * C * 2 + BD * C * 2 + C * BD * 2);
   static constexpr uint32_t TXB = (uint32_t)(C * BD * 2 + BD * C * 2 + 2 * BD * BD * 2);
+  static constexpr uint32_t TXQ = (uint32_t)(2 * C * BD * 2);  // q, k into X
+  static constexpr uint32_t TXG = (uint32_t)(C * BD * 2);      // per-channel g into YE
 };
 static_assert(BtLayout::BYTES + 1024 <= 227 * 1024, "shared memory of one CTA");
 static_assert(BtLayout::CTOT + NTG * BD * 4 <= BtLayout::COLP, "the dG totals fit in the G totals' place");
@@ -175,7 +177,8 @@ __device__ __noinline__ float3 pairwise_terms(const bf16* dpt, const float* Gf, 
 template <bool PC>
 __global__ void __launch_bounds__(BT_THREADS, 1)
     chunk_bwd_tc_kernel(ChunkBwdArgs a, const __grid_constant__ CUtensorMap dout_map,
-                        const __grid_constant__ CUtensorMap v_map) {
+                        const __grid_constant__ CUtensorMap v_map, const __grid_constant__ CUtensorMap q_map,
+                        const __grid_constant__ CUtensorMap k_map, const __grid_constant__ CUtensorMap g_map) {
   pdl_wait();
   pdl_trigger();
   typedef BtLayout L;
@@ -192,6 +195,7 @@ __global__ void __launch_bounds__(BT_THREADS, 1)
   uint64_t* bP34 = bars + 4;
   uint64_t* bP56 = bars + 5;
   uint64_t* bDrain = bars + 6;
+  uint64_t* fullQ = bars + 7;
   uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + L::TSLOT);
   float* beta_s = reinterpret_cast<float*>(sm + L::BETA);
   float* gsc = reinterpret_cast<float*>(sm + L::GSC);
@@ -213,6 +217,7 @@ __global__ void __launch_bounds__(BT_THREADS, 1)
     mbar_init(bP34, 1);
     mbar_init(bP56, 1);
     mbar_init(bDrain, 1);
+    mbar_init(fullQ, 1);
     fence_mbar_init();
   }
   if (warp == 0) {
@@ -254,9 +259,23 @@ __global__ void __launch_bounds__(BT_THREADS, 1)
     bulk_g2s(sm + L::S0T, static_cast<const bf16*>(a.res.state) + ch * (BD * BD), BD * BD * 2, fullB);
     bulk_g2s(sm + L::DS1T, static_cast<const bf16*>(a.ws.dstate) + ch * (BD * BD), BD * BD * 2, fullB);
   };
+  // group Q: q and k into the rows of X (the operand build rewrites them in place) and
+  // per-channel g (row-major) into YE, once P5 and P6 of the previous chunk have read them
+  auto load_q = [&](int m) {
+    int n, bh;
+    unit_of(m, n, bh);
+    mbar_arrive_expect_tx(fullQ, L::TXQ + (PC ? L::TXG : 0u));
+    const int b = bh / a.H, h = bh % a.H, tok = b * a.T + n * C;
+    tma_load_3d(sm + L::X, &q_map, 0, h, tok, fullQ);                           // q, columns 0-63
+    tma_load_3d(sm + L::X + 2 * C * 128, &q_map, 64, h, tok, fullQ);            // columns 64-127
+    tma_load_3d(sm + L::X + C * 128, &k_map, 0, h, tok, fullQ);                 // k, rows C..
+    tma_load_3d(sm + L::X + 2 * C * 128 + C * 128, &k_map, 64, h, tok, fullQ);
+    if (PC) tma_load_3d(sm + L::YE, &g_map, 0, h, tok, fullQ);
+  };
   if (tid == 0 && nunits > 0) {
     load_a(0);
     load_b(0);
+    load_q(0);
   }
 
   // ---- all 16 warps. Lane quarter qw = warp % 4 (TMEM lanes 32 qw .. + 31, a value
@@ -301,6 +320,7 @@ __global__ void __launch_bounds__(BT_THREADS, 1)
     const uint32_t par = (uint32_t)m & 1u;
     int n = 0, bh = 0;
     if (cur) unit_of(m, n, bh);
+    bool q_early = true;  // this chunk's group Q loads were issued at the start of (b)
     // this chunk's beta, read while the previous chunk's final epilogue runs
     float beta_pre = 0.f;
     if (cur && tid < C) {
@@ -330,6 +350,8 @@ __global__ void __launch_bounds__(BT_THREADS, 1)
       const int bs = BLK * blk;
       const bool unsafe1 = flags_s[0] != 0, unsafe2 = flags_s[1] != 0;
       const bool fast = !mask_form && !(unsafe1 || unsafe2);
+      q_early = mask_form || fast;  // X is not borrowed for G below
+      if (tid == 0 && cur && q_early) load_q(m);
       const bool blk1 = blk == 0;
       const bool pw_rows = !mask_form && !fast && (blk1 ? unsafe1 : unsafe2);
       const bool skip_x = pw_rows && blk1, skip_y = pw_rows && !blk1;
@@ -441,6 +463,11 @@ __global__ void __launch_bounds__(BT_THREADS, 1)
       }
     }
     if (!cur) break;
+    if (!q_early) {  // G of the previous chunk has left X (read by the pairwise sums)
+      fence_proxy_async();
+      epi_sync();
+      if (tid == 0) load_q(m);
+    }
     const int b = bh / a.H, h = bh % a.H;
     const size_t row0 = ((size_t)b * a.T + (size_t)n * C) * a.H + h;
     cur_n = n;
@@ -502,20 +529,21 @@ __global__ void __launch_bounds__(BT_THREADS, 1)
     // (e) dgam partials, G, the score operands. Thread: channel c = rowl, tokens
     // t_beg .. + TPT - 1 (value rows 2 TPT tg .. for dgam).
     const int c = rowl;
-    float qb[TPT], kb[TPT];  // the build's q and k, loaded ahead of the work in between
+    const bf16* graw = reinterpret_cast<const bf16*>(sm + L::YE);  // per-channel g [C][Dk]
+    float gl[TPT];
+    if (!PC) {
+#pragma unroll
+      for (int i = 0; i < TPT; ++i) gl[i] = ldg_bf16(gg + row0 + (size_t)(t_beg + i) * rs);
+    }
+    mbar_wait(fullQ, par, a.err);
+    float qb[TPT], kb[TPT];  // the build's q and k (X is rewritten in place below)
 #pragma unroll
     for (int i = 0; i < TPT; ++i) {
-      const size_t gi = (row0 + (size_t)(t_beg + i) * rs) * BD + c;
-      qb[i] = ldg_bf16(qg + gi);
-      kb[i] = ldg_bf16(kg + gi);
+      qb[i] = __bfloat162float(Xt.at(t_beg + i, c));
+      kb[i] = __bfloat162float(Xt.at(C + t_beg + i, c));
+      if (PC) gl[i] = __bfloat162float(graw[(t_beg + i) * BD + c]);
     }
     {  // this group's part of the inclusive cumulative log-decay of channel c
-      float gl[TPT];
-#pragma unroll
-      for (int i = 0; i < TPT; ++i) {
-        const size_t r = row0 + (size_t)(t_beg + i) * rs;
-        gl[i] = PC ? ldg_bf16(gg + r * BD + c) : ldg_bf16(gg + r);
-      }
       float s = 0.f;
 #pragma unroll
       for (int i = 0; i < TPT; ++i) {
@@ -665,8 +693,15 @@ __global__ void __launch_bounds__(BT_THREADS, 1)
       umma_commit(bP56);
     }
   }
-  // every MMA this CTA issued has completed before TMEM is freed
+  // every MMA and load this CTA issued has completed before TMEM is freed and the CTA
+  // retires (in normal operation all were waited for; after a failed wait maybe not)
   if (tid == 0) {
+    if (nunits > 0) {
+      const uint32_t lp = (uint32_t)(nunits - 1) & 1u;
+      mbar_drain(fullA, lp);
+      mbar_drain(fullB, lp);
+      mbar_drain(fullQ, lp);
+    }
     umma_commit(bDrain);
     mbar_drain(bDrain, 0u);
   }
@@ -681,6 +716,7 @@ __global__ void __launch_bounds__(BT_THREADS, 1)
 bool bwd_tc_applies(int DK, int DV) { return DK == BD && DV == BD; }
 
 cudaError_t launch_chunk_bwd_tc(const ChunkBwdArgs& a, cudaStream_t s) {
+  if ((long long)a.B * a.T > 0x7fffffffLL) return cudaErrorInvalidValue;  // TMA token coordinate
   auto encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(tensor_map_encode_fn());
   if (!encode) return cudaErrorNotSupported;
   CUtensorMap map;
@@ -688,14 +724,22 @@ cudaError_t launch_chunk_bwd_tc(const ChunkBwdArgs& a, cudaStream_t s) {
   const cuuint64_t strides[2] = {(cuuint64_t)BD * 2, (cuuint64_t)a.H * BD * 2};
   const cuuint32_t box[3] = {64, 1, (cuuint32_t)C};
   const cuuint32_t estr[3] = {1, 1, 1};
-  CUtensorMap vmap;  // v [B*T][H][Dv], same geometry as dout
-  if (encode(&map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(a.dout), dims, strides, box, estr,
-             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
-             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS ||
-      encode(&vmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(a.v), dims, strides, box, estr,
-             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
-             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+  const cuuint32_t gbox[3] = {BD, 1, (cuuint32_t)C};  // per-channel g: whole rows, row-major
+  // dout, v, q, k [B*T][H][128] (same geometry), g [B*T][H][Dk] when per channel
+  CUtensorMap vmap, qmap, kmap, gmap;
+  auto enc = [&](CUtensorMap* m, const void* p, const cuuint32_t* bx, CUtensorMapSwizzle sw) {
+    return encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(p), dims, strides, bx, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  };
+  if (!enc(&map, a.dout, box, CU_TENSOR_MAP_SWIZZLE_128B) || !enc(&vmap, a.v, box, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !enc(&qmap, a.q, box, CU_TENSOR_MAP_SWIZZLE_128B) || !enc(&kmap, a.k, box, CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;
+  if (a.per_channel) {
+    if (!enc(&gmap, a.g, gbox, CU_TENSOR_MAP_SWIZZLE_NONE)) return cudaErrorInvalidValue;
+  } else {
+    gmap = qmap;  // not read: one decay per token arrives by plain loads
+  }
   const int bytes = BtLayout::BYTES + 1024;
   auto kern = a.per_channel ? chunk_bwd_tc_kernel<true> : chunk_bwd_tc_kernel<false>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
@@ -707,7 +751,7 @@ cudaError_t launch_chunk_bwd_tc(const ChunkBwdArgs& a, cudaStream_t s) {
   const int grid = units < nsm ? units : nsm;
   if (grid == 0) return cudaSuccess;
   prof_mark(K_BWD_TC, s, true);
-  e = launch_pdl(kern, dim3(grid), dim3(BT_THREADS), bytes, s, a, map, vmap);
+  e = launch_pdl(kern, dim3(grid), dim3(BT_THREADS), bytes, s, a, map, vmap, qmap, kmap, gmap);
   prof_mark(K_BWD_TC, s, false);
   return e;
 }
