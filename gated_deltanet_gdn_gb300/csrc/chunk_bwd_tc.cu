@@ -68,8 +68,8 @@ struct BtLayout {
   static constexpr int S0T = UT + BD * C * 2;      // S0^T [Dv][Dk]
   static constexpr int DS1T = S0T + BD * BD * 2;   // dS1^T [Dv][Dk]
   // operands built per chunk
-  static constexpr int X = DS1T + BD * BD * 2;     // [Xq ; Xk] [2C][Dk]
-  static constexpr int YE = X + 2 * C * BD * 2;    // Ye [C][Dk]
+  static constexpr int X = DS1T + BD * BD * 2;     // [Xq | Xk]^T [Dk][2C] (q ; k land here first)
+  static constexpr int YE = X + 2 * C * BD * 2;    // Ye^T [Dk][C] (per-channel g lands here first)
   static constexpr int DP = YE + C * BD * 2;       // [dAqk ; dAkk] [2C][C]
   // small arrays (fp32)
   static constexpr int BETA = DP + 2 * C * C * 2;  // [C]
@@ -106,6 +106,9 @@ __device__ __forceinline__ float ldg_bf16(const bf16* p) {
 __device__ __forceinline__ uint32_t pack2_bf16(float x, float y) {
   __nv_bfloat162 h = __floats2bfloat162_rn(x, y);
   return *reinterpret_cast<uint32_t*>(&h);
+}
+__device__ __forceinline__ uint4 pack8_bf16(const float* x) {
+  return make_uint4(pack2_bf16(x[0], x[1]), pack2_bf16(x[2], x[3]), pack2_bf16(x[4], x[5]), pack2_bf16(x[6], x[7]));
 }
 
 // Sums over the 32 lanes of a warp of TPT = 16 values per lane at once (recursive
@@ -294,8 +297,9 @@ __global__ void __launch_bounds__(BT_THREADS, 1)
   const bf16* bg = static_cast<const bf16*>(a.beta);
   const size_t rs = (size_t)a.H;  // token stride in rows
   Tile<bf16, 2 * C, BD> DYt{reinterpret_cast<bf16*>(sm + L::DY)};
-  Tile<bf16, 2 * C, BD> Xt{reinterpret_cast<bf16*>(sm + L::X)};
-  Tile<bf16, C, BD> Yet{reinterpret_cast<bf16*>(sm + L::YE)};
+  Tile<bf16, 2 * C, BD> Xt{reinterpret_cast<bf16*>(sm + L::X)};      // q ; k as loaded
+  Tile<bf16, BD, 2 * C> XTt{reinterpret_cast<bf16*>(sm + L::X)};     // [Xq | Xk]^T, built in their place
+  Tile<bf16, BD, C> YeTt{reinterpret_cast<bf16*>(sm + L::YE)};       // Ye^T
   Tile<bf16, 2 * C, C> DPt{reinterpret_cast<bf16*>(sm + L::DP)};
   const bf16* S0T = reinterpret_cast<const bf16*>(sm + L::S0T);
   const bf16* DS1T = reinterpret_cast<const bf16*>(sm + L::DS1T);
@@ -305,8 +309,8 @@ __global__ void __launch_bounds__(BT_THREADS, 1)
   constexpr uint32_t id_p2 = umma_idesc_bf16(128, C, false, true);     // DY (K-major) x U^T (MN-major)
   constexpr uint32_t id_p3 = umma_idesc_bf16(128, 2 * C, true, false); // S0 (MN-major) x DY^T (K-major)
   constexpr uint32_t id_p4 = umma_idesc_bf16(128, C, true, true);      // dS1 (MN-major) x U^T (MN-major)
-  constexpr uint32_t id_p5 = umma_idesc_bf16(128, 2 * C, true, false); // Ye^T (MN-major) x DP^T (K-major)
-  constexpr uint32_t id_p6 = umma_idesc_bf16(128, C, true, true);      // X^T (MN-major) x DP (MN-major)
+  constexpr uint32_t id_p5 = umma_idesc_bf16(128, 2 * C, false, false); // Ye^T (K-major) x DP^T (K-major)
+  constexpr uint32_t id_p6 = umma_idesc_bf16(128, C, false, true);      // X^T (K-major) x DP (MN-major)
 
   // per-thread values that live from the operand build to the final epilogue: G of this
   // thread's channel over its TPT tokens, and G at the block boundary and the last token
@@ -650,15 +654,23 @@ __global__ void __launch_bounds__(BT_THREADS, 1)
       const bool unsafe1 = flags_s[0] != 0, unsafe2 = flags_s[1] != 0;
       const bool dead_x = !mask_form && blk == 0 && unsafe1;
       const bool dead_y = !mask_form && blk == 1 && unsafe2;
+      // row c of X^T and Ye^T: this thread's tokens in 16-byte pieces of eight
 #pragma unroll
-      for (int i = 0; i < TPT; ++i) {
-        const int t = t_beg + i;
-        const float d = Greg[i] - Gb;
-        const float e1 = mask_form ? 1.f : dead_x ? 0.f : __expf(d);
-        const float e2 = mask_form ? 1.f : dead_y ? 0.f : __expf(-d);
-        Xt.at(t, c) = __float2bfloat16_rn(qb[i] * e1);
-        Xt.at(C + t, c) = __float2bfloat16_rn(beta_s[t] * kb[i] * e1);
-        Yet.at(t, c) = __float2bfloat16_rn(kb[i] * e2);
+      for (int h8 = 0; h8 < TPT / 8; ++h8) {
+        float xq[8], xk[8], ye[8];
+#pragma unroll
+        for (int ii = 0; ii < 8; ++ii) {
+          const int i = 8 * h8 + ii, t = t_beg + i;
+          const float d = Greg[i] - Gb;
+          const float e1 = mask_form ? 1.f : dead_x ? 0.f : __expf(d);
+          const float e2 = mask_form ? 1.f : dead_y ? 0.f : __expf(-d);
+          xq[ii] = qb[i] * e1;
+          xk[ii] = beta_s[t] * kb[i] * e1;
+          ye[ii] = kb[i] * e2;
+        }
+        *reinterpret_cast<uint4*>(XTt.ptr(c, t_beg + 8 * h8)) = pack8_bf16(xq);
+        *reinterpret_cast<uint4*>(XTt.ptr(c, C + t_beg + 8 * h8)) = pack8_bf16(xk);
+        *reinterpret_cast<uint4*>(YeTt.ptr(c, t_beg + 8 * h8)) = pack8_bf16(ye);
       }
       uint32_t qk[TPT];  // q and k of this channel and token group for the final epilogue
 #pragma unroll
@@ -679,16 +691,16 @@ __global__ void __launch_bounds__(BT_THREADS, 1)
     if (tid == 0) {
       tc_fence_after();
       {  // P5: D5 = Ye^T DP^T (M = Dk, N = 2C, K = C)
-        const uint64_t dA = desc_mnmajor(sm + L::YE, C * 128), dB = desc_kmajor(sm + L::DP);
+        const uint64_t dA = desc_kmajor(sm + L::YE), dB = desc_kmajor(sm + L::DP);
 #pragma unroll
         for (int ks = 0; ks < C / 16; ++ks)
-          umma_bf16(tm + TC_D5, kstep_mnmajor(dA, ks), kstep_kmajor(dB, ks, 2 * C * 128), id_p5, ks > 0);
+          umma_bf16(tm + TC_D5, kstep_kmajor(dA, ks, BD * 128), kstep_kmajor(dB, ks, 2 * C * 128), id_p5, ks > 0);
       }
       {  // P6: D6 = X^T DP (M = Dk, N = C, K = 2C)
-        const uint64_t dA = desc_mnmajor(sm + L::X, 2 * C * 128), dB = desc_mnmajor(sm + L::DP, 2 * C * 128);
+        const uint64_t dA = desc_kmajor(sm + L::X), dB = desc_mnmajor(sm + L::DP, 2 * C * 128);
 #pragma unroll
         for (int ks = 0; ks < 2 * C / 16; ++ks)
-          umma_bf16(tm + TC_D6, kstep_mnmajor(dA, ks), kstep_mnmajor(dB, ks), id_p6, ks > 0);
+          umma_bf16(tm + TC_D6, kstep_kmajor(dA, ks, BD * 128), kstep_mnmajor(dB, ks), id_p6, ks > 0);
       }
       umma_commit(bP56);
     }
