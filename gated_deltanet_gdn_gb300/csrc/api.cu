@@ -96,6 +96,7 @@ ResidualPtrs residual_ptrs(const gdn_dims* d, void* base) {
   r.gam = reinterpret_cast<float*>(b + L.gam);
   r.state = b + L.state;
   r.u = b + L.u;
+  r.progress = reinterpret_cast<unsigned*>(b + L.progress);
   if (qk_norm(d)) {
     r.qn = b + L.qn;
     r.kn = b + L.kn;

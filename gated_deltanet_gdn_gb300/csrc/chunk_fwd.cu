@@ -26,6 +26,7 @@
 //   chunk_scan_fwd_kernel  grid (Dv/64, B*H), 256 threads: A6, fp32 state slice in
 //                          registers; chunk records arrive by cp.async.bulk on mbarriers
 //   chunk_out_kernel       grid (chunks, B*H), 256 threads: outputs from stored states
+#include "chunk_out.cuh"
 #include "chunk_prep.cuh"
 #include "common.cuh"
 #include "kernels.h"
@@ -523,68 +524,14 @@ __global__ void __launch_bounds__(SCAN_THREADS) chunk_scan_fwd_kernel(ChunkFwdAr
 }
 
 // ------------------------------------------------------------------ outputs
-// O = (scale Q-hat) S0 + (scale Aqk) U per chunk, from the scan's chunk-start states and U.
-constexpr int OUT_THREADS = 256;
-
-template <class T, int DK, int DV>
-struct OutLayout {
-  static constexpr int ES = (int)sizeof(T);
-  static constexpr int QH = 0;                         // [C][DK]
-  static constexpr int AQ = a1k(QH + C * DK * ES);     // [C][C]
-  static constexpr int S0 = a1k(AQ + C * C * ES);      // S0^T [DV][DK]
-  static constexpr int U = a1k(S0 + DK * DV * ES);     // U^T [DV][C], then the output tile
-  static constexpr int BYTES = a1k(U + C * DV * ES);
-};
-
+// O = (scale Q-hat) S0 + (scale Aqk) U per chunk, from the scan's chunk-start states and U
+// (out_unit, chunk_out.cuh).
 template <class T, int DK, int DV>
 __global__ void __launch_bounds__(OUT_THREADS) chunk_out_kernel(ChunkFwdArgs a) {
   pdl_wait();
   pdl_trigger();
-  typedef OutLayout<T, DK, DV> L;
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* sm = align1024(smem_raw);
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int n = blockIdx.x, bh = blockIdx.y, b = bh / a.H, h = bh % a.H;
-  const int N = a.T / C;
-  const size_t ch = (size_t)bh * N + n;
-  constexpr int EPC = 16 / (int)sizeof(T);
-  Tile<T, C, DK> Qs{reinterpret_cast<T*>(sm + L::QH)};
-  Tile<T, C, C> As{reinterpret_cast<T*>(sm + L::AQ)};
-  Tile<T, DV, DK> S0s{reinterpret_cast<T*>(sm + L::S0)};
-  Tile<T, DV, C> Us{reinterpret_cast<T*>(sm + L::U)};
-  {
-    const T* s1 = static_cast<const T*>(a.res.qh) + ch * (C * DK);
-    for (int i = tid; i < C * DK / EPC; i += OUT_THREADS) cp_async16(Qs.p + i * EPC, s1 + i * EPC);
-    const T* s2 = static_cast<const T*>(a.res.aqk) + ch * (C * C);
-    for (int i = tid; i < C * C / EPC; i += OUT_THREADS) cp_async16(As.p + i * EPC, s2 + i * EPC);
-    const T* s3 = static_cast<const T*>(a.res.state) + ch * (DK * DV);
-    for (int i = tid; i < DK * DV / EPC; i += OUT_THREADS) cp_async16(S0s.p + i * EPC, s3 + i * EPC);
-    const T* s4 = static_cast<const T*>(a.res.u) + ch * (C * DV);
-    for (int i = tid; i < C * DV / EPC; i += OUT_THREADS) cp_async16(Us.p + i * EPC, s4 + i * EPC);
-  }
-  cp_async_commit();
-  cp_async_wait<0>();
-  __syncthreads();
-  const int m0 = 16 * (warp & 3), n0 = (warp >> 2) * (DV / 2);
-  constexpr int NW = DV / 16;
-  float o[1][NW][4];
-  zero(o);
-  Gemm<T>::template runk<1, NW, 0, DK>(o, aview<false>(Qs), bview<false>(S0s), m0, n0, lane);
-  Gemm<T>::template runk<1, NW, 0, C>(o, aview<false>(As), bview<false>(Us), m0, n0, lane);
-  __syncthreads();  // U consumed: stage the output tile in its place
-  Tile<T, C, DV> Os{reinterpret_cast<T*>(sm + L::U)};
-#pragma unroll
-  for (int nt = 0; nt < NW; ++nt)
-#pragma unroll
-    for (int e = 0; e < 4; ++e)
-      Os.at(m0 + frag_row(lane, e), n0 + 8 * nt + frag_col(lane, e)) = from_f32<T>(o[0][nt][e]);
-  __syncthreads();
-  T* out = static_cast<T*>(a.out);
-  const size_t row0 = ((size_t)b * a.T + (size_t)n * C) * a.H + h;
-  for (int i = tid; i < C * DV / EPC; i += OUT_THREADS) {
-    const int r = i / (DV / EPC), c0 = (i % (DV / EPC)) * EPC;
-    copy16(out + (row0 + (size_t)r * a.H) * DV + c0, Os.ptr(r, c0));
-  }
+  out_unit<T, DK, DV>(a, blockIdx.x, blockIdx.y, align1024(smem_raw), threadIdx.x);
 }
 
 template <class T, int DK, int DV>
@@ -604,8 +551,9 @@ cudaError_t launch_fwd_t(const ChunkFwdArgs& a, cudaStream_t s) {
       prof_mark(K_PREP, s, false);
     }
   }
+  bool outputs_done = false;
   if (scan_tc_applies(a.bf16, DK, DV)) {
-    if ((e = launch_scan_fwd_tc(a, s)) != cudaSuccess) return e;
+    if ((e = launch_scan_fwd_tc(a, s, &outputs_done)) != cudaSuccess) return e;
   } else {
     const int bytes = ScanLayout<T, DK>::BYTES + 1024;
     auto kern = chunk_scan_fwd_kernel<T, DK, DV>;
@@ -616,7 +564,7 @@ cudaError_t launch_fwd_t(const ChunkFwdArgs& a, cudaStream_t s) {
     prof_mark(K_SCAN_FWD, s, false);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
-  if (N > 0) {
+  if (N > 0 && !outputs_done) {
     const int bytes = OutLayout<T, DK, DV>::BYTES + 1024;
     auto kern = chunk_out_kernel<T, DK, DV>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);

@@ -136,6 +136,10 @@ __global__ void __launch_bounds__(PTC_THREADS, 2)
     mbar_init(bar_v, 1);
     fence_mbar_init();
   }
+  // the forward scan's per-(batch, head) chunk counters start at zero (read only after
+  // this kernel has completed)
+  if (blockIdx.x == 0 && a.res.progress)
+    for (int i = tid; i < a.B * a.H; i += PTC_THREADS) a.res.progress[i * PROGRESS_STRIDE] = 0u;
   if (warp == 0) {
     tmem_alloc(tslot, PTC_TMEM_COLS);
     tmem_relinquish();

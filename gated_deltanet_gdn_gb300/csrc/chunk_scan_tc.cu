@@ -26,6 +26,7 @@
 
 #include <mutex>
 
+#include "chunk_out.cuh"
 #include "common.cuh"
 #include "kernels.h"
 #include "umma.cuh"
@@ -36,6 +37,7 @@ namespace {
 constexpr int TD = 128;                 // Dk = Dv
 constexpr int COMPUTE_THREADS = 256;    // warps 0-7
 constexpr int TC_THREADS = COMPUTE_THREADS + 32;  // + the producer warp
+constexpr int FWD_THREADS = TC_THREADS + 32;      // forward: + the publisher warp
 constexpr uint32_t TMEM_COLS = 256;     // S^T or dS^T: columns 0..127; U^T or dU^T: 128..191
 constexpr int PANEL_C = C * 128;        // bytes of one 64-column panel of a [C][*] bf16 tile
 constexpr int PANEL_D = TD * 128;       // bytes of one 64-column panel of a [Dv][*] bf16 tile
@@ -145,11 +147,18 @@ struct TcFwdLayout {
   static constexpr int UA = SA + 2 * TD * TD * 2;  // U^T bf16 [Dv][C], two buffers
   static constexpr int BAR = UA + 2 * TD * C * 2;  // full[STAGES], empty[STAGES], u, s, drain
   static constexpr int TSLOT = BAR + 8 * (2 * STAGES + 3);
-  static constexpr int BYTES = TSLOT + 16;
+  static constexpr int BYTES = TSLOT + 16;  // TMEM address, then the publication counter
   static constexpr uint32_t TX = (uint32_t)(3 * C * TD * 2 + TD * 4);
 };
 
-__global__ void __launch_bounds__(TC_THREADS, 1) chunk_scan_fwd_tc_kernel(ChunkFwdArgs a) {
+// with_out: the grid is cooperative and CTAs B*H.. are output CTAs. Each takes chunk-heads
+// (n, bh) in chunk-major order; its warp 8 waits until the scan CTA of bh has published
+// that its records of chunk n are stored (a.res.progress[bh] > n) and bulk-loads that
+// chunk's four records into one of two stages, while warps 0-7 form the outputs of the
+// chunk in the other (out_compute_store). The scan CTAs publish after the bulk copies of a
+// chunk's state and U records have completed. Output CTAs only wait on scan CTAs, never
+// the other way round.
+__global__ void __launch_bounds__(FWD_THREADS, 1) chunk_scan_fwd_tc_kernel(ChunkFwdArgs a, int with_out) {
   pdl_wait();  // no early trigger: one wave for the whole scan, successors must not park beside it
   typedef TcFwdLayout L;
   extern __shared__ uint8_t smem_raw[];
@@ -157,6 +166,51 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_scan_fwd_tc_kernel(ChunkF
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int bh = blockIdx.x;
   const int N = a.T / C;
+  const int BH = a.B * a.H;
+  if (bh >= BH) {  // ---- output CTA: warp 8 loads, warps 0-7 compute (two stages)
+    typedef OutLayout<bf16, TD, TD> OL;
+    constexpr int OSTAGE = a1k(OL::BYTES);
+    uint64_t* ofull = reinterpret_cast<uint64_t*>(sm + 2 * OSTAGE);
+    uint64_t* oempty = ofull + 2;
+    const int units = N * BH, ncons = (int)gridDim.x - BH;
+    const int first = bh - BH;
+    const int count = first < units ? (units - first + ncons - 1) / ncons : 0;
+    if (tid == 0) {
+      for (int s2 = 0; s2 < 2; ++s2) {
+        mbar_init(&ofull[s2], 1);
+        mbar_init(&oempty[s2], 1);
+      }
+      fence_mbar_init();
+    }
+    __syncthreads();
+    if (warp == COMPUTE_THREADS / 32 + 1) return;  // (no publisher in an output CTA)
+    if (warp == COMPUTE_THREADS / 32) {
+      if (lane == 0) {
+        for (int k = 0; k < count; ++k) {
+          const int u = first + k * ncons, n = u / BH, ob = u % BH, s2 = k & 1;
+          if (k >= 2) mbar_wait(&oempty[s2], (uint32_t)((k - 2) >> 1) & 1u, a.err);
+          wait_counter(a.res.progress + (size_t)ob * PROGRESS_STRIDE, (unsigned)(n + 1), a.err);
+          fence_proxy_async_global();
+          const size_t ch = (size_t)ob * N + n;
+          uint8_t* st = sm + s2 * OSTAGE;
+          mbar_arrive_expect_tx(&ofull[s2], (uint32_t)(2 * C * TD * 2 + C * C * 2 + TD * TD * 2));
+          bulk_g2s(st + OL::QH, static_cast<const bf16*>(a.res.qh) + ch * (C * TD), C * TD * 2, &ofull[s2]);
+          bulk_g2s(st + OL::AQ, static_cast<const bf16*>(a.res.aqk) + ch * (C * C), C * C * 2, &ofull[s2]);
+          bulk_g2s(st + OL::S0, static_cast<const bf16*>(a.res.state) + ch * (TD * TD), TD * TD * 2, &ofull[s2]);
+          bulk_g2s(st + OL::U, static_cast<const bf16*>(a.res.u) + ch * (C * TD), C * TD * 2, &ofull[s2]);
+        }
+        drain_ring(ofull, 2, count);
+      }
+      return;
+    }
+    for (int k = 0; k < count; ++k) {
+      const int u = first + k * ncons, n = u / BH, ob = u % BH, s2 = k & 1;
+      mbar_wait(&ofull[s2], (uint32_t)(k >> 1) & 1u, a.err);
+      out_compute_store<bf16, TD, TD>(a, n, ob, sm + s2 * OSTAGE, tid, [] { compute_sync(); });
+      if (tid == 0) mbar_arrive(&oempty[s2]);
+    }
+    return;
+  }
   uint64_t* full = reinterpret_cast<uint64_t*>(sm + L::BAR);
   uint64_t* empty = full + L::STAGES;
   uint64_t* bar_u = empty + L::STAGES;
@@ -175,6 +229,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_scan_fwd_tc_kernel(ChunkF
     mbar_init(bar_s, 1);
     mbar_init(bar_d, 1);
     fence_mbar_init();
+    *reinterpret_cast<unsigned*>(sm + L::TSLOT + 8) = 0u;  // chunks published
   }
   if (warp == 0) {
     tmem_alloc(tslot, TMEM_COLS);
@@ -185,6 +240,26 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_scan_fwd_tc_kernel(ChunkF
   tc_fence_after();
   const uint32_t tm = *tslot;
 
+  unsigned* pub_s = reinterpret_cast<unsigned*>(sm + L::TSLOT + 8);
+  if (warp == COMPUTE_THREADS / 32 + 1) {  // ---- publisher (output CTAs beside the scan)
+    // Thread 0 sets pub_s to the number of chunks whose state and U records are stored
+    // (after their bulk copies completed); this thread forwards the latest value to the
+    // output CTAs with a GPU-scope release, which so stays off the chunk chain.
+    if (lane == 0 && with_out) {
+      unsigned last = 0;
+      for (uint32_t i = 0; last < (unsigned)N && i < WAIT_MAX_TRIES; ++i) {
+        const unsigned v = ld_acquire_cta(pub_s);
+        if (v > last) {
+          st_release_gpu(a.res.progress + (size_t)bh * PROGRESS_STRIDE, v);
+          last = v;
+        } else {
+          __nanosleep(256);
+        }
+      }
+      if (last < (unsigned)N) atomicOr(a.err, ERR_WAIT_TIMEOUT);
+    }
+    return;
+  }
   if (warp == COMPUTE_THREADS / 32) {  // ---- producer
     if (lane == 0) {
       for (int n = 0; n < N; ++n) {
@@ -250,6 +325,11 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_scan_fwd_tc_kernel(ChunkF
       for (int ks = 0; ks < TD / 16; ++ks)
         umma_bf16(tm + 128, kstep_k(dSa, ks, PANEL_D), kstep_k(dW, ks, PANEL_C), id_1, ks > 0);
       umma_commit_to(bar_u);
+      if (with_out && n > 0) {  // every bulk group but this chunk's state: chunks < n stored
+        bulk_wait1();
+        fence_proxy_async_global();
+        st_release_cta(pub_s, (unsigned)n);
+      }
     }
     // S^T <- S^T diag(gam) while the tensor cores form U^T (the S^T update comes after
     // the next barrier)
@@ -302,6 +382,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_scan_fwd_tc_kernel(ChunkF
   }
   if (tid == 0) {  // record stores and every issued MMA complete before TMEM is freed
     bulk_wait0();
+    if (with_out) {
+      fence_proxy_async_global();
+      st_release_cta(pub_s, (unsigned)N);
+    }
     drain_mma(bar_d);
   }
   tc_fence_before();
@@ -514,13 +598,37 @@ void* tensor_map_encode_fn() {
 
 bool scan_tc_applies(int bf16_operands, int DK, int DV) { return bf16_operands && DK == TD && DV == TD; }
 
-cudaError_t launch_scan_fwd_tc(const ChunkFwdArgs& a, cudaStream_t s) {
-  const int bytes = TcFwdLayout::BYTES + 1024;
+cudaError_t launch_scan_fwd_tc(const ChunkFwdArgs& a, cudaStream_t s, bool* outputs_done) {
+  *outputs_done = false;
+  constexpr int OB = 2 * a1k(OutLayout<bf16, TD, TD>::BYTES) + 4 * 8;  // two output stages + barriers
+  const int bytes = (TcFwdLayout::BYTES > OB ? TcFwdLayout::BYTES : OB) + 1024;
   cudaError_t e = cudaFuncSetAttribute(chunk_scan_fwd_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
   if (e != cudaSuccess) return e;
+  int dev = 0, nsm = 0, coop = 0;
+  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+  if ((e = cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+  if ((e = cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev)) != cudaSuccess) return e;
+  const int BH = a.B * a.H;
+  // outputs beside the scan when SMs are left over: one cooperative grid of one CTA per SM
+  // (the kernel's shared memory admits one), so every output CTA's wait has its scan CTA
+  // resident
+  const bool with_out = a.res.progress && coop && BH < nsm && a.T / C > 0;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(with_out ? nsm : BH);
+  cfg.blockDim = dim3(FWD_THREADS);
+  cfg.dynamicSmemBytes = bytes;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeCooperative;
+  attr[1].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = with_out ? 2 : 1;
   prof_mark(K_SCAN_FWD_TC, s, true);
-  e = launch_pdl(chunk_scan_fwd_tc_kernel, dim3(a.B * a.H), dim3(TC_THREADS), bytes, s, a);
+  e = cudaLaunchKernelEx(&cfg, chunk_scan_fwd_tc_kernel, a, (int)with_out);
   prof_mark(K_SCAN_FWD_TC, s, false);
+  if (e == cudaSuccess) *outputs_done = with_out;
   return e;
 }
 

@@ -480,6 +480,46 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, unsign
   return false;
 }
 
+// Counters between CTAs of one grid (the forward scan and the output CTAs beside it):
+// release store / acquire load at GPU scope, and the fence that orders the bulk copies'
+// global writes (async proxy) before the release.
+__device__ __forceinline__ void st_release_gpu(unsigned* p, unsigned v) {
+  asm volatile("st.release.gpu.global.u32 [%0], %1;\n" ::"l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ unsigned ld_acquire_gpu(const unsigned* p) {
+  unsigned v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];\n" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ void st_release_cta(unsigned* p, unsigned v) {
+  asm volatile("st.release.cta.shared.u32 [%0], %1;\n" ::"r"(smem_u32(p)), "r"(v) : "memory");
+}
+__device__ __forceinline__ unsigned ld_acquire_cta(const unsigned* p) {
+  unsigned v;
+  asm volatile("ld.acquire.cta.shared.u32 %0, [%1];\n" : "=r"(v) : "r"(smem_u32(p)) : "memory");
+  return v;
+}
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;\n" ::: "memory");
+}
+// all but the most recently committed bulk group have completed (writes included)
+__device__ __forceinline__ void bulk_wait1() { asm volatile("cp.async.bulk.wait_group 1;\n" ::: "memory"); }
+
+// Bounded wait, by one thread, until *p >= target (a counter another CTA of the same
+// cooperative grid raises with st_release_gpu): same limits and early give-up on the
+// error word as mbar_wait, with a short sleep between polls.
+__device__ __forceinline__ bool wait_counter(const unsigned* p, unsigned target, unsigned* err) {
+  for (uint32_t i = 0; i < WAIT_MAX_TRIES; ++i) {
+    if (ld_acquire_gpu(p) >= target) return true;
+    if (i >= WAIT_BAIL_TRIES && (i & 255u) == 0 && err &&
+        (*reinterpret_cast<volatile unsigned*>(err) & ERR_WAIT_TIMEOUT))
+      return false;
+    __nanosleep(512);
+  }
+  if (err) atomicOr(err, ERR_WAIT_TIMEOUT);
+  return false;
+}
+
 // Bounded wait used only to drain: the completion of copies or tensor-core operations
 // this CTA issued itself, before it frees tensor memory or retires. It does not give up
 // early on the error word (operations already issued complete on their own) and

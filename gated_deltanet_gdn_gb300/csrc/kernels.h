@@ -13,6 +13,9 @@ constexpr int NT = 32;      // value columns per warp column group of the mma.sy
 constexpr int NTS = 64;     // value columns per state-scan CTA (two record slices)
 constexpr float SAFE_SPREAD = 80.f;  // max decay spread (nats) for row-scaled in-block scores
 constexpr int FLAG_PAIRWISE = 1;     // dims.flags bit: in-block scores always pairwise
+// the forward scan's chunk counters, one per (batch, head), each on its own 128-byte line
+// (counter bh at progress[bh * PROGRESS_STRIDE])
+constexpr int PROGRESS_STRIDE = 32;
 
 // Per (batch, head) and chunk, the forward writes these records. Byte sizes of one record
 // for operand element size es; every record starts 1024-byte aligned inside its region.
@@ -22,8 +25,10 @@ constexpr int FLAG_PAIRWISE = 1;     // dims.flags bit: in-block scores always p
 // dS^T [Dv][Dk] and dU^T [Dv][C].
 struct ResidualLayout {
   // region base offsets in bytes from the residual pointer (qn, kn, qinv, kinv: only with
-  // the q/k L2 normalisation, the normalised rows and their inverse norms)
-  size_t aqk, tmat, wneg, up, qh, kt, gam, state, u, qn, kn, qinv, kinv, total;
+  // the q/k L2 normalisation, the normalised rows and their inverse norms; progress: one
+  // counter per (batch, head) through which the tensor-core forward scan tells the output
+  // CTAs beside it how many chunks' records are stored)
+  size_t aqk, tmat, wneg, up, qh, kt, gam, state, u, progress, qn, kn, qinv, kinv, total;
   // bytes of one chunk-head record
   size_t aqk_b, tmat_b, w_b, up_b, qh_b, kt_b, gam_b, state_b, u_b;
 };
@@ -61,6 +66,8 @@ inline ResidualLayout residual_layout(int B, int T, int H, int DK, int DV, int e
   put(L.gam, L.gam_b);
   put(L.state, L.state_b);
   put(L.u, L.u_b);
+  L.progress = off;
+  off = align_up(off + (size_t)B * H * PROGRESS_STRIDE * 4, 1024);
   if (qk_norm) {
     const size_t rows = (size_t)B * T * H;
     L.qn = off;
@@ -121,6 +128,7 @@ struct ResidualPtrs {
   void *aqk, *tmat, *wneg, *up, *qh, *kt;
   float* gam;
   void *state, *u;
+  unsigned* progress;  // [B*H][PROGRESS_STRIDE]: chunks whose state and U records the forward scan has stored
   void *qn, *kn;  // normalised q, k rows (q/k L2 normalisation only)
   float *qinv, *kinv;
 };
@@ -217,7 +225,8 @@ cudaError_t launch_recurrent(const RecurrentArgs& a, cudaStream_t s);
 cudaError_t launch_chunk_grads(const ChunkBwdArgs& a, cudaStream_t s);  // part of launch_chunk_bwd
 // The tensor-core (tcgen05) state scans, used when scan_tc_applies(bf16, Dk, Dv).
 bool scan_tc_applies(int bf16_operands, int DK, int DV);
-cudaError_t launch_scan_fwd_tc(const ChunkFwdArgs& a, cudaStream_t s);
+// outputs_done: the launch also formed every chunk's outputs (output CTAs beside the scan)
+cudaError_t launch_scan_fwd_tc(const ChunkFwdArgs& a, cudaStream_t s, bool* outputs_done);
 cudaError_t launch_scan_bwd_tc(const ChunkBwdArgs& a, cudaStream_t s);
 // The chunk preparation on tcgen05 (chunk_prep_tc.cu), bf16 operands with Dk = Dv = 128.
 bool prep_tc_applies(int bf16_operands, int DK, int DV);

@@ -135,7 +135,11 @@ size_t gdn_chunk_bwd_workspace_bytes(const gdn_dims* dims);
  * Steps: per-chunk cumulative log-decay, boundary-split decay-factorised
  * scores (marin.community note, section Approach), the WY/UT triangular solve
  * (atomic-ops Features: chunk scores -> WY block solve -> recompute ->
- * inter-chunk scan), then the sequential state scan over chunks. */
+ * inter-chunk scan), then the sequential state scan over chunks.
+ * With bf16 operands, Dk = Dv = 128 and fewer (batch, head) pairs than SMs,
+ * the scan and the chunk outputs run as one cooperative launch of one CTA per
+ * SM (output CTAs beside the scan CTAs, synchronised through counters in the
+ * residual buffer); it starts once every CTA can be resident at once. */
 int gdn_chunk_fwd(const gdn_dims* dims, const void* q, const void* k, const void* v,
                   const void* g, const void* beta, const float* h0, float scale, void* out,
                   float* h_final, void* residuals, void* stream);
@@ -169,7 +173,7 @@ int gdn_chunk_bwd(const gdn_dims* dims, const void* q, const void* k, const void
  * are the caller's, exactly as in gdn_chunk_fwd; only the residual records the
  * forward passes between its kernels live in a static device array compiled
  * into the library, GDN_NOALLOC_SCRATCH_BYTES (32 MiB) on every GPU that loads
- * the library, held until the process exits. That fits up to 255 chunk-heads
+ * the library, held until the process exits. That fits up to 254 chunk-heads
  * (B * H * T/64) at Dk = Dv = 128 in bf16 (127 in fp32), e.g. B=1, H=3,
  * T=4096; larger problems return GDN_ERR_SCRATCH_LIMIT, before anything is
  * enqueued, and must use gdn_chunk_fwd.
@@ -182,7 +186,8 @@ int gdn_chunk_bwd(const gdn_dims* dims, const void* q, const void* k, const void
  * call shares the one array: calls whose work overlaps on the GPU (on two
  * streams, or from two threads) race on it and must be serialised by the
  * caller. The array keeps the last call's contents; nothing in it needs to
- * start at zero because each call writes every record before reading it. No
+ * start at zero because each call writes every record (and resets the forward
+ * scan's chunk counters) before reading it. No
  * cudaMalloc, cudaFree or allocating library routine is called. The residual
  * records are not available afterwards, so this call cannot feed
  * gdn_chunk_bwd. Arguments and other errors as gdn_chunk_fwd. */
