@@ -222,7 +222,7 @@ def kernel_work(B, T, H, D, es=2):
 # the files the chunk kernels (the ones profiles/traffic.json covers) are compiled from
 CHUNK_KERNEL_SOURCES = ("chunk_fwd.cu", "chunk_bwd.cu", "chunk_grads.cu", "chunk_scan_tc.cu",
                         "chunk_prep_tc.cu", "chunk_bwd_tc.cu", "chunk_prep.cuh", "chunk_dqa.cuh",
-                        "common.cuh", "umma.cuh", "kernels.h")
+                        "chunk_out.cuh", "common.cuh", "umma.cuh", "kernels.h")
 
 
 def kernel_source_hash():
@@ -350,6 +350,10 @@ def run_gdn(args, world, rank, local):
     gdn.gdn_profile_enable(False)
     total = sum(v[0] for v in prof.values()) or 1.0
     work = kernel_work(w.B, w.T, w.H, w.Dk)
+    if "chunk_scan_fwd_tc_kernel" in prof and "chunk_out_kernel" not in prof:
+        # the forward scan's launch also formed the chunk outputs (output CTAs beside it)
+        work["chunk_scan_fwd_tc_kernel"] = tuple(
+            x + y for x, y in zip(work["chunk_scan_fwd_tc_kernel"], work["chunk_out_kernel"]))
     peaks = load_peaks()
     traffic = load_traffic()
     kernels = {}

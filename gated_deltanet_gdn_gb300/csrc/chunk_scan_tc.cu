@@ -37,12 +37,18 @@ namespace {
 constexpr int TD = 128;                 // Dk = Dv
 constexpr int COMPUTE_THREADS = 256;    // warps 0-7
 constexpr int TC_THREADS = COMPUTE_THREADS + 32;  // + the producer warp
-constexpr int FWD_THREADS = TC_THREADS + 32;      // forward: + the publisher warp
+// the forward: 16 compute warps (four per TMEM lane quarter, each on a quarter of the
+// state's columns), the producer warp and the publisher warp
+constexpr int FWD_COMPUTE = 512;
+constexpr int FWD_PRODUCER = FWD_COMPUTE / 32, FWD_PUBLISHER = FWD_PRODUCER + 1;
+constexpr int FWD_THREADS = FWD_COMPUTE + 64;
 constexpr uint32_t TMEM_COLS = 256;     // S^T or dS^T: columns 0..127; U^T or dU^T: 128..191
 constexpr int PANEL_C = C * 128;        // bytes of one 64-column panel of a [C][*] bf16 tile
 constexpr int PANEL_D = TD * 128;       // bytes of one 64-column panel of a [Dv][*] bf16 tile
 
 __device__ __forceinline__ void compute_sync() { asm volatile("bar.sync 1, 256;\n" ::: "memory"); }
+__device__ __forceinline__ void fwd_sync() { asm volatile("bar.sync 1, 512;\n" ::: "memory"); }
+__device__ __forceinline__ void out_sync() { asm volatile("bar.sync 2, 256;\n" ::: "memory"); }
 
 __device__ __forceinline__ uint32_t pack_bf16(float x, float y) {
   __nv_bfloat162 h = __floats2bfloat162_rn(x, y);
@@ -183,8 +189,8 @@ __global__ void __launch_bounds__(FWD_THREADS, 1) chunk_scan_fwd_tc_kernel(Chunk
       fence_mbar_init();
     }
     __syncthreads();
-    if (warp == COMPUTE_THREADS / 32 + 1) return;  // (no publisher in an output CTA)
-    if (warp == COMPUTE_THREADS / 32) {
+    if (warp >= OUT_THREADS / 32 && warp != FWD_PRODUCER) return;  // warps 0-7 compute, one loads
+    if (warp == FWD_PRODUCER) {
       if (lane == 0) {
         for (int k = 0; k < count; ++k) {
           const int u = first + k * ncons, n = u / BH, ob = u % BH, s2 = k & 1;
@@ -206,7 +212,7 @@ __global__ void __launch_bounds__(FWD_THREADS, 1) chunk_scan_fwd_tc_kernel(Chunk
     for (int k = 0; k < count; ++k) {
       const int u = first + k * ncons, n = u / BH, ob = u % BH, s2 = k & 1;
       mbar_wait(&ofull[s2], (uint32_t)(k >> 1) & 1u, a.err);
-      out_compute_store<bf16, TD, TD>(a, n, ob, sm + s2 * OSTAGE, tid, [] { compute_sync(); });
+      out_compute_store<bf16, TD, TD>(a, n, ob, sm + s2 * OSTAGE, tid, [] { out_sync(); });
       if (tid == 0) mbar_arrive(&oempty[s2]);
     }
     return;
@@ -241,7 +247,7 @@ __global__ void __launch_bounds__(FWD_THREADS, 1) chunk_scan_fwd_tc_kernel(Chunk
   const uint32_t tm = *tslot;
 
   unsigned* pub_s = reinterpret_cast<unsigned*>(sm + L::TSLOT + 8);
-  if (warp == COMPUTE_THREADS / 32 + 1) {  // ---- publisher (output CTAs beside the scan)
+  if (warp == FWD_PUBLISHER) {  // ---- publisher (output CTAs beside the scan)
     // Thread 0 sets pub_s to the number of chunks whose state and U records are stored
     // (after their bulk copies completed); this thread forwards the latest value to the
     // output CTAs with a GPU-scope release, which so stays off the chunk chain.
@@ -260,7 +266,7 @@ __global__ void __launch_bounds__(FWD_THREADS, 1) chunk_scan_fwd_tc_kernel(Chunk
     }
     return;
   }
-  if (warp == COMPUTE_THREADS / 32) {  // ---- producer
+  if (warp == FWD_PRODUCER) {  // ---- producer
     if (lane == 0) {
       for (int n = 0; n < N; ++n) {
         const int s = n % L::STAGES, k = n / L::STAGES;
@@ -279,17 +285,14 @@ __global__ void __launch_bounds__(FWD_THREADS, 1) chunk_scan_fwd_tc_kernel(Chunk
   }
 
   // ---- compute warps
-  const int row = 32 * (warp & 3) + lane, half = warp >> 2;
+  // thread: TMEM lane row (value column), state columns 32 qtr .. + 31, U^T tokens 16 qtr ..
+  const int row = 32 * (warp & 3) + lane, qtr = warp >> 2;
   const uint32_t tl = tm + ((uint32_t)(32 * (warp & 3)) << 16);  // this warp's lane quarter
   const size_t sb = (size_t)bh * TD * TD;
   {
-    float lo[32], hi[32];
-    for (int i = 0; i < 32; ++i) {
-      lo[i] = a.h0 ? a.h0[sb + (size_t)(64 * half + i) * TD + row] : 0.f;
-      hi[i] = a.h0 ? a.h0[sb + (size_t)(64 * half + 32 + i) * TD + row] : 0.f;
-    }
-    tmem_st32(tl + 64 * half, lo);
-    tmem_st32(tl + 64 * half + 32, hi);
+    float x[32];
+    for (int i = 0; i < 32; ++i) x[i] = a.h0 ? a.h0[sb + (size_t)(32 * qtr + i) * TD + row] : 0.f;
+    tmem_st32(tl + 32 * qtr, x);
     tmem_wait_st();
   }
   constexpr uint32_t id_1 = umma_idesc_bf16(128, C, false, false);  // S^T (-W)^T
@@ -311,11 +314,12 @@ __global__ void __launch_bounds__(FWD_THREADS, 1) chunk_scan_fwd_tc_kernel(Chunk
     }
     mbar_wait(&full[s], (uint32_t)(n / L::STAGES) & 1u, a.err);
     // S^T -> bf16 operand (the chunk-start state record)
-    float xs[64];
-    state_copy_out(tl + 64 * half, Sa, row, 64 * half, xs);
+    float xs[32];
+    tmem_ld32(tl + 32 * qtr, xs);
+    store_row32(Sa, row, 32 * qtr, xs);
     fence_proxy_async();
     tc_fence_before();
-    compute_sync();
+    fwd_sync();
     if (tid == 0) {
       tc_fence_after();
       bulk_s2g(state_rec + ch * (TD * TD), Sa.p, TD * TD * 2);
@@ -333,17 +337,33 @@ __global__ void __launch_bounds__(FWD_THREADS, 1) chunk_scan_fwd_tc_kernel(Chunk
     }
     // S^T <- S^T diag(gam) while the tensor cores form U^T (the S^T update comes after
     // the next barrier)
-    state_scale_back(tl + 64 * half, 64 * half, reinterpret_cast<const float*>(st + L::GAM), xs);
+    {
+      const float* gam = reinterpret_cast<const float*>(st + L::GAM) + 32 * qtr;
+#pragma unroll
+      for (int i = 0; i < 32; i += 4) {
+        const float4 g4 = *reinterpret_cast<const float4*>(gam + i);
+        xs[i] *= g4.x;
+        xs[i + 1] *= g4.y;
+        xs[i + 2] *= g4.z;
+        xs[i + 3] *= g4.w;
+      }
+      tmem_st32(tl + 32 * qtr, xs);
+      tmem_wait_st();
+    }
     mbar_wait(bar_u, ph_u, a.err);
     ph_u ^= 1u;
     tc_fence_after();
     {  // U^T row = U'^T row + (S^T (-W)^T) row -> bf16 operand (the U record)
-      float x[32];
-      tmem_ld32(tl + 128 + 32 * half, x);
+      uint32_t r16[16];
+      tmem_ld16_nowait(tl + 128 + 16 * qtr, r16);
+      tmem_wait_ld();
+      float x[16];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) x[i] = __uint_as_float(r16[i]);
       const bf16* up = reinterpret_cast<const bf16*>(st + L::UP);
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const uint4 u = *reinterpret_cast<const uint4*>(up + Sw<bf16, TD, C>::off(row, 32 * half + 8 * q));
+      for (int q = 0; q < 2; ++q) {
+        const uint4 u = *reinterpret_cast<const uint4*>(up + Sw<bf16, TD, C>::off(row, 16 * qtr + 8 * q));
         const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&u);
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
@@ -352,13 +372,21 @@ __global__ void __launch_bounds__(FWD_THREADS, 1) chunk_scan_fwd_tc_kernel(Chunk
           x[8 * q + 2 * e + 1] += f.y;
         }
       }
-      store_row32(Ua, row, 32 * half, x);
+#pragma unroll
+      for (int q = 0; q < 2; ++q) {
+        uint4 u;
+        u.x = pack_bf16(x[8 * q + 0], x[8 * q + 1]);
+        u.y = pack_bf16(x[8 * q + 2], x[8 * q + 3]);
+        u.z = pack_bf16(x[8 * q + 4], x[8 * q + 5]);
+        u.w = pack_bf16(x[8 * q + 6], x[8 * q + 7]);
+        *reinterpret_cast<uint4*>(Ua.ptr(row, 16 * qtr + 8 * q)) = u;
+      }
     }
     fence_proxy_async();
     tc_fence_before();
     // the record stores of the previous chunk have read the buffers the next chunk writes
     if (tid == 0) bulk_wait_read1();
-    compute_sync();
+    fwd_sync();
     if (tid == 0) {
       tc_fence_after();
       bulk_s2g(u_rec + ch * (C * TD), Ua.p, C * TD * 2);
@@ -375,10 +403,10 @@ __global__ void __launch_bounds__(FWD_THREADS, 1) chunk_scan_fwd_tc_kernel(Chunk
     tc_fence_after();
   }
   if (a.h_final) {
-    float x[64];
-    tmem_ld64(tl + 64 * half, x);
+    float x[32];
+    tmem_ld32(tl + 32 * qtr, x);
 #pragma unroll
-    for (int i = 0; i < 64; ++i) a.h_final[sb + (size_t)(64 * half + i) * TD + row] = x[i];
+    for (int i = 0; i < 32; ++i) a.h_final[sb + (size_t)(32 * qtr + i) * TD + row] = x[i];
   }
   if (tid == 0) {  // record stores and every issued MMA complete before TMEM is freed
     bulk_wait0();
@@ -389,7 +417,7 @@ __global__ void __launch_bounds__(FWD_THREADS, 1) chunk_scan_fwd_tc_kernel(Chunk
     drain_mma(bar_d);
   }
   tc_fence_before();
-  compute_sync();
+  fwd_sync();
   tc_fence_after();
   if (warp == 0) tmem_dealloc(tm, TMEM_COLS);
 }
