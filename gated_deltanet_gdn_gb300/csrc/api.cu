@@ -68,7 +68,6 @@ int check_dims(const gdn_dims* d, bool chunked) {
   if ((d->Dk != 64 && d->Dk != 128) || (d->Dv != 64 && d->Dv != 128)) return GDN_ERR_UNSUPPORTED;
   if ((long long)d->B * d->H > 65535) return GDN_ERR_UNSUPPORTED;  // grid y limit
   if (d->flags & ~(GDN_FLAG_PAIRWISE_WITHIN_BLOCK | GDN_FLAG_QK_L2NORM)) return GDN_ERR_INVALID_ARG;
-  if (chunked && d->Dk != d->Dv) return GDN_ERR_UNSUPPORTED;
   if (chunked && d->T % GDN_CHUNK != 0) return GDN_ERR_SHAPE;
   return GDN_OK;
 }
@@ -371,7 +370,7 @@ const char* gdn_status_string(int s) {
   switch (s) {
     case GDN_OK: return "ok";
     case GDN_ERR_INVALID_ARG: return "invalid argument (NULL or misaligned pointer, bad size or flag)";
-    case GDN_ERR_UNSUPPORTED: return "unsupported configuration (Dk, Dv in {64, 128}; chunked path Dk == Dv; bf16-only backward)";
+    case GDN_ERR_UNSUPPORTED: return "unsupported configuration (Dk, Dv in {64, 128}; bf16-only chunked backward)";
     case GDN_ERR_SHAPE: return "T must be a multiple of 64 on the chunked path";
     case GDN_ERR_CUDA: return "CUDA launch or runtime error";
     case GDN_ERR_INTERNAL: return "a kernel reported an error (a bounded wait timed out, or a replay fill count out of range)";

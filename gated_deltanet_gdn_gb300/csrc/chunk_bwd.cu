@@ -458,7 +458,8 @@ cudaError_t launch_bwd_t(const ChunkBwdArgs& a, cudaStream_t s) {
 
 cudaError_t launch_chunk_bwd(const ChunkBwdArgs& a, cudaStream_t s) {
   if (a.B * a.H == 0) return cudaSuccess;
-  return a.DK == 64 ? launch_bwd_t<64, 64>(a, s) : launch_bwd_t<128, 128>(a, s);
+  if (a.DK == 64) return a.DV == 64 ? launch_bwd_t<64, 64>(a, s) : launch_bwd_t<64, 128>(a, s);
+  return a.DV == 64 ? launch_bwd_t<128, 64>(a, s) : launch_bwd_t<128, 128>(a, s);
 }
 
 }  // namespace gdn

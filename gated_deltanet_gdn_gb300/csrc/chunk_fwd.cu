@@ -578,7 +578,8 @@ cudaError_t launch_fwd_t(const ChunkFwdArgs& a, cudaStream_t s) {
 
 template <class T>
 cudaError_t launch_fwd_dims(const ChunkFwdArgs& a, cudaStream_t s) {
-  return a.DK == 64 ? launch_fwd_t<T, 64, 64>(a, s) : launch_fwd_t<T, 128, 128>(a, s);
+  if (a.DK == 64) return a.DV == 64 ? launch_fwd_t<T, 64, 64>(a, s) : launch_fwd_t<T, 64, 128>(a, s);
+  return a.DV == 64 ? launch_fwd_t<T, 128, 64>(a, s) : launch_fwd_t<T, 128, 128>(a, s);
 }
 
 }  // namespace

@@ -44,9 +44,10 @@
  * check returns a gdn_status and enqueues nothing:
  *   GDN_ERR_INVALID_ARG  NULL dims or required pointer, negative sizes, a
  *                        pointer not aligned to 16 bytes, scale not finite
- *   GDN_ERR_UNSUPPORTED  Dk or Dv not in {64, 128}, Dk != Dv on the chunked
- *                        path, unknown dtype, a float32 chunked backward (the
- *                        chunked backward is bfloat16 only), B * H > 65535
+ *   GDN_ERR_UNSUPPORTED  Dk or Dv not in {64, 128} (each on its own: Dk != Dv
+ *                        is supported everywhere), unknown dtype, a float32
+ *                        chunked backward (the chunked backward is bfloat16
+ *                        only), B * H > 65535
  *   GDN_ERR_SHAPE        chunked calls with T not a multiple of 64
  *   GDN_ERR_CUDA         a launch was rejected (cudaGetLastError); faults that
  *                        happen later surface at the caller's next

@@ -80,7 +80,7 @@ def test_invalid_arguments_are_rejected_on_the_host(lib):
     assert fwd(None, p, p, p, p, p, None, f, p, None, p, None) == binding.GDN_ERR_INVALID_ARG
     # unsupported widths / dtype / flags / shape
     assert fwd(ctypes.byref(_dims(Dk=96)), p, p, p, p, p, None, f, p, None, p, None) == binding.GDN_ERR_UNSUPPORTED
-    assert fwd(ctypes.byref(_dims(Dk=64, Dv=128)), p, p, p, p, p, None, f, p, None, p, None) == binding.GDN_ERR_UNSUPPORTED
+    assert fwd(ctypes.byref(_dims(Dk=64, Dv=96)), p, p, p, p, p, None, f, p, None, p, None) == binding.GDN_ERR_UNSUPPORTED
     assert fwd(ctypes.byref(_dims(dtype=7)), p, p, p, p, p, None, f, p, None, p, None) == binding.GDN_ERR_UNSUPPORTED
     assert fwd(ctypes.byref(_dims(flags=8)), p, p, p, p, p, None, f, p, None, p, None) == binding.GDN_ERR_INVALID_ARG
     assert fwd(ctypes.byref(_dims(T=100)), p, p, p, p, p, None, f, p, None, p, None) == binding.GDN_ERR_SHAPE

@@ -174,3 +174,20 @@ def test_concurrent_backward_calls_on_two_streams():
         ref = oracle_bwd(host)
         for n in GRADS:
             assert rel(grads[n], ref[n]) <= TOL["bf16"], (n, rel(grads[n], ref[n]))
+
+
+@pytest.mark.parametrize("per_channel", [True, False])
+@pytest.mark.parametrize("Dk,Dv", [(64, 128), (128, 64)])
+def test_unequal_key_value_widths(per_channel, Dk, Dv):
+    """Dk != Dv on the chunked path (the gated-deltanet kernel card, Requirements and
+    limits, allows unequal key and value widths): forward and backward against the
+    oracle, bf16 inputs."""
+    w = WORKLOADS["train_fwdbwd"].with_(B=2, T=192, H=2, Dk=Dk, Dv=Dv, g_per_channel=per_channel,
+                                        g_mult=1.0 if per_channel else 0.1, h0_std=0.3)
+    host = make_inputs(w)
+    out, hT, grads = _fwd_bwd(cuda_inputs(host))
+    o_ref, h_ref = oracle_fwd(host)
+    assert rel(out, o_ref) <= TOL["bf16"] and rel(hT, h_ref) <= TOL["bf16"]
+    ref = oracle_bwd(host)
+    for n in GRADS:
+        assert rel(grads[n], ref[n]) <= TOL["bf16"], (n, rel(grads[n], ref[n]))

@@ -114,3 +114,18 @@ def test_qk_l2norm_forward_fp32():
     assert rel(out, o_ref) <= TOL["f32"] and rel(hT, h_ref) <= TOL["f32"]
     plain = gdn.gdn_chunk_residual_bytes(gdn.make_dims(d["q"], d["v"], d["g"]))
     assert res.numel() > plain
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("per_channel", [True, False])
+@pytest.mark.parametrize("Dk,Dv", [(64, 128), (128, 64)])
+def test_unequal_key_value_widths(dtype, per_channel, Dk, Dv):
+    """Dk != Dv on the chunked forward (the gated-deltanet kernel card, Requirements and
+    limits, allows unequal key and value widths), fp32 and bf16 inputs."""
+    w = WORKLOADS["train_fwd_f32"].with_(B=2, T=192, H=3, Dk=Dk, Dv=Dv, dtype=dtype,
+                                         g_per_channel=per_channel, g_mult=1.0, h0_std=0.3)
+    host = make_inputs(w)
+    o_ref, h_ref = oracle_fwd(host)
+    out, hT = _fwd(cuda_inputs(host))
+    assert rel(out, o_ref) <= TOL[dtype], rel(out, o_ref)
+    assert rel(hT, h_ref) <= TOL[dtype], rel(hT, h_ref)
