@@ -304,10 +304,10 @@ def gdn_replay_state(ckpt, buffer, fill, L: int, *, h_out=None) -> torch.Tensor:
 def gdn_selftest_wait_timeout(max_tries: int = 1024, device: Optional[torch.device] = None,
                               cycles: Optional[torch.Tensor] = None) -> None:
     """Launch the library's wait-timeout self-test kernel (see include/gdn.h). cycles: an
-    optional int64 device tensor of two elements for the kernel's cycle counts."""
+    optional int64 device tensor of three elements for the kernel's cycle counts."""
     dev = device if device is not None else torch.device("cuda", torch.cuda.current_device())
     if cycles is not None:
-        assert cycles.dtype == torch.int64 and cycles.numel() >= 2 and cycles.is_contiguous()
+        assert cycles.dtype == torch.int64 and cycles.numel() >= 3 and cycles.is_contiguous()
     with torch.cuda.device(dev):
         st = load().gdn_selftest_wait_timeout(int(max_tries), _ptr(cycles), _stream(dev))
     _check("gdn_selftest_wait_timeout", st)

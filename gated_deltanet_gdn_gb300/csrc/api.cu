@@ -35,17 +35,24 @@ unsigned* device_error_word() {
 
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
-// One thread waits on an mbarrier that nothing ever arrives on, giving up after max_tries
-// tries exactly as the kernels' own bounded waits do: the error word gets
-// ERR_WAIT_TIMEOUT and the kernel returns normally. Then it runs SELFTEST_LATER_WAITS
-// of the kernels' own waits (mbar_wait) on the same barrier, which must give up soon
-// after WAIT_BAIL_TRIES tries because the error word is now set. With `cycles` non-NULL
-// it records the clock cycles of the first wait and of the later ones together.
+// One thread first waits, with the kernels' own bounded cross-CTA counter wait
+// (wait_counter, as the forward's output CTAs wait on the scan), for a counter that
+// nothing raises, giving up after max_tries polls: the error word gets ERR_WAIT_TIMEOUT.
+// Then it waits on an mbarrier that nothing ever arrives on, giving up after max_tries
+// tries exactly as the kernels' own bounded waits do, and runs SELFTEST_LATER_WAITS of
+// the kernels' own waits (mbar_wait) on the same barrier, which must give up soon after
+// WAIT_BAIL_TRIES tries because the error word is set. The kernel returns normally. With
+// `cycles` non-NULL it records the clock cycles of the first mbarrier wait, of the later
+// ones together, and of the counter wait (0 had it succeeded).
 constexpr int SELFTEST_LATER_WAITS = 4;
+__device__ unsigned g_selftest_counter = 0;  // never raised
 __global__ void wait_timeout_selftest_kernel(unsigned* err, unsigned max_tries, unsigned long long* cycles) {
   __shared__ uint64_t bar;
   mbar_init(&bar, 1);
   fence_mbar_init();
+  const long long c0 = clock64();
+  const bool counter_ok = wait_counter(&g_selftest_counter, 1u, err, max_tries);
+  const long long c1 = clock64();
   const long long t0 = clock64();
   for (unsigned i = 0; i < max_tries; ++i)
     if (mbar_try_wait(&bar, 0u)) return;
@@ -57,6 +64,7 @@ __global__ void wait_timeout_selftest_kernel(unsigned* err, unsigned max_tries, 
   if (cycles) {
     cycles[0] = (unsigned long long)(t1 - t0);
     cycles[1] = (unsigned long long)(t2 - t1);
+    cycles[2] = counter_ok ? 0ull : (unsigned long long)(c1 - c0);
   }
 }
 

@@ -259,6 +259,10 @@ __global__ void __launch_bounds__(FWD_THREADS, 1) chunk_scan_fwd_tc_kernel(Chunk
           st_release_gpu(a.res.progress + (size_t)bh * PROGRESS_STRIDE, v);
           last = v;
         } else {
+          // after a time-out anywhere the scan's waits give up early; so does this one
+          if (i >= WAIT_BAIL_TRIES && (i & 255u) == 0 &&
+              (*reinterpret_cast<volatile unsigned*>(a.err) & ERR_WAIT_TIMEOUT))
+            break;
           __nanosleep(256);
         }
       }

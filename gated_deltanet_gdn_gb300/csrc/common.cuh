@@ -508,8 +508,9 @@ __device__ __forceinline__ void bulk_wait1() { asm volatile("cp.async.bulk.wait_
 // Bounded wait, by one thread, until *p >= target (a counter another CTA of the same
 // cooperative grid raises with st_release_gpu): same limits and early give-up on the
 // error word as mbar_wait, with a short sleep between polls.
-__device__ __forceinline__ bool wait_counter(const unsigned* p, unsigned target, unsigned* err) {
-  for (uint32_t i = 0; i < WAIT_MAX_TRIES; ++i) {
+__device__ __forceinline__ bool wait_counter(const unsigned* p, unsigned target, unsigned* err,
+                                             uint32_t max_tries = WAIT_MAX_TRIES) {
+  for (uint32_t i = 0; i < max_tries; ++i) {
     if (ld_acquire_gpu(p) >= target) return true;
     if (i >= WAIT_BAIL_TRIES && (i & 255u) == 0 && err &&
         (*reinterpret_cast<volatile unsigned*>(err) & ERR_WAIT_TIMEOUT))

@@ -247,18 +247,20 @@ int gdn_replay_decode(const gdn_dims* dims, int L, const void* q, const void* k,
 int gdn_replay_state(const gdn_dims* dims, int L, const float* ckpt, const void* buffer,
                      const int* fill, float* h_out, void* stream);
 
-/* Self-test of the failure path: launches a one-thread kernel that waits on an
- * mbarrier nothing arrives on and gives up after max_tries tries (1 .. 65536),
- * like every wait in the library's kernels. The kernel then sets bit 1 of the
- * device error word, runs four more of the kernels' own bounded waits on the same
- * barrier (each must give up after 4096 tries or a little more, because the
- * error word is set: after one time-out the library's later waits end early
+/* Self-test of the failure path: launches a one-thread kernel that first waits,
+ * with the library's cross-CTA counter wait (the one the forward's output CTAs use
+ * on the scan), for a counter nothing raises, and gives up after max_tries polls
+ * (1 .. 65536), setting bit 1 of the device error word. It then waits on an
+ * mbarrier nothing arrives on and gives up after max_tries tries, like every wait
+ * in the library's kernels, runs four more of the kernels' own bounded waits on
+ * the same barrier (each must give up after 4096 tries or a little more, because
+ * the error word is set: after one time-out the library's later waits end early
  * instead of running their full count), and returns; the context stays usable.
  * The next gdn_check_device_error returns GDN_ERR_INTERNAL. cycles: NULL, or a
- * 16-byte aligned device buffer of two unsigned 64-bit words that receives the
- * clock cycles of the first wait and of the four later waits together. Not
- * part of the method: it lets a caller or a test see the error path work
- * without a GPU fault. */
+ * 16-byte aligned device buffer of three unsigned 64-bit words that receives the
+ * clock cycles of the first mbarrier wait, of the four later waits together and
+ * of the counter wait. Not part of the method: it lets a caller or a test see
+ * the error path work without a GPU fault. */
 int gdn_selftest_wait_timeout(unsigned max_tries, unsigned long long* cycles, void* stream);
 
 /* Reads and clears the library's device error word on the current device

@@ -31,13 +31,15 @@ def test_waits_after_a_timeout_give_up_early():
     later waits together take a few times the cycles of its first 4096-try wait, where
     four full waits would take about a thousand times as many."""
     assert gdn.gdn_check_device_error() == gdn.binding.GDN_OK
-    cycles = torch.zeros(2, dtype=torch.int64, device="cuda")
+    cycles = torch.zeros(3, dtype=torch.int64, device="cuda")
     gdn.gdn_selftest_wait_timeout(4096, cycles=cycles)
-    first, later = (int(x) for x in cycles.cpu())
+    first, later, counter = (int(x) for x in cycles.cpu())
     assert gdn.gdn_check_device_error() == gdn.binding.GDN_ERR_INTERNAL
-    print(f"first wait {first} cycles, four later waits {later} cycles")
+    print(f"first wait {first} cycles, four later waits {later} cycles, counter wait {counter} cycles")
     assert first > 0 and later > 0
     assert later < 4 * 4 * first, (first, later)
+    # the cross-CTA counter wait ran out (it never saw the counter raised) and reported it
+    assert counter > 0
 
 
 def test_selftest_rejects_unbounded_requests():
