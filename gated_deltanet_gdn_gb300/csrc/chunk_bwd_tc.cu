@@ -30,11 +30,13 @@
 // dAqk and dAkk, and the operands are q, beta k and k themselves.
 //
 // Roles (512 threads, one CTA per SM, persistent over chunk-heads): all sixteen warps run
-// the epilogues, four per TMEM lane quarter, each on a quarter of the chunk's tokens (16);
-// thread 0 also issues every MMA and every load, each load as soon as the
-// buffer it fills is released (T and dU^T once P1 has read them, the rest once P2-P4 and
-// the gamma-gradient sums have), so the next chunk's loads overlap this chunk's later
-// phases. Every wait is bounded.
+// the epilogues, four per TMEM lane quarter, each on a quarter of the chunk's tokens (16).
+// Thread 0 also issues P1, P2, P5 and the loads, thread 32 P3 and P6 and the group B
+// loads, thread 64 P4: a tcgen05.mma issue stalls its thread for about as long as the
+// tensor pipe takes to accept it, so the issue work is spread over three warps. Each load
+// is issued as soon as the buffer it fills is released (T and dU^T once P1 has read them,
+// q and k once P5 and P6 have, the rest once P2-P4 and the gamma-gradient sums have), so
+// the next chunk's loads overlap this chunk's later phases. Every wait is bounded.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -217,9 +219,9 @@ __global__ void __launch_bounds__(BT_THREADS, 1)
     mbar_init(fullB, 1);
     mbar_init(bP1, 1);
     mbar_init(bP2, 1);
-    mbar_init(bP34, 1);
-    mbar_init(bP56, 1);
-    mbar_init(bDrain, 1);
+    mbar_init(bP34, 2);  // P3 (thread 32) and P4 (thread 64)
+    mbar_init(bP56, 2);  // P5 (thread 0) and P6 (thread 32)
+    mbar_init(bDrain, 3);  // every issuing thread: 0, 32, 64
     mbar_init(fullQ, 1);
     fence_mbar_init();
   }
@@ -516,12 +518,19 @@ __global__ void __launch_bounds__(BT_THREADS, 1)
           umma_bf16(tm + TC_P2, kstep_kmajor(dA, ks, 2 * C * 128), kstep_mnmajor(dB, ks), id_p2, ks > 0);
         umma_commit(bP2);
       }
+    } else if (tid == 32) {  // P3 and P4 from two more warps: each issue stall is per thread
+      mbar_wait(fullB, par, a.err);
+      tc_fence_after();
       {  // P3: D3 = S0 DY^T (M = Dk, N = 2C, K = Dv)
         const uint64_t dA = desc_mnmajor(sm + L::S0T, BD * 128), dB = desc_kmajor(sm + L::DY);
 #pragma unroll
         for (int ks = 0; ks < BD / 16; ++ks)
           umma_bf16(tm + TC_D3, kstep_mnmajor(dA, ks), kstep_kmajor(dB, ks, 2 * C * 128), id_p3, ks > 0);
       }
+      umma_commit(bP34);
+    } else if (tid == 64) {
+      mbar_wait(fullB, par, a.err);
+      tc_fence_after();
       {  // P4: D4 = dS1 U^T (M = Dk, N = C, K = Dv)
         const uint64_t dA = desc_mnmajor(sm + L::DS1T, BD * 128), dB = desc_mnmajor(sm + L::UT, BD * 128);
 #pragma unroll
@@ -696,6 +705,9 @@ __global__ void __launch_bounds__(BT_THREADS, 1)
         for (int ks = 0; ks < C / 16; ++ks)
           umma_bf16(tm + TC_D5, kstep_kmajor(dA, ks, BD * 128), kstep_kmajor(dB, ks, 2 * C * 128), id_p5, ks > 0);
       }
+      umma_commit(bP56);
+    } else if (tid == 32) {
+      tc_fence_after();
       {  // P6: D6 = X^T DP (M = Dk, N = C, K = 2C)
         const uint64_t dA = desc_kmajor(sm + L::X), dB = desc_mnmajor(sm + L::DP, 2 * C * 128);
 #pragma unroll
@@ -714,6 +726,8 @@ __global__ void __launch_bounds__(BT_THREADS, 1)
       mbar_drain(fullB, lp);
       mbar_drain(fullQ, lp);
     }
+  }
+  if (tid == 0 || tid == 32 || tid == 64) {  // each issuing thread's products
     umma_commit(bDrain);
     mbar_drain(bDrain, 0u);
   }
