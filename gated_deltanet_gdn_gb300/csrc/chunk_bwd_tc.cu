@@ -31,9 +31,10 @@
 //
 // Roles (512 threads, one CTA per SM, persistent over chunk-heads): all sixteen warps run
 // the epilogues, four per TMEM lane quarter, each on a quarter of the chunk's tokens (16).
-// Thread 0 also issues P1, P2, P5 and the loads, thread 32 P3 and P6 and the group B
-// loads, thread 64 P4: a tcgen05.mma issue stalls its thread for about as long as the
-// tensor pipe takes to accept it, so the issue work is spread over three warps. Each load
+// Thread 0 also issues P2 and the group A and q/k/g loads, thread 32 P3 and the group B
+// loads, thread 64 P4 and P5, thread 96 P1 and P6: a tcgen05.mma issue stalls its thread
+// for about as long as the tensor pipe takes to accept it, so the issue work is spread
+// over four warps. Each load
 // is issued as soon as the buffer it fills is released (T and dU^T once P1 has read them,
 // q and k once P5 and P6 have, the rest once P2-P4 and the gamma-gradient sums have), so
 // the next chunk's loads overlap this chunk's later phases. Every wait is bounded.
@@ -220,8 +221,8 @@ __global__ void __launch_bounds__(BT_THREADS, 1)
     mbar_init(bP1, 1);
     mbar_init(bP2, 1);
     mbar_init(bP34, 2);  // P3 (thread 32) and P4 (thread 64)
-    mbar_init(bP56, 2);  // P5 (thread 0) and P6 (thread 32)
-    mbar_init(bDrain, 3);  // every issuing thread: 0, 32, 64
+    mbar_init(bP56, 2);  // P5 (thread 64) and P6 (thread 96)
+    mbar_init(bDrain, 4);  // every issuing thread: 0, 32, 64, 96
     mbar_init(fullQ, 1);
     fence_mbar_init();
   }
@@ -334,7 +335,7 @@ __global__ void __launch_bounds__(BT_THREADS, 1)
       beta_pre = ldg_bf16(bg + r);
     }
     // (a) P1 of this chunk: Y^T = dU^T T
-    if (cur && tid == 0) {
+    if (cur && tid == 96) {
       mbar_wait(fullA, par, a.err);
       tc_fence_after();
       const uint64_t dA = desc_kmajor(sm + L::DUT), dB = desc_mnmajor(sm + L::TM, C * 128);
@@ -697,7 +698,7 @@ __global__ void __launch_bounds__(BT_THREADS, 1)
       mbar_wait(bP34, par, a.err);
       load_b(m + 1);
     }
-    if (tid == 0) {
+    if (tid == 64) {
       tc_fence_after();
       {  // P5: D5 = Ye^T DP^T (M = Dk, N = 2C, K = C)
         const uint64_t dA = desc_kmajor(sm + L::YE), dB = desc_kmajor(sm + L::DP);
@@ -706,7 +707,7 @@ __global__ void __launch_bounds__(BT_THREADS, 1)
           umma_bf16(tm + TC_D5, kstep_kmajor(dA, ks, BD * 128), kstep_kmajor(dB, ks, 2 * C * 128), id_p5, ks > 0);
       }
       umma_commit(bP56);
-    } else if (tid == 32) {
+    } else if (tid == 96) {
       tc_fence_after();
       {  // P6: D6 = X^T DP (M = Dk, N = C, K = 2C)
         const uint64_t dA = desc_kmajor(sm + L::X), dB = desc_mnmajor(sm + L::DP, 2 * C * 128);
@@ -727,7 +728,7 @@ __global__ void __launch_bounds__(BT_THREADS, 1)
       mbar_drain(fullQ, lp);
     }
   }
-  if (tid == 0 || tid == 32 || tid == 64) {  // each issuing thread's products
+  if (tid == 0 || tid == 32 || tid == 64 || tid == 96) {  // each issuing thread's products
     umma_commit(bDrain);
     mbar_drain(bDrain, 0u);
   }
