@@ -31,10 +31,10 @@
 //
 // Roles (512 threads, one CTA per SM, persistent over chunk-heads): all sixteen warps run
 // the epilogues, four per TMEM lane quarter, each on a quarter of the chunk's tokens (16).
-// Thread 0 also issues P2 and the group A and q/k/g loads, thread 32 P3 and the group B
-// loads, thread 64 P4 and P5, thread 96 P1 and P6: a tcgen05.mma issue stalls its thread
-// for about as long as the tensor pipe takes to accept it, so the issue work is spread
-// over four warps. Each load
+// Thread 0 issues P2, thread 32 P3 and the group B loads, thread 64 P4 and P5, thread 96
+// P1 and P6, thread 128 the group A loads and thread 160 the q/k/g loads: a tcgen05.mma
+// or bulk-copy issue stalls its thread, so the issue work is spread over six warps (the
+// loads of the first chunk are issued by thread 0 at the start). Each load
 // is issued as soon as the buffer it fills is released (T and dU^T once P1 has read them,
 // q and k once P5 and P6 have, the rest once P2-P4 and the gamma-gradient sums have), so
 // the next chunk's loads overlap this chunk's later phases. Every wait is bounded.
@@ -358,7 +358,7 @@ __global__ void __launch_bounds__(BT_THREADS, 1)
       const bool unsafe1 = flags_s[0] != 0, unsafe2 = flags_s[1] != 0;
       const bool fast = !mask_form && !(unsafe1 || unsafe2);
       q_early = mask_form || fast;  // X is not borrowed for G below
-      if (tid == 0 && cur && q_early) load_q(m);
+      if (tid == 160 && cur && q_early) load_q(m);
       const bool blk1 = blk == 0;
       const bool pw_rows = !mask_form && !fast && (blk1 ? unsafe1 : unsafe2);
       const bool skip_x = pw_rows && blk1, skip_y = pw_rows && !blk1;
@@ -473,7 +473,7 @@ __global__ void __launch_bounds__(BT_THREADS, 1)
     if (!q_early) {  // G of the previous chunk has left X (read by the pairwise sums)
       fence_proxy_async();
       epi_sync();
-      if (tid == 0) load_q(m);
+      if (tid == 160) load_q(m);
     }
     const int b = bh / a.H, h = bh % a.H;
     const size_t row0 = ((size_t)b * a.T + (size_t)n * C) * a.H + h;
@@ -508,8 +508,8 @@ __global__ void __launch_bounds__(BT_THREADS, 1)
     tc_fence_before();
     epi_sync();
     // (d) P2, P3, P4; P1 has read T and dU^T: the next chunk's group A loads
+    if (tid == 128 && m + 1 < nunits) load_a(m + 1);
     if (tid == 0) {
-      if (m + 1 < nunits) load_a(m + 1);
       mbar_wait(fullB, par, a.err);
       tc_fence_after();
       {  // P2: D2 = DY U^T (M = 2C tokens, N = C, K = Dv)
