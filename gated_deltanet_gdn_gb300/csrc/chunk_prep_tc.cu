@@ -266,12 +266,6 @@ __global__ void __launch_bounds__(PTC_THREADS, 2)
       umma_commit(bar);
     }
     mma_done();
-    // v is needed from A5 on: it streams into Y (read by the finished score products)
-    if (tid == 0) {
-      mbar_arrive_expect_tx(bar_v, L::TX_V);
-      tma_load_3d(sm + L::Y, &v_map, 0, h, tok, bar_v);
-      tma_load_3d(sm + L::Y + C * 128, &v_map, 64, h, tok, bar_v);
-    }
     // scores epilogue. Thread: row t' = rowl of [Aqk ; Akk], key columns 32 half .. + 31.
     AkkTile Akk{reinterpret_cast<float*>(sm + L::XS)};  // XS was read by the finished product
     {
@@ -362,6 +356,13 @@ __global__ void __launch_bounds__(PTC_THREADS, 2)
         Tb.at(o + i, o + j) = __float2bfloat16_rn(t[i] * bj);
       }
     } else {
+      // v is needed from the W / U' products on: it streams into Y (read by the finished
+      // score products), issued by a warp that has time while warps 0 and 1 substitute
+      if (tid == PTC_THREADS - 32) {
+        mbar_arrive_expect_tx(bar_v, L::TX_V);
+        tma_load_3d(sm + L::Y, &v_map, 0, h, tok, bar_v);
+        tma_load_3d(sm + L::Y + C * 128, &v_map, 64, h, tok, bar_v);
+      }
       // 16-byte pieces: 0..127 the zero blocks (T, Tb: 32 rows x 4 pieces each), 128..255
       // A21 (32 rows x 4 pieces of 8 columns)
       for (int i = tid - 64; i < 256; i += PTC_THREADS - 64) {
