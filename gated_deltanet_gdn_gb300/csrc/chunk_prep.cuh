@@ -20,8 +20,9 @@ __device__ __forceinline__ void tri_index(int p, int& i, int& j) {
 
 // In-block pairwise scores (A4) for the blocks flagged unsafe: 4 lanes per (i, j) pair,
 // each summing a quarter of the channels, reduced with two xor shuffles. Writes
-// scale * sum q k E into the Aqk staging tile and beta_i * sum k k E (i > j) into Akk.
-template <class T, int DK, int NTHR>
+// scale * sum q k E into the Aqk staging tile and beta_i * sum k k E (i > j) into Akk
+// (at [i][j], or at [j][i] when AKK_T: the tensor-core preparation keeps Akk transposed).
+template <class T, int DK, int NTHR, bool AKK_T = false>
 __device__ __noinline__ void prep_pairwise(bool unsafe1, bool unsafe2, const T* q, const T* k, size_t row0,
                                            size_t rs, FTile<C, DK> Gs, Tile<T, C, C> Tst, FTile<C, C, 4> Akk,
                                            const float* beta_s, float scale, int tid) {
@@ -53,7 +54,10 @@ __device__ __noinline__ void prep_pairwise(bool unsafe1, bool unsafe2, const T* 
       sk += __shfl_xor_sync(0xffffffffu, sk, 2);
       if (valid && quarter == 0) {
         Tst.at(bs + i, bs + j) = from_f32<T>(scale * sq);
-        if (i > j) Akk.at(bs + i, bs + j) = beta_s[bs + i] * sk;
+        if (i > j) {
+          if (AKK_T) Akk.at(bs + j, bs + i) = beta_s[bs + i] * sk;
+          else Akk.at(bs + i, bs + j) = beta_s[bs + i] * sk;
+        }
       }
     }
   }

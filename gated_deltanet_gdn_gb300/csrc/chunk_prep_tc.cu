@@ -46,7 +46,7 @@ constexpr uint32_t PTC_TMEM_COLS = 256;
 // then U'^T (64 columns)
 constexpr int TP_S = 0, TP_X = 64, TP_T21 = 128, TP_W = 0, TP_U = 128;
 
-typedef FTile<C, C, 4> AkkTile;  // fp32 Akk (padded rows)
+typedef FTile<C, C, 4> AkkTile;  // fp32 Akk, transposed: at(j, i) = Akk[i][j] (padded rows)
 
 struct PtcLayout {
   static constexpr int G = 0;                    // fp32 [C][Dk] cumulative log-decay
@@ -93,6 +93,21 @@ __device__ __forceinline__ void unpack8(float (&x)[8], const uint4 u) {
     x[2 * e] = __low2float(h);
     x[2 * e + 1] = __high2float(h);
   }
+}
+// Packed fp32 pairs (f32x2 arithmetic): one instruction does the fp32 operation on both
+// halves, each rounded as the scalar one.
+__device__ __forceinline__ uint64_t f2_pack(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void f2_unpack(uint64_t r, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(r));
+}
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
 }
 __device__ __forceinline__ void ld8f(float (&x)[8], const float* p) {
   const float4 a = *reinterpret_cast<const float4*>(p), b = *reinterpret_cast<const float4*>(p + 4);
@@ -299,13 +314,13 @@ __global__ void __launch_bounds__(PTC_THREADS, 2)
         for (int jj = 0; jj < 32; ++jj) {
           const int j = 32 * half + jj;
           const float dec = mask_form && j < t ? __expf(Gt - Gs.at(j, 0)) : 1.f;
-          Akk.at(t, j) = j < t ? br * d[jj] * dec : 0.f;
+          Akk.at(j, t) = j < t ? br * d[jj] * dec : 0.f;  // transposed: lanes write one row
         }
       }
     }
     __syncthreads();
     if (unsafe1 || unsafe2) {
-      prep_pairwise<bf16, PT, PTC_THREADS>(unsafe1, unsafe2, q, k, row0, rs, Gs, Tst, Akk, beta_s,
+      prep_pairwise<bf16, PT, PTC_THREADS, true>(unsafe1, unsafe2, q, k, row0, rs, Gs, Tst, Akk, beta_s,
                                            a.scale, tid);
       __syncthreads();
     }
@@ -324,29 +339,40 @@ __global__ void __launch_bounds__(PTC_THREADS, 2)
       // Column j of the block's inverse, right-looking in groups of four rows:
       // acc[i] = sum over finished rows kk of A[i][kk] T[kk][j]; a group's four entries
       // T[i][j] = -acc[i] (1 on the diagonal, 0 above) follow from the rows before them
-      // inside the group, then every later row takes the group's four terms at once.
+      // inside the group, then every later row takes the group's four terms at once. The
+      // accumulators of rows 2p and 2p + 1 form one packed fp32 pair (fma.rn.f32x2: each
+      // half is the scalar fmaf, in the same order), fed by 16-byte loads of Akk^T that
+      // hold one column of four consecutive rows.
       const int o = BLK * warp, j = lane;
-      float t[BLK], acc[BLK];
+      float t[BLK];
+      uint64_t acc2[BLK / 2];
 #pragma unroll
-      for (int i = 0; i < BLK; ++i) acc[i] = 0.f;
+      for (int p2 = 0; p2 < BLK / 2; ++p2) acc2[p2] = f2_pack(0.f, 0.f);
 #pragma unroll
       for (int mg = 0; mg < BLK / 4; ++mg) {
         const int m = 4 * mg;
+        float am[4];
+        f2_unpack(acc2[m / 2], am[0], am[1]);
+        f2_unpack(acc2[m / 2 + 1], am[2], am[3]);
 #pragma unroll
         for (int ii = 0; ii < 4; ++ii) {
           const int i = m + ii;
-          float x = acc[i];
+          float x = am[ii];
 #pragma unroll
-          for (int kk = 0; kk < ii; ++kk) x = fmaf(Akk.at(o + i, o + m + kk), t[m + kk], x);
+          for (int kk = 0; kk < ii; ++kk) x = fmaf(Akk.at(o + m + kk, o + i), t[m + kk], x);
           t[i] = i == j ? 1.f : (i > j ? -x : 0.f);
         }
+        uint64_t tt[4];
 #pragma unroll
-        for (int i = m + 4; i < BLK; ++i) {
-          const float4 a4 = *reinterpret_cast<const float4*>(&Akk.at(o + i, o + m));
-          acc[i] = fmaf(a4.x, t[m], acc[i]);
-          acc[i] = fmaf(a4.y, t[m + 1], acc[i]);
-          acc[i] = fmaf(a4.z, t[m + 2], acc[i]);
-          acc[i] = fmaf(a4.w, t[m + 3], acc[i]);
+        for (int q = 0; q < 4; ++q) tt[q] = f2_pack(t[m + q], t[m + q]);
+#pragma unroll
+        for (int i = m + 4; i < BLK; i += 4) {  // rows i .. i + 3: two packed pairs
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const float4 a4 = *reinterpret_cast<const float4*>(&Akk.at(o + m + q, o + i));
+            acc2[i / 2] = f2_fma(f2_pack(a4.x, a4.y), tt[q], acc2[i / 2]);
+            acc2[i / 2 + 1] = f2_fma(f2_pack(a4.z, a4.w), tt[q], acc2[i / 2 + 1]);
+          }
         }
       }
       const float bj = beta_s[o + j];
@@ -372,7 +398,8 @@ __global__ void __launch_bounds__(PTC_THREADS, 2)
           *reinterpret_cast<uint4*>(Tb.ptr(r, BLK + c)) = make_uint4(0u, 0u, 0u, 0u);
         } else {
           float x[8];
-          ld8f(x, &Akk.at(BLK + r, c));
+#pragma unroll
+          for (int e = 0; e < 8; ++e) x[e] = Akk.at(c + e, BLK + r);
           *reinterpret_cast<uint4*>(AT.ptr(BLK + r, c)) = pack8(x);
         }
       }
