@@ -204,7 +204,8 @@ def gdn_chunk_bwd(q, k, v, g, beta, h0, residuals, dout, dh_final=None,
                   scale: Optional[float] = None, *, workspace=None, flags: int = 0,
                   need_dh0: bool = True, grads: Optional[Dict[str, torch.Tensor]] = None
                   ) -> Dict[str, torch.Tensor]:
-    """Chunked backward (bf16). Returns dq, dk, dv, dg, dbeta (input dtype) and dh0 (fp32).
+    """Chunked backward (bf16 or fp32, the forward's dtype). Returns dq, dk, dv, dg, dbeta
+    (input dtype) and dh0 (fp32).
     ``grads`` may supply preallocated output tensors under those names."""
     dev = q.device
     dims = make_dims(q, v, g, flags)
@@ -339,7 +340,7 @@ def gdn_kernel_name(i: int) -> str:
 
 
 class GatedDeltaRule(torch.autograd.Function):
-    """Chunked gated delta rule with the library's backward (bf16 for gradients)."""
+    """Chunked gated delta rule with the library's backward (bf16 or fp32)."""
 
     @staticmethod
     def forward(ctx, q, k, v, g, beta, h0, scale, flags):

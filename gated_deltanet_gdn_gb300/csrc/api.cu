@@ -234,7 +234,6 @@ int gdn_chunk_bwd(const gdn_dims* d, const void* q, const void* k, const void* v
                   void* dbeta, float* dh0, void* workspace, void* stream) {
   int st = check_dims(d, true);
   if (st != GDN_OK) return st;
-  if (d->dtype != GDN_BF16) return GDN_ERR_UNSUPPORTED;
   if (!std::isfinite(scale)) return GDN_ERR_INVALID_ARG;
   const bool work = (long long)d->B * d->H * d->T > 0;
   const int es = esize(d);
@@ -253,7 +252,7 @@ int gdn_chunk_bwd(const gdn_dims* d, const void* q, const void* k, const void* v
   ChunkBwdArgs a{};
   a.B = d->B; a.T = d->T; a.H = d->H; a.DK = d->Dk; a.DV = d->Dv;
   a.per_channel = d->g_per_channel ? 1 : 0;
-  a.bf16 = 1;
+  a.bf16 = d->dtype == GDN_BF16;
   a.flags = d->flags;
   a.q = q; a.k = k; a.v = v; a.g = g; a.beta = beta; a.scale = scale;
   if (residuals) a.res = residual_ptrs(d, const_cast<void*>(residuals));
@@ -271,7 +270,7 @@ int gdn_chunk_bwd(const gdn_dims* d, const void* q, const void* k, const void* v
   cudaError_t e = launch_chunk_bwd(a, s);
   if (e == cudaSuccess && norm)
     e = launch_l2norm_bwd(dq, dk, a.res.qn, a.res.kn, a.res.qinv, a.res.kinv, (size_t)d->B * d->T * d->H, d->Dk,
-                          1, s);
+                          a.bf16, s);
   return launch_status(e);
 }
 
@@ -378,7 +377,7 @@ const char* gdn_status_string(int s) {
   switch (s) {
     case GDN_OK: return "ok";
     case GDN_ERR_INVALID_ARG: return "invalid argument (NULL or misaligned pointer, bad size or flag)";
-    case GDN_ERR_UNSUPPORTED: return "unsupported configuration (Dk, Dv in {64, 128}; bf16-only chunked backward)";
+    case GDN_ERR_UNSUPPORTED: return "unsupported configuration (Dk, Dv in {64, 128}; dtype bf16 or fp32)";
     case GDN_ERR_SHAPE: return "T must be a multiple of 64 on the chunked path";
     case GDN_ERR_CUDA: return "CUDA launch or runtime error";
     case GDN_ERR_INTERNAL: return "a kernel reported an error (a bounded wait timed out, or a replay fill count out of range)";

@@ -1,4 +1,5 @@
-// Chunked backward of the gated delta rule (bf16 operands, fp32 state and accumulation).
+// Chunked backward of the gated delta rule (bf16 or fp32 operands, fp32 state and
+// accumulation).
 //
 // Hand-derived from the chunked forward (see chunk_fwd.cu). With dS1 the gradient of the
 // state leaving a chunk and dO the output gradient of its tokens:
@@ -40,10 +41,13 @@ constexpr int DST_CG = DST_THREADS / 128;  // column groups of the state-product
 
 // ------------------------------------------------------------------ reverse state scan
 // One CTA per (batch*head, NTS = 64 value columns), 8 warps; warp w owns gradient rows
-// (w & 3) * Dk/4 .. + Dk/4 and columns 32 (w >> 2) .. + 31 of the slice.
-template <int DK>
+// (w & 3) * Dk/4 .. + Dk/4 and columns 32 (w >> 2) .. + 31 of the slice. bf16 records
+// are double-buffered (the next chunk loads during this one); fp32 records take twice
+// the room, so one stage, loaded at the top of its step.
+template <class T, int DK>
 struct RScanLayout {
-  static constexpr int ES = 2;
+  static constexpr int ES = (int)sizeof(T);
+  static constexpr int STAGES = ES == 2 ? 2 : 1;
   static constexpr int W = 0;                      // -W          [C][DK]
   static constexpr int QH = W + C * DK * ES;       // scale Q-hat [C][DK]
   static constexpr int KT = QH + C * DK * ES;      // K-tilde     [C][DK]
@@ -51,23 +55,22 @@ struct RScanLayout {
   static constexpr int GAM = AQK + C * C * ES;     // float [DK]
   static constexpr int DO = a1k(GAM + DK * 4);     // dO slice    [C][NTS]
   static constexpr int STAGE = a1k(DO + C * NTS * ES);
-  static constexpr int DSS = 2 * STAGE;            // dS operand, transposed [NTS][DK]
+  static constexpr int DSS = STAGES * STAGE;       // dS operand, transposed [NTS][DK]
   static constexpr int DUS = a1k(DSS + DK * NTS * ES);  // dU, transposed  [NTS][C]
   static constexpr int BAR = a1k(DUS + C * NTS * ES);
   static constexpr int BYTES = BAR + 64;
   static constexpr uint32_t TX = (uint32_t)(3 * C * DK * ES + C * C * ES + DK * 4);
 };
 
-template <int DK, int DV>
+template <class T, int DK, int DV>
 __global__ void __launch_bounds__(RSCAN_THREADS) chunk_scan_bwd_kernel(ChunkBwdArgs a) {
-  typedef bf16 T;
-  typedef RScanLayout<DK> L;
+  typedef RScanLayout<T, DK> L;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = align1024(smem_raw);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int tile = blockIdx.x, bh = blockIdx.y, b = bh / a.H, h = bh % a.H;
   const int N = a.T / C;
-  constexpr int MTS = DK / 64, EPC = 8;
+  constexpr int MTS = DK / 64, EPC = 16 / (int)sizeof(T), STAGES = L::STAGES;
   const int rg = warp & 3, cg = warp >> 2;
   const int srow = rg * 16 * MTS, col0 = 32 * cg;
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + L::BAR);
@@ -88,8 +91,7 @@ __global__ void __launch_bounds__(RSCAN_THREADS) chunk_scan_bwd_kernel(ChunkBwdA
         dS[mt][nt][e] = a.dh_final ? a.dh_final[sb + (size_t)r * DV + c] : 0.f;
       }
   if (tid == 0) {
-    mbar_init(&bars[0], 1);
-    mbar_init(&bars[1], 1);
+    for (int i = 0; i < STAGES; ++i) mbar_init(&bars[i], 1);
     fence_mbar_init();
   }
   __syncthreads();
@@ -99,10 +101,10 @@ __global__ void __launch_bounds__(RSCAN_THREADS) chunk_scan_bwd_kernel(ChunkBwdA
     const size_t ch = (size_t)bh * N + n;
     if (tid == 0) {
       mbar_arrive_expect_tx(&bars[s], L::TX);
-      bulk_g2s(st + L::W, static_cast<const T*>(a.res.wneg) + ch * (C * DK), C * DK * 2, &bars[s]);
-      bulk_g2s(st + L::QH, static_cast<const T*>(a.res.qh) + ch * (C * DK), C * DK * 2, &bars[s]);
-      bulk_g2s(st + L::KT, static_cast<const T*>(a.res.kt) + ch * (C * DK), C * DK * 2, &bars[s]);
-      bulk_g2s(st + L::AQK, static_cast<const T*>(a.res.aqk) + ch * (C * C), C * C * 2, &bars[s]);
+      bulk_g2s(st + L::W, static_cast<const T*>(a.res.wneg) + ch * (C * DK), C * DK * L::ES, &bars[s]);
+      bulk_g2s(st + L::QH, static_cast<const T*>(a.res.qh) + ch * (C * DK), C * DK * L::ES, &bars[s]);
+      bulk_g2s(st + L::KT, static_cast<const T*>(a.res.kt) + ch * (C * DK), C * DK * L::ES, &bars[s]);
+      bulk_g2s(st + L::AQK, static_cast<const T*>(a.res.aqk) + ch * (C * C), C * C * L::ES, &bars[s]);
       bulk_g2s(st + L::GAM, a.res.gam + ch * DK, DK * 4, &bars[s]);
     }
     Tile<T, C, NTS> dOt{reinterpret_cast<T*>(st + L::DO)};
@@ -113,13 +115,15 @@ __global__ void __launch_bounds__(RSCAN_THREADS) chunk_scan_bwd_kernel(ChunkBwdA
     }
     cp_async_commit();
   };
-  if (N > 0) issue(N - 1, 0);
+  // step it works on chunk N - 1 - it in stage it % STAGES; its loads were issued
+  // STAGES - 1 steps earlier
+  for (int i = 0; i < STAGES - 1 && i < N; ++i) issue(N - 1 - i, i);
 
   for (int it = 0; it < N; ++it) {
-    const int n = N - 1 - it, s = it & 1;
-    const uint32_t par = (uint32_t)(it >> 1) & 1u;
-    const bool more = it + 1 < N;
-    if (more) issue(n - 1, s ^ 1);
+    const int n = N - 1 - it, s = it % STAGES;
+    const uint32_t par = (uint32_t)(it / STAGES) & 1u;
+    const bool more = STAGES > 1 && it + 1 < N;  // a later chunk's dO group is in flight
+    if (it + STAGES - 1 < N) issue(n - (STAGES - 1), (it + STAGES - 1) % STAGES);
     uint8_t* st = sm + s * L::STAGE;
     Tile<T, C, DK> Wt{reinterpret_cast<T*>(st + L::W)};
     Tile<T, C, DK> Qt{reinterpret_cast<T*>(st + L::QH)};
@@ -172,7 +176,7 @@ __global__ void __launch_bounds__(RSCAN_THREADS) chunk_scan_bwd_kernel(ChunkBwdA
   }
   cp_async_wait<0>();
   if (tid == 0) {  // every load landed and the residual stores complete before the CTA retires
-    drain_ring(bars, 2, N);
+    drain_ring(bars, STAGES, N);
     bulk_wait0();
   }
   if (a.dh0) {
@@ -196,37 +200,38 @@ __global__ void __launch_bounds__(RSCAN_THREADS) chunk_scan_bwd_kernel(ChunkBwdA
 // dBk = -Y S0^T, dK-tilde = U dS1^T, dAkk = -Y U^T (j < t), dgam = rowsum(dS1 * S0).
 // The products without the reverse scan's results, after the CUDA-core scan (the
 // tensor-core scan runs them as extra CTAs of its own launch).
-template <int DK, int DV>
-__global__ void __launch_bounds__(DQA_THREADS, 2) chunk_dqa_kernel(ChunkBwdArgs a) {
+template <class T, int DK, int DV>
+__global__ void __launch_bounds__(DQA_THREADS, sizeof(T) == 2 ? 2 : 1) chunk_dqa_kernel(ChunkBwdArgs a) {
   pdl_wait();
   pdl_trigger();
   extern __shared__ uint8_t smem_raw[];
-  dqa_units<DK, DV>(a, align1024(smem_raw), blockIdx.x, gridDim.x, threadIdx.x);
+  dqa_units<T, DK, DV>(a, align1024(smem_raw), blockIdx.x, gridDim.x, threadIdx.x);
 }
 
-template <int DK, int DV>
+template <class T, int DK, int DV>
 struct DstLayout {
-  static constexpr int TM = 0;                       // T     [C][C]
-  static constexpr int V = a1k(TM + C * C * 2);      // v     [C][DV], then dv; then S0^T panel 1
-  static constexpr int U = a1k(V + C * DV * 2);      // U^T   [DV][C]
-  static constexpr int DU = a1k(U + C * DV * 2);     // dU^T  [DV][C], then Y [C][DV]
-  static constexpr int S0P = a1k(DU + C * DV * 2);   // S0^T  [DV][64], one 64-channel panel
-  static constexpr int DSP = a1k(S0P + DV * 64 * 2); // dS1^T [DV][64], one 64-channel panel
-  static constexpr int BETA = a1k(DSP + DV * 64 * 2);
+  static constexpr int ES = (int)sizeof(T);
+  static constexpr int TM = 0;                        // T     [C][C]
+  static constexpr int V = a1k(TM + C * C * ES);      // v     [C][DV], then dv; then S0^T panel 1
+  static constexpr int U = a1k(V + C * DV * ES);      // U^T   [DV][C]
+  static constexpr int DU = a1k(U + C * DV * ES);     // dU^T  [DV][C], then Y [C][DV]
+  static constexpr int S0P = a1k(DU + C * DV * ES);   // S0^T  [DV][64], one 64-channel panel
+  static constexpr int DSP = a1k(S0P + DV * 64 * ES); // dS1^T [DV][64], one 64-channel panel
+  static constexpr int BETA = a1k(DSP + DV * 64 * ES);
   static constexpr int DB = BETA + C * 4;            // float [DST_CG][C]
   static constexpr int GQ = DB + DST_CG * C * 4;     // float [DST_THREADS / 32][DK] dgam partials
   static constexpr int BYTES = GQ + (DST_THREADS / 32) * DK * 4;
 };
 
-// Two CTAs per SM: while one computes, the other's loads are in flight. The state and
-// state-gradient records are taken one 64-channel panel (16 KiB each) at a time; the
-// second S0^T panel is prefetched into v's buffer as soon as dv has left it.
-template <int DK, int DV>
-__global__ void __launch_bounds__(DST_THREADS, 2) chunk_dstate_kernel(ChunkBwdArgs a) {
+// Two CTAs per SM with bf16 records (one with fp32): while one computes, the other's
+// loads are in flight. The state and state-gradient records are taken one 64-channel
+// panel at a time; the second S0^T panel is prefetched into v's buffer as soon as dv has
+// left it.
+template <class T, int DK, int DV>
+__global__ void __launch_bounds__(DST_THREADS, sizeof(T) == 2 ? 2 : 1) chunk_dstate_kernel(ChunkBwdArgs a) {
   pdl_wait();
   pdl_trigger();
-  typedef bf16 T;
-  typedef DstLayout<DK, DV> L;
+  typedef DstLayout<T, DK, DV> L;
   constexpr int NPAN = DK / 64;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = align1024(smem_raw);
@@ -234,7 +239,7 @@ __global__ void __launch_bounds__(DST_THREADS, 2) chunk_dstate_kernel(ChunkBwdAr
   const int n = blockIdx.x, bh = blockIdx.y, b = bh / a.H, h = bh % a.H;
   const int N = a.T / C;
   const size_t ch = (size_t)bh * N + n;
-  constexpr int EPC = 8;
+  constexpr int EPC = 16 / (int)sizeof(T);
   Tile<T, C, C> Ts{reinterpret_cast<T*>(sm + L::TM)};
   Tile<T, C, DV> Vs{reinterpret_cast<T*>(sm + L::V)};
   Tile<T, DV, C> Us{reinterpret_cast<T*>(sm + L::U)};    // U^T
@@ -372,10 +377,9 @@ __global__ void __launch_bounds__(DST_THREADS, 2) chunk_dstate_kernel(ChunkBwdAr
     float acc0 = 0.f, acc1 = 0.f;
 #pragma unroll
     for (int v2 = vq * VQ; v2 < (vq + 1) * VQ; ++v2) {
-      const __nv_bfloat162 x = *reinterpret_cast<const __nv_bfloat162*>(ds1.ptr(v2, c));
-      const __nv_bfloat162 z = *reinterpret_cast<const __nv_bfloat162*>(s0.ptr(v2, c));
-      acc0 = fmaf(__low2float(x), __low2float(z), acc0);
-      acc1 = fmaf(__high2float(x), __high2float(z), acc1);
+      const float2 x = ld2(ds1.ptr(v2, c)), z = ld2(s0.ptr(v2, c));
+      acc0 = fmaf(x.x, z.x, acc0);
+      acc1 = fmaf(x.y, z.y, acc1);
     }
     gq[vq * DK + 64 * p + c] = acc0;
     gq[vq * DK + 64 * p + c + 1] = acc1;
@@ -413,20 +417,21 @@ __global__ void __launch_bounds__(DST_THREADS, 2) chunk_dstate_kernel(ChunkBwdAr
   }
 }
 
-template <int DK, int DV>
+template <class T, int DK, int DV>
 cudaError_t launch_bwd_t(const ChunkBwdArgs& a, cudaStream_t s) {
   const int N = a.T / C, BH = a.B * a.H;
+  const int bf16_ops = sizeof(T) == 2;
   cudaError_t e;
-  // Dk = Dv = 128: the tensor-core reverse scan, then one fused tensor-core kernel for
-  // every chunk product and gradient (chunk_bwd_tc.cu). Dk = 64: the CUDA-core scan, then
-  // the products that need no scan result (chunk_dqa.cuh), the state products, the score
-  // gradients and the channel-group sums.
-  const bool tc = scan_tc_applies(1, DK, DV);
+  // bf16 with Dk = Dv = 128: the tensor-core reverse scan, then one fused tensor-core
+  // kernel for every chunk product and gradient (chunk_bwd_tc.cu). Otherwise (Dk = 64, or
+  // fp32 operands): the CUDA-core scan, then the products that need no scan result
+  // (chunk_dqa.cuh), the state products, the score gradients and the channel-group sums.
+  const bool tc = scan_tc_applies(bf16_ops, DK, DV);
   if (tc) {
     if ((e = launch_scan_bwd_tc(a, s)) != cudaSuccess) return e;
   } else {
-    const int bytes = RScanLayout<DK>::BYTES + 1024;
-    auto kern = chunk_scan_bwd_kernel<DK, DV>;
+    const int bytes = RScanLayout<T, DK>::BYTES + 1024;
+    auto kern = chunk_scan_bwd_kernel<T, DK, DV>;
     if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes)) != cudaSuccess) return e;
     prof_mark(K_SCAN_BWD, s, true);
     kern<<<dim3(DV / NTS, BH), RSCAN_THREADS, bytes, s>>>(a);
@@ -434,18 +439,18 @@ cudaError_t launch_bwd_t(const ChunkBwdArgs& a, cudaStream_t s) {
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   if (N == 0) return cudaSuccess;
-  if (bwd_tc_applies(DK, DV)) return launch_chunk_bwd_tc(a, s);
+  if (bf16_ops && bwd_tc_applies(DK, DV)) return launch_chunk_bwd_tc(a, s);
   if (!tc) {
-    const int bytes = DqaLayout<DK, DV>::BYTES + 1024;
-    auto kern = chunk_dqa_kernel<DK, DV>;
+    const int bytes = DqaLayout<T, DK, DV>::BYTES + 1024;
+    auto kern = chunk_dqa_kernel<T, DK, DV>;
     if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes)) != cudaSuccess) return e;
     prof_mark(K_DQA, s, true);
     if ((e = launch_pdl(kern, dim3(N * BH), dim3(DQA_THREADS), bytes, s, a)) != cudaSuccess) return e;
     prof_mark(K_DQA, s, false);
   }
   {
-    const int bytes = DstLayout<DK, DV>::BYTES + 1024;
-    auto kern = chunk_dstate_kernel<DK, DV>;
+    const int bytes = DstLayout<T, DK, DV>::BYTES + 1024;
+    auto kern = chunk_dstate_kernel<T, DK, DV>;
     if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes)) != cudaSuccess) return e;
     prof_mark(K_DSTATE, s, true);
     if ((e = launch_pdl(kern, dim3(N, BH), dim3(DST_THREADS), bytes, s, a)) != cudaSuccess) return e;
@@ -454,12 +459,17 @@ cudaError_t launch_bwd_t(const ChunkBwdArgs& a, cudaStream_t s) {
   return launch_chunk_grads(a, s);
 }
 
+template <class T>
+cudaError_t launch_bwd_dims(const ChunkBwdArgs& a, cudaStream_t s) {
+  if (a.DK == 64) return a.DV == 64 ? launch_bwd_t<T, 64, 64>(a, s) : launch_bwd_t<T, 64, 128>(a, s);
+  return a.DV == 64 ? launch_bwd_t<T, 128, 64>(a, s) : launch_bwd_t<T, 128, 128>(a, s);
+}
+
 }  // namespace
 
 cudaError_t launch_chunk_bwd(const ChunkBwdArgs& a, cudaStream_t s) {
   if (a.B * a.H == 0) return cudaSuccess;
-  if (a.DK == 64) return a.DV == 64 ? launch_bwd_t<64, 64>(a, s) : launch_bwd_t<64, 128>(a, s);
-  return a.DV == 64 ? launch_bwd_t<128, 64>(a, s) : launch_bwd_t<128, 128>(a, s);
+  return a.bf16 ? launch_bwd_dims<bf16>(a, s) : launch_bwd_dims<float>(a, s);
 }
 
 }  // namespace gdn

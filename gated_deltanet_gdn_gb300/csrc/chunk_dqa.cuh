@@ -1,8 +1,8 @@
 // The chunk products of the backward that need only forward records and dO:
 //   dQ-hat = scale dO S0^T  and  dAqk = scale (dO U^T) masked j <= t
 // (chunked WY backward, see chunk_bwd.cu), as a kernel of their own after the CUDA-core
-// reverse scan (Dk = 64; at Dk = Dv = 128 the fused tensor-core kernel of chunk_bwd_tc.cu
-// computes them with the other chunk products).
+// reverse scan (Dk = 64, or fp32 operands; with bf16 at Dk = Dv = 128 the fused
+// tensor-core kernel of chunk_bwd_tc.cu computes them with the other chunk products).
 #pragma once
 
 #include "common.cuh"
@@ -17,22 +17,22 @@ constexpr int DQA_CG = DQA_THREADS / 128;  // column groups (4 row groups of war
 // The DQA_THREADS threads of the kernel synchronise on named barrier 2.
 __device__ __forceinline__ void dqa_sync() { asm volatile("bar.sync 2, 256;\n" ::: "memory"); }
 
-template <int DK, int DV>
+template <class T, int DK, int DV>
 struct DqaLayout {
-  static constexpr int DO = 0;                       // dO    [C][DV]
-  static constexpr int U = a1k(DO + C * DV * 2);     // U^T   [DV][C]
-  static constexpr int S0 = a1k(U + C * DV * 2);     // S0^T  [DV][DK], as 64-channel panels
-  static constexpr int BYTES = a1k(S0 + DV * DK * 2);
+  static constexpr int ES = (int)sizeof(T);
+  static constexpr int DO = 0;                        // dO    [C][DV]
+  static constexpr int U = a1k(DO + C * DV * ES);     // U^T   [DV][C]
+  static constexpr int S0 = a1k(U + C * DV * ES);     // S0^T  [DV][DK], as 64-channel panels
+  static constexpr int BYTES = a1k(S0 + DV * DK * ES);
 };
 
 // Chunk-heads unit0, unit0 + stride, ... Called by threads 0 .. DQA_THREADS - 1 of a CTA;
 // sm is its 1024-byte aligned shared memory.
-template <int DK, int DV>
+template <class T, int DK, int DV>
 __device__ __forceinline__ void dqa_units(const ChunkBwdArgs& a, uint8_t* sm, int unit0, int stride, int tid) {
-  typedef bf16 T;
-  typedef DqaLayout<DK, DV> L;
+  typedef DqaLayout<T, DK, DV> L;
   constexpr int NPAN = DK / 64;
-  constexpr int EPC = 8;
+  constexpr int EPC = 16 / (int)sizeof(T);
   const int lane = tid & 31, warp = tid >> 5;
   const int N = a.T / C, units = N * a.B * a.H;
 #pragma unroll 1

@@ -1,4 +1,5 @@
-// Chunk-parallel gradients of the chunked gated delta rule backward (bf16 operands).
+// Chunk-parallel gradients of the chunked gated delta rule backward (bf16 or fp32
+// operands, fp32 arithmetic).
 //
 // One CTA per (64-channel group, chunk, batch*head). Inputs: q, k, g, beta of the
 // chunk and the state products dQ-hat, dBk, dK-tilde, dAqk, dAkk, dgam written by
@@ -23,22 +24,24 @@ namespace gdn {
 namespace {
 
 constexpr int GR_THREADS = 256;
-constexpr int HC = 64;  // channels per CTA (one 128-byte panel of a bf16 C x Dk record)
+constexpr int HC = 64;  // channels per CTA (one 128-byte panel of a bf16 C x Dk record, two of fp32)
 
+template <class T>
 struct GrLayout {
+  static constexpr int ES = (int)sizeof(T);
   static constexpr int GLD = HC + 8;                  // padded fp32 row
   static constexpr int G = 0;                         // float [C][GLD]
   static constexpr int Q = a1k(G + C * GLD * 4);      // q     [C][HC]
-  static constexpr int K = a1k(Q + C * HC * 2);       // k     [C][HC]
-  static constexpr int X = a1k(K + C * HC * 2);       // query-side rows q e1
-  static constexpr int XB = X + C * HC * 2;           // query-side rows beta k e1
-  static constexpr int Y = a1k(XB + C * HC * 2);      // key-side rows k e2
-  static constexpr int DQH = a1k(Y + C * HC * 2);     // dQ-hat   [C][HC]
-  static constexpr int DBK = a1k(DQH + C * HC * 2);   // dBk      [C][HC]
-  static constexpr int DKT = a1k(DBK + C * HC * 2);   // dK-tilde [C][HC]
-  static constexpr int DAQ = a1k(DKT + C * HC * 2);   // dAqk [C][C]
-  static constexpr int DAK = a1k(DAQ + C * C * 2);    // dAkk [C][C]
-  static constexpr int BETA = a1k(DAK + C * C * 2);   // float [C]
+  static constexpr int K = a1k(Q + C * HC * ES);      // k     [C][HC]
+  static constexpr int X = a1k(K + C * HC * ES);      // query-side rows q e1
+  static constexpr int XB = X + C * HC * ES;          // query-side rows beta k e1
+  static constexpr int Y = a1k(XB + C * HC * ES);     // key-side rows k e2
+  static constexpr int DQH = a1k(Y + C * HC * ES);    // dQ-hat   [C][HC]
+  static constexpr int DBK = a1k(DQH + C * HC * ES);  // dBk      [C][HC]
+  static constexpr int DKT = a1k(DBK + C * HC * ES);  // dK-tilde [C][HC]
+  static constexpr int DAQ = a1k(DKT + C * HC * ES);  // dAqk [C][C]
+  static constexpr int DAK = a1k(DAQ + C * C * ES);   // dAkk [C][C]
+  static constexpr int BETA = a1k(DAK + C * C * ES);  // float [C]
   static constexpr int DIAG = BETA + C * 4;           // float [C] diagonal of dAqk
   static constexpr int DBS = DIAG + C * 4;            // float [2][C] dbeta partials
   static constexpr int COLS = DBS + 2 * C * 4;        // float [4][HC] K-tilde column partials
@@ -46,15 +49,17 @@ struct GrLayout {
   static constexpr int GSC = GCOL + HC * 4;           // float [C] scalar decay per token
   static constexpr int BYTES = GSC + C * 4;
   static constexpr int DG = X;                        // float [C][HC] dG staging over X and XB
-  static_assert(XB - X == C * HC * 2, "dG staging spans X and XB");
+  static_assert(2 * C * HC * ES >= C * HC * 4 && XB - X == C * HC * ES, "dG staging spans X and XB");
 };
 
-typedef Tile<bf16, C, HC> HTile;
+template <class T>
+using HTile = Tile<T, C, HC>;
 
 // sum over j in [j0, j1] of dP(r, j) y(j, c) exp(G(r,c) - G(j,c)) (in-block x side)
-__device__ __noinline__ float pw_dx(const Tile<bf16, C, C>* dP, const HTile* ys, const float* G, int r, int c,
+template <class T>
+__device__ __noinline__ float pw_dx(const Tile<T, C, C>* dP, const HTile<T>* ys, const float* G, int r, int c,
                                     int j0, int j1) {
-  constexpr int LD = GrLayout::GLD;
+  constexpr int LD = GrLayout<T>::GLD;
   const float Gr = G[r * LD + c];
   float s = 0.f;
   for (int j = j0; j <= j1; ++j)
@@ -62,9 +67,10 @@ __device__ __noinline__ float pw_dx(const Tile<bf16, C, C>* dP, const HTile* ys,
   return s;
 }
 // sum over t in [t0, t1] of dP(t, j) w_t x(t, c) exp(G(t,c) - G(j,c)) (in-block y side)
-__device__ __noinline__ float pw_dy(const Tile<bf16, C, C>* dP, const HTile* xs, const float* w, const float* G,
+template <class T>
+__device__ __noinline__ float pw_dy(const Tile<T, C, C>* dP, const HTile<T>* xs, const float* w, const float* G,
                                     int j, int c, int t0, int t1) {
-  constexpr int LD = GrLayout::GLD;
+  constexpr int LD = GrLayout<T>::GLD;
   const float Gj = G[j * LD + c];
   float s = 0.f;
   for (int t = t0; t <= t1; ++t) {
@@ -74,12 +80,13 @@ __device__ __noinline__ float pw_dy(const Tile<bf16, C, C>* dP, const HTile* xs,
   return s;
 }
 
-template <bool PC>
-__global__ void __launch_bounds__(GR_THREADS, 2) chunk_grads_kernel(ChunkBwdArgs a) {
+// bf16: two CTAs per SM; fp32 tiles take one SM's shared memory, so all registers are free
+template <class T, bool PC>
+__global__ void __launch_bounds__(GR_THREADS, sizeof(T) == 2 ? 2 : 1) chunk_grads_kernel(ChunkBwdArgs a) {
   pdl_wait();
   pdl_trigger();
-  typedef bf16 T;
-  typedef GrLayout L;
+  typedef GrLayout<T> L;
+  typedef HTile<T> HT;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = align1024(smem_raw);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -89,16 +96,16 @@ __global__ void __launch_bounds__(GR_THREADS, 2) chunk_grads_kernel(ChunkBwdArgs
   const size_t row0 = ((size_t)b * a.T + (size_t)n * C) * a.H + h;
   const size_t rs = a.H;
   const int cbase = grp * HC;  // first channel of this CTA
-  constexpr int EPC = 8;
+  constexpr int EPC = 16 / (int)sizeof(T);
   float* Gp = reinterpret_cast<float*>(sm + L::G);
   auto Gat = [&](int r, int c) -> float& { return Gp[r * L::GLD + c]; };
-  HTile Qs{reinterpret_cast<T*>(sm + L::Q)};
-  HTile Ks{reinterpret_cast<T*>(sm + L::K)};
-  HTile Xs{reinterpret_cast<T*>(sm + L::X)};
-  HTile Ys{reinterpret_cast<T*>(sm + L::Y)};
-  HTile dQh{reinterpret_cast<T*>(sm + L::DQH)};
-  HTile dBk{reinterpret_cast<T*>(sm + L::DBK)};
-  HTile dKt{reinterpret_cast<T*>(sm + L::DKT)};
+  HT Qs{reinterpret_cast<T*>(sm + L::Q)};
+  HT Ks{reinterpret_cast<T*>(sm + L::K)};
+  HT Xs{reinterpret_cast<T*>(sm + L::X)};
+  HT Ys{reinterpret_cast<T*>(sm + L::Y)};
+  HT dQh{reinterpret_cast<T*>(sm + L::DQH)};
+  HT dBk{reinterpret_cast<T*>(sm + L::DBK)};
+  HT dKt{reinterpret_cast<T*>(sm + L::DKT)};
   Tile<T, C, C> dAq{reinterpret_cast<T*>(sm + L::DAQ)};
   Tile<T, C, C> dAk{reinterpret_cast<T*>(sm + L::DAK)};
   float* beta_s = reinterpret_cast<float*>(sm + L::BETA);
@@ -133,7 +140,7 @@ __global__ void __launch_bounds__(GR_THREADS, 2) chunk_grads_kernel(ChunkBwdArgs
   }
   cp_async_commit();
   {
-    // the C x Dk records are 64-column panels: this CTA's panel is contiguous
+    // the C x Dk records are column panels of 128 bytes: this CTA's 64 columns are contiguous
     const size_t pan = ch * (C * (size_t)DK) + (size_t)grp * C * HC;
     const T* s1 = static_cast<const T*>(a.ws.dqh) + pan;
     const T* s2 = static_cast<const T*>(a.ws.dbk) + pan;
@@ -191,7 +198,7 @@ __global__ void __launch_bounds__(GR_THREADS, 2) chunk_grads_kernel(ChunkBwdArgs
 
   // row-scaled operands, one pass: X = q e1, XB = beta k e1 (query side), Y = k e2 (key side),
   // with e1 = exp(G - G_b), e2 = exp(G_b - G) about the block boundary b
-  HTile XBs{reinterpret_cast<T*>(sm + L::XB)};
+  HT XBs{reinterpret_cast<T*>(sm + L::XB)};
   static_assert(C * (HC / 4) % GR_THREADS == 0, "whole passes");
 #pragma unroll
   for (int i = tid; i < C * (HC / 4); i += GR_THREADS) {
@@ -222,11 +229,9 @@ __global__ void __launch_bounds__(GR_THREADS, 2) chunk_grads_kernel(ChunkBwdArgs
       if (j < t) {
         const float Gt = Gat(t, 0);
         const float e0 = __expf(Gt - gsc_cum(j)), e1 = j + 1 < t ? __expf(Gt - gsc_cum(j + 1)) : 0.f;
-        __nv_bfloat162* pq = reinterpret_cast<__nv_bfloat162*>(dAq.ptr(t, j));
-        __nv_bfloat162* pk = reinterpret_cast<__nv_bfloat162*>(dAk.ptr(t, j));
-        const float2 fq = __bfloat1622float2(*pq), fk = __bfloat1622float2(*pk);
-        *pq = __floats2bfloat162_rn(fq.x * e0, j + 1 < t ? fq.y * e1 : fq.y);
-        *pk = __floats2bfloat162_rn(fk.x * e0, j + 1 < t ? fk.y * e1 : fk.y);
+        const float2 fq = ld2(dAq.ptr(t, j)), fk = ld2(dAk.ptr(t, j));
+        store2(dAq.ptr(t, j), fq.x * e0, j + 1 < t ? fq.y * e1 : fq.y);
+        store2(dAk.ptr(t, j), fk.x * e0, j + 1 < t ? fk.y * e1 : fk.y);
       }
     }
   }
@@ -296,21 +301,15 @@ __global__ void __launch_bounds__(GR_THREADS, 2) chunk_grads_kernel(ChunkBwdArgs
       for (int e = 0; e < 4; e += 2) {
         const int r = m0 + frag_row(lane, e);
         const float2 G2 = *reinterpret_cast<const float2*>(&Gat(r, c));
-        const __nv_bfloat162 k2 = *reinterpret_cast<const __nv_bfloat162*>(Ks.ptr(r, c));
-        const __nv_bfloat162 q2 = *reinterpret_cast<const __nv_bfloat162*>(Qs.ptr(r, c));
-        const __nv_bfloat162 h2 = *reinterpret_cast<const __nv_bfloat162*>(dQh.ptr(r, c));
-        const __nv_bfloat162 b2 = *reinterpret_cast<const __nv_bfloat162*>(dBk.ptr(r, c));
-        const __nv_bfloat162 t2 = *reinterpret_cast<const __nv_bfloat162*>(dKt.ptr(r, c));
+        const float2 k2 = ld2(Ks.ptr(r, c)), q2 = ld2(Qs.ptr(r, c)), h2 = ld2(dQh.ptr(r, c));
+        const float2 b2 = ld2(dBk.ptr(r, c)), t2 = ld2(dKt.ptr(r, c));
         const float br = beta_s[r], dg = diag_s[r];
         float oq[2], ok[2];
 #pragma unroll
         for (int u = 0; u < 2; ++u) {
           const float G = u ? G2.y : G2.x, Gb = u ? gb.y : gb.x, GC = u ? gc.y : gc.x;
-          const float kf = u ? __high2float(k2) : __low2float(k2);
-          const float qf = u ? __high2float(q2) : __low2float(q2);
-          const float dqh = u ? __high2float(h2) : __low2float(h2);
-          const float dbk = u ? __high2float(b2) : __low2float(b2);
-          const float dkt = u ? __high2float(t2) : __low2float(t2);
+          const float kf = u ? k2.y : k2.x, qf = u ? q2.y : q2.x;
+          const float dqh = u ? h2.y : h2.x, dbk = u ? b2.y : b2.x, dkt = u ? t2.y : t2.x;
           const float e1 = MASK ? 1.f : __expf(G - Gb), e2 = MASK ? 1.f : __expf(Gb - G);
           const float gm = MASK ? rgm[e >> 1] : FAST ? eb[u] * e1 : __expf(G);
           const float kd = MASK ? rkd[e >> 1] : FAST ? ecb[u] * e2 : __expf(GC - G);
@@ -416,7 +415,7 @@ __global__ void __launch_bounds__(GR_THREADS, 2) chunk_grads_kernel(ChunkBwdArgs
 }
 
 // dbeta = dbeta_v + the channel groups' partials (and scalar-decay dg), fixed order.
-template <bool PC>
+template <class T, bool PC>
 __global__ void chunk_bwd_finalize_kernel(ChunkBwdArgs a) {
   pdl_wait();
   pdl_trigger();
@@ -430,22 +429,20 @@ __global__ void chunk_bwd_finalize_kernel(ChunkBwdArgs a) {
     const size_t row = ((size_t)b * a.T + (size_t)n * C + t) * a.H + h;
     float db = a.ws.dbv[ch * C + t] + a.ws.dbpart[(ch * 2) * C + t];
     if (NGRP > 1) db += a.ws.dbpart[(ch * 2 + 1) * C + t];
-    static_cast<bf16*>(a.dbeta)[row] = from_f32<bf16>(db);
+    static_cast<T*>(a.dbeta)[row] = from_f32<T>(db);
     if (!PC) {
       float s = a.ws.dgpart[(ch * 2) * C + t];
       if (NGRP > 1) s += a.ws.dgpart[(ch * 2 + 1) * C + t];
-      static_cast<bf16*>(a.dg)[row] = from_f32<bf16>(s);
+      static_cast<T*>(a.dg)[row] = from_f32<T>(s);
     }
   }
 }
 
-}  // namespace
-
-cudaError_t launch_chunk_grads(const ChunkBwdArgs& a, cudaStream_t s) {
-  if (a.B * a.H == 0 || a.T == 0) return cudaSuccess;
+template <class T>
+cudaError_t launch_grads_t(const ChunkBwdArgs& a, cudaStream_t s) {
   const int N = a.T / C, BH = a.B * a.H;
-  const int bytes = GrLayout::BYTES + 1024;
-  auto kern = a.per_channel ? chunk_grads_kernel<true> : chunk_grads_kernel<false>;
+  const int bytes = GrLayout<T>::BYTES + 1024;
+  auto kern = a.per_channel ? chunk_grads_kernel<T, true> : chunk_grads_kernel<T, false>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
   if (e != cudaSuccess) return e;
   prof_mark(K_GRADS, s, true);
@@ -454,10 +451,17 @@ cudaError_t launch_chunk_grads(const ChunkBwdArgs& a, cudaStream_t s) {
   const size_t total = (size_t)BH * a.T;
   const int blocks = (int)((total + 255) / 256 < 4096 ? (total + 255) / 256 : 4096);
   prof_mark(K_FINALIZE, s, true);
-  e = launch_pdl(a.per_channel ? chunk_bwd_finalize_kernel<true> : chunk_bwd_finalize_kernel<false>, dim3(blocks),
-                 dim3(256), 0, s, a);
+  e = launch_pdl(a.per_channel ? chunk_bwd_finalize_kernel<T, true> : chunk_bwd_finalize_kernel<T, false>,
+                 dim3(blocks), dim3(256), 0, s, a);
   prof_mark(K_FINALIZE, s, false);
   return e;
+}
+
+}  // namespace
+
+cudaError_t launch_chunk_grads(const ChunkBwdArgs& a, cudaStream_t s) {
+  if (a.B * a.H == 0 || a.T == 0) return cudaSuccess;
+  return a.bf16 ? launch_grads_t<bf16>(a, s) : launch_grads_t<float>(a, s);
 }
 
 }  // namespace gdn

@@ -544,6 +544,11 @@ __device__ __forceinline__ void drain_ring(uint64_t* bars, int stages, int count
 __device__ __forceinline__ void copy16(void* dst, const void* src) {
   *reinterpret_cast<uint4*>(dst) = *reinterpret_cast<const uint4*>(src);
 }
+// Two consecutive elements (4 bytes of bf16, 8 bytes of fp32) as floats.
+__device__ __forceinline__ float2 ld2(const bf16* p) {
+  return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(p));
+}
+__device__ __forceinline__ float2 ld2(const float* p) { return *reinterpret_cast<const float2*>(p); }
 // Four consecutive elements (8 bytes of bf16, 16 bytes of fp32) as floats.
 __device__ __forceinline__ void ld4(float (&x)[4], const bf16* p) {
   const uint2 u = *reinterpret_cast<const uint2*>(p);

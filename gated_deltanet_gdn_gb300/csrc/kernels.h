@@ -104,9 +104,10 @@ inline BwdWorkspaceLayout bwd_workspace_layout(int B, int T, int H, int DK, int 
   };
   put(L.du, L.du_b);
   put(L.dstate, L.dstate_b);
-  // Dk = Dv = 128 runs the fused chunk-gradient kernel (chunk_bwd_tc.cu), which needs only
-  // dU and dS from the reverse scan; the other regions serve the Dk = 64 kernels
-  if (DK == 128 && DV == 128) {
+  // bf16 with Dk = Dv = 128 runs the fused chunk-gradient kernel (chunk_bwd_tc.cu), which
+  // needs only dU and dS from the reverse scan; the other regions serve the CUDA-core
+  // kernels (Dk = 64, or fp32 operands)
+  if (es == 2 && DK == 128 && DV == 128) {
     L.total = off;
     return L;
   }
@@ -231,7 +232,7 @@ cudaError_t launch_scan_bwd_tc(const ChunkBwdArgs& a, cudaStream_t s);
 // The chunk preparation on tcgen05 (chunk_prep_tc.cu), bf16 operands with Dk = Dv = 128.
 bool prep_tc_applies(int bf16_operands, int DK, int DV);
 cudaError_t launch_chunk_prep_tc(const ChunkFwdArgs& a, cudaStream_t s);
-// The fused chunk-gradient kernel on tcgen05 (chunk_bwd_tc.cu), for Dk = Dv = 128 (bf16);
+// The fused chunk-gradient kernel on tcgen05 (chunk_bwd_tc.cu), for bf16 with Dk = Dv = 128;
 // it needs only the du and dstate parts of the backward workspace.
 bool bwd_tc_applies(int DK, int DV);
 cudaError_t launch_chunk_bwd_tc(const ChunkBwdArgs& a, cudaStream_t s);

@@ -45,9 +45,8 @@
  *   GDN_ERR_INVALID_ARG  NULL dims or required pointer, negative sizes, a
  *                        pointer not aligned to 16 bytes, scale not finite
  *   GDN_ERR_UNSUPPORTED  Dk or Dv not in {64, 128} (each on its own: Dk != Dv
- *                        is supported everywhere), unknown dtype, a float32
- *                        chunked backward (the chunked backward is bfloat16
- *                        only), B * H > 65535
+ *                        is supported everywhere), unknown dtype,
+ *                        B * H > 65535
  *   GDN_ERR_SHAPE        chunked calls with T not a multiple of 64
  *   GDN_ERR_CUDA         a launch was rejected (cudaGetLastError); faults that
  *                        happen later surface at the caller's next
@@ -156,8 +155,9 @@ int gdn_chunk_fwd(const gdn_dims* dims, const void* q, const void* k, const void
  * Same inputs as the forward plus the residuals it wrote, dout [B,T,H,Dv] and
  * dh_final (NULL = zeros). Writes dq, dk, dv, dg, dbeta and dh0 (may be NULL).
  * workspace: gdn_chunk_bwd_workspace_bytes(dims) bytes, 256-byte aligned,
- * caller-owned, overwritten. bfloat16 only (dims.dtype == GDN_BF16); errors as
- * listed at the top of this file. */
+ * caller-owned, overwritten. dims.dtype is that of the forward call that wrote
+ * the residuals (bfloat16 or float32 operands; the state gradient is fp32 in
+ * both); errors as listed at the top of this file. */
 int gdn_chunk_bwd(const gdn_dims* dims, const void* q, const void* k, const void* v,
                   const void* g, const void* beta, const float* h0, float scale,
                   const void* residuals, const void* dout, const float* dh_final, void* dq,

@@ -93,10 +93,11 @@ def test_invalid_arguments_are_rejected_on_the_host(lib):
     assert fwd(ctypes.byref(_dims()), p, p, p, p, p, None, ctypes.c_float(float("nan")), p, None, p, None) == binding.GDN_ERR_INVALID_ARG
     # empty problems are accepted without touching the device
     assert fwd(ctypes.byref(_dims(B=0)), None, None, None, None, None, None, f, None, None, None, None) == binding.GDN_OK
-    # backward: float32 is not supported; workspace required
+    # backward: same widths and dtypes as the forward; workspace required
     bwd = lib.gdn_chunk_bwd
     args = [p, p, p, p, p, None, f, p, p, None, p, p, p, p, p, None, p, None]
-    assert bwd(ctypes.byref(_dims(dtype=binding.GDN_F32)), *args) == binding.GDN_ERR_UNSUPPORTED
+    assert bwd(ctypes.byref(_dims(Dk=64, Dv=96)), *args) == binding.GDN_ERR_UNSUPPORTED
+    assert bwd(ctypes.byref(_dims(dtype=7)), *args) == binding.GDN_ERR_UNSUPPORTED
     bad = list(args)
     bad[16] = None  # workspace
     assert bwd(ctypes.byref(_dims()), *bad) == binding.GDN_ERR_INVALID_ARG

@@ -1,5 +1,6 @@
 """GPU parity of the chunked backward (gdn_chunk_bwd) against the oracle's
-hand-derived float64 reverse pass (rel-L2 <= 2e-2 per gradient, bf16 inputs).
+hand-derived float64 reverse pass: rel-L2 <= 2e-2 per gradient with bf16 inputs,
+1e-4 with fp32 inputs.
 
 Includes the training-shape fwd+bwd workload (B8 T4096 H6 D128 bf16) at full
 size with the same launch the benchmark times; the oracle checks every
@@ -12,7 +13,7 @@ import torch
 import gated_deltanet_gdn_gb300 as gdn
 from gated_deltanet_gdn_gb300.synthetic import WORKLOADS, make_inputs
 
-from helpers import TOL, cuda_inputs, oracle_bwd, oracle_fwd, rel
+from helpers import TOL, cuda_inputs, head_slice, oracle_bwd, oracle_fwd, rel
 
 pytestmark = pytest.mark.gpu
 GRADS = ("dq", "dk", "dv", "dg", "dbeta", "dh0")
@@ -191,3 +192,70 @@ def test_unequal_key_value_widths(per_channel, Dk, Dv):
     ref = oracle_bwd(host)
     for n in GRADS:
         assert rel(grads[n], ref[n]) <= TOL["bf16"], (n, rel(grads[n], ref[n]))
+
+
+# ------------------------------------------------------------------ fp32 operands
+@pytest.mark.parametrize("per_channel", [True, False])
+@pytest.mark.parametrize("Dk,Dv", [(64, 64), (128, 128), (64, 128), (128, 64)])
+@pytest.mark.parametrize("flags", [0, gdn.GDN_FLAG_PAIRWISE_WITHIN_BLOCK])
+def test_fp32_small_parity(per_channel, Dk, Dv, flags):
+    """fp32 inputs through the CUDA-core backward chain (every width pair), rel-L2 <= 1e-4
+    per gradient against the float64 oracle."""
+    w = WORKLOADS["train_fwd_f32"].with_(B=2, T=192, H=2, Dk=Dk, Dv=Dv, g_per_channel=per_channel,
+                                         g_mult=1.0 if per_channel else 0.1, h0_std=0.3)
+    host = make_inputs(w)
+    out, hT, grads = _fwd_bwd(cuda_inputs(host), flags)
+    assert grads["dq"].dtype == torch.float32
+    ref = oracle_bwd(host)
+    for n in GRADS:
+        assert rel(grads[n], ref[n]) <= TOL["f32"], (n, rel(grads[n], ref[n]))
+
+
+def test_fp32_extreme_decay_and_wipes():
+    """fp32: strong per-channel decay (the pairwise in-block fallback) and a scalar decay
+    with near-total wipes, each against the oracle at 1e-4."""
+    for w in (WORKLOADS["train_fwd_f32"].with_(B=1, T=128, H=2, Dk=64, Dv=64, g_mu=3.0, g_mult=1.0,
+                                               h0_std=0.5),
+              WORKLOADS["recurrent"].with_(B=1, T=256, H=2, Dk=64, Dv=64, wipe_every=96)):
+        host = make_inputs(w)
+        _, _, grads = _fwd_bwd(cuda_inputs(host))
+        ref = oracle_bwd(host)
+        for n in GRADS:
+            assert rel(grads[n], ref[n]) <= TOL["f32"], (w.name, n, rel(grads[n], ref[n]))
+
+
+def test_fp32_autograd_and_qk_l2norm():
+    """fp32 through the autograd wrapper, with and without the q/k L2 normalisation."""
+    names = dict(q="dq", k="dk", v="dv", g="dg", beta="dbeta", h0="dh0")
+    for flags, norm in ((0, False), (gdn.GDN_FLAG_QK_L2NORM, True)):
+        w = WORKLOADS["train_fwd_f32"].with_(B=1, T=128, H=2, h0_std=0.2, normalize_qk=not norm)
+        host = make_inputs(w)
+        d = cuda_inputs(host)
+        leaves = {n: d[n].clone().requires_grad_(True) for n in names}
+        out, hT = gdn.gated_delta_rule(leaves["q"], leaves["k"], leaves["v"], leaves["g"], leaves["beta"],
+                                       leaves["h0"], flags=flags)
+        (out * d["dout"]).sum().backward(retain_graph=True)
+        hT.backward(d["dh_final"])
+        ref = oracle_bwd(host, qk_l2norm=norm)
+        for n, gn in names.items():
+            assert rel(leaves[n].grad, ref[gn]) <= TOL["f32"], (norm, n, rel(leaves[n].grad, ref[gn]))
+
+
+def test_fp32_training_shape_slice():
+    """B4 T4096 H6 D128 fp32 (the fp32 training shape): forward and backward at full size,
+    every (batch, head) pair of the first two batches against the oracle at 1e-4."""
+    w = WORKLOADS["train_fwd_f32"]
+    host = make_inputs(w)
+    out, hT, grads = _fwd_bwd(cuda_inputs(host))
+    torch.cuda.synchronize()
+    pairs = [(b, h) for b in range(2) for h in range(w.H)]
+    ref = oracle_bwd(host, pairs)
+    report = {}
+    for n in GRADS:
+        state = n == "dh0"
+        got = head_slice(grads[n].cpu(), pairs, state=state)
+        report[n] = rel(got, ref[n])
+        assert report[n] <= TOL["f32"], (n, report[n])
+    print("\nfp32 training shape B4 T4096 H6 D128, batches 0-1, rel-L2 vs oracle:")
+    for n, r in report.items():
+        print(f"  {n:8s} {r:.3e}")
