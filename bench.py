@@ -216,7 +216,10 @@ def kernel_work(B, T, H, D, es=2):
     per["chunk_prep_tc_kernel"] = per["chunk_prep_kernel"]
     per["chunk_scan_fwd_tc_kernel"] = per["chunk_scan_fwd_kernel"]
     per["chunk_scan_bwd_tc_kernel"] = per["chunk_scan_bwd_kernel"]
-    return {k: (b * n, f * n) for k, (b, f) in per.items()}
+    out = {k: (b * n, f * n) for k, (b, f) in per.items()}
+    # zeroes the single backward launch's counters: one 128-byte line per (batch, head) + one
+    out["chunk_bwd_sync_zero_kernel"] = (B * H * 128 + 128, 0)
+    return out
 
 
 # the files the chunk kernels (the ones profiles/traffic.json covers) are compiled from
@@ -354,6 +357,10 @@ def run_gdn(args, world, rank, local):
         # the forward scan's launch also formed the chunk outputs (output CTAs beside it)
         work["chunk_scan_fwd_tc_kernel"] = tuple(
             x + y for x, y in zip(work["chunk_scan_fwd_tc_kernel"], work["chunk_out_kernel"]))
+    if "chunk_bwd_tc_kernel" in prof and "chunk_scan_bwd_tc_kernel" not in prof:
+        # the gradient launch also ran the reverse scan (scan CTAs beside the gradient CTAs)
+        work["chunk_bwd_tc_kernel"] = tuple(
+            x + y for x, y in zip(work["chunk_bwd_tc_kernel"], work["chunk_scan_bwd_tc_kernel"]))
     peaks = load_peaks()
     traffic = load_traffic()
     kernels = {}

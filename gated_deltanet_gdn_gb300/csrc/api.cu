@@ -128,6 +128,8 @@ BwdWorkspacePtrs workspace_ptrs(const gdn_dims* d, void* base) {
   w.dbv = reinterpret_cast<float*>(b + L.dbv);
   w.dbpart = reinterpret_cast<float*>(b + L.dbpart);
   w.dgpart = reinterpret_cast<float*>(b + L.dgpart);
+  w.sync = reinterpret_cast<unsigned*>(b + L.sync);
+  w.sync_bytes = L.sync_bytes;
   return w;
 }
 
@@ -151,7 +153,8 @@ const char* kKernelNames[K_COUNT] = {"chunk_prep_kernel",    "chunk_scan_fwd_ker
                                      "chunk_scan_fwd_tc_kernel", "chunk_scan_bwd_tc_kernel",
                                      "decode_kernel", "l2norm_rows_kernel", "l2norm_bwd_kernel",
                                      "replay_decode_kernel", "replay_state_kernel", "chunk_dqa_kernel",
-                                     "chunk_bwd_tc_kernel", "chunk_prep_tc_kernel"};
+                                     "chunk_bwd_tc_kernel", "chunk_prep_tc_kernel",
+                                     "chunk_bwd_sync_zero_kernel"};
 
 }  // namespace
 

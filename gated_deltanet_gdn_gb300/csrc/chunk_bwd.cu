@@ -422,14 +422,13 @@ cudaError_t launch_bwd_t(const ChunkBwdArgs& a, cudaStream_t s) {
   const int N = a.T / C, BH = a.B * a.H;
   const int bf16_ops = sizeof(T) == 2;
   cudaError_t e;
-  // bf16 with Dk = Dv = 128: the tensor-core reverse scan, then one fused tensor-core
-  // kernel for every chunk product and gradient (chunk_bwd_tc.cu). Otherwise (Dk = 64, or
-  // fp32 operands): the CUDA-core scan, then the products that need no scan result
-  // (chunk_dqa.cuh), the state products, the score gradients and the channel-group sums.
-  const bool tc = scan_tc_applies(bf16_ops, DK, DV);
-  if (tc) {
-    if ((e = launch_scan_bwd_tc(a, s)) != cudaSuccess) return e;
-  } else {
+  // bf16 with Dk = Dv = 128: the tensor-core reverse scan and one fused tensor-core kernel
+  // for every chunk product and gradient (chunk_bwd_tc.cu), in one launch where they fit
+  // side by side. Otherwise (Dk = 64, or fp32 operands): the CUDA-core scan, then the
+  // products that need no scan result (chunk_dqa.cuh), the state products, the score
+  // gradients and the channel-group sums.
+  if (scan_tc_applies(bf16_ops, DK, DV) && bwd_tc_applies(DK, DV)) return launch_chunk_bwd_tc(a, s);
+  {
     const int bytes = RScanLayout<T, DK>::BYTES + 1024;
     auto kern = chunk_scan_bwd_kernel<T, DK, DV>;
     if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes)) != cudaSuccess) return e;
@@ -439,8 +438,7 @@ cudaError_t launch_bwd_t(const ChunkBwdArgs& a, cudaStream_t s) {
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   if (N == 0) return cudaSuccess;
-  if (bf16_ops && bwd_tc_applies(DK, DV)) return launch_chunk_bwd_tc(a, s);
-  if (!tc) {
+  {
     const int bytes = DqaLayout<T, DK, DV>::BYTES + 1024;
     auto kern = chunk_dqa_kernel<T, DK, DV>;
     if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes)) != cudaSuccess) return e;

@@ -41,6 +41,7 @@
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
+#include "chunk_scan_tc.cuh"
 #include "common.cuh"
 #include "kernels.h"
 #include "umma.cuh"
@@ -88,7 +89,8 @@ struct BtLayout {
                                                    // epilogue only; GX is read before it)
   static constexpr int FLAGS = DGAM + NTG * BD * 4;  // int [4]: unsafe1, unsafe2
   static constexpr int BAR = FLAGS + 16;           // 8 mbarriers
-  static constexpr int TSLOT = BAR + 8 * 8;
+  static constexpr int UNITS = BAR + 8 * 8;        // int [4]: claimed units (fused launch)
+  static constexpr int TSLOT = UNITS + 16;         // TMEM address (both roles)
   static constexpr int BYTES = TSLOT + 16;
   static constexpr uint32_t TXA = (uint32_t)(C * C * 2 + BD * C * 2 + C * BD * 2);
   static constexpr uint32_t TXB = (uint32_t)(C * BD * 2 + BD * C * 2 + 2 * BD * BD * 2);
@@ -96,6 +98,18 @@ struct BtLayout {
   static constexpr uint32_t TXG = (uint32_t)(C * BD * 2);      // per-channel g into YE
 };
 static_assert(BtLayout::BYTES + 1024 <= 227 * 1024, "shared memory of one CTA");
+static_assert(TcBwdLayout::BYTES <= BtLayout::TSLOT, "the reverse scan role leaves the TMEM address alone");
+
+// The fused launch: CTAs 0 .. nscan - 1 first run the reverse scan of (batch, head)
+// blockIdx.x (rscan_role) and publish its progress; every CTA then claims chunk-heads from
+// the queue in the order the scan finishes them (all heads' last chunk first) and waits,
+// before it loads a chunk's dU and dS records, until that chunk's head has published them.
+// queue NULL: no scan, a static stride over the chunk-heads.
+struct BwdSync {
+  unsigned* progress;  // [B*H][PROGRESS_STRIDE]: chunks the reverse scan has finished
+  unsigned* queue;     // the next unit to claim
+  int nscan;
+};
 static_assert(BtLayout::CTOT + NTG * BD * 4 <= BtLayout::COLP, "the dG totals fit in the G totals' place");
 
 __device__ __forceinline__ void epi_sync() { asm volatile("bar.sync 1, 512;\n" ::: "memory"); }
@@ -184,15 +198,37 @@ template <bool PC>
 __global__ void __launch_bounds__(BT_THREADS, 1)
     chunk_bwd_tc_kernel(ChunkBwdArgs a, const __grid_constant__ CUtensorMap dout_map,
                         const __grid_constant__ CUtensorMap v_map, const __grid_constant__ CUtensorMap q_map,
-                        const __grid_constant__ CUtensorMap k_map, const __grid_constant__ CUtensorMap g_map) {
+                        const __grid_constant__ CUtensorMap k_map, const __grid_constant__ CUtensorMap g_map,
+                        BwdSync sync) {
   pdl_wait();
   pdl_trigger();
   typedef BtLayout L;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = align1024(smem_raw);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int N = a.T / C, units = N * a.B * a.H;
-  const int nunits = (units - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x;
+  const int BH = a.B * a.H, N = a.T / C, units = N * BH;
+  const bool fused = sync.queue != nullptr;
+  // static stride: this CTA's units; fused: claimed one ahead into units_s[m % 4]
+  const int nunits = fused ? 0 : (units - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x;
+  int* units_s = reinterpret_cast<int*>(sm + L::UNITS);
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + L::TSLOT);
+  const bool scan_cta = (int)blockIdx.x < sync.nscan;
+  if (scan_cta && tid == 0) rscan_init(sm);
+  if (warp == 0) {
+    tmem_alloc(tslot, BT_TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tm = *tslot;
+  if (scan_cta) {  // the reverse scan first; then this CTA joins the gradient work
+    rscan_role(a, &dout_map, sm, tm, blockIdx.x, sync.progress);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (tid == 0) rscan_inval(sm);
+  }
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + L::BAR);
   uint64_t* fullA = bars + 0;
   uint64_t* fullB = bars + 1;
@@ -202,7 +238,6 @@ __global__ void __launch_bounds__(BT_THREADS, 1)
   uint64_t* bP56 = bars + 5;
   uint64_t* bDrain = bars + 6;
   uint64_t* fullQ = bars + 7;
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + L::TSLOT);
   float* beta_s = reinterpret_cast<float*>(sm + L::BETA);
   float* gsc = reinterpret_cast<float*>(sm + L::GSC);
   float* diag_s = reinterpret_cast<float*>(sm + L::DIAG);
@@ -224,27 +259,38 @@ __global__ void __launch_bounds__(BT_THREADS, 1)
     mbar_init(bP56, 2);  // P5 (thread 64) and P6 (thread 96)
     mbar_init(bDrain, 4);  // every issuing thread: 0, 32, 64, 96
     mbar_init(fullQ, 1);
+    if (fused) units_s[0] = (int)atomicAdd(sync.queue, 1u);
     fence_mbar_init();
   }
-  if (warp == 0) {
-    tmem_alloc(tslot, BT_TMEM_COLS);
-    tmem_relinquish();
-  }
-  tc_fence_before();
   __syncthreads();
-  tc_fence_after();
-  const uint32_t tm = *tslot;
 
+  // the m-th unit of this CTA: static, head-major; fused, in the order the reverse scan
+  // finishes chunks (unit index = (N - 1 - n) * B*H + bh)
+  auto valid = [&](int m) { return fused ? units_s[m & 3] < units : m < nunits; };
   auto unit_of = [&](int m, int& n, int& bh) {
-    const int u = (int)blockIdx.x + m * (int)gridDim.x;
-    bh = u / N;
-    n = u % N;
+    if (fused) {
+      const int u = units_s[m & 3], it = u / BH;
+      bh = u - it * BH;
+      n = N - 1 - it;
+    } else {
+      const int u = (int)blockIdx.x + m * (int)gridDim.x;
+      bh = u / N;
+      n = u % N;
+    }
+  };
+  // fused: the reverse scan has stored chunk n's dU and dS records
+  auto wait_scan = [&](int n, int bh) {
+    if (fused) {
+      wait_counter(sync.progress + (size_t)bh * PROGRESS_STRIDE, (unsigned)(N - n), a.err);
+      fence_proxy_async_global();
+    }
   };
 
   // loads, issued by thread 0: group A (T, dU^T, v) and group B (dO, U^T, S0^T, dS1^T)
   auto load_a = [&](int m) {
     int n, bh;
     unit_of(m, n, bh);
+    wait_scan(n, bh);
     const size_t ch = (size_t)bh * N + n;
     mbar_arrive_expect_tx(fullA, L::TXA);
     bulk_g2s(sm + L::TM, static_cast<const bf16*>(a.res.tmat) + ch * (C * C), C * C * 2, fullA);
@@ -256,6 +302,7 @@ __global__ void __launch_bounds__(BT_THREADS, 1)
   auto load_b = [&](int m) {
     int n, bh;
     unit_of(m, n, bh);
+    wait_scan(n, bh);
     const size_t ch = (size_t)bh * N + n;
     mbar_arrive_expect_tx(fullB, L::TXB);
     const int b = bh / a.H, h = bh % a.H, tok = b * a.T + n * C;
@@ -278,7 +325,7 @@ __global__ void __launch_bounds__(BT_THREADS, 1)
     tma_load_3d(sm + L::X + 2 * C * 128 + C * 128, &k_map, 64, h, tok, fullQ);
     if (PC) tma_load_3d(sm + L::YE, &g_map, 0, h, tok, fullQ);
   };
-  if (tid == 0 && nunits > 0) {
+  if (tid == 0 && valid(0)) {
     load_a(0);
     load_b(0);
     load_q(0);
@@ -320,13 +367,18 @@ __global__ void __launch_bounds__(BT_THREADS, 1)
   float Greg[TPT];
   float Gb = 0.f, GC = 0.f;
   int cur_n = 0, cur_bh = 0;  // the chunk whose final epilogue is pending
+  int nproc = 0;              // units this CTA processed
+  unsigned nxt = 0;           // thread 0, fused: the unit claimed for step m + 1
 
 #pragma unroll 1
-  for (int m = 0; m <= nunits; ++m) {
-    const bool cur = m < nunits;
+  for (int m = 0;; ++m) {
+    const bool cur = valid(m);
     const uint32_t par = (uint32_t)m & 1u;
     int n = 0, bh = 0;
     if (cur) unit_of(m, n, bh);
+    // claimed now, published to units_s before the barrier that precedes the first load
+    // of step m + 1 (the atomic's latency hides behind the epilogues in between)
+    if (fused && cur && tid == 0) nxt = atomicAdd(sync.queue, 1u);
     bool q_early = true;  // this chunk's group Q loads were issued at the start of (b)
     // this chunk's beta, read while the previous chunk's final epilogue runs
     float beta_pre = 0.f;
@@ -469,7 +521,10 @@ __global__ void __launch_bounds__(BT_THREADS, 1)
                                                             (dgp_s[2 * C + t] + dgp_s[3 * C + t]));
       }
     }
-    if (!cur) break;
+    if (!cur) {
+      nproc = m;
+      break;
+    }
     if (!q_early) {  // G of the previous chunk has left X (read by the pairwise sums)
       fence_proxy_async();
       epi_sync();
@@ -504,11 +559,12 @@ __global__ void __launch_bounds__(BT_THREADS, 1)
       const float p = warp_sum16(pv, lane);
       if ((lane & 1) == 0) dbv_s[qw * C + t_beg + (lane >> 1)] = p;
     }
+    if (fused && tid == 0) units_s[(m + 1) & 3] = (int)nxt;
     fence_proxy_async();  // the Y rows are read by the tensor cores
     tc_fence_before();
     epi_sync();
     // (d) P2, P3, P4; P1 has read T and dU^T: the next chunk's group A loads
-    if (tid == 128 && m + 1 < nunits) load_a(m + 1);
+    if (tid == 128 && valid(m + 1)) load_a(m + 1);
     if (tid == 0) {
       mbar_wait(fullB, par, a.err);
       tc_fence_after();
@@ -691,7 +747,7 @@ __global__ void __launch_bounds__(BT_THREADS, 1)
     fence_proxy_async();  // X, Ye and the score-gradient tile are read by the tensor cores
     tc_fence_before();
     epi_sync();
-    if (tid == 32 && m + 1 < nunits) {
+    if (tid == 32 && valid(m + 1)) {
       // P2-P4 and the gamma-gradient sums have read dO, U^T, S0^T and dS1^T: the next
       // chunk's group B loads (the Y rows of DY are written after this chunk's final
       // epilogue, which waits for P3)
@@ -721,8 +777,8 @@ __global__ void __launch_bounds__(BT_THREADS, 1)
   // every MMA and load this CTA issued has completed before TMEM is freed and the CTA
   // retires (in normal operation all were waited for; after a failed wait maybe not)
   if (tid == 0) {
-    if (nunits > 0) {
-      const uint32_t lp = (uint32_t)(nunits - 1) & 1u;
+    if (nproc > 0) {
+      const uint32_t lp = (uint32_t)(nproc - 1) & 1u;
       mbar_drain(fullA, lp);
       mbar_drain(fullB, lp);
       mbar_drain(fullQ, lp);
@@ -738,11 +794,22 @@ __global__ void __launch_bounds__(BT_THREADS, 1)
   if (warp == 0) tmem_dealloc(tm, BT_TMEM_COLS);
 }
 
+// Zeroes the fused launch's counters. Launched without programmatic serialisation, so it
+// starts after every earlier kernel of the stream has finished with them (a previous
+// backward call on the same workspace included); it lets the fused launch be scheduled at
+// once, whose griddepcontrol.wait then waits for the zeros. A kernel rather than a memset:
+// a memset may queue on a copy engine behind the caller's host copies.
+__global__ void chunk_bwd_sync_zero_kernel(unsigned* p, int n) {
+  pdl_trigger();
+  for (int i = threadIdx.x; i < n; i += blockDim.x) p[i] = 0u;
+}
+
 }  // namespace
 
 bool bwd_tc_applies(int DK, int DV) { return DK == BD && DV == BD; }
 
 cudaError_t launch_chunk_bwd_tc(const ChunkBwdArgs& a, cudaStream_t s) {
+  if (a.T / C == 0) return launch_scan_bwd_tc(a, s);  // no chunks: dh0 = dh_final only
   if ((long long)a.B * a.T > 0x7fffffffLL) return cudaErrorInvalidValue;  // TMA token coordinate
   auto encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(tensor_map_encode_fn());
   if (!encode) return cudaErrorNotSupported;
@@ -771,14 +838,44 @@ cudaError_t launch_chunk_bwd_tc(const ChunkBwdArgs& a, cudaStream_t s) {
   auto kern = a.per_channel ? chunk_bwd_tc_kernel<true> : chunk_bwd_tc_kernel<false>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
   if (e != cudaSuccess) return e;
-  int dev = 0, nsm = 0;
+  int dev = 0, nsm = 0, coop = 0;
   if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
   if ((e = cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
-  const int units = (a.T / C) * a.B * a.H;
-  const int grid = units < nsm ? units : nsm;
-  if (grid == 0) return cudaSuccess;
+  if ((e = cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev)) != cudaSuccess) return e;
+  const int BH = a.B * a.H, units = (a.T / C) * BH;
+  // Fewer (batch, head) pairs than SMs: one cooperative grid of one CTA per SM (the shared
+  // memory admits one), so every wait of a gradient CTA has the scan CTA it waits for
+  // resident. The counters start from zero on every call (chunk_bwd_sync_zero_kernel).
+  const bool fused = coop && BH < nsm && units > 0 && a.ws.sync && a.ws.sync_bytes > 0;
+  if (!fused) {
+    if ((e = launch_scan_bwd_tc(a, s)) != cudaSuccess) return e;
+    const int grid = units < nsm ? units : nsm;
+    if (grid == 0) return cudaSuccess;
+    prof_mark(K_BWD_TC, s, true);
+    e = launch_pdl(kern, dim3(grid), dim3(BT_THREADS), bytes, s, a, map, vmap, qmap, kmap, gmap,
+                   BwdSync{nullptr, nullptr, 0});
+    prof_mark(K_BWD_TC, s, false);
+    return e;
+  }
+  prof_mark(K_BWD_SYNC, s, true);
+  chunk_bwd_sync_zero_kernel<<<1, 256, 0, s>>>(a.ws.sync, (int)(a.ws.sync_bytes / 4));
+  prof_mark(K_BWD_SYNC, s, false);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  BwdSync sync{a.ws.sync, a.ws.sync + (size_t)BH * PROGRESS_STRIDE, BH};
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(nsm);
+  cfg.blockDim = dim3(BT_THREADS);
+  cfg.dynamicSmemBytes = bytes;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeCooperative;
+  attr[1].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
   prof_mark(K_BWD_TC, s, true);
-  e = launch_pdl(kern, dim3(grid), dim3(BT_THREADS), bytes, s, a, map, vmap, qmap, kmap, gmap);
+  e = cudaLaunchKernelEx(&cfg, kern, a, map, vmap, qmap, kmap, gmap, sync);
   prof_mark(K_BWD_TC, s, false);
   return e;
 }

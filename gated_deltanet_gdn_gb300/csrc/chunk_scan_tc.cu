@@ -11,22 +11,25 @@
 // dU = scale Aqk^T dO + K-tilde dS, dS0 = diag(gam) dS + scale Q-hat^T dO - W^T dU
 // (the chunked WY form of the token recurrence; see chunk_fwd.cu and chunk_bwd.cu).
 //
-// Warp roles (288 threads): warps 0-7 move the state between TMEM and shared memory,
-// thread (w, l) owning TMEM lane 32 (w % 4) + l and column half w / 4; warp 8 is the
-// producer that streams each chunk's records into a ring of stages (cp.async.bulk, and a
-// TMA tensor load for dO) as soon as the tensor cores release a stage. Thread 0 issues
-// every tcgen05.mma (bf16 x bf16 -> fp32 in TMEM) on 128-byte swizzled tiles: the
-// records exactly as the preparation kernel stored them (K-major or MN-major operands,
-// no transposition) and the bf16 copies of S^T / U^T the compute warps write from TMEM
+// Forward warp roles (576 threads): warps 0-15 move the state between TMEM and shared
+// memory, four per TMEM lane quarter (thread (w, l) owns lane 32 (w % 4) + l and a quarter
+// of the columns); warp 16 is the producer that streams each chunk's records into a ring
+// of stages (cp.async.bulk) as soon as the tensor cores release a stage; warp 17
+// publishes progress to the output CTAs beside the scan. Thread 0 issues every
+// tcgen05.mma (bf16 x bf16 -> fp32 in TMEM) on 128-byte swizzled tiles: the records
+// exactly as the preparation kernel stored them (K-major or MN-major operands, no
+// transposition) and the bf16 copies of S^T / U^T the compute warps write from TMEM
 // (double-buffered), which bulk copies also store as the chunk-start state and U records
-// the later kernels read. The compute warps add U' to the forward's U^T. Every wait is
-// bounded and sets the device error word.
+// the later kernels read. The compute warps add U' to the forward's U^T. The reverse scan
+// is the role rscan_role of chunk_scan_tc.cuh (eight compute warps, a producer warp),
+// run here by a kernel of its own. Every wait is bounded and sets the device error word.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
 #include <mutex>
 
 #include "chunk_out.cuh"
+#include "chunk_scan_tc.cuh"
 #include "common.cuh"
 #include "kernels.h"
 #include "umma.cuh"
@@ -34,112 +37,14 @@
 namespace gdn {
 namespace {
 
-constexpr int TD = 128;                 // Dk = Dv
-constexpr int COMPUTE_THREADS = 256;    // warps 0-7
-constexpr int TC_THREADS = COMPUTE_THREADS + 32;  // + the producer warp
 // the forward: 16 compute warps (four per TMEM lane quarter, each on a quarter of the
 // state's columns), the producer warp and the publisher warp
 constexpr int FWD_COMPUTE = 512;
 constexpr int FWD_PRODUCER = FWD_COMPUTE / 32, FWD_PUBLISHER = FWD_PRODUCER + 1;
 constexpr int FWD_THREADS = FWD_COMPUTE + 64;
-constexpr uint32_t TMEM_COLS = 256;     // S^T or dS^T: columns 0..127; U^T or dU^T: 128..191
-constexpr int PANEL_C = C * 128;        // bytes of one 64-column panel of a [C][*] bf16 tile
-constexpr int PANEL_D = TD * 128;       // bytes of one 64-column panel of a [Dv][*] bf16 tile
 
-__device__ __forceinline__ void compute_sync() { asm volatile("bar.sync 1, 256;\n" ::: "memory"); }
 __device__ __forceinline__ void fwd_sync() { asm volatile("bar.sync 1, 512;\n" ::: "memory"); }
 __device__ __forceinline__ void out_sync() { asm volatile("bar.sync 2, 256;\n" ::: "memory"); }
-
-__device__ __forceinline__ uint32_t pack_bf16(float x, float y) {
-  __nv_bfloat162 h = __floats2bfloat162_rn(x, y);
-  return *reinterpret_cast<uint32_t*>(&h);
-}
-
-// Row `row` of a bf16 tile with 128-byte panels, 32 consecutive columns from c0 (a
-// multiple of 32): four 16-byte stores.
-template <int ROWS, int COLS>
-__device__ __forceinline__ void store_row32(Tile<bf16, ROWS, COLS> t, int row, int c0, const float* x) {
-#pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    uint4 u;
-    u.x = pack_bf16(x[8 * q + 0], x[8 * q + 1]);
-    u.y = pack_bf16(x[8 * q + 2], x[8 * q + 3]);
-    u.z = pack_bf16(x[8 * q + 4], x[8 * q + 5]);
-    u.w = pack_bf16(x[8 * q + 6], x[8 * q + 7]);
-    *reinterpret_cast<uint4*>(t.ptr(row, c0 + 8 * q)) = u;
-  }
-}
-
-// Two 32-column TMEM loads of this thread's lane, one completion wait.
-__device__ __forceinline__ void tmem_ld64(uint32_t taddr, float* v) {
-  uint32_t r[64];
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x64.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
-      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32,%33,%34,%35,%36,%37,%38,%39,"
-      "%40,%41,%42,%43,%44,%45,%46,%47,%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63}, [%64];\n"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
-        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
-        "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31]),
-        "=r"(r[32]), "=r"(r[33]), "=r"(r[34]), "=r"(r[35]), "=r"(r[36]), "=r"(r[37]), "=r"(r[38]), "=r"(r[39]),
-        "=r"(r[40]), "=r"(r[41]), "=r"(r[42]), "=r"(r[43]), "=r"(r[44]), "=r"(r[45]), "=r"(r[46]), "=r"(r[47]),
-        "=r"(r[48]), "=r"(r[49]), "=r"(r[50]), "=r"(r[51]), "=r"(r[52]), "=r"(r[53]), "=r"(r[54]), "=r"(r[55]),
-        "=r"(r[56]), "=r"(r[57]), "=r"(r[58]), "=r"(r[59]), "=r"(r[60]), "=r"(r[61]), "=r"(r[62]), "=r"(r[63])
-      : "r"(taddr)
-      : "memory");
-  asm volatile("tcgen05.wait::ld.sync.aligned;\n" ::: "memory");
-#pragma unroll
-  for (int i = 0; i < 64; ++i) v[i] = __uint_as_float(r[i]);
-}
-
-// S^T row slice (64 fp32 columns of this thread's lane from `col`): load it from TMEM
-// into x and write its bf16 copy into the operand tile.
-__device__ __forceinline__ void state_copy_out(uint32_t taddr, Tile<bf16, TD, TD> Sa, int row, int col, float* x) {
-  tmem_ld64(taddr, x);
-  store_row32(Sa, row, col, x);
-  store_row32(Sa, row, col + 32, x + 32);
-}
-// Put the slice back into TMEM scaled column-wise by gam (the decay of the state).
-__device__ __forceinline__ void state_scale_back(uint32_t taddr, int col, const float* gam, float* x) {
-#pragma unroll
-  for (int i = 0; i < 64; i += 4) {
-    const float4 g = *reinterpret_cast<const float4*>(gam + col + i);
-    x[i] *= g.x;
-    x[i + 1] *= g.y;
-    x[i + 2] *= g.z;
-    x[i + 3] *= g.w;
-  }
-  float lo[32], hi[32];
-#pragma unroll
-  for (int i = 0; i < 32; ++i) {
-    lo[i] = x[i];
-    hi[i] = x[32 + i];
-  }
-  tmem_st32(taddr, lo);
-  tmem_st32(taddr + 32, hi);
-  tmem_wait_st();
-}
-
-// Descriptor helpers. A 128-byte swizzled descriptor's start address field holds
-// address / 16 in 14 bits, so moving inside a tile is an add to the low word.
-__device__ __forceinline__ uint64_t desc_k(const void* base) { return umma_desc_sw128(smem_u32(base), 16, 1024); }
-__device__ __forceinline__ uint64_t desc_mn(const void* base, int panel) {
-  return umma_desc_sw128(smem_u32(base), (uint32_t)panel, 1024);
-}
-// K step ks of a K-major operand whose 64-column panels are `panel` bytes apart
-__device__ __forceinline__ uint64_t kstep_k(uint64_t d, int ks, int panel) {
-  return d + (uint64_t)(((ks >> 2) * panel + (ks & 3) * 32) >> 4);
-}
-// K step ks (16 rows of 128 bytes) of an MN-major operand
-__device__ __forceinline__ uint64_t kstep_mn(uint64_t d, int ks) { return d + (uint64_t)((ks * 2048) >> 4); }
-
-__device__ __forceinline__ void umma_commit_to(uint64_t* bar) { umma_commit(bar); }
-
-// Every MMA this thread issued has completed (one commit on a barrier used only here).
-__device__ __forceinline__ void drain_mma(uint64_t* bar) {
-  umma_commit(bar);
-  mbar_drain(bar, 0u);
-}
 
 // ------------------------------------------------------------------ forward
 struct TcFwdLayout {
@@ -427,52 +332,16 @@ __global__ void __launch_bounds__(FWD_THREADS, 1) chunk_scan_fwd_tc_kernel(Chunk
 }
 
 // ------------------------------------------------------------------ reverse
-struct TcBwdLayout {
-  static constexpr int W = 0;                    // -W          [C][Dk] (MN-major B of dS^T)
-  static constexpr int QH = W + C * TD * 2;      // scale Q-hat [C][Dk] (MN-major B of dS^T)
-  static constexpr int KT = QH + C * TD * 2;     // K-tilde     [C][Dk] (K-major B of dU^T)
-  static constexpr int DO = KT + C * TD * 2;     // dO          [C][Dv] (MN-major A)
-  static constexpr int AQK = DO + C * TD * 2;    // scale Aqk   [C][C]  (MN-major B of dU^T)
-  static constexpr int STAGE = AQK + C * C * 2;
-  static constexpr int STAGES = 2;
-  static constexpr int GAM = STAGES * STAGE;     // gam [STAGES][Dk] fp32
-  static constexpr int SA = a1k(GAM + STAGES * TD * 4);  // dS^T bf16 [Dv][Dk], two buffers
-  static constexpr int UA = SA + 2 * TD * TD * 2;  // dU^T bf16 [Dv][C]
-  static constexpr int BAR = UA + TD * C * 2;      // full[STAGES], empty[STAGES], u, s, drain
-  static constexpr int TSLOT = BAR + 8 * (2 * STAGES + 3);
-  static constexpr int BYTES = TSLOT + 16;
-  static constexpr uint32_t TX = (uint32_t)(4 * C * TD * 2 + C * C * 2 + TD * 4);
-};
-
+// One CTA per (batch, head): the reverse scan alone (rscan_role, chunk_scan_tc.cuh), used
+// when the fused backward launch of chunk_bwd_tc.cu does not apply.
 __global__ void __launch_bounds__(TC_THREADS, 1)
     chunk_scan_bwd_tc_kernel(ChunkBwdArgs a, const __grid_constant__ CUtensorMap dout_map) {
   pdl_wait();  // no early trigger: one wave for the whole scan, successors must not park beside it
-  typedef TcBwdLayout L;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = align1024(smem_raw);
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int bh = blockIdx.x, b = bh / a.H, h = bh % a.H;
-  const int N = a.T / C;
-  uint64_t* full = reinterpret_cast<uint64_t*>(sm + L::BAR);
-  uint64_t* empty = full + L::STAGES;
-  uint64_t* bar_u = empty + L::STAGES;
-  uint64_t* bar_s = bar_u + 1;
-  uint64_t* bar_d = bar_s + 1;
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + L::TSLOT);
-  bf16* const sa_buf = reinterpret_cast<bf16*>(sm + L::SA);
-  Tile<bf16, TD, C> Ua{reinterpret_cast<bf16*>(sm + L::UA)};
-  float* const gams = reinterpret_cast<float*>(sm + L::GAM);
-
-  if (tid == 0) {
-    for (int s = 0; s < L::STAGES; ++s) {
-      mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 1);
-    }
-    mbar_init(bar_u, 1);
-    mbar_init(bar_s, 1);
-    mbar_init(bar_d, 1);
-    fence_mbar_init();
-  }
+  const int warp = threadIdx.x >> 5;
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + TcBwdLayout::TSLOT);
+  if (threadIdx.x == 0) rscan_init(sm);
   if (warp == 0) {
     tmem_alloc(tslot, TMEM_COLS);
     tmem_relinquish();
@@ -481,129 +350,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tm = *tslot;
-
-  if (warp == COMPUTE_THREADS / 32) {  // ---- producer: chunks in reverse order
-    if (lane == 0) {
-      for (int it = 0; it < N; ++it) {
-        const int n = N - 1 - it, s = it % L::STAGES, k = it / L::STAGES;
-        if (k > 0) mbar_wait(&empty[s], (uint32_t)(k - 1) & 1u, a.err);
-        uint8_t* st = sm + s * L::STAGE;
-        const size_t ch = (size_t)bh * N + n;
-        mbar_arrive_expect_tx(&full[s], L::TX);
-        bulk_g2s(st + L::W, static_cast<const bf16*>(a.res.wneg) + ch * (C * TD), C * TD * 2, &full[s]);
-        bulk_g2s(st + L::QH, static_cast<const bf16*>(a.res.qh) + ch * (C * TD), C * TD * 2, &full[s]);
-        bulk_g2s(st + L::KT, static_cast<const bf16*>(a.res.kt) + ch * (C * TD), C * TD * 2, &full[s]);
-        bulk_g2s(st + L::AQK, static_cast<const bf16*>(a.res.aqk) + ch * (C * C), C * C * 2, &full[s]);
-        bulk_g2s(gams + s * TD, a.res.gam + ch * TD, TD * 4, &full[s]);
-        const int tok = b * a.T + n * C;
-        tma_load_3d(st + L::DO, &dout_map, 0, h, tok, &full[s]);
-        tma_load_3d(st + L::DO + PANEL_C, &dout_map, 64, h, tok, &full[s]);
-      }
-      drain_ring(full, L::STAGES, N);
-    }
-    return;
-  }
-
-  // ---- compute warps
-  const int row = 32 * (warp & 3) + lane, half = warp >> 2;
-  const uint32_t tl = tm + ((uint32_t)(32 * (warp & 3)) << 16);
-  const size_t sb = (size_t)bh * TD * TD;
-  {
-    float lo[32], hi[32];
-    for (int i = 0; i < 32; ++i) {
-      lo[i] = a.dh_final ? a.dh_final[sb + (size_t)(64 * half + i) * TD + row] : 0.f;
-      hi[i] = a.dh_final ? a.dh_final[sb + (size_t)(64 * half + 32 + i) * TD + row] : 0.f;
-    }
-    tmem_st32(tl + 64 * half, lo);
-    tmem_st32(tl + 64 * half + 32, hi);
-    tmem_wait_st();
-  }
-  constexpr uint32_t id_a = umma_idesc_bf16(128, C, true, true);    // dO^T Aqk
-  constexpr uint32_t id_b = umma_idesc_bf16(128, C, false, false);  // dS^T K-tilde^T
-  constexpr uint32_t id_c = umma_idesc_bf16(128, TD, true, true);   // dO^T Q-hat
-  constexpr uint32_t id_d = umma_idesc_bf16(128, TD, false, true);  // dU^T (-W)
-  bf16* dstate_rec = static_cast<bf16*>(a.ws.dstate);
-  bf16* du_rec = static_cast<bf16*>(a.ws.du);
-  uint32_t ph_u = 0, ph_s = 0;
-#pragma unroll 1
-  for (int it = 0; it < N; ++it) {
-    const int n = N - 1 - it, s = it % L::STAGES;
-    uint8_t* st = sm + s * L::STAGE;
-    const size_t ch = (size_t)bh * N + n;
-    Tile<bf16, TD, TD> Sa{sa_buf + (it & 1) * (TD * TD)};
-    if (it > 0) {
-      mbar_wait(bar_s, ph_s, a.err);
-      ph_s ^= 1u;
-      tc_fence_after();
-    }
-    mbar_wait(&full[s], (uint32_t)(it / L::STAGES) & 1u, a.err);
-    // dS^T -> bf16 operand (the record of the gradient leaving chunk n)
-    float xs[64];
-    state_copy_out(tl + 64 * half, Sa, row, 64 * half, xs);
-    fence_proxy_async();
-    tc_fence_before();
-    if (tid == 0) bulk_wait_read0();  // the previous dU record store has read Ua
-    compute_sync();
-    if (tid == 0) {
-      tc_fence_after();
-      bulk_s2g(dstate_rec + ch * (TD * TD), Sa.p, TD * TD * 2);
-      bulk_commit();
-      const uint64_t dSa = desc_k(Sa.p);
-      const uint64_t dDo = desc_mn(st + L::DO, PANEL_C), dAq = desc_mn(st + L::AQK, PANEL_C);
-      const uint64_t dKt = desc_k(st + L::KT);
-#pragma unroll
-      for (int ks = 0; ks < C / 16; ++ks) umma_bf16(tm + 128, kstep_mn(dDo, ks), kstep_mn(dAq, ks), id_a, ks > 0);
-#pragma unroll
-      for (int ks = 0; ks < TD / 16; ++ks)
-        umma_bf16(tm + 128, kstep_k(dSa, ks, PANEL_D), kstep_k(dKt, ks, PANEL_C), id_b, 1u);
-      umma_commit_to(bar_u);
-    }
-    // dS^T <- dS^T diag(gam) while the tensor cores form dU^T; every product into dS^T
-    // comes after the next barrier
-    state_scale_back(tl + 64 * half, 64 * half, gams + s * TD, xs);
-    mbar_wait(bar_u, ph_u, a.err);
-    ph_u ^= 1u;
-    tc_fence_after();
-    {  // dU^T row -> bf16 operand (the dU record)
-      float x[32];
-      tmem_ld32(tl + 128 + 32 * half, x);
-      store_row32(Ua, row, 32 * half, x);
-    }
-    fence_proxy_async();
-    tc_fence_before();
-    // the dS record store of the previous chunk has read the buffer the next one writes
-    if (tid == 0) bulk_wait_read1();
-    compute_sync();
-    if (tid == 0) {
-      tc_fence_after();
-      bulk_s2g(du_rec + ch * (C * TD), Ua.p, C * TD * 2);
-      bulk_commit();
-      const uint64_t dW = desc_mn(st + L::W, PANEL_C), dUa = desc_k(Ua.p);
-      const uint64_t dDo = desc_mn(st + L::DO, PANEL_C), dQh = desc_mn(st + L::QH, PANEL_C);
-#pragma unroll
-      for (int ks = 0; ks < C / 16; ++ks) umma_bf16(tm, kstep_mn(dDo, ks), kstep_mn(dQh, ks), id_c, 1u);
-#pragma unroll
-      for (int ks = 0; ks < C / 16; ++ks) umma_bf16(tm, kstep_k(dUa, ks, PANEL_D), kstep_mn(dW, ks), id_d, 1u);
-      umma_commit_to(&empty[s]);
-      umma_commit_to(bar_s);
-    }
-  }
-  if (N > 0) {
-    mbar_wait(bar_s, ph_s, a.err);
-    tc_fence_after();
-  }
-  if (a.dh0) {
-    float x[64];
-    tmem_ld64(tl + 64 * half, x);
-#pragma unroll
-    for (int i = 0; i < 64; ++i) a.dh0[sb + (size_t)(64 * half + i) * TD + row] = x[i];
-  }
-  if (tid == 0) {  // record stores and every issued MMA complete before TMEM is freed
-    bulk_wait0();
-    drain_mma(bar_d);
-  }
+  rscan_role(a, &dout_map, sm, tm, blockIdx.x, nullptr);
   tc_fence_before();
-  compute_sync();
+  __syncthreads();
   tc_fence_after();
   if (warp == 0) tmem_dealloc(tm, TMEM_COLS);
 }
@@ -669,12 +418,13 @@ cudaError_t launch_scan_bwd_tc(const ChunkBwdArgs& a, cudaStream_t s) {
   // tokens, 128-byte swizzled like the shared-memory tiles
   PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
   if (!encode) return cudaErrorNotSupported;
-  CUtensorMap map;
+  CUtensorMap map{};  // with no chunks (T = 0) nothing is loaded: dh0 = dh_final
   const cuuint64_t dims[3] = {(cuuint64_t)TD, (cuuint64_t)a.H, (cuuint64_t)a.B * a.T};
   const cuuint64_t strides[2] = {(cuuint64_t)TD * 2, (cuuint64_t)a.H * TD * 2};
   const cuuint32_t box[3] = {64, 1, (cuuint32_t)C};
   const cuuint32_t estr[3] = {1, 1, 1};
-  if (encode(&map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(a.dout), dims, strides, box, estr,
+  if (a.T / C > 0 &&
+      encode(&map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(a.dout), dims, strides, box, estr,
              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
     return cudaErrorInvalidValue;

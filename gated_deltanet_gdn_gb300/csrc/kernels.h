@@ -34,8 +34,11 @@ struct ResidualLayout {
 };
 
 struct BwdWorkspaceLayout {
-  size_t du, dstate, dqh, dbk, dkt, daqk, dakk, dgam, dbv, dbpart, dgpart, total;
-  size_t du_b, dstate_b, dqh_b, dbk_b, dkt_b, daqk_b, dakk_b, dgam_b, dbv_b, dbpart_b, dgpart_b;
+  // sync (bf16 with Dk = Dv = 128 only): the fused backward launch's counters, sync_bytes
+  // bytes, zeroed before each launch: one per (batch, head) on its own 128-byte line (chunks
+  // the reverse scan has finished), then the work queue's next unit on a line of its own
+  size_t du, dstate, sync, dqh, dbk, dkt, daqk, dakk, dgam, dbv, dbpart, dgpart, total;
+  size_t du_b, dstate_b, sync_bytes, dqh_b, dbk_b, dkt_b, daqk_b, dakk_b, dgam_b, dbv_b, dbpart_b, dgpart_b;
 };
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -108,6 +111,9 @@ inline BwdWorkspaceLayout bwd_workspace_layout(int B, int T, int H, int DK, int 
   // needs only dU and dS from the reverse scan; the other regions serve the CUDA-core
   // kernels (Dk = 64, or fp32 operands)
   if (es == 2 && DK == 128 && DV == 128) {
+    L.sync_bytes = (size_t)B * H * PROGRESS_STRIDE * 4 + 128;
+    L.sync = off;
+    off = align_up(off + L.sync_bytes, 1024);
     L.total = off;
     return L;
   }
@@ -136,6 +142,8 @@ struct ResidualPtrs {
 struct BwdWorkspacePtrs {
   void *du, *dstate, *dqh, *dbk, *dkt, *daqk, *dakk;
   float *dgam, *dbv, *dbpart, *dgpart;
+  unsigned* sync;     // [B*H][PROGRESS_STRIDE] then the queue line (bf16, Dk = Dv = 128)
+  size_t sync_bytes;  // 0 when the layout has no sync region
 };
 
 struct ChunkFwdArgs {
@@ -214,7 +222,8 @@ enum KernelId {
   K_DQA = 15,           // chunk_dqa_kernel (Dk = 64 path)
   K_BWD_TC = 16,        // chunk_bwd_tc_kernel: every chunk product of the backward, fused, tcgen05
   K_PREP_TC = 17,       // chunk_prep_tc_kernel: the chunk preparation on tcgen05
-  K_COUNT = 18
+  K_BWD_SYNC = 18,      // chunk_bwd_sync_zero_kernel: zeroes the fused backward's counters
+  K_COUNT = 19
 };
 // Records a CUDA event on s before (begin = true) or after a launch when timing is on.
 void prof_mark(KernelId id, cudaStream_t s, bool begin);
@@ -232,8 +241,10 @@ cudaError_t launch_scan_bwd_tc(const ChunkBwdArgs& a, cudaStream_t s);
 // The chunk preparation on tcgen05 (chunk_prep_tc.cu), bf16 operands with Dk = Dv = 128.
 bool prep_tc_applies(int bf16_operands, int DK, int DV);
 cudaError_t launch_chunk_prep_tc(const ChunkFwdArgs& a, cudaStream_t s);
-// The fused chunk-gradient kernel on tcgen05 (chunk_bwd_tc.cu), for bf16 with Dk = Dv = 128;
-// it needs only the du and dstate parts of the backward workspace.
+// The backward of bf16 with Dk = Dv = 128 on tcgen05 (chunk_bwd_tc.cu): the reverse scan and
+// the fused chunk-gradient kernel, as one cooperative launch when the (batch, head) pairs
+// leave SMs free (the gradient CTAs take each chunk as soon as the scan has finished it),
+// else as two launches; it needs only the du, dstate and sync parts of the workspace.
 bool bwd_tc_applies(int DK, int DV);
 cudaError_t launch_chunk_bwd_tc(const ChunkBwdArgs& a, cudaStream_t s);
 // cuTensorMapEncodeTiled through the runtime's driver entry point, resolved once (NULL if

@@ -290,10 +290,12 @@ int gdn_version(void);
  * operands with Dk = Dv = 128), 10 single-token decode (replaces 5 when T = 1),
  * 11 q/k L2 normalisation, 12 its reverse (GDN_FLAG_QK_L2NORM only),
  * 13 replay decode, 14 replay state fold, 15 the backward's products that need
- * no reverse-scan result (Dk = 64 operands), 16 the fused chunk gradients on
- * tcgen05 tensor cores (replaces 3, 4, 6 and 15 for bf16 operands with
- * Dk = Dv = 128), 17 chunk preparation on tcgen05 tensor cores (replaces 0 for
- * bf16 operands with Dk = Dv = 128); gdn_kernel_name(id) names them
+ * no reverse-scan result (Dk = 64 or fp32 operands), 16 the fused chunk
+ * gradients on tcgen05 tensor cores (replaces 3, 4, 6 and 15 for bf16 operands
+ * with Dk = Dv = 128; when B * H is below the SM count the same launch also runs
+ * the reverse scan, which then replaces 9 too), 17 chunk preparation on tcgen05
+ * tensor cores (replaces 0 for bf16 operands with Dk = Dv = 128), 18 the zeroing
+ * of that single backward launch's counters; gdn_kernel_name(id) names them
  * ("" for an unknown id). Not part of the paper's method: instrumentation. */
 int gdn_profile_enable(int on);
 int gdn_profile_read(double* ms, int* launches, int n);
