@@ -225,7 +225,7 @@ def kernel_work(B, T, H, D, es=2):
 # the files the chunk kernels (the ones profiles/traffic.json covers) are compiled from
 CHUNK_KERNEL_SOURCES = ("chunk_fwd.cu", "chunk_bwd.cu", "chunk_grads.cu", "chunk_scan_tc.cu",
                         "chunk_prep_tc.cu", "chunk_bwd_tc.cu", "chunk_prep.cuh", "chunk_dqa.cuh",
-                        "chunk_out.cuh", "common.cuh", "umma.cuh", "kernels.h")
+                        "chunk_out.cuh", "chunk_scan_tc.cuh", "common.cuh", "umma.cuh", "kernels.h")
 
 
 def kernel_source_hash():
