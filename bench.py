@@ -574,7 +574,7 @@ def decode_leg(dev):
     kernel so that no host launch gap falls inside the measurement. B32 H48 (state
     201 MB > L2): 30 steps back to back between two CUDA events, all queued behind a
     spin kernel first. Then replay decode on the B32 batch and the 2048-token prefill
-    of the same geometry."""
+    of the same geometry, token-recurrent and through the chunked forward."""
     import torch
 
     import gated_deltanet_gdn_gb300 as gdn
@@ -636,6 +636,27 @@ def decode_leg(dev):
     torch.cuda.synchronize()
     ms = e0.elapsed_time(e1) / 3
     res["prefill_B2_T2048_H48"] = {"ms": round(ms, 4), "tokens_per_s": round(w.B * w.T / (ms / 1e3), 1)}
+    # the same prefill through the chunked forward (out and h_final; scalar decay with the
+    # wipes), fp32 operands and bf16 operands, residuals preallocated
+    for dt in ("f32", "bf16"):
+        wv = w.with_(dtype=dt)
+        dv = {k: (None if v is None else v.to(dev)) for k, v in make_inputs(wv).items()}
+        dims = gdn.make_dims(dv["q"], dv["v"], dv["g"], 0)
+        rbuf = torch.empty(gdn.gdn_chunk_residual_bytes(dims), dtype=torch.uint8, device=dev)
+        for _ in range(3):
+            gdn.gdn_chunk_fwd(dv["q"], dv["k"], dv["v"], dv["g"], dv["beta"], None, residuals=rbuf)
+        torch.cuda.synchronize()
+        e0.record()
+        for _ in range(10):
+            gdn.gdn_chunk_fwd(dv["q"], dv["k"], dv["v"], dv["g"], dv["beta"], None, residuals=rbuf)
+        e1.record()
+        torch.cuda.synchronize()
+        cms = e0.elapsed_time(e1) / 10
+        res["prefill_chunked_B2_T2048_H48_" + dt] = {
+            "ms": round(cms, 4), "tokens_per_s": round(w.B * w.T / (cms / 1e3), 1),
+            "speedup_vs_recurrent": round(ms / cms, 2),
+            "workload": "B2 T2048 H48 Dk=Dv=128 %s operands, scalar decay with wipes, chunked forward" % dt}
+        del dv, rbuf
     peaks = load_peaks()
     res["hbm_peak_gbs"] = peaks["hbm_gbs"]
     return res
