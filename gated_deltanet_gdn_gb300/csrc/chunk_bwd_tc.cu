@@ -278,10 +278,13 @@ __global__ void __launch_bounds__(BT_THREADS, 1)
       n = u % N;
     }
   };
-  // fused: the reverse scan has stored chunk n's dU and dS records
-  auto wait_scan = [&](int n, int bh) {
+  // fused: the reverse scan has stored chunk n's dU and dS records. Group A's loader
+  // acquires the head's counter; group B's loads of the same chunk are issued later by
+  // another thread, after CTA barriers that follow that acquire, so they need only the
+  // proxy fence (a GPU-scope acquire costs about 700 cycles of the issuing warp)
+  auto wait_scan = [&](int n, int bh, bool acquire) {
     if (fused) {
-      wait_counter(sync.progress + (size_t)bh * PROGRESS_STRIDE, (unsigned)(N - n), a.err);
+      if (acquire) wait_counter(sync.progress + (size_t)bh * PROGRESS_STRIDE, (unsigned)(N - n), a.err);
       fence_proxy_async_global();
     }
   };
@@ -290,7 +293,7 @@ __global__ void __launch_bounds__(BT_THREADS, 1)
   auto load_a = [&](int m) {
     int n, bh;
     unit_of(m, n, bh);
-    wait_scan(n, bh);
+    wait_scan(n, bh, true);
     const size_t ch = (size_t)bh * N + n;
     mbar_arrive_expect_tx(fullA, L::TXA);
     bulk_g2s(sm + L::TM, static_cast<const bf16*>(a.res.tmat) + ch * (C * C), C * C * 2, fullA);
@@ -299,10 +302,10 @@ __global__ void __launch_bounds__(BT_THREADS, 1)
     tma_load_3d(sm + L::VT, &v_map, 0, h, tok, fullA);                // v, columns 0-63
     tma_load_3d(sm + L::VT + C * 128, &v_map, 64, h, tok, fullA);     // columns 64-127
   };
-  auto load_b = [&](int m) {
+  auto load_b = [&](int m) {  // after load_a(m): by the same thread, or past CTA barriers
     int n, bh;
     unit_of(m, n, bh);
-    wait_scan(n, bh);
+    wait_scan(n, bh, false);
     const size_t ch = (size_t)bh * N + n;
     mbar_arrive_expect_tx(fullB, L::TXB);
     const int b = bh / a.H, h = bh % a.H, tok = b * a.T + n * C;
@@ -367,8 +370,13 @@ __global__ void __launch_bounds__(BT_THREADS, 1)
   float Greg[TPT];
   float Gb = 0.f, GC = 0.f;
   int cur_n = 0, cur_bh = 0;  // the chunk whose final epilogue is pending
-  int nproc = 0;              // units this CTA processed
-  unsigned nxt = 0;           // thread 0, fused: the unit claimed for step m + 1
+  int nproc = 0;  // units this CTA processed
+  // thread 0, fused: units are claimed two steps ahead, so that an atomic's round trip
+  // has a whole step to return before its value is needed (a step-ahead claim held
+  // thread 0 about 450 cycles per step). pend0: the unit of step m + 1, stored into
+  // units_s during step m; pend1: the unit of step m + 2, claimed at the top of step m.
+  unsigned pend0 = 0, pend1 = 0;
+  if (fused && tid == 0) pend0 = units_s[0] < units ? atomicAdd(sync.queue, 1u) : (unsigned)units;
 
 #pragma unroll 1
   for (int m = 0;; ++m) {
@@ -376,9 +384,7 @@ __global__ void __launch_bounds__(BT_THREADS, 1)
     const uint32_t par = (uint32_t)m & 1u;
     int n = 0, bh = 0;
     if (cur) unit_of(m, n, bh);
-    // claimed now, published to units_s before the barrier that precedes the first load
-    // of step m + 1 (the atomic's latency hides behind the epilogues in between)
-    if (fused && cur && tid == 0) nxt = atomicAdd(sync.queue, 1u);
+    if (fused && cur && tid == 0) pend1 = pend0 < (unsigned)units ? atomicAdd(sync.queue, 1u) : (unsigned)units;
     bool q_early = true;  // this chunk's group Q loads were issued at the start of (b)
     // this chunk's beta, read while the previous chunk's final epilogue runs
     float beta_pre = 0.f;
@@ -559,7 +565,10 @@ __global__ void __launch_bounds__(BT_THREADS, 1)
       const float p = warp_sum16(pv, lane);
       if ((lane & 1) == 0) dbv_s[qw * C + t_beg + (lane >> 1)] = p;
     }
-    if (fused && tid == 0) units_s[(m + 1) & 3] = (int)nxt;
+    if (fused && tid == 0) {  // before the barrier that precedes the first load of step m + 1
+      units_s[(m + 1) & 3] = (int)pend0;
+      pend0 = pend1;
+    }
     fence_proxy_async();  // the Y rows are read by the tensor cores
     tc_fence_before();
     epi_sync();
