@@ -856,16 +856,18 @@ cudaError_t launch_chunk_bwd_tc(const ChunkBwdArgs& a, cudaStream_t s) {
   // memory admits one), so every wait of a gradient CTA has the scan CTA it waits for
   // resident. The counters start from zero on every call (chunk_bwd_sync_zero_kernel).
   const bool fused = coop && BH < nsm && units > 0 && a.ws.sync && a.ws.sync_bytes > 0;
-  if (!fused) {
-    if ((e = launch_scan_bwd_tc(a, s)) != cudaSuccess) return e;
+  auto two_launches = [&]() {  // the reverse scan, then the gradients over a static stride
+    cudaError_t e2;
+    if ((e2 = launch_scan_bwd_tc(a, s)) != cudaSuccess) return e2;
     const int grid = units < nsm ? units : nsm;
     if (grid == 0) return cudaSuccess;
     prof_mark(K_BWD_TC, s, true);
-    e = launch_pdl(kern, dim3(grid), dim3(BT_THREADS), bytes, s, a, map, vmap, qmap, kmap, gmap,
-                   BwdSync{nullptr, nullptr, 0});
+    e2 = launch_pdl(kern, dim3(grid), dim3(BT_THREADS), bytes, s, a, map, vmap, qmap, kmap, gmap,
+                    BwdSync{nullptr, nullptr, 0});
     prof_mark(K_BWD_TC, s, false);
-    return e;
-  }
+    return e2;
+  };
+  if (!fused) return two_launches();
   prof_mark(K_BWD_SYNC, s, true);
   chunk_bwd_sync_zero_kernel<<<1, 256, 0, s>>>(a.ws.sync, (int)(a.ws.sync_bytes / 4));
   prof_mark(K_BWD_SYNC, s, false);
@@ -886,6 +888,11 @@ cudaError_t launch_chunk_bwd_tc(const ChunkBwdArgs& a, cudaStream_t s) {
   prof_mark(K_BWD_TC, s, true);
   e = cudaLaunchKernelEx(&cfg, kern, a, map, vmap, qmap, kmap, gmap, sync);
   prof_mark(K_BWD_TC, s, false);
+  if (e == cudaErrorCooperativeLaunchTooLarge) {
+    // the context cannot keep a CTA on every SM at once (an SM-limited partition)
+    (void)cudaGetLastError();
+    return two_launches();
+  }
   return e;
 }
 

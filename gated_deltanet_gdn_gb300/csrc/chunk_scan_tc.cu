@@ -393,7 +393,7 @@ cudaError_t launch_scan_fwd_tc(const ChunkFwdArgs& a, cudaStream_t s, bool* outp
   // outputs beside the scan when SMs are left over: one cooperative grid of one CTA per SM
   // (the kernel's shared memory admits one), so every output CTA's wait has its scan CTA
   // resident
-  const bool with_out = a.res.progress && coop && BH < nsm && a.T / C > 0;
+  bool with_out = a.res.progress && coop && BH < nsm && a.T / C > 0;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(with_out ? nsm : BH);
   cfg.blockDim = dim3(FWD_THREADS);
@@ -408,6 +408,15 @@ cudaError_t launch_scan_fwd_tc(const ChunkFwdArgs& a, cudaStream_t s, bool* outp
   cfg.numAttrs = with_out ? 2 : 1;
   prof_mark(K_SCAN_FWD_TC, s, true);
   e = cudaLaunchKernelEx(&cfg, chunk_scan_fwd_tc_kernel, a, (int)with_out);
+  if (e == cudaErrorCooperativeLaunchTooLarge && with_out) {
+    // the context cannot keep a CTA on every SM at once (an SM-limited partition): the
+    // scan alone, and the outputs by their own kernel after it
+    (void)cudaGetLastError();
+    with_out = false;
+    cfg.gridDim = dim3(BH);
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, chunk_scan_fwd_tc_kernel, a, 0);
+  }
   prof_mark(K_SCAN_FWD_TC, s, false);
   if (e == cudaSuccess) *outputs_done = with_out;
   return e;

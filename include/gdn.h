@@ -139,7 +139,9 @@ size_t gdn_chunk_bwd_workspace_bytes(const gdn_dims* dims);
  * With bf16 operands, Dk = Dv = 128 and fewer (batch, head) pairs than SMs,
  * the scan and the chunk outputs run as one cooperative launch of one CTA per
  * SM (output CTAs beside the scan CTAs, synchronised through counters in the
- * residual buffer); it starts once every CTA can be resident at once. */
+ * residual buffer); it starts once every CTA can be resident at once. Where the
+ * context cannot hold one CTA per SM at once (an SM-limited partition), the scan
+ * and the outputs run as two launches instead. */
 int gdn_chunk_fwd(const gdn_dims* dims, const void* q, const void* k, const void* v,
                   const void* g, const void* beta, const float* h0, float scale, void* out,
                   float* h_final, void* residuals, void* stream);
@@ -155,7 +157,11 @@ int gdn_chunk_fwd(const gdn_dims* dims, const void* q, const void* k, const void
  * Same inputs as the forward plus the residuals it wrote, dout [B,T,H,Dv] and
  * dh_final (NULL = zeros). Writes dq, dk, dv, dg, dbeta and dh0 (may be NULL).
  * workspace: gdn_chunk_bwd_workspace_bytes(dims) bytes, 256-byte aligned,
- * caller-owned, overwritten. dims.dtype is that of the forward call that wrote
+ * caller-owned, overwritten. With bf16 operands, Dk = Dv = 128 and fewer
+ * (batch, head) pairs than SMs, the reverse scan and the chunk gradients run as
+ * one cooperative launch of one CTA per SM, synchronised through counters in
+ * the workspace that a one-CTA kernel zeroes before it (two launches where the
+ * context cannot hold that grid). dims.dtype is that of the forward call that wrote
  * the residuals (bfloat16 or float32 operands; the state gradient is fp32 in
  * both); errors as listed at the top of this file. */
 int gdn_chunk_bwd(const gdn_dims* dims, const void* q, const void* k, const void* v,
