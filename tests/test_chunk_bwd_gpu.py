@@ -2,7 +2,8 @@
 hand-derived float64 reverse pass: rel-L2 <= 2e-2 per gradient with bf16 inputs,
 1e-4 with fp32 inputs.
 
-Includes the training-shape fwd+bwd workload (B8 T4096 H6 D128 bf16) at full
+Also: a training step captured in a CUDA graph replays bitwise. Includes the
+training-shape fwd+bwd workload (B8 T4096 H6 D128 bf16) at full
 size with the same launch the benchmark times; the oracle checks every
 (batch, head) pair there.
 """
@@ -286,3 +287,57 @@ def test_fp32_training_shape_slice():
     print("\nfp32 training shape B4 T4096 H6 D128, batches 0-1, rel-L2 vs oracle:")
     for n, r in report.items():
         print(f"  {n:8s} {r:.3e}")
+
+
+def _graph_step_buffers(d):
+    dims = gdn.make_dims(d["q"], d["v"], d["g"], 0)
+    bufs = {
+        "res": torch.empty(gdn.gdn_chunk_residual_bytes(dims), dtype=torch.uint8, device="cuda"),
+        "ws": torch.empty(gdn.gdn_chunk_bwd_workspace_bytes(dims), dtype=torch.uint8, device="cuda"),
+        "out": torch.empty_like(d["v"]),
+        "hT": torch.empty((dims.B, dims.H, dims.Dk, dims.Dv), dtype=torch.float32, device="cuda"),
+    }
+    grads = {"dq": torch.empty_like(d["q"]), "dk": torch.empty_like(d["k"]), "dv": torch.empty_like(d["v"]),
+             "dg": torch.empty_like(d["g"]), "dbeta": torch.empty_like(d["beta"]),
+             "dh0": torch.empty((dims.B, dims.H, dims.Dk, dims.Dv), dtype=torch.float32, device="cuda")}
+    return bufs, grads
+
+
+@pytest.mark.parametrize("H", [3, 80])
+def test_cuda_graph_capture_of_a_training_step(H):
+    """A chunked fwd + bwd step captured in a CUDA graph replays to the same bits as the
+    eager calls, twice: with B*H below the SM count (cooperative single launches,
+    programmatic dependent launches and the counter-zeroing kernel inside the graph) and
+    above it (split launches)."""
+    w = WORKLOADS["train_fwdbwd"].with_(B=2, T=256, H=H, h0_std=0.2)
+    d = cuda_inputs(make_inputs(w))
+    bufs, grads = _graph_step_buffers(d)
+
+    def step():
+        gdn.gdn_chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], d["h0"], out=bufs["out"],
+                          h_final=bufs["hT"], residuals=bufs["res"])
+        gdn.gdn_chunk_bwd(d["q"], d["k"], d["v"], d["g"], d["beta"], d["h0"], bufs["res"], d["dout"],
+                          d["dh_final"], workspace=bufs["ws"], grads=grads)
+
+    step()
+    torch.cuda.synchronize()
+    eager = {n: t.clone() for n, t in grads.items()}
+    eager["out"], eager["hT"] = bufs["out"].clone(), bufs["hT"].clone()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        step()
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        step()
+    for _ in range(2):
+        for t in list(grads.values()) + [bufs["out"], bufs["hT"]]:
+            t.zero_()
+        graph.replay()
+        torch.cuda.synchronize()
+        got = dict(grads, out=bufs["out"], hT=bufs["hT"])
+        for n, t in eager.items():
+            assert torch.equal(got[n], t), n
+    assert gdn.gdn_check_device_error() == gdn.binding.GDN_OK
