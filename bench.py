@@ -442,18 +442,20 @@ def run_gdn(args, world, rank, local):
 def variants_leg(args, w, host, dev):
     """The same fwd+bwd step for the input variants the library also supports: q/k
     L2-normalised in the library (GDN_FLAG_QK_L2NORM, raw q and k of norm ~ sqrt(Dk)), one
-    scalar decay per head (g [B,T,H]) and fp32 operands (the CUDA-core kernel chain).
-    CUDA events around N steps each."""
+    scalar decay per head (g [B,T,H]), fp32 operands (the CUDA-core kernel chain), and the
+    long-context shape B1 T32768 H16 (16 scan chains of 512 chunks). CUDA events around N
+    steps each."""
     import torch
 
     import gated_deltanet_gdn_gb300 as gdn
-    from gated_deltanet_gdn_gb300.synthetic import make_inputs
+    from gated_deltanet_gdn_gb300.synthetic import WORKLOADS, make_inputs
 
     res = {}
     n = max(3, min(100, args.steps))
     for name, wv, flags in (("qk_l2norm", w.with_(normalize_qk=False), gdn.GDN_FLAG_QK_L2NORM),
                             ("scalar_decay", w.with_(g_per_channel=False, g_kind="logsigmoid", g_mu=2.0), 0),
-                            ("fp32", w.with_(dtype="f32"), 0)):
+                            ("fp32", w.with_(dtype="f32"), 0),
+                            ("long_context", WORKLOADS["long_context"], 0)):
         d = {k: (None if v is None else v.to(dev)) for k, v in make_inputs(wv).items()}
         dims = gdn.make_dims(d["q"], d["v"], d["g"], flags)
         res_buf = torch.empty(gdn.gdn_chunk_residual_bytes(dims), dtype=torch.uint8, device=dev)
@@ -478,7 +480,9 @@ def variants_leg(args, w, host, dev):
                      "workload": "B%d T%d H%d D%d %s, %s" % (
                          wv.B, wv.T, wv.H, wv.Dk, wv.dtype,
                          "raw q/k normalised in the library" if flags else
-                         "fp32 operands" if name == "fp32" else "scalar decay logsigmoid(N(2,1)) per head")}
+                         "fp32 operands" if name == "fp32" else
+                         "long context, per-channel decay -softplus(N(-1,1)), nonzero h0" if name == "long_context"
+                         else "scalar decay logsigmoid(N(2,1)) per head")}
         del d, res_buf, ws
     return res
 
