@@ -17,13 +17,12 @@
 // stage kernels that reuse forward residuals, with the pairwise-decay score backward
 // as one of them; the staging here is this library's own.
 //
-// Kernels
+// Kernels of the CUDA-core path (Dk = 64, or fp32 operands; bf16 with Dk = Dv = 128 runs
+// chunk_bwd_tc.cu instead), launched in this order on the caller's stream:
 //   chunk_scan_bwd_kernel   grid (Dv/64, B*H), 256 threads, sequential over chunks in
 //                           reverse: dS in registers, writes dU and dS1 per chunk, dh0
-//   chunk_dqa_kernel        grid (chunks, B*H), 256 threads: dQ-hat and dAqk, the products
-//                           that need only forward records and dO; launched on a second
-//                           stream so that it runs beside the reverse scan, whose one CTA
-//                           per (b, h) leaves most SMs free
+//   chunk_dqa_kernel        one CTA per chunk-head, 256 threads: dQ-hat and dAqk, the
+//                           products that need only forward records and dO
 //   chunk_dstate_kernel     grid (chunks, B*H), 256 threads: the products with dU and dS1
 //                           (contractions over Dv) and dgam
 //   chunk_grads_kernel      (chunk_grads.cu) everything else

@@ -38,6 +38,14 @@
 // is issued as soon as the buffer it fills is released (T and dU^T once P1 has read them,
 // q and k once P5 and P6 have, the rest once P2-P4 and the gamma-gradient sums have), so
 // the next chunk's loads overlap this chunk's later phases. Every wait is bounded.
+//
+// Two launch shapes. With fewer (batch, head) pairs than SMs, one cooperative grid of one
+// CTA per SM runs the reverse scan as well: CTAs 0 .. B*H-1 first run rscan_role
+// (chunk_scan_tc.cuh) for their (batch, head), publishing as they go how many chunks'
+// dU and dS records are stored, then join the others, which take chunk-heads from a queue
+// in the order the scan finishes them and wait (bounded) on those counters before loading
+// a chunk's records. Otherwise the reverse scan is a launch of its own before this one,
+// and the CTAs stride over the chunk-heads.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
