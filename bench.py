@@ -484,7 +484,62 @@ def variants_leg(args, w, host, dev):
                          "long context, per-channel decay -softplus(N(-1,1)), nonzero h0" if name == "long_context"
                          else "scalar decay logsigmoid(N(2,1)) per head")}
         del d, res_buf, ws
+    res["chunk128_forward"] = chunk128_leg(args, w, host, dev)
     return res
+
+
+def chunk128_leg(args, w, host, dev):
+    """The forward alone on the headline inputs with 64-token chunks (the step's forward)
+    and with 128-token chunks (GDN_FLAG_CHUNK128: the 64-token blocks' records from the
+    same preparation, merged, then the CUDA-core scan and outputs over 128-token chunks;
+    forward only). CUDA events around N calls each, the per-kernel split of the 128-token
+    forward from the library's launch events, and its whole-forward bytes against HBM:
+    q, k, v, g, beta and h0 read, out and h_final written, plus the chunk-start states
+    (bf16, one per 128-token chunk) written once."""
+    import torch
+
+    import gated_deltanet_gdn_gb300 as gdn
+
+    d = {k: (None if v is None else v.to(dev)) for k, v in host.items()}
+    n = max(3, min(100, args.steps))
+    out = {}
+    for name, flags in (("chunk64", 0), ("chunk128", gdn.GDN_FLAG_CHUNK128)):
+        dims = gdn.make_dims(d["q"], d["v"], d["g"], flags)
+        rbuf = torch.empty(gdn.gdn_chunk_residual_bytes(dims), dtype=torch.uint8, device=dev)
+
+        def fwd():
+            return gdn.gdn_chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], d["h0"], residuals=rbuf,
+                                     flags=flags)
+
+        for _ in range(3):
+            fwd()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(n):
+            fwd()
+        e1.record()
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / n
+        out[name] = {"ms": round(ms, 4), "tokens_per_s": round(w.B * w.T / (ms / 1e3), 1)}
+        if flags:
+            gdn.gdn_profile_enable(True)
+            for _ in range(n):
+                fwd()
+            prof = gdn.gdn_profile_read()
+            gdn.gdn_profile_enable(False)
+            out[name]["kernels_ms"] = {k: round(v[0] / max(1, v[1]), 4) for k, v in prof.items()}
+            BTH, D = w.B * w.T * w.H, w.Dk
+            fwd_bytes = BTH * (4 * D * 2 + 2) + 2 * w.B * w.H * D * D * 4 + BTH * D * 2 \
+                + (w.T // 128) * w.B * w.H * D * D * 2
+            peaks = load_peaks()
+            gbs = fwd_bytes / (ms / 1e3) / 1e9
+            out[name]["roofline"] = {"bound": "hbm", "method_bytes": int(fwd_bytes), "achieved": round(gbs, 1),
+                                     "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                                     "frac": round(gbs / peaks["hbm_gbs"], 4)}
+        del rbuf
+    out["workload"] = "forward only, B%d T%d H%d D%d bf16, per-channel decay" % (w.B, w.T, w.H, w.Dk)
+    return out
 
 
 def e2e_leg(args, host, d, step, outputs, world):

@@ -27,7 +27,9 @@ GDN_F32 = 0
 GDN_BF16 = 1
 GDN_FLAG_PAIRWISE_WITHIN_BLOCK = 1
 GDN_FLAG_QK_L2NORM = 2
+GDN_FLAG_CHUNK128 = 4
 GDN_CHUNK = 64
+GDN_CHUNK128 = 128
 
 # every symbol include/gdn.h declares
 EXPORTED = ("gdn_chunk_residual_bytes", "gdn_chunk_bwd_workspace_bytes", "gdn_chunk_fwd",
@@ -35,7 +37,7 @@ EXPORTED = ("gdn_chunk_residual_bytes", "gdn_chunk_bwd_workspace_bytes", "gdn_ch
             "gdn_version", "gdn_profile_enable", "gdn_profile_read", "gdn_kernel_name",
             "gdn_chunk_fwd_noalloc", "gdn_replay_buffer_bytes", "gdn_replay_decode",
             "gdn_replay_state", "gdn_selftest_wait_timeout")
-KERNEL_COUNT = 19
+KERNEL_COUNT = 20
 GDN_REPLAY_MAX_TOKENS = 8
 
 

@@ -19,7 +19,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(PKG, "_build")
 LIB_PATH = os.path.join(PKG, "libgdn.so")
 SOURCES = ["api.cu", "recurrent.cu", "decode.cu", "l2norm.cu", "chunk_fwd.cu", "chunk_bwd.cu",
-           "chunk_grads.cu", "chunk_scan_tc.cu", "chunk_bwd_tc.cu", "chunk_prep_tc.cu", "noalloc.cu", "replay.cu"]
+           "chunk_grads.cu", "chunk_scan_tc.cu", "chunk_bwd_tc.cu", "chunk_prep_tc.cu", "chunk_merge.cu", "noalloc.cu", "replay.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC",
                      "--expt-relaxed-constexpr", "-I", INCLUDE]

@@ -75,8 +75,9 @@ int check_dims(const gdn_dims* d, bool chunked) {
   if (d->dtype != GDN_F32 && d->dtype != GDN_BF16) return GDN_ERR_UNSUPPORTED;
   if ((d->Dk != 64 && d->Dk != 128) || (d->Dv != 64 && d->Dv != 128)) return GDN_ERR_UNSUPPORTED;
   if ((long long)d->B * d->H > 65535) return GDN_ERR_UNSUPPORTED;  // grid y limit
-  if (d->flags & ~(GDN_FLAG_PAIRWISE_WITHIN_BLOCK | GDN_FLAG_QK_L2NORM)) return GDN_ERR_INVALID_ARG;
-  if (chunked && d->T % GDN_CHUNK != 0) return GDN_ERR_SHAPE;
+  if (d->flags & ~(GDN_FLAG_PAIRWISE_WITHIN_BLOCK | GDN_FLAG_QK_L2NORM | GDN_FLAG_CHUNK128))
+    return GDN_ERR_INVALID_ARG;
+  if (chunked && d->T % ((d->flags & GDN_FLAG_CHUNK128) ? GDN_CHUNK128 : GDN_CHUNK) != 0) return GDN_ERR_SHAPE;
   return GDN_OK;
 }
 
@@ -89,9 +90,29 @@ bool optional_ok(const void* p) { return !p || aligned(p, 16); }
 bool gate_ok(const void* p, bool has_work, int es) { return !has_work || (p && aligned(p, es)); }
 
 bool qk_norm(const gdn_dims* d) { return (d->flags & GDN_FLAG_QK_L2NORM) != 0; }
+bool chunk128(const gdn_dims* d) { return (d->flags & GDN_FLAG_CHUNK128) != 0; }
+
+ResidualLayout residual_layout_of(const gdn_dims* d) {
+  return residual_layout(d->B, d->T, d->H, d->Dk, d->Dv, esize(d), qk_norm(d), chunk128(d));
+}
+
+Residual128Ptrs residual128_ptrs(const gdn_dims* d, void* base) {
+  const ResidualLayout L = residual_layout_of(d);
+  char* b = static_cast<char*>(base);
+  Residual128Ptrs r;
+  r.aqk = b + L.aqk2;
+  r.wneg = b + L.wneg2;
+  r.up = b + L.up2;
+  r.qh = b + L.qh2;
+  r.kt = b + L.kt2;
+  r.gam = reinterpret_cast<float*>(b + L.gam2);
+  r.state = b + L.state2;
+  r.u = b + L.u2;
+  return r;
+}
 
 ResidualPtrs residual_ptrs(const gdn_dims* d, void* base) {
-  const ResidualLayout L = residual_layout(d->B, d->T, d->H, d->Dk, d->Dv, esize(d), qk_norm(d));
+  const ResidualLayout L = residual_layout_of(d);
   char* b = static_cast<char*>(base);
   ResidualPtrs r;
   r.aqk = b + L.aqk;
@@ -154,7 +175,7 @@ const char* kKernelNames[K_COUNT] = {"chunk_prep_kernel",    "chunk_scan_fwd_ker
                                      "decode_kernel", "l2norm_rows_kernel", "l2norm_bwd_kernel",
                                      "replay_decode_kernel", "replay_state_kernel", "chunk_dqa_kernel",
                                      "chunk_bwd_tc_kernel", "chunk_prep_tc_kernel",
-                                     "chunk_bwd_sync_zero_kernel"};
+                                     "chunk_bwd_sync_zero_kernel", "chunk_merge128_kernel"};
 
 }  // namespace
 
@@ -187,11 +208,11 @@ extern "C" {
 
 size_t gdn_chunk_residual_bytes(const gdn_dims* d) {
   if (check_dims(d, true) != GDN_OK) return 0;
-  return residual_layout(d->B, d->T, d->H, d->Dk, d->Dv, esize(d), qk_norm(d)).total;
+  return residual_layout_of(d).total;
 }
 
 size_t gdn_chunk_bwd_workspace_bytes(const gdn_dims* d) {
-  if (check_dims(d, true) != GDN_OK) return 0;
+  if (check_dims(d, true) != GDN_OK || chunk128(d)) return 0;
   return bwd_workspace_layout(d->B, d->T, d->H, d->Dk, d->Dv, esize(d)).total;
 }
 
@@ -217,7 +238,10 @@ int gdn_chunk_fwd(const gdn_dims* d, const void* q, const void* k, const void* v
   a.flags = d->flags;
   a.q = q; a.k = k; a.v = v; a.g = g; a.beta = beta; a.h0 = h0; a.scale = scale;
   a.out = out; a.h_final = h_final;
-  if (residuals) a.res = residual_ptrs(d, residuals);
+  if (residuals) {
+    a.res = residual_ptrs(d, residuals);
+    if (chunk128(d)) a.res2 = residual128_ptrs(d, residuals);
+  }
   a.err = device_error_word();
   if (!a.err) return GDN_ERR_CUDA;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -237,6 +261,7 @@ int gdn_chunk_bwd(const gdn_dims* d, const void* q, const void* k, const void* v
                   void* dbeta, float* dh0, void* workspace, void* stream) {
   int st = check_dims(d, true);
   if (st != GDN_OK) return st;
+  if (chunk128(d)) return GDN_ERR_UNSUPPORTED;  // the backward works on 64-token chunks only
   if (!std::isfinite(scale)) return GDN_ERR_INVALID_ARG;
   const bool work = (long long)d->B * d->H * d->T > 0;
   const int es = esize(d);

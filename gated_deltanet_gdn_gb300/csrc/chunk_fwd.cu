@@ -380,40 +380,55 @@ __global__ void __launch_bounds__(PREP_THREADS) chunk_prep_kernel(ChunkFwdArgs a
 // Only the recurrence is sequential: U = U' + (-W) S and S <- diag(gam) S + K-tilde^T U.
 // The outputs O = (scale Q-hat) S + (scale Aqk) U need no sequential order and are
 // produced afterwards by chunk_out_kernel from the states and U this scan stores.
-template <class T, int DK>
+// CC: chunk length, C or C2 (128-token chunks, whose records chunk_merge.cu forms)
+template <class T, int DK, int CC = C>
 struct ScanLayout {
   static constexpr int ES = (int)sizeof(T);
-  static constexpr int W = 0;                        // -W        [C][DK]
-  static constexpr int KT = W + C * DK * ES;         // K-tilde   [C][DK]
-  static constexpr int UP = KT + C * DK * ES;        // U'^T rows of this slice [NTS][C]
-  static constexpr int GAM = UP + C * NTS * ES;      // float [DK]
+  static constexpr int W = 0;                         // -W        [CC][DK]
+  static constexpr int KT = W + CC * DK * ES;         // K-tilde   [CC][DK]
+  static constexpr int UP = KT + CC * DK * ES;        // U'^T rows of this slice [NTS][CC]
+  static constexpr int GAM = UP + CC * NTS * ES;      // float [DK]
   static constexpr int STAGE = a1k(GAM + DK * 4);
-  static constexpr int STAGES = ES == 2 ? 4 : 1;
-  static constexpr int SS = STAGES * STAGE;          // state operand, transposed [NTS][DK]
-  static constexpr int US = a1k(SS + DK * NTS * ES); // U, transposed [NTS][C]
-  static constexpr int BAR = a1k(US + C * NTS * ES);
+  static constexpr int STAGES = ES == 2 ? (CC == C ? 4 : 2) : 1;
+  static constexpr int SS = STAGES * STAGE;           // state operand, transposed [NTS][DK]
+  static constexpr int US = a1k(SS + DK * NTS * ES);  // U, transposed [NTS][CC]
+  static constexpr int BAR = a1k(US + CC * NTS * ES);
   static constexpr int BYTES = BAR + 64;
-  static constexpr uint32_t TX = (uint32_t)(2 * C * DK * ES + C * NTS * ES + DK * 4);
+  static constexpr uint32_t TX = (uint32_t)(2 * CC * DK * ES + CC * NTS * ES + DK * 4);
 };
 
+// The records a scan or output kernel over CC-token chunks reads and writes.
+struct ChunkRecs {
+  void *aqk, *wneg, *up, *qh, *kt;
+  const float* gam;
+  void *state, *u;
+};
+template <int CC>
+__device__ __forceinline__ ChunkRecs chunk_recs(const ChunkFwdArgs& a) {
+  if (CC == C) return ChunkRecs{a.res.aqk, a.res.wneg, a.res.up, a.res.qh, a.res.kt, a.res.gam, a.res.state, a.res.u};
+  return ChunkRecs{a.res2.aqk, a.res2.wneg, a.res2.up, a.res2.qh, a.res2.kt, a.res2.gam, a.res2.state, a.res2.u};
+}
+
 // One CTA per (batch*head, NTS = 64 value columns), 8 warps. Warp w owns state rows
-// (w & 3) * Dk/4 .. + Dk/4 and columns 32 (w >> 2) .. + 31 of the slice. The state and U
-// records are stored transposed (value rows): S^T [Dv][Dk] and U^T [Dv][C]; this CTA
-// writes their rows tile * NTS .. + NTS - 1.
-template <class T, int DK, int DV>
+// (w & 3) * Dk/4 .. + Dk/4 and columns 32 (w >> 2) .. + 31 of the slice, and rows
+// (w & 3) * CC/4 .. + CC/4 of U. The state and U records are stored transposed (value
+// rows): S^T [Dv][Dk] and U^T [Dv][CC]; this CTA writes their rows tile * NTS .. + NTS - 1.
+template <class T, int DK, int DV, int CC = C>
 __global__ void __launch_bounds__(SCAN_THREADS) chunk_scan_fwd_kernel(ChunkFwdArgs a) {
-  typedef ScanLayout<T, DK> L;
+  typedef ScanLayout<T, DK, CC> L;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = align1024(smem_raw);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int tile = blockIdx.x, bh = blockIdx.y;
-  const int N = a.T / C;
+  const int N = a.T / CC;
+  const ChunkRecs R = chunk_recs<CC>(a);
   constexpr int MTS = DK / 64;    // m16 tiles of state rows per warp
+  constexpr int MU = CC / 64;     // m16 tiles of U rows per warp
   const int rg = warp & 3, cg = warp >> 2;
-  const int srow = rg * 16 * MTS, col0 = 32 * cg;
+  const int srow = rg * 16 * MTS, col0 = 32 * cg, urow = rg * 16 * MU;
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + L::BAR);
   Tile<T, NTS, DK> Ss{reinterpret_cast<T*>(sm + L::SS)};  // S^T rows of this slice
-  Tile<T, NTS, C> Us{reinterpret_cast<T*>(sm + L::US)};   // U^T rows of this slice
+  Tile<T, NTS, CC> Us{reinterpret_cast<T*>(sm + L::US)};  // U^T rows of this slice
 
   float S[MTS][4][4];
   const size_t sb = (size_t)bh * DK * DV;
@@ -439,16 +454,16 @@ __global__ void __launch_bounds__(SCAN_THREADS) chunk_scan_fwd_kernel(ChunkFwdAr
     uint8_t* st = sm + s * L::STAGE;
     const size_t ch = (size_t)bh * N + n;
     mbar_arrive_expect_tx(&bars[s], L::TX);
-    bulk_g2s(st + L::W, static_cast<const T*>(a.res.wneg) + ch * (C * DK), C * DK * sizeof(T), &bars[s]);
-    bulk_g2s(st + L::KT, static_cast<const T*>(a.res.kt) + ch * (C * DK), C * DK * sizeof(T), &bars[s]);
+    bulk_g2s(st + L::W, static_cast<const T*>(R.wneg) + ch * (CC * DK), CC * DK * sizeof(T), &bars[s]);
+    bulk_g2s(st + L::KT, static_cast<const T*>(R.kt) + ch * (CC * DK), CC * DK * sizeof(T), &bars[s]);
     {  // rows tile * NTS .. + NTS - 1 of U'^T: one piece per column panel
-      constexpr int PW = Sw<T, DV, C>::PW;
-      const T* src = static_cast<const T*>(a.res.up) + ch * (C * DV);
-      for (int p = 0; p < C / PW; ++p)
+      constexpr int PW = Sw<T, DV, CC>::PW;
+      const T* src = static_cast<const T*>(R.up) + ch * (CC * DV);
+      for (int p = 0; p < CC / PW; ++p)
         bulk_g2s(st + L::UP + p * NTS * PW * sizeof(T), src + (size_t)p * DV * PW + (size_t)tile * NTS * PW,
                  NTS * PW * sizeof(T), &bars[s]);
     }
-    bulk_g2s(st + L::GAM, a.res.gam + ch * DK, DK * 4, &bars[s]);
+    bulk_g2s(st + L::GAM, R.gam + ch * DK, DK * 4, &bars[s]);
   };
   if (tid == 0)
     for (int n = 0; n < L::STAGES - 1 && n < N; ++n) issue(n);
@@ -459,9 +474,9 @@ __global__ void __launch_bounds__(SCAN_THREADS) chunk_scan_fwd_kernel(ChunkFwdAr
     // refill the stage freed at the end of the previous step
     if (tid == 0 && n + L::STAGES - 1 < N) issue(n + L::STAGES - 1);
     uint8_t* st = sm + s * L::STAGE;
-    Tile<T, C, DK> Wt{reinterpret_cast<T*>(st + L::W)};
-    Tile<T, C, DK> Kt{reinterpret_cast<T*>(st + L::KT)};
-    Tile<T, NTS, C> Up{reinterpret_cast<T*>(st + L::UP)};  // this slice's rows of U'^T
+    Tile<T, CC, DK> Wt{reinterpret_cast<T*>(st + L::W)};
+    Tile<T, CC, DK> Kt{reinterpret_cast<T*>(st + L::KT)};
+    Tile<T, NTS, CC> Up{reinterpret_cast<T*>(st + L::UP)};  // this slice's rows of U'^T
     const float* gam = reinterpret_cast<const float*>(st + L::GAM);
     const size_t ch = (size_t)bh * N + n;
 
@@ -476,23 +491,25 @@ __global__ void __launch_bounds__(SCAN_THREADS) chunk_scan_fwd_kernel(ChunkFwdAr
     mbar_wait(&bars[s], par, a.err);
     __syncthreads();
     if (tid == 0) {  // residual: chunk-start state
-      store_row_block<T, DV, DK>(static_cast<T*>(a.res.state) + ch * (DK * DV), Ss.p, tile * NTS, NTS);
+      store_row_block<T, DV, DK>(static_cast<T*>(R.state) + ch * (DK * DV), Ss.p, tile * NTS, NTS);
       bulk_commit();
     }
-    float ws[1][4][4];
+    float ws[MU][4][4];
     zero(ws);
-    Gemm<T>::template runk<1, 4, 0, DK>(ws, aview<false>(Wt), bview<false>(Ss), 16 * rg, col0, lane);
+    Gemm<T>::template runk<MU, 4, 0, DK>(ws, aview<false>(Wt), bview<false>(Ss), urow, col0, lane);
 #pragma unroll
-    for (int nt = 0; nt < 4; ++nt)
+    for (int mt = 0; mt < MU; ++mt)
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int r = 16 * rg + frag_row(lane, e), c = col0 + 8 * nt + frag_col(lane, e);
-        Us.at(c, r) = from_f32<T>(to_f32(Up.at(c, r)) + ws[0][nt][e]);
-      }
+      for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int r = urow + 16 * mt + frag_row(lane, e), c = col0 + 8 * nt + frag_col(lane, e);
+          Us.at(c, r) = from_f32<T>(to_f32(Up.at(c, r)) + ws[mt][nt][e]);
+        }
     fence_proxy_async();
     __syncthreads();
     if (tid == 0) {  // residual: U
-      store_row_block<T, DV, C>(static_cast<T*>(a.res.u) + ch * (C * DV), Us.p, tile * NTS, NTS);
+      store_row_block<T, DV, CC>(static_cast<T*>(R.u) + ch * (CC * DV), Us.p, tile * NTS, NTS);
       bulk_commit();
     }
 #pragma unroll
@@ -501,7 +518,7 @@ __global__ void __launch_bounds__(SCAN_THREADS) chunk_scan_fwd_kernel(ChunkFwdAr
       for (int nt = 0; nt < 4; ++nt)
 #pragma unroll
         for (int e = 0; e < 4; ++e) S[mt][nt][e] *= gam[srow + 16 * mt + frag_row(lane, e)];
-    Gemm<T>::template runk<MTS, 4, 0, C>(S, aview<true>(Kt), bview<false>(Us), srow, col0, lane);
+    Gemm<T>::template runk<MTS, 4, 0, CC>(S, aview<true>(Kt), bview<false>(Us), srow, col0, lane);
     if (tid == 0) bulk_wait_read0();  // the bulk stores have read Ss and Us before they are rewritten
     __syncthreads();
   }
@@ -525,13 +542,41 @@ __global__ void __launch_bounds__(SCAN_THREADS) chunk_scan_fwd_kernel(ChunkFwdAr
 
 // ------------------------------------------------------------------ outputs
 // O = (scale Q-hat) S0 + (scale Aqk) U per chunk, from the scan's chunk-start states and U
-// (out_unit, chunk_out.cuh).
-template <class T, int DK, int DV>
+// (out_unit, chunk_out.cuh); one CTA per 64 rows of a chunk.
+template <class T, int DK, int DV, int CC = C>
 __global__ void __launch_bounds__(OUT_THREADS) chunk_out_kernel(ChunkFwdArgs a) {
   pdl_wait();
   pdl_trigger();
   extern __shared__ uint8_t smem_raw[];
-  out_unit<T, DK, DV>(a, blockIdx.x, blockIdx.y, align1024(smem_raw), threadIdx.x);
+  const ChunkRecs R = chunk_recs<CC>(a);
+  out_unit<T, DK, DV, CC>(a, R.qh, R.aqk, R.state, R.u, blockIdx.x, blockIdx.y, align1024(smem_raw), threadIdx.x);
+}
+
+// 128-token chunks: the 64-token blocks' records from the preparation, merged
+// (chunk_merge.cu), then the scan and the outputs over the 128-token chunks.
+template <class T, int DK, int DV>
+cudaError_t launch_fwd128_rest(const ChunkFwdArgs& a, cudaStream_t s) {
+  const int BH = a.B * a.H;
+  cudaError_t e = launch_chunk_merge128(a, s);
+  if (e != cudaSuccess) return e;
+  {
+    const int bytes = ScanLayout<T, DK, C2>::BYTES + 1024;
+    auto kern = chunk_scan_fwd_kernel<T, DK, DV, C2>;
+    if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes)) != cudaSuccess)
+      return e;
+    prof_mark(K_SCAN_FWD, s, true);
+    kern<<<dim3(DV / NTS, BH), SCAN_THREADS, bytes, s>>>(a);
+    prof_mark(K_SCAN_FWD, s, false);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
+  if (a.T == 0) return cudaSuccess;
+  const int bytes = OutLayout<T, DK, DV, C2>::BYTES + 1024;
+  auto kern = chunk_out_kernel<T, DK, DV, C2>;
+  if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes)) != cudaSuccess) return e;
+  prof_mark(K_OUT, s, true);
+  e = launch_pdl(kern, dim3(a.T / C, BH), dim3(OUT_THREADS), bytes, s, a);
+  prof_mark(K_OUT, s, false);
+  return e;
 }
 
 template <class T, int DK, int DV>
@@ -551,6 +596,7 @@ cudaError_t launch_fwd_t(const ChunkFwdArgs& a, cudaStream_t s) {
       prof_mark(K_PREP, s, false);
     }
   }
+  if (a.flags & FLAG_CHUNK128) return launch_fwd128_rest<T, DK, DV>(a, s);
   bool outputs_done = false;
   if (scan_tc_applies(a.bf16, DK, DV)) {
     if ((e = launch_scan_fwd_tc(a, s, &outputs_done)) != cudaSuccess) return e;

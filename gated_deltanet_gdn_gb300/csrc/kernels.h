@@ -9,10 +9,12 @@ namespace gdn {
 
 constexpr int C = 64;       // chunk length (tokens)
 constexpr int BLK = 32;     // block length inside a chunk
+constexpr int C2 = 128;     // chunk length with FLAG_CHUNK128: two 64-token blocks
 constexpr int NT = 32;      // value columns per warp column group of the mma.sync scans
 constexpr int NTS = 64;     // value columns per state-scan CTA (two record slices)
 constexpr float SAFE_SPREAD = 80.f;  // max decay spread (nats) for row-scaled in-block scores
 constexpr int FLAG_PAIRWISE = 1;     // dims.flags bit: in-block scores always pairwise
+constexpr int FLAG_CHUNK128 = 4;     // dims.flags bit: the forward works on 128-token chunks
 // the forward scan's chunk counters, one per (batch, head), each on its own 128-byte line
 // (counter bh at progress[bh * PROGRESS_STRIDE])
 constexpr int PROGRESS_STRIDE = 32;
@@ -31,6 +33,10 @@ struct ResidualLayout {
   size_t aqk, tmat, wneg, up, qh, kt, gam, state, u, progress, qn, kn, qinv, kinv, total;
   // bytes of one chunk-head record
   size_t aqk_b, tmat_b, w_b, up_b, qh_b, kt_b, gam_b, state_b, u_b;
+  // with 128-token chunks: the 128-token records (merged from the 64-token blocks' aqk,
+  // wneg, up, qh, kt and gam above; state and u of the 128-token chunks), same forms with
+  // C2 in place of C; the 64-token layout then has no state or u records
+  size_t aqk2, wneg2, up2, qh2, kt2, gam2, state2, u2;
 };
 
 struct BwdWorkspaceLayout {
@@ -43,7 +49,8 @@ struct BwdWorkspaceLayout {
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-inline ResidualLayout residual_layout(int B, int T, int H, int DK, int DV, int es, bool qk_norm = false) {
+inline ResidualLayout residual_layout(int B, int T, int H, int DK, int DV, int es, bool qk_norm = false,
+                                      bool chunk128 = false) {
   ResidualLayout L{};
   const size_t n = (size_t)B * H * (T / C);
   L.aqk_b = (size_t)C * C * es;
@@ -61,14 +68,30 @@ inline ResidualLayout residual_layout(int B, int T, int H, int DK, int DV, int e
     off = align_up(off + rec * n, 1024);
   };
   put(L.aqk, L.aqk_b);
-  put(L.tmat, L.tmat_b);
+  put(L.tmat, L.tmat_b);  // written by the preparation; read by the backward only
   put(L.wneg, L.w_b);
   put(L.up, L.up_b);
   put(L.qh, L.qh_b);
   put(L.kt, L.kt_b);
   put(L.gam, L.gam_b);
-  put(L.state, L.state_b);
-  put(L.u, L.u_b);
+  if (chunk128) {
+    const size_t n2 = n / 2;
+    auto put2 = [&](size_t& field, size_t rec) {
+      field = off;
+      off = align_up(off + rec * n2, 1024);
+    };
+    put2(L.aqk2, (size_t)C2 * C2 * es);
+    put2(L.wneg2, (size_t)C2 * DK * es);
+    put2(L.up2, (size_t)C2 * DV * es);
+    put2(L.qh2, (size_t)C2 * DK * es);
+    put2(L.kt2, (size_t)C2 * DK * es);
+    put2(L.gam2, (size_t)DK * 4);
+    put2(L.state2, L.state_b);
+    put2(L.u2, (size_t)C2 * DV * es);
+  } else {
+    put(L.state, L.state_b);
+    put(L.u, L.u_b);
+  }
   L.progress = off;
   off = align_up(off + (size_t)B * H * PROGRESS_STRIDE * 4, 1024);
   if (qk_norm) {
@@ -139,6 +162,12 @@ struct ResidualPtrs {
   void *qn, *kn;  // normalised q, k rows (q/k L2 normalisation only)
   float *qinv, *kinv;
 };
+// The 128-token chunks' records (FLAG_CHUNK128 only).
+struct Residual128Ptrs {
+  void *aqk, *wneg, *up, *qh, *kt;
+  float* gam;
+  void *state, *u;
+};
 struct BwdWorkspacePtrs {
   void *du, *dstate, *dqh, *dbk, *dkt, *daqk, *dakk;
   float *dgam, *dbv, *dbpart, *dgpart;
@@ -154,6 +183,7 @@ struct ChunkFwdArgs {
   void* out;
   float* h_final;
   ResidualPtrs res;
+  Residual128Ptrs res2;  // FLAG_CHUNK128: the 128-token records
   unsigned* err;
 };
 
@@ -223,7 +253,8 @@ enum KernelId {
   K_BWD_TC = 16,        // chunk_bwd_tc_kernel: every chunk product of the backward, fused, tcgen05
   K_PREP_TC = 17,       // chunk_prep_tc_kernel: the chunk preparation on tcgen05
   K_BWD_SYNC = 18,      // chunk_bwd_sync_zero_kernel: zeroes the fused backward's counters
-  K_COUNT = 19
+  K_MERGE = 19,         // chunk_merge128_kernel: two 64-token blocks -> one 128-token chunk
+  K_COUNT = 20
 };
 // Records a CUDA event on s before (begin = true) or after a launch when timing is on.
 void prof_mark(KernelId id, cudaStream_t s, bool begin);
@@ -241,6 +272,9 @@ cudaError_t launch_scan_bwd_tc(const ChunkBwdArgs& a, cudaStream_t s);
 // The chunk preparation on tcgen05 (chunk_prep_tc.cu), bf16 operands with Dk = Dv = 128.
 bool prep_tc_applies(int bf16_operands, int DK, int DV);
 cudaError_t launch_chunk_prep_tc(const ChunkFwdArgs& a, cudaStream_t s);
+// The merge of each pair of 64-token blocks' records into one 128-token chunk's records
+// (chunk_merge.cu), FLAG_CHUNK128 only.
+cudaError_t launch_chunk_merge128(const ChunkFwdArgs& a, cudaStream_t s);
 // The backward of bf16 with Dk = Dv = 128 on tcgen05 (chunk_bwd_tc.cu): the reverse scan and
 // the fused chunk-gradient kernel, as one cooperative launch when the (batch, head) pairs
 // leave SMs free (the gradient CTAs take each chunk as soon as the scan has finished it),

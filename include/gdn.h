@@ -47,7 +47,8 @@
  *   GDN_ERR_UNSUPPORTED  Dk or Dv not in {64, 128} (each on its own: Dk != Dv
  *                        is supported everywhere), unknown dtype,
  *                        B * H > 65535
- *   GDN_ERR_SHAPE        chunked calls with T not a multiple of 64
+ *   GDN_ERR_SHAPE        chunked calls with T not a multiple of 64 (128 with
+ *                        GDN_FLAG_CHUNK128)
  *   GDN_ERR_CUDA         a launch was rejected (cudaGetLastError); faults that
  *                        happen later surface at the caller's next
  *                        synchronisation on the stream
@@ -91,6 +92,16 @@ typedef enum { GDN_F32 = 0, GDN_BF16 = 1 } gdn_dtype;
  * it the residual buffer also holds the normalised rows, so
  * gdn_chunk_residual_bytes depends on the flag. */
 #define GDN_FLAG_QK_L2NORM 2
+/* gdn_chunk_fwd works on 128-token chunks, each two 64-token blocks, instead
+ * of 64-token chunks: the chunk of KernelConfig's bt = 2 bc (atomic-ops 0.1.0,
+ * section API) with the 64-query x 64-key cross-block score tile of the
+ * marin.community note "factoring GDN-2 decay on TPU" (section Approach),
+ * whose factors are taken about the last token of the first block. T must be a
+ * multiple of GDN_CHUNK128 (else GDN_ERR_SHAPE); gdn_chunk_residual_bytes
+ * depends on the flag. Forward only: gdn_chunk_bwd returns GDN_ERR_UNSUPPORTED
+ * and gdn_chunk_bwd_workspace_bytes 0 with it. gdn_recurrent and the replay
+ * calls ignore it. Results agree with the 64-token chunking to rounding. */
+#define GDN_FLAG_CHUNK128 4
 
 typedef struct {
   int B, T, H;       /* batch, tokens, heads */
@@ -100,9 +111,11 @@ typedef struct {
   int flags;         /* GDN_FLAG_* */
 } gdn_dims;
 
-/* Chunk size of the chunked path (tokens) and its split into two blocks. */
+/* Chunk size of the chunked path (tokens) and its split into two blocks;
+ * GDN_CHUNK128 with GDN_FLAG_CHUNK128. */
 #define GDN_CHUNK 64
 #define GDN_BLOCK 32
+#define GDN_CHUNK128 128
 
 /* Bytes of the residual buffer that gdn_chunk_fwd fills and gdn_chunk_bwd
  * reads: per 64-token chunk and head, the chunk-start state, the chunk's
@@ -113,18 +126,22 @@ typedef struct {
  * Features (the backward stages reuse forward residuals instead of recomputing
  * them); the records themselves are this library's. It plays the part of the
  * memory estimate that page's API offers (estimate_memory): the caller sizes
- * and owns the buffer. */
+ * and owns the buffer. With GDN_FLAG_CHUNK128 it also holds the 128-token
+ * chunks' records (the 64-token blocks' records are formed first, then
+ * merged). */
 size_t gdn_chunk_residual_bytes(const gdn_dims* dims);
 
 /* Bytes of scratch that gdn_chunk_bwd needs (reverse-scan outputs and the
- * per-chunk state-gradient products). Returns 0 for invalid dims.
+ * per-chunk state-gradient products). Returns 0 for invalid dims and with
+ * GDN_FLAG_CHUNK128 (no backward for 128-token chunks).
  * Source: atomic-ops 0.1.0, sections Features and Limitations (the backward is
  * a chain of stage kernels whose intermediate results are passed between
  * them, one of them the pairwise-decay score backward); this buffer holds what
  * this library's stages pass. Caller-owned, like the residual buffer. */
 size_t gdn_chunk_bwd_workspace_bytes(const gdn_dims* dims);
 
-/* Chunked forward (training / prefill), T a multiple of 64.
+/* Chunked forward (training / prefill), T a multiple of 64 (of 128 with
+ * GDN_FLAG_CHUNK128).
  *   h0        initial state, NULL = zeros
  *   scale     output scale (the Python binding passes Dk^-0.5 by default)
  *   out       [B,T,H,Dv] result
@@ -141,7 +158,12 @@ size_t gdn_chunk_bwd_workspace_bytes(const gdn_dims* dims);
  * SM (output CTAs beside the scan CTAs, synchronised through counters in the
  * residual buffer); it starts once every CTA can be resident at once. Where the
  * context cannot hold one CTA per SM at once (an SM-limited partition), the scan
- * and the outputs run as two launches instead. */
+ * and the outputs run as two launches instead. With GDN_FLAG_CHUNK128 the
+ * 64-token blocks' records are formed as above, a merge kernel combines each
+ * pair into the records of one 128-token chunk (the cross-block score tile and
+ * the off-diagonal block of the WY inverse, T21 = -T22 A21 T11, as products),
+ * and the state scan and the outputs run on the CUDA-core kernels over
+ * 128-token chunks: half the sequential steps and half the chunk-start states. */
 int gdn_chunk_fwd(const gdn_dims* dims, const void* q, const void* k, const void* v,
                   const void* g, const void* beta, const float* h0, float scale, void* out,
                   float* h_final, void* residuals, void* stream);

@@ -66,6 +66,15 @@ def test_size_queries(lib):
     rn = lib.gdn_chunk_residual_bytes(ctypes.byref(_dims(flags=binding.GDN_FLAG_QK_L2NORM)))
     rows = 2 * 128 * 3
     assert r + rows * (2 * D * 2 + 2 * 4) <= rn <= r + rows * (2 * D * 2 + 2 * 4) + 4 * 1024
+    # 128-token chunks: the 64-token blocks' records (no state or U) plus, per 128-token
+    # chunk-head, Aqk [128][128], -W, U', Q-hat, K-tilde [128][D], gam, state and U
+    f128 = binding.GDN_FLAG_CHUNK128
+    r128 = lib.gdn_chunk_residual_bytes(ctypes.byref(_dims(flags=f128)))
+    n2 = n // 2
+    want128 = want_r - n * (D * D * 2 + C * D * 2) + n2 * (128 * 128 * 2 + 5 * 128 * D * 2 + D * D * 2 + D * 4)
+    assert want128 <= r128 <= want128 + 18 * 1024
+    assert lib.gdn_chunk_residual_bytes(ctypes.byref(_dims(T=192, flags=f128))) == 0  # T % 128 != 0
+    assert lib.gdn_chunk_bwd_workspace_bytes(ctypes.byref(_dims(flags=f128))) == 0  # no 128-token backward
 
 
 def _fake(addr=1 << 20):
@@ -84,6 +93,11 @@ def test_invalid_arguments_are_rejected_on_the_host(lib):
     assert fwd(ctypes.byref(_dims(dtype=7)), p, p, p, p, p, None, f, p, None, p, None) == binding.GDN_ERR_UNSUPPORTED
     assert fwd(ctypes.byref(_dims(flags=8)), p, p, p, p, p, None, f, p, None, p, None) == binding.GDN_ERR_INVALID_ARG
     assert fwd(ctypes.byref(_dims(T=100)), p, p, p, p, p, None, f, p, None, p, None) == binding.GDN_ERR_SHAPE
+    f128 = binding.GDN_FLAG_CHUNK128
+    assert fwd(ctypes.byref(_dims(T=192, flags=f128)), p, p, p, p, p, None, f, p, None, p,
+               None) == binding.GDN_ERR_SHAPE
+    assert fwd(ctypes.byref(_dims(flags=f128 | 8)), p, p, p, p, p, None, f, p, None, p,
+               None) == binding.GDN_ERR_INVALID_ARG
     assert fwd(ctypes.byref(_dims(B=-1)), p, p, p, p, p, None, f, p, None, p, None) == binding.GDN_ERR_INVALID_ARG
     # NULL and misaligned required pointers, missing residuals, non-finite scale
     assert fwd(ctypes.byref(_dims()), None, p, p, p, p, None, f, p, None, p, None) == binding.GDN_ERR_INVALID_ARG
@@ -98,6 +112,7 @@ def test_invalid_arguments_are_rejected_on_the_host(lib):
     args = [p, p, p, p, p, None, f, p, p, None, p, p, p, p, p, None, p, None]
     assert bwd(ctypes.byref(_dims(Dk=64, Dv=96)), *args) == binding.GDN_ERR_UNSUPPORTED
     assert bwd(ctypes.byref(_dims(dtype=7)), *args) == binding.GDN_ERR_UNSUPPORTED
+    assert bwd(ctypes.byref(_dims(flags=binding.GDN_FLAG_CHUNK128)), *args) == binding.GDN_ERR_UNSUPPORTED
     bad = list(args)
     bad[16] = None  # workspace
     assert bwd(ctypes.byref(_dims()), *bad) == binding.GDN_ERR_INVALID_ARG

@@ -387,6 +387,37 @@ def test_chunked_form_with_128_token_chunks_equals_token_serial(per_channel):
         assert oracle.rel_l2(gm[n], gr[n]) < 1e-10, n
 
 
+@pytest.mark.parametrize("per_channel", [True, False])
+def test_two_64_token_blocks_merge_into_one_128_token_chunk(per_channel):
+    """The merge the 128-token forward performs, in float64: from each 64-token block's
+    own chunk quantities (relative to the block's start) the 128-token chunk's follow as
+    M = -W2 Kt1^T (= -T22 A21), W = [W1; W2 diag(gam1) - M W1], U' = [U'1; U'2 + M U'1],
+    Qh = [Qh1; Qh2 diag(gam1)], Kt = [Kt1 diag(gam2); Kt2], gam = gam1 gam2 and
+    Aqk = [[Aqk1, 0], [Qh2 Kt1^T, Aqk2]], equal to the direct 128-token chunk."""
+    w = WORKLOADS["tiny_fwd"].with_(T=128, H=1, Dk=8, Dv=6, h0_std=0.5, g_per_channel=per_channel)
+    a = _arrays(w)
+    g = cm._expand_g(a["g"], 8)
+    args = [a["q"][0, :, 0], a["k"][0, :, 0], a["v"][0, :, 0], g[0, :, 0], a["beta"][0, :, 0]]
+    full = cm.chunk_local(*args, factored=False)
+    b1 = cm.chunk_local(*[x[:64] for x in args], factored=False)
+    b2 = cm.chunk_local(*[x[64:] for x in args], factored=False)
+    M = -b2["W"] @ b1["Kt"].T
+    # M is -T22 A21, A21 the cross-block rows 64.. x columns ..63 of the 128-token Akk
+    assert np.allclose(M, -b2["T"] @ full["Akk"][64:, :64], rtol=0, atol=1e-12)
+    want = dict(W=np.vstack([b1["W"], b2["W"] * b1["gam"] - M @ b1["W"]]),
+                Up=np.vstack([b1["Up"], b2["Up"] + M @ b1["Up"]]),
+                Qh=np.vstack([b1["Qh"], b2["Qh"] * b1["gam"]]),
+                Kt=np.vstack([b1["Kt"] * b2["gam"], b2["Kt"]]),
+                gam=b1["gam"] * b2["gam"])
+    aqk = np.zeros((128, 128))
+    aqk[:64, :64] = b1["Aqk"]
+    aqk[64:, 64:] = b2["Aqk"]
+    aqk[64:, :64] = b2["Qh"] @ b1["Kt"].T
+    want["Aqk"] = aqk
+    for n, x in want.items():
+        assert oracle.rel_l2(x, full[n]) < 1e-12, n
+
+
 def test_transition_matrix_form_equals_token_serial():
     """The chunk recurrence as one affine map, S1 = diag(gam) S0 - K~^T W S0 + K~^T U',
     equals the token-serial oracle (the alternative scan form of the next-steps list)."""
