@@ -489,13 +489,15 @@ def variants_leg(args, w, host, dev):
 
 
 def chunk128_leg(args, w, host, dev):
-    """The forward alone on the headline inputs with 64-token chunks (the step's forward)
-    and with 128-token chunks (GDN_FLAG_CHUNK128: the 64-token blocks' records from the
-    same preparation, merged, then the CUDA-core scan and outputs over 128-token chunks;
-    forward only). CUDA events around N calls each, the per-kernel split of the 128-token
-    forward from the library's launch events, and its whole-forward bytes against HBM:
-    q, k, v, g, beta and h0 read, out and h_final written, plus the chunk-start states
-    (bf16, one per 128-token chunk) written once."""
+    """The forward alone, and forward + backward, on the headline inputs with 64-token
+    chunks (the step) and with 128-token chunks (GDN_FLAG_CHUNK128: the 64-token blocks'
+    records from the same preparation, merged, then the CUDA-core scan and outputs over
+    128-token chunks; the backward's reverse scan over 128-token chunks, the 64-token
+    blocks' records across each block boundary, then the 64-token chunk gradients). CUDA
+    events around N calls each, the per-kernel split of the 128-token forward and backward
+    from the library's launch events, and the forward's bytes against HBM: q, k, v, g,
+    beta and h0 read, out and h_final written, plus the chunk-start states (bf16, one per
+    128-token chunk) written once."""
     import torch
 
     import gated_deltanet_gdn_gb300 as gdn
@@ -537,8 +539,34 @@ def chunk128_leg(args, w, host, dev):
             out[name]["roofline"] = {"bound": "hbm", "method_bytes": int(fwd_bytes), "achieved": round(gbs, 1),
                                      "peak": peaks["hbm_gbs"], "unit": "GB/s",
                                      "frac": round(gbs / peaks["hbm_gbs"], 4)}
-        del rbuf
-    out["workload"] = "forward only, B%d T%d H%d D%d bf16, per-channel decay" % (w.B, w.T, w.H, w.Dk)
+        ws = torch.empty(gdn.gdn_chunk_bwd_workspace_bytes(dims), dtype=torch.uint8, device=dev)
+
+        def step():
+            fwd()
+            gdn.gdn_chunk_bwd(d["q"], d["k"], d["v"], d["g"], d["beta"], d["h0"], rbuf, d["dout"],
+                              d["dh_final"], workspace=ws, flags=flags)
+
+        for _ in range(3):
+            step()
+        torch.cuda.synchronize()
+        e0.record()
+        for _ in range(n):
+            step()
+        e1.record()
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / n
+        out[name]["fwd_bwd_ms"] = round(ms, 4)
+        out[name]["fwd_bwd_tokens_per_s"] = round(w.B * w.T / (ms / 1e3), 1)
+        if flags:
+            gdn.gdn_profile_enable(True)
+            for _ in range(n):
+                step()
+            prof = gdn.gdn_profile_read()
+            gdn.gdn_profile_enable(False)
+            out[name]["fwd_bwd_kernels_ms"] = {k: round(v[0] / n, 4) for k, v in prof.items()}
+        del rbuf, ws
+    out["workload"] = "forward, and forward + backward, B%d T%d H%d D%d bf16, per-channel decay" % (
+        w.B, w.T, w.H, w.Dk)
     return out
 
 

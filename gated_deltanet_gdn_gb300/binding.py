@@ -37,7 +37,7 @@ EXPORTED = ("gdn_chunk_residual_bytes", "gdn_chunk_bwd_workspace_bytes", "gdn_ch
             "gdn_version", "gdn_profile_enable", "gdn_profile_read", "gdn_kernel_name",
             "gdn_chunk_fwd_noalloc", "gdn_replay_buffer_bytes", "gdn_replay_decode",
             "gdn_replay_state", "gdn_selftest_wait_timeout")
-KERNEL_COUNT = 20
+KERNEL_COUNT = 21
 GDN_REPLAY_MAX_TOKENS = 8
 
 

@@ -175,7 +175,8 @@ const char* kKernelNames[K_COUNT] = {"chunk_prep_kernel",    "chunk_scan_fwd_ker
                                      "decode_kernel", "l2norm_rows_kernel", "l2norm_bwd_kernel",
                                      "replay_decode_kernel", "replay_state_kernel", "chunk_dqa_kernel",
                                      "chunk_bwd_tc_kernel", "chunk_prep_tc_kernel",
-                                     "chunk_bwd_sync_zero_kernel", "chunk_merge128_kernel"};
+                                     "chunk_bwd_sync_zero_kernel", "chunk_merge128_kernel",
+                                     "chunk_mid128_kernel"};
 
 }  // namespace
 
@@ -212,7 +213,8 @@ size_t gdn_chunk_residual_bytes(const gdn_dims* d) {
 }
 
 size_t gdn_chunk_bwd_workspace_bytes(const gdn_dims* d) {
-  if (check_dims(d, true) != GDN_OK || chunk128(d)) return 0;
+  if (check_dims(d, true) != GDN_OK) return 0;
+  if (chunk128(d) && d->dtype != GDN_BF16) return 0;  // 128-token backward: bf16 operands only
   return bwd_workspace_layout(d->B, d->T, d->H, d->Dk, d->Dv, esize(d)).total;
 }
 
@@ -261,7 +263,9 @@ int gdn_chunk_bwd(const gdn_dims* d, const void* q, const void* k, const void* v
                   void* dbeta, float* dh0, void* workspace, void* stream) {
   int st = check_dims(d, true);
   if (st != GDN_OK) return st;
-  if (chunk128(d)) return GDN_ERR_UNSUPPORTED;  // the backward works on 64-token chunks only
+  // 128-token chunks: bf16 operands only (one stage of fp32 128-token records would not
+  // fit the reverse scan's shared memory)
+  if (chunk128(d) && d->dtype != GDN_BF16) return GDN_ERR_UNSUPPORTED;
   if (!std::isfinite(scale)) return GDN_ERR_INVALID_ARG;
   const bool work = (long long)d->B * d->H * d->T > 0;
   const int es = esize(d);
@@ -283,7 +287,10 @@ int gdn_chunk_bwd(const gdn_dims* d, const void* q, const void* k, const void* v
   a.bf16 = d->dtype == GDN_BF16;
   a.flags = d->flags;
   a.q = q; a.k = k; a.v = v; a.g = g; a.beta = beta; a.scale = scale;
-  if (residuals) a.res = residual_ptrs(d, const_cast<void*>(residuals));
+  if (residuals) {
+    a.res = residual_ptrs(d, const_cast<void*>(residuals));
+    if (chunk128(d)) a.res2 = residual128_ptrs(d, const_cast<void*>(residuals));
+  }
   a.dout = dout; a.dh_final = dh_final;
   a.dq = dq; a.dk = dk; a.dv = dv; a.dg = dg; a.dbeta = dbeta; a.dh0 = dh0;
   if (workspace) a.ws = workspace_ptrs(d, workspace);

@@ -26,6 +26,8 @@
 //   chunk_dstate_kernel     grid (chunks, B*H), 256 threads: the products with dU and dS1
 //                           (contractions over Dv) and dgam
 //   chunk_grads_kernel      (chunk_grads.cu) everything else
+// With 128-token chunks (GDN_FLAG_CHUNK128) the reverse scan runs over them and
+// chunk_mid128_kernel forms the 64-token blocks' records before the chunk products.
 #include "chunk_dqa.cuh"
 #include "common.cuh"
 #include "kernels.h"
@@ -43,39 +45,51 @@ constexpr int DST_CG = DST_THREADS / 128;  // column groups of the state-product
 // (w & 3) * Dk/4 .. + Dk/4 and columns 32 (w >> 2) .. + 31 of the slice. bf16 records
 // are double-buffered (the next chunk loads during this one); fp32 records take twice
 // the room, so one stage, loaded at the top of its step.
-template <class T, int DK>
+// CC: chunk length. With CC = C2 (128-token chunks, bf16 operands only: one stage of
+// 128-token records fills the shared memory) the scan reads the 128-token records, stores
+// the gradient of the state leaving each 128-token chunk as the dS1 record of its second
+// 64-token block and no dU (chunk_mid128_kernel forms the 64-token blocks' dU and the
+// first block's dS1 from it).
+template <class T, int DK, int CC = C>
 struct RScanLayout {
   static constexpr int ES = (int)sizeof(T);
-  static constexpr int STAGES = ES == 2 ? 2 : 1;
-  static constexpr int W = 0;                      // -W          [C][DK]
-  static constexpr int QH = W + C * DK * ES;       // scale Q-hat [C][DK]
-  static constexpr int KT = QH + C * DK * ES;      // K-tilde     [C][DK]
-  static constexpr int AQK = KT + C * DK * ES;     // scale Aqk   [C][C]
-  static constexpr int GAM = AQK + C * C * ES;     // float [DK]
-  static constexpr int DO = a1k(GAM + DK * 4);     // dO slice    [C][NTS]
-  static constexpr int STAGE = a1k(DO + C * NTS * ES);
-  static constexpr int DSS = STAGES * STAGE;       // dS operand, transposed [NTS][DK]
-  static constexpr int DUS = a1k(DSS + DK * NTS * ES);  // dU, transposed  [NTS][C]
-  static constexpr int BAR = a1k(DUS + C * NTS * ES);
+  static constexpr int STAGES = ES == 2 && CC == C ? 2 : 1;
+  static constexpr int W = 0;                       // -W          [CC][DK]
+  static constexpr int QH = W + CC * DK * ES;       // scale Q-hat [CC][DK]
+  static constexpr int KT = QH + CC * DK * ES;      // K-tilde     [CC][DK]
+  static constexpr int AQK = KT + CC * DK * ES;     // scale Aqk   [CC][CC]
+  static constexpr int GAM = AQK + CC * CC * ES;    // float [DK]
+  static constexpr int DO = a1k(GAM + DK * 4);      // dO slice    [CC][NTS]
+  static constexpr int STAGE = a1k(DO + CC * NTS * ES);
+  static constexpr int DSS = STAGES * STAGE;        // dS operand, transposed [NTS][DK]
+  static constexpr int DUS = a1k(DSS + DK * NTS * ES);  // dU, transposed  [NTS][CC]
+  static constexpr int BAR = a1k(DUS + CC * NTS * ES);
   static constexpr int BYTES = BAR + 64;
-  static constexpr uint32_t TX = (uint32_t)(3 * C * DK * ES + C * C * ES + DK * 4);
+  static constexpr uint32_t TX = (uint32_t)(3 * CC * DK * ES + CC * CC * ES + DK * 4);
 };
 
-template <class T, int DK, int DV>
+template <class T, int DK, int DV, int CC = C>
 __global__ void __launch_bounds__(RSCAN_THREADS) chunk_scan_bwd_kernel(ChunkBwdArgs a) {
-  typedef RScanLayout<T, DK> L;
+  typedef RScanLayout<T, DK, CC> L;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = align1024(smem_raw);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int tile = blockIdx.x, bh = blockIdx.y, b = bh / a.H, h = bh % a.H;
-  const int N = a.T / C;
+  const int N = a.T / CC;
   constexpr int MTS = DK / 64, EPC = 16 / (int)sizeof(T), STAGES = L::STAGES;
+  constexpr int MU = CC / 64;  // m16 tiles of dU rows per warp
   const int rg = warp & 3, cg = warp >> 2;
-  const int srow = rg * 16 * MTS, col0 = 32 * cg;
+  const int srow = rg * 16 * MTS, col0 = 32 * cg, urow = rg * 16 * MU;
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + L::BAR);
   Tile<T, NTS, DK> dSs{reinterpret_cast<T*>(sm + L::DSS)};  // dS^T rows of this slice
-  Tile<T, NTS, C> dUs{reinterpret_cast<T*>(sm + L::DUS)};   // dU^T rows of this slice
+  Tile<T, NTS, CC> dUs{reinterpret_cast<T*>(sm + L::DUS)};  // dU^T rows of this slice
   const T* dout = static_cast<const T*>(a.dout);
+  // the CC-token records: the 64-token ones, or those of the 128-token chunks
+  const void* rw = CC == C ? a.res.wneg : a.res2.wneg;
+  const void* rq = CC == C ? a.res.qh : a.res2.qh;
+  const void* rk = CC == C ? a.res.kt : a.res2.kt;
+  const void* ra = CC == C ? a.res.aqk : a.res2.aqk;
+  const float* rg_ = CC == C ? a.res.gam : a.res2.gam;
 
   float dS[MTS][4][4];
   const size_t sb = (size_t)bh * DK * DV;
@@ -100,15 +114,15 @@ __global__ void __launch_bounds__(RSCAN_THREADS) chunk_scan_bwd_kernel(ChunkBwdA
     const size_t ch = (size_t)bh * N + n;
     if (tid == 0) {
       mbar_arrive_expect_tx(&bars[s], L::TX);
-      bulk_g2s(st + L::W, static_cast<const T*>(a.res.wneg) + ch * (C * DK), C * DK * L::ES, &bars[s]);
-      bulk_g2s(st + L::QH, static_cast<const T*>(a.res.qh) + ch * (C * DK), C * DK * L::ES, &bars[s]);
-      bulk_g2s(st + L::KT, static_cast<const T*>(a.res.kt) + ch * (C * DK), C * DK * L::ES, &bars[s]);
-      bulk_g2s(st + L::AQK, static_cast<const T*>(a.res.aqk) + ch * (C * C), C * C * L::ES, &bars[s]);
-      bulk_g2s(st + L::GAM, a.res.gam + ch * DK, DK * 4, &bars[s]);
+      bulk_g2s(st + L::W, static_cast<const T*>(rw) + ch * (CC * DK), CC * DK * L::ES, &bars[s]);
+      bulk_g2s(st + L::QH, static_cast<const T*>(rq) + ch * (CC * DK), CC * DK * L::ES, &bars[s]);
+      bulk_g2s(st + L::KT, static_cast<const T*>(rk) + ch * (CC * DK), CC * DK * L::ES, &bars[s]);
+      bulk_g2s(st + L::AQK, static_cast<const T*>(ra) + ch * (CC * CC), CC * CC * L::ES, &bars[s]);
+      bulk_g2s(st + L::GAM, rg_ + ch * DK, DK * 4, &bars[s]);
     }
-    Tile<T, C, NTS> dOt{reinterpret_cast<T*>(st + L::DO)};
-    const size_t row0 = ((size_t)b * a.T + (size_t)n * C) * a.H + h;
-    for (int i = tid; i < C * NTS / EPC; i += RSCAN_THREADS) {
+    Tile<T, CC, NTS> dOt{reinterpret_cast<T*>(st + L::DO)};
+    const size_t row0 = ((size_t)b * a.T + (size_t)n * CC) * a.H + h;
+    for (int i = tid; i < CC * NTS / EPC; i += RSCAN_THREADS) {
       const int r = i / (NTS / EPC), c0 = (i % (NTS / EPC)) * EPC;
       cp_async16(dOt.ptr(r, c0), dout + (row0 + (size_t)r * a.H) * DV + tile * NTS + c0);
     }
@@ -124,13 +138,16 @@ __global__ void __launch_bounds__(RSCAN_THREADS) chunk_scan_bwd_kernel(ChunkBwdA
     const bool more = STAGES > 1 && it + 1 < N;  // a later chunk's dO group is in flight
     if (it + STAGES - 1 < N) issue(n - (STAGES - 1), (it + STAGES - 1) % STAGES);
     uint8_t* st = sm + s * L::STAGE;
-    Tile<T, C, DK> Wt{reinterpret_cast<T*>(st + L::W)};
-    Tile<T, C, DK> Qt{reinterpret_cast<T*>(st + L::QH)};
-    Tile<T, C, DK> Kt{reinterpret_cast<T*>(st + L::KT)};
-    Tile<T, C, C> At{reinterpret_cast<T*>(st + L::AQK)};
-    Tile<T, C, NTS> dOt{reinterpret_cast<T*>(st + L::DO)};
+    Tile<T, CC, DK> Wt{reinterpret_cast<T*>(st + L::W)};
+    Tile<T, CC, DK> Qt{reinterpret_cast<T*>(st + L::QH)};
+    Tile<T, CC, DK> Kt{reinterpret_cast<T*>(st + L::KT)};
+    Tile<T, CC, CC> At{reinterpret_cast<T*>(st + L::AQK)};
+    Tile<T, CC, NTS> dOt{reinterpret_cast<T*>(st + L::DO)};
     const float* gam = reinterpret_cast<const float*>(st + L::GAM);
     const size_t ch = (size_t)bh * N + n;
+    // the 64-token record that takes this chunk's dS1: the chunk itself, or the second
+    // block of the 128-token chunk
+    const size_t chd = CC == C ? ch : (size_t)bh * (a.T / C) + 2 * (size_t)n + 1;
 
 #pragma unroll
     for (int mt = 0; mt < MTS; ++mt)
@@ -144,21 +161,23 @@ __global__ void __launch_bounds__(RSCAN_THREADS) chunk_scan_bwd_kernel(ChunkBwdA
     mbar_wait(&bars[s], par, a.err);
     __syncthreads();
     if (tid == 0) {  // gradient of the state leaving chunk n
-      store_row_block<T, DV, DK>(static_cast<T*>(a.ws.dstate) + ch * (DK * DV), dSs.p, tile * NTS, NTS);
+      store_row_block<T, DV, DK>(static_cast<T*>(a.ws.dstate) + chd * (DK * DV), dSs.p, tile * NTS, NTS);
       bulk_commit();
     }
-    float du[1][4][4];
+    float du[MU][4][4];
     zero(du);
-    Gemm<T>::template runk<1, 4, 0, C>(du, aview<true>(At), bview<true>(dOt), 16 * rg, col0, lane);
-    Gemm<T>::template runk<1, 4, 0, DK>(du, aview<false>(Kt), bview<false>(dSs), 16 * rg, col0, lane);
+    Gemm<T>::template runk<MU, 4, 0, CC>(du, aview<true>(At), bview<true>(dOt), urow, col0, lane);
+    Gemm<T>::template runk<MU, 4, 0, DK>(du, aview<false>(Kt), bview<false>(dSs), urow, col0, lane);
 #pragma unroll
-    for (int nt = 0; nt < 4; ++nt)
+    for (int mt = 0; mt < MU; ++mt)
 #pragma unroll
-      for (int e = 0; e < 4; ++e)
-        dUs.at(col0 + 8 * nt + frag_col(lane, e), 16 * rg + frag_row(lane, e)) = from_f32<T>(du[0][nt][e]);
+      for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          dUs.at(col0 + 8 * nt + frag_col(lane, e), urow + 16 * mt + frag_row(lane, e)) = from_f32<T>(du[mt][nt][e]);
     fence_proxy_async();
     __syncthreads();
-    if (tid == 0) {
+    if (CC == C && tid == 0) {
       store_row_block<T, DV, C>(static_cast<T*>(a.ws.du) + ch * (C * DV), dUs.p, tile * NTS, NTS);
       bulk_commit();
     }
@@ -168,8 +187,8 @@ __global__ void __launch_bounds__(RSCAN_THREADS) chunk_scan_bwd_kernel(ChunkBwdA
       for (int nt = 0; nt < 4; ++nt)
 #pragma unroll
         for (int e = 0; e < 4; ++e) dS[mt][nt][e] *= gam[srow + 16 * mt + frag_row(lane, e)];
-    Gemm<T>::template runk<MTS, 4, 0, C>(dS, aview<true>(Qt), bview<true>(dOt), srow, col0, lane);
-    Gemm<T>::template runk<MTS, 4, 0, C>(dS, aview<true>(Wt), bview<false>(dUs), srow, col0, lane);
+    Gemm<T>::template runk<MTS, 4, 0, CC>(dS, aview<true>(Qt), bview<true>(dOt), srow, col0, lane);
+    Gemm<T>::template runk<MTS, 4, 0, CC>(dS, aview<true>(Wt), bview<false>(dUs), srow, col0, lane);
     if (tid == 0) bulk_wait_read0();  // the bulk stores have read dSs and dUs before they are rewritten
     __syncthreads();
   }
@@ -416,18 +435,249 @@ __global__ void __launch_bounds__(DST_THREADS, sizeof(T) == 2 ? 2 : 1) chunk_dst
   }
 }
 
+// ------------------------------------------------------------------ 128-token chunks
+// The backward over 128-token chunks (FLAG_CHUNK128, bf16 operands). The reverse scan runs
+// over the 128-token chunks, half the sequential steps, and stores the gradient of the
+// state leaving each 128-token chunk (dS_end) as the dS1 record of its second 64-token
+// block. Per 128-token chunk this kernel then forms, from the two blocks' own records
+// (block 1 and block 2, each relative to its own start, as the preparation wrote them),
+// what the 64-token chunk products read: one reverse step and one forward step of the
+// 64-token recurrence across the block boundary,
+//   dU2   = scale Aqk2^T dO2 + K-tilde2 dS_end                  (block 2's dU)
+//   dSmid = diag(gam2) dS_end + scale Q-hat2^T dO2 - W2^T dU2    (block 1's dS1)
+//   dU1   = scale Aqk1^T dO1 + K-tilde1 dSmid                    (block 1's dU)
+//   Smid  = diag(gam1) S + K-tilde1^T U1                         (block 2's chunk-start state)
+// with S the 128-token chunk's start state and U1, U2 the halves of its U (the 64-token
+// deltas are the 128-token ones). All in value-major form, as the records are stored.
+// One CTA of 256 threads per 128-token chunk-head.
+constexpr int MID_THREADS = 256;
+
+template <class T, int DK, int DV>
+struct MidLayout {
+  static constexpr int ES = (int)sizeof(T);
+  static constexpr int DO1 = 0;                        // dO of block 1 [C][DV]
+  static constexpr int A1 = a1k(DO1 + C * DV * ES);    // scale Aqk of block 1 [C][C]
+  static constexpr int K1 = a1k(A1 + C * C * ES);      // K-tilde of block 1 [C][DK]
+  static constexpr int DS = a1k(K1 + C * DK * ES);     // dS_end^T [DV][DK], then dSmid^T
+  static constexpr int U1 = a1k(DS + DV * DK * ES);    // U1^T [DV][C]
+  static constexpr int DU2 = a1k(U1 + DV * C * ES);    // dU2^T [DV][C]
+  static constexpr int GAM = a1k(DU2 + DV * C * ES);   // float gam1 [DK], gam2 [DK]
+  // read only until dSmid is formed; then S^T [DV][DK] (from DO2) and Smid^T (from Q2)
+  static constexpr int DO2 = a1k(GAM + 2 * DK * 4);    // dO of block 2
+  static constexpr int A2 = a1k(DO2 + C * DV * ES);    // scale Aqk of block 2
+  static constexpr int K2 = a1k(A2 + C * C * ES);      // K-tilde of block 2
+  static constexpr int Q2 = a1k(K2 + C * DK * ES);     // scale Q-hat of block 2 [C][DK]
+  static constexpr int W2 = a1k(Q2 + C * DK * ES);     // -W of block 2
+  static constexpr int BYTES = a1k(W2 + C * DK * ES);
+  static constexpr int S0 = DO2, SMID = Q2;
+  static_assert(Q2 - DO2 >= DV * DK * ES && BYTES - Q2 >= DV * DK * ES, "state tiles fit the freed space");
+};
+
+template <class T, int DK, int DV>
+__global__ void __launch_bounds__(MID_THREADS) chunk_mid128_kernel(ChunkBwdArgs a) {
+  pdl_wait();  // dS_end comes from the reverse scan launched just before
+  pdl_trigger();
+  typedef MidLayout<T, DK, DV> L;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = align1024(smem_raw);
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int m = blockIdx.x, bh = blockIdx.y, b = bh / a.H, h = bh % a.H;
+  const int N = a.T / C, N2 = a.T / C2;
+  const size_t c1 = (size_t)bh * N + 2 * m, c2 = c1 + 1, cm = (size_t)bh * N2 + m;
+  constexpr int EPC = 16 / (int)sizeof(T);
+  Tile<T, C, DV> dO1s{reinterpret_cast<T*>(sm + L::DO1)};
+  Tile<T, C, DV> dO2s{reinterpret_cast<T*>(sm + L::DO2)};
+  Tile<T, C, C> A1s{reinterpret_cast<T*>(sm + L::A1)};
+  Tile<T, C, C> A2s{reinterpret_cast<T*>(sm + L::A2)};
+  Tile<T, C, DK> Q2s{reinterpret_cast<T*>(sm + L::Q2)};
+  Tile<T, C, DK> W2s{reinterpret_cast<T*>(sm + L::W2)};
+  Tile<T, C, DK> K1s{reinterpret_cast<T*>(sm + L::K1)};
+  Tile<T, C, DK> K2s{reinterpret_cast<T*>(sm + L::K2)};
+  Tile<T, DV, DK> dSs{reinterpret_cast<T*>(sm + L::DS)};
+  Tile<T, DV, C> U1s{reinterpret_cast<T*>(sm + L::U1)};
+  Tile<T, DV, C> dU2s{reinterpret_cast<T*>(sm + L::DU2)};
+  float* g1s = reinterpret_cast<float*>(sm + L::GAM);
+  float* g2s = g1s + DK;
+
+  const T* dout = static_cast<const T*>(a.dout);
+  const size_t row0 = ((size_t)b * a.T + (size_t)m * C2) * a.H + h;
+  for (int i = tid; i < C * DV / EPC; i += MID_THREADS) {
+    const int r = i / (DV / EPC), c0 = (i % (DV / EPC)) * EPC;
+    cp_async16(dO1s.ptr(r, c0), dout + (row0 + (size_t)r * a.H) * DV + c0);
+    cp_async16(dO2s.ptr(r, c0), dout + (row0 + (size_t)(C + r) * a.H) * DV + c0);
+  }
+  auto rec = [&](T* dst, const void* base, size_t ch, int elems) {
+    const T* src = static_cast<const T*>(base) + ch * elems;
+    for (int i = tid; i < elems / EPC; i += MID_THREADS) cp_async16(dst + i * EPC, src + i * EPC);
+  };
+  rec(A1s.p, a.res.aqk, c1, C * C);
+  rec(A2s.p, a.res.aqk, c2, C * C);
+  rec(Q2s.p, a.res.qh, c2, C * DK);
+  rec(W2s.p, a.res.wneg, c2, C * DK);
+  rec(K1s.p, a.res.kt, c1, C * DK);
+  rec(K2s.p, a.res.kt, c2, C * DK);
+  rec(dSs.p, a.ws.dstate, c2, DV * DK);
+  {  // U1^T: the first C columns of the 128-token U^T image are its first DV x C elements
+    const T* src = static_cast<const T*>(a.res2.u) + cm * (C2 * DV);
+    for (int i = tid; i < DV * C / EPC; i += MID_THREADS) cp_async16(U1s.p + i * EPC, src + i * EPC);
+  }
+  cp_async_commit();
+  for (int c = tid; c < DK; c += MID_THREADS) {
+    g1s[c] = a.res.gam[c1 * DK + c];
+    g2s[c] = a.res.gam[c2 * DK + c];
+  }
+  {  // block 2's U: the second half of the 128-token U^T image, global to global, every
+     // load of a thread before its first store
+    const T* src = static_cast<const T*>(a.res2.u) + cm * (C2 * DV) + (size_t)DV * C;
+    T* dst = static_cast<T*>(a.res.u) + c2 * (C * DV);
+    constexpr int NIT = DV * C / EPC / MID_THREADS;
+    static_assert(DV * C / EPC % MID_THREADS == 0, "whole passes");
+    uint4 v[NIT];
+#pragma unroll
+    for (int it = 0; it < NIT; ++it) v[it] = *reinterpret_cast<const uint4*>(src + (tid + it * MID_THREADS) * EPC);
+#pragma unroll
+    for (int it = 0; it < NIT; ++it) *reinterpret_cast<uint4*>(dst + (tid + it * MID_THREADS) * EPC) = v[it];
+  }
+  cp_async_wait<0>();
+  __syncthreads();
+
+  // warp w: value rows 16 MT (w & 3) .., columns (w >> 2) N / 2 .. of a [DV][N] result
+  constexpr int MT = DV / 64, NC = C / 16, NK = DK / 16;
+  const int m0 = 16 * MT * (warp & 3), hf = warp >> 2;
+  {  // dU2^T = dO2^T (scale Aqk2) + dS_end^T K-tilde2^T
+    float acc[MT][NC][4];
+    zero(acc);
+    Gemm<T>::template runk<MT, NC, 0, C>(acc, aview<true>(dO2s), bview<true>(A2s), m0, hf * (C / 2), lane);
+    Gemm<T>::template runk<MT, NC, 0, DK>(acc, aview<false>(dSs), bview<false>(K2s), m0, hf * (C / 2), lane);
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+      for (int nt = 0; nt < NC; ++nt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          dU2s.at(m0 + 16 * mt + frag_row(lane, e), hf * (C / 2) + 8 * nt + frag_col(lane, e)) =
+              from_f32<T>(acc[mt][nt][e]);
+  }
+  __syncthreads();  // dU2 complete; dS_end is next read only element by element, in place
+  {  // dSmid^T = dS_end^T diag(gam2) + dO2^T (scale Q-hat2) + dU2^T (-W2)
+    float acc[MT][NK][4];
+    zero(acc);
+    Gemm<T>::template runk<MT, NK, 0, C>(acc, aview<true>(dO2s), bview<true>(Q2s), m0, hf * (DK / 2), lane);
+    Gemm<T>::template runk<MT, NK, 0, C>(acc, aview<false>(dU2s), bview<true>(W2s), m0, hf * (DK / 2), lane);
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+      for (int nt = 0; nt < NK; ++nt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int v = m0 + 16 * mt + frag_row(lane, e), c = hf * (DK / 2) + 8 * nt + frag_col(lane, e);
+          dSs.at(v, c) = from_f32<T>(fmaf(to_f32(dSs.at(v, c)), g2s[c], acc[mt][nt][e]));
+        }
+  }
+  __syncthreads();  // dO2, Aqk2, K-tilde2, Q-hat2 and -W2 are dead: S^T arrives in their place
+  Tile<T, DV, DK> S0s{reinterpret_cast<T*>(sm + L::S0)};
+  Tile<T, DV, DK> Sms{reinterpret_cast<T*>(sm + L::SMID)};
+  rec(S0s.p, a.res2.state, cm, DV * DK);
+  cp_async_commit();
+  {  // records: block 2's dU, block 1's dS1 and U
+    T* du2 = static_cast<T*>(a.ws.du) + c2 * (C * DV);
+    T* ds1 = static_cast<T*>(a.ws.dstate) + c1 * (DK * DV);
+    T* u1 = static_cast<T*>(a.res.u) + c1 * (C * DV);
+    for (int i = tid; i < DV * C / EPC; i += MID_THREADS) {
+      copy16(du2 + i * EPC, dU2s.p + i * EPC);
+      copy16(u1 + i * EPC, U1s.p + i * EPC);
+    }
+    for (int i = tid; i < DV * DK / EPC; i += MID_THREADS) copy16(ds1 + i * EPC, dSs.p + i * EPC);
+  }
+  {  // dU1^T = dO1^T (scale Aqk1) + dSmid^T K-tilde1^T, straight to its record
+    float acc[MT][NC][4];
+    zero(acc);
+    Gemm<T>::template runk<MT, NC, 0, C>(acc, aview<true>(dO1s), bview<true>(A1s), m0, hf * (C / 2), lane);
+    Gemm<T>::template runk<MT, NC, 0, DK>(acc, aview<false>(dSs), bview<false>(K1s), m0, hf * (C / 2), lane);
+    T* du1 = static_cast<T*>(a.ws.du) + c1 * (C * DV);
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+      for (int nt = 0; nt < NC; ++nt)
+#pragma unroll
+        for (int e = 0; e < 4; e += 2) {
+          const int v = m0 + 16 * mt + frag_row(lane, e), t = hf * (C / 2) + 8 * nt + frag_col(lane, e);
+          store2(du1 + Sw<T, DV, C>::off(v, t), acc[mt][nt][e], acc[mt][nt][e + 1]);
+        }
+  }
+  {  // Smid^T = S^T diag(gam1) + U1^T K-tilde1, staged; block 1's state is S itself
+    float acc[MT][NK][4];
+    zero(acc);
+    Gemm<T>::template runk<MT, NK, 0, C>(acc, aview<false>(U1s), bview<true>(K1s), m0, hf * (DK / 2), lane);
+    cp_async_wait<0>();
+    __syncthreads();  // S^T has landed
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+      for (int nt = 0; nt < NK; ++nt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int v = m0 + 16 * mt + frag_row(lane, e), c = hf * (DK / 2) + 8 * nt + frag_col(lane, e);
+          Sms.at(v, c) = from_f32<T>(fmaf(to_f32(S0s.at(v, c)), g1s[c], acc[mt][nt][e]));
+        }
+  }
+  __syncthreads();
+  T* st1 = static_cast<T*>(a.res.state) + c1 * (DK * DV);
+  T* st2 = static_cast<T*>(a.res.state) + c2 * (DK * DV);
+  for (int i = tid; i < DV * DK / EPC; i += MID_THREADS) {
+    copy16(st1 + i * EPC, S0s.p + i * EPC);
+    copy16(st2 + i * EPC, Sms.p + i * EPC);
+  }
+}
+
+// The reverse scan over 128-token chunks, then the 64-token blocks' records (bf16 only).
+template <class T, int DK, int DV>
+cudaError_t launch_rscan128(const ChunkBwdArgs& a, cudaStream_t s) {
+  if constexpr (sizeof(T) != 2) {
+    return cudaErrorNotSupported;  // one stage of fp32 128-token records exceeds the shared memory
+  } else {
+    const int BH = a.B * a.H;
+    cudaError_t e;
+    {
+      const int bytes = RScanLayout<T, DK, C2>::BYTES + 1024;
+      auto kern = chunk_scan_bwd_kernel<T, DK, DV, C2>;
+      if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes)) != cudaSuccess)
+        return e;
+      prof_mark(K_SCAN_BWD, s, true);
+      kern<<<dim3(DV / NTS, BH), RSCAN_THREADS, bytes, s>>>(a);
+      prof_mark(K_SCAN_BWD, s, false);
+      if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    }
+    if (a.T < C2) return cudaSuccess;
+    const int bytes = MidLayout<T, DK, DV>::BYTES + 1024;
+    auto kern = chunk_mid128_kernel<T, DK, DV>;
+    if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes)) != cudaSuccess) return e;
+    prof_mark(K_MID, s, true);
+    e = launch_pdl(kern, dim3(a.T / C2, BH), dim3(MID_THREADS), bytes, s, a);
+    prof_mark(K_MID, s, false);
+    return e;
+  }
+}
+
 template <class T, int DK, int DV>
 cudaError_t launch_bwd_t(const ChunkBwdArgs& a, cudaStream_t s) {
   const int N = a.T / C, BH = a.B * a.H;
   const int bf16_ops = sizeof(T) == 2;
+  const bool c128 = (a.flags & FLAG_CHUNK128) != 0;
   cudaError_t e;
   // bf16 with Dk = Dv = 128: the tensor-core reverse scan and one fused tensor-core kernel
   // for every chunk product and gradient (chunk_bwd_tc.cu), in one launch where they fit
   // side by side. Otherwise (Dk = 64, or fp32 operands): the CUDA-core scan, then the
   // products that need no scan result (chunk_dqa.cuh), the state products, the score
-  // gradients and the channel-group sums.
-  if (scan_tc_applies(bf16_ops, DK, DV) && bwd_tc_applies(DK, DV)) return launch_chunk_bwd_tc(a, s);
-  {
+  // gradients and the channel-group sums. With 128-token chunks the scan runs over them
+  // and chunk_mid128_kernel forms the 64-token blocks' records; the chunk products follow.
+  const bool tc = scan_tc_applies(bf16_ops, DK, DV) && bwd_tc_applies(DK, DV);
+  if (c128) {
+    if ((e = launch_rscan128<T, DK, DV>(a, s)) != cudaSuccess) return e;
+    if (tc) return launch_chunk_bwd_tc(a, s, true);
+  } else if (tc) {
+    return launch_chunk_bwd_tc(a, s);
+  } else {
     const int bytes = RScanLayout<T, DK>::BYTES + 1024;
     auto kern = chunk_scan_bwd_kernel<T, DK, DV>;
     if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes)) != cudaSuccess) return e;

@@ -825,8 +825,8 @@ __global__ void chunk_bwd_sync_zero_kernel(unsigned* p, int n) {
 
 bool bwd_tc_applies(int DK, int DV) { return DK == BD && DV == BD; }
 
-cudaError_t launch_chunk_bwd_tc(const ChunkBwdArgs& a, cudaStream_t s) {
-  if (a.T / C == 0) return launch_scan_bwd_tc(a, s);  // no chunks: dh0 = dh_final only
+cudaError_t launch_chunk_bwd_tc(const ChunkBwdArgs& a, cudaStream_t s, bool grads_only) {
+  if (a.T / C == 0) return grads_only ? cudaSuccess : launch_scan_bwd_tc(a, s);  // dh0 = dh_final only
   if ((long long)a.B * a.T > 0x7fffffffLL) return cudaErrorInvalidValue;  // TMA token coordinate
   auto encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(tensor_map_encode_fn());
   if (!encode) return cudaErrorNotSupported;
@@ -866,7 +866,7 @@ cudaError_t launch_chunk_bwd_tc(const ChunkBwdArgs& a, cudaStream_t s) {
   const bool fused = coop && BH < nsm && units > 0 && a.ws.sync && a.ws.sync_bytes > 0;
   auto two_launches = [&]() {  // the reverse scan, then the gradients over a static stride
     cudaError_t e2;
-    if ((e2 = launch_scan_bwd_tc(a, s)) != cudaSuccess) return e2;
+    if (!grads_only && (e2 = launch_scan_bwd_tc(a, s)) != cudaSuccess) return e2;
     const int grid = units < nsm ? units : nsm;
     if (grid == 0) return cudaSuccess;
     prof_mark(K_BWD_TC, s, true);
@@ -875,7 +875,7 @@ cudaError_t launch_chunk_bwd_tc(const ChunkBwdArgs& a, cudaStream_t s) {
     prof_mark(K_BWD_TC, s, false);
     return e2;
   };
-  if (!fused) return two_launches();
+  if (!fused || grads_only) return two_launches();
   prof_mark(K_BWD_SYNC, s, true);
   chunk_bwd_sync_zero_kernel<<<1, 256, 0, s>>>(a.ws.sync, (int)(a.ws.sync_bytes / 4));
   prof_mark(K_BWD_SYNC, s, false);

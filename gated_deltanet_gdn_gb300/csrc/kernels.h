@@ -35,7 +35,7 @@ struct ResidualLayout {
   size_t aqk_b, tmat_b, w_b, up_b, qh_b, kt_b, gam_b, state_b, u_b;
   // with 128-token chunks: the 128-token records (merged from the 64-token blocks' aqk,
   // wneg, up, qh, kt and gam above; state and u of the 128-token chunks), same forms with
-  // C2 in place of C; the 64-token layout then has no state or u records
+  // C2 in place of C; the 64-token state and u records are then written by the backward
   size_t aqk2, wneg2, up2, qh2, kt2, gam2, state2, u2;
 };
 
@@ -74,6 +74,8 @@ inline ResidualLayout residual_layout(int B, int T, int H, int DK, int DV, int e
   put(L.qh, L.qh_b);
   put(L.kt, L.kt_b);
   put(L.gam, L.gam_b);
+  put(L.state, L.state_b);  // with 128-token chunks: formed by the backward, per 64-token block
+  put(L.u, L.u_b);
   if (chunk128) {
     const size_t n2 = n / 2;
     auto put2 = [&](size_t& field, size_t rec) {
@@ -88,9 +90,6 @@ inline ResidualLayout residual_layout(int B, int T, int H, int DK, int DV, int e
     put2(L.gam2, (size_t)DK * 4);
     put2(L.state2, L.state_b);
     put2(L.u2, (size_t)C2 * DV * es);
-  } else {
-    put(L.state, L.state_b);
-    put(L.u, L.u_b);
   }
   L.progress = off;
   off = align_up(off + (size_t)B * H * PROGRESS_STRIDE * 4, 1024);
@@ -192,6 +191,7 @@ struct ChunkBwdArgs {
   const void *q, *k, *v, *g, *beta;
   float scale;
   ResidualPtrs res;
+  Residual128Ptrs res2;  // FLAG_CHUNK128: the 128-token records
   const void* dout;
   const float* dh_final;
   void *dq, *dk, *dv, *dg, *dbeta;
@@ -254,7 +254,8 @@ enum KernelId {
   K_PREP_TC = 17,       // chunk_prep_tc_kernel: the chunk preparation on tcgen05
   K_BWD_SYNC = 18,      // chunk_bwd_sync_zero_kernel: zeroes the fused backward's counters
   K_MERGE = 19,         // chunk_merge128_kernel: two 64-token blocks -> one 128-token chunk
-  K_COUNT = 20
+  K_MID = 20,           // chunk_mid128_kernel: the 64-token blocks' dU, dS1, states and U
+  K_COUNT = 21
 };
 // Records a CUDA event on s before (begin = true) or after a launch when timing is on.
 void prof_mark(KernelId id, cudaStream_t s, bool begin);
@@ -280,7 +281,9 @@ cudaError_t launch_chunk_merge128(const ChunkFwdArgs& a, cudaStream_t s);
 // leave SMs free (the gradient CTAs take each chunk as soon as the scan has finished it),
 // else as two launches; it needs only the du, dstate and sync parts of the workspace.
 bool bwd_tc_applies(int DK, int DV);
-cudaError_t launch_chunk_bwd_tc(const ChunkBwdArgs& a, cudaStream_t s);
+// grads_only: the chunk gradients alone, over a static stride, from dU and dS1 records that
+// are already in the workspace (the backward over 128-token chunks forms them first)
+cudaError_t launch_chunk_bwd_tc(const ChunkBwdArgs& a, cudaStream_t s, bool grads_only = false);
 // cuTensorMapEncodeTiled through the runtime's driver entry point, resolved once (NULL if
 // the driver does not provide it); callers cast it to PFN_cuTensorMapEncodeTiled_v12000.
 void* tensor_map_encode_fn();

@@ -98,9 +98,12 @@ typedef enum { GDN_F32 = 0, GDN_BF16 = 1 } gdn_dtype;
  * marin.community note "factoring GDN-2 decay on TPU" (section Approach),
  * whose factors are taken about the last token of the first block. T must be a
  * multiple of GDN_CHUNK128 (else GDN_ERR_SHAPE); gdn_chunk_residual_bytes
- * depends on the flag. Forward only: gdn_chunk_bwd returns GDN_ERR_UNSUPPORTED
- * and gdn_chunk_bwd_workspace_bytes 0 with it. gdn_recurrent and the replay
- * calls ignore it. Results agree with the 64-token chunking to rounding. */
+ * depends on the flag. gdn_chunk_bwd takes it with bf16 operands (pass the
+ * flags of the forward that filled the residuals); with fp32 operands it
+ * returns GDN_ERR_UNSUPPORTED and gdn_chunk_bwd_workspace_bytes 0 (one stage
+ * of fp32 128-token records does not fit the reverse scan's shared memory).
+ * gdn_recurrent and the replay calls ignore it. Results agree with the
+ * 64-token chunking to rounding. */
 #define GDN_FLAG_CHUNK128 4
 
 typedef struct {
@@ -132,8 +135,8 @@ typedef struct {
 size_t gdn_chunk_residual_bytes(const gdn_dims* dims);
 
 /* Bytes of scratch that gdn_chunk_bwd needs (reverse-scan outputs and the
- * per-chunk state-gradient products). Returns 0 for invalid dims and with
- * GDN_FLAG_CHUNK128 (no backward for 128-token chunks).
+ * per-chunk state-gradient products). Returns 0 for invalid dims and for
+ * GDN_FLAG_CHUNK128 with fp32 operands.
  * Source: atomic-ops 0.1.0, sections Features and Limitations (the backward is
  * a chain of stage kernels whose intermediate results are passed between
  * them, one of them the pairwise-decay score backward); this buffer holds what
@@ -185,7 +188,11 @@ int gdn_chunk_fwd(const gdn_dims* dims, const void* q, const void* k, const void
  * the workspace that a one-CTA kernel zeroes before it (two launches where the
  * context cannot hold that grid). dims.dtype is that of the forward call that wrote
  * the residuals (bfloat16 or float32 operands; the state gradient is fp32 in
- * both); errors as listed at the top of this file. */
+ * both); errors as listed at the top of this file. With GDN_FLAG_CHUNK128
+ * (bf16): the reverse scan runs over the 128-token chunks, a kernel forms the
+ * 64-token blocks' dU, dS, chunk-start states and U across each block boundary
+ * (one reverse and one forward step of the 64-token recurrence), and the
+ * 64-token chunk gradients follow. */
 int gdn_chunk_bwd(const gdn_dims* dims, const void* q, const void* k, const void* v,
                   const void* g, const void* beta, const float* h0, float scale,
                   const void* residuals, const void* dout, const float* dh_final, void* dq,

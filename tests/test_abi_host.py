@@ -66,15 +66,18 @@ def test_size_queries(lib):
     rn = lib.gdn_chunk_residual_bytes(ctypes.byref(_dims(flags=binding.GDN_FLAG_QK_L2NORM)))
     rows = 2 * 128 * 3
     assert r + rows * (2 * D * 2 + 2 * 4) <= rn <= r + rows * (2 * D * 2 + 2 * 4) + 4 * 1024
-    # 128-token chunks: the 64-token blocks' records (no state or U) plus, per 128-token
-    # chunk-head, Aqk [128][128], -W, U', Q-hat, K-tilde [128][D], gam, state and U
+    # 128-token chunks: the 64-token records (their states and U formed by the backward)
+    # plus, per 128-token chunk-head, Aqk [128][128], -W, U', Q-hat, K-tilde [128][D], gam,
+    # state and U
     f128 = binding.GDN_FLAG_CHUNK128
     r128 = lib.gdn_chunk_residual_bytes(ctypes.byref(_dims(flags=f128)))
     n2 = n // 2
-    want128 = want_r - n * (D * D * 2 + C * D * 2) + n2 * (128 * 128 * 2 + 5 * 128 * D * 2 + D * D * 2 + D * 4)
+    want128 = want_r + n2 * (128 * 128 * 2 + 5 * 128 * D * 2 + D * D * 2 + D * 4)
     assert want128 <= r128 <= want128 + 18 * 1024
     assert lib.gdn_chunk_residual_bytes(ctypes.byref(_dims(T=192, flags=f128))) == 0  # T % 128 != 0
-    assert lib.gdn_chunk_bwd_workspace_bytes(ctypes.byref(_dims(flags=f128))) == 0  # no 128-token backward
+    # the 128-token backward (bf16 operands only) passes the 64-token blocks' dU and dS1
+    assert lib.gdn_chunk_bwd_workspace_bytes(ctypes.byref(_dims(flags=f128))) == w
+    assert lib.gdn_chunk_bwd_workspace_bytes(ctypes.byref(_dims(flags=f128, dtype=binding.GDN_F32))) == 0
 
 
 def _fake(addr=1 << 20):
@@ -112,7 +115,8 @@ def test_invalid_arguments_are_rejected_on_the_host(lib):
     args = [p, p, p, p, p, None, f, p, p, None, p, p, p, p, p, None, p, None]
     assert bwd(ctypes.byref(_dims(Dk=64, Dv=96)), *args) == binding.GDN_ERR_UNSUPPORTED
     assert bwd(ctypes.byref(_dims(dtype=7)), *args) == binding.GDN_ERR_UNSUPPORTED
-    assert bwd(ctypes.byref(_dims(flags=binding.GDN_FLAG_CHUNK128)), *args) == binding.GDN_ERR_UNSUPPORTED
+    assert bwd(ctypes.byref(_dims(flags=binding.GDN_FLAG_CHUNK128, dtype=binding.GDN_F32)),
+               *args) == binding.GDN_ERR_UNSUPPORTED
     bad = list(args)
     bad[16] = None  # workspace
     assert bwd(ctypes.byref(_dims()), *bad) == binding.GDN_ERR_INVALID_ARG

@@ -1,19 +1,25 @@
-"""GPU parity of the chunked forward over 128-token chunks (GDN_FLAG_CHUNK128: two
-64-token blocks per chunk, merged by chunk_merge128_kernel) against the float64 oracle.
+"""GPU parity of the chunked forward and backward over 128-token chunks
+(GDN_FLAG_CHUNK128: two 64-token blocks per chunk, merged by chunk_merge128_kernel; the
+backward's reverse scan over the 128-token chunks, then chunk_mid128_kernel and the
+64-token chunk products) against the float64 oracle.
 
-Cases span several 128-token chunks, fp32 (rel-L2 <= 1e-4) and bf16 (<= 2e-2), per-channel
-and scalar decay, every width pair, both in-block score paths, decay strong enough that the
-cross-block factors underflow, the q/k L2 normalisation, the allocation-free entry point,
-the training-shape forward workload (B4 T4096 H6 D128) on every head, agreement with the
-64-token chunking, determinism and the shape and backward refusals.
+Forward cases span several 128-token chunks, fp32 (rel-L2 <= 1e-4) and bf16 (<= 2e-2),
+per-channel and scalar decay, every width pair, both in-block score paths, decay strong
+enough that the cross-block factors underflow, the q/k L2 normalisation, the
+allocation-free entry point and the training-shape forward workload (B4 T4096 H6 D128) on
+every head. Backward cases (bf16): every width pair, both decay forms, no h0 and no
+dh_final, autograd, and the training-shape fwd+bwd workload (B8 T4096 H6 D128) on every
+head. Plus agreement with the 64-token chunking, determinism and the shape and dtype
+refusals.
 """
+import numpy as np
 import pytest
 import torch
 
 import gated_deltanet_gdn_gb300 as gdn
 from gated_deltanet_gdn_gb300.synthetic import WORKLOADS, make_inputs
 
-from helpers import TOL, cuda_inputs, oracle_fwd, rel
+from helpers import TOL, cuda_inputs, oracle_bwd, oracle_fwd, rel
 
 pytestmark = pytest.mark.gpu
 
@@ -126,9 +132,95 @@ def test_edge_cases():
     with pytest.raises(gdn.GdnError) as ei:  # 64-token multiple, not a 128-token one
         _fwd(cuda_inputs(make_inputs(w.with_(T=192))))
     assert ei.value.status == 3  # GDN_ERR_SHAPE
-    d = cuda_inputs(make_inputs(WORKLOADS["train_fwdbwd"].with_(B=1, T=256, H=2)))
+    d = cuda_inputs(make_inputs(WORKLOADS["train_fwdbwd"].with_(B=1, T=256, H=2, dtype="f32")))
     _, _, res = gdn.gdn_chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], d["h0"], flags=F128)
     with pytest.raises(gdn.GdnError) as ei:
         gdn.gdn_chunk_bwd(d["q"], d["k"], d["v"], d["g"], d["beta"], d["h0"], res, d["dout"], flags=F128)
-    assert ei.value.status == 2  # GDN_ERR_UNSUPPORTED: no backward over 128-token chunks
+    assert ei.value.status == 2  # GDN_ERR_UNSUPPORTED: fp32 backward over 128-token chunks
     assert gdn.gdn_check_device_error() == gdn.binding.GDN_OK
+
+
+# ---------------------------------------------------------------- backward
+GRADS = ("dq", "dk", "dv", "dg", "dbeta", "dh0")
+
+
+def _fwd_bwd(d, flags=F128):
+    out, hT, res = gdn.gdn_chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], d["h0"], flags=flags)
+    grads = gdn.gdn_chunk_bwd(d["q"], d["k"], d["v"], d["g"], d["beta"], d["h0"], res, d["dout"],
+                              d["dh_final"], flags=flags)
+    return out, hT, grads
+
+
+@pytest.mark.parametrize("per_channel", [True, False])
+@pytest.mark.parametrize("Dk,Dv", [(64, 64), (128, 128), (64, 128), (128, 64)])
+def test_backward_parity(per_channel, Dk, Dv):
+    w = WORKLOADS["train_fwdbwd"].with_(B=2, T=384, H=3, Dk=Dk, Dv=Dv, g_per_channel=per_channel,
+                                        g_mult=1.0 if per_channel else 0.1, h0_std=0.3)
+    host = make_inputs(w)
+    _, _, grads = _fwd_bwd(cuda_inputs(host))
+    ref = oracle_bwd(host)
+    print("C=128 bwd pc=%d %dx%d: " % (per_channel, Dk, Dv) +
+          " ".join("%s %.2e" % (n, rel(grads[n], ref[n])) for n in GRADS))
+    for n in GRADS:
+        assert rel(grads[n], ref[n]) <= TOL["bf16"], (n, rel(grads[n], ref[n]))
+
+
+def test_backward_without_h0_or_final_gradient_and_autograd():
+    w = WORKLOADS["train_fwdbwd"].with_(B=1, T=256, H=3, h0_std=0.0)
+    host = make_inputs(w)
+    host["dh_final"] = None
+    d = cuda_inputs(host)
+    out, hT, res = gdn.gdn_chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], None, flags=F128)
+    grads = gdn.gdn_chunk_bwd(d["q"], d["k"], d["v"], d["g"], d["beta"], None, res, d["dout"], None,
+                              flags=F128)
+    ref = oracle_bwd(host)
+    for n in GRADS:
+        assert rel(grads[n], ref[n]) <= TOL["bf16"], (n, rel(grads[n], ref[n]))
+    host = make_inputs(w.with_(h0_std=0.2))
+    d = cuda_inputs(host)
+    leaves = {n: d[n].clone().requires_grad_(True) for n in ("q", "k", "v", "g", "beta", "h0")}
+    out, hT = gdn.gated_delta_rule(leaves["q"], leaves["k"], leaves["v"], leaves["g"], leaves["beta"],
+                                   leaves["h0"], flags=F128)
+    (out.float() * d["dout"].float()).sum().backward(retain_graph=True)
+    hT.backward(d["dh_final"])
+    ref = oracle_bwd(host)
+    names = dict(q="dq", k="dk", v="dv", g="dg", beta="dbeta", h0="dh0")
+    for n, gn in names.items():
+        assert rel(leaves[n].grad, ref[gn]) <= TOL["bf16"], (n, rel(leaves[n].grad, ref[gn]))
+
+
+def test_backward_agrees_with_64_token_chunks_and_is_deterministic():
+    w = WORKLOADS["train_fwdbwd"].with_(B=2, T=512, H=4, h0_std=0.2)
+    d = cuda_inputs(make_inputs(w))
+    _, _, g1 = _fwd_bwd(d)
+    _, _, g2 = _fwd_bwd(d)
+    _, _, g0 = _fwd_bwd(d, 0)
+    for n in GRADS:
+        assert torch.equal(g1[n], g2[n]), n
+        x, y = g1[n].float(), g0[n].float()
+        assert float((x - y).norm() / y.norm()) < 1e-2, n
+
+
+def test_training_shape_fwd_bwd_workload():
+    """B8 T4096 H6 D128 bf16 over 128-token chunks: every (batch, head) pair of out,
+    h_final and every gradient against the oracle, per tensor and per pair (<= 2e-2)."""
+    w = WORKLOADS["train_fwdbwd"]
+    host = make_inputs(w)
+    out, hT, grads = _fwd_bwd(cuda_inputs(host))
+    torch.cuda.synchronize()
+    o_ref, h_ref = oracle_fwd(host)
+    ref = oracle_bwd(host)
+    got = dict(grads, out=out, h_final=hT)
+    refs = dict(ref, out=o_ref, h_final=h_ref)
+    print("\nC=128 training shape B8 T4096 H6 D128 bf16, rel-L2 vs oracle (all 48 heads; worst pair):")
+    for n in ("out", "h_final") + GRADS:
+        state = n in ("h_final", "dh0")
+        g = got[n].detach().double().cpu().numpy()
+        y = refs[n]
+        B, H = (g.shape[0], g.shape[1]) if state else (g.shape[0], g.shape[2])
+        per = np.array([[np.linalg.norm((g[b, h] - y[b, h]) if state else (g[b, :, h] - y[b, :, h])) /
+                         np.linalg.norm(y[b, h] if state else y[b, :, h]) for h in range(H)] for b in range(B)])
+        whole = rel(got[n], refs[n])
+        print(f"  {n:8s} {whole:.3e}  worst pair {per.max():.3e}")
+        assert whole <= TOL["bf16"], (n, whole)
+        assert per.max() <= TOL["bf16"], (n, per.max())
