@@ -189,6 +189,24 @@ def test_backward_without_h0_or_final_gradient_and_autograd():
         assert rel(leaves[n].grad, ref[gn]) <= TOL["bf16"], (n, rel(leaves[n].grad, ref[gn]))
 
 
+def test_many_heads_and_qk_l2norm_backward():
+    """More (batch, head) pairs than SMs (the merge, mid-block and gradient grids span
+    several waves, the gradients take their static stride), then the q/k L2
+    normalisation through the backward (dq, dk with respect to the raw q, k)."""
+    w = WORKLOADS["train_fwdbwd"].with_(B=4, T=256, H=48, h0_std=0.2)
+    host = make_inputs(w)
+    _, _, grads = _fwd_bwd(cuda_inputs(host))
+    ref = oracle_bwd(host)
+    for n in GRADS:
+        assert rel(grads[n], ref[n]) <= TOL["bf16"], (n, rel(grads[n], ref[n]))
+    w = WORKLOADS["train_fwdbwd"].with_(B=1, T=256, H=2, normalize_qk=False, h0_std=0.1)
+    host = make_inputs(w)
+    _, _, grads = _fwd_bwd(cuda_inputs(host), F128 | gdn.GDN_FLAG_QK_L2NORM)
+    ref = oracle_bwd(host, qk_l2norm=True)
+    for n in GRADS:
+        assert rel(grads[n], ref[n]) <= TOL["bf16"], (n, rel(grads[n], ref[n]))
+
+
 def test_backward_agrees_with_64_token_chunks_and_is_deterministic():
     w = WORKLOADS["train_fwdbwd"].with_(B=2, T=512, H=4, h0_std=0.2)
     d = cuda_inputs(make_inputs(w))
