@@ -242,3 +242,43 @@ def test_training_shape_fwd_bwd_workload():
         print(f"  {n:8s} {whole:.3e}  worst pair {per.max():.3e}")
         assert whole <= TOL["bf16"], (n, whole)
         assert per.max() <= TOL["bf16"], (n, per.max())
+
+
+def test_cuda_graph_capture_of_a_training_step():
+    """A fwd + bwd step over 128-token chunks captured in a CUDA graph replays to the same
+    bits as the eager calls (every launch of the path on the caller's stream)."""
+    w = WORKLOADS["train_fwdbwd"].with_(B=2, T=256, H=3, h0_std=0.2)
+    d = cuda_inputs(make_inputs(w))
+    dims = gdn.make_dims(d["q"], d["v"], d["g"], F128)
+    res = torch.empty(gdn.gdn_chunk_residual_bytes(dims), dtype=torch.uint8, device="cuda")
+    ws = torch.empty(gdn.gdn_chunk_bwd_workspace_bytes(dims), dtype=torch.uint8, device="cuda")
+    out, hT = torch.empty_like(d["v"]), torch.empty_like(d["h0"])
+    grads = {"dq": torch.empty_like(d["q"]), "dk": torch.empty_like(d["k"]), "dv": torch.empty_like(d["v"]),
+             "dg": torch.empty_like(d["g"]), "dbeta": torch.empty_like(d["beta"]), "dh0": torch.empty_like(d["h0"])}
+
+    def step():
+        gdn.gdn_chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], d["h0"], out=out, h_final=hT, residuals=res,
+                          flags=F128)
+        gdn.gdn_chunk_bwd(d["q"], d["k"], d["v"], d["g"], d["beta"], d["h0"], res, d["dout"], d["dh_final"],
+                          workspace=ws, grads=grads, flags=F128)
+
+    step()
+    torch.cuda.synchronize()
+    eager = dict({n: t.clone() for n, t in grads.items()}, out=out.clone(), hT=hT.clone())
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        step()
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        step()
+    for t in list(grads.values()) + [out, hT]:
+        t.zero_()
+    graph.replay()
+    torch.cuda.synchronize()
+    got = dict(grads, out=out, hT=hT)
+    for n, t in eager.items():
+        assert torch.equal(got[n], t), n
+    assert gdn.gdn_check_device_error() == gdn.binding.GDN_OK
