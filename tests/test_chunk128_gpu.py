@@ -19,7 +19,7 @@ import torch
 import gated_deltanet_gdn_gb300 as gdn
 from gated_deltanet_gdn_gb300.synthetic import WORKLOADS, make_inputs
 
-from helpers import TOL, cuda_inputs, oracle_bwd, oracle_fwd, rel
+from helpers import TOL, cuda_inputs, head_slice, oracle_bwd, oracle_fwd, rel
 
 pytestmark = pytest.mark.gpu
 
@@ -282,3 +282,21 @@ def test_cuda_graph_capture_of_a_training_step():
     for n, t in eager.items():
         assert torch.equal(got[n], t), n
     assert gdn.gdn_check_device_error() == gdn.binding.GDN_OK
+
+
+def test_long_context_shape():
+    """B1 T32768 H16 D128 bf16 over 128-token chunks (256 steps per scan chain): out and
+    h_final of every head, and every gradient of four heads, against the oracle."""
+    w = WORKLOADS["long_context"]
+    host = make_inputs(w)
+    out, hT, grads = _fwd_bwd(cuda_inputs(host))
+    torch.cuda.synchronize()
+    o_ref, h_ref = oracle_fwd(host)
+    print("\nC=128 long context: out %.3e h_final %.3e" % (rel(out, o_ref), rel(hT, h_ref)))
+    assert rel(out, o_ref) <= TOL["bf16"] and rel(hT, h_ref) <= TOL["bf16"]
+    pairs = [(0, 0), (0, 5), (0, 10), (0, 15)]
+    ref = oracle_bwd(host, pairs)
+    for n in GRADS:
+        got = head_slice(grads[n].cpu(), pairs, state=(n == "dh0"))
+        print("  %s %.3e" % (n, rel(got, ref[n])))
+        assert rel(got, ref[n]) <= TOL["bf16"], (n, rel(got, ref[n]))
